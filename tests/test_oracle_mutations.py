@@ -1,0 +1,92 @@
+"""Planted mistakes in the oracle must fail a pin.
+
+Each case copies moe_oracle.c, plants one plausible mistake (a dropped term, a
+wrong index, a flipped comparison, a floor for a ceiling ...), builds it, and
+checks that at least one of the pins in test_oracle_pins.py fails against it.
+The real oracle source is never modified.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+from oracle import build as obuild
+from tests import test_oracle_pins as pins
+
+MUTATIONS = {
+    "butterfly_drops_partner": ("t[p] = s[p] + s[p ^ o];", "t[p] = s[p] + s[p];"),
+    "lane_layout_interleaved": ("int h = stripe + 8 * p + t;", "int h = stripe + p + 32 * t;"),
+    "stripe_order_reversed": ("for (int stripe = 0; stripe < H; stripe += 256)",
+                              "for (int stripe = H - 256; stripe >= 0; stripe -= 256)"),
+    "ties_to_higher_id": ("if (best < 0 || key > bk)", "if (best < 0 || key >= bk)"),
+    "exp_drops_ln2_tail": ("r = fmaf(-n, LN2_LO, r);", "r = r;"),
+    "exp_short_taylor": ("float p = C[7];", "float p = 0.0f;"),
+    "weights_not_normalised": ("w[j] = a[j] / S;", "w[j] = a[j];"),
+    "coreset_ascending_mass": ("Q[order[p]] < Q[e]", "Q[order[p]] > Q[e]"),
+    "threshold_floor": ("if ((q << s) != prod) q += 1;", ";"),
+    "threshold_strict": ("while (c < nt && run < theta)", "while (c < nt && run <= theta)"),
+    "renorm_over_all_slots": ("if (idx[j] >= 0 && idx[j] < E && in_core[idx[j]]) s = s + w[j];",
+                              "s = s + w[j];"),
+    "disabled_redivides": ("for (int j = 0; j < k; ++j) wo[j] = w[j];\n                continue;",
+                           "for (int j = 0; j < k; ++j) wo[j] = w[j];"),
+    "silu_sign": ("hbuf[i] = g / (1.0 + exp(-g)) * u;", "hbuf[i] = g / (1.0 + exp(g)) * u;"),
+    "forward_first_slot_weight": ("double wj = (double)J->w_renorm[(size_t)r * J->k + j];",
+                                  "double wj = (double)J->w_renorm[(size_t)r * J->k];"),
+    "forward_drops_shared": ("moe_oracle_expert_ffn(xr, J->sg, J->su, J->sd, J->H, J->Is, yr);",
+                             "memset(yr, 0, sizeof(double) * (size_t)J->H);"),
+    "down_proj_transposed": ("const uint16_t* dh = wd + (size_t)h * I;",
+                             "const uint16_t* dh = wd + (size_t)(h % I) * I;"),
+}
+
+PINS = [
+    pins.test_exp_c_special_values, pins.test_exp_c_within_two_ulp_of_exp,
+    pins.test_logit_lane_order_hand_value, pins.test_logit_butterfly_hand_value,
+    pins.test_logit_stripe_order_hand_value, pins.test_logit_within_summation_bound,
+    pins.test_topk_is_sorted_selection, pins.test_topk_ties_go_to_lower_id,
+    pins.test_weights_equal_full_softmax_then_renormalised,
+    pins.test_coreset_brute_force_tiny_config, pins.test_coreset_threshold_hand_example,
+    pins.test_coreset_threshold_is_ceiling, pins.test_coreset_disabled_is_plain_topk,
+    pins.test_expert_ffn_hand_value, pins.test_expert_ffn_matches_dense_fp64,
+    pins.test_forward_matches_dense_moe_fp64,
+] + [lambda m, s=s: pins.test_coreset_brute_force_random_tiny(m, s) for s in range(4)]
+
+
+def _build_mutant(name: str, tmp: str) -> str:
+    old, new = MUTATIONS[name]
+    src = open(obuild.SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique/found: {name}"
+    path = os.path.join(tmp, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    so = os.path.join(tmp, f"lib{name}.so")
+    subprocess.run(["gcc", *obuild.CFLAGS, "-w", path, "-o", so, "-lm", "-lpthread"], check=True)
+    return so
+
+
+def _fails_some_pin() -> bool:
+    for pin in PINS:
+        try:
+            pin(oracle)
+        except Exception:
+            return True
+    return False
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name):
+    with tempfile.TemporaryDirectory() as tmp:
+        so = _build_mutant(name, tmp)
+        try:
+            oracle.use_library(so)
+            assert _fails_some_pin(), f"no pin caught the planted mistake {name!r}"
+        finally:
+            oracle.use_library(None)
+
+
+def test_unmutated_oracle_passes_every_pin():
+    oracle.use_library(None)
+    assert not _fails_some_pin()
