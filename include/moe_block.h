@@ -1,0 +1,169 @@
+/*
+ * moe_block.h -- C ABI of the block-coreset sparse mixture-of-experts FFN
+ * (libmoeblock.so, CUDA, sm_103a).
+ *
+ * The layer, as the source pages state it:
+ *   - model card "Clover-35B-A3B-Preview -- CMF", intro: an MoE with 256
+ *     experts, top-8, plus one shared expert, evaluated on every denoising
+ *     pass over a block of 32 rows;
+ *   - same page, Usage: the block's experts are restricted to the set that
+ *     carries 90% of its routing; block size 8, 16 or 32;
+ *   - InfiniLM PR #604 (Clover on Hygon DCUs), Summary and Notes: preview
+ *     passes route through the block coreset, the commit pass replays the
+ *     full route (coreset disabled).
+ * The pages give no API; the three calls below follow that statement of the
+ * problem: route every row, restrict each block to its coreset, evaluate the
+ * experts and the shared expert.
+ *
+ * Conventions for every call:
+ *   - Pointers named x, y, w_*, topk_*, keep, core_size, block_offsets,
+ *     workspace ... are DEVICE pointers owned by the caller; the library
+ *     allocates no device memory and keeps no pointer beyond the call, except
+ *     the weight pointers given to moe_plan_create (kept for the plan's life).
+ *   - bf16 tensors are row-major with the last dimension contiguous.
+ *   - Every call validates its arguments on the host first; on error it
+ *     returns a negative moe_status, launches nothing, and moe_last_error()
+ *     returns a message (thread-local).  On success the work is enqueued on
+ *     `stream` and the call returns without synchronising; nothing is copied
+ *     back to the host.
+ *   - Anomalies that only the device can see (an expert id out of range,
+ *     non-finite logits, block offsets that are not monotone, a row whose
+ *     coreset weights are all zero, a pipeline wait that gave up) are counted
+ *     in a status word inside the workspace; read it with
+ *     moe_read_device_status().  No kernel traps.
+ *   - Calls on one stream with one workspace are ordered; calls that share a
+ *     workspace must not run concurrently on different streams.
+ */
+#ifndef MOE_BLOCK_H
+#define MOE_BLOCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, bad size or value */
+    MOE_ERR_UNSUPPORTED = -2,  /* shape outside what the kernels implement */
+    MOE_ERR_WORKSPACE = -3,    /* workspace too small or misaligned */
+    MOE_ERR_CUDA = -4          /* a CUDA runtime or driver call failed */
+} moe_status;
+
+/* Layer shape and the largest call the workspace must hold.
+ *   H   hidden size; multiple of 256 (the router's summation stripes)
+ *   E   routed experts; 1..1024
+ *   k   experts per row; 1..32 and <= E
+ *   I   routed-expert intermediate size; multiple of 64
+ *   Is  shared-expert intermediate size; multiple of 64
+ *   max_rows    largest R of any call (>= 1)
+ *   max_blocks  largest nb of any call (>= 1) */
+typedef struct moe_dims {
+    int32_t H, E, k, I, Is;
+    int32_t max_rows, max_blocks;
+} moe_dims;
+
+/* Opaque host object: the shape, the weight pointers and their TMA tensor maps. */
+typedef struct moe_plan moe_plan;
+
+/* Device status word (uint32 counters), see moe_read_device_status. */
+enum {
+    MOE_STATUS_NONFINITE_LOGITS = 0,  /* logits that were NaN or +-inf */
+    MOE_STATUS_BAD_EXPERT_ID = 1,     /* top-k ids outside [0, E) (skipped) */
+    MOE_STATUS_BAD_OFFSETS = 2,       /* blocks with offsets out of order/range */
+    MOE_STATUS_EMPTY_ROWS = 3,        /* rows left with only the shared expert */
+    MOE_STATUS_WAIT_TIMEOUT = 4,      /* GEMM pipeline waits that gave up */
+    MOE_STATUS_WORDS = 8
+};
+
+/* Bytes of device workspace needed for calls up to `dims`; 0 on invalid dims.
+ * The workspace must be 256-byte aligned. */
+size_t moe_workspace_bytes(const moe_dims* dims);
+
+/* Create a plan.  Weights (device, bf16, row-major, 16-byte aligned):
+ *   w_router [E, H]   router (one row per expert)
+ *   w_gate   [E, I, H], w_up [E, I, H], w_down [E, H, I]   routed experts
+ *   ws_gate  [Is, H],   ws_up [Is, H],   ws_down [H, Is]     shared expert
+ * Expert e computes  W_down[e] (silu(W_gate[e] x) * (W_up[e] x)).
+ * Must be called with the device that owns the weights current.  On success
+ * *out receives a plan that the caller frees with moe_plan_destroy. */
+moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const void* w_gate,
+                           const void* w_up, const void* w_down, const void* ws_gate,
+                           const void* ws_up, const void* ws_down, moe_plan** out);
+
+void moe_plan_destroy(moe_plan* plan);
+
+/* Router: logits, top-k and weights for every row.
+ * (Model card, intro: "256 experts top-8".)
+ *   x             [R, H] bf16 rows; R <= max_rows
+ *   block_offsets [nb + 1] int32: block b holds rows block_offsets[b] ..
+ *                 block_offsets[b+1]-1; 0 = first <= ... <= last = R
+ *   logit_bias    [nb, E] fp32 added to row r's logits for r in block b, or NULL
+ *   topk_idx      [R, k] int32 out: experts by (logit desc, id asc)
+ *   topk_w        [R, k] fp32 out: softmax over the k selected logits
+ * Logits are fp32 sums of exact bf16 products in a fixed order (stripes of 256
+ * along H; lane p of 32 owns elements 8p..8p+7 of each stripe and adds them in
+ * ascending H; the 32 partial sums combine by an xor butterfly), so top-k ids
+ * are reproducible bit for bit.  NaN logits rank last (counted). */
+moe_status moe_block_route(const moe_plan* plan, const void* x, int32_t R,
+                           const int32_t* block_offsets, int32_t nb, const float* logit_bias,
+                           int32_t* topk_idx, float* topk_w, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream);
+
+/* Block coreset and renormalisation.
+ * (Model card, Usage: the block's experts restricted to the set carrying 90% of
+ * its routing; InfiniLM PR #604, Notes: full-route replay = coreset disabled.)
+ * Per block: mass q = floor(w * 2^32) per (row, slot) as exact integers,
+ * Q_e = sum over the block's rows; theta = ceil(tau * sum_e Q_e) exactly;
+ * experts ordered by (Q desc, id asc); the coreset is the shortest prefix whose
+ * mass reaches theta.  tau >= 1 (or +inf) disables the coreset: every touched
+ * expert is kept and w_renorm = topk_w bit for bit.  Otherwise each row's
+ * surviving weights are divided by their sum (fp32, rank order); dropped slots
+ * get 0; a row with no surviving weight keeps only the shared expert.
+ *   tau        (0, inf]; NaN or <= 0 is rejected
+ *   keep       [nb, ceil(E/32)] uint32 out: bit e of block b = expert e kept
+ *   core_size  [nb] int32 out: coreset size
+ *   w_renorm   [R, k] fp32 out
+ *   n_empty    [nb] int32 out (or NULL): rows left with only the shared expert */
+moe_status moe_block_coreset(const moe_plan* plan, int32_t R, const int32_t* block_offsets,
+                             int32_t nb, const int32_t* topk_idx, const float* topk_w,
+                             float tau, uint32_t* keep, int32_t* core_size, float* w_renorm,
+                             int32_t* n_empty, void* workspace, size_t workspace_bytes,
+                             moe_stream_t stream);
+
+/* Expert evaluation and combine.
+ * (Model card, intro: top-8 experts plus a shared expert.)
+ *   y[r] = S(x[r]) + sum over slots j of row r whose expert is kept for r's
+ *          block of w_renorm[r, j] * E_{topk_idx[r, j]}(x[r])
+ * with S the shared expert.  bf16 MMA with fp32 accumulation; the SwiGLU
+ * hidden activations are rounded to bf16 before the down projection.
+ *   y      [R, H] bf16 out
+ *   y_f32  [R, H] fp32 out (the sum before the bf16 rounding), or NULL
+ * Each touched expert's weights are streamed from HBM once per call. */
+moe_status moe_block_forward(const moe_plan* plan, const void* x, int32_t R,
+                             const int32_t* block_offsets, int32_t nb, const int32_t* topk_idx,
+                             const float* w_renorm, const uint32_t* keep, void* y, float* y_f32,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Copy the MOE_STATUS_WORDS counters to out[] (host); synchronises `stream`. */
+moe_status moe_read_device_status(const void* workspace, moe_stream_t stream, uint32_t* out);
+
+/* Zero the status counters (enqueued on `stream`). */
+moe_status moe_clear_device_status(void* workspace, moe_stream_t stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_BLOCK_H */

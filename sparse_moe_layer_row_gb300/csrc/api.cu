@@ -1,0 +1,297 @@
+// Host side of libmoeblock: plan, workspace layout, argument validation, TMA
+// tensor maps and the launch sequence of each C-ABI call.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kernels.cuh"
+
+using namespace moe;
+
+struct moe_plan {
+    moe_dims d;
+    int device;
+    int num_sms;
+    const void *wr, *wg, *wu, *wd, *sg, *su, *sd;
+    CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+moe_status fail(moe_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+moe_status ok() {
+    g_last_error.clear();
+    return MOE_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor map, row-major [d2][d1][d0] (rank 2 if d2 == 0), box (64, box1[, 1]),
+// 128-byte swizzle, out-of-bounds elements read as zero.
+bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint32_t box1, CUtensorMapL2promotion l2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint32_t rank = d2 ? 3 : 2;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {64, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+moe_status check_dims(const moe_dims* d) {
+    if (!d) return fail(MOE_ERR_INVALID_ARG, "dims is NULL");
+    if (d->H <= 0 || d->H % 256)
+        return fail(MOE_ERR_UNSUPPORTED, "H=%d must be a positive multiple of 256", d->H);
+    if (d->E < 1 || d->E > 1024) return fail(MOE_ERR_UNSUPPORTED, "E=%d must be in [1, 1024]", d->E);
+    if (d->k < 1 || d->k > 32 || d->k > d->E)
+        return fail(MOE_ERR_UNSUPPORTED, "k=%d must be in [1, min(32, E)]", d->k);
+    if (d->I <= 0 || d->I % 64) return fail(MOE_ERR_UNSUPPORTED, "I=%d must be a positive multiple of 64", d->I);
+    if (d->Is <= 0 || d->Is % 64)
+        return fail(MOE_ERR_UNSUPPORTED, "Is=%d must be a positive multiple of 64", d->Is);
+    if (d->max_rows < 1 || d->max_blocks < 1)
+        return fail(MOE_ERR_INVALID_ARG, "max_rows=%d and max_blocks=%d must be >= 1", d->max_rows,
+                    d->max_blocks);
+    if ((int64_t)d->max_rows * d->k > (1 << 30) || (int64_t)d->max_rows * d->H > (int64_t)1 << 34)
+        return fail(MOE_ERR_UNSUPPORTED, "max_rows=%d too large", d->max_rows);
+    return MOE_OK;
+}
+
+moe_status check_call(const moe_plan* p, int32_t R, const int32_t* off, int32_t nb, void* ws,
+                      size_t ws_bytes) {
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+    if (R < 0 || R > p->d.max_rows)
+        return fail(MOE_ERR_INVALID_ARG, "R=%d outside [0, max_rows=%d]", R, p->d.max_rows);
+    if (nb < 1 || nb > p->d.max_blocks)
+        return fail(MOE_ERR_INVALID_ARG, "nb=%d outside [1, max_blocks=%d]", nb, p->d.max_blocks);
+    if (!off || !aligned(off, 4)) return fail(MOE_ERR_INVALID_ARG, "block_offsets NULL or misaligned");
+    if (!ws || !aligned(ws, 256)) return fail(MOE_ERR_WORKSPACE, "workspace NULL or not 256-byte aligned");
+    const size_t need = make_layout(p->d).total;
+    if (ws_bytes < need)
+        return fail(MOE_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device)
+        return fail(MOE_ERR_INVALID_ARG, "current device %d is not the plan's device %d", dev,
+                    p->device);
+    return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_version(void) { return 100; }
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+size_t moe_workspace_bytes(const moe_dims* dims) {
+    if (check_dims(dims) != MOE_OK) return 0;
+    return make_layout(*dims).total;
+}
+
+moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const void* w_gate,
+                           const void* w_up, const void* w_down, const void* ws_gate,
+                           const void* ws_up, const void* ws_down, moe_plan** out) {
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    moe_status s = check_dims(dims);
+    if (s != MOE_OK) return s;
+    const void* ws[7] = {w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down};
+    const char* names[7] = {"w_router", "w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down"};
+    for (int i = 0; i < 7; ++i)
+        if (!ws[i] || !aligned(ws[i], 16))
+            return fail(MOE_ERR_INVALID_ARG, "%s is NULL or not 16-byte aligned", names[i]);
+    moe_plan* p = new moe_plan();
+    p->d = *dims;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e == cudaSuccess) e = gemm_set_attributes();
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "device query");
+    }
+    p->wr = w_router; p->wg = w_gate; p->wu = w_up; p->wd = w_down;
+    p->sg = ws_gate; p->su = ws_up; p->sd = ws_down;
+    const moe_dims& d = *dims;
+    const auto L2W = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+    bool good = encode_bf16(&p->tm_wg, w_gate, d.H, d.I, d.E, 16, L2W) &&
+                encode_bf16(&p->tm_wu, w_up, d.H, d.I, d.E, 16, L2W) &&
+                encode_bf16(&p->tm_wd, w_down, d.I, d.H, d.E, 128, L2W) &&
+                encode_bf16(&p->tm_sg, ws_gate, d.H, d.Is, 0, 16, L2W) &&
+                encode_bf16(&p->tm_su, ws_up, d.H, d.Is, 0, 16, L2W) &&
+                encode_bf16(&p->tm_sd, ws_down, d.Is, d.H, 0, 128, L2W);
+    if (!good) {
+        delete p;
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight tensor");
+    }
+    *out = p;
+    return ok();
+}
+
+void moe_plan_destroy(moe_plan* plan) { delete plan; }
+
+moe_status moe_block_route(const moe_plan* p, const void* x, int32_t R,
+                           const int32_t* block_offsets, int32_t nb, const float* logit_bias,
+                           int32_t* topk_idx, float* topk_w, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream) {
+    moe_status s = check_call(p, R, block_offsets, nb, workspace, workspace_bytes);
+    if (s != MOE_OK) return s;
+    if (!x || !aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
+    if (!topk_idx || !topk_w || !aligned(topk_idx, 4) || !aligned(topk_w, 4))
+        return fail(MOE_ERR_INVALID_ARG, "topk_idx/topk_w NULL or misaligned");
+    if (logit_bias && !aligned(logit_bias, 4)) return fail(MOE_ERR_INVALID_ARG, "logit_bias misaligned");
+    if (R == 0) return ok();
+    const Layout L = make_layout(p->d);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(at<uint8_t>(workspace, L.route_cnt), 0,
+                                    sizeof(uint32_t) * (size_t)((R + 3) / 4), st);
+    if (e != cudaSuccess) return cuda_fail(e, "route counters");
+    RouteArgs a{static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(p->wr),
+                logit_bias, block_offsets, R, p->d.H, p->d.E, p->d.k, nb,
+                at<float>(workspace, L.logits), at<uint32_t>(workspace, L.route_cnt), topk_idx,
+                topk_w, at<uint32_t>(workspace, L.status)};
+    e = launch_route(a, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    return ok();
+}
+
+moe_status moe_block_coreset(const moe_plan* p, int32_t R, const int32_t* block_offsets,
+                             int32_t nb, const int32_t* topk_idx, const float* topk_w, float tau,
+                             uint32_t* keep, int32_t* core_size, float* w_renorm,
+                             int32_t* n_empty, void* workspace, size_t workspace_bytes,
+                             moe_stream_t stream) {
+    moe_status s = check_call(p, R, block_offsets, nb, workspace, workspace_bytes);
+    if (s != MOE_OK) return s;
+    if (!(tau > 0.0f)) return fail(MOE_ERR_INVALID_ARG, "tau=%g must be > 0 (and not NaN)", (double)tau);
+    if (!topk_idx || !topk_w || !keep || !core_size || !w_renorm)
+        return fail(MOE_ERR_INVALID_ARG, "a required coreset pointer is NULL");
+    const void* ps[6] = {topk_idx, topk_w, keep, core_size, w_renorm, n_empty};
+    for (const void* q : ps)
+        if (q && !aligned(q, 4)) return fail(MOE_ERR_INVALID_ARG, "coreset pointer misaligned");
+    const Layout L = make_layout(p->d);
+    CoresetArgs a{block_offsets, topk_idx, topk_w, R, p->d.E, p->d.k, nb, tau, keep, core_size,
+                  w_renorm, n_empty, at<uint32_t>(workspace, L.status)};
+    cudaError_t e = launch_coreset(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "coreset launch");
+    return ok();
+}
+
+moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
+                             const int32_t* block_offsets, int32_t nb, const int32_t* topk_idx,
+                             const float* w_renorm, const uint32_t* keep, void* y, float* y_f32,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    moe_status s = check_call(p, R, block_offsets, nb, workspace, workspace_bytes);
+    if (s != MOE_OK) return s;
+    if (!x || !aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
+    if (!y || !aligned(y, 16)) return fail(MOE_ERR_INVALID_ARG, "y is NULL or not 16-byte aligned");
+    if (y_f32 && !aligned(y_f32, 16)) return fail(MOE_ERR_INVALID_ARG, "y_f32 not 16-byte aligned");
+    if (!topk_idx || !w_renorm || !keep || !aligned(topk_idx, 4) || !aligned(w_renorm, 4) ||
+        !aligned(keep, 4))
+        return fail(MOE_ERR_INVALID_ARG, "topk_idx/w_renorm/keep NULL or misaligned");
+    if (R == 0) return ok();
+    const moe_dims& d = p->d;
+    const Layout L = make_layout(d);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int nt = R <= 64 ? kSmallN : kLargeN;
+
+    ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, static_cast<const __nv_bfloat16*>(x),
+                   R, d.H, d.E, d.k, d.I, d.Is, nb, nt,
+                   at<int32_t>(workspace, L.row_block), at<int32_t>(workspace, L.count),
+                   at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
+                   at<int4>(workspace, L.units_gu), at<int4>(workspace, L.units_dn),
+                   at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
+                   at<__nv_bfloat16>(workspace, L.xp), at<float>(workspace, L.y32),
+                   at<uint32_t>(workspace, L.status)};
+    GemmMaps gu{}, dn{};
+    const auto L2A = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+    gu.a0 = p->tm_wg; gu.a1 = p->tm_wu; gu.a2 = p->tm_sg; gu.a3 = p->tm_su;
+    dn.a0 = p->tm_wd; dn.a1 = p->tm_wd; dn.a2 = p->tm_sd; dn.a3 = p->tm_sd;
+    bool good = encode_bf16(&gu.b0, at<void>(workspace, L.xp), d.H, (uint64_t)L.max_pairs, 0, 16, L2A) &&
+                encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, 16, L2A) &&
+                encode_bf16(&dn.b0, at<void>(workspace, L.h), d.I, (uint64_t)L.max_pairs, 0, 16, L2A) &&
+                encode_bf16(&dn.b1, at<void>(workspace, L.hs), d.Is, (uint64_t)d.max_rows, 0, 16, L2A);
+    if (!good) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation tensor");
+    GemmArgs ga{at<int4>(workspace, L.units_gu), at<int32_t>(workspace, L.misc) + 1, d.E, d.H, d.I,
+                d.Is, at<__nv_bfloat16>(workspace, L.h), at<__nv_bfloat16>(workspace, L.hs),
+                at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
+                at<float>(workspace, L.y32), at<uint32_t>(workspace, L.status)};
+    cudaError_t e = launch_scatter(sa, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
+    e = launch_gemm(0, nt, gu, ga, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
+    GemmArgs gd = ga;
+    gd.units = at<int4>(workspace, L.units_dn);
+    gd.n_units = at<int32_t>(workspace, L.misc) + 2;
+    e = launch_gemm(1, nt, dn, gd, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
+    FinalArgs fa{at<float>(workspace, L.y32), static_cast<__nv_bfloat16*>(y), y_f32,
+                 (size_t)R * d.H};
+    e = launch_finalize(fa, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+    return ok();
+}
+
+moe_status moe_read_device_status(const void* workspace, moe_stream_t stream, uint32_t* out) {
+    if (!workspace || !aligned(workspace, 256) || !out)
+        return fail(MOE_ERR_INVALID_ARG, "workspace or out invalid");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(out, workspace, sizeof(uint32_t) * MOE_STATUS_WORDS,
+                                    cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    return ok();
+}
+
+moe_status moe_clear_device_status(void* workspace, moe_stream_t stream) {
+    if (!workspace || !aligned(workspace, 256)) return fail(MOE_ERR_INVALID_ARG, "workspace invalid");
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t) * MOE_STATUS_WORDS,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    return ok();
+}
+
+}  // extern "C"

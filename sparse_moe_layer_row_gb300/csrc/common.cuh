@@ -1,0 +1,265 @@
+// Shared device helpers of libmoeblock: status counters, workspace layout and
+// thin inline-PTX wrappers for mbarrier, TMA (cp.async.bulk.tensor) and the
+// 5th-generation tensor core (tcgen05 + TMEM) on sm_103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_block.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Workspace layout (byte offsets from the caller's workspace base).  Every
+// region starts on a 1024-byte boundary (TMA needs 16 B; 1 KB keeps rows of
+// the bf16 staging buffers on swizzle-atom boundaries).
+
+struct Layout {
+    size_t status;       // uint32[MOE_STATUS_WORDS]
+    size_t route_cnt;    // uint32[ceil(max_rows/4)]   router row-group tickets
+    size_t logits;       // fp32 [max_rows, E]        router logits (before bias)
+    size_t row_block;    // int32 [max_rows]
+    size_t count;        // int32 [E]                 surviving pairs per expert
+    size_t expert_off;   // int32 [E + 1]
+    size_t misc;         // int32[16]: [0] ticket, [1] units gate/up, [2] units down, [3] pairs
+    size_t units_gu;     // int4 [max_units_gu]
+    size_t units_dn;     // int4 [max_units_dn]
+    size_t pair_row;     // int32 [max_pairs]
+    size_t pair_w;       // fp32 [max_pairs]
+    size_t xp;           // bf16 [max_pairs, H]       rows of x in pair order
+    size_t h;            // bf16 [max_pairs, I]       routed SwiGLU activations
+    size_t hs;           // bf16 [max_rows, Is]       shared-expert activations
+    size_t y32;          // fp32 [max_rows, H]        combine accumulator
+    size_t total;
+    int64_t max_pairs, max_units_gu, max_units_dn;
+};
+
+// Rows of x per unit of grouped-GEMM work (the MMA N extent) for the two
+// kernel shapes; a call picks one from its row count.
+constexpr int kSmallN = 32;
+constexpr int kLargeN = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline Layout make_layout(const moe_dims& d) {
+    Layout L{};
+    const int64_t R = d.max_rows, E = d.E, H = d.H;
+    const int64_t P = R * d.k;
+    // Unit counts with the smaller chunk size bound both kernel shapes.
+    const int64_t chunks = (P + kSmallN - 1) / kSmallN + E;
+    const int64_t schunks = (R + kSmallN - 1) / kSmallN;
+    L.max_pairs = P;
+    L.max_units_gu = chunks * (d.I / 64) + schunks * (d.Is / 64);
+    L.max_units_dn = (chunks + schunks) * (H / 128);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
+    L.status = take(sizeof(uint32_t) * 64);
+    L.route_cnt = take(sizeof(uint32_t) * (size_t)((R + 3) / 4));
+    L.logits = take(sizeof(float) * (size_t)(R * E));
+    L.row_block = take(sizeof(int32_t) * (size_t)R);
+    L.count = take(sizeof(int32_t) * (size_t)E);
+    L.expert_off = take(sizeof(int32_t) * (size_t)(E + 1));
+    L.misc = take(sizeof(int32_t) * 16);
+    L.units_gu = take(sizeof(int4) * (size_t)L.max_units_gu);
+    L.units_dn = take(sizeof(int4) * (size_t)L.max_units_dn);
+    L.pair_row = take(sizeof(int32_t) * (size_t)P);
+    L.pair_w = take(sizeof(float) * (size_t)P);
+    L.xp = take(2 * (size_t)(P * H));
+    L.h = take(2 * (size_t)(P * d.I));
+    L.hs = take(2 * (size_t)(R * d.Is));
+    L.y32 = take(sizeof(float) * (size_t)(R * H));
+    L.total = o;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// device helpers
+
+__device__ __forceinline__ void status_add(uint32_t* status, int word, uint32_t v) {
+    if (v) atomicAdd(status + word, v);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ---------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// `limit_ns`, giving up early when another role of the CTA raised `abort`.
+// Returns false when it gave up (the caller then records the timeout and
+// leaves its loop); no wait in this library is unbounded.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// ---- TMA ----------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- tcgen05 / TMEM -------------------------------------------------------------
+
+// Allocate `ncols` TMEM columns (power of two >= 32); the whole warp calls it.
+// The allocated base address is written to shared memory at `slot`.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major bf16 operand stored as rows of
+// 128 bytes (64 elements) in the 128-byte swizzle pattern TMA writes; groups of
+// 8 rows (1 KB) follow each other, so the stride-dimension offset is 1024 B.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+    d |= (uint64_t)1 << 16;                          // leading-dim offset (unused here)
+    d |= (uint64_t)(1024u >> 4) << 32;               // stride-dim offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                          // descriptor version (tcgen05)
+    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 accumulator,
+// both operands K-major, shape M x N.
+__device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
+    uint32_t d = 0;
+    d |= 1u << 4;                          // D format: f32
+    d |= 1u << 7;                          // A format: bf16
+    d |= 1u << 10;                         // B format: bf16
+    d |= (uint32_t)(N >> 3) << 17;         // N / 8
+    d |= (uint32_t)(M >> 4) << 24;         // M / 16
+    return d;
+}
+
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread completes.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// 32 lanes x 16 columns of 32-bit TMEM data: thread i of the warp receives
+// lane (base lane + i), columns col .. col+15.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- small math ---------------------------------------------------------------
+
+__device__ __forceinline__ int find_block(const int32_t* off, int nb, int r) {
+    // largest b in [0, nb) with off[b] <= r (off need not be valid: result is clamped)
+    int lo = 0, hi = nb - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(off + mid) <= r) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+}  // namespace moe

@@ -1,0 +1,198 @@
+// Block coreset: restrict each block's experts to the smallest set carrying a
+// fraction tau of the block's routing mass, then renormalise each row.
+//
+// Model card "Clover-35B-A3B-Preview -- CMF", Usage: "the block's experts
+// restricted to the set that carries 90% of its routing"; InfiniLM PR #604,
+// Summary (preview passes use block coreset routing) and Notes (full-route
+// replay: the coreset disabled, here tau >= 1).
+//
+// The arithmetic is exact so that membership matches bit for bit:
+//   * q = floor(w * 2^32) per (row, slot) (w in [0, 1], the scaling is exact);
+//     Q_e = sum of q over the block (64-bit integers, any order);
+//   * theta = ceil(tau * T), T = sum_e Q_e, with tau = M * 2^-s taken from its
+//     fp32 encoding and the product formed in 128 bits;
+//   * experts ranked by (Q desc, id asc); the coreset is the shortest prefix
+//     of that order whose mass reaches theta: its size is the number of ranks
+//     whose exclusive prefix mass is still below theta.
+// One CTA per block.
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr int kCoreThreads = 256;
+constexpr int kMaxE = 1024;
+
+__device__ __forceinline__ uint64_t mass_threshold(float tau, uint64_t T) {
+    const uint32_t u = __float_as_uint(tau);
+    const uint32_t ex = (u >> 23) & 0xFFu;
+    const uint64_t M = ex ? ((u & 0x7FFFFFu) | 0x800000u) : (u & 0x7FFFFFu);
+    const int s = ex ? 150 - (int)ex : 149;
+    const unsigned __int128 prod = (unsigned __int128)M * T;
+    if (prod == 0) return 0;
+    if (s >= 128) return 1;
+    unsigned __int128 q = prod >> s;
+    if ((q << s) != prod) q += 1;
+    return (uint64_t)q;
+}
+
+// Exclusive block-wide scan of one uint64 per thread; returns the block total in *total.
+__device__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t* warp_sums, uint64_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        uint64_t ws = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t t = __shfl_up_sync(0xffffffffu, ws, o);
+            if (lane >= o) ws += t;
+        }
+        if (lane < nw) warp_sums[lane] = ws;  // inclusive warp prefix
+    }
+    __syncthreads();
+    const uint64_t before = warp ? warp_sums[warp - 1] : 0;
+    *total = warp_sums[(blockDim.x >> 5) - 1];
+    __syncthreads();
+    return before + incl - v;
+}
+
+__global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
+    __shared__ unsigned long long Q[kMaxE];
+    __shared__ uint32_t touched[kMaxE / 32];
+    __shared__ uint32_t incore[kMaxE / 32];
+    __shared__ int32_t sorted[kMaxE];
+    __shared__ uint64_t warp_sums[32];
+    __shared__ int s_bad, s_empty;
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int E = a.E, k = a.k;
+    const int words = (E + 31) >> 5;
+    const int r0 = a.off[b], r1 = a.off[b + 1];
+    const bool valid = 0 <= r0 && r0 <= r1 && r1 <= a.R;
+    if (!valid) {
+        if (tid == 0) {
+            status_add(a.status, MOE_STATUS_BAD_OFFSETS, 1);
+            a.core_size[b] = 0;
+            if (a.n_empty) a.n_empty[b] = 0;
+        }
+        for (int w = tid; w < words; w += blockDim.x) a.keep[(size_t)b * words + w] = 0;
+        return;
+    }
+    for (int e = tid; e < E; e += blockDim.x) Q[e] = 0;
+    for (int w = tid; w < kMaxE / 32; w += blockDim.x) { touched[w] = 0; incore[w] = 0; }
+    if (tid == 0) { s_bad = 0; s_empty = 0; }
+    __syncthreads();
+    const int npairs = (r1 - r0) * k;
+    int bad = 0;
+    for (int p = tid; p < npairs; p += blockDim.x) {
+        const size_t i = (size_t)r0 * k + p;
+        const int e = a.topk_idx[i];
+        if (e < 0 || e >= E) { ++bad; continue; }
+        const float w = a.topk_w[i];
+        const unsigned long long q =
+            (w >= 0.0f && w <= 1.0f) ? __float2ull_rz(__fmul_rn(w, 4294967296.0f)) : 0ull;
+        atomicAdd(&Q[e], q);
+        atomicOr(&touched[e >> 5], 1u << (e & 31));
+    }
+    if (bad) atomicAdd(&s_bad, bad);
+    __syncthreads();
+    // block total T and touched count
+    uint64_t part = 0;
+    for (int e = tid; e < E; e += blockDim.x) part += Q[e];
+    uint64_t T;
+    (void)block_excl_scan_u64(part, warp_sums, &T);
+    int nt = 0;
+    for (int w = 0; w < words; ++w) nt += __popc(touched[w]);
+
+    const bool disabled = !(a.tau < 1.0f);
+    int c;
+    if (disabled) {
+        c = nt;
+        for (int w = tid; w < words; w += blockDim.x) incore[w] = touched[w];
+    } else {
+        const uint64_t theta = mass_threshold(a.tau, T);
+        // rank of each touched expert under (Q desc, id asc)
+        for (int e = tid; e < E; e += blockDim.x) {
+            if (!((touched[e >> 5] >> (e & 31)) & 1u)) continue;
+            const uint64_t qe = Q[e];
+            int rank = 0;
+            for (int f = 0; f < E; ++f) {
+                if (!((touched[f >> 5] >> (f & 31)) & 1u)) continue;
+                const uint64_t qf = Q[f];
+                rank += (qf > qe) || (qf == qe && f < e);
+            }
+            sorted[rank] = e;
+        }
+        __syncthreads();
+        // exclusive prefix of Q in rank order; each thread owns a contiguous run of ranks
+        const int per = (nt + blockDim.x - 1) / blockDim.x;
+        const int i0 = min(nt, tid * per), i1 = min(nt, i0 + per);
+        uint64_t local = 0;
+        for (int i = i0; i < i1; ++i) local += Q[sorted[i]];
+        uint64_t tot;
+        uint64_t run = block_excl_scan_u64(local, warp_sums, &tot);
+        int below = 0;
+        for (int i = i0; i < i1; ++i) {
+            below += run < theta;
+            run += Q[sorted[i]];
+        }
+        // c = number of ranks whose exclusive prefix is below theta
+        uint64_t cnt_total;
+        (void)block_excl_scan_u64((uint64_t)below, warp_sums, &cnt_total);
+        c = (int)cnt_total;
+        for (int i = tid; i < c; i += blockDim.x) {
+            const int e = sorted[i];
+            atomicOr(&incore[e >> 5], 1u << (e & 31));
+        }
+    }
+    __syncthreads();
+    for (int w = tid; w < words; w += blockDim.x) a.keep[(size_t)b * words + w] = incore[w];
+    if (tid == 0) a.core_size[b] = c;
+    // renormalise rows
+    int empty = 0;
+    for (int r = r0 + tid; r < r1; r += blockDim.x) {
+        const int32_t* idx = a.topk_idx + (size_t)r * k;
+        const float* w = a.topk_w + (size_t)r * k;
+        float* wo = a.w_renorm + (size_t)r * k;
+        if (disabled) {
+            for (int j = 0; j < k; ++j) wo[j] = w[j];
+            continue;
+        }
+        float s = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[j];
+            if (e >= 0 && e < E && ((incore[e >> 5] >> (e & 31)) & 1u)) s = __fadd_rn(s, w[j]);
+        }
+        if (s == 0.0f) {
+            for (int j = 0; j < k; ++j) wo[j] = 0.0f;
+            ++empty;
+            continue;
+        }
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[j];
+            const bool in = e >= 0 && e < E && ((incore[e >> 5] >> (e & 31)) & 1u);
+            wo[j] = in ? __fdiv_rn(w[j], s) : 0.0f;
+        }
+    }
+    if (empty) atomicAdd(&s_empty, empty);
+    __syncthreads();
+    if (tid == 0) {
+        if (a.n_empty) a.n_empty[b] = s_empty;
+        status_add(a.status, MOE_STATUS_EMPTY_ROWS, (uint32_t)s_empty);
+        status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)s_bad);
+    }
+}
+
+cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t st) {
+    if (a.nb <= 0) return cudaSuccess;
+    k_coreset<<<a.nb, kCoreThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

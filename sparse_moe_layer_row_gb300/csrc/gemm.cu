@@ -1,0 +1,290 @@
+// Grouped SwiGLU expert GEMMs on the 5th-generation tensor core (sm_103a).
+//
+// Expert e computes W_down[e] (silu(W_gate[e] x) * (W_up[e] x)) for every row
+// x routed to it (model card "Clover-35B-A3B-Preview -- CMF", intro: top-8 of
+// 256 experts plus a shared expert; the shared expert is one more group).
+//
+// Orientation ("weights as M"): a unit of work is (group g, weight tile m,
+// a chunk of at most NMAX rows of x).  The MMA is D[128 x N] = A[128 x K] B^T
+// with A = 128 weight rows (K-major, straight from the [E, rows, K] weight
+// tensor by a 3-D TMA box whose outer coordinate is the expert id) and
+// B = N rows of activations (K-major).  So each touched expert's weights
+// stream through shared memory once per launch, whatever the number of rows
+// routed to it, and N only has to be a multiple of 16.
+//
+//  gate/up:  A rows 32q..32q+15 = gate rows, 32q+16..32q+31 = up rows of the
+//            same 16 intermediate indices (q = 0..3), so every TMEM lane
+//            quadrant holds matching gate and up rows and the epilogue pairs
+//            them with one warp shuffle: h = silu(g) * u, stored as bf16.
+//  down:     A = 128 rows of W_down[e] (hidden outputs), B = rows of h; the
+//            epilogue scales by the pair's renormalised weight and adds into
+//            the fp32 accumulator y32[row, :] (the shared expert with weight 1).
+//
+// Pipeline (one CTA per SM, persistent over the unit list):
+//   warp 0 lane 0  TMA producer: STAGES-deep ring of (A tile, B tile) stages
+//   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per 64-wide stage,
+//                  tcgen05.commit frees the stage; accumulators double-buffered
+//                  in TMEM so the epilogue of one unit overlaps the next unit
+//   warps 2..5     epilogue: tcgen05.ld 32 lanes x 16 columns, math, stores
+// Every wait is bounded (see mbar_wait_bounded): a wait that gives up raises
+// a CTA-wide abort flag and a device status counter; all roles then leave
+// their loops, the producer waits (bounded) for the stages in flight, and the
+// TMEM is released before the CTA exits.
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legal wait
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s when draining after an abort
+
+template <int NMAX, int STAGES>
+struct GemmCfg {
+    static constexpr int kABytes = 128 * 128;
+    static constexpr int kBBytes = NMAX * 128;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBarOff = STAGES * kStageBytes;
+    static constexpr int kSmem = kBarOff + 256 + 1024;
+    static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static_assert(NMAX % 16 == 0 && NMAX <= 256, "MMA N extent");
+};
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+template <int MODE, int NMAX, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+       const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
+       const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+       GemmArgs a) {
+    using C = GemmCfg<NMAX, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const int nunits = __ldg(a.n_units);
+    if ((int)blockIdx.x >= nunits) return;  // uniform: no unit for this CTA
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (sbase - raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kBarOff);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* never = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
+        *abort_flag = 0;
+        *never = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmA2);
+        prefetch_tmap(&tmA3); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto give_up = [&]() {
+        if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+                const int4 un = __ldg(a.units + u);
+                const int g = un.x, m = un.y, start = un.z, n = un.w;
+                const int nb16 = (n + 15) >> 4;
+                const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
+                const uint32_t bytes = (uint32_t)(C::kABytes + nb16 * 2048);
+                const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
+                for (int kb = 0; kb < (K >> 6); ++kb) {
+                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full + stage, bytes);
+                    const uint32_t sA = sbase + stage * C::kStageBytes;
+                    const uint32_t sB = sA + C::kABytes;
+                    const int kc = kb * 64;
+                    if (MODE == kGateUp) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int rows = m * 64 + q * 16;
+                            if (g == a.E) {
+                                tma_load_2d(sA + (q * 32) * 128, &tmA2, kc, rows, full + stage);
+                                tma_load_2d(sA + (q * 32 + 16) * 128, &tmA3, kc, rows, full + stage);
+                            } else {
+                                tma_load_3d(sA + (q * 32) * 128, &tmA0, kc, rows, g, full + stage);
+                                tma_load_3d(sA + (q * 32 + 16) * 128, &tmA1, kc, rows, g, full + stage);
+                            }
+                        }
+                    } else {
+                        if (g == a.E) tma_load_2d(sA, &tmA2, kc, m * 128, full + stage);
+                        else tma_load_3d(sA, &tmA0, kc, m * 128, g, full + stage);
+                    }
+                    for (int t = 0; t < nb16; ++t)
+                        tma_load_2d(sB + t * 2048, mB, kc, start + t * 16, full + stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Drain: every stage must be released by the MMA before the CTA
+            // exits (all copies landed, all reads done).  Bounded; after an
+            // abort the MMA may never release, so the wait gives up quickly.
+            for (int i = 0; i < STAGES; ++i) {
+                const uint64_t lim = *abort_flag ? kDrainLimitNs : kWaitLimitNs;
+                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, never, lim)) {
+                    give_up();
+                    break;
+                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------ MMA issuer
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+                const int4 un = __ldg(a.units + u);
+                const int g = un.x, n = un.w;
+                const int n16 = (n + 15) & ~15;
+                const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
+                const uint32_t idesc = idesc_bf16_f32(128, n16);
+                if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * NMAX);
+                for (int kb = 0; kb < (K >> 6); ++kb) {
+                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = sbase + stage * C::kStageBytes;
+                    const uint32_t sB = sA + C::kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16(d, smem_desc_sw128(sA + kk * 32), smem_desc_sw128(sB + kk * 32),
+                                    idesc, (kb | kk) != 0);
+                    tc_commit(empty + stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(tfull + acc);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+            const int4 un = __ldg(a.units + u);
+            const int g = un.x, m = un.y, start = un.z, n = un.w;
+            const int n16 = (n + 15) & ~15;
+            const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitLimitNs);
+            if (__any_sync(0xffffffffu, !ok)) { give_up(); break; }
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NMAX);
+            for (int c = 0; c < n16; c += 16) {
+                float v[16];
+                tmem_ld16(tb + (uint32_t)c, v);
+                if (MODE == kGateUp) {
+                    const bool is_gate = lane < 16;
+                    const int il = m * 64 + q * 16 + (lane & 15);
+                    __nv_bfloat16* out = g == a.E ? a.hs : a.h;
+                    const int ld = g == a.E ? a.Is : a.I;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const float send = is_gate ? v[8 + t] : v[t];
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        const int col = c + (is_gate ? t : 8 + t);
+                        const float gv = is_gate ? v[t] : recv;
+                        const float uv = is_gate ? recv : v[8 + t];
+                        if (col < n)
+                            out[(size_t)(start + col) * ld + il] = __float2bfloat16_rn(silu(gv) * uv);
+                    }
+                } else {
+                    const int hrow = m * 128 + q * 32 + lane;
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int col = c + t;
+                        if (col < n) {
+                            int row;
+                            float w;
+                            if (g == a.E) { row = start + col; w = 1.0f; }
+                            else { row = __ldg(a.pair_row + start + col); w = __ldg(a.pair_w + start + col); }
+                            atomicAdd(a.y32 + (size_t)row * a.H + hrow, w * v[t]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty + acc);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+
+template <int MODE, int NMAX, int STAGES>
+static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int grid, cudaStream_t st) {
+    using C = GemmCfg<NMAX, STAGES>;
+    k_gemm<MODE, NMAX, STAGES><<<grid, 192, C::kSmem, st>>>(mp.a0, mp.a1, mp.a2, mp.a3, mp.b0,
+                                                             mp.b1, a);
+    return cudaGetLastError();
+}
+
+template <int MODE, int NMAX, int STAGES>
+static cudaError_t set_attr() {
+    using C = GemmCfg<NMAX, STAGES>;
+    return cudaFuncSetAttribute(k_gemm<MODE, NMAX, STAGES>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+}
+
+constexpr int kSmallStages = 10;
+constexpr int kLargeStages = 4;
+
+cudaError_t gemm_set_attributes() {
+    cudaError_t e;
+    if ((e = set_attr<kGateUp, kSmallN, kSmallStages>()) != cudaSuccess) return e;
+    if ((e = set_attr<kDown, kSmallN, kSmallStages>()) != cudaSuccess) return e;
+    if ((e = set_attr<kGateUp, kLargeN, kLargeStages>()) != cudaSuccess) return e;
+    return set_attr<kDown, kLargeN, kLargeStages>();
+}
+
+cudaError_t launch_gemm(int mode, int nt, const GemmMaps& mp, const GemmArgs& a, int grid,
+                        cudaStream_t st) {
+    if (nt == kSmallN)
+        return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStages>(mp, a, grid, st)
+                               : launch_one<kDown, kSmallN, kSmallStages>(mp, a, grid, st);
+    return mode == kGateUp ? launch_one<kGateUp, kLargeN, kLargeStages>(mp, a, grid, st)
+                           : launch_one<kDown, kLargeN, kLargeStages>(mp, a, grid, st);
+}
+
+}  // namespace moe

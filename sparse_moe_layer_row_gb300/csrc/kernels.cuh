@@ -1,0 +1,81 @@
+// Argument blocks and launchers of the kernels of libmoeblock (router.cu,
+// coreset.cu, scatter.cu, gemm.cu); the host code in api.cu fills them in.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+struct RouteArgs {
+    const __nv_bfloat16* x;
+    const __nv_bfloat16* wr;
+    const float* bias;
+    const int32_t* off;
+    int R, H, E, k, nb;
+    float* logits;
+    uint32_t* cnt;
+    int32_t* topk_idx;
+    float* topk_w;
+    uint32_t* status;
+};
+struct CoresetArgs {
+    const int32_t* off;
+    const int32_t* topk_idx;
+    const float* topk_w;
+    int R, E, k, nb;
+    float tau;
+    uint32_t* keep;
+    int32_t* core_size;
+    float* w_renorm;
+    int32_t* n_empty;
+    uint32_t* status;
+};
+struct ScatterArgs {
+    const int32_t* off;
+    const int32_t* topk_idx;
+    const float* w_renorm;
+    const uint32_t* keep;
+    const __nv_bfloat16* x;
+    int R, H, E, k, I, Is, nb, nt;
+    int32_t* row_block;
+    int32_t* count;
+    int32_t* expert_off;
+    int32_t* misc;
+    int4* units_gu;
+    int4* units_dn;
+    int32_t* pair_row;
+    float* pair_w;
+    __nv_bfloat16* xp;
+    float* y32;
+    uint32_t* status;
+};
+struct FinalArgs {
+    const float* y32;
+    __nv_bfloat16* y;
+    float* y_f32;
+    size_t n;
+};
+struct GemmArgs {
+    const int4* units;
+    const int32_t* n_units;
+    int E, H, I, Is;
+    __nv_bfloat16* h;
+    __nv_bfloat16* hs;
+    const int32_t* pair_row;
+    const float* pair_w;
+    float* y32;
+    uint32_t* status;
+};
+struct GemmMaps {
+    CUtensorMap a0, a1, a2, a3, b0, b1;
+};
+cudaError_t launch_route(const RouteArgs&, int num_sms, cudaStream_t);
+cudaError_t launch_coreset(const CoresetArgs&, cudaStream_t);
+cudaError_t launch_scatter(const ScatterArgs&, int num_sms, cudaStream_t);
+cudaError_t launch_finalize(const FinalArgs&, int num_sms, cudaStream_t);
+cudaError_t gemm_set_attributes();
+cudaError_t launch_gemm(int mode, int nt, const GemmMaps&, const GemmArgs&, int grid, cudaStream_t);
+
+enum { kGateUp = 0, kDown = 1 };
+
+}  // namespace moe

@@ -1,0 +1,277 @@
+"""Python binding of libmoeblock (include/moe_block.h): argument marshalling only.
+
+Every step of the layer runs in the CUDA kernels of the library; this module
+checks tensor devices, dtypes and shapes, passes raw pointers and the current
+CUDA stream through ctypes, and turns a non-OK status into an exception.
+There is no CPU fallback: without the compiled library (or without a CUDA
+device) every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+STATUS_NAMES = ("nonfinite_logits", "bad_expert_id", "bad_offsets", "empty_rows", "wait_timeout")
+STATUS_WORDS = 8
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"moe status {status}: {msg}")
+        self.status = status
+
+
+class moe_dims(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("I", ctypes.c_int32), ("Is", ctypes.c_int32), ("max_rows", ctypes.c_int32),
+                ("max_blocks", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """The loaded libmoeblock.so.  Raises if it is not built (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise ImportError(f"libmoeblock.so is not built ({path}); run "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        _build.build()
+    L = ctypes.CDLL(path)
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    L.moe_version.restype = i32
+    L.moe_last_error.restype = ctypes.c_char_p
+    L.moe_workspace_bytes.restype = sz
+    L.moe_workspace_bytes.argtypes = [ctypes.POINTER(moe_dims)]
+    L.moe_plan_create.restype = ctypes.c_int
+    L.moe_plan_create.argtypes = [ctypes.POINTER(moe_dims), P, P, P, P, P, P, P,
+                                  ctypes.POINTER(P)]
+    L.moe_plan_destroy.restype = None
+    L.moe_plan_destroy.argtypes = [P]
+    L.moe_block_route.restype = ctypes.c_int
+    L.moe_block_route.argtypes = [P, P, i32, P, i32, P, P, P, P, sz, P]
+    L.moe_block_coreset.restype = ctypes.c_int
+    L.moe_block_coreset.argtypes = [P, i32, P, i32, P, P, ctypes.c_float, P, P, P, P, P, sz, P]
+    L.moe_block_forward.restype = ctypes.c_int
+    L.moe_block_forward.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, sz, P]
+    L.moe_read_device_status.restype = ctypes.c_int
+    L.moe_read_device_status.argtypes = [P, P, P]
+    L.moe_clear_device_status.restype = ctypes.c_int
+    L.moe_clear_device_status.argtypes = [P, P]
+    _lib = L
+    return L
+
+
+def _check(rc: int):
+    if rc != MOE_OK:
+        raise MoeError(rc, load().moe_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def moe_version() -> int:
+    return int(load().moe_version())
+
+
+def moe_workspace_bytes(dims: moe_dims) -> int:
+    return int(load().moe_workspace_bytes(ctypes.byref(dims)))
+
+
+class Plan:
+    """moe_plan_create / moe_plan_destroy.  Keeps the weight tensors alive."""
+
+    def __init__(self, dims: moe_dims, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down):
+        d = dims
+        _need(w_router, "w_router", torch.bfloat16, (d.E, d.H))
+        _need(w_gate, "w_gate", torch.bfloat16, (d.E, d.I, d.H))
+        _need(w_up, "w_up", torch.bfloat16, (d.E, d.I, d.H))
+        _need(w_down, "w_down", torch.bfloat16, (d.E, d.H, d.I))
+        _need(ws_gate, "ws_gate", torch.bfloat16, (d.Is, d.H))
+        _need(ws_up, "ws_up", torch.bfloat16, (d.Is, d.H))
+        _need(ws_down, "ws_down", torch.bfloat16, (d.H, d.Is))
+        self.dims = d
+        self.weights = (w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down)
+        self.device = w_router.device
+        h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _check(load().moe_plan_create(ctypes.byref(d), *[_ptr(w) for w in self.weights],
+                                          ctypes.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None) and self.handle.value:
+            load().moe_plan_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_bytes(self) -> int:
+        return moe_workspace_bytes(self.dims)
+
+    def new_workspace(self) -> torch.Tensor:
+        return torch.empty(self.workspace_bytes(), dtype=torch.uint8, device=self.device)
+
+
+def moe_block_route(plan: Plan, x, block_offsets, logit_bias, topk_idx, topk_w, workspace,
+                    stream=None):
+    d = plan.dims
+    R = x.shape[0]
+    nb = block_offsets.shape[0] - 1
+    _need(x, "x", torch.bfloat16, (R, d.H))
+    _need(block_offsets, "block_offsets", torch.int32)
+    if logit_bias is not None:
+        _need(logit_bias, "logit_bias", torch.float32, (nb, d.E))
+    _need(topk_idx, "topk_idx", torch.int32, (R, d.k))
+    _need(topk_w, "topk_w", torch.float32, (R, d.k))
+    _need(workspace, "workspace", torch.uint8)
+    _check(load().moe_block_route(plan.handle, _ptr(x), R, _ptr(block_offsets), nb,
+                                  _ptr(logit_bias), _ptr(topk_idx), _ptr(topk_w),
+                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_block_coreset(plan: Plan, block_offsets, topk_idx, topk_w, tau: float, keep, core_size,
+                      w_renorm, n_empty, workspace, stream=None):
+    d = plan.dims
+    R = topk_idx.shape[0]
+    nb = block_offsets.shape[0] - 1
+    _need(block_offsets, "block_offsets", torch.int32)
+    _need(topk_idx, "topk_idx", torch.int32, (R, d.k))
+    _need(topk_w, "topk_w", torch.float32, (R, d.k))
+    _need(keep, "keep", torch.int32, (nb, (d.E + 31) // 32))
+    _need(core_size, "core_size", torch.int32, (nb,))
+    _need(w_renorm, "w_renorm", torch.float32, (R, d.k))
+    if n_empty is not None:
+        _need(n_empty, "n_empty", torch.int32, (nb,))
+    _need(workspace, "workspace", torch.uint8)
+    _check(load().moe_block_coreset(plan.handle, R, _ptr(block_offsets), nb, _ptr(topk_idx),
+                                    _ptr(topk_w), ctypes.c_float(tau), _ptr(keep),
+                                    _ptr(core_size), _ptr(w_renorm), _ptr(n_empty),
+                                    _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_block_forward(plan: Plan, x, block_offsets, topk_idx, w_renorm, keep, y, y_f32, workspace,
+                      stream=None):
+    d = plan.dims
+    R = x.shape[0]
+    nb = block_offsets.shape[0] - 1
+    _need(x, "x", torch.bfloat16, (R, d.H))
+    _need(block_offsets, "block_offsets", torch.int32)
+    _need(topk_idx, "topk_idx", torch.int32, (R, d.k))
+    _need(w_renorm, "w_renorm", torch.float32, (R, d.k))
+    _need(keep, "keep", torch.int32, (nb, (d.E + 31) // 32))
+    _need(y, "y", torch.bfloat16, (R, d.H))
+    if y_f32 is not None:
+        _need(y_f32, "y_f32", torch.float32, (R, d.H))
+    _need(workspace, "workspace", torch.uint8)
+    _check(load().moe_block_forward(plan.handle, _ptr(x), R, _ptr(block_offsets), nb,
+                                    _ptr(topk_idx), _ptr(w_renorm), _ptr(keep), _ptr(y),
+                                    _ptr(y_f32), _ptr(workspace), workspace.numel(),
+                                    _stream(stream)))
+
+
+def moe_read_device_status(workspace: torch.Tensor, stream=None) -> dict:
+    _need(workspace, "workspace", torch.uint8)
+    out = (ctypes.c_uint32 * STATUS_WORDS)()
+    _check(load().moe_read_device_status(_ptr(workspace), _stream(stream), out))
+    return {name: int(out[i]) for i, name in enumerate(STATUS_NAMES)}
+
+
+def moe_clear_device_status(workspace: torch.Tensor, stream=None):
+    _need(workspace, "workspace", torch.uint8)
+    _check(load().moe_clear_device_status(_ptr(workspace), _stream(stream)))
+
+
+class MoeBlockLayer:
+    """The whole pass: route -> coreset -> forward, with its own workspace and buffers.
+
+    Weights are the seven bf16 tensors of moe_plan_create; ``max_rows`` and
+    ``max_blocks`` size the workspace.  ``__call__`` enqueues three C-ABI calls
+    on the current stream and returns y (bf16 [R, H]).
+    """
+
+    def __init__(self, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, k: int,
+                 max_rows: int, max_blocks: int):
+        E, H = w_router.shape
+        I = w_gate.shape[1]
+        Is = ws_gate.shape[0]
+        self.dims = moe_dims(H, E, k, I, Is, max_rows, max_blocks)
+        self.plan = Plan(self.dims, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down)
+        dev = w_router.device
+        self.workspace = self.plan.new_workspace()
+        R, nb, words = max_rows, max_blocks, (E + 31) // 32
+        self._topk_idx = torch.empty(R, k, dtype=torch.int32, device=dev)
+        self._topk_w = torch.empty(R, k, dtype=torch.float32, device=dev)
+        self._w_renorm = torch.empty(R, k, dtype=torch.float32, device=dev)
+        self._keep = torch.empty(nb, words, dtype=torch.int32, device=dev)
+        self._core = torch.empty(nb, dtype=torch.int32, device=dev)
+        self._empty = torch.empty(nb, dtype=torch.int32, device=dev)
+        self._y = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+
+    def route(self, x, block_offsets, bias=None, stream=None):
+        R = x.shape[0]
+        idx, w = self._topk_idx[:R], self._topk_w[:R]
+        moe_block_route(self.plan, x, block_offsets, bias, idx, w, self.workspace, stream)
+        return idx, w
+
+    def coreset(self, block_offsets, topk_idx, topk_w, tau, stream=None):
+        R = topk_idx.shape[0]
+        nb = block_offsets.shape[0] - 1
+        keep, core, empty = self._keep[:nb], self._core[:nb], self._empty[:nb]
+        wr = self._w_renorm[:R]
+        moe_block_coreset(self.plan, block_offsets, topk_idx, topk_w, tau, keep, core, wr, empty,
+                          self.workspace, stream)
+        return keep, core, wr, empty
+
+    def forward(self, x, block_offsets, topk_idx, w_renorm, keep, y=None, y_f32=None,
+                stream=None):
+        R = x.shape[0]
+        y = self._y[:R] if y is None else y
+        moe_block_forward(self.plan, x, block_offsets, topk_idx, w_renorm, keep, y, y_f32,
+                          self.workspace, stream)
+        return y
+
+    def __call__(self, x, block_offsets, tau: float, bias=None, y=None, y_f32=None, stream=None):
+        idx, w = self.route(x, block_offsets, bias, stream)
+        keep, _, wr, _ = self.coreset(block_offsets, idx, w, tau, stream)
+        return self.forward(x, block_offsets, idx, wr, keep, y, y_f32, stream)
+
+    def status(self, stream=None) -> dict:
+        return moe_read_device_status(self.workspace, stream)

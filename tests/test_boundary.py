@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+symbol the public header declares, and rejects invalid arguments on the host
+with a status and a message, before any CUDA work."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from sparse_moe_layer_row_gb300 import build as cbuild
+from sparse_moe_layer_row_gb300 import moe_block as mb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return mb.load()
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"\b(moe_[a-z_0-9]+)\s*\(", src):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("moe_block_route", "moe_block_coreset", "moe_block_forward"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_version(lib):
+    assert mb.moe_version() >= 100
+
+
+def dims(**kw):
+    d = dict(H=2048, E=256, k=8, I=512, Is=512, max_rows=32, max_blocks=1)
+    d.update(kw)
+    return mb.moe_dims(**d)
+
+
+def test_workspace_bytes_valid_and_monotone(lib):
+    a = mb.moe_workspace_bytes(dims())
+    b = mb.moe_workspace_bytes(dims(max_rows=8192, max_blocks=256))
+    assert 0 < a < b
+    assert a % 1024 == 0
+
+
+@pytest.mark.parametrize("bad", [dict(H=0), dict(H=1000), dict(E=0), dict(E=1025), dict(k=0),
+                                 dict(k=33), dict(E=4, k=5), dict(I=100), dict(Is=0),
+                                 dict(max_rows=0), dict(max_blocks=0)], ids=str)
+def test_workspace_bytes_rejects_bad_dims(lib, bad):
+    assert mb.moe_workspace_bytes(dims(**bad)) == 0
+    assert lib.moe_last_error().decode() != ""
+
+
+def test_plan_create_rejects_null_and_misaligned_weights(lib):
+    h = ctypes.c_void_p()
+    rc = lib.moe_plan_create(ctypes.byref(dims()), *([None] * 7), ctypes.byref(h))
+    assert rc == -1 and b"w_router" in lib.moe_last_error()
+    ptrs = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(7)]
+    ptrs[3] = ctypes.c_void_p(0x40008)
+    rc = lib.moe_plan_create(ctypes.byref(dims()), *ptrs, ctypes.byref(h))
+    assert rc == -1 and b"w_down" in lib.moe_last_error()
+    rc = lib.moe_plan_create(ctypes.byref(dims(H=100)), *ptrs, ctypes.byref(h))
+    assert rc == -2
+    rc = lib.moe_plan_create(None, *ptrs, ctypes.byref(h))
+    assert rc == -1
+
+
+def test_calls_reject_null_plan(lib):
+    ws = ctypes.c_void_p(0x100000)
+    rc = lib.moe_block_route(None, ws, 4, ws, 1, None, ws, ws, ws, 1 << 20, None)
+    assert rc == -1 and b"plan" in lib.moe_last_error()
+    rc = lib.moe_block_coreset(None, 4, ws, 1, ws, ws, ctypes.c_float(0.9), ws, ws, ws, None, ws,
+                               1 << 20, None)
+    assert rc == -1
+    rc = lib.moe_block_forward(None, ws, 4, ws, 1, ws, ws, ws, ws, None, ws, 1 << 20, None)
+    assert rc == -1
+
+
+def test_status_calls_reject_bad_workspace(lib):
+    out = (ctypes.c_uint32 * 8)()
+    assert lib.moe_read_device_status(None, None, out) == -1
+    assert lib.moe_read_device_status(ctypes.c_void_p(0x100010), None, out) == -1
+    assert lib.moe_clear_device_status(None, None) == -1
+
+
+def test_binding_requires_cuda_tensors():
+    x = torch.zeros(4, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mb._need(x, "x", torch.bfloat16, (4, 256))
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(mb, "_lib", None)
+    monkeypatch.setattr(cbuild, "LIB", "/nonexistent/libmoeblock.so")
+    with pytest.raises(ImportError):
+        mb.load()
+
+
+def test_product_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "sparse_moe_layer_row_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", src, re.M), f
+                assert "moe_oracle" not in src, f

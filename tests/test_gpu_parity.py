@@ -1,0 +1,195 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on seeded synthetic inputs.
+
+Routing ids and weights, coreset membership and renormalised weights are
+compared bit for bit; layer outputs within |d| <= 2e-3 + 1e-2 |ref|.
+Full-size workloads compare routing and coreset on every row and the layer
+output on a sample of rows that the oracle evaluates one by one.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from sparse_moe_layer_row_gb300 import moe_block, workloads as W
+from tests.parity_util import (Case, assert_close, assert_coreset_equal, assert_route_equal)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    moe_block.load()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def _full(case: Case, tau=None, rows=None):
+    g = case.run(tau)
+    ref = case.oracle_route()
+    assert_route_equal(g, ref)
+    case.oracle_coreset(tau)
+    assert_coreset_equal(g, ref)
+    case.oracle_forward(rows=rows)
+    err = assert_close(g["y32"], ref["y"], rows, "y_f32")
+    assert_close(g["y"], ref["y"], rows, "y (bf16)")
+    assert case.status["wait_timeout"] == 0 and case.status["bad_expert_id"] == 0
+    return err
+
+
+def test_tiny_config():
+    case = Case(W.TINY)
+    _full(case)
+
+
+def test_tiny_config_coreset_disabled():
+    case = Case(W.TINY)
+    _full(case, tau=1.0)
+    assert case.gpu["core"][0] == len(set(case.gpu["idx"].reshape(-1).tolist()))
+
+
+@pytest.mark.parametrize("tau", [0.9, 0.5, 0.99, 1.0])
+def test_block32_full_shape(tau):
+    case = Case(W.BLOCK32)
+    _full(case, tau=tau)
+
+
+def test_blocks16_zipf_bias():
+    case = Case(W.BLOCKS16_ZIPF)
+    rows = list(range(0, 512, 9))
+    _full(case, rows=rows)
+    sizes = case.gpu["core"]
+    assert sizes.min() < sizes.max(), "Zipf bias should make coreset sizes vary across blocks"
+
+
+@pytest.mark.parametrize("w", W.ROWS2048, ids=lambda w: w.name)
+def test_rows2048(w):
+    case = Case(w)
+    rows = list(range(0, 2048, 61)) + [2047]
+    _full(case, rows=rows)
+
+
+def test_prefill8192():
+    case = Case(W.PREFILL8192)
+    rows = list(range(0, 8192, 257)) + [8191]
+    _full(case, rows=rows)
+
+
+# --------------------------------------------------------------------------- edge cases
+
+def _small(H=256, E=16, k=4, I=128, Is=128, rows=(32,), tau=0.9, seed=5, sigma_r=0.05):
+    return W.Workload(name="edge", H=H, E=E, k=k, I=I, Is=Is, block_rows=tuple(rows), tau=tau,
+                      sigma_r=sigma_r, x_seed=seed, w_seed=seed)
+
+
+@pytest.mark.parametrize("rows", [(1,), (3,), (5, 0, 7), (13, 1, 1, 30), (37, 64, 50)],
+                         ids=str)
+def test_ragged_blocks_and_rows(rows):
+    _full(Case(_small(rows=rows)))
+
+
+@pytest.mark.parametrize("E,k", [(20, 1), (20, 20), (37, 5), (64, 8), (40, 32)])
+def test_expert_counts(E, k):
+    _full(Case(_small(E=E, k=k, rows=(16, 9))))
+
+
+@pytest.mark.parametrize("H,I,Is", [(512, 64, 192), (768, 320, 64), (256, 576, 128)])
+def test_hidden_and_intermediate_sizes(H, I, Is):
+    _full(Case(_small(H=H, I=I, Is=Is, rows=(24, 8))))
+
+
+def test_many_rows_small_shape_multichunk():
+    """More than 256 rows per expert: several row chunks per expert and per shared unit."""
+    w = _small(E=4, k=2, rows=(200, 300, 100), H=256, I=128, Is=64)
+    _full(Case(w), rows=list(range(0, 600, 7)))
+
+
+def test_router_ties_go_to_lower_id():
+    w = _small()
+    T = W.make_tensors(w, device="cuda")
+    T.w_router[9] = T.w_router[2]
+    T.w_router[14] = T.w_router[2]
+    _full(Case(w, T=T))
+
+
+def test_nonfinite_logits_counted_and_ranked_last():
+    w = _small()
+    T = W.make_tensors(w, device="cuda")
+    bias = torch.zeros(1, w.E, dtype=torch.float32, device="cuda")
+    bias[0, 3] = float("nan")
+    bias[0, 5] = float("-inf")
+    case = Case(w, T=T, bias=bias)
+    g = case.run()
+    ref = case.oracle_route()
+    assert_route_equal(g, ref)
+    assert case.status["nonfinite_logits"] == ref["nonfinite"] == 2 * w.R
+    assert not np.isin(g["idx"], [3, 5]).any()
+
+
+def test_empty_rows_keep_shared_expert_only():
+    """At a very low tau the coreset shrinks to the heaviest expert or two; rows that
+    selected none of them keep only the shared expert."""
+    w = _small(E=32, k=2, rows=(32,), tau=0.05)
+    case = Case(w)
+    g = case.run()
+    ref = case.oracle_route()
+    assert_route_equal(g, ref)
+    case.oracle_coreset()
+    assert_coreset_equal(g, ref)
+    assert int(ref["empty"].sum()) > 0
+    case.oracle_forward()
+    assert_close(g["y32"], ref["y"])
+    assert case.status["empty_rows"] == int(ref["empty"].sum())
+
+
+def test_bad_expert_ids_are_counted_not_fatal():
+    w = _small()
+    case = Case(w)
+    L = case.layer
+    idx, wt = L.route(case.x, case.off)
+    keep, core, wr, empty = L.coreset(case.off, idx, wt, w.tau)
+    idx2 = idx.clone()
+    idx2[0, 0] = w.E + 5
+    idx2[1, 1] = -2
+    moe_block.moe_clear_device_status(L.workspace)
+    L.coreset(case.off, idx2, wt, w.tau)
+    y = L.forward(case.x, case.off, idx2, wr, keep)
+    torch.cuda.synchronize()
+    st = L.status()
+    assert st["bad_expert_id"] == 2 and st["wait_timeout"] == 0
+    assert torch.isfinite(y.float()).all()
+
+
+def test_bad_block_offsets_are_counted():
+    w = _small(rows=(16, 16))
+    case = Case(w)
+    bad = torch.tensor([0, 20, 12], dtype=torch.int32, device="cuda")
+    idx, wt = case.layer.route(case.x, case.off)
+    moe_block.moe_clear_device_status(case.layer.workspace)
+    case.layer.coreset(bad, idx, wt, w.tau)
+    torch.cuda.synchronize()
+    assert case.layer.status()["bad_offsets"] == 1
+
+
+def test_repeat_calls_are_deterministic_in_routing():
+    case = Case(W.TINY)
+    g1 = {k: v.copy() for k, v in case.run().items()}
+    g2 = case.run()
+    for key in ("idx", "w", "keep", "wr", "core"):
+        assert np.array_equal(np.asarray(g1[key]), np.asarray(g2[key])), key
+    assert np.allclose(g1["y32"], g2["y32"], rtol=1e-6, atol=1e-6)
+
+
+def test_workspace_reuse_across_shapes():
+    """One layer sized for the largest call serves smaller calls in between."""
+    w = _small(rows=(64, 64))
+    T = W.make_tensors(w, device="cuda")
+    big = Case(w, T=T)
+    _full(big)
+    small_off = torch.tensor([0, 5], dtype=torch.int32, device="cuda")
+    x5 = T.x[:5].contiguous()
+    c2 = Case(w, T=T, block_offsets=[0, 5], x=x5)
+    _full(c2)
