@@ -1,0 +1,437 @@
+"""Benchmark of the block-coreset MoE FFN on GB300.
+
+One step = one pass of the whole layer over one batch: route -> coreset ->
+forward, through the C ABI of libmoeblock, replayed as a CUDA graph with the
+inputs resident in HBM.  L2 is flushed (a 256 MiB write) between steps,
+outside the timed events.  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Under torchrun (N > 1) every rank runs the same workload shape on its own
+GPU with its own rows (weak scaling); rank 0 prints the line with the
+maximum time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_moe_layer_row_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE block-layer rows/s and expert-weight HBM GB/s (% of roofline) on 1 GB300"
+DEFAULT_WORKLOAD = W.BLOCK32.name
+FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 8   # route, coreset, prep, count, fill, gate/up, down, final
+
+
+# --------------------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+def rank_workload(w: W.Workload, rank: int) -> int:
+    """x seed of a rank: same shape, distinct rows (weak scaling; no data exchange)."""
+    return w.x_seed + 7919 * rank
+
+
+def reduce_max(value: float, ws: int, device=None) -> float:
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh", "kernels.cuh"):
+        with open(os.path.join(ROOT, "sparse_moe_layer_row_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per gate/up launch from a committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "gateup_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    entry = rec.get(workload)
+    if not entry or entry.get("source_hash") != gemm_source_hash():
+        return None
+    return float(entry["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not getattr(self, "out", ""):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def accounting(w: W.Workload, R: int, n_core_experts: int, n_pairs: int):
+    """Algorithmic bytes and flops of one step and of one gate/up launch."""
+    H, E, I, Is = w.H, w.E, w.I, w.Is
+    expert_bytes = 3 * H * I * 2
+    shared_bytes = 3 * H * Is * 2
+    router_bytes = E * H * 2
+    step_bytes = n_core_experts * expert_bytes + shared_bytes + router_bytes + 2 * R * H * 2
+    step_flops = 2.0 * R * H * E + n_pairs * 6.0 * H * I + R * 6.0 * H * Is
+    # gate/up launch: the touched experts' and the shared expert's gate and up
+    # weights plus the rows of x, each read once (intermediates are not counted)
+    gu_bytes = n_core_experts * 2 * H * I * 2 + 2 * H * Is * 2 + R * H * 2
+    weight_bytes = n_core_experts * expert_bytes + shared_bytes + router_bytes
+    return dict(step_bytes=step_bytes, step_flops=step_flops, gu_bytes=gu_bytes,
+                weight_bytes=weight_bytes)
+
+
+# --------------------------------------------------------------------------- oracle arm
+
+def oracle_step(w: W.Workload, x_u16, wr_u16, off, bias, experts_fn, shared, nthreads):
+    import oracle
+    idx, wt, _, _ = oracle.route(x_u16, wr_u16, off, w.k, bias=bias, nthreads=nthreads)
+    keep, core, wr, empty, _ = oracle.coreset(off, idx, wt, w.E, w.tau)
+    used = oracle.surviving_experts(idx, keep, off, w.E)
+    y = oracle.forward(x_u16, off, idx, wr, keep, experts_fn(used), shared, w.E,
+                       nthreads=nthreads)
+    return y, len(used)
+
+
+def oracle_inputs(w: W.Workload, x_seed: int):
+    """Inputs of the workload as numpy bf16 bit patterns (generated on a GPU when
+    one is present, for speed; the generator is device-independent)."""
+    import oracle  # noqa: F401
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+
+    def u16(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    x = u16(W.make_x(w, dev, seed=x_seed))
+    wr = u16(W.make_router(w, dev))
+    sg, su, sd = (u16(t) for t in W.make_shared(w, dev))
+    bias = W.zipf_bias(w, seed=x_seed)
+    bias = None if bias is None else bias.numpy()
+    cache = {}
+
+    def experts_fn(used):
+        need = [e for e in used if e not in cache]
+        for e in need:
+            cache[e] = tuple(u16(W.make_expert_slice(w, which, e, e + 1, dev)[0])
+                             for which in ("gate", "up", "down"))
+        return {e: cache[e] for e in used}
+
+    return x, wr, np.asarray(w.block_offsets(), np.int32), bias, experts_fn, (sg, su, sd)
+
+
+def cpu_baseline(w: W.Workload, x_seed: int, budget_s: float = 10.0, max_steps: int = 50):
+    import oracle
+    nthreads = oracle.default_threads()
+    x, wr, off, bias, experts_fn, shared = oracle_inputs(w, x_seed)
+    oracle_step(w, x, wr, off, bias, experts_fn, shared, nthreads)  # warm: experts generated
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_steps:
+        oracle_step(w, x, wr, off, bias, experts_fn, shared, nthreads)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": w.R * n / dt, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{n} full steps of {w.name} ({w.R} rows; route+coreset+fp64 FFN), "
+                      f"{dt:.2f} s"}
+
+
+def run_reference(args, w: W.Workload):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    nthreads = oracle.default_threads()
+    x, wr, off, bias, experts_fn, shared = oracle_inputs(w, rank_workload(w, 0))
+    for _ in range(args.warmup):
+        oracle_step(w, x, wr, off, bias, experts_fn, shared, nthreads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, x, wr, off, bias, experts_fn, shared, nthreads)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = w.R * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, "CPU oracle; no GPU"),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nthreads, "kind": "oracle",
+                         "sample": f"{args.steps} full steps of {w.name} ({w.R} rows each)"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w: W.Workload, l2: str):
+    return {"workload": w.name, "rows": w.R, "blocks": w.nb, "block_rows": w.block_rows[0],
+            "hidden": w.H, "experts": w.E, "top_k": w.k, "intermediate": w.I,
+            "shared_intermediate": w.Is, "coreset_mass": w.tau, "l2": l2,
+            "parallelism": "replicas (weak scaling by rows)"}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, w: W.Workload):
+    from sparse_moe_layer_row_gb300 import moe_block
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    moe_block.load()
+    x_seed = rank_workload(w, rank)
+    T = W.make_tensors(w, device=dev, x_seed=x_seed)
+    layer = moe_block.MoeBlockLayer(T.w_router, T.w_gate, T.w_up, T.w_down, T.ws_gate, T.ws_up,
+                                    T.ws_down, k=w.k, max_rows=w.R, max_blocks=w.nb)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    y = torch.empty(w.R, w.H, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        layer(T.x, T.block_offsets, w.tau, bias=T.bias, y=y)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize()
+    st = layer.status()
+    if st["wait_timeout"] or st["bad_expert_id"]:
+        raise RuntimeError(f"device status after warm-up: {st}")
+
+    # routing facts for the accounting (deterministic, identical every step)
+    idx = layer._topk_idx[:w.R].cpu().numpy()
+    keep = layer._keep[:w.nb].cpu().numpy().view(np.uint32)
+    off = np.asarray(w.block_offsets())
+    used, pairs = set(), 0
+    for b in range(w.nb):
+        for r in range(off[b], off[b + 1]):
+            for e in idx[r]:
+                if (keep[b, e // 32] >> (e % 32)) & 1:
+                    used.add(int(e))
+                    pairs += 1
+    acc = accounting(w, w.R, len(used), pairs)
+
+    # capture one step as a graph; the forward records 5 events around its kernels
+    fwd_ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    layer.plan.set_forward_events(fwd_ev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    layer.plan.set_forward_events(None)
+    torch.cuda.synchronize()
+
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    step_ms, gu_ms, dn_ms, sc_ms = [], [], [], []
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(float(i))
+                step_ev[i][0].record(stream)
+                graph.replay()
+                step_ev[i][1].record(stream)
+                # kernel events are overwritten by the next replay: read them now
+                step_ev[i][1].synchronize()
+                step_ms.append(step_ev[i][0].elapsed_time(step_ev[i][1]))
+                sc_ms.append(fwd_ev[0].elapsed_time(fwd_ev[1]))
+                gu_ms.append(fwd_ev[1].elapsed_time(fwd_ev[2]))
+                dn_ms.append(fwd_ev[2].elapsed_time(fwd_ev[3]))
+        torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = reduce_max(sum(step_ms), ws, dev)
+    clocks = clk.summary()
+
+    # end to end through the public API with host buffers (pinned), no graph
+    x_host = T.x.cpu().pin_memory()
+    off_host = T.block_offsets.cpu().pin_memory()
+    y_host = torch.empty(w.R, w.H, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(T.x)
+    off_dev = torch.empty_like(T.block_offsets)
+    e2e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            x_dev.copy_(x_host, non_blocking=True)
+            off_dev.copy_(off_host, non_blocking=True)
+            y_host.copy_(layer(x_dev, off_dev, w.tau, bias=T.bias), non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_ms = 0.0
+        for i in range(e2e_steps):
+            flush.fill_(float(i))
+            e0.record(stream)
+            x_dev.copy_(x_host, non_blocking=True)
+            off_dev.copy_(off_host, non_blocking=True)
+            y_host.copy_(layer(x_dev, off_dev, w.tau, bias=T.bias), non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            e2e_ms += e0.elapsed_time(e1)
+    e2e_ms = reduce_max(e2e_ms, ws, dev)
+    h2d = x_host.numel() * 2 + off_host.numel() * 4
+    d2h = y_host.numel() * 2
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peaks = load_peaks()
+    t_step = total_ms / 1e3 / args.steps
+    t_gu = statistics.mean(gu_ms) / 1e3
+    value = w.R * ws * args.steps / (total_ms / 1e3)
+    achieved = acc["gu_bytes"] / t_gu / 1e9
+    traffic = recorded_traffic(w.name)
+    step_frac = max(acc["step_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                    acc["step_flops"] / (peaks["bf16_tflops_sustained"] * 1e12)) / t_step
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,s) bf16 inputs and weights; no trained weights)",
+        "config": config_of(w, f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)"),
+        "expert_weight_gbs": acc["weight_bytes"] / t_step / 1e9,
+        "step_roofline_frac": step_frac,
+        "roofline": {"bound": "hbm", "kernel": "k_gemm gate/up (tcgen05)",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": acc["gu_bytes"],
+                     "launch_us": t_gu * 1e6, "peak_source": peaks["source"]},
+        "kernel_us": {"scatter": 1e3 * statistics.mean(sc_ms), "gate_up": t_gu * 1e6,
+                      "down": 1e3 * statistics.mean(dn_ms)},
+        "coreset": {"experts": len(used), "pairs": pairs},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": w.R * ws * e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, x_seed, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = W.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

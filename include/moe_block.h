@@ -82,7 +82,9 @@ enum {
 };
 
 /* Bytes of device workspace needed for calls up to `dims`; 0 on invalid dims.
- * The workspace must be 256-byte aligned. */
+ * The workspace must be 256-byte aligned.  Its status counters are whatever
+ * the memory held: zero them once (moe_clear_device_status or a memset)
+ * before reading them. */
 size_t moe_workspace_bytes(const moe_dims* dims);
 
 /* Create a plan.  Weights (device, bf16, row-major, 16-byte aligned):
@@ -149,6 +151,19 @@ moe_status moe_block_forward(const moe_plan* plan, const void* x, int32_t R,
                              const int32_t* block_offsets, int32_t nb, const int32_t* topk_idx,
                              const float* w_renorm, const uint32_t* keep, void* y, float* y_f32,
                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Same type as cudaEvent_t. */
+typedef struct CUevent_st* moe_event_t;
+
+/* Optional per-kernel timing of moe_block_forward.  With n_events == 5 the
+ * forward records, on its stream, events[0] before the pair scatter,
+ * events[1] before the gate/up GEMM, events[2] before the down GEMM,
+ * events[3] before the final bf16 store and events[4] after it.  The events
+ * belong to the caller and must outlive every forward that records them;
+ * n_events == 0 (events NULL) turns the recording off.  Not thread-safe
+ * against concurrent forwards on the same plan. */
+moe_status moe_plan_set_forward_events(moe_plan* plan, moe_event_t const* events,
+                                       int32_t n_events);
 
 /* Copy the MOE_STATUS_WORDS counters to out[] (host); synchronises `stream`. */
 moe_status moe_read_device_status(const void* workspace, moe_stream_t stream, uint32_t* out);

@@ -18,6 +18,8 @@ struct moe_plan {
     int num_sms;
     const void *wr, *wg, *wu, *wd, *sg, *su, *sd;
     CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd;
+    cudaEvent_t fwd_events[5];
+    int n_fwd_events;
 };
 
 namespace {
@@ -236,10 +238,12 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     const moe_dims& d = p->d;
     const Layout L = make_layout(d);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int nt = R <= 64 ? kSmallN : kLargeN;
+    const bool small = R <= 64;
+    const int nt_gu = small ? kSmallN : kLargeN;
+    const int nt_dn = small ? kSmallN : kLargeNDown;
 
     ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, static_cast<const __nv_bfloat16*>(x),
-                   R, d.H, d.E, d.k, d.I, d.Is, nb, nt,
+                   R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
                    at<int32_t>(workspace, L.row_block), at<int32_t>(workspace, L.count),
                    at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
                    at<int4>(workspace, L.units_gu), at<int4>(workspace, L.units_dn),
@@ -252,26 +256,57 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     dn.a0 = p->tm_wd; dn.a1 = p->tm_wd; dn.a2 = p->tm_sd; dn.a3 = p->tm_sd;
     bool good = encode_bf16(&gu.b0, at<void>(workspace, L.xp), d.H, (uint64_t)L.max_pairs, 0, 16, L2A) &&
                 encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, 16, L2A) &&
-                encode_bf16(&dn.b0, at<void>(workspace, L.h), d.I, (uint64_t)L.max_pairs, 0, 16, L2A) &&
-                encode_bf16(&dn.b1, at<void>(workspace, L.hs), d.Is, (uint64_t)d.max_rows, 0, 16, L2A);
+                encode_bf16(&dn.b0, at<void>(workspace, L.h), 2 * (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
+                            16, L2A) &&
+                encode_bf16(&dn.b1, at<void>(workspace, L.hs), 2 * (uint64_t)d.Is,
+                            (uint64_t)d.max_rows, 0, 16, L2A);
     if (!good) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation tensor");
     GemmArgs ga{at<int4>(workspace, L.units_gu), at<int32_t>(workspace, L.misc) + 1, d.E, d.H, d.I,
                 d.Is, at<__nv_bfloat16>(workspace, L.h), at<__nv_bfloat16>(workspace, L.hs),
                 at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
                 at<float>(workspace, L.y32), at<uint32_t>(workspace, L.status)};
-    cudaError_t e = launch_scatter(sa, p->num_sms, st);
+    // Under stream capture an event record must be an external node to be
+    // recorded at every graph launch (a plain record only orders the capture).
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (p->n_fwd_events == 5 && cudaStreamIsCapturing(st, &cap) != cudaSuccess)
+        return fail(MOE_ERR_CUDA, "cudaStreamIsCapturing failed");
+    const unsigned ev_flags =
+        cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    auto mark = [&](int i) {
+        return p->n_fwd_events == 5 ? cudaEventRecordWithFlags(p->fwd_events[i], st, ev_flags)
+                                    : cudaSuccess;
+    };
+    cudaError_t e = mark(0);
+    if (e == cudaSuccess) e = launch_scatter(sa, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
-    e = launch_gemm(0, nt, gu, ga, p->num_sms, st);
+    if ((e = mark(1)) == cudaSuccess) e = launch_gemm(kGateUp, small, gu, ga, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
     GemmArgs gd = ga;
     gd.units = at<int4>(workspace, L.units_dn);
     gd.n_units = at<int32_t>(workspace, L.misc) + 2;
-    e = launch_gemm(1, nt, dn, gd, p->num_sms, st);
+    if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, small, dn, gd, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
     FinalArgs fa{at<float>(workspace, L.y32), static_cast<__nv_bfloat16*>(y), y_f32,
                  (size_t)R * d.H};
-    e = launch_finalize(fa, p->num_sms, st);
+    if ((e = mark(3)) == cudaSuccess) e = launch_finalize(fa, p->num_sms, st);
+    if (e == cudaSuccess) e = mark(4);
     if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+    return ok();
+}
+
+moe_status moe_plan_set_forward_events(moe_plan* p, moe_event_t const* events,
+                                       int32_t n_events) {
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+    if (n_events == 0) {
+        p->n_fwd_events = 0;
+        return ok();
+    }
+    if (n_events != 5 || !events) return fail(MOE_ERR_INVALID_ARG, "need exactly 5 events");
+    for (int i = 0; i < 5; ++i) {
+        if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "event %d is NULL", i);
+        p->fwd_events[i] = reinterpret_cast<cudaEvent_t>(events[i]);
+    }
+    p->n_fwd_events = 5;
     return ok();
 }
 

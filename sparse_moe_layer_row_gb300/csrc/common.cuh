@@ -30,17 +30,20 @@ struct Layout {
     size_t pair_row;     // int32 [max_pairs]
     size_t pair_w;       // fp32 [max_pairs]
     size_t xp;           // bf16 [max_pairs, H]       rows of x in pair order
-    size_t h;            // bf16 [max_pairs, I]       routed SwiGLU activations
-    size_t hs;           // bf16 [max_rows, Is]       shared-expert activations
+    size_t h;            // bf16 [max_pairs, 2I]      routed SwiGLU activations, hi | lo
+    size_t hs;           // bf16 [max_rows, 2Is]      shared-expert activations, hi | lo
     size_t y32;          // fp32 [max_rows, H]        combine accumulator
     size_t total;
     int64_t max_pairs, max_units_gu, max_units_dn;
 };
 
-// Rows of x per unit of grouped-GEMM work (the MMA N extent) for the two
-// kernel shapes; a call picks one from its row count.
+// Rows of x per unit of grouped-GEMM work (the MMA N extent).  A call with
+// few rows uses kSmallN for both GEMMs; otherwise the gate/up GEMM takes
+// kLargeN rows per unit and the down GEMM, whose B operand is twice as wide
+// (hi and lo parts of h), kLargeNDown.
 constexpr int kSmallN = 32;
 constexpr int kLargeN = 256;
+constexpr int kLargeNDown = 128;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -68,8 +71,8 @@ inline Layout make_layout(const moe_dims& d) {
     L.pair_row = take(sizeof(int32_t) * (size_t)P);
     L.pair_w = take(sizeof(float) * (size_t)P);
     L.xp = take(2 * (size_t)(P * H));
-    L.h = take(2 * (size_t)(P * d.I));
-    L.hs = take(2 * (size_t)(R * d.Is));
+    L.h = take(2 * (size_t)(P * 2 * d.I));
+    L.hs = take(2 * (size_t)(R * 2 * d.Is));
     L.y32 = take(sizeof(float) * (size_t)(R * H));
     L.total = o;
     return L;

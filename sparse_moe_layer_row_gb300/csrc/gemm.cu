@@ -15,10 +15,15 @@
 //  gate/up:  A rows 32q..32q+15 = gate rows, 32q+16..32q+31 = up rows of the
 //            same 16 intermediate indices (q = 0..3), so every TMEM lane
 //            quadrant holds matching gate and up rows and the epilogue pairs
-//            them with one warp shuffle: h = silu(g) * u, stored as bf16.
-//  down:     A = 128 rows of W_down[e] (hidden outputs), B = rows of h; the
-//            epilogue scales by the pair's renormalised weight and adds into
-//            the fp32 accumulator y32[row, :] (the shared expert with weight 1).
+//            them with one warp shuffle: h = silu(g) * u, stored as two bf16
+//            parts hi = bf16(h), lo = bf16(h - hi) (about 16 significant bits;
+//            one bf16 alone puts the rounding of h at the edge of the output
+//            tolerance).
+//  down:     A = 128 rows of W_down[e] (hidden outputs), B = the hi and the lo
+//            rows of h: two MMAs per K step into one accumulator, so W_down
+//            is read once; the epilogue scales by the pair's renormalised
+//            weight and adds into the fp32 accumulator y32[row, :] (the
+//            shared expert with weight 1).
 //
 // Pipeline (one CTA per SM, persistent over the unit list):
 //   warp 0 lane 0  TMA producer: STAGES-deep ring of (A tile, B tile) stages
@@ -37,10 +42,11 @@ namespace moe {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legal wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s when draining after an abort
 
-template <int NMAX, int STAGES>
+template <int MODE, int NMAX, int STAGES>
 struct GemmCfg {
+    static constexpr int kBParts = MODE == kDown ? 2 : 1;  // down: hi and lo parts of h
     static constexpr int kABytes = 128 * 128;
-    static constexpr int kBBytes = NMAX * 128;
+    static constexpr int kBBytes = kBParts * NMAX * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kBarOff = STAGES * kStageBytes;
     static constexpr int kSmem = kBarOff + 256 + 1024;
@@ -57,7 +63,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
        GemmArgs a) {
-    using C = GemmCfg<NMAX, STAGES>;
+    using C = GemmCfg<MODE, NMAX, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     const int nunits = __ldg(a.n_units);
     if ((int)blockIdx.x >= nunits) return;  // uniform: no unit for this CTA
@@ -104,7 +110,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const int g = un.x, m = un.y, start = un.z, n = un.w;
                 const int nb16 = (n + 15) >> 4;
                 const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
-                const uint32_t bytes = (uint32_t)(C::kABytes + nb16 * 2048);
+                const uint32_t bytes = (uint32_t)(C::kABytes + C::kBParts * nb16 * 2048);
                 const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
                 for (int kb = 0; kb < (K >> 6); ++kb) {
                     if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -134,6 +140,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                     for (int t = 0; t < nb16; ++t)
                         tma_load_2d(sB + t * 2048, mB, kc, start + t * 16, full + stage);
+                    if (MODE == kDown)  // lo part of h: columns K .. 2K-1 of the same rows
+                        for (int t = 0; t < nb16; ++t)
+                            tma_load_2d(sB + NMAX * 128 + t * 2048, mB, K + kc, start + t * 16,
+                                        full + stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -177,9 +187,12 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     const uint32_t sA = sbase + stage * C::kStageBytes;
                     const uint32_t sB = sA + C::kABytes;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_bf16(d, smem_desc_sw128(sA + kk * 32), smem_desc_sw128(sB + kk * 32),
-                                    idesc, (kb | kk) != 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(sA + kk * 32);
+                        tc_mma_bf16(d, ad, smem_desc_sw128(sB + kk * 32), idesc, (kb | kk) != 0);
+                        if (MODE == kDown)
+                            tc_mma_bf16(d, ad, smem_desc_sw128(sB + NMAX * 128 + kk * 32), idesc, 1u);
+                    }
                     tc_commit(empty + stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -218,8 +231,14 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         const int col = c + (is_gate ? t : 8 + t);
                         const float gv = is_gate ? v[t] : recv;
                         const float uv = is_gate ? recv : v[8 + t];
-                        if (col < n)
-                            out[(size_t)(start + col) * ld + il] = __float2bfloat16_rn(silu(gv) * uv);
+                        if (col < n) {
+                            const float hv = silu(gv) * uv;
+                            const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+                            const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
+                            __nv_bfloat16* o = out + (size_t)(start + col) * (2 * ld);
+                            o[il] = hi;
+                            o[ld + il] = lo;
+                        }
                     }
                 } else {
                     const int hrow = m * 128 + q * 32 + lane;
@@ -254,7 +273,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 
 template <int MODE, int NMAX, int STAGES>
 static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int grid, cudaStream_t st) {
-    using C = GemmCfg<NMAX, STAGES>;
+    using C = GemmCfg<MODE, NMAX, STAGES>;
     k_gemm<MODE, NMAX, STAGES><<<grid, 192, C::kSmem, st>>>(mp.a0, mp.a1, mp.a2, mp.a3, mp.b0,
                                                              mp.b1, a);
     return cudaGetLastError();
@@ -262,29 +281,31 @@ static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int grid, c
 
 template <int MODE, int NMAX, int STAGES>
 static cudaError_t set_attr() {
-    using C = GemmCfg<NMAX, STAGES>;
+    using C = GemmCfg<MODE, NMAX, STAGES>;
     return cudaFuncSetAttribute(k_gemm<MODE, NMAX, STAGES>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
 }
 
-constexpr int kSmallStages = 10;
-constexpr int kLargeStages = 4;
+// (rows per unit, pipeline depth) of each kernel shape: small = few rows per
+// expert (weight streaming, deep ring); large = many rows (tensor-core bound).
+constexpr int kSmallStagesGU = 10, kSmallStagesDN = 8;
+constexpr int kLargeStagesGU = 4, kLargeStagesDN = 4;
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
-    if ((e = set_attr<kGateUp, kSmallN, kSmallStages>()) != cudaSuccess) return e;
-    if ((e = set_attr<kDown, kSmallN, kSmallStages>()) != cudaSuccess) return e;
-    if ((e = set_attr<kGateUp, kLargeN, kLargeStages>()) != cudaSuccess) return e;
-    return set_attr<kDown, kLargeN, kLargeStages>();
+    if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU>()) != cudaSuccess) return e;
+    if ((e = set_attr<kDown, kSmallN, kSmallStagesDN>()) != cudaSuccess) return e;
+    if ((e = set_attr<kGateUp, kLargeN, kLargeStagesGU>()) != cudaSuccess) return e;
+    return set_attr<kDown, kLargeNDown, kLargeStagesDN>();
 }
 
-cudaError_t launch_gemm(int mode, int nt, const GemmMaps& mp, const GemmArgs& a, int grid,
+cudaError_t launch_gemm(int mode, bool small, const GemmMaps& mp, const GemmArgs& a, int grid,
                         cudaStream_t st) {
-    if (nt == kSmallN)
-        return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStages>(mp, a, grid, st)
-                               : launch_one<kDown, kSmallN, kSmallStages>(mp, a, grid, st);
-    return mode == kGateUp ? launch_one<kGateUp, kLargeN, kLargeStages>(mp, a, grid, st)
-                           : launch_one<kDown, kLargeN, kLargeStages>(mp, a, grid, st);
+    if (small)
+        return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStagesGU>(mp, a, grid, st)
+                               : launch_one<kDown, kSmallN, kSmallStagesDN>(mp, a, grid, st);
+    return mode == kGateUp ? launch_one<kGateUp, kLargeN, kLargeStagesGU>(mp, a, grid, st)
+                           : launch_one<kDown, kLargeNDown, kLargeStagesDN>(mp, a, grid, st);
 }
 
 }  // namespace moe

@@ -36,7 +36,8 @@ struct ScatterArgs {
     const float* w_renorm;
     const uint32_t* keep;
     const __nv_bfloat16* x;
-    int R, H, E, k, I, Is, nb, nt;
+    int R, H, E, k, I, Is, nb;
+    int nt_gu, nt_dn;   // rows per unit of the gate/up and of the down GEMM
     int32_t* row_block;
     int32_t* count;
     int32_t* expert_off;
@@ -59,8 +60,8 @@ struct GemmArgs {
     const int4* units;
     const int32_t* n_units;
     int E, H, I, Is;
-    __nv_bfloat16* h;
-    __nv_bfloat16* hs;
+    __nv_bfloat16* h;     // [pairs, 2I]: bf16 hi part | bf16 lo part
+    __nv_bfloat16* hs;    // [rows, 2Is]
     const int32_t* pair_row;
     const float* pair_w;
     float* y32;
@@ -74,7 +75,8 @@ cudaError_t launch_coreset(const CoresetArgs&, cudaStream_t);
 cudaError_t launch_scatter(const ScatterArgs&, int num_sms, cudaStream_t);
 cudaError_t launch_finalize(const FinalArgs&, int num_sms, cudaStream_t);
 cudaError_t gemm_set_attributes();
-cudaError_t launch_gemm(int mode, int nt, const GemmMaps&, const GemmArgs&, int grid, cudaStream_t);
+cudaError_t launch_gemm(int mode, bool small, const GemmMaps&, const GemmArgs&, int grid,
+                        cudaStream_t);
 
 enum { kGateUp = 0, kDown = 1 };
 

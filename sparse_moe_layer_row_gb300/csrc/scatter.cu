@@ -97,34 +97,37 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_count(ScatterArgs a) {
     const int mt_gu = a.I / 64, mt_gs = a.Is / 64, mt_dn = a.H / 128;
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
-    int sum = 0, chunks = 0;
+    int sum = 0, ch_gu = 0, ch_dn = 0;
     for (int f = e0; f < e1; ++f) {
         const int n = __ldcg(a.count + f);
         sum += n;
-        chunks += (n + a.nt - 1) / a.nt;
+        ch_gu += (n + a.nt_gu - 1) / a.nt_gu;
+        ch_dn += (n + a.nt_dn - 1) / a.nt_dn;
     }
-    int tot_pairs, tot_chunks;
+    int tot_pairs, tot_gu, tot_dn;
     int p = block_excl_scan_i32(sum, warp_sums, &tot_pairs);
-    int ch = block_excl_scan_i32(chunks, warp_sums, &tot_chunks);
-    const int s_chunks = (a.R + a.nt - 1) / a.nt;
+    int cg = block_excl_scan_i32(ch_gu, warp_sums, &tot_gu);
+    int cd = block_excl_scan_i32(ch_dn, warp_sums, &tot_dn);
     // shared expert (group E) first: it has the most rows
-    const int base_gu = s_chunks * mt_gs, base_dn = s_chunks * mt_dn;
+    const int base_gu = (a.R + a.nt_gu - 1) / a.nt_gu * mt_gs;
+    const int base_dn = (a.R + a.nt_dn - 1) / a.nt_dn * mt_dn;
     if (threadIdx.x == 0) {
-        write_units(a.units_gu, 0, E, 0, a.R, a.nt, mt_gs);
-        write_units(a.units_dn, 0, E, 0, a.R, a.nt, mt_dn);
+        write_units(a.units_gu, 0, E, 0, a.R, a.nt_gu, mt_gs);
+        write_units(a.units_dn, 0, E, 0, a.R, a.nt_dn, mt_dn);
     }
     for (int f = e0; f < e1; ++f) {
         const int n = __ldcg(a.count + f);
         a.expert_off[f] = p;
-        write_units(a.units_gu, base_gu + ch * mt_gu, f, p, n, a.nt, mt_gu);
-        write_units(a.units_dn, base_dn + ch * mt_dn, f, p, n, a.nt, mt_dn);
+        write_units(a.units_gu, base_gu + cg * mt_gu, f, p, n, a.nt_gu, mt_gu);
+        write_units(a.units_dn, base_dn + cd * mt_dn, f, p, n, a.nt_dn, mt_dn);
         p += n;
-        ch += (n + a.nt - 1) / a.nt;
+        cg += (n + a.nt_gu - 1) / a.nt_gu;
+        cd += (n + a.nt_dn - 1) / a.nt_dn;
     }
     if (threadIdx.x == 0) {
         a.expert_off[E] = tot_pairs;
-        a.misc[1] = base_gu + tot_chunks * mt_gu;
-        a.misc[2] = base_dn + tot_chunks * mt_dn;
+        a.misc[1] = base_gu + tot_gu * mt_gu;
+        a.misc[2] = base_dn + tot_dn * mt_dn;
         a.misc[3] = tot_pairs;
         a.misc[0] = 0;
     }

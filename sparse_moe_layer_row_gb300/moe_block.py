@@ -67,6 +67,8 @@ def load(build_if_missing: bool = False):
     L.moe_block_coreset.argtypes = [P, i32, P, i32, P, P, ctypes.c_float, P, P, P, P, P, sz, P]
     L.moe_block_forward.restype = ctypes.c_int
     L.moe_block_forward.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, sz, P]
+    L.moe_plan_set_forward_events.restype = ctypes.c_int
+    L.moe_plan_set_forward_events.argtypes = [P, P, i32]
     L.moe_read_device_status.restype = ctypes.c_int
     L.moe_read_device_status.argtypes = [P, P, P]
     L.moe_clear_device_status.restype = ctypes.c_int
@@ -143,11 +145,29 @@ class Plan:
         except Exception:
             pass
 
+    def set_forward_events(self, events):
+        """Record 5 torch.cuda.Event(enable_timing=True) around the forward's kernels
+        (before scatter, gate/up GEMM, down GEMM, final store; after the store).
+        None turns the recording off."""
+        if not events:
+            _check(load().moe_plan_set_forward_events(self.handle, None, 0))
+            self._events = None
+            return
+        if len(events) != 5:
+            raise ValueError("need 5 events")
+        for ev in events:
+            if ev.cuda_event == 0:
+                ev.record()  # torch creates the CUDA event lazily
+        arr = (ctypes.c_void_p * 5)(*[ev.cuda_event for ev in events])
+        _check(load().moe_plan_set_forward_events(self.handle, arr, 5))
+        self._events = events
+
     def workspace_bytes(self) -> int:
         return moe_workspace_bytes(self.dims)
 
     def new_workspace(self) -> torch.Tensor:
-        return torch.empty(self.workspace_bytes(), dtype=torch.uint8, device=self.device)
+        """A zeroed workspace (zero status counters)."""
+        return torch.zeros(self.workspace_bytes(), dtype=torch.uint8, device=self.device)
 
 
 def moe_block_route(plan: Plan, x, block_offsets, logit_bias, topk_idx, topk_w, workspace,
