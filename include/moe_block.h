@@ -152,6 +152,30 @@ moe_status moe_block_forward(const moe_plan* plan, const void* x, int32_t R,
                              const float* w_renorm, const uint32_t* keep, void* y, float* y_f32,
                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* Router for callers that cannot allocate device memory (no counterpart on the
+ * pages: an addition for deployment).  Some callers cannot hand the library a
+ * workspace, e.g. an engine that reserves all of its device memory up front,
+ * or a plugin allowed to touch only the buffers it is given.  This call does
+ * what moe_block_route does, with the same kernel and bit-identical outputs,
+ * but keeps the router's scratch (logits and tickets) in a 1 MiB array
+ * compiled into the library, which every GPU that loads the library holds
+ * until the library is unloaded.  The caller still passes x, block_offsets,
+ * logit_bias, topk_idx and topk_w as for moe_block_route.
+ *   - Allocates nothing and calls no allocating routine.
+ *   - Rejects with MOE_ERR_UNSUPPORTED any call whose scratch
+ *     (4*R*E + 4*ceil(R/4) rounded up to 256, + 256 bytes) exceeds 1 MiB:
+ *     at E = 256, R <= 1022.
+ *   - All calls share the array.  The tickets are cleared on `stream` at the
+ *     start of each call; calls that overlap on the GPU (other streams, other
+ *     host threads) race on the array and must not be issued.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make it before any stream capture.
+ *   - Non-finite logits are counted in the array, not reported. */
+moe_status moe_block_route_noalloc(const moe_plan* plan, const void* x, int32_t R,
+                                   const int32_t* block_offsets, int32_t nb,
+                                   const float* logit_bias, int32_t* topk_idx, float* topk_w,
+                                   moe_stream_t stream);
+
 /* Same type as cudaEvent_t. */
 typedef struct CUevent_st* moe_event_t;
 

@@ -123,6 +123,20 @@ moe_status cuda_fail(cudaError_t e, const char* what) {
 
 }  // namespace
 
+bool moe::plan_view(const moe_plan* p, PlanView* out) {
+    if (!p || !out) return false;
+    out->d = p->d;
+    out->device = p->device;
+    out->num_sms = p->num_sms;
+    out->w_router = p->wr;
+    return true;
+}
+
+moe_status moe::set_error(moe_status s, const char* msg) {
+    g_last_error = msg ? msg : "";
+    return s;
+}
+
 extern "C" {
 
 int32_t moe_version(void) { return 100; }

@@ -80,4 +80,15 @@ cudaError_t launch_gemm(int mode, bool small, const GemmMaps&, const GemmArgs&, 
 
 enum { kGateUp = 0, kDown = 1 };
 
+// Read-only view of a plan for entry points outside api.cu, and the setter of
+// the thread's last-error message (both implemented in api.cu).
+struct PlanView {
+    moe_dims d;
+    int device;
+    int num_sms;
+    const void* w_router;
+};
+bool plan_view(const moe_plan* plan, PlanView* out);
+moe_status set_error(moe_status s, const char* msg);
+
 }  // namespace moe

@@ -67,6 +67,8 @@ def load(build_if_missing: bool = False):
     L.moe_block_coreset.argtypes = [P, i32, P, i32, P, P, ctypes.c_float, P, P, P, P, P, sz, P]
     L.moe_block_forward.restype = ctypes.c_int
     L.moe_block_forward.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, sz, P]
+    L.moe_block_route_noalloc.restype = ctypes.c_int
+    L.moe_block_route_noalloc.argtypes = [P, P, i32, P, i32, P, P, P, P]
     L.moe_plan_set_forward_events.restype = ctypes.c_int
     L.moe_plan_set_forward_events.argtypes = [P, P, i32]
     L.moe_read_device_status.restype = ctypes.c_int
@@ -185,6 +187,25 @@ def moe_block_route(plan: Plan, x, block_offsets, logit_bias, topk_idx, topk_w, 
     _check(load().moe_block_route(plan.handle, _ptr(x), R, _ptr(block_offsets), nb,
                                   _ptr(logit_bias), _ptr(topk_idx), _ptr(topk_w),
                                   _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def moe_block_route_noalloc(plan: Plan, x, block_offsets, logit_bias, topk_idx, topk_w,
+                            stream=None):
+    """moe_block_route without a workspace, for callers that cannot allocate device
+    memory: the scratch is a 1 MiB array inside the library (see the header for
+    the size limit, and for why overlapping calls must not be issued)."""
+    d = plan.dims
+    R = x.shape[0]
+    nb = block_offsets.shape[0] - 1
+    _need(x, "x", torch.bfloat16, (R, d.H))
+    _need(block_offsets, "block_offsets", torch.int32)
+    if logit_bias is not None:
+        _need(logit_bias, "logit_bias", torch.float32, (nb, d.E))
+    _need(topk_idx, "topk_idx", torch.int32, (R, d.k))
+    _need(topk_w, "topk_w", torch.float32, (R, d.k))
+    _check(load().moe_block_route_noalloc(plan.handle, _ptr(x), R, _ptr(block_offsets), nb,
+                                          _ptr(logit_bias), _ptr(topk_idx), _ptr(topk_w),
+                                          _stream(stream)))
 
 
 def moe_block_coreset(plan: Plan, block_offsets, topk_idx, topk_w, tau: float, keep, core_size,
