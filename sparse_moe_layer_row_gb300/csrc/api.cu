@@ -174,11 +174,11 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
     p->sg = ws_gate; p->su = ws_up; p->sd = ws_down;
     const moe_dims& d = *dims;
     const auto L2W = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
-    bool good = encode_bf16(&p->tm_wg, w_gate, d.H, d.I, d.E, 16, L2W) &&
-                encode_bf16(&p->tm_wu, w_up, d.H, d.I, d.E, 16, L2W) &&
+    bool good = encode_bf16(&p->tm_wg, w_gate, d.H, d.I, d.E, 64, L2W) &&
+                encode_bf16(&p->tm_wu, w_up, d.H, d.I, d.E, 64, L2W) &&
                 encode_bf16(&p->tm_wd, w_down, d.I, d.H, d.E, 128, L2W) &&
-                encode_bf16(&p->tm_sg, ws_gate, d.H, d.Is, 0, 16, L2W) &&
-                encode_bf16(&p->tm_su, ws_up, d.H, d.Is, 0, 16, L2W) &&
+                encode_bf16(&p->tm_sg, ws_gate, d.H, d.Is, 0, 64, L2W) &&
+                encode_bf16(&p->tm_su, ws_up, d.H, d.Is, 0, 64, L2W) &&
                 encode_bf16(&p->tm_sd, ws_down, d.Is, d.H, 0, 128, L2W);
     if (!good) {
         delete p;

@@ -12,12 +12,13 @@
 // stream through shared memory once per launch, whatever the number of rows
 // routed to it, and N only has to be a multiple of 16.
 //
-//  gate/up:  A rows 32q..32q+15 = gate rows, 32q+16..32q+31 = up rows of the
-//            same 16 intermediate indices (q = 0..3), so every TMEM lane
-//            quadrant holds matching gate and up rows and the epilogue pairs
-//            them with one warp shuffle: h = silu(g) * u, stored as two bf16
-//            parts hi = bf16(h), lo = bf16(h - hi) (about 16 significant bits;
-//            one bf16 alone puts the rounding of h at the edge of the output
+//  gate/up:  A rows 0..63 = gate rows, 64..127 = up rows of the same 64
+//            intermediate indices (two 64-row TMA boxes per stage).  TMEM lane
+//            quadrants 0-1 hold g, 2-3 hold u; the epilogue warps trade half
+//            of each 16-column chunk through shared memory and each computes
+//            h = silu(g) * u for its half, stored as two bf16 parts
+//            hi = bf16(h), lo = bf16(h - hi) (about 16 significant bits; one
+//            bf16 alone puts the rounding of h at the edge of the output
 //            tolerance).
 //  down:     A = 128 rows of W_down[e] (hidden outputs), B = the hi and the lo
 //            rows of h: two MMAs per K step into one accumulator, so W_down
@@ -48,7 +49,9 @@ struct GemmCfg {
     static constexpr int kABytes = 128 * 128;
     static constexpr int kBBytes = kBParts * NMAX * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kBarOff = STAGES * kStageBytes;
+    static constexpr int kXchgOff = STAGES * kStageBytes;        // gate/up g <-> u exchange
+    static constexpr int kXchgBytes = MODE == kGateUp ? 2 * 64 * 9 * 4 : 0;
+    static constexpr int kBarOff = kXchgOff + kXchgBytes;
     static constexpr int kSmem = kBarOff + 256 + 1024;
     static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
@@ -75,14 +78,19 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* xbar = tempty + 2;  // [2] gate/up epilogue exchange (128 arrivals each)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull + i, 1);
+            mbar_init(tempty + i, 128);
+            mbar_init(xbar + i, 128);
+        }
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -123,16 +131,13 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     const uint32_t sB = sA + C::kABytes;
                     const int kc = kb * 64;
                     if (MODE == kGateUp) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int rows = m * 64 + q * 16;
-                            if (g == a.E) {
-                                tma_load_2d(sA + (q * 32) * 128, &tmA2, kc, rows, full + stage);
-                                tma_load_2d(sA + (q * 32 + 16) * 128, &tmA3, kc, rows, full + stage);
-                            } else {
-                                tma_load_3d(sA + (q * 32) * 128, &tmA0, kc, rows, g, full + stage);
-                                tma_load_3d(sA + (q * 32 + 16) * 128, &tmA1, kc, rows, g, full + stage);
-                            }
+                        const int rows = m * 64;
+                        if (g == a.E) {
+                            tma_load_2d(sA, &tmA2, kc, rows, full + stage);
+                            tma_load_2d(sA + 64 * 128, &tmA3, kc, rows, full + stage);
+                        } else {
+                            tma_load_3d(sA, &tmA0, kc, rows, g, full + stage);
+                            tma_load_3d(sA + 64 * 128, &tmA1, kc, rows, g, full + stage);
                         }
                     } else {
                         if (g == a.E) tma_load_2d(sA, &tmA2, kc, m * 128, full + stage);
@@ -206,8 +211,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+        uint32_t acc_phase = 0, xphase = 0;
+        bool alive = true;
+        for (int u = blockIdx.x; alive && u < nunits; u += gridDim.x) {
             const int4 un = __ldg(a.units + u);
             const int g = un.x, m = un.y, start = un.z, n = un.w;
             const int n16 = (n + 15) & ~15;
@@ -216,21 +222,37 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             __syncwarp();
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NMAX);
-            for (int c = 0; c < n16; c += 16) {
+            for (int c = 0; alive && c < n16; c += 16) {
                 float v[16];
+                __syncwarp();  // tcgen05.ld is warp-collective
                 tmem_ld16(tb + (uint32_t)c, v);
                 if (MODE == kGateUp) {
-                    const bool is_gate = lane < 16;
-                    const int il = m * 64 + q * 16 + (lane & 15);
-                    __nv_bfloat16* out = g == a.E ? a.hs : a.h;
-                    const int ld = g == a.E ? a.Is : a.I;
+                    // quadrants 0-1: gate rows, 2-3: up rows of intermediate index r
+                    const bool is_gate = q < 2;
+                    const int r = (q & 1) * 32 + lane;
+                    float* xg = reinterpret_cast<float*>(base + C::kXchgOff);  // [64][9]: g, cols 8..15
+                    float* xu = xg + 64 * 9;                                    // [64][9]: u, cols 0..7
 #pragma unroll
                     for (int t = 0; t < 8; ++t) {
-                        const float send = is_gate ? v[8 + t] : v[t];
-                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        if (is_gate) xg[r * 9 + t] = v[8 + t];
+                        else xu[r * 9 + t] = v[t];
+                    }
+                    // the four epilogue warps meet through an mbarrier (bounded wait)
+                    mbar_arrive(xbar);
+                    if (__any_sync(0xffffffffu,
+                                   !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitLimitNs))) {
+                        give_up();
+                        alive = false;
+                        break;
+                    }
+                    __nv_bfloat16* out = g == a.E ? a.hs : a.h;
+                    const int ld = g == a.E ? a.Is : a.I;
+                    const int il = m * 64 + r;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
                         const int col = c + (is_gate ? t : 8 + t);
-                        const float gv = is_gate ? v[t] : recv;
-                        const float uv = is_gate ? recv : v[8 + t];
+                        const float gv = is_gate ? v[t] : xg[r * 9 + t];
+                        const float uv = is_gate ? xu[r * 9 + t] : v[8 + t];
                         if (col < n) {
                             const float hv = silu(gv) * uv;
                             const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
@@ -240,6 +262,14 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             o[ld + il] = lo;
                         }
                     }
+                    mbar_arrive(xbar + 1);  // the buffer is reused by the next chunk
+                    if (__any_sync(0xffffffffu,
+                                   !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitLimitNs))) {
+                        give_up();
+                        alive = false;
+                        break;
+                    }
+                    xphase ^= 1u;
                 } else {
                     const int hrow = m * 128 + q * 32 + lane;
 #pragma unroll
@@ -255,6 +285,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                 }
             }
+            if (!alive) break;
             tc_fence_before();
             mbar_arrive(tempty + acc);
             acc ^= 1;
