@@ -61,7 +61,7 @@ struct GemmCfg {
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 template <int MODE, int NMAX, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
 k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
@@ -318,9 +318,11 @@ static cudaError_t set_attr() {
 }
 
 // (rows per unit, pipeline depth) of each kernel shape: small = few rows per
-// expert (weight streaming, deep ring); large = many rows (tensor-core bound).
-constexpr int kSmallStagesGU = 10, kSmallStagesDN = 8;
+// expert (weight streaming: two CTAs per SM, each with its own ring, keep more
+// TMA streams in flight); large = many rows (tensor-core bound, one CTA per SM).
+constexpr int kSmallStagesGU = 5, kSmallStagesDN = 4;
 constexpr int kLargeStagesGU = 4, kLargeStagesDN = 4;
+constexpr int kSmallCtasPerSm = 2;
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
@@ -332,9 +334,11 @@ cudaError_t gemm_set_attributes() {
 
 cudaError_t launch_gemm(int mode, bool small, const GemmMaps& mp, const GemmArgs& a, int grid,
                         cudaStream_t st) {
-    if (small)
+    if (small) {
+        grid *= kSmallCtasPerSm;
         return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStagesGU>(mp, a, grid, st)
                                : launch_one<kDown, kSmallN, kSmallStagesDN>(mp, a, grid, st);
+    }
     return mode == kGateUp ? launch_one<kGateUp, kLargeN, kLargeStagesGU>(mp, a, grid, st)
                            : launch_one<kDown, kLargeNDown, kLargeStagesDN>(mp, a, grid, st);
 }
