@@ -61,7 +61,7 @@ typedef enum moe_status {
  *   k   experts per row; 1..32 and <= E
  *   I   routed-expert intermediate size; multiple of 64
  *   Is  shared-expert intermediate size; multiple of 64
- *   max_rows    largest R of any call (>= 1)
+ *   max_rows    largest R of any call (1 .. 2^21)
  *   max_blocks  largest nb of any call (>= 1) */
 typedef struct moe_dims {
     int32_t H, E, k, I, Is;

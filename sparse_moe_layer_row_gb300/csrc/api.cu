@@ -18,6 +18,8 @@ struct moe_plan {
     int num_sms;
     const void *wr, *wg, *wu, *wd, *sg, *su, *sd;
     CUtensorMap tm_wg, tm_wu, tm_wd, tm_sg, tm_su, tm_sd;
+    CUtensorMap tm_wr;    // router weights for the tensor-core screening (E <= 256)
+    bool tc_route;        // the large-batch router applies to this shape
     cudaEvent_t fwd_events[5];
     int n_fwd_events;
 };
@@ -88,8 +90,9 @@ moe_status check_dims(const moe_dims* d) {
     if (d->max_rows < 1 || d->max_blocks < 1)
         return fail(MOE_ERR_INVALID_ARG, "max_rows=%d and max_blocks=%d must be >= 1", d->max_rows,
                     d->max_blocks);
-    if ((int64_t)d->max_rows * d->k > (1 << 30) || (int64_t)d->max_rows * d->H > (int64_t)1 << 34)
-        return fail(MOE_ERR_UNSUPPORTED, "max_rows=%d too large", d->max_rows);
+    if (d->max_rows > (1 << 21) || (int64_t)d->max_rows * d->k > (1 << 30) ||
+        (int64_t)d->max_rows * d->H > (int64_t)1 << 34)
+        return fail(MOE_ERR_UNSUPPORTED, "max_rows=%d too large (at most 2^21)", d->max_rows);
     return MOE_OK;
 }
 
@@ -166,6 +169,7 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e == cudaSuccess) e = gemm_set_attributes();
+    if (e == cudaSuccess) e = route_tc_set_attributes();
     if (e != cudaSuccess) {
         delete p;
         return cuda_fail(e, "device query");
@@ -180,6 +184,10 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
                 encode_bf16(&p->tm_sg, ws_gate, d.H, d.Is, 0, 64, L2W) &&
                 encode_bf16(&p->tm_su, ws_up, d.H, d.Is, 0, 64, L2W) &&
                 encode_bf16(&p->tm_sd, ws_down, d.Is, d.H, 0, 128, L2W);
+    p->tc_route = d.E <= 256 && d.E % 16 == 0 && d.k <= 16;
+    if (good && p->tc_route)
+        good = encode_bf16(&p->tm_wr, w_router, d.H, d.E, 0, (uint32_t)d.E,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (!good) {
         delete p;
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight tensor");
@@ -203,6 +211,20 @@ moe_status moe_block_route(const moe_plan* p, const void* x, int32_t R,
     if (R == 0) return ok();
     const Layout L = make_layout(p->d);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (p->tc_route && R >= kTcRouteMinRows) {
+        CUtensorMap tm_x;
+        if (!encode_bf16(&tm_x, x, p->d.H, (uint64_t)R, 0, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for x");
+        RouteTcArgs ta{static_cast<const __nv_bfloat16*>(x),
+                       static_cast<const __nv_bfloat16*>(p->wr), logit_bias, block_offsets, R,
+                       p->d.H, p->d.E, p->d.k, nb, at<float>(workspace, L.xnorm),
+                       at<float>(workspace, L.wnorm), at<int32_t>(workspace, L.cand),
+                       at<int32_t>(workspace, L.cand_cnt), topk_idx, topk_w,
+                       at<uint32_t>(workspace, L.status)};
+        cudaError_t e = launch_route_tc(ta, tm_x, p->tm_wr, p->num_sms, st);
+        if (e != cudaSuccess) return cuda_fail(e, "route launch");
+        return ok();
+    }
     cudaError_t e = cudaMemsetAsync(at<uint8_t>(workspace, L.route_cnt), 0,
                                     sizeof(uint32_t) * (size_t)((R + 3) / 4), st);
     if (e != cudaSuccess) return cuda_fail(e, "route counters");

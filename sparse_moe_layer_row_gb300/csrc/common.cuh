@@ -21,6 +21,10 @@ struct Layout {
     size_t status;       // uint32[MOE_STATUS_WORDS]
     size_t route_cnt;    // uint32[ceil(max_rows/4)]   router row-group tickets
     size_t logits;       // fp32 [max_rows, E]        router logits (before bias)
+    size_t xnorm;        // fp32 [max_rows]           |x_r|_2 (large-batch router)
+    size_t wnorm;        // fp32 [E]                  |w_e|_2
+    size_t cand;         // int32 [max_rows, 32]      router candidates per row
+    size_t cand_cnt;     // int32 [max_rows]
     size_t row_block;    // int32 [max_rows]
     size_t count;        // int32 [E]                 surviving pairs per expert
     size_t expert_off;   // int32 [E + 1]
@@ -62,6 +66,10 @@ inline Layout make_layout(const moe_dims& d) {
     L.status = take(sizeof(uint32_t) * 64);
     L.route_cnt = take(sizeof(uint32_t) * (size_t)((R + 3) / 4));
     L.logits = take(sizeof(float) * (size_t)(R * E));
+    L.xnorm = take(sizeof(float) * (size_t)R);
+    L.wnorm = take(sizeof(float) * (size_t)E);
+    L.cand = take(sizeof(int32_t) * (size_t)R * 32);
+    L.cand_cnt = take(sizeof(int32_t) * (size_t)R);
     L.row_block = take(sizeof(int32_t) * (size_t)R);
     L.count = take(sizeof(int32_t) * (size_t)E);
     L.expert_off = take(sizeof(int32_t) * (size_t)(E + 1));

@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
     __shared__ uint32_t touched[kMaxE / 32];
     __shared__ uint32_t incore[kMaxE / 32];
     __shared__ int32_t sorted[kMaxE];
+    __shared__ unsigned long long keys[kMaxE];
     __shared__ uint64_t warp_sums[32];
     __shared__ int s_bad, s_empty;
     const int b = blockIdx.x, tid = threadIdx.x;
@@ -117,16 +118,24 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
         for (int w = tid; w < words; w += blockDim.x) incore[w] = touched[w];
     } else {
         const uint64_t theta = mass_threshold(a.tau, T);
-        // rank of each touched expert under (Q desc, id asc)
+        // rank of each touched expert under (Q desc, id asc): one 64-bit key per
+        // expert, (Q << 10 | (1023 - e)) + 1 for touched experts, 0 otherwise
+        // (Q < 2^53 since a block holds fewer than 2^21 rows).
+        for (int e = tid; e < E; e += blockDim.x)
+            keys[e] = ((touched[e >> 5] >> (e & 31)) & 1u)
+                          ? ((unsigned long long)Q[e] << 10 | (unsigned long long)(1023 - e)) + 1ull
+                          : 0ull;
+        __syncthreads();
         for (int e = tid; e < E; e += blockDim.x) {
-            if (!((touched[e >> 5] >> (e & 31)) & 1u)) continue;
-            const uint64_t qe = Q[e];
+            const unsigned long long ke = keys[e];
+            if (!ke) continue;
             int rank = 0;
-            for (int f = 0; f < E; ++f) {
-                if (!((touched[f >> 5] >> (f & 31)) & 1u)) continue;
-                const uint64_t qf = Q[f];
-                rank += (qf > qe) || (qf == qe && f < e);
+            int f = 0;
+            for (; f + 8 <= E; f += 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) rank += keys[f + j] > ke;
             }
+            for (; f < E; ++f) rank += keys[f] > ke;
             sorted[rank] = e;
         }
         __syncthreads();

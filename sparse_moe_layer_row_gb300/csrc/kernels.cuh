@@ -18,6 +18,23 @@ struct RouteArgs {
     float* topk_w;
     uint32_t* status;
 };
+// Large-batch router (tensor-core screening + exact recompute of candidates).
+constexpr int kCandCap = 32;      // candidates kept per row before falling back
+constexpr int kTcRouteMinRows = 256;
+struct RouteTcArgs {
+    const __nv_bfloat16* x;
+    const __nv_bfloat16* wr;
+    const float* bias;
+    const int32_t* off;
+    int R, H, E, k, nb;
+    float* xnorm;         // [R]
+    float* wnorm;         // [E]
+    int32_t* cand;        // [R, kCandCap]
+    int32_t* cand_cnt;    // [R]; -1: recompute every expert of the row
+    int32_t* topk_idx;
+    float* topk_w;
+    uint32_t* status;
+};
 struct CoresetArgs {
     const int32_t* off;
     const int32_t* topk_idx;
@@ -71,6 +88,9 @@ struct GemmMaps {
     CUtensorMap a0, a1, a2, a3, b0, b1;
 };
 cudaError_t launch_route(const RouteArgs&, int num_sms, cudaStream_t);
+cudaError_t route_tc_set_attributes();
+cudaError_t launch_route_tc(const RouteTcArgs&, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                            int num_sms, cudaStream_t);
 cudaError_t launch_coreset(const CoresetArgs&, cudaStream_t);
 cudaError_t launch_scatter(const ScatterArgs&, int num_sms, cudaStream_t);
 cudaError_t launch_finalize(const FinalArgs&, int num_sms, cudaStream_t);

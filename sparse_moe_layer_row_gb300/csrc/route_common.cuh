@@ -1,0 +1,121 @@
+// Pieces of the routing arithmetic shared by the two router paths (router.cu:
+// fixed-order SIMT logits for small batches; router_tc.cu: tensor-core
+// screening + exact recompute of the candidates for large batches).  Both
+// paths produce bit-identical logits, top-k ids and weights.
+//
+// Model card "Clover-35B-A3B-Preview -- CMF", intro: each row is routed to the
+// top 8 of 256 experts.  The arithmetic (fixed so that ids are reproducible):
+//   * z[r,e] = sum_h x[r,h] W[e,h] in fp32.  Each bf16*bf16 product is exact in
+//     fp32, so an fma adding it equals the add of the rounded product.  h is
+//     cut into stripes of 256; lane p of a warp owns elements 8p..8p+7 of every
+//     stripe and accumulates them in ascending h; the 32 lane sums are combined
+//     in the xor-butterfly pattern (partner distance 16, 8, 4, 2, 1).
+//   * z += bias[b,e] (optional), then z += 0 (turns -0 into +0).
+//   * top-k by (z descending, id ascending), NaN below every number.
+//   * w_j = a_j / (a_0 + ... + a_{k-1}) with a_j = exp_c(z_j - z_0), summed in
+//     rank order; exp_c is a Cody-Waite range reduction (ln 2 split into a
+//     12-significant-bit head 2839/4096 and an fp32 tail) followed by the
+//     degree-7 Taylor polynomial of e^r in Horner form with fused multiply-adds
+//     and a final scaling by 2^n through the exponent field.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace moe {
+
+// e^t for t <= 0 (see above).
+__device__ __forceinline__ float exp_c(float t) {
+    const float kLog2e = 1.44269504088896341f;
+    const float kLn2Hi = 0.693115234375f;                                   // 2839 / 4096
+    const float kLn2Lo = (float)(0.69314718055994530942 - 0.693115234375);  // ln 2 - head
+    if (t != t) return 0.0f;
+    if (t < -87.0f) return 0.0f;
+    const float n = rintf(__fmul_rn(t, kLog2e));
+    float r = __fmaf_rn(-n, kLn2Hi, t);
+    r = __fmaf_rn(-n, kLn2Lo, r);
+    float p = (float)(1.0 / 5040.0);
+    p = __fmaf_rn(p, r, (float)(1.0 / 720.0));
+    p = __fmaf_rn(p, r, (float)(1.0 / 120.0));
+    p = __fmaf_rn(p, r, (float)(1.0 / 24.0));
+    p = __fmaf_rn(p, r, (float)(1.0 / 6.0));
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    const int ni = (int)n;
+    return __fmul_rn(p, __uint_as_float((uint32_t)(ni + 127) << 23));
+}
+
+// Order-preserving key: larger float -> larger key; NaN -> 0.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    if (f != f) return 0u;
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+__device__ __forceinline__ void bf16x8(uint4 v, float* f) {
+    f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+    f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+// z -> z + bias, + 0, as the contract states.
+__device__ __forceinline__ float finish_logit(float dot, const float* bias_row, int e) {
+    float z = dot;
+    if (bias_row) z = __fadd_rn(z, __ldg(bias_row + e));
+    return __fadd_rn(z, 0.0f);
+}
+
+// Warp top-k over entries spread across lanes: lane entry i holds (key[i],
+// id[i]) when bit i of `valid` is set.  Order: key descending, id ascending.
+// Lane j < k receives the j-th entry in my_id / my_key.  k must not exceed
+// the number of valid entries in the warp.
+template <int NI>
+__device__ __forceinline__ void warp_topk(const uint32_t (&key)[NI], const uint32_t (&id)[NI],
+                                          uint32_t valid, int k, int lane, uint32_t& my_id,
+                                          uint32_t& my_key) {
+    uint32_t taken = ~valid;
+    my_id = 0;
+    my_key = 0;
+    for (int j = 0; j < k; ++j) {
+        uint32_t bk = 0, bid = 0xFFFFFFFFu;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            if ((taken >> i) & 1u) continue;
+            if (bi < 0 || key[i] > bk || (key[i] == bk && id[i] < bid)) {
+                bk = key[i];
+                bid = id[i];
+                bi = i;
+            }
+        }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
+        const uint32_t cand = (bi >= 0 && bk == mk) ? bid : 0xFFFFFFFFu;
+        const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+        if (bi >= 0 && bid == win) taken |= 1u << bi;
+        if (lane == j) {
+            my_id = win;
+            my_key = mk;
+        }
+    }
+}
+
+// Softmax over the k selected logits (lane j < k holds rank j) and the store.
+__device__ __forceinline__ void write_topk(int32_t* idx_out, float* w_out, int k, int lane,
+                                           uint32_t my_id, uint32_t my_key) {
+    const float zj = key_value(my_key);
+    const float m = __shfl_sync(0xffffffffu, zj, 0);
+    const float aj = lane < k ? exp_c(__fsub_rn(zj, m)) : 0.0f;
+    float S = 0.0f;
+    for (int j = 0; j < k; ++j) S = __fadd_rn(S, __shfl_sync(0xffffffffu, aj, j));
+    if (lane < k) {
+        idx_out[lane] = (int32_t)my_id;
+        w_out[lane] = __fdiv_rn(aj, S);
+    }
+}
+
+}  // namespace moe

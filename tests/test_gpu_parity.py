@@ -193,3 +193,46 @@ def test_workspace_reuse_across_shapes():
     x5 = T.x[:5].contiguous()
     c2 = Case(w, T=T, block_offsets=[0, 5], x=x5)
     _full(c2)
+
+
+# --------------------------------------------------------------------------- large-batch router
+
+def _route_only(case: Case):
+    L = case.layer
+    idx, wt = L.route(case.x, case.off, case.bias)
+    torch.cuda.synchronize()
+    g = dict(idx=idx.cpu().numpy().copy(), w=wt.cpu().numpy().copy())
+    ref = case.oracle_route()
+    assert_route_equal(g, ref)
+    return g, ref
+
+
+@pytest.mark.parametrize("R,E,k,H", [(256, 256, 8, 256), (300, 48, 6, 512), (1000, 256, 16, 256),
+                                     (513, 64, 1, 256), (257, 16, 4, 768)], ids=str)
+def test_tensor_core_router_shapes(R, E, k, H):
+    """Batches of >= 256 rows take the tensor-core screening path (E <= 256,
+    E % 16 == 0, k <= 16); ids and weights stay bit-identical to the oracle."""
+    w = _small(H=H, E=E, k=k, rows=(R,), sigma_r=0.02)
+    _route_only(Case(w))
+
+
+def test_tensor_core_router_ties_and_blocks():
+    w = _small(E=64, k=8, rows=(100, 200, 84), sigma_r=0.02)
+    T = W.make_tensors(w, device="cuda")
+    T.w_router[40] = T.w_router[3]
+    T.w_router[63] = T.w_router[3]
+    bias = torch.randn(3, w.E, generator=torch.Generator().manual_seed(1)).to("cuda") * 0.1
+    _route_only(Case(w, T=T, bias=bias))
+
+
+def test_tensor_core_router_nonfinite_rows_fall_back():
+    """NaN / -inf logits leave fewer comparable values; such rows are recomputed
+    over every expert and still match the oracle."""
+    w = _small(E=32, k=8, rows=(300,), sigma_r=0.02)
+    T = W.make_tensors(w, device="cuda")
+    bias = torch.zeros(1, w.E, dtype=torch.float32, device="cuda")
+    bias[0, :20] = float("nan")
+    bias[0, 20:26] = float("-inf")
+    case = Case(w, T=T, bias=bias)
+    g, ref = _route_only(case)
+    assert (g["idx"][:, :6] >= 26).all()
