@@ -2,8 +2,9 @@
 
 One step = one pass of the whole layer over one batch: route -> coreset ->
 forward, through the C ABI of libmoeblock, replayed as a CUDA graph with the
-inputs resident in HBM.  L2 is flushed (a 256 MiB write) between steps,
-outside the timed events.  Prints ONE JSON line.
+inputs resident in HBM.  L2 is flushed between steps, outside the timed
+events: a 256 MiB write, then a 256 MiB read of another buffer, so the step
+starts with no dirty lines to write back.  Prints ONE JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
@@ -283,6 +284,12 @@ def run_gpu(args, w: W.Workload):
     layer = moe_block.MoeBlockLayer(T.w_router, T.w_gate, T.w_up, T.w_down, T.ws_gate, T.ws_up,
                                     T.ws_down, k=w.k, max_rows=w.R, max_blocks=w.nb)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2(i):
+        flush.fill_(float(i))
+        torch.sum(flush_rd, dim=0, out=flush_out)
     stream = torch.cuda.Stream(device=dev)
     y = torch.empty(w.R, w.H, dtype=torch.bfloat16, device=dev)
 
@@ -327,7 +334,7 @@ def run_gpu(args, w: W.Workload):
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
             for i in range(args.steps):
-                flush.fill_(float(i))
+                flush_l2(i)
                 step_ev[i][0].record(stream)
                 graph.replay()
                 step_ev[i][1].record(stream)
@@ -341,6 +348,36 @@ def run_gpu(args, w: W.Workload):
     barrier(ws)
     total_ms = reduce_max(sum(step_ms), ws, dev)
     clocks = clk.summary()
+
+    # per-phase breakdown (not the headline): the three calls as separate graphs,
+    # replayed back to back behind the L2 flush so no host gap falls inside
+    phase_ms = {"route": [], "coreset": [], "forward": []}
+    graphs = {}
+    idx_t, w_t = layer._topk_idx[:w.R], layer._topk_w[:w.R]
+    keep_t, wr_t = layer._keep[:w.nb], layer._w_renorm[:w.R]
+    calls = {
+        "route": lambda: layer.route(T.x, T.block_offsets, T.bias),
+        "coreset": lambda: layer.coreset(T.block_offsets, idx_t, w_t, w.tau),
+        "forward": lambda: layer.forward(T.x, T.block_offsets, idx_t, wr_t, keep_t, y=y),
+    }
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs[name] = g
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(min(args.steps, 50)):
+            flush_l2(i)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            evs[0].record(stream)
+            for j, name in enumerate(("route", "coreset", "forward")):
+                graphs[name].replay()
+                evs[j + 1].record(stream)
+            evs[3].synchronize()
+            for j, name in enumerate(("route", "coreset", "forward")):
+                phase_ms[name].append(evs[j].elapsed_time(evs[j + 1]))
+    torch.cuda.synchronize()
 
     # end to end through the public API with host buffers (pinned), no graph
     x_host = T.x.cpu().pin_memory()
@@ -359,7 +396,7 @@ def run_gpu(args, w: W.Workload):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2e_ms = 0.0
         for i in range(e2e_steps):
-            flush.fill_(float(i))
+            flush_l2(i)
             e0.record(stream)
             x_dev.copy_(x_host, non_blocking=True)
             off_dev.copy_(off_host, non_blocking=True)
@@ -390,7 +427,8 @@ def run_gpu(args, w: W.Workload):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,s) bf16 inputs and weights; no trained weights)",
-        "config": config_of(w, f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)"),
+        "config": config_of(w, f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, then "
+                               f"{FLUSH_BYTES >> 20} MiB read of another buffer)"),
         "expert_weight_gbs": acc["weight_bytes"] / t_step / 1e9,
         "step_roofline_frac": step_frac,
         "roofline": {"bound": "hbm", "kernel": "k_gemm gate/up (tcgen05)",
@@ -400,6 +438,7 @@ def run_gpu(args, w: W.Workload):
                      "launch_us": t_gu * 1e6, "peak_source": peaks["source"]},
         "kernel_us": {"scatter": 1e3 * statistics.mean(sc_ms), "gate_up": t_gu * 1e6,
                       "down": 1e3 * statistics.mean(dn_ms)},
+        "phase_us": {k: 1e3 * statistics.median(v) for k, v in phase_ms.items()},
         "coreset": {"experts": len(used), "pairs": pairs},
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clocks,

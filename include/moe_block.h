@@ -163,8 +163,8 @@ moe_status moe_block_forward(const moe_plan* plan, const void* x, int32_t R,
  * logit_bias, topk_idx and topk_w as for moe_block_route.
  *   - Allocates nothing and calls no allocating routine.
  *   - Rejects with MOE_ERR_UNSUPPORTED any call whose scratch
- *     (4*R*E + 4*ceil(R/4) rounded up to 256, + 256 bytes) exceeds 1 MiB:
- *     at E = 256, R <= 1022.
+ *     (4*R*E + 4*R rounded up to 256, + 256 bytes) exceeds 1 MiB:
+ *     at E = 256, R <= 1019.
  *   - All calls share the array.  The tickets are cleared on `stream` at the
  *     start of each call; calls that overlap on the GPU (other streams, other
  *     host threads) race on the array and must not be issued.

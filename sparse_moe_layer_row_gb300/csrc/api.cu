@@ -186,7 +186,8 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
                 encode_bf16(&p->tm_sd, ws_down, d.Is, d.H, 0, 128, L2W);
     p->tc_route = d.E <= 256 && d.E % 16 == 0 && d.k <= 16;
     if (good && p->tc_route)
-        good = encode_bf16(&p->tm_wr, w_router, d.H, d.E, 0, (uint32_t)d.E,
+        good = encode_bf16(&p->tm_wr, w_router, d.H, d.E, 0,
+                           (uint32_t)((d.E > 128 && d.E % 32 == 0) ? d.E / 2 : d.E),
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
     if (!good) {
         delete p;
@@ -218,15 +219,14 @@ moe_status moe_block_route(const moe_plan* p, const void* x, int32_t R,
         RouteTcArgs ta{static_cast<const __nv_bfloat16*>(x),
                        static_cast<const __nv_bfloat16*>(p->wr), logit_bias, block_offsets, R,
                        p->d.H, p->d.E, p->d.k, nb, at<float>(workspace, L.xnorm),
-                       at<float>(workspace, L.wnorm), at<int32_t>(workspace, L.cand),
-                       at<int32_t>(workspace, L.cand_cnt), topk_idx, topk_w,
+                       at<float>(workspace, L.wnorm), at<float>(workspace, L.logits), topk_idx, topk_w,
                        at<uint32_t>(workspace, L.status)};
         cudaError_t e = launch_route_tc(ta, tm_x, p->tm_wr, p->num_sms, st);
         if (e != cudaSuccess) return cuda_fail(e, "route launch");
         return ok();
     }
     cudaError_t e = cudaMemsetAsync(at<uint8_t>(workspace, L.route_cnt), 0,
-                                    sizeof(uint32_t) * (size_t)((R + 3) / 4), st);
+                                    sizeof(uint32_t) * (size_t)R, st);
     if (e != cudaSuccess) return cuda_fail(e, "route counters");
     RouteArgs a{static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(p->wr),
                 logit_bias, block_offsets, R, p->d.H, p->d.E, p->d.k, nb,
@@ -274,13 +274,14 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     const moe_dims& d = p->d;
     const Layout L = make_layout(d);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const bool small = R <= 64;
+    const bool small = R <= kSmallRows;
     const int nt_gu = small ? kSmallN : kLargeN;
     const int nt_dn = small ? kSmallN : kLargeNDown;
 
     ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, static_cast<const __nv_bfloat16*>(x),
                    R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
-                   at<int32_t>(workspace, L.row_block), at<int32_t>(workspace, L.count),
+                   at<int32_t>(workspace, L.prank), at<int32_t>(workspace, L.hist),
+                   at<int32_t>(workspace, L.count),
                    at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
                    at<int4>(workspace, L.units_gu), at<int4>(workspace, L.units_dn),
                    at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
@@ -290,15 +291,17 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     const auto L2A = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
     gu.a0 = p->tm_wg; gu.a1 = p->tm_wu; gu.a2 = p->tm_sg; gu.a3 = p->tm_su;
     dn.a0 = p->tm_wd; dn.a1 = p->tm_wd; dn.a2 = p->tm_sd; dn.a3 = p->tm_sd;
-    bool good = encode_bf16(&gu.b0, at<void>(workspace, L.xp), d.H, (uint64_t)L.max_pairs, 0, 16, L2A) &&
-                encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, 16, L2A) &&
+    const uint32_t box = small ? 16 : 64;   // B rows per TMA box (see k_gemm)
+    bool good = encode_bf16(&gu.b0, at<void>(workspace, L.xp), d.H, (uint64_t)L.max_pairs, 0, box, L2A) &&
+                encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
+                encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
                 encode_bf16(&dn.b0, at<void>(workspace, L.h), 2 * (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
-                            16, L2A) &&
+                            box, L2A) &&
                 encode_bf16(&dn.b1, at<void>(workspace, L.hs), 2 * (uint64_t)d.Is,
-                            (uint64_t)d.max_rows, 0, 16, L2A);
+                            (uint64_t)d.max_rows, 0, box, L2A);
     if (!good) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation tensor");
     GemmArgs ga{at<int4>(workspace, L.units_gu), at<int32_t>(workspace, L.misc) + 1, d.E, d.H, d.I,
-                d.Is, at<__nv_bfloat16>(workspace, L.h), at<__nv_bfloat16>(workspace, L.hs),
+                d.Is, R, at<__nv_bfloat16>(workspace, L.h), at<__nv_bfloat16>(workspace, L.hs),
                 at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
                 at<float>(workspace, L.y32), at<uint32_t>(workspace, L.status)};
     // Under stream capture an event record must be an external node to be
@@ -313,7 +316,7 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
                                     : cudaSuccess;
     };
     cudaError_t e = mark(0);
-    if (e == cudaSuccess) e = launch_scatter(sa, p->num_sms, st);
+    if (e == cudaSuccess) e = launch_scatter(sa, small, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
     if ((e = mark(1)) == cudaSuccess) e = launch_gemm(kGateUp, small, gu, ga, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");

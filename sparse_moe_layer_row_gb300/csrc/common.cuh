@@ -19,13 +19,12 @@ namespace moe {
 
 struct Layout {
     size_t status;       // uint32[MOE_STATUS_WORDS]
-    size_t route_cnt;    // uint32[ceil(max_rows/4)]   router row-group tickets
+    size_t route_cnt;    // uint32[max_rows]          router row / row-group tickets
     size_t logits;       // fp32 [max_rows, E]        router logits (before bias)
     size_t xnorm;        // fp32 [max_rows]           |x_r|_2 (large-batch router)
     size_t wnorm;        // fp32 [E]                  |w_e|_2
-    size_t cand;         // int32 [max_rows, 32]      router candidates per row
-    size_t cand_cnt;     // int32 [max_rows]
-    size_t row_block;    // int32 [max_rows]
+    size_t prank;        // int32 [max_pairs]         pair rank within (block, expert)
+    size_t hist;         // int32 [max_blocks, E]     pairs per (block, expert) / bases
     size_t count;        // int32 [E]                 surviving pairs per expert
     size_t expert_off;   // int32 [E + 1]
     size_t misc;         // int32[16]: [0] ticket, [1] units gate/up, [2] units down, [3] pairs
@@ -64,13 +63,12 @@ inline Layout make_layout(const moe_dims& d) {
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
     L.status = take(sizeof(uint32_t) * 64);
-    L.route_cnt = take(sizeof(uint32_t) * (size_t)((R + 3) / 4));
+    L.route_cnt = take(sizeof(uint32_t) * (size_t)R);
     L.logits = take(sizeof(float) * (size_t)(R * E));
     L.xnorm = take(sizeof(float) * (size_t)R);
     L.wnorm = take(sizeof(float) * (size_t)E);
-    L.cand = take(sizeof(int32_t) * (size_t)R * 32);
-    L.cand_cnt = take(sizeof(int32_t) * (size_t)R);
-    L.row_block = take(sizeof(int32_t) * (size_t)R);
+    L.prank = take(sizeof(int32_t) * (size_t)P);
+    L.hist = take(sizeof(int32_t) * (size_t)d.max_blocks * (size_t)E);
     L.count = take(sizeof(int32_t) * (size_t)E);
     L.expert_off = take(sizeof(int32_t) * (size_t)(E + 1));
     L.misc = take(sizeof(int32_t) * 16);
@@ -101,6 +99,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Kernel launch through cudaLaunchKernelEx (one call site style for all kernels).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 // ---- mbarrier ---------------------------------------------------------------
@@ -170,6 +180,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Gather four rows (r0..r3, one-row box of the map) at column c0 into 4
+// consecutive box rows of shared memory; rows out of range read as zero.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int c0, int r0,
+                                            int r1, int r2, int r3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -67,7 +67,6 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
     __shared__ unsigned long long Q[kMaxE];
     __shared__ uint32_t touched[kMaxE / 32];
     __shared__ uint32_t incore[kMaxE / 32];
-    __shared__ int32_t sorted[kMaxE];
     __shared__ unsigned long long keys[kMaxE];
     __shared__ uint64_t warp_sums[32];
     __shared__ int s_bad, s_empty;
@@ -112,54 +111,36 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
     for (int w = 0; w < words; ++w) nt += __popc(touched[w]);
 
     const bool disabled = !(a.tau < 1.0f);
-    int c;
     if (disabled) {
-        c = nt;
         for (int w = tid; w < words; w += blockDim.x) incore[w] = touched[w];
     } else {
         const uint64_t theta = mass_threshold(a.tau, T);
-        // rank of each touched expert under (Q desc, id asc): one 64-bit key per
-        // expert, (Q << 10 | (1023 - e)) + 1 for touched experts, 0 otherwise
-        // (Q < 2^53 since a block holds fewer than 2^21 rows).
+        // Order (Q desc, id asc) as one 64-bit key per expert: (Q << 10 | (1023 - e)) + 1
+        // for touched experts, 0 otherwise (Q < 2^53: a block has fewer than 2^21 rows).
         for (int e = tid; e < E; e += blockDim.x)
             keys[e] = ((touched[e >> 5] >> (e & 31)) & 1u)
                           ? ((unsigned long long)Q[e] << 10 | (unsigned long long)(1023 - e)) + 1ull
                           : 0ull;
         __syncthreads();
+        // An expert is in the coreset iff the mass of the experts ranked above it
+        // is still below theta: the greedy prefix in (Q desc, id asc) order stops
+        // at the first expert whose inclusion reaches theta.
         for (int e = tid; e < E; e += blockDim.x) {
             const unsigned long long ke = keys[e];
             if (!ke) continue;
-            int rank = 0;
+            unsigned long long above = 0;
             int f = 0;
             for (; f + 8 <= E; f += 8) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) rank += keys[f + j] > ke;
+                for (int j = 0; j < 8; ++j) above += keys[f + j] > ke ? Q[f + j] : 0ull;
             }
-            for (; f < E; ++f) rank += keys[f] > ke;
-            sorted[rank] = e;
-        }
-        __syncthreads();
-        // exclusive prefix of Q in rank order; each thread owns a contiguous run of ranks
-        const int per = (nt + blockDim.x - 1) / blockDim.x;
-        const int i0 = min(nt, tid * per), i1 = min(nt, i0 + per);
-        uint64_t local = 0;
-        for (int i = i0; i < i1; ++i) local += Q[sorted[i]];
-        uint64_t tot;
-        uint64_t run = block_excl_scan_u64(local, warp_sums, &tot);
-        int below = 0;
-        for (int i = i0; i < i1; ++i) {
-            below += run < theta;
-            run += Q[sorted[i]];
-        }
-        // c = number of ranks whose exclusive prefix is below theta
-        uint64_t cnt_total;
-        (void)block_excl_scan_u64((uint64_t)below, warp_sums, &cnt_total);
-        c = (int)cnt_total;
-        for (int i = tid; i < c; i += blockDim.x) {
-            const int e = sorted[i];
-            atomicOr(&incore[e >> 5], 1u << (e & 31));
+            for (; f < E; ++f) above += keys[f] > ke ? Q[f] : 0ull;
+            if (above < theta) atomicOr(&incore[e >> 5], 1u << (e & 31));
         }
     }
+    __syncthreads();
+    int c = 0;
+    for (int w = 0; w < words; ++w) c += __popc(incore[w]);
     __syncthreads();
     for (int w = tid; w < words; w += blockDim.x) a.keep[(size_t)b * words + w] = incore[w];
     if (tid == 0) a.core_size[b] = c;
@@ -200,8 +181,7 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
 
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t st) {
     if (a.nb <= 0) return cudaSuccess;
-    k_coreset<<<a.nb, kCoreThreads, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_coreset, dim3(a.nb), dim3(kCoreThreads), 0, st, a);
 }
 
 }  // namespace moe

@@ -46,6 +46,9 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s when draining after 
 template <int MODE, int NMAX, int STAGES>
 struct GemmCfg {
     static constexpr int kBParts = MODE == kDown ? 2 : 1;  // down: hi and lo parts of h
+    // rows per B box: 16 for the streaming shape, 64 for the large shape (fewer
+    // TMA instructions per stage; NMAX is a multiple of it)
+    static constexpr int kBoxRows = NMAX >= 64 ? 64 : 16;
     static constexpr int kABytes = 128 * 128;
     static constexpr int kBBytes = kBParts * NMAX * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -55,7 +58,7 @@ struct GemmCfg {
     static constexpr int kSmem = kBarOff + 256 + 1024;
     static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
-    static_assert(NMAX % 16 == 0 && NMAX <= 256, "MMA N extent");
+    static_assert(NMAX % 16 == 0 && NMAX <= 256 && NMAX % (NMAX >= 64 ? 64 : 16) == 0, "MMA N extent");
 };
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
@@ -65,11 +68,11 @@ __global__ void __launch_bounds__(192, 2)
 k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
-       GemmArgs a) {
+       const __grid_constant__ CUtensorMap tmBg, GemmArgs a) {
     using C = GemmCfg<MODE, NMAX, STAGES>;
+    // small gate/up units gather their rows of x (pair_row) with TMA gather4
+    constexpr bool kGather = MODE == kGateUp && NMAX == kSmallN;
     extern __shared__ uint8_t smem_raw[];
-    const int nunits = __ldg(a.n_units);
-    if ((int)blockIdx.x >= nunits) return;  // uniform: no unit for this CTA
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -94,42 +97,58 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
-        prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmA2);
-        prefetch_tmap(&tmA3); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
     }
     if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmA2);
+        prefetch_tmap(&tmA3); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
+        if (kGather) prefetch_tmap(&tmBg);
+    }
+    const int nunits = __ldg(a.n_units);
 
     auto give_up = [&]() {
         if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
     };
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------------ TMA producer
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-                const int4 un = __ldg(a.units + u);
-                const int g = un.x, m = un.y, start = un.z, n = un.w;
-                const int nb16 = (n + 15) >> 4;
-                const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
-                const uint32_t bytes = (uint32_t)(C::kABytes + C::kBParts * nb16 * 2048);
-                const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
-                for (int kb = 0; kb < (K >> 6); ++kb) {
-                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitLimitNs)) {
-                        give_up();
-                        ok = false;
-                        break;
-                    }
+        // ---------------------------------------------------------- TMA producer
+        // (the whole warp runs the loop; lane 0 issues the copies)
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+            const int4 un = __ldg(a.units + u);
+            const int g = un.x, m = un.y, start = un.z, n = un.w;
+            // B rows actually loaded: gathered units load ceil(n/4) rows x 4; the
+            // others whole boxes of kBoxRows.  Rows of the tile past n only feed
+            // output columns that are never read, so they need not be loaded.
+            const int nb4 = (n + 3) >> 2;
+            const int nbox = (n + C::kBoxRows - 1) / C::kBoxRows;
+            const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
+            const uint32_t bbytes = kGather ? (uint32_t)nb4 * 512u
+                                            : (uint32_t)(nbox * C::kBoxRows * 128);
+            const uint32_t bytes = (uint32_t)C::kABytes + C::kBParts * bbytes;
+            const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
+            // rows of x for a gathered unit (one per lane; rows >= R read as zero)
+            int prow = a.R;
+            if (kGather && lane < n)
+                prow = g == a.E ? start + lane : __ldg(a.pair_row + start + lane);
+            for (int kb = 0; kb < (K >> 6); ++kb) {
+                const bool w_ok = mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitLimitNs);
+                if (__any_sync(0xffffffffu, !w_ok)) {
+                    if (lane == 0) give_up();
+                    ok = false;
+                    break;
+                }
+                const uint32_t sA = sbase + stage * C::kStageBytes;
+                const uint32_t sB = sA + C::kABytes;
+                const int kc = kb * 64;
+                if (lane == 0) {
                     mbar_expect_tx(full + stage, bytes);
-                    const uint32_t sA = sbase + stage * C::kStageBytes;
-                    const uint32_t sB = sA + C::kABytes;
-                    const int kc = kb * 64;
                     if (MODE == kGateUp) {
                         const int rows = m * 64;
                         if (g == a.E) {
@@ -143,18 +162,31 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (g == a.E) tma_load_2d(sA, &tmA2, kc, m * 128, full + stage);
                         else tma_load_3d(sA, &tmA0, kc, m * 128, g, full + stage);
                     }
-                    for (int t = 0; t < nb16; ++t)
-                        tma_load_2d(sB + t * 2048, mB, kc, start + t * 16, full + stage);
-                    if (MODE == kDown)  // lo part of h: columns K .. 2K-1 of the same rows
-                        for (int t = 0; t < nb16; ++t)
-                            tma_load_2d(sB + NMAX * 128 + t * 2048, mB, K + kc, start + t * 16,
-                                        full + stage);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                if (kGather) {
+                    for (int t = 0; t < nb4; ++t) {
+                        const int r0 = __shfl_sync(0xffffffffu, prow, (4 * t + 0) & 31);
+                        const int r1 = __shfl_sync(0xffffffffu, prow, (4 * t + 1) & 31);
+                        const int r2 = __shfl_sync(0xffffffffu, prow, (4 * t + 2) & 31);
+                        const int r3 = __shfl_sync(0xffffffffu, prow, (4 * t + 3) & 31);
+                        if (lane == 0) tma_gather4(sB + t * 512, &tmBg, kc, r0, r1, r2, r3, full + stage);
+                    }
+                } else if (lane == 0) {
+                    constexpr int kBoxBytes = C::kBoxRows * 128;
+                    for (int t = 0; t < nbox; ++t)
+                        tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, full + stage);
+                    if (MODE == kDown)  // lo part of h: columns K .. 2K-1 of the same rows
+                        for (int t = 0; t < nbox; ++t)
+                            tma_load_2d(sB + NMAX * 128 + t * kBoxBytes, mB, K + kc,
+                                        start + t * C::kBoxRows, full + stage);
+                }
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
-            // Drain: every stage must be released by the MMA before the CTA
-            // exits (all copies landed, all reads done).  Bounded; after an
-            // abort the MMA may never release, so the wait gives up quickly.
+        }
+        // Drain: every stage must be released by the MMA before the CTA
+        // exits (all copies landed, all reads done).  Bounded; after an
+        // abort the MMA may never release, so the wait gives up quickly.
+        if (lane == 0) {
             for (int i = 0; i < STAGES; ++i) {
                 const uint64_t lim = *abort_flag ? kDrainLimitNs : kWaitLimitNs;
                 if (!mbar_wait_bounded(empty + stage, phase ^ 1u, never, lim)) {
@@ -280,7 +312,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             float w;
                             if (g == a.E) { row = start + col; w = 1.0f; }
                             else { row = __ldg(a.pair_row + start + col); w = __ldg(a.pair_w + start + col); }
-                            atomicAdd(a.y32 + (size_t)row * a.H + hrow, w * v[t]);
+                            if ((unsigned)row < (unsigned)a.R)
+                                atomicAdd(a.y32 + (size_t)row * a.H + hrow, w * v[t]);
                         }
                     }
                 }
@@ -305,9 +338,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 template <int MODE, int NMAX, int STAGES>
 static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int grid, cudaStream_t st) {
     using C = GemmCfg<MODE, NMAX, STAGES>;
-    k_gemm<MODE, NMAX, STAGES><<<grid, 192, C::kSmem, st>>>(mp.a0, mp.a1, mp.a2, mp.a3, mp.b0,
-                                                             mp.b1, a);
-    return cudaGetLastError();
+    return launch_kernel(k_gemm<MODE, NMAX, STAGES>, dim3(grid), dim3(192), C::kSmem, st, mp.a0, mp.a1,
+                      mp.a2, mp.a3, mp.b0, mp.b1, mp.bg, a);
 }
 
 template <int MODE, int NMAX, int STAGES>

@@ -29,8 +29,7 @@ struct RouteTcArgs {
     int R, H, E, k, nb;
     float* xnorm;         // [R]
     float* wnorm;         // [E]
-    int32_t* cand;        // [R, kCandCap]
-    int32_t* cand_cnt;    // [R]; -1: recompute every expert of the row
+    float* logits;        // [R, E] approximate logits (tensor cores)
     int32_t* topk_idx;
     float* topk_w;
     uint32_t* status;
@@ -55,7 +54,8 @@ struct ScatterArgs {
     const __nv_bfloat16* x;
     int R, H, E, k, I, Is, nb;
     int nt_gu, nt_dn;   // rows per unit of the gate/up and of the down GEMM
-    int32_t* row_block;
+    int32_t* prank;       // [R * k] rank of a pair among its block's pairs of its expert, or -1
+    int32_t* hist;        // [nb, E] pairs per (block, expert), then their base offsets
     int32_t* count;
     int32_t* expert_off;
     int32_t* misc;
@@ -77,6 +77,7 @@ struct GemmArgs {
     const int4* units;
     const int32_t* n_units;
     int E, H, I, Is;
+    int R;                // rows of x (gathered row indices >= R read as zero)
     __nv_bfloat16* h;     // [pairs, 2I]: bf16 hi part | bf16 lo part
     __nv_bfloat16* hs;    // [rows, 2Is]
     const int32_t* pair_row;
@@ -86,13 +87,17 @@ struct GemmArgs {
 };
 struct GemmMaps {
     CUtensorMap a0, a1, a2, a3, b0, b1;
+    CUtensorMap bg;   // x with a one-row box: TMA gather4 of routed rows (small batches)
 };
+// Small batches (R <= kSmallRows): one-CTA bookkeeping and gathered x rows.
+constexpr int kSmallRows = 32;
+constexpr int kMaxExperts = 1024;
 cudaError_t launch_route(const RouteArgs&, int num_sms, cudaStream_t);
 cudaError_t route_tc_set_attributes();
 cudaError_t launch_route_tc(const RouteTcArgs&, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                             int num_sms, cudaStream_t);
 cudaError_t launch_coreset(const CoresetArgs&, cudaStream_t);
-cudaError_t launch_scatter(const ScatterArgs&, int num_sms, cudaStream_t);
+cudaError_t launch_scatter(const ScatterArgs&, bool small, int num_sms, cudaStream_t);
 cudaError_t launch_finalize(const FinalArgs&, int num_sms, cudaStream_t);
 cudaError_t gemm_set_attributes();
 cudaError_t launch_gemm(int mode, bool small, const GemmMaps&, const GemmArgs&, int grid,

@@ -14,8 +14,8 @@
 //     library, for as long as the library stays loaded.
 //   * Calls needing more scratch than that are rejected with
 //     MOE_ERR_UNSUPPORTED and nothing is launched.  A call needs 4 * R * E
-//     bytes of logits, 4 * ceil(R / 4) bytes of tickets rounded up to 256, and
-//     256 bytes of status; at E = 256 that allows up to 1022 rows.
+//     bytes of logits, 4 * R bytes of tickets rounded up to 256, and 256
+//     bytes of status; at E = 256 that allows up to 1019 rows.
 //   * All calls share the one array, which keeps what the last call left in
 //     it. The tickets that must start at zero are cleared on the stream at the
 //     start of every call. Calls that overlap on the GPU (different streams,
@@ -82,7 +82,7 @@ extern "C" moe_status moe_block_route_noalloc(const moe_plan* plan, const void* 
         return set_error(MOE_ERR_INVALID_ARG, "topk_idx/topk_w NULL or misaligned");
     if (logit_bias && !aligned_to(logit_bias, 4))
         return set_error(MOE_ERR_INVALID_ARG, "logit_bias misaligned");
-    const size_t cnt_bytes = align_up(sizeof(uint32_t) * (size_t)((R + 3) / 4), 256);
+    const size_t cnt_bytes = align_up(sizeof(uint32_t) * (size_t)R, 256);
     const size_t logit_bytes = sizeof(float) * (size_t)R * (size_t)pv.d.E;
     if (kStatusBytes + cnt_bytes + logit_bytes > kNoAllocScratchBytes)
         return set_error(MOE_ERR_UNSUPPORTED,

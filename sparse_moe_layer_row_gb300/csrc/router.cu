@@ -3,7 +3,7 @@
 // in route_common.cuh (model card "Clover-35B-A3B-Preview -- CMF", intro:
 // top-8 of 256 experts).
 //
-// One warp computes a 4-row x 8-expert tile of logits: 32 accumulators per
+// Medium batches: one warp computes a 4-row x 8-expert tile of logits: 32 accumulators per
 // lane, the stripes' loads double-buffered in registers.  The 32 lane sums of
 // the 32 accumulators are reduced with a transposed butterfly (each step keeps
 // half of the accumulators and trades the other half with the partner lane),
@@ -140,7 +140,95 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
     }
 }
 
+// Small batches: one warp computes 1 row x 4 experts, with all of its stripes'
+// loads in flight at once (groups of 8 stripes), so the latency of one memory
+// round trip is paid instead of one per stripe; the four accumulators are
+// reduced by two transposed halving steps and three plain butterfly steps
+// (the same pairs as the contract's butterfly); a ticket per row lets the
+// warp finishing a row run its top-k.
+constexpr int kSmallRouteRows = 64;
+constexpr int kSmET = 4;
+constexpr int kSmPD = 8;   // stripes in flight per warp
+
+__global__ void __launch_bounds__(256, 1) k_route_small(RouteArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int n_eg = (a.E + kSmET - 1) / kSmET;
+    const int ntasks = a.R * n_eg;
+    for (int t = warp; t < ntasks; t += nwarps) {
+        const int row = t / n_eg, eg = t - row * n_eg;
+        const __nv_bfloat16* xr = a.x + (size_t)row * a.H;
+        float acc[kSmET];
+#pragma unroll
+        for (int i = 0; i < kSmET; ++i) acc[i] = 0.0f;
+        for (int s0 = 0; s0 < a.H; s0 += kSmPD * 256) {
+            uint4 xv[kSmPD], wv[kSmPD][kSmET];
+#pragma unroll
+            for (int si = 0; si < kSmPD; ++si) {
+                const int col = s0 + si * 256 + lane * 8;
+                const bool in = col < a.H;
+                xv[si] = in ? __ldg(reinterpret_cast<const uint4*>(xr + col)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int e = 0; e < kSmET; ++e) {
+                    const int ex = eg * kSmET + e;
+                    wv[si][e] = (in && ex < a.E)
+                        ? __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)ex * a.H + col))
+                        : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int si = 0; si < kSmPD; ++si) {
+                if (s0 + si * 256 >= a.H) break;
+                float xf[8];
+                bf16x8(xv[si], xf);
+#pragma unroll
+                for (int e = 0; e < kSmET; ++e) {
+                    float wf[8];
+                    bf16x8(wv[si][e], wf);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[e] = __fmaf_rn(xf[q], wf[q], acc[e]);
+                }
+            }
+        }
+        // halving at partner distances 16 and 8 (4 -> 1 accumulators), then
+        // plain butterfly steps at 4, 2, 1; lane holds expert (lane >> 3) & 3
+#pragma unroll
+        for (int o = 16, h = 2; o >= 8; o >>= 1, h >>= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < h; ++i) {
+                const float send = upper ? acc[i] : acc[i + h];
+                const float keep = upper ? acc[i + h] : acc[i];
+                acc[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+            }
+        }
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) acc[0] = __fadd_rn(acc[0], __shfl_xor_sync(0xffffffffu, acc[0], o));
+        {
+            const int ex = eg * kSmET + ((lane >> 3) & 3);
+            if ((lane & 7) == 0 && ex < a.E) a.logits[(size_t)row * a.E + ex] = acc[0];
+        }
+        __syncwarp();
+        __threadfence();
+        uint32_t old = 0;
+        if (lane == 0) old = atomicAdd(a.cnt + row, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == (uint32_t)(n_eg - 1)) {
+            __threadfence();
+            if (lane == 0) a.cnt[row] = 0u;  // ready for the next call
+            route_topk(a, row, row + 1, lane);
+        }
+    }
+}
+
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
+    if (a.R <= kSmallRouteRows) {
+        const long tasks = (long)a.R * ((a.E + kSmET - 1) / kSmET);
+        long blocks = (tasks + 7) / 8;  // 8 warps per CTA
+        if (blocks < 1) blocks = 1;
+        return launch_kernel(k_route_small, dim3((unsigned)blocks), dim3(256), 0, st, a);
+    }
     const int n_rg = (a.R + kRT - 1) / kRT;
     const int n_eg = (a.E + kET - 1) / kET;
     const long tasks = (long)n_rg * n_eg;
@@ -151,8 +239,7 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t st) {
     const long cap = (long)num_sms * (32 / wpc);
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    k_route<<<(unsigned)blocks, (unsigned)(32 * wpc), 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_route, dim3((unsigned)blocks), dim3((unsigned)(32 * wpc)), 0, st, a);
 }
 
 }  // namespace moe

@@ -20,10 +20,11 @@
 // fewer than k comparable logits) are recomputed over all experts.
 //
 // Kernels: k_route_norms (|x_r| and |w_e|), k_route_tc (persistent; TMA ->
-// tcgen05 -> TMEM, one 128-row tile per unit, all E <= 256 experts as the MMA
-// N extent; epilogue thread = one row: k-th value and candidate list) and
-// k_route_exact (one warp per row: candidates 16 at a time in the contract
-// order, top-k, softmax).
+// tcgen05 -> TMEM; a unit is a 128-row tile times one half (or all) of the
+// experts; the epilogue stores the approximate logits) and k_route_exact (one
+// warp per row: the k-th approximate value by warp reductions, the candidate
+// list by ballots, then the candidates 16 at a time in the contract order,
+// top-k and softmax).
 #include "route_common.cuh"
 
 namespace moe {
@@ -39,8 +40,7 @@ struct TcCfg {
     static constexpr int kABytes = 128 * 128;
     static constexpr int kBBytes = 256 * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kWnOff = kTcStages * kStageBytes;   // fp32 |w_e| (256)
-    static constexpr int kBarOff = kWnOff + 256 * 4;
+    static constexpr int kBarOff = kTcStages * kStageBytes;
     static constexpr int kSmem = kBarOff + 256 + 1024;
 };
 
@@ -72,15 +72,16 @@ __global__ void __launch_bounds__(256) k_route_norms(RouteTcArgs a) {
 
 __global__ void __launch_bounds__(192, 1)
 k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-           RouteTcArgs a) {
+           RouteTcArgs a, int nsplit) {
     using C = TcCfg;
     extern __shared__ uint8_t smem_raw[];
     const int ntiles = (a.R + 127) / 128;
-    if ((int)blockIdx.x >= ntiles) return;
+    const int nunits = ntiles * nsplit;
+    const int NH = a.E / nsplit;  // experts per unit (MMA N)
+    if ((int)blockIdx.x >= nunits) return;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (sbase - raw);
-    float* sw = reinterpret_cast<float*>(base + C::kWnOff);
     uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kBarOff);
     uint64_t* empty = full + kTcStages;
     uint64_t* tfull = empty + kTcStages;
@@ -89,23 +90,23 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int E = a.E;
 
-    for (int e = threadIdx.x; e < E; e += blockDim.x) sw[e] = __ldg(a.wnorm + e);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
-        prefetch_tmap(&tm_x);
-        prefetch_tmap(&tm_w);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tm_x);
+        prefetch_tmap(&tm_w);
+    }
     auto give_up = [&]() {
         if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
     };
@@ -116,8 +117,9 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            const uint32_t bytes = (uint32_t)(C::kABytes + E * 128);
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            const uint32_t bytes = (uint32_t)(C::kABytes + NH * 128);
+            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+                const int t = u / nsplit, sp = u - t * nsplit;
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kTcWaitNs)) {
                         give_up();
@@ -127,7 +129,7 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     mbar_expect_tx(full + stage, bytes);
                     const uint32_t sA = sbase + stage * C::kStageBytes;
                     tma_load_2d(sA, &tm_x, kb * 64, t * 128, full + stage);
-                    tma_load_2d(sA + C::kABytes, &tm_w, kb * 64, 0, full + stage);
+                    tma_load_2d(sA + C::kABytes, &tm_w, kb * 64, sp * NH, full + stage);
                     if (++stage == kTcStages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -142,8 +144,8 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            const uint32_t idesc = idesc_bf16_f32(128, E);
-            for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+            const uint32_t idesc = idesc_bf16_f32(128, NH);
+            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
                 if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kTcWaitNs)) {
                     give_up();
                     break;
@@ -173,78 +175,29 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
         }
     } else {
-        // epilogue: thread = row
+        // epilogue: thread = row; store the approximate logits
         const int q = warp & 3;
-        float wmax = 0.0f;
-        for (int e = 0; e < E; ++e) wmax = fmaxf(wmax, sw[e]);
-        const float G = (float)a.H * 0x1p-21f;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+            const int t = u / nsplit, sp = u - t * nsplit;
             const bool okw = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kTcWaitNs);
             if (__any_sync(0xffffffffu, !okw)) { give_up(); break; }
             __syncwarp();
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
             const int row = t * 128 + q * 32 + lane;
-            const bool valid = row < a.R;
-            const float* brow =
-                (valid && a.bias) ? a.bias + (size_t)find_block(a.off, a.nb, row) * E : nullptr;
-            const float xn = valid ? __ldg(a.xnorm + row) : 0.0f;
-            const float gx = G * xn;
-            // pass 1: the k-th largest approximate logit (NaN never enters)
-            float top[kTcKMax];
-#pragma unroll
-            for (int i = 0; i < kTcKMax; ++i) top[i] = -INFINITY;
-            float kth = -INFINITY;
-            uint32_t nonfinite = 0;
-            for (int c = 0; c < E; c += 16) {
+            float* out = a.logits + (size_t)row * a.E + sp * NH;
+            for (int c = 0; c < NH; c += 16) {
                 float v[16];
                 __syncwarp();
                 tmem_ld16(tb + (uint32_t)c, v);
+                if (row < a.R) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float z = v[i];
-                    if (brow) z = __fadd_rn(z, __ldg(brow + c + i));
-                    nonfinite += !isfinite(z);
-                    if (z > kth) {
-                        // insert into the descending list top[0..k-1]
-#pragma unroll
-                        for (int j = kTcKMax - 1; j >= 0; --j) {
-                            const float above = j > 0 ? top[j > 0 ? j - 1 : 0] : INFINITY;
-                            if (j < a.k && z > top[j]) top[j] = z > above ? above : z;
-                        }
-#pragma unroll
-                        for (int j = 0; j < kTcKMax; ++j)
-                            if (j == a.k - 1) kth = top[j];
-                    }
+                    for (int i = 0; i < 16; i += 4)
+                        *reinterpret_cast<float4*>(out + c + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
                 }
             }
-            const float T = kth;
-            const float thr = T - (gx * wmax + slack(T));
-            // pass 2: candidates in increasing expert order
-            int cnt = 0;
-            int32_t* cl = a.cand + (size_t)(valid ? row : 0) * kCandCap;
-            for (int c = 0; c < E; c += 16) {
-                float v[16];
-                __syncwarp();
-                tmem_ld16(tb + (uint32_t)c, v);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float z = v[i];
-                    if (brow) z = __fadd_rn(z, __ldg(brow + c + i));
-                    if (z + (gx * sw[c + i] + slack(z)) >= thr) {
-                        if (valid && cnt < kCandCap) cl[cnt] = c + i;
-                        ++cnt;
-                    }
-                }
-            }
-            if (valid) {
-                const bool full_row = !(T > -INFINITY) || cnt > kCandCap || cnt < a.k;
-                a.cand_cnt[row] = full_row ? -1 : cnt;
-            }
-            nonfinite = __reduce_add_sync(0xffffffffu, valid ? nonfinite : 0u);
-            if (lane == 0) status_add(a.status, MOE_STATUS_NONFINITE_LOGITS, nonfinite);
             tc_fence_before();
             mbar_arrive(tempty + acc);
             acc ^= 1;
@@ -266,12 +219,55 @@ __global__ void __launch_bounds__(256) k_route_exact(RouteTcArgs a) {
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    __shared__ int32_t s_cand[8][kCandCap];
+    const int wib = threadIdx.x >> 5;
+    const float G = (float)a.H * 0x1p-21f;
+    // max_e |w_e| (every warp of the CTA computes the same value)
+    float wmax = 0.0f;
+    for (int e = lane; e < a.E; e += 32) wmax = fmaxf(wmax, __ldg(a.wnorm + e));
+    wmax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(wmax)));
     for (int r = warp; r < a.R; r += nwarps) {
-        const int cc = __ldg(a.cand_cnt + r);
-        const bool full_row = cc < 0;
-        const int n = full_row ? a.E : cc;
-        const int32_t* cl = a.cand + (size_t)r * kCandCap;
         const float* brow = a.bias ? a.bias + (size_t)find_block(a.off, a.nb, r) * a.E : nullptr;
+        const float gx = G * __ldg(a.xnorm + r);
+        // screening on the approximate logits: the k-th value and the candidates
+        uint32_t akey[8], aid[8];
+        float az[8];
+        uint32_t avalid = 0, nonfinite = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            akey[i] = 0;
+            aid[i] = (uint32_t)e;
+            az[i] = 0.0f;
+            if (e < a.E) {
+                float z = __ldg(a.logits + (size_t)r * a.E + e);
+                if (brow) z = __fadd_rn(z, __ldg(brow + e));
+                nonfinite += !isfinite(z);
+                az[i] = z;
+                akey[i] = order_key(z);
+                avalid |= 1u << i;
+            }
+        }
+        nonfinite = __reduce_add_sync(0xffffffffu, nonfinite);
+        if (lane == 0) status_add(a.status, MOE_STATUS_NONFINITE_LOGITS, nonfinite);
+        uint32_t kid, kkey;
+        warp_topk<8>(akey, aid, avalid, a.k, lane, kid, kkey);
+        const float T = key_value(__shfl_sync(0xffffffffu, kkey, a.k - 1));
+        const float thr = T - (gx * wmax + slack(T));
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            const bool c = ((avalid >> i) & 1u) && az[i] + (gx * __ldg(a.wnorm + (e < a.E ? e : 0)) + slack(az[i])) >= thr;
+            const uint32_t m = __ballot_sync(0xffffffffu, c);
+            const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+            if (c && pos < kCandCap) s_cand[wib][pos] = e;
+            cnt += __popc(m);
+        }
+        __syncwarp();
+        const bool full_row = !(T > -INFINITY) || cnt > kCandCap || cnt < a.k;
+        const int n = full_row ? a.E : cnt;
+        const int32_t* cl = s_cand[wib];
         const __nv_bfloat16* xr = a.x + (size_t)r * a.H;
         uint32_t key[NG], id[NG];
         uint32_t valid = 0;
@@ -284,7 +280,7 @@ __global__ void __launch_bounds__(256) k_route_exact(RouteTcArgs a) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int ci = g * 16 + i;
-                ex[i] = ci < n ? (full_row ? ci : __ldg(cl + ci)) : -1;
+                ex[i] = ci < n ? (full_row ? ci : cl[ci]) : -1;
             }
             float acc[16];
 #pragma unroll
@@ -335,6 +331,7 @@ __global__ void __launch_bounds__(256) k_route_exact(RouteTcArgs a) {
         warp_topk<NG>(key, id, valid, a.k, lane, my_id, my_key);
         write_topk(a.topk_idx + (size_t)r * a.k, a.topk_w + (size_t)r * a.k, a.k, lane, my_id,
                    my_key);
+        __syncwarp();  // s_cand is rewritten by the next row
     }
 }
 
@@ -347,14 +344,18 @@ cudaError_t launch_route_tc(const RouteTcArgs& a, const CUtensorMap& tm_x, const
                             int num_sms, cudaStream_t st) {
     long nb = (long)(a.R + a.E + 7) / 8;
     if (nb > (long)num_sms * 8) nb = (long)num_sms * 8;
-    k_route_norms<<<(unsigned)(nb < 1 ? 1 : nb), 256, 0, st>>>(a);
+    cudaError_t e = launch_kernel(k_route_norms, dim3((unsigned)(nb < 1 ? 1 : nb)), dim3(256), 0, st, a);
     const int ntiles = (a.R + 127) / 128;
-    const int grid = ntiles < num_sms ? ntiles : num_sms;
-    k_route_tc<<<grid, 192, TcCfg::kSmem, st>>>(tm_x, tm_w, a);
+    const int nsplit = (a.E > 128 && a.E % 32 == 0) ? 2 : 1;
+    const int nunits = ntiles * nsplit;
+    const int grid = nunits < num_sms ? nunits : num_sms;
+    if (e == cudaSuccess)
+        e = launch_kernel(k_route_tc, dim3(grid), dim3(192), TcCfg::kSmem, st, tm_x, tm_w, a, nsplit);
     long eb = (long)(a.R + 7) / 8;
     if (eb > (long)num_sms * 16) eb = (long)num_sms * 16;
-    k_route_exact<<<(unsigned)(eb < 1 ? 1 : eb), 256, 0, st>>>(a);
-    return cudaGetLastError();
+    if (e == cudaSuccess)
+        e = launch_kernel(k_route_exact, dim3((unsigned)(eb < 1 ? 1 : eb)), dim3(256), 0, st, a);
+    return e;
 }
 
 }  // namespace moe

@@ -45,26 +45,6 @@ __device__ int block_excl_scan_i32(int v, int* warp_sums, int* total) {
     return before + incl - v;
 }
 
-// Row -> block map, zeroed combine accumulator, reset ticket.
-__global__ void k_fwd_prep(ScatterArgs a) {
-    const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const size_t nth = (size_t)gridDim.x * blockDim.x;
-    for (size_t r = tid; r < (size_t)a.R; r += nth) a.row_block[r] = find_block(a.off, a.nb, (int)r);
-    const size_t n4 = (size_t)a.R * a.H / 4;
-    float4* y4 = reinterpret_cast<float4*>(a.y32);
-    for (size_t i = tid; i < n4; i += nth) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (tid == 0) a.misc[0] = 0;
-}
-
-__device__ __forceinline__ int slots_for(const ScatterArgs& a, int r, int e) {
-    const int b = a.row_block[r];
-    const int words = (a.E + 31) >> 5;
-    if (!((__ldg(a.keep + (size_t)b * words + (e >> 5)) >> (e & 31)) & 1u)) return 0;
-    int c = 0;
-    for (int j = 0; j < a.k; ++j) c += __ldg(a.topk_idx + (size_t)r * a.k + j) == e;
-    return c;
-}
-
 // Units of one group: chunks of nt pairs x weight tiles; chunk-major so the
 // CTAs that run neighbouring units share the same rows of x (L2 reuse).
 __device__ void write_units(int4* out, int base, int g, int start, int n, int nt, int mtiles) {
@@ -75,111 +55,248 @@ __device__ void write_units(int4* out, int base, int g, int start, int n, int nt
     }
 }
 
-// One CTA per expert: count its surviving pairs; the last CTA builds offsets and units.
-__global__ void __launch_bounds__(kScatThreads) k_scatter_count(ScatterArgs a) {
-    __shared__ int warp_sums[32];
-    __shared__ int s_last;
-    const int e = blockIdx.x;
-    int c = 0;
-    for (int r = threadIdx.x; r < a.R; r += blockDim.x) c += slots_for(a, r, e);
-    int total;
-    (void)block_excl_scan_i32(c, warp_sums, &total);
-    if (threadIdx.x == 0) {
-        a.count[e] = total;
-        __threadfence();
-        s_last = atomicAdd(a.misc, 1) == (int)gridDim.x - 1;
+// Large batches: a counting sort of the surviving (row, slot) pairs by expert,
+// in three kernels, all parallel over blocks of rows:
+//   k_scatter_hist   per block: pairs per expert (hist[b][e]) and each pair's
+//                    rank among the block's pairs of its expert, rows in order
+//                    (rows are taken 32 at a time, so any block size works)
+//   k_scatter_scan   one CTA: base[b][e] = offset of expert e + pairs of e in
+//                    earlier blocks (in place over hist), expert offsets, the
+//                    unit lists of both GEMMs
+//   k_scatter_place  per block: pair lists and the staging copy of x rows,
+//                    and a slice of the zeroed combine accumulator
+// A row that names the same expert twice contributes its first slot only
+// (later duplicates are counted as bad ids).
+constexpr int kHistRows = 32;
+
+__global__ void __launch_bounds__(kScatThreads) k_scatter_hist(ScatterArgs a) {
+    __shared__ uint8_t s_slot[kHistRows][kMaxExperts];
+    __shared__ int s_run[kMaxExperts];
+    __shared__ int s_dup;
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int E = a.E, k = a.k;
+    const int words = (E + 31) >> 5;
+    int r0 = a.off[b], r1 = a.off[b + 1];
+    if (!(0 <= r0 && r0 <= r1 && r1 <= a.R)) r1 = r0 = 0;  // counted by the coreset call
+    for (int e = tid; e < E; e += blockDim.x) s_run[e] = 0;
+    if (tid == 0) s_dup = 0;
+    for (int c0 = r0; c0 < r1; c0 += kHistRows) {
+        const int nr = min(kHistRows, r1 - c0);
+        __syncthreads();
+        for (int i = tid; i < nr * E; i += blockDim.x) s_slot[i / E][i % E] = 0xFF;
+        __syncthreads();
+        for (int rr = tid; rr < nr; rr += blockDim.x) {
+            const int r = c0 + rr;
+            int dup = 0;
+            for (int j = 0; j < k; ++j) {
+                const int e = a.topk_idx[(size_t)r * k + j];
+                a.prank[(size_t)r * k + j] = -1;
+                if (e < 0 || e >= E) continue;
+                if (!((a.keep[(size_t)b * words + (e >> 5)] >> (e & 31)) & 1u)) continue;
+                if (s_slot[rr][e] != 0xFF) { ++dup; continue; }
+                s_slot[rr][e] = (uint8_t)j;
+            }
+            if (dup) atomicAdd(&s_dup, dup);
+        }
+        __syncthreads();
+        for (int e = tid; e < E; e += blockDim.x) {
+            int run = s_run[e];
+            for (int rr = 0; rr < nr; ++rr) {
+                const int j = s_slot[rr][e];
+                if (j == 0xFF) continue;
+                a.prank[(size_t)(c0 + rr) * k + j] = run++;
+            }
+            s_run[e] = run;
+        }
     }
     __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    // --- last CTA: offsets over experts, then the unit lists ---
-    const int E = a.E;
+    for (int e = tid; e < E; e += blockDim.x) a.hist[(size_t)b * E + e] = s_run[e];
+    if (tid == 0) status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)s_dup);
+}
+
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
+    __shared__ int warp_sums[32];
+    __shared__ int s_tot[kMaxExperts];
+    const int tid = threadIdx.x, E = a.E, nb = a.nb;
+    // per expert: its total over blocks (thread e, and e + 1024 ...)
+    for (int e = tid; e < E; e += blockDim.x) {
+        int t = 0;
+        for (int b = 0; b < nb; ++b) t += a.hist[(size_t)b * E + e];
+        s_tot[e] = t;
+    }
+    __syncthreads();
     const int mt_gu = a.I / 64, mt_gs = a.Is / 64, mt_dn = a.H / 128;
     const int per = (E + blockDim.x - 1) / blockDim.x;
-    const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
     int sum = 0, ch_gu = 0, ch_dn = 0;
     for (int f = e0; f < e1; ++f) {
-        const int n = __ldcg(a.count + f);
-        sum += n;
-        ch_gu += (n + a.nt_gu - 1) / a.nt_gu;
-        ch_dn += (n + a.nt_dn - 1) / a.nt_dn;
+        sum += s_tot[f];
+        ch_gu += (s_tot[f] + a.nt_gu - 1) / a.nt_gu;
+        ch_dn += (s_tot[f] + a.nt_dn - 1) / a.nt_dn;
     }
     int tot_pairs, tot_gu, tot_dn;
     int p = block_excl_scan_i32(sum, warp_sums, &tot_pairs);
     int cg = block_excl_scan_i32(ch_gu, warp_sums, &tot_gu);
     int cd = block_excl_scan_i32(ch_dn, warp_sums, &tot_dn);
-    // shared expert (group E) first: it has the most rows
     const int base_gu = (a.R + a.nt_gu - 1) / a.nt_gu * mt_gs;
     const int base_dn = (a.R + a.nt_dn - 1) / a.nt_dn * mt_dn;
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         write_units(a.units_gu, 0, E, 0, a.R, a.nt_gu, mt_gs);
         write_units(a.units_dn, 0, E, 0, a.R, a.nt_dn, mt_dn);
     }
     for (int f = e0; f < e1; ++f) {
-        const int n = __ldcg(a.count + f);
+        const int n = s_tot[f];
         a.expert_off[f] = p;
+        a.count[f] = n;
         write_units(a.units_gu, base_gu + cg * mt_gu, f, p, n, a.nt_gu, mt_gu);
         write_units(a.units_dn, base_dn + cd * mt_dn, f, p, n, a.nt_dn, mt_dn);
+        // base[b][f] (in place over hist): offset of f + pairs of f in blocks before b
+        int run = p;
+        for (int b = 0; b < nb; ++b) {
+            const int h = a.hist[(size_t)b * E + f];
+            a.hist[(size_t)b * E + f] = run;
+            run += h;
+        }
         p += n;
         cg += (n + a.nt_gu - 1) / a.nt_gu;
         cd += (n + a.nt_dn - 1) / a.nt_dn;
     }
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         a.expert_off[E] = tot_pairs;
         a.misc[1] = base_gu + tot_gu * mt_gu;
         a.misc[2] = base_dn + tot_dn * mt_dn;
         a.misc[3] = tot_pairs;
-        a.misc[0] = 0;
     }
 }
 
-// One CTA per expert: pair lists in (row, slot) order and the staged rows of x.
-__global__ void __launch_bounds__(kScatThreads) k_scatter_fill(ScatterArgs a) {
-    __shared__ int warp_sums[32];
-    __shared__ int list_row[kScatThreads * 4];
-    __shared__ int list_pos[kScatThreads * 4];
-    const int e = blockIdx.x;
-    const int n_e = a.count[e];
-    if (n_e == 0) return;
-    int pos0 = a.expert_off[e];
+// grid: nb * kPlaceSplit CTAs; CTA (b, part) takes a strided share of block b's pairs.
+constexpr int kPlaceSplit = 4;
+
+__global__ void __launch_bounds__(kScatThreads) k_scatter_place(ScatterArgs a) {
+    const int b = blockIdx.x / kPlaceSplit, part = blockIdx.x % kPlaceSplit;
+    const int E = a.E, k = a.k;
+    int r0 = a.off[b], r1 = a.off[b + 1];
+    if (!(0 <= r0 && r0 <= r1 && r1 <= a.R)) r1 = r0 = 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int hv = a.H / 8;  // uint4 per row of x
-    for (int r0 = 0; r0 < a.R; r0 += blockDim.x) {
-        const int r = r0 + threadIdx.x;
-        const int c = r < a.R ? slots_for(a, r, e) : 0;
-        int total;
-        int pos = pos0 + block_excl_scan_i32(c, warp_sums, &total);
-        if (c) {
-            int li = pos - pos0;
-            for (int j = 0; j < a.k; ++j) {
-                if (a.topk_idx[(size_t)r * a.k + j] != e) continue;
-                a.pair_row[pos] = r;
-                a.pair_w[pos] = a.w_renorm[(size_t)r * a.k + j];
-                if (li < kScatThreads * 4) { list_row[li] = r; list_pos[li] = pos; }
-                ++pos;
-                ++li;
-            }
+    // one warp per pair: lists, then its row of x (uint4 per lane, 8 in flight)
+    for (int p = r0 * k + part * nw + warp; p < r1 * k; p += nw * kPlaceSplit) {
+        const int rk = a.prank[p];
+        if (rk < 0) continue;
+        const int e = a.topk_idx[p];
+        const int pos = a.hist[(size_t)b * E + e] + rk;
+        const int r = p / k;
+        if (lane == 0) {
+            a.pair_row[pos] = r;
+            a.pair_w[pos] = a.w_renorm[p];
         }
-        __syncthreads();
-        // copy the listed rows of x (total may exceed the list only with duplicate ids)
-        const int listed = min(total, kScatThreads * 4);
-        for (int i = threadIdx.x; i < listed * hv; i += blockDim.x) {
-            const int l = i / hv, v = i - l * hv;
-            const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)list_row[l] * a.H);
-            uint4* dst = reinterpret_cast<uint4*>(a.xp + (size_t)list_pos[l] * a.H);
-            dst[v] = __ldg(src + v);
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)r * a.H);
+        uint4* dst = reinterpret_cast<uint4*>(a.xp + (size_t)pos * a.H);
+        for (int v = lane; v < hv; v += 32 * 8) {
+            uint4 t[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (v + 32 * i < hv) t[i] = __ldg(src + v + 32 * i);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (v + 32 * i < hv) dst[v + 32 * i] = t[i];
         }
-        if (total > kScatThreads * 4) {
-            // rare: more pairs than the list holds; copy the rest straight from the pair list
-            for (int i = threadIdx.x + listed * hv; i < total * hv; i += blockDim.x) {
-                const int l = i / hv, v = i - l * hv;
-                const int pp = pos0 + l;
-                const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)a.pair_row[pp] * a.H);
-                reinterpret_cast<uint4*>(a.xp + (size_t)pp * a.H)[v] = __ldg(src + v);
-            }
-        }
-        pos0 += total;
-        __syncthreads();
     }
+    // zero the combine accumulator (grid-stride over all CTAs)
+    const size_t n4 = (size_t)a.R * a.H / 4;
+    float4* y4 = reinterpret_cast<float4*>(a.y32);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (size_t)gridDim.x * blockDim.x)
+        y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Small batches (R <= kSmallRows): the whole bookkeeping in one CTA, no
+// staging copy of x (the gate/up GEMM gathers the rows with TMA gather4).
+// Same outputs as the three-kernel path: pair lists in row order per expert,
+// expert offsets, unit lists, a zeroed accumulator.  A row that names the same
+// expert twice contributes its first slot only (later duplicates are counted
+// as bad ids), so the counts and the lists always agree.
+constexpr int kSmallThreads = 512;
+
+__global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) {
+    __shared__ uint8_t s_slot[kSmallRows][kMaxExperts];   // slot of expert e in row r, or 0xFF
+    __shared__ int s_cnt[kMaxExperts];
+    __shared__ int warp_sums[32];
+    __shared__ int s_dup;
+    const int tid = threadIdx.x;
+    const int E = a.E, k = a.k, R = a.R;
+    const int words = (E + 31) >> 5;
+    for (int i = tid; i < R * E; i += blockDim.x) s_slot[i / E][i % E] = 0xFF;
+    if (tid == 0) s_dup = 0;
+    __syncthreads();
+    // one thread per row: mark its surviving slots (first slot wins)
+    for (int r = tid; r < R; r += blockDim.x) {
+        const int b = find_block(a.off, a.nb, r);
+        int dup = 0;
+        for (int j = 0; j < k; ++j) {
+            const int e = a.topk_idx[(size_t)r * k + j];
+            if (e < 0 || e >= E) continue;
+            if (!((a.keep[(size_t)b * words + (e >> 5)] >> (e & 31)) & 1u)) continue;
+            if (s_slot[r][e] != 0xFF) { ++dup; continue; }
+            s_slot[r][e] = (uint8_t)j;
+        }
+        if (dup) atomicAdd(&s_dup, dup);
+    }
+    __syncthreads();
+    // per expert: its rows (walk the rows in order)
+    for (int e = tid; e < E; e += blockDim.x) {
+        int n = 0;
+        for (int r = 0; r < R; ++r) n += s_slot[r][e] != 0xFF;
+        s_cnt[e] = n;
+    }
+    __syncthreads();
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    int sum = 0, ch = 0;
+    for (int f = e0; f < e1; ++f) {
+        sum += s_cnt[f];
+        ch += (s_cnt[f] + a.nt_gu - 1) / a.nt_gu;
+    }
+    int tot_pairs, tot_ch;
+    int pp = block_excl_scan_i32(sum, warp_sums, &tot_pairs);
+    int cc = block_excl_scan_i32(ch, warp_sums, &tot_ch);
+    const int mt_gu = a.I / 64, mt_gs = a.Is / 64, mt_dn = a.H / 128;
+    const int s_chunks = (R + a.nt_gu - 1) / a.nt_gu;   // nt_gu == nt_dn here
+    const int base_gu = s_chunks * mt_gs, base_dn = s_chunks * mt_dn;
+    if (tid == 0) {
+        write_units(a.units_gu, 0, E, 0, R, a.nt_gu, mt_gs);
+        write_units(a.units_dn, 0, E, 0, R, a.nt_dn, mt_dn);
+    }
+    for (int f = e0; f < e1; ++f) {
+        const int n = s_cnt[f];
+        a.expert_off[f] = pp;
+        a.count[f] = n;
+        write_units(a.units_gu, base_gu + cc * mt_gu, f, pp, n, a.nt_gu, mt_gu);
+        write_units(a.units_dn, base_dn + cc * mt_dn, f, pp, n, a.nt_dn, mt_dn);
+        int pos = pp;
+        for (int r = 0; r < R && pos < pp + n; ++r) {
+            const int j = s_slot[r][f];
+            if (j == 0xFF) continue;
+            a.pair_row[pos] = r;
+            a.pair_w[pos] = a.w_renorm[(size_t)r * k + j];
+            ++pos;
+        }
+        pp += n;
+        cc += (n + a.nt_gu - 1) / a.nt_gu;
+    }
+    if (tid == 0) {
+        a.expert_off[E] = tot_pairs;
+        a.misc[1] = base_gu + tot_ch * mt_gu;
+        a.misc[2] = base_dn + tot_ch * mt_dn;
+        a.misc[3] = tot_pairs;
+        status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)s_dup);
+    }
+    // zero the combine accumulator
+    const size_t n4 = (size_t)R * a.H / 4;
+    float4* y4 = reinterpret_cast<float4*>(a.y32);
+    for (size_t i = tid; i < n4; i += blockDim.x) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void k_finalize(FinalArgs a) {
@@ -197,23 +314,21 @@ __global__ void k_finalize(FinalArgs a) {
     }
 }
 
-cudaError_t launch_scatter(const ScatterArgs& a, int num_sms, cudaStream_t st) {
-    const size_t work = (size_t)a.R * a.H / 4;
-    long blocks = (long)((work + 255) / 256);
-    if (blocks > (long)num_sms * 8) blocks = (long)num_sms * 8;
-    if (blocks < 1) blocks = 1;
-    k_fwd_prep<<<(unsigned)blocks, 256, 0, st>>>(a);
-    k_scatter_count<<<a.E, kScatThreads, 0, st>>>(a);
-    k_scatter_fill<<<a.E, kScatThreads, 0, st>>>(a);
-    return cudaGetLastError();
+cudaError_t launch_scatter(const ScatterArgs& a, bool small, int num_sms, cudaStream_t st) {
+    (void)num_sms;
+    if (small) return launch_kernel(k_scatter_small, dim3(1), dim3(kSmallThreads), 0, st, a);
+    cudaError_t e = launch_kernel(k_scatter_hist, dim3(a.nb), dim3(kScatThreads), 0, st, a);
+    if (e == cudaSuccess) e = launch_kernel(k_scatter_scan, dim3(1), dim3(kScanThreads), 0, st, a);
+    if (e == cudaSuccess)
+        e = launch_kernel(k_scatter_place, dim3(a.nb * kPlaceSplit), dim3(kScatThreads), 0, st, a);
+    return e;
 }
 
 cudaError_t launch_finalize(const FinalArgs& a, int num_sms, cudaStream_t st) {
     long blocks = (long)((a.n / 4 + 255) / 256);
     if (blocks > (long)num_sms * 8) blocks = (long)num_sms * 8;
     if (blocks < 1) blocks = 1;
-    k_finalize<<<(unsigned)blocks, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_finalize, dim3((unsigned)blocks), dim3(256), 0, st, a);
 }
 
 }  // namespace moe
