@@ -78,6 +78,7 @@ enum {
     MOE_STATUS_BAD_OFFSETS = 2,       /* blocks with offsets out of order/range */
     MOE_STATUS_EMPTY_ROWS = 3,        /* rows left with only the shared expert */
     MOE_STATUS_WAIT_TIMEOUT = 4,      /* GEMM pipeline waits that gave up */
+    MOE_STATUS_NONFINITE_OUTPUT = 5,  /* 256-column pieces of y with a non-finite value */
     MOE_STATUS_WORDS = 8
 };
 
@@ -143,7 +144,10 @@ moe_status moe_block_coreset(const moe_plan* plan, int32_t R, const int32_t* blo
  *   y[r] = S(x[r]) + sum over slots j of row r whose expert is kept for r's
  *          block of w_renorm[r, j] * E_{topk_idx[r, j]}(x[r])
  * with S the shared expert.  bf16 MMA with fp32 accumulation; the SwiGLU
- * hidden activations are rounded to bf16 before the down projection.
+ * activations enter the down projection as two bf16 parts (hi + lo, about 16
+ * significant bits); each expert's weighted output and the shared output are
+ * staged in fp16 (|value| < 65504) and summed in fp32 per row in a fixed order
+ * (shared expert, then the row's slots in rank order), so y is reproducible.
  *   y      [R, H] bf16 out
  *   y_f32  [R, H] fp32 out (the sum before the bf16 rounding), or NULL
  * Each touched expert's weights are streamed from HBM once per call. */

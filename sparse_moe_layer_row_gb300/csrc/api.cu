@@ -285,7 +285,7 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
                    at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
                    at<int4>(workspace, L.units_gu), at<int4>(workspace, L.units_dn),
                    at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
-                   at<__nv_bfloat16>(workspace, L.xp), at<float>(workspace, L.y32),
+                   at<__nv_bfloat16>(workspace, L.xp), at<int32_t>(workspace, L.inv),
                    at<uint32_t>(workspace, L.status)};
     GemmMaps gu{}, dn{};
     const auto L2A = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
@@ -303,7 +303,7 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     GemmArgs ga{at<int4>(workspace, L.units_gu), at<int32_t>(workspace, L.misc) + 1, d.E, d.H, d.I,
                 d.Is, R, at<__nv_bfloat16>(workspace, L.h), at<__nv_bfloat16>(workspace, L.hs),
                 at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
-                at<float>(workspace, L.y32), at<uint32_t>(workspace, L.status)};
+                at<__half>(workspace, L.ys), (int)L.max_pairs, at<uint32_t>(workspace, L.status)};
     // Under stream capture an event record must be an external node to be
     // recorded at every graph launch (a plain record only orders the capture).
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -325,11 +325,12 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     gd.n_units = at<int32_t>(workspace, L.misc) + 2;
     if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, small, dn, gd, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
-    FinalArgs fa{at<float>(workspace, L.y32), static_cast<__nv_bfloat16*>(y), y_f32,
-                 (size_t)R * d.H};
-    if ((e = mark(3)) == cudaSuccess) e = launch_finalize(fa, p->num_sms, st);
+    CombineArgs ca{at<__half>(workspace, L.ys), at<int32_t>(workspace, L.inv), R, d.H, d.k,
+                   (int)L.max_pairs, static_cast<__nv_bfloat16*>(y), y_f32,
+                   at<uint32_t>(workspace, L.status)};
+    if ((e = mark(3)) == cudaSuccess) e = launch_combine(ca, p->num_sms, st);
     if (e == cudaSuccess) e = mark(4);
-    if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     return ok();
 }
 

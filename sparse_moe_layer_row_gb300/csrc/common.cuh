@@ -35,7 +35,8 @@ struct Layout {
     size_t xp;           // bf16 [max_pairs, H]       rows of x in pair order
     size_t h;            // bf16 [max_pairs, 2I]      routed SwiGLU activations, hi | lo
     size_t hs;           // bf16 [max_rows, 2Is]      shared-expert activations, hi | lo
-    size_t y32;          // fp32 [max_rows, H]        combine accumulator
+    size_t inv;          // int32 [max_pairs]         staging row of each (row, slot)
+    size_t ys;           // fp16 [max_pairs + max_rows, H] staged per-pair and shared outputs
     size_t total;
     int64_t max_pairs, max_units_gu, max_units_dn;
 };
@@ -79,7 +80,8 @@ inline Layout make_layout(const moe_dims& d) {
     L.xp = take(2 * (size_t)(P * H));
     L.h = take(2 * (size_t)(P * 2 * d.I));
     L.hs = take(2 * (size_t)(R * 2 * d.Is));
-    L.y32 = take(sizeof(float) * (size_t)(R * H));
+    L.inv = take(sizeof(int32_t) * (size_t)P);
+    L.ys = take(2 * (size_t)(P + R) * (size_t)H);
     L.total = o;
     return L;
 }

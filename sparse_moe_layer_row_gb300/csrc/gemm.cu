@@ -23,8 +23,8 @@
 //  down:     A = 128 rows of W_down[e] (hidden outputs), B = the hi and the lo
 //            rows of h: two MMAs per K step into one accumulator, so W_down
 //            is read once; the epilogue scales by the pair's renormalised
-//            weight and adds into the fp32 accumulator y32[row, :] (the
-//            shared expert with weight 1).
+//            weight and stages the pair's output row in fp16 (the shared
+//            expert with weight 1, in its own rows); k_combine sums the rows.
 //
 // Pipeline (one CTA per SM, persistent over the unit list):
 //   warp 0 lane 0  TMA producer: STAGES-deep ring of (A tile, B tile) stages
@@ -53,7 +53,7 @@ struct GemmCfg {
     static constexpr int kBBytes = kBParts * NMAX * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kXchgOff = STAGES * kStageBytes;        // gate/up g <-> u exchange
-    static constexpr int kXchgBytes = MODE == kGateUp ? 2 * 64 * 9 * 4 : 0;
+    static constexpr int kXchgBytes = MODE == kGateUp ? 2 * 64 * 9 * 4 : 16 * 128 * 2;
     static constexpr int kBarOff = kXchgOff + kXchgBytes;
     static constexpr int kSmem = kBarOff + 256 + 1024;
     static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
@@ -303,19 +303,42 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                     xphase ^= 1u;
                 } else {
-                    const int hrow = m * 128 + q * 32 + lane;
+                    // weighted fp16 outputs of 16 pairs: transpose through shared
+                    // memory so each pair's 128 columns leave as one 256-B segment
+                    __half* xs = reinterpret_cast<__half*>(base + C::kXchgOff);  // [16][128]
+                    const int hl = q * 32 + lane;
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         const int col = c + t;
-                        if (col < n) {
-                            int row;
-                            float w;
-                            if (g == a.E) { row = start + col; w = 1.0f; }
-                            else { row = __ldg(a.pair_row + start + col); w = __ldg(a.pair_w + start + col); }
-                            if ((unsigned)row < (unsigned)a.R)
-                                atomicAdd(a.y32 + (size_t)row * a.H + hrow, w * v[t]);
+                        const float w = (g == a.E || col >= n) ? 1.0f : __ldg(a.pair_w + start + col);
+                        xs[t * 128 + hl] = __float2half_rn(w * v[t]);
+                    }
+                    mbar_arrive(xbar);
+                    if (__any_sync(0xffffffffu,
+                                   !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitLimitNs))) {
+                        give_up();
+                        alive = false;
+                        break;
+                    }
+                    const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue warps
+                    const size_t row0 = (size_t)(g == a.E ? a.shared_row0 : 0) + start + c;
+#pragma unroll
+                    for (int s2 = 0; s2 < 2; ++s2) {
+                        const int idx = et + 128 * s2;      // 16 rows x 16 segments of 16 B
+                        const int t = idx >> 4, seg = idx & 15;
+                        if (c + t < n) {
+                            const uint4 val = *reinterpret_cast<const uint4*>(xs + t * 128 + seg * 8);
+                            *reinterpret_cast<uint4*>(a.ys + (row0 + t) * a.H + m * 128 + seg * 8) = val;
                         }
                     }
+                    mbar_arrive(xbar + 1);  // the buffer is reused by the next chunk
+                    if (__any_sync(0xffffffffu,
+                                   !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitLimitNs))) {
+                        give_up();
+                        alive = false;
+                        break;
+                    }
+                    xphase ^= 1u;
                 }
             }
             if (!alive) break;

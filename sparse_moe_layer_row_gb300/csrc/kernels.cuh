@@ -2,6 +2,8 @@
 // coreset.cu, scatter.cu, gemm.cu); the host code in api.cu fills them in.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -64,14 +66,17 @@ struct ScatterArgs {
     int32_t* pair_row;
     float* pair_w;
     __nv_bfloat16* xp;
-    float* y32;
+    int32_t* inv;         // [R * k] staging row of (row, slot), or -1
     uint32_t* status;
 };
-struct FinalArgs {
-    const float* y32;
+// y[r] = shared output + sum over surviving slots (rank order) of staged outputs
+struct CombineArgs {
+    const __half* ys;     // [max_pairs + max_rows, H] staged per-pair / shared outputs
+    const int32_t* inv;   // [R * k]
+    int R, H, k, shared_row0;
     __nv_bfloat16* y;
     float* y_f32;
-    size_t n;
+    uint32_t* status;
 };
 struct GemmArgs {
     const int4* units;
@@ -82,7 +87,8 @@ struct GemmArgs {
     __nv_bfloat16* hs;    // [rows, 2Is]
     const int32_t* pair_row;
     const float* pair_w;
-    float* y32;
+    __half* ys;           // [max_pairs + max_rows, H] staged outputs (down GEMM)
+    int shared_row0;      // staging row of the shared expert's row 0
     uint32_t* status;
 };
 struct GemmMaps {
@@ -98,7 +104,7 @@ cudaError_t launch_route_tc(const RouteTcArgs&, const CUtensorMap& tm_x, const C
                             int num_sms, cudaStream_t);
 cudaError_t launch_coreset(const CoresetArgs&, cudaStream_t);
 cudaError_t launch_scatter(const ScatterArgs&, bool small, int num_sms, cudaStream_t);
-cudaError_t launch_finalize(const FinalArgs&, int num_sms, cudaStream_t);
+cudaError_t launch_combine(const CombineArgs&, int num_sms, cudaStream_t);
 cudaError_t gemm_set_attributes();
 cudaError_t launch_gemm(int mode, bool small, const GemmMaps&, const GemmArgs&, int grid,
                         cudaStream_t);

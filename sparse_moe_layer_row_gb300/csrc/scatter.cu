@@ -116,9 +116,19 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_hist(ScatterArgs a) {
 
 constexpr int kScanThreads = 1024;
 
+constexpr int kDownGroup = 32;
+
+// Units of one group in weight-tile-major order (all row chunks of tile 0, then tile 1 ...).
+__device__ void write_units_mmajor(int4* out, int base, int g, int start, int n, int nt, int mtiles) {
+    int u = base;
+    for (int m = 0; m < mtiles; ++m)
+        for (int c0 = 0; c0 < n; c0 += nt) out[u++] = make_int4(g, m, start + c0, min(nt, n - c0));
+}
+
 __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     __shared__ int warp_sums[32];
     __shared__ int s_tot[kMaxExperts];
+    __shared__ int s_cd[kMaxExperts + 1];
     const int tid = threadIdx.x, E = a.E, nb = a.nb;
     // per expert: its total over blocks (thread e, and e + 1024 ...)
     for (int e = tid; e < E; e += blockDim.x) {
@@ -144,14 +154,35 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     const int base_dn = (a.R + a.nt_dn - 1) / a.nt_dn * mt_dn;
     if (tid == 0) {
         write_units(a.units_gu, 0, E, 0, a.R, a.nt_gu, mt_gs);
-        write_units(a.units_dn, 0, E, 0, a.R, a.nt_dn, mt_dn);
+        write_units_mmajor(a.units_dn, 0, E, 0, a.R, a.nt_dn, mt_dn);
     }
+    // down units: expert groups of kDownGroup, each group ordered weight-tile
+    // major, so the CTAs running at one time add into one 128-column slab of
+    // the accumulator for the group's rows (it stays in L2) and each group's
+    // activations are reused from L2 across its weight tiles.
+    {  // chunk prefix of each expert
+        int q = cd;
+        for (int f = e0; f < e1; ++f) {
+            s_cd[f] = q;
+            q += (s_tot[f] + a.nt_dn - 1) / a.nt_dn;
+        }
+    }
+    if (tid == 0) s_cd[E] = tot_dn;
+    __syncthreads();
     for (int f = e0; f < e1; ++f) {
         const int n = s_tot[f];
         a.expert_off[f] = p;
         a.count[f] = n;
         write_units(a.units_gu, base_gu + cg * mt_gu, f, p, n, a.nt_gu, mt_gu);
-        write_units(a.units_dn, base_dn + cd * mt_dn, f, p, n, a.nt_dn, mt_dn);
+        {
+            const int g0 = f / kDownGroup * kDownGroup, g1 = min(E, g0 + kDownGroup);
+            const int gbase = s_cd[g0], gchunks = s_cd[g1] - gbase;
+            for (int m = 0; m < mt_dn; ++m) {
+                int u = base_dn + gbase * mt_dn + m * gchunks + (s_cd[f] - gbase);
+                for (int c0 = 0; c0 < n; c0 += a.nt_dn)
+                    a.units_dn[u++] = make_int4(f, m, p + c0, min(a.nt_dn, n - c0));
+            }
+        }
         // base[b][f] (in place over hist): offset of f + pairs of f in blocks before b
         int run = p;
         for (int b = 0; b < nb; ++b) {
@@ -161,7 +192,6 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
         }
         p += n;
         cg += (n + a.nt_gu - 1) / a.nt_gu;
-        cd += (n + a.nt_dn - 1) / a.nt_dn;
     }
     if (tid == 0) {
         a.expert_off[E] = tot_pairs;
@@ -184,13 +214,17 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_place(ScatterArgs a) {
     // one warp per pair: lists, then its row of x (uint4 per lane, 8 in flight)
     for (int p = r0 * k + part * nw + warp; p < r1 * k; p += nw * kPlaceSplit) {
         const int rk = a.prank[p];
-        if (rk < 0) continue;
+        if (rk < 0) {
+            if (lane == 0) a.inv[p] = -1;
+            continue;
+        }
         const int e = a.topk_idx[p];
         const int pos = a.hist[(size_t)b * E + e] + rk;
         const int r = p / k;
         if (lane == 0) {
             a.pair_row[pos] = r;
             a.pair_w[pos] = a.w_renorm[p];
+            a.inv[p] = pos;
         }
         const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)r * a.H);
         uint4* dst = reinterpret_cast<uint4*>(a.xp + (size_t)pos * a.H);
@@ -204,12 +238,6 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_place(ScatterArgs a) {
                 if (v + 32 * i < hv) dst[v + 32 * i] = t[i];
         }
     }
-    // zero the combine accumulator (grid-stride over all CTAs)
-    const size_t n4 = (size_t)a.R * a.H / 4;
-    float4* y4 = reinterpret_cast<float4*>(a.y32);
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-         i += (size_t)gridDim.x * blockDim.x)
-        y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // Small batches (R <= kSmallRows): the whole bookkeeping in one CTA, no
@@ -235,8 +263,13 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
     for (int r = tid; r < R; r += blockDim.x) {
         const int b = find_block(a.off, a.nb, r);
         int dup = 0;
+        int ids[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < k) ids[j] = a.topk_idx[(size_t)r * k + j];
         for (int j = 0; j < k; ++j) {
-            const int e = a.topk_idx[(size_t)r * k + j];
+            a.inv[(size_t)r * k + j] = -1;
+            const int e = ids[j];
             if (e < 0 || e >= E) continue;
             if (!((a.keep[(size_t)b * words + (e >> 5)] >> (e & 31)) & 1u)) continue;
             if (s_slot[r][e] != 0xFF) { ++dup; continue; }
@@ -281,6 +314,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
             if (j == 0xFF) continue;
             a.pair_row[pos] = r;
             a.pair_w[pos] = a.w_renorm[(size_t)r * k + j];
+            a.inv[(size_t)r * k + j] = pos;
             ++pos;
         }
         pp += n;
@@ -293,24 +327,72 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
         a.misc[3] = tot_pairs;
         status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)s_dup);
     }
-    // zero the combine accumulator
-    const size_t n4 = (size_t)R * a.H / 4;
-    float4* y4 = reinterpret_cast<float4*>(a.y32);
-    for (size_t i = tid; i < n4; i += blockDim.x) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-__global__ void k_finalize(FinalArgs a) {
-    const size_t n4 = a.n / 4;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-         i += (size_t)gridDim.x * blockDim.x) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.y32) + i);
-        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-        uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t*>(&lo);
-        packed.y = *reinterpret_cast<uint32_t*>(&hi);
-        reinterpret_cast<uint2*>(a.y)[i] = packed;
-        if (a.y_f32) reinterpret_cast<float4*>(a.y_f32)[i] = v;
+// One warp per (row, 256 columns): y = staged shared output + the row's staged
+// expert outputs, added in fp32 in rank order (shared first, then the slots);
+// lane owns 8 consecutive columns.  All of a task's contributions are loaded
+// before they are added, eight at a time, so the loads overlap.
+__global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int nchunk = a.H / 256;
+    const int ntasks = a.R * nchunk;
+    for (int t = warp; t < ntasks; t += nwarps) {
+        const int r = t / nchunk;
+        const int c = (t - r * nchunk) * 256 + lane * 8;
+        const int pos = lane < a.k ? a.inv[(size_t)r * a.k + lane] : -1;
+        float acc[8];
+        {
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(a.ys + (size_t)(a.shared_row0 + r) * a.H + c);
+            const __half2* hv = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(hv[i]);
+                acc[2 * i] = f.x;
+                acc[2 * i + 1] = f.y;
+            }
+        }
+        for (int j0 = 0; j0 < a.k; j0 += 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int p = __shfl_sync(0xffffffffu, pos, (j0 + j) & 31);
+                v[j] = (j0 + j < a.k && p >= 0)
+                           ? *reinterpret_cast<const uint4*>(a.ys + (size_t)p * a.H + c)
+                           : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int p = __shfl_sync(0xffffffffu, pos, (j0 + j) & 31);
+                if (j0 + j >= a.k || p < 0) continue;
+                const __half2* hv = reinterpret_cast<const __half2*>(&v[j]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __half22float2(hv[i]);
+                    acc[2 * i] += f.x;
+                    acc[2 * i + 1] += f.y;
+                }
+            }
+        }
+        bool finite = true;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) finite = finite && isfinite(acc[i]);
+        uint4 o;
+        __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ob[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        *reinterpret_cast<uint4*>(a.y + (size_t)r * a.H + c) = o;
+        if (a.y_f32) {
+            float4* yf = reinterpret_cast<float4*>(a.y_f32 + (size_t)r * a.H + c);
+            yf[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            yf[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+        // counted per (row, 256-column chunk) that holds a non-finite value
+        if (__any_sync(0xffffffffu, !finite) && lane == 0)
+            status_add(a.status, MOE_STATUS_NONFINITE_OUTPUT, 1);
     }
 }
 
@@ -324,11 +406,11 @@ cudaError_t launch_scatter(const ScatterArgs& a, bool small, int num_sms, cudaSt
     return e;
 }
 
-cudaError_t launch_finalize(const FinalArgs& a, int num_sms, cudaStream_t st) {
-    long blocks = (long)((a.n / 4 + 255) / 256);
-    if (blocks > (long)num_sms * 8) blocks = (long)num_sms * 8;
+cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st) {
+    long blocks = ((long)a.R * (a.H / 256) + 7) / 8;
+    if (blocks > (long)num_sms * 16) blocks = (long)num_sms * 16;
     if (blocks < 1) blocks = 1;
-    return launch_kernel(k_finalize, dim3((unsigned)blocks), dim3(256), 0, st, a);
+    return launch_kernel(k_combine, dim3((unsigned)blocks), dim3(256), 0, st, a);
 }
 
 }  // namespace moe

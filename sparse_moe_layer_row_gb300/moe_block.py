@@ -16,7 +16,8 @@ import torch
 from . import build as _build
 
 MOE_OK = 0
-STATUS_NAMES = ("nonfinite_logits", "bad_expert_id", "bad_offsets", "empty_rows", "wait_timeout")
+STATUS_NAMES = ("nonfinite_logits", "bad_expert_id", "bad_offsets", "empty_rows", "wait_timeout",
+                "nonfinite_output")
 STATUS_WORDS = 8
 
 
