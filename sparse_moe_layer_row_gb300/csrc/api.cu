@@ -184,7 +184,7 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
                 encode_bf16(&p->tm_sg, ws_gate, d.H, d.Is, 0, 64, L2W) &&
                 encode_bf16(&p->tm_su, ws_up, d.H, d.Is, 0, 64, L2W) &&
                 encode_bf16(&p->tm_sd, ws_down, d.Is, d.H, 0, 128, L2W);
-    p->tc_route = d.E <= 256 && d.E % 16 == 0 && d.k <= 16;
+    p->tc_route = d.E <= 256 && d.E % 16 == 0 && d.k <= 16 && d.H <= 6144;
     if (good && p->tc_route)
         good = encode_bf16(&p->tm_wr, w_router, d.H, d.E, 0,
                            (uint32_t)((d.E > 128 && d.E % 32 == 0) ? d.E / 2 : d.E),
@@ -218,7 +218,7 @@ moe_status moe_block_route(const moe_plan* p, const void* x, int32_t R,
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for x");
         RouteTcArgs ta{static_cast<const __nv_bfloat16*>(x),
                        static_cast<const __nv_bfloat16*>(p->wr), logit_bias, block_offsets, R,
-                       p->d.H, p->d.E, p->d.k, nb, at<float>(workspace, L.xnorm),
+                       p->d.H, p->d.E, p->d.k, nb,
                        at<float>(workspace, L.wnorm), at<float>(workspace, L.logits), topk_idx, topk_w,
                        at<uint32_t>(workspace, L.status)};
         cudaError_t e = launch_route_tc(ta, tm_x, p->tm_wr, p->num_sms, st);
@@ -278,14 +278,15 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     const int nt_gu = small ? kSmallN : kLargeN;
     const int nt_dn = small ? kSmallN : kLargeNDown;
 
-    ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, static_cast<const __nv_bfloat16*>(x),
-                   R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
+    ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
+                   small ? 64 : 128,
                    at<int32_t>(workspace, L.prank), at<int32_t>(workspace, L.hist),
                    at<int32_t>(workspace, L.count),
                    at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
                    at<int4>(workspace, L.units_gu), at<int4>(workspace, L.units_dn),
                    at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
-                   at<__nv_bfloat16>(workspace, L.xp), at<int32_t>(workspace, L.inv),
+                   static_cast<const __nv_bfloat16*>(x), at<__nv_bfloat16>(workspace, L.xp),
+                   at<int32_t>(workspace, L.inv),
                    at<uint32_t>(workspace, L.status)};
     GemmMaps gu{}, dn{};
     const auto L2A = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;

@@ -21,7 +21,6 @@ struct Layout {
     size_t status;       // uint32[MOE_STATUS_WORDS]
     size_t route_cnt;    // uint32[max_rows]          router row / row-group tickets
     size_t logits;       // fp32 [max_rows, E]        router logits (before bias)
-    size_t xnorm;        // fp32 [max_rows]           |x_r|_2 (large-batch router)
     size_t wnorm;        // fp32 [E]                  |w_e|_2
     size_t prank;        // int32 [max_pairs]         pair rank within (block, expert)
     size_t hist;         // int32 [max_blocks, E]     pairs per (block, expert) / bases
@@ -32,7 +31,7 @@ struct Layout {
     size_t units_dn;     // int4 [max_units_dn]
     size_t pair_row;     // int32 [max_pairs]
     size_t pair_w;       // fp32 [max_pairs]
-    size_t xp;           // bf16 [max_pairs, H]       rows of x in pair order
+    size_t xp;           // bf16 [max_pairs, H]       rows of x in pair order (large calls)
     size_t h;            // bf16 [max_pairs, 2I]      routed SwiGLU activations, hi | lo
     size_t hs;           // bf16 [max_rows, 2Is]      shared-expert activations, hi | lo
     size_t inv;          // int32 [max_pairs]         staging row of each (row, slot)
@@ -43,10 +42,9 @@ struct Layout {
 
 // Rows of x per unit of grouped-GEMM work (the MMA N extent).  A call with
 // few rows uses kSmallN for both GEMMs; otherwise the gate/up GEMM takes
-// kLargeN rows per unit and the down GEMM, whose B operand is twice as wide
-// (hi and lo parts of h), kLargeNDown.
+// kLargeN rows per unit and the down GEMM kLargeNDown.
 constexpr int kSmallN = 32;
-constexpr int kLargeN = 256;
+constexpr int kLargeN = 128;
 constexpr int kLargeNDown = 128;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -66,7 +64,6 @@ inline Layout make_layout(const moe_dims& d) {
     L.status = take(sizeof(uint32_t) * 64);
     L.route_cnt = take(sizeof(uint32_t) * (size_t)R);
     L.logits = take(sizeof(float) * (size_t)(R * E));
-    L.xnorm = take(sizeof(float) * (size_t)R);
     L.wnorm = take(sizeof(float) * (size_t)E);
     L.prank = take(sizeof(int32_t) * (size_t)P);
     L.hist = take(sizeof(int32_t) * (size_t)d.max_blocks * (size_t)E);
@@ -283,6 +280,32 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Two 32-lane x 16-column loads (e.g. the gate and the up accumulator of the
+// same rows), one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float* va, float* vb) {
+    uint32_t r[16], q[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(ta));
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]),
+          "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]),
+          "=r"(q[13]), "=r"(q[14]), "=r"(q[15])
+        : "r"(tb));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(q[i]);
+    }
 }
 
 // ---- small math ---------------------------------------------------------------

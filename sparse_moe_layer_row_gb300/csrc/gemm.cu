@@ -45,19 +45,31 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s when draining after 
 
 template <int MODE, int NMAX, int STAGES>
 struct GemmCfg {
+    // gate/up: the streaming shape (NMAX == kSmallN) packs 64 gate + 64 up rows
+    // into one 128-row A tile and trades g and u in the epilogue; the large
+    // shape loads 128 gate rows and 128 up rows into two accumulators, so a
+    // TMEM lane holds g and u of the same intermediate index.
+    static constexpr bool kSplitGU = MODE == kGateUp && NMAX != kSmallN;
+    static constexpr int kGURows = kSplitGU ? 128 : 64;  // intermediate rows per gate/up unit
     static constexpr int kBParts = MODE == kDown ? 2 : 1;  // down: hi and lo parts of h
     // rows per B box: 16 for the streaming shape, 64 for the large shape (fewer
     // TMA instructions per stage; NMAX is a multiple of it)
     static constexpr int kBoxRows = NMAX >= 64 ? 64 : 16;
-    static constexpr int kABytes = 128 * 128;
+    static constexpr int kABytes = (kSplitGU ? 2 : 1) * 128 * 128;
     static constexpr int kBBytes = kBParts * NMAX * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kXchgOff = STAGES * kStageBytes;        // gate/up g <-> u exchange
-    static constexpr int kXchgBytes = MODE == kGateUp ? 2 * 64 * 9 * 4 : 16 * 128 * 2;
-    static constexpr int kBarOff = kXchgOff + kXchgBytes;
+    static constexpr int kXchgOff = STAGES * kStageBytes;
+    // gate/up streaming shape: g <-> u exchange; down: the unit's fp16 output tile
+    static constexpr int kXchgBytes =
+        MODE == kGateUp ? (kSplitGU ? 0 : 2 * 64 * 9 * 4) : NMAX * 128 * 2;
+    static constexpr int kRowsOff = kXchgOff + kXchgBytes;             // gate/up: rows of x of a unit
+    static constexpr int kRowsBytes = MODE == kGateUp && NMAX == kSmallN ? NMAX * 4 : 0;
+    static constexpr int kBarOff = kRowsOff + kRowsBytes;
     static constexpr int kSmem = kBarOff + 256 + 1024;
-    static constexpr int kTmemCols = 2 * NMAX < 32 ? 32 : 2 * NMAX;
+    static constexpr int kAccCols = (kSplitGU ? 2 : 1) * NMAX;   // TMEM columns per accumulator
+    static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
     static_assert(NMAX % 16 == 0 && NMAX <= 256 && NMAX % (NMAX >= 64 ? 64 : 16) == 0, "MMA N extent");
 };
 
@@ -70,7 +82,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
        const __grid_constant__ CUtensorMap tmBg, GemmArgs a) {
     using C = GemmCfg<MODE, NMAX, STAGES>;
-    // small gate/up units gather their rows of x (pair_row) with TMA gather4
+    // small routed gate/up units gather their rows of x (pair_row) with TMA
+    // gather4; large ones read the rows from the pair-ordered copy of x (TMA
+    // gather4 moves about 7 bytes per clock per SM: enough for 32-row tiles,
+    // far too few for 256-row ones)
     constexpr bool kGather = MODE == kGateUp && NMAX == kSmallN;
     extern __shared__ uint8_t smem_raw[];
 
@@ -105,8 +120,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     const uint32_t tmem = *tmem_slot;
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmA2);
-        prefetch_tmap(&tmA3); prefetch_tmap(&tmB0); prefetch_tmap(&tmB1);
+        prefetch_tmap(&tmA3); prefetch_tmap(&tmB1);
         if (kGather) prefetch_tmap(&tmBg);
+        else prefetch_tmap(&tmB0);  // pair-ordered x (gate/up) or h (down)
     }
     const int nunits = __ldg(a.n_units);
 
@@ -120,23 +136,29 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
+        int* s_rows = reinterpret_cast<int*>(base + C::kRowsOff);
         for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
             const int4 un = __ldg(a.units + u);
             const int g = un.x, m = un.y, start = un.z, n = un.w;
             // B rows actually loaded: gathered units load ceil(n/4) rows x 4; the
             // others whole boxes of kBoxRows.  Rows of the tile past n only feed
             // output columns that are never read, so they need not be loaded.
+            const bool gathered = kGather && g != a.E;
             const int nb4 = (n + 3) >> 2;
             const int nbox = (n + C::kBoxRows - 1) / C::kBoxRows;
             const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
-            const uint32_t bbytes = kGather ? (uint32_t)nb4 * 512u
-                                            : (uint32_t)(nbox * C::kBoxRows * 128);
+            const uint32_t bbytes = gathered ? (uint32_t)nb4 * 512u
+                                             : (uint32_t)(nbox * C::kBoxRows * 128);
             const uint32_t bytes = (uint32_t)C::kABytes + C::kBParts * bbytes;
             const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
-            // rows of x for a gathered unit (one per lane; rows >= R read as zero)
-            int prow = a.R;
-            if (kGather && lane < n)
-                prow = g == a.E ? start + lane : __ldg(a.pair_row + start + lane);
+            if (gathered) {
+                // the unit's rows of x, padded to a multiple of 4 with R (read as zeros);
+                // copies of the previous unit took their coordinates when issued
+                __syncwarp();
+                for (int i = lane; i < nb4 * 4; i += 32)
+                    s_rows[i] = i < n ? __ldg(a.pair_row + start + i) : a.R;
+                __syncwarp();
+            }
             for (int kb = 0; kb < (K >> 6); ++kb) {
                 const bool w_ok = mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitLimitNs);
                 if (__any_sync(0xffffffffu, !w_ok)) {
@@ -150,35 +172,42 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 if (lane == 0) {
                     mbar_expect_tx(full + stage, bytes);
                     if (MODE == kGateUp) {
-                        const int rows = m * 64;
-                        if (g == a.E) {
-                            tma_load_2d(sA, &tmA2, kc, rows, full + stage);
-                            tma_load_2d(sA + 64 * 128, &tmA3, kc, rows, full + stage);
-                        } else {
-                            tma_load_3d(sA, &tmA0, kc, rows, g, full + stage);
-                            tma_load_3d(sA + 64 * 128, &tmA1, kc, rows, g, full + stage);
+                        // 64-row boxes: gate rows, then up rows (rows past I read as zeros)
+                        constexpr int kHalf = C::kGURows / 64;  // boxes per weight
+                        const int rows = m * C::kGURows;
+#pragma unroll
+                        for (int hb = 0; hb < kHalf; ++hb) {
+                            const uint32_t dg = sA + hb * 64 * 128, du = dg + kHalf * 64 * 128;
+                            if (g == a.E) {
+                                tma_load_2d(dg, &tmA2, kc, rows + 64 * hb, full + stage);
+                                tma_load_2d(du, &tmA3, kc, rows + 64 * hb, full + stage);
+                            } else {
+                                tma_load_3d(dg, &tmA0, kc, rows + 64 * hb, g, full + stage);
+                                tma_load_3d(du, &tmA1, kc, rows + 64 * hb, g, full + stage);
+                            }
                         }
                     } else {
                         if (g == a.E) tma_load_2d(sA, &tmA2, kc, m * 128, full + stage);
                         else tma_load_3d(sA, &tmA0, kc, m * 128, g, full + stage);
                     }
-                }
-                if (kGather) {
-                    for (int t = 0; t < nb4; ++t) {
-                        const int r0 = __shfl_sync(0xffffffffu, prow, (4 * t + 0) & 31);
-                        const int r1 = __shfl_sync(0xffffffffu, prow, (4 * t + 1) & 31);
-                        const int r2 = __shfl_sync(0xffffffffu, prow, (4 * t + 2) & 31);
-                        const int r3 = __shfl_sync(0xffffffffu, prow, (4 * t + 3) & 31);
-                        if (lane == 0) tma_gather4(sB + t * 512, &tmBg, kc, r0, r1, r2, r3, full + stage);
-                    }
-                } else if (lane == 0) {
-                    constexpr int kBoxBytes = C::kBoxRows * 128;
-                    for (int t = 0; t < nbox; ++t)
-                        tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, full + stage);
-                    if (MODE == kDown)  // lo part of h: columns K .. 2K-1 of the same rows
+                    if (!gathered) {
+                        constexpr int kBoxBytes = C::kBoxRows * 128;
                         for (int t = 0; t < nbox; ++t)
-                            tma_load_2d(sB + NMAX * 128 + t * kBoxBytes, mB, K + kc,
-                                        start + t * C::kBoxRows, full + stage);
+                            tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, full + stage);
+                        if (MODE == kDown)  // lo part of h: columns K .. 2K-1 of the same rows
+                            for (int t = 0; t < nbox; ++t)
+                                tma_load_2d(sB + NMAX * 128 + t * kBoxBytes, mB, K + kc,
+                                            start + t * C::kBoxRows, full + stage);
+                    }
+                }
+                if (gathered) {
+                    // the gathers are spread over the lanes (issued after the
+                    // expected byte count is posted by lane 0)
+                    __syncwarp();
+                    for (int t = lane; t < nb4; t += 32) {
+                        const int4 rr = *reinterpret_cast<const int4*>(s_rows + 4 * t);
+                        tma_gather4(sB + t * 512, &tmBg, kc, rr.x, rr.y, rr.z, rr.w, full + stage);
+                    }
                 }
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
@@ -213,7 +242,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(acc * NMAX);
+                const uint32_t d = tmem + (uint32_t)(acc * C::kAccCols);
                 for (int kb = 0; kb < (K >> 6); ++kb) {
                     if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs)) {
                         give_up();
@@ -226,7 +255,11 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = smem_desc_sw128(sA + kk * 32);
-                        tc_mma_bf16(d, ad, smem_desc_sw128(sB + kk * 32), idesc, (kb | kk) != 0);
+                        const uint64_t bd = smem_desc_sw128(sB + kk * 32);
+                        tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
+                        if (C::kSplitGU)  // up rows into the second accumulator
+                            tc_mma_bf16(d + NMAX, smem_desc_sw128(sA + 128 * 128 + kk * 32), bd, idesc,
+                                        (kb | kk) != 0);
                         if (MODE == kDown)
                             tc_mma_bf16(d, ad, smem_desc_sw128(sB + NMAX * 128 + kk * 32), idesc, 1u);
                     }
@@ -253,12 +286,37 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             if (__any_sync(0xffffffffu, !ok)) { give_up(); break; }
             __syncwarp();
             tc_fence_after();
-            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NMAX);
-            for (int c = 0; alive && c < n16; c += 16) {
-                float v[16];
-                __syncwarp();  // tcgen05.ld is warp-collective
-                tmem_ld16(tb + (uint32_t)c, v);
-                if (MODE == kGateUp) {
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
+            bool released = false;  // accumulator handed back to the MMA warp
+            if (C::kSplitGU) {
+                // lane = intermediate index il: g in columns [0, N), u in [N, 2N)
+                __nv_bfloat16* out = g == a.E ? a.hs : a.h;
+                const int ld = g == a.E ? a.Is : a.I;
+                const int il = m * 128 + q * 32 + lane;
+                for (int c = 0; c < n16; c += 16) {
+                    float gv[16], uv[16];
+                    __syncwarp();  // tcgen05.ld is warp-collective
+                    tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(NMAX + c), gv, uv);
+                    if (il < ld) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const int col = c + t;
+                            if (col < n) {
+                                const float hv = silu(gv[t]) * uv[t];
+                                const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+                                const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
+                                __nv_bfloat16* o = out + (size_t)(start + col) * (2 * ld);
+                                o[il] = hi;
+                                o[ld + il] = lo;
+                            }
+                        }
+                    }
+                }
+            } else if (MODE == kGateUp) {
+                for (int c = 0; alive && c < n16; c += 16) {
+                    float v[16];
+                    __syncwarp();  // tcgen05.ld is warp-collective
+                    tmem_ld16(tb + (uint32_t)c, v);
                     // quadrants 0-1: gate rows, 2-3: up rows of intermediate index r
                     const bool is_gate = q < 2;
                     const int r = (q & 1) * 32 + lane;
@@ -302,48 +360,55 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         break;
                     }
                     xphase ^= 1u;
-                } else {
-                    // weighted fp16 outputs of 16 pairs: transpose through shared
-                    // memory so each pair's 128 columns leave as one 256-B segment
-                    __half* xs = reinterpret_cast<__half*>(base + C::kXchgOff);  // [16][128]
-                    const int hl = q * 32 + lane;
+                }
+            } else {
+                // weighted fp16 outputs of the unit's pairs, staged in shared
+                // memory ([pair][128 hidden]) so each pair's 128 columns leave as
+                // one 256-byte segment; the accumulator is released before the
+                // copy-out
+                __half* xs = reinterpret_cast<__half*>(base + C::kXchgOff);
+                const int hl = q * 32 + lane;
+                for (int c = 0; c < n16; c += 16) {
+                    float v[16];
+                    __syncwarp();  // tcgen05.ld is warp-collective
+                    tmem_ld16(tb + (uint32_t)c, v);
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         const int col = c + t;
                         const float w = (g == a.E || col >= n) ? 1.0f : __ldg(a.pair_w + start + col);
-                        xs[t * 128 + hl] = __float2half_rn(w * v[t]);
+                        xs[col * 128 + hl] = __float2half_rn(w * v[t]);
                     }
-                    mbar_arrive(xbar);
-                    if (__any_sync(0xffffffffu,
-                                   !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitLimitNs))) {
-                        give_up();
-                        alive = false;
-                        break;
-                    }
-                    const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue warps
-                    const size_t row0 = (size_t)(g == a.E ? a.shared_row0 : 0) + start + c;
-#pragma unroll
-                    for (int s2 = 0; s2 < 2; ++s2) {
-                        const int idx = et + 128 * s2;      // 16 rows x 16 segments of 16 B
-                        const int t = idx >> 4, seg = idx & 15;
-                        if (c + t < n) {
-                            const uint4 val = *reinterpret_cast<const uint4*>(xs + t * 128 + seg * 8);
-                            *reinterpret_cast<uint4*>(a.ys + (row0 + t) * a.H + m * 128 + seg * 8) = val;
-                        }
-                    }
-                    mbar_arrive(xbar + 1);  // the buffer is reused by the next chunk
-                    if (__any_sync(0xffffffffu,
-                                   !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitLimitNs))) {
-                        give_up();
-                        alive = false;
-                        break;
-                    }
-                    xphase ^= 1u;
                 }
+                tc_fence_before();
+                mbar_arrive(tempty + acc);
+                released = true;
+                mbar_arrive(xbar);
+                if (__any_sync(0xffffffffu, !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitLimitNs))) {
+                    give_up();
+                    alive = false;
+                    break;
+                }
+                const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue warps
+                const size_t row0 = (size_t)(g == a.E ? a.shared_row0 : 0) + start;
+                for (int idx = et; idx < n * 16; idx += 128) {  // n rows x 16 segments of 16 B
+                    const int t = idx >> 4, seg = idx & 15;
+                    const uint4 val = *reinterpret_cast<const uint4*>(xs + t * 128 + seg * 8);
+                    *reinterpret_cast<uint4*>(a.ys + (row0 + t) * a.H + m * 128 + seg * 8) = val;
+                }
+                mbar_arrive(xbar + 1);  // the tile is rewritten by the next unit
+                if (__any_sync(0xffffffffu,
+                               !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitLimitNs))) {
+                    give_up();
+                    alive = false;
+                    break;
+                }
+                xphase ^= 1u;
             }
             if (!alive) break;
-            tc_fence_before();
-            mbar_arrive(tempty + acc);
+            if (!released) {
+                tc_fence_before();
+                mbar_arrive(tempty + acc);
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }

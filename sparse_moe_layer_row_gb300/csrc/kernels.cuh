@@ -29,7 +29,6 @@ struct RouteTcArgs {
     const float* bias;
     const int32_t* off;
     int R, H, E, k, nb;
-    float* xnorm;         // [R]
     float* wnorm;         // [E]
     float* logits;        // [R, E] approximate logits (tensor cores)
     int32_t* topk_idx;
@@ -53,19 +52,20 @@ struct ScatterArgs {
     const int32_t* topk_idx;
     const float* w_renorm;
     const uint32_t* keep;
-    const __nv_bfloat16* x;
     int R, H, E, k, I, Is, nb;
     int nt_gu, nt_dn;   // rows per unit of the gate/up and of the down GEMM
+    int gu_rows;        // intermediate rows per gate/up unit (64 or 128)
     int32_t* prank;       // [R * k] rank of a pair among its block's pairs of its expert, or -1
-    int32_t* hist;        // [nb, E] pairs per (block, expert), then their base offsets
-    int32_t* count;
+    int32_t* hist;        // [nb, E] pairs per (block, expert), then bases within the expert
+    int32_t* count;       // [E] surviving pairs per expert
     int32_t* expert_off;
     int32_t* misc;
     int4* units_gu;
     int4* units_dn;
     int32_t* pair_row;
     float* pair_w;
-    __nv_bfloat16* xp;
+    const __nv_bfloat16* x;
+    __nv_bfloat16* xp;    // [pairs, H] rows of x in pair order (large calls)
     int32_t* inv;         // [R * k] staging row of (row, slot), or -1
     uint32_t* status;
 };

@@ -48,12 +48,13 @@ __device__ __forceinline__ float slack(float z) { return fabsf(z) * 0x1p-20f + 0
 
 }  // namespace
 
+// |w_e|_2 of every router row (times 1.001, which covers the rounding of the sum).
 __global__ void __launch_bounds__(256) k_route_norms(RouteTcArgs a) {
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    for (int v = warp; v < a.R + a.E; v += nwarps) {
-        const __nv_bfloat16* p = v < a.R ? a.x + (size_t)v * a.H : a.wr + (size_t)(v - a.R) * a.H;
+    for (int e = warp; e < a.E; e += nwarps) {
+        const __nv_bfloat16* p = a.wr + (size_t)e * a.H;
         float s = 0.0f;
         for (int c = lane * 8; c < a.H; c += 256) {
             float f[8];
@@ -63,10 +64,7 @@ __global__ void __launch_bounds__(256) k_route_norms(RouteTcArgs a) {
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) {
-            const float nrm = sqrtf(s) * 1.001f;  // covers the rounding of the sum
-            if (v < a.R) a.xnorm[v] = nrm; else a.wnorm[v - a.R] = nrm;
-        }
+        if (lane == 0) a.wnorm[e] = sqrtf(s) * 1.001f;
     }
 }
 
@@ -212,149 +210,291 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     }
 }
 
-// One warp per row: exact logits of the candidates, 16 at a time, in the
-// contract order; then top-k and softmax.
-__global__ void __launch_bounds__(256) k_route_exact(RouteTcArgs a) {
-    constexpr int NG = 16;  // groups of 16 candidates: up to 256 experts
-    const int lane = threadIdx.x & 31;
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    __shared__ int32_t s_cand[8][kCandCap];
-    const int wib = threadIdx.x >> 5;
+// Exact logits of every expert of row r (the fallback for rows whose
+// screening is inconclusive), 16 at a time in the contract order; then top-k
+// and softmax.  One warp.
+__device__ __noinline__ void exact_full_row(const RouteTcArgs& a, int r, const float* brow, int lane) {
+    constexpr int NG = 16;  // groups of 16 experts: up to 256
+    const __nv_bfloat16* xr = a.x + (size_t)r * a.H;
+    uint32_t key[NG], id[NG];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) { key[g] = 0; id[g] = 0xFFFFFFFFu; }
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        if (g * 16 >= a.E) break;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int s = 0; s < a.H; s += 256) {
+            const int col = s + lane * 8;
+            float xf[8];
+            bf16x8(__ldg(reinterpret_cast<const uint4*>(xr + col)), xf);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int e = g * 16 + i;
+                float wf[8];
+                const uint4 wv = e < a.E
+                    ? __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)e * a.H + col))
+                    : make_uint4(0, 0, 0, 0);
+                bf16x8(wv, wf);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i] = __fmaf_rn(xf[j], wf[j], acc[i]);
+            }
+        }
+        // transposed halving over partner distances 16, 8, 4, 2 (16 -> 1
+        // accumulators), then a plain butterfly step at distance 1: the
+        // same pairs as the contract's butterfly.
+#pragma unroll
+        for (int o = 16, h = 8; o >= 2; o >>= 1, h >>= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < h; ++i) {
+                const float send = upper ? acc[i] : acc[i + h];
+                const float keep = upper ? acc[i + h] : acc[i];
+                acc[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+            }
+        }
+        const float dot = __fadd_rn(acc[0], __shfl_xor_sync(0xffffffffu, acc[0], 1));
+        const int e = g * 16 + (lane >> 1);  // lanes 2i and 2i+1 hold expert g*16 + i
+        if ((lane & 1) == 0 && e < a.E) {
+            key[g] = order_key(finish_logit(dot, brow, e));
+            id[g] = (uint32_t)e;
+            valid |= 1u << g;
+        }
+    }
+    uint32_t my_id, my_key;
+    warp_topk<NG>(key, id, valid, a.k, lane, my_id, my_key);
+    write_topk(a.topk_idx + (size_t)r * a.k, a.topk_w + (size_t)r * a.k, a.k, lane, my_id, my_key);
+}
+
+// A CTA takes tiles of kExRows rows.
+//   1. warp w screens row w of the tile: converts x_r to fp32 in shared
+//      memory, forms |x_r|, finds the k-th approximate logit T and lists the
+//      candidates;
+//   2. the tile's (row, candidate) pairs are shared out over the 8 warps, two
+//      per pass: each lane accumulates its elements of both dot products in
+//      the contract order, one halving step at partner distance 16 leaves
+//      candidate 0 in lanes 0-15 and candidate 1 in lanes 16-31, and the
+//      plain butterfly at 8, 4, 2, 1 finishes both;
+//   3. warp w takes top-k and softmax of row w over its candidates.
+// x tile layout: [row][stripe][half][lane] float4, so that each lane's eight
+// values of a stripe are two conflict-free 16-byte reads.
+constexpr int kExRows = 8;
+constexpr int kExMaxH = 6144;  // x tile in shared memory: kExRows * H fp32
+
+__global__ void __launch_bounds__(256, 2) k_route_exact(RouteTcArgs a) {
+    extern __shared__ __align__(16) uint8_t ex_smem[];
+    float4* s_x = reinterpret_cast<float4*>(ex_smem);  // [kExRows][H/256][2][32]
+    __shared__ int32_t s_ce[kExRows * kCandCap];  // candidate expert of each slot
+    __shared__ float s_cz[kExRows * kCandCap];    // its exact logit (bias added)
+    __shared__ int s_cnt[kExRows];                // candidates of the row; -1: all experts
+    __shared__ int s_blk[kExRows];                // block of the row (bias row)
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nstripes = a.H >> 8;
     const float G = (float)a.H * 0x1p-21f;
-    // max_e |w_e| (every warp of the CTA computes the same value)
+    // max_e |w_e| (every warp computes the same value)
     float wmax = 0.0f;
     for (int e = lane; e < a.E; e += 32) wmax = fmaxf(wmax, __ldg(a.wnorm + e));
     wmax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(wmax)));
-    for (int r = warp; r < a.R; r += nwarps) {
-        const float* brow = a.bias ? a.bias + (size_t)find_block(a.off, a.nb, r) * a.E : nullptr;
-        const float gx = G * __ldg(a.xnorm + r);
-        // screening on the approximate logits: the k-th value and the candidates
-        uint32_t akey[8], aid[8];
-        float az[8];
-        uint32_t avalid = 0, nonfinite = 0;
+    const int ntiles = (a.R + kExRows - 1) / kExRows;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int r = tile * kExRows + w;
+        // ------------------------------------------------ 1. screening of row r
+        if (r < a.R) {
+            const __nv_bfloat16* xr = a.x + (size_t)r * a.H;
+            float4* sx = s_x + (size_t)w * nstripes * 64;
+            float ss = 0.0f;
+            for (int st = 0; st < nstripes; ++st) {
+                float f[8];
+                bf16x8(__ldg(reinterpret_cast<const uint4*>(xr + st * 256 + lane * 8)), f);
+                sx[st * 64 + lane] = make_float4(f[0], f[1], f[2], f[3]);
+                sx[st * 64 + 32 + lane] = make_float4(f[4], f[5], f[6], f[7]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i;
-            akey[i] = 0;
-            aid[i] = (uint32_t)e;
-            az[i] = 0.0f;
-            if (e < a.E) {
-                float z = __ldg(a.logits + (size_t)r * a.E + e);
-                if (brow) z = __fadd_rn(z, __ldg(brow + e));
-                nonfinite += !isfinite(z);
-                az[i] = z;
-                akey[i] = order_key(z);
-                avalid |= 1u << i;
+                for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
             }
-        }
-        nonfinite = __reduce_add_sync(0xffffffffu, nonfinite);
-        if (lane == 0) status_add(a.status, MOE_STATUS_NONFINITE_LOGITS, nonfinite);
-        uint32_t kid, kkey;
-        warp_topk<8>(akey, aid, avalid, a.k, lane, kid, kkey);
-        const float T = key_value(__shfl_sync(0xffffffffu, kkey, a.k - 1));
-        const float thr = T - (gx * wmax + slack(T));
-        int cnt = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i;
-            const bool c = ((avalid >> i) & 1u) && az[i] + (gx * __ldg(a.wnorm + (e < a.E ? e : 0)) + slack(az[i])) >= thr;
-            const uint32_t m = __ballot_sync(0xffffffffu, c);
-            const int pos = cnt + __popc(m & ((1u << lane) - 1u));
-            if (c && pos < kCandCap) s_cand[wib][pos] = e;
-            cnt += __popc(m);
-        }
-        __syncwarp();
-        const bool full_row = !(T > -INFINITY) || cnt > kCandCap || cnt < a.k;
-        const int n = full_row ? a.E : cnt;
-        const int32_t* cl = s_cand[wib];
-        const __nv_bfloat16* xr = a.x + (size_t)r * a.H;
-        uint32_t key[NG], id[NG];
-        uint32_t valid = 0;
+            for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float gx = G * (sqrtf(ss) * 1.001f);  // 1.001 covers the rounding of the sum
+            const int blk = a.bias ? find_block(a.off, a.nb, r) : 0;
+            const float* brow = a.bias ? a.bias + (size_t)blk * a.E : nullptr;
+            uint32_t sk[8];
+            float az[8];
+            uint32_t nonfinite = 0;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) { key[g] = 0; id[g] = 0xFFFFFFFFu; }
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-            if (g * 16 >= n) break;
-            int ex[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int ci = g * 16 + i;
-                ex[i] = ci < n ? (full_row ? ci : cl[ci]) : -1;
-            }
-            float acc[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-            for (int s = 0; s < a.H; s += 256) {
-                const int col = s + lane * 8;
-                float xf[8];
-                bf16x8(__ldg(reinterpret_cast<const uint4*>(xr + col)), xf);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float wf[8];
-                    const uint4 wv = ex[i] >= 0
-                        ? __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)ex[i] * a.H + col))
-                        : make_uint4(0, 0, 0, 0);
-                    bf16x8(wv, wf);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[i] = __fmaf_rn(xf[j], wf[j], acc[i]);
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                sk[i] = 0;
+                az[i] = 0.0f;
+                if (e < a.E) {
+                    float z = __ldg(a.logits + (size_t)r * a.E + e);
+                    if (brow) z = __fadd_rn(z, __ldg(brow + e));
+                    nonfinite += !isfinite(z);
+                    az[i] = z;
+                    sk[i] = order_key(z);
                 }
             }
-            // transposed halving over partner distances 16, 8, 4, 2 (16 -> 1
-            // accumulators), then a plain butterfly step at distance 1: the
-            // same pairs as the contract's butterfly.
+            nonfinite = __reduce_add_sync(0xffffffffu, nonfinite);
+            if (lane == 0) status_add(a.status, MOE_STATUS_NONFINITE_LOGITS, nonfinite);
+            // T = the k-th largest approximate logit: each lane sorts its eight
+            // keys (descending), then k rounds pop the warp's largest head
 #pragma unroll
-            for (int o = 16, h = 8; o >= 2; o >>= 1, h >>= 1) {
-                const bool upper = (lane & o) != 0;
+            for (int rnd = 0; rnd < 8; ++rnd)
 #pragma unroll
-                for (int i = 0; i < h; ++i) {
-                    const float send = upper ? acc[i] : acc[i + h];
-                    const float keep = upper ? acc[i + h] : acc[i];
-                    acc[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+                for (int i = rnd & 1; i + 1 < 8; i += 2) {
+                    const uint32_t hi = max(sk[i], sk[i + 1]), lo = min(sk[i], sk[i + 1]);
+                    sk[i] = hi;
+                    sk[i + 1] = lo;
+                }
+            uint32_t tkey = 0;
+            for (int j = 0; j < a.k; ++j) {
+                tkey = __reduce_max_sync(0xffffffffu, sk[0]);
+                const uint32_t win = __reduce_min_sync(0xffffffffu, sk[0] == tkey ? (uint32_t)lane : 32u);
+                if ((uint32_t)lane == win) {
+#pragma unroll
+                    for (int i = 0; i < 7; ++i) sk[i] = sk[i + 1];
+                    sk[7] = 0;
                 }
             }
-            const float other = __shfl_xor_sync(0xffffffffu, acc[0], 1);
-            const float dot = __fadd_rn(acc[0], other);
-            // lane 2i (and 2i+1) now hold candidate g*16 + i
-            const int ci = lane >> 1;
-            int e = -1;
+            const float T = key_value(tkey);
+            const float thr = T - (gx * wmax + slack(T));
+            int cnt = 0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (i == ci) e = ex[i];
-            if ((lane & 1) == 0 && e >= 0) {
-                key[g] = order_key(finish_logit(dot, brow, e));
-                id[g] = (uint32_t)e;
-                valid |= 1u << g;
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                const bool c = e < a.E && az[i] + (gx * __ldg(a.wnorm + (e < a.E ? e : 0)) + slack(az[i])) >= thr;
+                const uint32_t m = __ballot_sync(0xffffffffu, c);
+                const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+                if (c && pos < kCandCap) s_ce[w * kCandCap + pos] = e;
+                cnt += __popc(m);
+            }
+            const bool full_row = !(T > -INFINITY) || cnt > kCandCap || cnt < a.k;
+            if (lane == 0) {
+                s_cnt[w] = full_row ? -1 : cnt;
+                s_blk[w] = blk;
+            }
+        } else if (lane == 0) {
+            s_cnt[w] = 0;
+        }
+        __syncthreads();
+        // ------------------------------------- 2. exact logits of the candidates
+        {
+            const int cr = lane < kExRows ? max(s_cnt[lane], 0) : 0;
+            int incl = cr;
+#pragma unroll
+            for (int o = 1; o < kExRows; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const int total = __shfl_sync(0xffffffffu, incl, kExRows - 1);
+            const int excl = incl - cr;  // lane i < kExRows: first slot of row i
+            for (int t0 = 2 * w; t0 < total; t0 += 2 * kExRows) {
+                int row[2], e[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = t0 + h;
+                    const uint32_t m = __ballot_sync(0xffffffffu, lane < kExRows && excl <= t);
+                    const int rr = __popc(m) - 1;
+                    const int first = __shfl_sync(0xffffffffu, excl, rr & 31);
+                    row[h] = rr;
+                    e[h] = t < total ? s_ce[rr * kCandCap + (t - first)] : -1;
+                }
+                float acc0 = 0.0f, acc1 = 0.0f;
+                const float4* x0 = s_x + (size_t)row[0] * nstripes * 64 + lane;
+                const float4* x1 = s_x + (size_t)row[1] * nstripes * 64 + lane;
+                for (int s0 = 0; s0 < nstripes; s0 += 8) {
+                    uint4 w0[8], w1[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int col = (s0 + i) * 256 + lane * 8;
+                        const bool in = s0 + i < nstripes;
+                        w0[i] = in ? __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)e[0] * a.H + col))
+                                   : make_uint4(0, 0, 0, 0);
+                        w1[i] = (in && e[1] >= 0)
+                                    ? __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)e[1] * a.H + col))
+                                    : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (s0 + i >= nstripes) break;
+                        const int st = s0 + i;
+                        float wf[8];
+                        float4 p = x0[st * 64], q = x0[st * 64 + 32];
+                        bf16x8(w0[i], wf);
+                        acc0 = __fmaf_rn(p.x, wf[0], acc0); acc0 = __fmaf_rn(p.y, wf[1], acc0);
+                        acc0 = __fmaf_rn(p.z, wf[2], acc0); acc0 = __fmaf_rn(p.w, wf[3], acc0);
+                        acc0 = __fmaf_rn(q.x, wf[4], acc0); acc0 = __fmaf_rn(q.y, wf[5], acc0);
+                        acc0 = __fmaf_rn(q.z, wf[6], acc0); acc0 = __fmaf_rn(q.w, wf[7], acc0);
+                        p = x1[st * 64];
+                        q = x1[st * 64 + 32];
+                        bf16x8(w1[i], wf);
+                        acc1 = __fmaf_rn(p.x, wf[0], acc1); acc1 = __fmaf_rn(p.y, wf[1], acc1);
+                        acc1 = __fmaf_rn(p.z, wf[2], acc1); acc1 = __fmaf_rn(p.w, wf[3], acc1);
+                        acc1 = __fmaf_rn(q.x, wf[4], acc1); acc1 = __fmaf_rn(q.y, wf[5], acc1);
+                        acc1 = __fmaf_rn(q.z, wf[6], acc1); acc1 = __fmaf_rn(q.w, wf[7], acc1);
+                    }
+                }
+                // halving at distance 16: lanes 0-15 keep candidate 0, 16-31 candidate 1
+                const bool upper = (lane & 16) != 0;
+                float v = __fadd_rn(upper ? acc1 : acc0,
+                                    __shfl_xor_sync(0xffffffffu, upper ? acc0 : acc1, 16));
+#pragma unroll
+                for (int o = 8; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+                const int h = lane >> 4;
+                if ((lane & 15) == 0 && e[h] >= 0) {
+                    const float* brow = a.bias ? a.bias + (size_t)s_blk[row[h]] * a.E : nullptr;
+                    s_cz[t0 + h] = finish_logit(v, brow, e[h]);
+                }
             }
         }
-        uint32_t my_id, my_key;
-        warp_topk<NG>(key, id, valid, a.k, lane, my_id, my_key);
-        write_topk(a.topk_idx + (size_t)r * a.k, a.topk_w + (size_t)r * a.k, a.k, lane, my_id,
-                   my_key);
-        __syncwarp();  // s_cand is rewritten by the next row
+        __syncthreads();
+        // ------------------------------------------------- 3. top-k of row r
+        if (r < a.R) {
+            const int c = s_cnt[w];
+            const float* brow = a.bias ? a.bias + (size_t)s_blk[w] * a.E : nullptr;
+            if (c >= 0) {
+                // slots of row w start after the candidates of rows 0..w-1
+                int first = 0;
+                for (int i = 0; i < w; ++i) first += max(s_cnt[i], 0);
+                uint32_t key[1] = {0u}, id[1] = {0xFFFFFFFFu};
+                if (lane < c) {
+                    key[0] = order_key(s_cz[first + lane]);
+                    id[0] = (uint32_t)s_ce[w * kCandCap + lane];
+                }
+                uint32_t my_id, my_key;
+                warp_topk<1>(key, id, lane < c ? 1u : 0u, a.k, lane, my_id, my_key);
+                write_topk(a.topk_idx + (size_t)r * a.k, a.topk_w + (size_t)r * a.k, a.k, lane,
+                           my_id, my_key);
+            } else {
+                exact_full_row(a, r, brow, lane);
+            }
+        }
+        __syncthreads();  // the tile's shared memory is rewritten by the next tile
     }
 }
 
 cudaError_t route_tc_set_attributes() {
-    return cudaFuncSetAttribute(k_route_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TcCfg::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_route_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TcCfg::kSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_route_exact, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kExRows * kExMaxH * 4);
 }
 
 cudaError_t launch_route_tc(const RouteTcArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                             int num_sms, cudaStream_t st) {
-    long nb = (long)(a.R + a.E + 7) / 8;
-    if (nb > (long)num_sms * 8) nb = (long)num_sms * 8;
-    cudaError_t e = launch_kernel(k_route_norms, dim3((unsigned)(nb < 1 ? 1 : nb)), dim3(256), 0, st, a);
+    cudaError_t e = launch_kernel(k_route_norms, dim3((unsigned)((a.E + 7) / 8)), dim3(256), 0, st, a);
     const int ntiles = (a.R + 127) / 128;
     const int nsplit = (a.E > 128 && a.E % 32 == 0) ? 2 : 1;
     const int nunits = ntiles * nsplit;
     const int grid = nunits < num_sms ? nunits : num_sms;
     if (e == cudaSuccess)
         e = launch_kernel(k_route_tc, dim3(grid), dim3(192), TcCfg::kSmem, st, tm_x, tm_w, a, nsplit);
-    long eb = (long)(a.R + 7) / 8;
-    if (eb > (long)num_sms * 16) eb = (long)num_sms * 16;
+    const long ntiles_ex = (a.R + kExRows - 1) / kExRows;
+    const long eb = ntiles_ex < (long)num_sms * 2 ? ntiles_ex : (long)num_sms * 2;
     if (e == cudaSuccess)
-        e = launch_kernel(k_route_exact, dim3((unsigned)(eb < 1 ? 1 : eb)), dim3(256), 0, st, a);
+        e = launch_kernel(k_route_exact, dim3((unsigned)eb), dim3(256),
+                          (size_t)kExRows * a.H * 4, st, a);
     return e;
 }
 

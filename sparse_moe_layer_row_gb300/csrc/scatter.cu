@@ -7,10 +7,10 @@
 // surviving pair appear in the work lists.
 //
 // Pair order inside an expert is (row ascending, slot ascending), so the work
-// list, the staging copy of x and the GEMM tiles are the same on every run.
-// Nothing here waits on another CTA: the per-expert counts are combined by the
-// last CTA to finish (ticket counter), which then writes the offsets and the
-// unit lists for the GEMM launches that follow on the same stream.
+// lists and the GEMM tiles are the same on every run.  Nothing here waits on
+// another CTA: the per-expert totals are combined by the last CTA to finish
+// (ticket counter), which then writes the offsets and the unit lists for the
+// GEMM launches that follow on the same stream.
 #include "kernels.cuh"
 
 namespace moe {
@@ -60,11 +60,13 @@ __device__ void write_units(int4* out, int base, int g, int start, int n, int nt
 //   k_scatter_hist   per block: pairs per expert (hist[b][e]) and each pair's
 //                    rank among the block's pairs of its expert, rows in order
 //                    (rows are taken 32 at a time, so any block size works)
-//   k_scatter_scan   one CTA: base[b][e] = offset of expert e + pairs of e in
-//                    earlier blocks (in place over hist), expert offsets, the
-//                    unit lists of both GEMMs
-//   k_scatter_place  per block: pair lists and the staging copy of x rows,
-//                    and a slice of the zeroed combine accumulator
+//   k_scatter_scan   one warp per expert: base[b][e] = pairs of e in earlier
+//                    blocks (in place over hist) and the expert's total; the
+//                    last CTA to finish forms the expert offsets and the unit
+//                    lists of both GEMMs
+//   k_scatter_place  per block: each surviving pair's position, the pair
+//                    lists (row, weight), the inverse map (row, slot) -> pair
+//                    and the copy of x in pair order read by the gate/up GEMM
 // A row that names the same expert twice contributes its first slot only
 // (later duplicates are counted as bad ids).
 constexpr int kHistRows = 32;
@@ -80,6 +82,7 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_hist(ScatterArgs a) {
     if (!(0 <= r0 && r0 <= r1 && r1 <= a.R)) r1 = r0 = 0;  // counted by the coreset call
     for (int e = tid; e < E; e += blockDim.x) s_run[e] = 0;
     if (tid == 0) s_dup = 0;
+    if (b == 0 && tid == 0) a.misc[0] = 0;  // ticket of k_scatter_scan (next launch)
     for (int c0 = r0; c0 < r1; c0 += kHistRows) {
         const int nr = min(kHistRows, r1 - c0);
         __syncthreads();
@@ -114,30 +117,49 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_hist(ScatterArgs a) {
     if (tid == 0) status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)s_dup);
 }
 
-constexpr int kScanThreads = 1024;
+constexpr int kScanThreads = 256;
 
 constexpr int kDownGroup = 32;
-
-// Units of one group in weight-tile-major order (all row chunks of tile 0, then tile 1 ...).
-__device__ void write_units_mmajor(int4* out, int base, int g, int start, int n, int nt, int mtiles) {
-    int u = base;
-    for (int m = 0; m < mtiles; ++m)
-        for (int c0 = 0; c0 < n; c0 += nt) out[u++] = make_int4(g, m, start + c0, min(nt, n - c0));
-}
 
 __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     __shared__ int warp_sums[32];
     __shared__ int s_tot[kMaxExperts];
     __shared__ int s_cd[kMaxExperts + 1];
-    const int tid = threadIdx.x, E = a.E, nb = a.nb;
-    // per expert: its total over blocks (thread e, and e + 1024 ...)
-    for (int e = tid; e < E; e += blockDim.x) {
-        int t = 0;
-        for (int b = 0; b < nb; ++b) t += a.hist[(size_t)b * E + e];
-        s_tot[e] = t;
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, E = a.E, nb = a.nb;
+    // ---- one warp per expert: exclusive scan of its column of hist over blocks
+    {
+        const int e = blockIdx.x * (kScanThreads / 32) + (tid >> 5);
+        if (e < E) {
+            int run = 0;
+            for (int b0 = 0; b0 < nb; b0 += 32) {
+                const int b = b0 + lane;
+                const int h = b < nb ? a.hist[(size_t)b * E + e] : 0;
+                int incl = h;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                if (b < nb) a.hist[(size_t)b * E + e] = run + incl - h;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) a.count[e] = run;
+        }
     }
     __syncthreads();
-    const int mt_gu = a.I / 64, mt_gs = a.Is / 64, mt_dn = a.H / 128;
+    if (tid == 0) {
+        __threadfence();
+        s_last = atomicAdd(a.misc, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // ---- last CTA: expert offsets and the unit lists
+    for (int f = tid; f < E; f += blockDim.x) s_tot[f] = __ldcg(a.count + f);
+    __syncthreads();
+    const int mt_gu = (a.I + a.gu_rows - 1) / a.gu_rows, mt_gs = (a.Is + a.gu_rows - 1) / a.gu_rows;
+    const int mt_dn = a.H / 128;
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
     int sum = 0, ch_gu = 0, ch_dn = 0;
@@ -150,16 +172,22 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     int p = block_excl_scan_i32(sum, warp_sums, &tot_pairs);
     int cg = block_excl_scan_i32(ch_gu, warp_sums, &tot_gu);
     int cd = block_excl_scan_i32(ch_dn, warp_sums, &tot_dn);
-    const int base_gu = (a.R + a.nt_gu - 1) / a.nt_gu * mt_gs;
-    const int base_dn = (a.R + a.nt_dn - 1) / a.nt_dn * mt_dn;
-    if (tid == 0) {
-        write_units(a.units_gu, 0, E, 0, a.R, a.nt_gu, mt_gs);
-        write_units_mmajor(a.units_dn, 0, E, 0, a.R, a.nt_dn, mt_dn);
+    const int sch_gu = (a.R + a.nt_gu - 1) / a.nt_gu, sch_dn = (a.R + a.nt_dn - 1) / a.nt_dn;
+    const int base_gu = sch_gu * mt_gs;
+    const int base_dn = sch_dn * mt_dn;
+    // shared-expert units (group E, all rows): gate/up chunk-major, down tile-major
+    for (int u = tid; u < base_gu; u += blockDim.x) {
+        const int c = u / mt_gs, m = u - c * mt_gs;
+        a.units_gu[u] = make_int4(E, m, c * a.nt_gu, min(a.nt_gu, a.R - c * a.nt_gu));
+    }
+    for (int u = tid; u < base_dn; u += blockDim.x) {
+        const int m = u / sch_dn, c = u - m * sch_dn;
+        a.units_dn[u] = make_int4(E, m, c * a.nt_dn, min(a.nt_dn, a.R - c * a.nt_dn));
     }
     // down units: expert groups of kDownGroup, each group ordered weight-tile
-    // major, so the CTAs running at one time add into one 128-column slab of
-    // the accumulator for the group's rows (it stays in L2) and each group's
-    // activations are reused from L2 across its weight tiles.
+    // major, so the CTAs running at one time write one 128-column slab for
+    // the group's pairs and each group's activations are reused from L2
+    // across its weight tiles.
     {  // chunk prefix of each expert
         int q = cd;
         for (int f = e0; f < e1; ++f) {
@@ -172,7 +200,6 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     for (int f = e0; f < e1; ++f) {
         const int n = s_tot[f];
         a.expert_off[f] = p;
-        a.count[f] = n;
         write_units(a.units_gu, base_gu + cg * mt_gu, f, p, n, a.nt_gu, mt_gu);
         {
             const int g0 = f / kDownGroup * kDownGroup, g1 = min(E, g0 + kDownGroup);
@@ -182,13 +209,6 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
                 for (int c0 = 0; c0 < n; c0 += a.nt_dn)
                     a.units_dn[u++] = make_int4(f, m, p + c0, min(a.nt_dn, n - c0));
             }
-        }
-        // base[b][f] (in place over hist): offset of f + pairs of f in blocks before b
-        int run = p;
-        for (int b = 0; b < nb; ++b) {
-            const int h = a.hist[(size_t)b * E + f];
-            a.hist[(size_t)b * E + f] = run;
-            run += h;
         }
         p += n;
         cg += (n + a.nt_gu - 1) / a.nt_gu;
@@ -201,47 +221,55 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     }
 }
 
-// grid: nb * kPlaceSplit CTAs; CTA (b, part) takes a strided share of block b's pairs.
-constexpr int kPlaceSplit = 4;
-
+// One CTA per block: a thread per (row, slot) of the block places the pair;
+// then one warp per placed pair copies its row of x into pair order.
 __global__ void __launch_bounds__(kScatThreads) k_scatter_place(ScatterArgs a) {
-    const int b = blockIdx.x / kPlaceSplit, part = blockIdx.x % kPlaceSplit;
+    __shared__ int2 s_pr[kScatThreads];  // (pair position, row) of this pass
+    const int b = blockIdx.x;
     const int E = a.E, k = a.k;
     int r0 = a.off[b], r1 = a.off[b + 1];
     if (!(0 <= r0 && r0 <= r1 && r1 <= a.R)) r1 = r0 = 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int hv = a.H / 8;  // uint4 per row of x
-    // one warp per pair: lists, then its row of x (uint4 per lane, 8 in flight)
-    for (int p = r0 * k + part * nw + warp; p < r1 * k; p += nw * kPlaceSplit) {
-        const int rk = a.prank[p];
-        if (rk < 0) {
-            if (lane == 0) a.inv[p] = -1;
-            continue;
+    for (int p0 = r0 * k; p0 < r1 * k; p0 += blockDim.x) {
+        const int p = p0 + threadIdx.x;
+        int2 pr = make_int2(-1, 0);
+        if (p < r1 * k) {
+            const int rk = a.prank[p];
+            if (rk < 0) {
+                a.inv[p] = -1;
+            } else {
+                const int e = a.topk_idx[p];
+                const int pos = a.expert_off[e] + a.hist[(size_t)b * E + e] + rk;
+                a.pair_row[pos] = p / k;
+                a.pair_w[pos] = a.w_renorm[p];
+                a.inv[p] = pos;
+                pr = make_int2(pos, p / k);
+            }
         }
-        const int e = a.topk_idx[p];
-        const int pos = a.hist[(size_t)b * E + e] + rk;
-        const int r = p / k;
-        if (lane == 0) {
-            a.pair_row[pos] = r;
-            a.pair_w[pos] = a.w_renorm[p];
-            a.inv[p] = pos;
-        }
-        const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)r * a.H);
-        uint4* dst = reinterpret_cast<uint4*>(a.xp + (size_t)pos * a.H);
-        for (int v = lane; v < hv; v += 32 * 8) {
-            uint4 t[8];
+        s_pr[threadIdx.x] = pr;
+        __syncthreads();
+        const int np = min((int)blockDim.x, r1 * k - p0);
+        for (int i = warp; i < np; i += nw) {
+            const int2 q = s_pr[i];
+            if (q.x < 0) continue;
+            const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)q.y * a.H);
+            uint4* dst = reinterpret_cast<uint4*>(a.xp + (size_t)q.x * a.H);
+            for (int v = lane; v < hv; v += 32 * 8) {
+                uint4 t[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (v + 32 * i < hv) t[i] = __ldg(src + v + 32 * i);
+                for (int j = 0; j < 8; ++j)
+                    if (v + 32 * j < hv) t[j] = __ldg(src + v + 32 * j);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (v + 32 * i < hv) dst[v + 32 * i] = t[i];
+                for (int j = 0; j < 8; ++j)
+                    if (v + 32 * j < hv) dst[v + 32 * j] = t[j];
+            }
         }
+        __syncthreads();
     }
 }
 
-// Small batches (R <= kSmallRows): the whole bookkeeping in one CTA, no
-// staging copy of x (the gate/up GEMM gathers the rows with TMA gather4).
+// Small batches (R <= kSmallRows): the whole bookkeeping in one CTA.
 // Same outputs as the three-kernel path: pair lists in row order per expert,
 // expert offsets, unit lists, a zeroed accumulator.  A row that names the same
 // expert twice contributes its first slot only (later duplicates are counted
@@ -295,7 +323,8 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
     int tot_pairs, tot_ch;
     int pp = block_excl_scan_i32(sum, warp_sums, &tot_pairs);
     int cc = block_excl_scan_i32(ch, warp_sums, &tot_ch);
-    const int mt_gu = a.I / 64, mt_gs = a.Is / 64, mt_dn = a.H / 128;
+    const int mt_gu = (a.I + a.gu_rows - 1) / a.gu_rows, mt_gs = (a.Is + a.gu_rows - 1) / a.gu_rows;
+    const int mt_dn = a.H / 128;
     const int s_chunks = (R + a.nt_gu - 1) / a.nt_gu;   // nt_gu == nt_dn here
     const int base_gu = s_chunks * mt_gs, base_dn = s_chunks * mt_dn;
     if (tid == 0) {
@@ -400,9 +429,10 @@ cudaError_t launch_scatter(const ScatterArgs& a, bool small, int num_sms, cudaSt
     (void)num_sms;
     if (small) return launch_kernel(k_scatter_small, dim3(1), dim3(kSmallThreads), 0, st, a);
     cudaError_t e = launch_kernel(k_scatter_hist, dim3(a.nb), dim3(kScatThreads), 0, st, a);
-    if (e == cudaSuccess) e = launch_kernel(k_scatter_scan, dim3(1), dim3(kScanThreads), 0, st, a);
+    const int scan_ctas = (a.E + kScanThreads / 32 - 1) / (kScanThreads / 32);
     if (e == cudaSuccess)
-        e = launch_kernel(k_scatter_place, dim3(a.nb * kPlaceSplit), dim3(kScatThreads), 0, st, a);
+        e = launch_kernel(k_scatter_scan, dim3(scan_ctas), dim3(kScanThreads), 0, st, a);
+    if (e == cudaSuccess) e = launch_kernel(k_scatter_place, dim3(a.nb), dim3(kScatThreads), 0, st, a);
     return e;
 }
 
