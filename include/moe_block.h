@@ -143,9 +143,10 @@ moe_status moe_block_coreset(const moe_plan* plan, int32_t R, const int32_t* blo
  * (Model card, intro: top-8 experts plus a shared expert.)
  *   y[r] = S(x[r]) + sum over slots j of row r whose expert is kept for r's
  *          block of w_renorm[r, j] * E_{topk_idx[r, j]}(x[r])
- * with S the shared expert.  bf16 MMA with fp32 accumulation; the SwiGLU
- * activations enter the down projection as two bf16 parts (hi + lo, about 16
- * significant bits); each expert's weighted output and the shared output are
+ * with S the shared expert.  bf16 MMA with fp32 accumulation; a routed pair's
+ * SwiGLU activations enter the down projection in bf16, the shared expert's
+ * as two bf16 parts (hi + lo, about 16 significant bits: its output enters
+ * every row with weight 1); each expert's weighted output and the shared output are
  * staged in fp16 (|value| < 65504) and summed in fp32 per row in a fixed order
  * (shared expert, then the row's slots in rank order), so y is reproducible.
  *   y      [R, H] bf16 out

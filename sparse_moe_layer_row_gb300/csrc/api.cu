@@ -184,7 +184,7 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
                 encode_bf16(&p->tm_sg, ws_gate, d.H, d.Is, 0, 64, L2W) &&
                 encode_bf16(&p->tm_su, ws_up, d.H, d.Is, 0, 64, L2W) &&
                 encode_bf16(&p->tm_sd, ws_down, d.Is, d.H, 0, 128, L2W);
-    p->tc_route = d.E <= 256 && d.E % 16 == 0 && d.k <= 16 && d.H <= 6144;
+    p->tc_route = d.E <= 256 && d.E % 16 == 0 && d.k <= 16 && d.H <= 8192;
     if (good && p->tc_route)
         good = encode_bf16(&p->tm_wr, w_router, d.H, d.E, 0,
                            (uint32_t)((d.E > 128 && d.E % 32 == 0) ? d.E / 2 : d.E),
@@ -296,7 +296,7 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     bool good = encode_bf16(&gu.b0, at<void>(workspace, L.xp), d.H, (uint64_t)L.max_pairs, 0, box, L2A) &&
                 encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
                 encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
-                encode_bf16(&dn.b0, at<void>(workspace, L.h), 2 * (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
+                encode_bf16(&dn.b0, at<void>(workspace, L.h), (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
                             box, L2A) &&
                 encode_bf16(&dn.b1, at<void>(workspace, L.hs), 2 * (uint64_t)d.Is,
                             (uint64_t)d.max_rows, 0, box, L2A);

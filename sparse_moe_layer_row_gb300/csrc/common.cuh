@@ -32,7 +32,7 @@ struct Layout {
     size_t pair_row;     // int32 [max_pairs]
     size_t pair_w;       // fp32 [max_pairs]
     size_t xp;           // bf16 [max_pairs, H]       rows of x in pair order (large calls)
-    size_t h;            // bf16 [max_pairs, 2I]      routed SwiGLU activations, hi | lo
+    size_t h;            // bf16 [max_pairs, I]       routed SwiGLU activations
     size_t hs;           // bf16 [max_rows, 2Is]      shared-expert activations, hi | lo
     size_t inv;          // int32 [max_pairs]         staging row of each (row, slot)
     size_t ys;           // fp16 [max_pairs + max_rows, H] staged per-pair and shared outputs
@@ -75,7 +75,7 @@ inline Layout make_layout(const moe_dims& d) {
     L.pair_row = take(sizeof(int32_t) * (size_t)P);
     L.pair_w = take(sizeof(float) * (size_t)P);
     L.xp = take(2 * (size_t)(P * H));
-    L.h = take(2 * (size_t)(P * 2 * d.I));
+    L.h = take(2 * (size_t)(P * d.I));
     L.hs = take(2 * (size_t)(R * 2 * d.Is));
     L.inv = take(sizeof(int32_t) * (size_t)P);
     L.ys = take(2 * (size_t)(P + R) * (size_t)H);

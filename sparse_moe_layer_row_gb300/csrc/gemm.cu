@@ -16,15 +16,20 @@
 //            intermediate indices (two 64-row TMA boxes per stage).  TMEM lane
 //            quadrants 0-1 hold g, 2-3 hold u; the epilogue warps trade half
 //            of each 16-column chunk through shared memory and each computes
-//            h = silu(g) * u for its half, stored as two bf16 parts
-//            hi = bf16(h), lo = bf16(h - hi) (about 16 significant bits; one
-//            bf16 alone puts the rounding of h at the edge of the output
-//            tolerance).
-//  down:     A = 128 rows of W_down[e] (hidden outputs), B = the hi and the lo
-//            rows of h: two MMAs per K step into one accumulator, so W_down
-//            is read once; the epilogue scales by the pair's renormalised
-//            weight and stages the pair's output row in fp16 (the shared
-//            expert with weight 1, in its own rows); k_combine sums the rows.
+//            h = silu(g) * u for its half.  Routed pairs store h in bf16; the
+//            shared expert, whose output enters every row with weight 1,
+//            stores two bf16 parts hi = bf16(h), lo = bf16(h - hi) (about 16
+//            significant bits).  The rounding of h is the largest error of
+//            the path: a routed pair's share of it is scaled by the pair's
+//            weight (the weights of a row sum to 1), the shared expert's is
+//            not, and one bf16 part there too would leave almost no margin in
+//            the output tolerance.
+//  down:     A = 128 rows of W_down[e] (hidden outputs), B = rows of h; for
+//            the shared expert the hi and the lo rows, two MMAs per K step
+//            into one accumulator, so W_down is read once; the epilogue
+//            scales by the pair's renormalised weight and stages the pair's
+//            output row in fp16 (the shared expert with weight 1, in its own
+//            rows); k_combine sums the rows.
 //
 // Pipeline (one CTA per SM, persistent over the unit list):
 //   warp 0 lane 0  TMA producer: STAGES-deep ring of (A tile, B tile) stages
@@ -51,7 +56,7 @@ struct GemmCfg {
     // TMEM lane holds g and u of the same intermediate index.
     static constexpr bool kSplitGU = MODE == kGateUp && NMAX != kSmallN;
     static constexpr int kGURows = kSplitGU ? 128 : 64;  // intermediate rows per gate/up unit
-    static constexpr int kBParts = MODE == kDown ? 2 : 1;  // down: hi and lo parts of h
+    static constexpr int kBParts = MODE == kDown ? 2 : 1;  // down: room for hi and lo parts of h
     // rows per B box: 16 for the streaming shape, 64 for the large shape (fewer
     // TMA instructions per stage; NMAX is a multiple of it)
     static constexpr int kBoxRows = NMAX >= 64 ? 64 : 16;
@@ -74,6 +79,19 @@ struct GemmCfg {
 };
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// h of (pair or shared row) p, intermediate index il: routed rows [p][ld] bf16;
+// shared rows [p][2 ld] = hi | lo.
+__device__ __forceinline__ void store_h(__nv_bfloat16* out, bool shared, int ld, int p, int il, float hv) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+    if (shared) {
+        __nv_bfloat16* o = out + (size_t)p * (2 * ld);
+        o[il] = hi;
+        o[ld + il] = __float2bfloat16_rn(hv - __bfloat162float(hi));
+    } else {
+        out[(size_t)p * ld + il] = hi;
+    }
+}
 
 template <int MODE, int NMAX, int STAGES>
 __global__ void __launch_bounds__(192, 2)
@@ -149,7 +167,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
             const uint32_t bbytes = gathered ? (uint32_t)nb4 * 512u
                                              : (uint32_t)(nbox * C::kBoxRows * 128);
-            const uint32_t bytes = (uint32_t)C::kABytes + C::kBParts * bbytes;
+            // down: the shared expert's units carry the lo part of h as well
+            const int parts = MODE == kDown && g == a.E ? 2 : 1;
+            const uint32_t bytes = (uint32_t)C::kABytes + parts * bbytes;
             const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
             if (gathered) {
                 // the unit's rows of x, padded to a multiple of 4 with R (read as zeros);
@@ -194,7 +214,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         constexpr int kBoxBytes = C::kBoxRows * 128;
                         for (int t = 0; t < nbox; ++t)
                             tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, full + stage);
-                        if (MODE == kDown)  // lo part of h: columns K .. 2K-1 of the same rows
+                        if (parts == 2)  // lo part of h: columns K .. 2K-1 of the same rows
                             for (int t = 0; t < nbox; ++t)
                                 tma_load_2d(sB + NMAX * 128 + t * kBoxBytes, mB, K + kc,
                                             start + t * C::kBoxRows, full + stage);
@@ -260,7 +280,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (C::kSplitGU)  // up rows into the second accumulator
                             tc_mma_bf16(d + NMAX, smem_desc_sw128(sA + 128 * 128 + kk * 32), bd, idesc,
                                         (kb | kk) != 0);
-                        if (MODE == kDown)
+                        if (MODE == kDown && g == a.E)
                             tc_mma_bf16(d, ad, smem_desc_sw128(sB + NMAX * 128 + kk * 32), idesc, 1u);
                     }
                     tc_commit(empty + stage);
@@ -302,12 +322,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         for (int t = 0; t < 16; ++t) {
                             const int col = c + t;
                             if (col < n) {
-                                const float hv = silu(gv[t]) * uv[t];
-                                const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
-                                const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
-                                __nv_bfloat16* o = out + (size_t)(start + col) * (2 * ld);
-                                o[il] = hi;
-                                o[ld + il] = lo;
+                                store_h(out, g == a.E, ld, start + col, il, silu(gv[t]) * uv[t]);
                             }
                         }
                     }
@@ -344,12 +359,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         const float gv = is_gate ? v[t] : xg[r * 9 + t];
                         const float uv = is_gate ? xu[r * 9 + t] : v[8 + t];
                         if (col < n) {
-                            const float hv = silu(gv) * uv;
-                            const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
-                            const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
-                            __nv_bfloat16* o = out + (size_t)(start + col) * (2 * ld);
-                            o[il] = hi;
-                            o[ld + il] = lo;
+                            store_h(out, g == a.E, ld, start + col, il, silu(gv) * uv);
                         }
                     }
                     mbar_arrive(xbar + 1);  // the buffer is reused by the next chunk

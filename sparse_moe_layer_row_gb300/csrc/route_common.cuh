@@ -6,7 +6,9 @@
 // Model card "Clover-35B-A3B-Preview -- CMF", intro: each row is routed to the
 // top 8 of 256 experts.  The arithmetic (fixed so that ids are reproducible):
 //   * z[r,e] = sum_h x[r,h] W[e,h] in fp32.  Each bf16*bf16 product is exact in
-//     fp32, so an fma adding it equals the add of the rounded product.  h is
+//     fp32, so an fma adding it equals the add of the rounded product (and the
+//     mixed-precision fma.rn.f32.bf16, which takes the bf16 operands as they
+//     are, gives the same bits as an fp32 fma of the widened operands).  h is
 //     cut into stripes of 256; lane p of a warp owns elements 8p..8p+7 of every
 //     stripe and accumulates them in ascending h; the 32 lane sums are combined
 //     in the xor-butterfly pattern (partner distance 16, 8, 4, 2, 1).
@@ -61,6 +63,26 @@ __device__ __forceinline__ void bf16x8(uint4 v, float* f) {
     f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xFFFF0000u);
     f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xFFFF0000u);
     f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+// acc = fma(x_j, w_j, acc) for the eight bf16 pairs of (x, w), j ascending
+// (element 2i is the low half of word i).
+__device__ __forceinline__ float fma_bf16x2(uint32_t x, uint32_t w, float acc) {
+    asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(x), "r"(w));
+    return acc;
+}
+
+__device__ __forceinline__ float dot8_bf16(uint4 x, uint4 w, float acc) {
+    acc = fma_bf16x2(x.x, w.x, acc);
+    acc = fma_bf16x2(x.y, w.y, acc);
+    acc = fma_bf16x2(x.z, w.z, acc);
+    return fma_bf16x2(x.w, w.w, acc);
 }
 
 // z -> z + bias, + 0, as the contract states.

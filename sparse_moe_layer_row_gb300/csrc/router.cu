@@ -93,19 +93,10 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
         for (int s = 0; s < a.H; s += 256) {
             Stripe nxt = cur;
             if (s + 256 < a.H) load_stripe(nxt, a, rg, eg, s + 256 + lane * 8);
-            float xf[kRT][8];
 #pragma unroll
-            for (int r = 0; r < kRT; ++r) bf16x8(cur.x[r], xf[r]);
+            for (int e = 0; e < kET; ++e)
 #pragma unroll
-            for (int e = 0; e < kET; ++e) {
-                float wf[8];
-                bf16x8(cur.w[e], wf);
-#pragma unroll
-                for (int r = 0; r < kRT; ++r)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        acc[r * kET + e] = __fmaf_rn(xf[r][q], wf[q], acc[r * kET + e]);
-            }
+                for (int r = 0; r < kRT; ++r) acc[r * kET + e] = dot8_bf16(cur.x[r], cur.w[e], acc[r * kET + e]);
             cur = nxt;
         }
         // transposed butterfly: after the step with partner distance o, lane
@@ -180,15 +171,8 @@ __global__ void __launch_bounds__(256, 1) k_route_small(RouteArgs a) {
 #pragma unroll
             for (int si = 0; si < kSmPD; ++si) {
                 if (s0 + si * 256 >= a.H) break;
-                float xf[8];
-                bf16x8(xv[si], xf);
 #pragma unroll
-                for (int e = 0; e < kSmET; ++e) {
-                    float wf[8];
-                    bf16x8(wv[si][e], wf);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[e] = __fmaf_rn(xf[q], wf[q], acc[e]);
-                }
+                for (int e = 0; e < kSmET; ++e) acc[e] = dot8_bf16(xv[si], wv[si][e], acc[e]);
             }
         }
         // halving at partner distances 16 and 8 (4 -> 1 accumulators), then

@@ -46,6 +46,10 @@ struct TcCfg {
 
 __device__ __forceinline__ float slack(float z) { return fabsf(z) * 0x1p-20f + 0x1p-100f; }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 }  // namespace
 
 // |w_e|_2 of every router row (times 1.001, which covers the rounding of the sum).
@@ -228,18 +232,14 @@ __device__ __noinline__ void exact_full_row(const RouteTcArgs& a, int r, const f
         for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
         for (int s = 0; s < a.H; s += 256) {
             const int col = s + lane * 8;
-            float xf[8];
-            bf16x8(__ldg(reinterpret_cast<const uint4*>(xr + col)), xf);
+            const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + col));
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int e = g * 16 + i;
-                float wf[8];
                 const uint4 wv = e < a.E
                     ? __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)e * a.H + col))
                     : make_uint4(0, 0, 0, 0);
-                bf16x8(wv, wf);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i] = __fmaf_rn(xf[j], wf[j], acc[i]);
+                acc[i] = dot8_bf16(xv, wv, acc[i]);
             }
         }
         // transposed halving over partner distances 16, 8, 4, 2 (16 -> 1
@@ -269,23 +269,23 @@ __device__ __noinline__ void exact_full_row(const RouteTcArgs& a, int r, const f
 }
 
 // A CTA takes tiles of kExRows rows.
-//   1. warp w screens row w of the tile: converts x_r to fp32 in shared
-//      memory, forms |x_r|, finds the k-th approximate logit T and lists the
-//      candidates;
+//   1. warp w screens row w of the tile: copies x_r to shared memory, forms
+//      |x_r|, finds the k-th approximate logit T and lists the candidates;
 //   2. the tile's (row, candidate) pairs are shared out over the 8 warps, two
 //      per pass: each lane accumulates its elements of both dot products in
 //      the contract order, one halving step at partner distance 16 leaves
 //      candidate 0 in lanes 0-15 and candidate 1 in lanes 16-31, and the
 //      plain butterfly at 8, 4, 2, 1 finishes both;
 //   3. warp w takes top-k and softmax of row w over its candidates.
-// x tile layout: [row][stripe][half][lane] float4, so that each lane's eight
-// values of a stripe are two conflict-free 16-byte reads.
+// The loads are latency bound (L2 round trips of a few thousand cycles), so
+// each step prefetches into L1 what a later step reads: the next pair's router
+// rows during a pair, the next tile's x row and logits during step 2.
 constexpr int kExRows = 8;
-constexpr int kExMaxH = 6144;  // x tile in shared memory: kExRows * H fp32
+constexpr int kExMaxH = 8192;  // x tile in shared memory: kExRows * H bf16
 
 __global__ void __launch_bounds__(256, 2) k_route_exact(RouteTcArgs a) {
     extern __shared__ __align__(16) uint8_t ex_smem[];
-    float4* s_x = reinterpret_cast<float4*>(ex_smem);  // [kExRows][H/256][2][32]
+    __nv_bfloat16* s_x = reinterpret_cast<__nv_bfloat16*>(ex_smem);  // [kExRows][H]
     __shared__ int32_t s_ce[kExRows * kCandCap];  // candidate expert of each slot
     __shared__ float s_cz[kExRows * kCandCap];    // its exact logit (bias added)
     __shared__ int s_cnt[kExRows];                // candidates of the row; -1: all experts
@@ -303,31 +303,43 @@ __global__ void __launch_bounds__(256, 2) k_route_exact(RouteTcArgs a) {
         // ------------------------------------------------ 1. screening of row r
         if (r < a.R) {
             const __nv_bfloat16* xr = a.x + (size_t)r * a.H;
-            float4* sx = s_x + (size_t)w * nstripes * 64;
-            float ss = 0.0f;
-            for (int st = 0; st < nstripes; ++st) {
-                float f[8];
-                bf16x8(__ldg(reinterpret_cast<const uint4*>(xr + st * 256 + lane * 8)), f);
-                sx[st * 64 + lane] = make_float4(f[0], f[1], f[2], f[3]);
-                sx[st * 64 + 32 + lane] = make_float4(f[4], f[5], f[6], f[7]);
+            __nv_bfloat16* sx = s_x + (size_t)w * a.H;
+            const int blk = a.bias ? find_block(a.off, a.nb, r) : 0;
+            const float* brow = a.bias ? a.bias + (size_t)blk * a.E : nullptr;
+            float az[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                az[i] = e < a.E ? __ldg(a.logits + (size_t)r * a.E + e) : 0.0f;
+            }
+            float ss = 0.0f;
+            for (int c0 = 0; c0 < a.H; c0 += 8 * 256) {
+                uint4 v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = c0 + i * 256 + lane * 8;
+                    if (c < a.H) v[i] = __ldg(reinterpret_cast<const uint4*>(xr + c));
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = c0 + i * 256 + lane * 8;
+                    if (c < a.H) {
+                        *reinterpret_cast<uint4*>(sx + c) = v[i];
+                        ss = dot8_bf16(v[i], v[i], ss);
+                    }
+                }
             }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
             const float gx = G * (sqrtf(ss) * 1.001f);  // 1.001 covers the rounding of the sum
-            const int blk = a.bias ? find_block(a.off, a.nb, r) : 0;
-            const float* brow = a.bias ? a.bias + (size_t)blk * a.E : nullptr;
             uint32_t sk[8];
-            float az[8];
             uint32_t nonfinite = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int e = lane + 32 * i;
                 sk[i] = 0;
-                az[i] = 0.0f;
                 if (e < a.E) {
-                    float z = __ldg(a.logits + (size_t)r * a.E + e);
+                    float z = az[i];
                     if (brow) z = __fadd_rn(z, __ldg(brow + e));
                     nonfinite += !isfinite(z);
                     az[i] = z;
@@ -388,20 +400,37 @@ __global__ void __launch_bounds__(256, 2) k_route_exact(RouteTcArgs a) {
             }
             const int total = __shfl_sync(0xffffffffu, incl, kExRows - 1);
             const int excl = incl - cr;  // lane i < kExRows: first slot of row i
+            {   // the next tile's row of this warp: x and approximate logits
+                const int rn = (tile + gridDim.x) * kExRows + w;
+                if (rn < a.R) {
+                    const __nv_bfloat16* xn = a.x + (size_t)rn * a.H;
+                    for (int c = lane * 64; c < a.H; c += 32 * 64) prefetch_l1(xn + c);
+                    if (lane * 32 < a.E) prefetch_l1(a.logits + (size_t)rn * a.E + lane * 32);
+                }
+            }
+            // expert of slot t (or -1 past the end) and its row in the tile
+            auto slot = [&](int t, int& rr) {
+                const uint32_t m = __ballot_sync(0xffffffffu, lane < kExRows && excl <= t);
+                rr = __popc(m) - 1;
+                const int first = __shfl_sync(0xffffffffu, excl, rr & 31);
+                return t < total ? s_ce[rr * kCandCap + (t - first)] : -1;
+            };
             for (int t0 = 2 * w; t0 < total; t0 += 2 * kExRows) {
                 int row[2], e[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int t = t0 + h;
-                    const uint32_t m = __ballot_sync(0xffffffffu, lane < kExRows && excl <= t);
-                    const int rr = __popc(m) - 1;
-                    const int first = __shfl_sync(0xffffffffu, excl, rr & 31);
-                    row[h] = rr;
-                    e[h] = t < total ? s_ce[rr * kCandCap + (t - first)] : -1;
+                e[0] = slot(t0, row[0]);
+                e[1] = slot(t0 + 1, row[1]);
+                {   // router rows of this warp's next pair
+                    int rdummy;
+                    const int n0 = slot(t0 + 2 * kExRows, rdummy);
+                    const int n1 = slot(t0 + 2 * kExRows + 1, rdummy);
+                    for (int c = lane * 64; c < a.H; c += 32 * 64) {
+                        if (n0 >= 0) prefetch_l1(a.wr + (size_t)n0 * a.H + c);
+                        if (n1 >= 0) prefetch_l1(a.wr + (size_t)n1 * a.H + c);
+                    }
                 }
                 float acc0 = 0.0f, acc1 = 0.0f;
-                const float4* x0 = s_x + (size_t)row[0] * nstripes * 64 + lane;
-                const float4* x1 = s_x + (size_t)row[1] * nstripes * 64 + lane;
+                const __nv_bfloat16* x0 = s_x + (size_t)row[0] * a.H + lane * 8;
+                const __nv_bfloat16* x1 = s_x + (size_t)row[1] * a.H + lane * 8;
                 for (int s0 = 0; s0 < nstripes; s0 += 8) {
                     uint4 w0[8], w1[8];
 #pragma unroll
@@ -417,21 +446,9 @@ __global__ void __launch_bounds__(256, 2) k_route_exact(RouteTcArgs a) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         if (s0 + i >= nstripes) break;
-                        const int st = s0 + i;
-                        float wf[8];
-                        float4 p = x0[st * 64], q = x0[st * 64 + 32];
-                        bf16x8(w0[i], wf);
-                        acc0 = __fmaf_rn(p.x, wf[0], acc0); acc0 = __fmaf_rn(p.y, wf[1], acc0);
-                        acc0 = __fmaf_rn(p.z, wf[2], acc0); acc0 = __fmaf_rn(p.w, wf[3], acc0);
-                        acc0 = __fmaf_rn(q.x, wf[4], acc0); acc0 = __fmaf_rn(q.y, wf[5], acc0);
-                        acc0 = __fmaf_rn(q.z, wf[6], acc0); acc0 = __fmaf_rn(q.w, wf[7], acc0);
-                        p = x1[st * 64];
-                        q = x1[st * 64 + 32];
-                        bf16x8(w1[i], wf);
-                        acc1 = __fmaf_rn(p.x, wf[0], acc1); acc1 = __fmaf_rn(p.y, wf[1], acc1);
-                        acc1 = __fmaf_rn(p.z, wf[2], acc1); acc1 = __fmaf_rn(p.w, wf[3], acc1);
-                        acc1 = __fmaf_rn(q.x, wf[4], acc1); acc1 = __fmaf_rn(q.y, wf[5], acc1);
-                        acc1 = __fmaf_rn(q.z, wf[6], acc1); acc1 = __fmaf_rn(q.w, wf[7], acc1);
+                        const int off = (s0 + i) * 256;
+                        acc0 = dot8_bf16(*reinterpret_cast<const uint4*>(x0 + off), w0[i], acc0);
+                        acc1 = dot8_bf16(*reinterpret_cast<const uint4*>(x1 + off), w1[i], acc1);
                     }
                 }
                 // halving at distance 16: lanes 0-15 keep candidate 0, 16-31 candidate 1
@@ -478,7 +495,7 @@ cudaError_t route_tc_set_attributes() {
                                          TcCfg::kSmem);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(k_route_exact, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kExRows * kExMaxH * 4);
+                                kExRows * kExMaxH * 2);
 }
 
 cudaError_t launch_route_tc(const RouteTcArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
@@ -494,7 +511,7 @@ cudaError_t launch_route_tc(const RouteTcArgs& a, const CUtensorMap& tm_x, const
     const long eb = ntiles_ex < (long)num_sms * 2 ? ntiles_ex : (long)num_sms * 2;
     if (e == cudaSuccess)
         e = launch_kernel(k_route_exact, dim3((unsigned)eb), dim3(256),
-                          (size_t)kExRows * a.H * 4, st, a);
+                          (size_t)kExRows * a.H * 2, st, a);
     return e;
 }
 
