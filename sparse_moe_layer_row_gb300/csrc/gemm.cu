@@ -56,12 +56,15 @@ struct GemmCfg {
     // TMEM lane holds g and u of the same intermediate index.
     static constexpr bool kSplitGU = MODE == kGateUp && NMAX != kSmallN;
     static constexpr int kGURows = kSplitGU ? 128 : 64;  // intermediate rows per gate/up unit
-    static constexpr int kBParts = MODE == kDown ? 2 : 1;  // down: room for hi and lo parts of h
+    // down: shared-expert units carry the hi and the lo part of h, kShN rows
+    // each, in the B region of NMAX routed rows (or of 2 * kShN rows)
+    static constexpr int kShN = MODE == kDown && NMAX >= 128 ? NMAX / 2 : NMAX;
+    static constexpr int kBRows = MODE == kDown ? (NMAX > 2 * kShN ? NMAX : 2 * kShN) : NMAX;
     // rows per B box: 16 for the streaming shape, 64 for the large shape (fewer
     // TMA instructions per stage; NMAX is a multiple of it)
     static constexpr int kBoxRows = NMAX >= 64 ? 64 : 16;
     static constexpr int kABytes = (kSplitGU ? 2 : 1) * 128 * 128;
-    static constexpr int kBBytes = kBParts * NMAX * 128;
+    static constexpr int kBBytes = kBRows * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kXchgOff = STAGES * kStageBytes;
     // gate/up streaming shape: g <-> u exchange; down: the unit's fp16 output tile
@@ -216,7 +219,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, full + stage);
                         if (parts == 2)  // lo part of h: columns K .. 2K-1 of the same rows
                             for (int t = 0; t < nbox; ++t)
-                                tma_load_2d(sB + NMAX * 128 + t * kBoxBytes, mB, K + kc,
+                                tma_load_2d(sB + C::kShN * 128 + t * kBoxBytes, mB, K + kc,
                                             start + t * C::kBoxRows, full + stage);
                     }
                 }
@@ -281,7 +284,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             tc_mma_bf16(d + NMAX, smem_desc_sw128(sA + 128 * 128 + kk * 32), bd, idesc,
                                         (kb | kk) != 0);
                         if (MODE == kDown && g == a.E)
-                            tc_mma_bf16(d, ad, smem_desc_sw128(sB + NMAX * 128 + kk * 32), idesc, 1u);
+                            tc_mma_bf16(d, ad, smem_desc_sw128(sB + C::kShN * 128 + kk * 32), idesc, 1u);
                     }
                     tc_commit(empty + stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -451,7 +454,7 @@ static cudaError_t set_attr() {
 // expert (weight streaming: two CTAs per SM, each with its own ring, keep more
 // TMA streams in flight); large = many rows (tensor-core bound, one CTA per SM).
 constexpr int kSmallStagesGU = 5, kSmallStagesDN = 4;
-constexpr int kLargeStagesGU = 4, kLargeStagesDN = 4;
+constexpr int kLargeStagesGU = 4, kLargeStagesDN = 3;
 constexpr int kSmallCtasPerSm = 2;
 
 cudaError_t gemm_set_attributes() {
