@@ -285,7 +285,6 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
                    at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
                    at<int4>(workspace, L.units_gu), at<int4>(workspace, L.units_dn),
                    at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
-                   static_cast<const __nv_bfloat16*>(x), at<__nv_bfloat16>(workspace, L.xp),
                    at<int32_t>(workspace, L.inv),
                    at<uint32_t>(workspace, L.status)};
     GemmMaps gu{}, dn{};
@@ -293,8 +292,7 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     gu.a0 = p->tm_wg; gu.a1 = p->tm_wu; gu.a2 = p->tm_sg; gu.a3 = p->tm_su;
     dn.a0 = p->tm_wd; dn.a1 = p->tm_wd; dn.a2 = p->tm_sd; dn.a3 = p->tm_sd;
     const uint32_t box = small ? 16 : 64;   // B rows per TMA box (see k_gemm)
-    bool good = encode_bf16(&gu.b0, at<void>(workspace, L.xp), d.H, (uint64_t)L.max_pairs, 0, box, L2A) &&
-                encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
+    bool good = encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
                 encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
                 encode_bf16(&dn.b0, at<void>(workspace, L.h), (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
                             box, L2A) &&
@@ -302,7 +300,8 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
                             (uint64_t)d.max_rows, 0, box, L2A);
     if (!good) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation tensor");
     GemmArgs ga{at<int4>(workspace, L.units_gu), at<int32_t>(workspace, L.misc) + 1, d.E, d.H, d.I,
-                d.Is, R, at<__nv_bfloat16>(workspace, L.h), at<__nv_bfloat16>(workspace, L.hs),
+                d.Is, R, static_cast<const __nv_bfloat16*>(x), at<__nv_bfloat16>(workspace, L.h),
+                at<__nv_bfloat16>(workspace, L.hs),
                 at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
                 at<__half>(workspace, L.ys), (int)L.max_pairs, at<uint32_t>(workspace, L.status)};
     // Under stream capture an event record must be an external node to be

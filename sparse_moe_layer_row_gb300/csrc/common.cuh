@@ -31,7 +31,6 @@ struct Layout {
     size_t units_dn;     // int4 [max_units_dn]
     size_t pair_row;     // int32 [max_pairs]
     size_t pair_w;       // fp32 [max_pairs]
-    size_t xp;           // bf16 [max_pairs, H]       rows of x in pair order (large calls)
     size_t h;            // bf16 [max_pairs, I]       routed SwiGLU activations
     size_t hs;           // bf16 [max_rows, 2Is]      shared-expert activations, hi | lo
     size_t inv;          // int32 [max_pairs]         staging row of each (row, slot)
@@ -76,7 +75,6 @@ inline Layout make_layout(const moe_dims& d) {
     L.units_dn = take(sizeof(int4) * (size_t)L.max_units_dn);
     L.pair_row = take(sizeof(int32_t) * (size_t)P);
     L.pair_w = take(sizeof(float) * (size_t)P);
-    L.xp = take(2 * (size_t)(P * H));
     L.h = take(2 * (size_t)(P * d.I));
     L.hs = take(2 * (size_t)(R * 2 * d.Is));
     L.inv = take(sizeof(int32_t) * (size_t)P);
@@ -162,6 +160,28 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             if (globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
+}
+
+// ---- cp.async (16-byte global -> shared copies, L2 only) ----------------------
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Make this thread's generic-proxy writes to shared memory visible to the
+// async proxy (TMA, tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---- TMA ----------------------------------------------------------------------

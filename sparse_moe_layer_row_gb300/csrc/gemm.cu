@@ -65,18 +65,28 @@ struct GemmCfg {
     static constexpr int kBoxRows = NMAX >= 64 ? 64 : 16;
     static constexpr int kABytes = (kSplitGU ? 2 : 1) * 128 * 128;
     static constexpr int kBBytes = kBRows * 128;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kXchgOff = STAGES * kStageBytes;
+    // large gate/up: the rows of x (B) are gathered by four loader warps with
+    // 16-byte cp.async into a ring of their own, deeper than the A ring
+    static constexpr bool kLoaders = kSplitGU;
+    static constexpr int kBStages = kLoaders ? 6 : 0;
+    static constexpr int kBLag = 4;  // stages a loader thread keeps in flight
+    static constexpr int kThreads = kLoaders ? 320 : 192;
+    static constexpr int kMinBlocks = kLoaders ? 1 : 2;
+    static constexpr int kStageBytes = kLoaders ? kABytes : kABytes + kBBytes;  // A ring stride
+    static constexpr int kBRingOff = STAGES * kStageBytes;
+    static constexpr int kXchgOff = kBRingOff + kBStages * kBBytes;
     // gate/up streaming shape: g <-> u exchange; down: the unit's fp16 output tile
     static constexpr int kXchgBytes =
         MODE == kGateUp ? (kSplitGU ? 0 : 2 * 64 * 9 * 4) : NMAX * 128 * 2;
     static constexpr int kRowsOff = kXchgOff + kXchgBytes;             // gate/up: rows of x of a unit
     static constexpr int kRowsBytes = MODE == kGateUp && NMAX == kSmallN ? NMAX * 4 : 0;
     static constexpr int kBarOff = kRowsOff + kRowsBytes;
-    static constexpr int kSmem = kBarOff + 256 + 1024;
+    static constexpr int kSmem = kBarOff + 512 + 1024;
     static constexpr int kAccCols = (kSplitGU ? 2 : 1) * NMAX;   // TMEM columns per accumulator
     static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static_assert(kBLag <= kBStages - 2 || !kLoaders, "a loader may hold back at most B stages - 2");
+    static_assert(8 * (2 * STAGES + 8 + 2 * kBStages) + 16 <= 512, "barrier region");
     static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
     static_assert(NMAX % 16 == 0 && NMAX <= 256 && NMAX % (NMAX >= 64 ? 64 : 16) == 0, "MMA N extent");
 };
@@ -97,7 +107,8 @@ __device__ __forceinline__ void store_h(__nv_bfloat16* out, bool shared, int ld,
 }
 
 template <int MODE, int NMAX, int STAGES>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(GemmCfg<MODE, NMAX, STAGES>::kThreads,
+                                  GemmCfg<MODE, NMAX, STAGES>::kMinBlocks)
 k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
@@ -117,8 +128,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
-    uint64_t* xbar = tempty + 2;  // [2] gate/up epilogue exchange (128 arrivals each)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2);
+    uint64_t* xbar = tempty + 2;  // [2] epilogue exchange (128 arrivals each)
+    uint64_t* bfull = xbar + 2;   // [kBStages] B ring (loaders)
+    uint64_t* bempty = bfull + C::kBStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bempty + C::kBStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;
 
@@ -130,6 +143,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             mbar_init(tempty + i, 128);
             mbar_init(xbar + i, 128);
         }
+        for (int s = 0; s < C::kBStages; ++s) { mbar_init(bfull + s, 128); mbar_init(bempty + s, 1); }
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -143,7 +157,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmA2);
         prefetch_tmap(&tmA3); prefetch_tmap(&tmB1);
         if (kGather) prefetch_tmap(&tmBg);
-        else prefetch_tmap(&tmB0);  // pair-ordered x (gate/up) or h (down)
+        if (MODE == kDown) prefetch_tmap(&tmB0);  // h
     }
     const int nunits = __ldg(a.n_units);
 
@@ -172,7 +186,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                                              : (uint32_t)(nbox * C::kBoxRows * 128);
             // down: the shared expert's units carry the lo part of h as well
             const int parts = MODE == kDown && g == a.E ? 2 : 1;
-            const uint32_t bytes = (uint32_t)C::kABytes + parts * bbytes;
+            const uint32_t bytes = (uint32_t)C::kABytes + (C::kLoaders ? 0u : parts * bbytes);
             const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
             if (gathered) {
                 // the unit's rows of x, padded to a multiple of 4 with R (read as zeros);
@@ -213,7 +227,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (g == a.E) tma_load_2d(sA, &tmA2, kc, m * 128, full + stage);
                         else tma_load_3d(sA, &tmA0, kc, m * 128, g, full + stage);
                     }
-                    if (!gathered) {
+                    if (!gathered && !C::kLoaders) {
                         constexpr int kBoxBytes = C::kBoxRows * 128;
                         for (int t = 0; t < nbox; ++t)
                             tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, full + stage);
@@ -251,8 +265,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------ MMA issuer
-            int stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, acc = 0, bstage = 0;
+            uint32_t phase = 0, acc_phase = 0, bphase = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
                 const int4 un = __ldg(a.units + u);
@@ -267,14 +281,16 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * C::kAccCols);
                 for (int kb = 0; kb < (K >> 6); ++kb) {
-                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs) ||
+                        (C::kLoaders && !mbar_wait_bounded(bfull + bstage, bphase, abort_flag, kWaitLimitNs))) {
                         give_up();
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sA = sbase + stage * C::kStageBytes;
-                    const uint32_t sB = sA + C::kABytes;
+                    const uint32_t sB = C::kLoaders ? sbase + C::kBRingOff + bstage * C::kBBytes
+                                                    : sA + C::kABytes;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = smem_desc_sw128(sA + kk * 32);
@@ -288,12 +304,67 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                     tc_commit(empty + stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (C::kLoaders) {
+                        tc_commit(bempty + bstage);
+                        if (++bstage == C::kBStages) { bstage = 0; bphase ^= 1u; }
+                    }
                 }
                 if (!ok) break;
                 tc_commit(tfull + acc);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------- B loaders (large gate/up)
+        // Row i of a unit (its pair's row of x; the shared expert's rows are
+        // start + i) is copied by 8 threads, 16 bytes each, into the 128-byte
+        // swizzled row of the B tile: chunk c of row i lands at chunk c ^ (i & 7).
+        // A thread signals a stage once kBLag newer stages are issued, after
+        // its copies of it have landed and are fenced for the async proxy.
+        const int lt = threadIdx.x - 192;            // 0..127
+        const int lw = lt >> 5, r4 = (lt & 31) >> 3, ch = lt & 7;
+        int bstage = 0, npend = 0;
+        uint32_t bphase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+            const int4 un = __ldg(a.units + u);
+            const int g = un.x, start = un.z, n = un.w;
+            constexpr int kRowsPerThread = NMAX / 16;
+            const __nv_bfloat16* src[kRowsPerThread];
+#pragma unroll
+            for (int j = 0; j < kRowsPerThread; ++j) {
+                const int i = j * 16 + lw * 4 + r4;
+                const int row = i < n ? (g == a.E ? start + i : __ldg(a.pair_row + start + i)) : -1;
+                src[j] = row >= 0 ? a.x + (size_t)row * a.H + ch * 8 : nullptr;
+            }
+            for (int kb = 0; kb < (a.H >> 6); ++kb) {
+                if (!mbar_wait_bounded(bempty + bstage, bphase ^ 1u, abort_flag, kWaitLimitNs)) {
+                    give_up();
+                    ok = false;
+                    break;
+                }
+                const uint32_t sB = sbase + C::kBRingOff + bstage * C::kBBytes;
+#pragma unroll
+                for (int j = 0; j < kRowsPerThread; ++j) {
+                    const int i = j * 16 + lw * 4 + r4;
+                    if (src[j]) cp_async16(sB + i * 128 + ((ch ^ (i & 7)) << 4), src[j] + kb * 64);
+                }
+                cp_async_commit();
+                if (npend == C::kBLag) {
+                    cp_async_wait<C::kBLag>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(bfull + (bstage + C::kBStages - C::kBLag) % C::kBStages);
+                } else {
+                    ++npend;
+                }
+                if (++bstage == C::kBStages) { bstage = 0; bphase ^= 1u; }
+            }
+        }
+        cp_async_wait<0>();  // nothing of this thread lands after the loop
+        if (ok) {
+            fence_proxy_async_smem();
+            for (int i = npend; i > 0; --i) mbar_arrive(bfull + (bstage + C::kBStages - i) % C::kBStages);
         }
     } else {
         // ---------------------------------------------------------- epilogue
@@ -439,7 +510,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 template <int MODE, int NMAX, int STAGES>
 static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int grid, cudaStream_t st) {
     using C = GemmCfg<MODE, NMAX, STAGES>;
-    return launch_kernel(k_gemm<MODE, NMAX, STAGES>, dim3(grid), dim3(192), C::kSmem, st, mp.a0, mp.a1,
+    return launch_kernel(k_gemm<MODE, NMAX, STAGES>, dim3(grid), dim3(C::kThreads), C::kSmem, st, mp.a0, mp.a1,
                       mp.a2, mp.a3, mp.b0, mp.b1, mp.bg, a);
 }
 

@@ -65,8 +65,6 @@ struct ScatterArgs {
     int4* units_dn;
     int32_t* pair_row;
     float* pair_w;
-    const __nv_bfloat16* x;
-    __nv_bfloat16* xp;    // [pairs, H] rows of x in pair order (large calls)
     int32_t* inv;         // [R * k] staging row of (row, slot), or -1
     uint32_t* status;
 };
@@ -84,8 +82,9 @@ struct GemmArgs {
     const int32_t* n_units;
     int E, H, I, Is;
     int R;                // rows of x (gathered row indices >= R read as zero)
-    __nv_bfloat16* h;     // [pairs, 2I]: bf16 hi part | bf16 lo part
-    __nv_bfloat16* hs;    // [rows, 2Is]
+    const __nv_bfloat16* x;  // [R, H] (rows gathered by the large gate/up loaders)
+    __nv_bfloat16* h;     // [pairs, I] routed activations (bf16)
+    __nv_bfloat16* hs;    // [rows, 2Is] shared activations: bf16 hi part | bf16 lo part
     const int32_t* pair_row;
     const float* pair_w;
     __half* ys;           // [max_pairs + max_rows, H] staged outputs (down GEMM)

@@ -65,8 +65,8 @@ __device__ void write_units(int4* out, int base, int g, int start, int n, int nt
 //                    last CTA to finish forms the expert offsets and the unit
 //                    lists of both GEMMs
 //   k_scatter_place  per block: each surviving pair's position, the pair
-//                    lists (row, weight), the inverse map (row, slot) -> pair
-//                    and the copy of x in pair order read by the gate/up GEMM
+//                    lists (row, weight) and the inverse map (row, slot) -> pair
+// No copy of x is made: the gate/up GEMM gathers its rows of x itself.
 // A row that names the same expert twice contributes its first slot only
 // (later duplicates are counted as bad ids).
 constexpr int kHistRows = 32;
@@ -221,51 +221,23 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     }
 }
 
-// One CTA per block: a thread per (row, slot) of the block places the pair;
-// then one warp per placed pair copies its row of x into pair order.
+// One CTA per block: a thread per (row, slot) of the block.
 __global__ void __launch_bounds__(kScatThreads) k_scatter_place(ScatterArgs a) {
-    __shared__ int2 s_pr[kScatThreads];  // (pair position, row) of this pass
     const int b = blockIdx.x;
     const int E = a.E, k = a.k;
     int r0 = a.off[b], r1 = a.off[b + 1];
     if (!(0 <= r0 && r0 <= r1 && r1 <= a.R)) r1 = r0 = 0;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int hv = a.H / 8;  // uint4 per row of x
-    for (int p0 = r0 * k; p0 < r1 * k; p0 += blockDim.x) {
-        const int p = p0 + threadIdx.x;
-        int2 pr = make_int2(-1, 0);
-        if (p < r1 * k) {
-            const int rk = a.prank[p];
-            if (rk < 0) {
-                a.inv[p] = -1;
-            } else {
-                const int e = a.topk_idx[p];
-                const int pos = a.expert_off[e] + a.hist[(size_t)b * E + e] + rk;
-                a.pair_row[pos] = p / k;
-                a.pair_w[pos] = a.w_renorm[p];
-                a.inv[p] = pos;
-                pr = make_int2(pos, p / k);
-            }
+    for (int p = r0 * k + threadIdx.x; p < r1 * k; p += blockDim.x) {
+        const int rk = a.prank[p];
+        if (rk < 0) {
+            a.inv[p] = -1;
+            continue;
         }
-        s_pr[threadIdx.x] = pr;
-        __syncthreads();
-        const int np = min((int)blockDim.x, r1 * k - p0);
-        for (int i = warp; i < np; i += nw) {
-            const int2 q = s_pr[i];
-            if (q.x < 0) continue;
-            const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)q.y * a.H);
-            uint4* dst = reinterpret_cast<uint4*>(a.xp + (size_t)q.x * a.H);
-            for (int v = lane; v < hv; v += 32 * 8) {
-                uint4 t[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (v + 32 * j < hv) t[j] = __ldg(src + v + 32 * j);
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (v + 32 * j < hv) dst[v + 32 * j] = t[j];
-            }
-        }
-        __syncthreads();
+        const int e = a.topk_idx[p];
+        const int pos = a.expert_off[e] + a.hist[(size_t)b * E + e] + rk;
+        a.pair_row[pos] = p / k;
+        a.pair_w[pos] = a.w_renorm[p];
+        a.inv[p] = pos;
     }
 }
 
