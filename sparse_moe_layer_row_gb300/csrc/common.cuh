@@ -100,6 +100,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialization, so it may be scheduled while the
+// kernel before it on the stream is still running.  The rule that keeps this
+// safe: a thread calls pdl_wait() -- which returns once the preceding kernel
+// has completed and its writes are visible -- before it reads or writes any
+// global memory that another kernel writes or reads; the only thing done
+// before it is reading the weights (read-only for every kernel).  pdl_trigger()
+// lets the next kernel be scheduled; it is called right after the wait, so at
+// most two kernels of a stream overlap.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Kernel launch through cudaLaunchKernelEx (one call site style for all kernels).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -109,6 +123,11 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 

@@ -64,6 +64,8 @@ __device__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t* warp_sums, uint64_
 }
 
 __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     __shared__ unsigned long long Q[kMaxE];
     __shared__ uint32_t touched[kMaxE / 32];
     __shared__ uint32_t incore[kMaxE / 32];

@@ -159,6 +159,17 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         if (kGather) prefetch_tmap(&tmBg);
         if (MODE == kDown) prefetch_tmap(&tmB0);  // h
     }
+    // Programmatic dependent launch (common.cuh).  Every role waits here for
+    // the preceding kernel, except the down GEMM's producer: the down GEMM
+    // follows the gate/up GEMM, and its first stages' W_down tiles do not
+    // depend on it, so the producer issues those before it waits (its unit
+    // list was written by the scatter, which the gate/up GEMM waited for
+    // before letting this kernel start).
+    constexpr bool kEarlyA = MODE == kDown;
+    if (!(kEarlyA && warp == 0)) {
+        pdl_wait();
+        pdl_trigger();
+    }
     const int nunits = __ldg(a.n_units);
 
     auto give_up = [&]() {
@@ -172,6 +183,30 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         uint32_t phase = 0;
         bool ok = true;
         int* s_rows = reinterpret_cast<int*>(base + C::kRowsOff);
+        // B copies of the first stages, held back until the wait (down GEMM)
+        struct HeldB { uint32_t sB; int g, start, nbox, K, kc; uint64_t* bar; };
+        HeldB held[kEarlyA ? STAGES : 1];
+        int nheld = 0;
+        bool waited = !kEarlyA;
+        auto issue_b = [&](uint32_t sB, int g, int start, int nbox, int K, int kc, uint64_t* bar) {
+            constexpr int kBoxBytes = C::kBoxRows * 128;
+            const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
+            for (int t = 0; t < nbox; ++t)
+                tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, bar);
+            if (MODE == kDown && g == a.E)  // lo part of h: columns K .. 2K-1 of the same rows
+                for (int t = 0; t < nbox; ++t)
+                    tma_load_2d(sB + C::kShN * 128 + t * kBoxBytes, mB, K + kc, start + t * C::kBoxRows, bar);
+        };
+        auto release_held = [&]() {
+            pdl_wait();
+            pdl_trigger();
+            if (lane == 0)
+                for (int i = 0; i < nheld; ++i)
+                    issue_b(held[i].sB, held[i].g, held[i].start, held[i].nbox, held[i].K, held[i].kc,
+                            held[i].bar);
+            nheld = 0;
+            waited = true;
+        };
         for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
             const int4 un = __ldg(a.units + u);
             const int g = un.x, m = un.y, start = un.z, n = un.w;
@@ -187,7 +222,6 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             // down: the shared expert's units carry the lo part of h as well
             const int parts = MODE == kDown && g == a.E ? 2 : 1;
             const uint32_t bytes = (uint32_t)C::kABytes + (C::kLoaders ? 0u : parts * bbytes);
-            const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
             if (gathered) {
                 // the unit's rows of x, padded to a multiple of 4 with R (read as zeros);
                 // copies of the previous unit took their coordinates when issued
@@ -228,15 +262,11 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         else tma_load_3d(sA, &tmA0, kc, m * 128, g, full + stage);
                     }
                     if (!gathered && !C::kLoaders) {
-                        constexpr int kBoxBytes = C::kBoxRows * 128;
-                        for (int t = 0; t < nbox; ++t)
-                            tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, full + stage);
-                        if (parts == 2)  // lo part of h: columns K .. 2K-1 of the same rows
-                            for (int t = 0; t < nbox; ++t)
-                                tma_load_2d(sB + C::kShN * 128 + t * kBoxBytes, mB, K + kc,
-                                            start + t * C::kBoxRows, full + stage);
+                        if (waited) issue_b(sB, g, start, nbox, K, kc, full + stage);
+                        else held[nheld] = HeldB{sB, g, start, nbox, K, kc, full + stage};
                     }
                 }
+                if (!waited && ++nheld == STAGES) release_held();
                 if (gathered) {
                     // the gathers are spread over the lanes (issued after the
                     // expected byte count is posted by lane 0)
@@ -249,6 +279,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
+        if (!waited) release_held();
         // Drain: every stage must be released by the MMA before the CTA
         // exits (all copies landed, all reads done).  Bounded; after an
         // abort the MMA may never release, so the wait gives up quickly.

@@ -77,6 +77,8 @@ __device__ __forceinline__ void load_stripe(Stripe& s, const RouteArgs& a, int r
 }
 
 __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -142,6 +144,8 @@ constexpr int kSmET = 4;
 constexpr int kSmPD = 8;   // stripes in flight per warp
 
 __global__ void __launch_bounds__(256, 1) k_route_small(RouteArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;

@@ -54,6 +54,8 @@ __device__ __forceinline__ void prefetch_l1(const void* p) {
 
 // |w_e|_2 of every router row (times 1.001, which covers the rounding of the sum).
 __global__ void __launch_bounds__(256) k_route_norms(RouteTcArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -75,6 +77,8 @@ __global__ void __launch_bounds__(256) k_route_norms(RouteTcArgs a) {
 __global__ void __launch_bounds__(192, 1)
 k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            RouteTcArgs a, int nsplit) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     using C = TcCfg;
     extern __shared__ uint8_t smem_raw[];
     const int ntiles = (a.R + 127) / 128;
@@ -284,6 +288,8 @@ constexpr int kExRows = 8;
 constexpr int kExMaxH = 8192;  // x tile in shared memory: kExRows * H bf16
 
 __global__ void __launch_bounds__(256, 2) k_route_exact(RouteTcArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     extern __shared__ __align__(16) uint8_t ex_smem[];
     __nv_bfloat16* s_x = reinterpret_cast<__nv_bfloat16*>(ex_smem);  // [kExRows][H]
     __shared__ int32_t s_ce[kExRows * kCandCap];  // candidate expert of each slot

@@ -72,6 +72,8 @@ __device__ void write_units(int4* out, int base, int g, int start, int n, int nt
 constexpr int kHistRows = 32;
 
 __global__ void __launch_bounds__(kScatThreads) k_scatter_hist(ScatterArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     __shared__ uint8_t s_slot[kHistRows][kMaxExperts];
     __shared__ int s_run[kMaxExperts];
     __shared__ int s_dup;
@@ -122,6 +124,8 @@ constexpr int kScanThreads = 256;
 constexpr int kDownGroup = 32;
 
 __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     __shared__ int warp_sums[32];
     __shared__ int s_tot[kMaxExperts];
     __shared__ int s_cd[kMaxExperts + 1];
@@ -223,6 +227,8 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
 
 // One CTA per block: a thread per (row, slot) of the block.
 __global__ void __launch_bounds__(kScatThreads) k_scatter_place(ScatterArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     const int b = blockIdx.x;
     const int E = a.E, k = a.k;
     int r0 = a.off[b], r1 = a.off[b + 1];
@@ -249,6 +255,8 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_place(ScatterArgs a) {
 constexpr int kSmallThreads = 512;
 
 __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     __shared__ uint8_t s_slot[kSmallRows][kMaxExperts];   // slot of expert e in row r, or 0xFF
     __shared__ int s_cnt[kMaxExperts];
     __shared__ int warp_sums[32];
@@ -335,6 +343,8 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
 // lane owns 8 consecutive columns.  All of a task's contributions are loaded
 // before they are added, eight at a time, so the loads overlap.
 __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
