@@ -133,17 +133,22 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
     }
 }
 
-// Small batches: one warp computes 1 row x 4 experts, with all of its stripes'
-// loads in flight at once (groups of 8 stripes), so the latency of one memory
-// round trip is paid instead of one per stripe; the four accumulators are
-// reduced by two transposed halving steps and three plain butterfly steps
+// Small batches: one warp computes 1 row x 4 experts.  Its stripes' loads are
+// issued four stripes at a time (registers), and every later stripe of the
+// row is prefetched into L1 first, so the warp pays about one memory round
+// trip; two CTAs per SM put a 32-row call in one wave.  The four accumulators
+// are reduced by two transposed halving steps and three plain butterfly steps
 // (the same pairs as the contract's butterfly); a ticket per row lets the
 // warp finishing a row run its top-k.
 constexpr int kSmallRouteRows = 64;
 constexpr int kSmET = 4;
-constexpr int kSmPD = 8;   // stripes in flight per warp
+constexpr int kSmPD = 4;   // stripes held in registers at a time
 
-__global__ void __launch_bounds__(256, 1) k_route_small(RouteArgs a) {
+__device__ __forceinline__ void prefetch_l1_line(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+__global__ void __launch_bounds__(256, 2) k_route_small(RouteArgs a) {
     pdl_wait();  // see common.cuh: nothing global is touched before
     pdl_trigger();
     const int lane = threadIdx.x & 31;
@@ -154,6 +159,14 @@ __global__ void __launch_bounds__(256, 1) k_route_small(RouteArgs a) {
     for (int t = warp; t < ntasks; t += nwarps) {
         const int row = t / n_eg, eg = t - row * n_eg;
         const __nv_bfloat16* xr = a.x + (size_t)row * a.H;
+        // L1 prefetch of stripes kSmPD.. of x and the four router rows: one
+        // 128-byte line per lane and step (a stripe of a row is 4 lines)
+        for (int l = lane; (kSmPD + l / 20) * 256 < a.H; l += 32) {
+            const int st = kSmPD + l / 20, r5 = (l % 20) >> 2, q = l & 3;
+            const int ex = eg * kSmET + r5 - 1;
+            const __nv_bfloat16* base = r5 == 0 ? xr : a.wr + (size_t)(ex < a.E ? ex : 0) * a.H;
+            prefetch_l1_line(base + st * 256 + q * 64);
+        }
         float acc[kSmET];
 #pragma unroll
         for (int i = 0; i < kSmET; ++i) acc[i] = 0.0f;
