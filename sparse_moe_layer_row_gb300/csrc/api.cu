@@ -279,7 +279,7 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     const int nt_dn = small ? kSmallN : kLargeNDown;
 
     ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
-                   small ? kSmallN : kLargeNDownShared, small ? 64 : 128,
+                   small ? 64 : 128,
                    at<int32_t>(workspace, L.prank), at<int32_t>(workspace, L.hist),
                    at<int32_t>(workspace, L.count),
                    at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),

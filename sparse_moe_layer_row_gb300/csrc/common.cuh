@@ -41,12 +41,10 @@ struct Layout {
 
 // Rows of x per unit of grouped-GEMM work (the MMA N extent).  A call with
 // few rows uses kSmallN for both GEMMs; otherwise the gate/up GEMM takes
-// kLargeN rows per unit and the down GEMM kLargeNDown (kLargeNDownShared for
-// the shared expert, whose units carry two parts of h).
+// kLargeN rows per unit and the down GEMM kLargeNDown.
 constexpr int kSmallN = 32;
 constexpr int kLargeN = 128;
 constexpr int kLargeNDown = 256;
-constexpr int kLargeNDownShared = kLargeNDown / 2;  // shared units carry hi and lo parts
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -24,12 +24,14 @@
 //            weight (the weights of a row sum to 1), the shared expert's is
 //            not, and one bf16 part there too would leave almost no margin in
 //            the output tolerance.
-//  down:     A = 128 rows of W_down[e] (hidden outputs), B = rows of h; for
-//            the shared expert the hi and the lo rows, two MMAs per K step
-//            into one accumulator, so W_down is read once; the epilogue
-//            scales by the pair's renormalised weight and stages the pair's
-//            output row in fp16 (the shared expert with weight 1, in its own
-//            rows); k_combine sums the rows.
+//  down:     A = 128 rows of W_down[e] (hidden outputs), B = rows of h.  For
+//            the shared expert K runs over [hi | lo] (its 2 Is columns of h)
+//            while A wraps around its Is columns: D = W (h_hi + h_lo), with
+//            full-width N tiles (an M = 128 MMA costs about the same for any
+//            N up to 256; measured: 535 cycles per four MMAs at N = 64, 582 at
+//            N = 256).  The epilogue scales by the pair's renormalised weight
+//            and stages the pair's output row in fp16 (the shared expert with
+//            weight 1, in its own rows); k_combine sums the rows.
 //
 // Pipeline (one CTA per SM, persistent over the unit list):
 //   warp 0 lane 0  TMA producer: STAGES-deep ring of (A tile, B tile) stages
@@ -56,15 +58,11 @@ struct GemmCfg {
     // TMEM lane holds g and u of the same intermediate index.
     static constexpr bool kSplitGU = MODE == kGateUp && NMAX != kSmallN;
     static constexpr int kGURows = kSplitGU ? 128 : 64;  // intermediate rows per gate/up unit
-    // down: shared-expert units carry the hi and the lo part of h, kShN rows
-    // each, in the B region of NMAX routed rows (or of 2 * kShN rows)
-    static constexpr int kShN = MODE == kDown && NMAX >= 128 ? NMAX / 2 : NMAX;
-    static constexpr int kBRows = MODE == kDown ? (NMAX > 2 * kShN ? NMAX : 2 * kShN) : NMAX;
     // rows per B box: 16 for the streaming shape, 64 for the large shape (fewer
     // TMA instructions per stage; NMAX is a multiple of it)
     static constexpr int kBoxRows = NMAX >= 64 ? 64 : 16;
     static constexpr int kABytes = (kSplitGU ? 2 : 1) * 128 * 128;
-    static constexpr int kBBytes = kBRows * 128;
+    static constexpr int kBBytes = NMAX * 128;
     // large gate/up: the rows of x (B) are gathered by four loader warps with
     // 16-byte cp.async into a ring of their own, deeper than the A ring
     static constexpr bool kLoaders = kSplitGU;
@@ -115,9 +113,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
        const __grid_constant__ CUtensorMap tmBg, GemmArgs a) {
     using C = GemmCfg<MODE, NMAX, STAGES>;
     // small routed gate/up units gather their rows of x (pair_row) with TMA
-    // gather4; large ones read the rows from the pair-ordered copy of x (TMA
-    // gather4 moves about 7 bytes per clock per SM: enough for 32-row tiles,
-    // far too few for 256-row ones)
+    // gather4; large ones with the loader warps (TMA gather4 moves about 7
+    // bytes per clock per SM: enough for 32-row tiles, far too few for larger)
     constexpr bool kGather = MODE == kGateUp && NMAX == kSmallN;
     extern __shared__ uint8_t smem_raw[];
 
@@ -189,13 +186,11 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         int nheld = 0;
         bool waited = !kEarlyA;
         auto issue_b = [&](uint32_t sB, int g, int start, int nbox, int K, int kc, uint64_t* bar) {
+            (void)K;
             constexpr int kBoxBytes = C::kBoxRows * 128;
             const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
             for (int t = 0; t < nbox; ++t)
                 tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, bar);
-            if (MODE == kDown && g == a.E)  // lo part of h: columns K .. 2K-1 of the same rows
-                for (int t = 0; t < nbox; ++t)
-                    tma_load_2d(sB + C::kShN * 128 + t * kBoxBytes, mB, K + kc, start + t * C::kBoxRows, bar);
         };
         auto release_held = [&]() {
             pdl_wait();
@@ -216,12 +211,13 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const bool gathered = kGather && g != a.E;
             const int nb4 = (n + 3) >> 2;
             const int nbox = (n + C::kBoxRows - 1) / C::kBoxRows;
-            const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
+            // K steps: gate/up H; down I (routed) or 2 Is (shared: h = [hi | lo],
+            // A wraps around its Is columns)
+            const int K = MODE == kGateUp ? a.H : (g == a.E ? 2 * a.Is : a.I);
+            const int Ka = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
             const uint32_t bbytes = gathered ? (uint32_t)nb4 * 512u
                                              : (uint32_t)(nbox * C::kBoxRows * 128);
-            // down: the shared expert's units carry the lo part of h as well
-            const int parts = MODE == kDown && g == a.E ? 2 : 1;
-            const uint32_t bytes = (uint32_t)C::kABytes + (C::kLoaders ? 0u : parts * bbytes);
+            const uint32_t bytes = (uint32_t)C::kABytes + (C::kLoaders ? 0u : bbytes);
             if (gathered) {
                 // the unit's rows of x, padded to a multiple of 4 with R (read as zeros);
                 // copies of the previous unit took their coordinates when issued
@@ -258,8 +254,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                             }
                         }
                     } else {
-                        if (g == a.E) tma_load_2d(sA, &tmA2, kc, m * 128, full + stage);
-                        else tma_load_3d(sA, &tmA0, kc, m * 128, g, full + stage);
+                        const int kca = kc % Ka;
+                        if (g == a.E) tma_load_2d(sA, &tmA2, kca, m * 128, full + stage);
+                        else tma_load_3d(sA, &tmA0, kca, m * 128, g, full + stage);
                     }
                     if (!gathered && !C::kLoaders) {
                         if (waited) issue_b(sB, g, start, nbox, K, kc, full + stage);
@@ -303,7 +300,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const int4 un = __ldg(a.units + u);
                 const int g = un.x, n = un.w;
                 const int n16 = (n + 15) & ~15;
-                const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
+                const int K = MODE == kGateUp ? a.H : (g == a.E ? 2 * a.Is : a.I);
                 const uint32_t idesc = idesc_bf16_f32(128, n16);
                 if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
                     give_up();
@@ -330,8 +327,6 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (C::kSplitGU)  // up rows into the second accumulator
                             tc_mma_bf16(d + NMAX, smem_desc_sw128(sA + 128 * 128 + kk * 32), bd, idesc,
                                         (kb | kk) != 0);
-                        if (MODE == kDown && g == a.E)
-                            tc_mma_bf16(d, ad, smem_desc_sw128(sB + C::kShN * 128 + kk * 32), idesc, 1u);
                     }
                     tc_commit(empty + stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -484,15 +479,16 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 __half* xs = reinterpret_cast<__half*>(base + C::kXchgOff);
                 const int hl = q * 32 + lane;
                 for (int c = 0; c < n16; c += 16) {
+                    // the chunk's pair weights first (not reordered across stores)
+                    float wv[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        wv[t] = (g == a.E || c + t >= n) ? 1.0f : __ldg(a.pair_w + start + c + t);
                     float v[16];
                     __syncwarp();  // tcgen05.ld is warp-collective
                     tmem_ld16(tb + (uint32_t)c, v);
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int col = c + t;
-                        const float w = (g == a.E || col >= n) ? 1.0f : __ldg(a.pair_w + start + col);
-                        xs[col * 128 + hl] = __float2half_rn(w * v[t]);
-                    }
+                    for (int t = 0; t < 16; ++t) xs[(c + t) * 128 + hl] = __float2half_rn(wv[t] * v[t]);
                 }
                 tc_fence_before();
                 mbar_arrive(tempty + acc);

@@ -54,7 +54,6 @@ struct ScatterArgs {
     const uint32_t* keep;
     int R, H, E, k, I, Is, nb;
     int nt_gu, nt_dn;   // rows per unit of the gate/up and of the down GEMM
-    int nt_ds;          // rows per shared-expert unit of the down GEMM
     int gu_rows;        // intermediate rows per gate/up unit (64 or 128)
     int32_t* prank;       // [R * k] rank of a pair among its block's pairs of its expert, or -1
     int32_t* hist;        // [nb, E] pairs per (block, expert), then bases within the expert

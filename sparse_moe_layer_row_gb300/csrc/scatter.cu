@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     int p = block_excl_scan_i32(sum, warp_sums, &tot_pairs);
     int cg = block_excl_scan_i32(ch_gu, warp_sums, &tot_gu);
     int cd = block_excl_scan_i32(ch_dn, warp_sums, &tot_dn);
-    const int sch_gu = (a.R + a.nt_gu - 1) / a.nt_gu, sch_dn = (a.R + a.nt_ds - 1) / a.nt_ds;
+    const int sch_gu = (a.R + a.nt_gu - 1) / a.nt_gu, sch_dn = (a.R + a.nt_dn - 1) / a.nt_dn;
     const int base_gu = sch_gu * mt_gs;
     const int base_dn = sch_dn * mt_dn;
     // shared-expert units (group E, all rows): gate/up chunk-major, down tile-major
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     }
     for (int u = tid; u < base_dn; u += blockDim.x) {
         const int m = u / sch_dn, c = u - m * sch_dn;
-        a.units_dn[u] = make_int4(E, m, c * a.nt_ds, min(a.nt_ds, a.R - c * a.nt_ds));
+        a.units_dn[u] = make_int4(E, m, c * a.nt_dn, min(a.nt_dn, a.R - c * a.nt_dn));
     }
     // down units: expert groups of kDownGroup, each group ordered weight-tile
     // major, so the CTAs running at one time write one 128-column slab for
