@@ -136,17 +136,27 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
         const int e = blockIdx.x * (kScanThreads / 32) + (tid >> 5);
         if (e < E) {
             int run = 0;
-            for (int b0 = 0; b0 < nb; b0 += 32) {
-                const int b = b0 + lane;
-                const int h = b < nb ? a.hist[(size_t)b * E + e] : 0;
-                int incl = h;
+            // 8 x 32 blocks per pass; all loads of a pass are issued before its
+            // stores (a load after a store to the same array would wait for it)
+            for (int b00 = 0; b00 < nb; b00 += 256) {
+                int hv[8];
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += t;
+                for (int j = 0; j < 8; ++j) {
+                    const int b = b00 + 32 * j + lane;
+                    hv[j] = b < nb ? a.hist[(size_t)b * E + e] : 0;
                 }
-                if (b < nb) a.hist[(size_t)b * E + e] = run + incl - h;
-                run += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int b = b00 + 32 * j + lane;
+                    int incl = hv[j];
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    if (b < nb) a.hist[(size_t)b * E + e] = run + incl - hv[j];
+                    run += __shfl_sync(0xffffffffu, incl, 31);
+                }
             }
             if (lane == 0) a.count[e] = run;
         }
