@@ -66,8 +66,8 @@ struct GemmCfg {
     // large gate/up: the rows of x (B) are gathered by four loader warps with
     // 16-byte cp.async into a ring of their own, deeper than the A ring
     static constexpr bool kLoaders = kSplitGU;
-    static constexpr int kBStages = kLoaders ? 6 : 0;
-    static constexpr int kBLag = 4;  // stages a loader thread keeps in flight
+    static constexpr int kBStages = kLoaders ? 4 : 0;
+    static constexpr int kBLag = 2;  // stages a loader thread keeps in flight
     static constexpr int kThreads = kLoaders ? 320 : 192;
     static constexpr int kMinBlocks = kLoaders ? 1 : 2;
     static constexpr int kStageBytes = kLoaders ? kABytes : kABytes + kBBytes;  // A ring stride
@@ -552,7 +552,7 @@ static cudaError_t set_attr() {
 // expert (weight streaming: two CTAs per SM, each with its own ring, keep more
 // TMA streams in flight); large = many rows (tensor-core bound, one CTA per SM).
 constexpr int kSmallStagesGU = 5, kSmallStagesDN = 4;
-constexpr int kLargeStagesGU = 4, kLargeStagesDN = 3;
+constexpr int kLargeStagesGU = 5, kLargeStagesDN = 3;
 constexpr int kSmallCtasPerSm = 2;
 
 cudaError_t gemm_set_attributes() {
