@@ -25,11 +25,13 @@
 //            not, and one bf16 part there too would leave almost no margin in
 //            the output tolerance.
 //  down:     A = 128 rows of W_down[e] (hidden outputs), B = rows of h.  For
-//            the shared expert K runs over [hi | lo] (its 2 Is columns of h)
-//            while A wraps around its Is columns: D = W (h_hi + h_lo), with
-//            full-width N tiles (an M = 128 MMA costs about the same for any
-//            N up to 256; measured: 535 cycles per four MMAs at N = 64, 582 at
-//            N = 256).  The epilogue scales by the pair's renormalised weight
+//            the shared expert, D = W (h_hi + h_lo): in the large shape K runs
+//            over [hi | lo] (its 2 Is columns of h) while A wraps around its Is
+//            columns, with full-width N tiles (an M = 128 MMA costs about the
+//            same for any N up to 256; measured: 535 cycles per four MMAs at
+//            N = 64, 582 at N = 256); the streaming shape, bound by weight
+//            bytes, loads both parts in one stage and issues two MMAs per K
+//            step instead (W read once).  The epilogue scales by the pair's renormalised weight
 //            and stages the pair's output row in fp16 (the shared expert with
 //            weight 1, in its own rows); k_combine sums the rows.
 //
@@ -62,7 +64,11 @@ struct GemmCfg {
     // TMA instructions per stage; NMAX is a multiple of it)
     static constexpr int kBoxRows = NMAX >= 64 ? 64 : 16;
     static constexpr int kABytes = (kSplitGU ? 2 : 1) * 128 * 128;
-    static constexpr int kBBytes = NMAX * 128;
+    // down, streaming shape: the shared expert's lo part of h rides in the same
+    // stage as its hi part (a second MMA per K step); the large shape runs the
+    // lo part as further K steps at the full tile width instead
+    static constexpr bool kDualLo = MODE == kDown && NMAX == kSmallN;
+    static constexpr int kBBytes = (kDualLo ? 2 : 1) * NMAX * 128;
     // large gate/up: the rows of x (B) are gathered by four loader warps with
     // 16-byte cp.async into a ring of their own, deeper than the A ring
     static constexpr bool kLoaders = kSplitGU;
@@ -186,11 +192,13 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         int nheld = 0;
         bool waited = !kEarlyA;
         auto issue_b = [&](uint32_t sB, int g, int start, int nbox, int K, int kc, uint64_t* bar) {
-            (void)K;
             constexpr int kBoxBytes = C::kBoxRows * 128;
             const CUtensorMap* mB = g == a.E ? &tmB1 : &tmB0;
             for (int t = 0; t < nbox; ++t)
                 tma_load_2d(sB + t * kBoxBytes, mB, kc, start + t * C::kBoxRows, bar);
+            if (C::kDualLo && g == a.E)  // lo part of h: columns K .. 2K-1 of the same rows
+                for (int t = 0; t < nbox; ++t)
+                    tma_load_2d(sB + NMAX * 128 + t * kBoxBytes, mB, K + kc, start + t * C::kBoxRows, bar);
         };
         auto release_held = [&]() {
             pdl_wait();
@@ -211,13 +219,15 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const bool gathered = kGather && g != a.E;
             const int nb4 = (n + 3) >> 2;
             const int nbox = (n + C::kBoxRows - 1) / C::kBoxRows;
-            // K steps: gate/up H; down I (routed) or 2 Is (shared: h = [hi | lo],
-            // A wraps around its Is columns)
-            const int K = MODE == kGateUp ? a.H : (g == a.E ? 2 * a.Is : a.I);
+            // K steps: gate/up H; down I (routed) or, for the shared expert, Is
+            // (streaming shape: hi and lo in one stage) or 2 Is (h = [hi | lo],
+            // A wrapping around its Is columns)
             const int Ka = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
+            const int K = MODE == kDown && g == a.E && !C::kDualLo ? 2 * a.Is : Ka;
             const uint32_t bbytes = gathered ? (uint32_t)nb4 * 512u
                                              : (uint32_t)(nbox * C::kBoxRows * 128);
-            const uint32_t bytes = (uint32_t)C::kABytes + (C::kLoaders ? 0u : bbytes);
+            const int parts = C::kDualLo && g == a.E ? 2 : 1;
+            const uint32_t bytes = (uint32_t)C::kABytes + (C::kLoaders ? 0u : parts * bbytes);
             if (gathered) {
                 // the unit's rows of x, padded to a multiple of 4 with R (read as zeros);
                 // copies of the previous unit took their coordinates when issued
@@ -300,7 +310,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const int4 un = __ldg(a.units + u);
                 const int g = un.x, n = un.w;
                 const int n16 = (n + 15) & ~15;
-                const int K = MODE == kGateUp ? a.H : (g == a.E ? 2 * a.Is : a.I);
+                const int K = MODE == kGateUp ? a.H
+                                              : (g == a.E ? (C::kDualLo ? a.Is : 2 * a.Is) : a.I);
                 const uint32_t idesc = idesc_bf16_f32(128, n16);
                 if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
                     give_up();
@@ -327,6 +338,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (C::kSplitGU)  // up rows into the second accumulator
                             tc_mma_bf16(d + NMAX, smem_desc_sw128(sA + 128 * 128 + kk * 32), bd, idesc,
                                         (kb | kk) != 0);
+                        if (C::kDualLo && g == a.E)  // shared expert: lo part of h
+                            tc_mma_bf16(d, ad, smem_desc_sw128(sB + NMAX * 128 + kk * 32), idesc, 1u);
                     }
                     tc_commit(empty + stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
