@@ -139,6 +139,22 @@ moe_status moe_block_coreset(const moe_plan* plan, int32_t R, const int32_t* blo
                              int32_t* n_empty, void* workspace, size_t workspace_bytes,
                              moe_stream_t stream);
 
+/* Block coreset under an expert budget.
+ * (InfiniLM PR #604, Summary: preview passes use block coreset routing with an
+ * "expert-budget"; the pages name the budget without defining it.  Reading:
+ * a cap on the number of experts a block keeps.)
+ * As moe_block_coreset, and then at most max_experts experts per block are
+ * kept: the first ones of the same (Q desc, id asc) order.  With tau >= 1 the
+ * budget applies to the touched experts.  The rows keep topk_w bit for bit
+ * only when tau >= 1 and the budget drops nothing; otherwise they are
+ * renormalised as above.
+ *   max_experts  >= 1: the cap; 0: no cap (= moe_block_coreset); < 0 rejected */
+moe_status moe_block_coreset_budget(const moe_plan* plan, int32_t R, const int32_t* block_offsets,
+                                    int32_t nb, const int32_t* topk_idx, const float* topk_w,
+                                    float tau, int32_t max_experts, uint32_t* keep,
+                                    int32_t* core_size, float* w_renorm, int32_t* n_empty,
+                                    void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* Expert evaluation and combine.
  * (Model card, intro: top-8 experts plus a shared expert.)
  *   y[r] = S(x[r]) + sum over slots j of row r whose expert is kept for r's

@@ -45,7 +45,7 @@ def _configure(L):
         L.moe_oracle_route.restype = ctypes.c_long
         L.moe_oracle_route.argtypes = [P, P, P, P, i, i, i, i, i, P, P, P, i]
         L.moe_oracle_coreset.restype = ctypes.c_long
-        L.moe_oracle_coreset.argtypes = [P, i, i, i, i, P, P, ctypes.c_float, P, P, P, P]
+        L.moe_oracle_coreset.argtypes = [P, i, i, i, i, P, P, ctypes.c_float, P, P, P, P, i]
         L.moe_oracle_expert_ffn.restype = None
         L.moe_oracle_expert_ffn.argtypes = [P, P, P, P, i, i, P]
         L.moe_oracle_forward.restype = ctypes.c_int
@@ -102,12 +102,14 @@ def route(x, w_router, block_offsets, k, bias=None, want_logits=False, nthreads=
     return idx, w, z, int(nf)
 
 
-def coreset(block_offsets, topk_idx, topk_w, E, tau):
+def coreset(block_offsets, topk_idx, topk_w, E, tau, max_experts=0):
     """Per-block coreset carrying >= tau of the block's routing mass, then renormalise.
 
     Model card "Clover-35B-A3B-Preview -- CMF", Usage (90% of the block's
-    routing); InfiniLM PR #604, Summary (block coreset routing).
-    Returns (keep uint32 [nb, ceil(E/32)], core_size int32 [nb],
+    routing); InfiniLM PR #604, Summary (block coreset routing; expert budget).
+    max_experts > 0 caps the coreset at that many experts: the first ones of
+    the (mass desc, id asc) order (the pages name the budget only; this is the
+    reading taken).  Returns (keep uint32 [nb, ceil(E/32)], core_size int32 [nb],
     w_renorm fp32 [R,k], n_empty int32 [nb], n_bad_ids).
     """
     off = np.ascontiguousarray(block_offsets, dtype=np.int32)
@@ -121,7 +123,8 @@ def coreset(block_offsets, topk_idx, topk_w, E, tau):
     wr = np.zeros((R, k), np.float32)
     ne = np.zeros(nb, np.int32)
     bad = lib().moe_oracle_coreset(_ptr(off), nb, R, E, k, _ptr(idx), _ptr(w),
-                                   ctypes.c_float(tau), _ptr(keep), _ptr(cs), _ptr(wr), _ptr(ne))
+                                   ctypes.c_float(tau), _ptr(keep), _ptr(cs), _ptr(wr), _ptr(ne),
+                                   int(max_experts))
     if bad < 0:
         raise ValueError("oracle coreset: invalid arguments")
     return keep, cs, wr, ne, int(bad)

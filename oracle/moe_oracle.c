@@ -37,7 +37,10 @@
  *  5. Coreset: tau >= 1 keeps every touched expert and leaves w unchanged.
  *     Otherwise theta = ceil(tau * T) computed exactly (tau is the fp32 value
  *     M * 2^-s), experts ordered by (Q descending, id ascending), and the
- *     coreset is the shortest prefix whose mass reaches theta.
+ *     coreset is the shortest prefix whose mass reaches theta.  An expert
+ *     budget B > 0 (InfiniLM PR #604, Summary, names it without defining it)
+ *     keeps at most the first B experts of that order; when it drops an
+ *     expert with tau >= 1, the rows are renormalised as in 6.
  *  6. Renormalise: per row, s' = sum of surviving w_j in rank order (fp32),
  *     w'_j = w_j / s', 0 for dropped j; a row with s' == 0 keeps only the
  *     shared expert and is counted as empty.
@@ -258,7 +261,7 @@ static uint64_t mass_threshold(float tau, uint64_t T) {
 long moe_oracle_coreset(const int32_t* block_offsets, int nb, int R, int E, int k,
                         const int32_t* topk_idx, const float* topk_w, float tau,
                         uint32_t* keep, int32_t* core_size, float* w_renorm,
-                        int32_t* n_empty) {
+                        int32_t* n_empty, int max_experts) {
     if (!topk_idx || !topk_w || !keep || !core_size || !w_renorm || E <= 0 || k <= 0 ||
         k > E || !check_offsets(block_offsets, nb, R) || !(tau > 0.0f))
         return ORC_ERR_ARG;
@@ -286,8 +289,14 @@ long moe_oracle_coreset(const int32_t* block_offsets, int nb, int R, int E, int 
         uint64_t T = 0;
         for (int e = 0; e < E; ++e)
             if (touched[e]) { order[nt++] = e; T += Q[e]; }
+        /* expert budget (InfiniLM PR #604, Summary: "expert-budget"; reading:
+         * at most max_experts of the block's experts are kept, the first ones of
+         * the same order; max_experts <= 0: no budget) */
+        const int cap = (max_experts > 0 && max_experts < nt) ? max_experts : nt;
+        /* rows keep their weights bit for bit only when nothing is dropped */
+        const int renorm = tau < 1.0f || cap < nt;
         int c;
-        if (tau >= 1.0f) {
+        if (!renorm) {
             c = nt;
             for (int i = 0; i < nt; ++i) in_core[order[i]] = 1;
         } else {
@@ -297,10 +306,15 @@ long moe_oracle_coreset(const int32_t* block_offsets, int nb, int R, int E, int 
                 while (p >= 0 && Q[order[p]] < Q[e]) { order[p + 1] = order[p]; --p; }
                 order[p + 1] = e;
             }
-            uint64_t theta = mass_threshold(tau, T);
-            uint64_t run = 0;
-            c = 0;
-            while (c < nt && run < theta) { run += Q[order[c]]; in_core[order[c]] = 1; ++c; }
+            if (tau >= 1.0f) {
+                c = cap;
+            } else {
+                uint64_t theta = mass_threshold(tau, T);
+                uint64_t run = 0;
+                c = 0;
+                while (c < cap && run < theta) { run += Q[order[c]]; ++c; }
+            }
+            for (int i = 0; i < c; ++i) in_core[order[i]] = 1;
         }
         core_size[b] = c;
         for (int wd = 0; wd < words; ++wd) {
@@ -314,7 +328,7 @@ long moe_oracle_coreset(const int32_t* block_offsets, int nb, int R, int E, int 
             const int32_t* idx = topk_idx + (size_t)r * k;
             const float* w = topk_w + (size_t)r * k;
             float* wo = w_renorm + (size_t)r * k;
-            if (tau >= 1.0f) {
+            if (!renorm) {
                 for (int j = 0; j < k; ++j) wo[j] = w[j];
                 continue;
             }

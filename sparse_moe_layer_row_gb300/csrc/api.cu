@@ -242,17 +242,27 @@ moe_status moe_block_coreset(const moe_plan* p, int32_t R, const int32_t* block_
                              uint32_t* keep, int32_t* core_size, float* w_renorm,
                              int32_t* n_empty, void* workspace, size_t workspace_bytes,
                              moe_stream_t stream) {
+    return moe_block_coreset_budget(p, R, block_offsets, nb, topk_idx, topk_w, tau, 0, keep,
+                                    core_size, w_renorm, n_empty, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_block_coreset_budget(const moe_plan* p, int32_t R, const int32_t* block_offsets,
+                                    int32_t nb, const int32_t* topk_idx, const float* topk_w,
+                                    float tau, int32_t max_experts, uint32_t* keep,
+                                    int32_t* core_size, float* w_renorm, int32_t* n_empty,
+                                    void* workspace, size_t workspace_bytes, moe_stream_t stream) {
     moe_status s = check_call(p, R, block_offsets, nb, workspace, workspace_bytes);
     if (s != MOE_OK) return s;
     if (!(tau > 0.0f)) return fail(MOE_ERR_INVALID_ARG, "tau=%g must be > 0 (and not NaN)", (double)tau);
+    if (max_experts < 0) return fail(MOE_ERR_INVALID_ARG, "max_experts=%d must be >= 0", max_experts);
     if (!topk_idx || !topk_w || !keep || !core_size || !w_renorm)
         return fail(MOE_ERR_INVALID_ARG, "a required coreset pointer is NULL");
     const void* ps[6] = {topk_idx, topk_w, keep, core_size, w_renorm, n_empty};
     for (const void* q : ps)
         if (q && !aligned(q, 4)) return fail(MOE_ERR_INVALID_ARG, "coreset pointer misaligned");
     const Layout L = make_layout(p->d);
-    CoresetArgs a{block_offsets, topk_idx, topk_w, R, p->d.E, p->d.k, nb, tau, keep, core_size,
-                  w_renorm, n_empty, at<uint32_t>(workspace, L.status)};
+    CoresetArgs a{block_offsets, topk_idx, topk_w, R, p->d.E, p->d.k, nb, tau, max_experts, keep,
+                  core_size, w_renorm, n_empty, at<uint32_t>(workspace, L.status)};
     cudaError_t e = launch_coreset(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "coreset launch");
     return ok();

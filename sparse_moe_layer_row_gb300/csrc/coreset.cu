@@ -13,7 +13,10 @@
 //     fp32 encoding and the product formed in 128 bits;
 //   * experts ranked by (Q desc, id asc); the coreset is the shortest prefix
 //     of that order whose mass reaches theta: its size is the number of ranks
-//     whose exclusive prefix mass is still below theta.
+//     whose exclusive prefix mass is still below theta;
+//   * an expert budget B > 0 (InfiniLM PR #604, Summary, names it without
+//     defining it) keeps at most the first B experts of that order; rows are
+//     copied unchanged only when tau >= 1 and nothing is dropped.
 // One CTA per block.
 #include "kernels.cuh"
 
@@ -113,10 +116,12 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
     for (int w = 0; w < words; ++w) nt += __popc(touched[w]);
 
     const bool disabled = !(a.tau < 1.0f);
-    if (disabled) {
+    const int cap = (a.max_experts > 0 && a.max_experts < nt) ? a.max_experts : nt;
+    const bool renorm = !disabled || cap < nt;  // else the rows keep their weights bit for bit
+    if (!renorm) {
         for (int w = tid; w < words; w += blockDim.x) incore[w] = touched[w];
     } else {
-        const uint64_t theta = mass_threshold(a.tau, T);
+        const uint64_t theta = disabled ? ~0ull : mass_threshold(a.tau, T);
         // Order (Q desc, id asc) as one 64-bit key per expert: (Q << 10 | (1023 - e)) + 1
         // for touched experts, 0 otherwise (Q < 2^53: a block has fewer than 2^21 rows).
         for (int e = tid; e < E; e += blockDim.x)
@@ -127,17 +132,27 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
         // An expert is in the coreset iff the mass of the experts ranked above it
         // is still below theta: the greedy prefix in (Q desc, id asc) order stops
         // at the first expert whose inclusion reaches theta.
+        // ... and, under the budget, iff fewer than `cap` experts rank above it
         for (int e = tid; e < E; e += blockDim.x) {
             const unsigned long long ke = keys[e];
             if (!ke) continue;
             unsigned long long above = 0;
+            int rank = 0;
             int f = 0;
             for (; f + 8 <= E; f += 8) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) above += keys[f + j] > ke ? Q[f + j] : 0ull;
+                for (int j = 0; j < 8; ++j) {
+                    const bool gt = keys[f + j] > ke;
+                    above += gt ? Q[f + j] : 0ull;
+                    rank += gt;
+                }
             }
-            for (; f < E; ++f) above += keys[f] > ke ? Q[f] : 0ull;
-            if (above < theta) atomicOr(&incore[e >> 5], 1u << (e & 31));
+            for (; f < E; ++f) {
+                const bool gt = keys[f] > ke;
+                above += gt ? Q[f] : 0ull;
+                rank += gt;
+            }
+            if ((disabled || above < theta) && rank < cap) atomicOr(&incore[e >> 5], 1u << (e & 31));
         }
     }
     __syncthreads();
@@ -152,7 +167,7 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
         const int32_t* idx = a.topk_idx + (size_t)r * k;
         const float* w = a.topk_w + (size_t)r * k;
         float* wo = a.w_renorm + (size_t)r * k;
-        if (disabled) {
+        if (!renorm) {
             for (int j = 0; j < k; ++j) wo[j] = w[j];
             continue;
         }

@@ -41,6 +41,7 @@ struct CoresetArgs {
     const float* topk_w;
     int R, E, k, nb;
     float tau;
+    int max_experts;      // expert budget per block (<= 0: none)
     uint32_t* keep;
     int32_t* core_size;
     float* w_renorm;

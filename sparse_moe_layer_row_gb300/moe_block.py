@@ -66,6 +66,9 @@ def load(build_if_missing: bool = False):
     L.moe_block_route.argtypes = [P, P, i32, P, i32, P, P, P, P, sz, P]
     L.moe_block_coreset.restype = ctypes.c_int
     L.moe_block_coreset.argtypes = [P, i32, P, i32, P, P, ctypes.c_float, P, P, P, P, P, sz, P]
+    L.moe_block_coreset_budget.restype = ctypes.c_int
+    L.moe_block_coreset_budget.argtypes = [P, i32, P, i32, P, P, ctypes.c_float, i32, P, P, P, P, P,
+                                           sz, P]
     L.moe_block_forward.restype = ctypes.c_int
     L.moe_block_forward.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, sz, P]
     L.moe_block_route_noalloc.restype = ctypes.c_int
@@ -210,7 +213,8 @@ def moe_block_route_noalloc(plan: Plan, x, block_offsets, logit_bias, topk_idx, 
 
 
 def moe_block_coreset(plan: Plan, block_offsets, topk_idx, topk_w, tau: float, keep, core_size,
-                      w_renorm, n_empty, workspace, stream=None):
+                      w_renorm, n_empty, workspace, stream=None, max_experts: int = 0):
+    """moe_block_coreset, or moe_block_coreset_budget when max_experts != 0."""
     d = plan.dims
     R = topk_idx.shape[0]
     nb = block_offsets.shape[0] - 1
@@ -223,6 +227,13 @@ def moe_block_coreset(plan: Plan, block_offsets, topk_idx, topk_w, tau: float, k
     if n_empty is not None:
         _need(n_empty, "n_empty", torch.int32, (nb,))
     _need(workspace, "workspace", torch.uint8)
+    if max_experts:
+        _check(load().moe_block_coreset_budget(plan.handle, R, _ptr(block_offsets), nb,
+                                               _ptr(topk_idx), _ptr(topk_w), ctypes.c_float(tau),
+                                               int(max_experts), _ptr(keep), _ptr(core_size),
+                                               _ptr(w_renorm), _ptr(n_empty), _ptr(workspace),
+                                               workspace.numel(), _stream(stream)))
+        return
     _check(load().moe_block_coreset(plan.handle, R, _ptr(block_offsets), nb, _ptr(topk_idx),
                                     _ptr(topk_w), ctypes.c_float(tau), _ptr(keep),
                                     _ptr(core_size), _ptr(w_renorm), _ptr(n_empty),
@@ -293,13 +304,13 @@ class MoeBlockLayer:
         moe_block_route(self.plan, x, block_offsets, bias, idx, w, self.workspace, stream)
         return idx, w
 
-    def coreset(self, block_offsets, topk_idx, topk_w, tau, stream=None):
+    def coreset(self, block_offsets, topk_idx, topk_w, tau, stream=None, max_experts=0):
         R = topk_idx.shape[0]
         nb = block_offsets.shape[0] - 1
         keep, core, empty = self._keep[:nb], self._core[:nb], self._empty[:nb]
         wr = self._w_renorm[:R]
         moe_block_coreset(self.plan, block_offsets, topk_idx, topk_w, tau, keep, core, wr, empty,
-                          self.workspace, stream)
+                          self.workspace, stream, max_experts=max_experts)
         return keep, core, wr, empty
 
     def forward(self, x, block_offsets, topk_idx, w_renorm, keep, y=None, y_f32=None,

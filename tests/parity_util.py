@@ -47,11 +47,11 @@ class Case:
             self.T.ws_up, self.T.ws_down, k=w.k, max_rows=max(self.R, 1), max_blocks=self.nb)
         moe_block.moe_clear_device_status(self.layer.workspace)
 
-    def run(self, tau: float | None = None):
+    def run(self, tau: float | None = None, max_experts: int = 0):
         tau = self.w.tau if tau is None else tau
         L = self.layer
         idx, wt = L.route(self.x, self.off, self.bias)
-        keep, core, wr, empty = L.coreset(self.off, idx, wt, tau)
+        keep, core, wr, empty = L.coreset(self.off, idx, wt, tau, max_experts=max_experts)
         y32 = torch.empty(self.R, self.w.H, dtype=torch.float32, device=self.dev)
         y = L.forward(self.x, self.off, idx, wr, keep, y_f32=y32)
         torch.cuda.synchronize()
@@ -73,10 +73,11 @@ class Case:
         self.ref = dict(idx=idx, w=wt, nonfinite=nf, off=off)
         return self.ref
 
-    def oracle_coreset(self, tau=None):
+    def oracle_coreset(self, tau=None, max_experts: int = 0):
         tau = self.w.tau if tau is None else tau
         r = self.ref
-        keep, core, wr, empty, bad = oracle.coreset(r["off"], r["idx"], r["w"], self.w.E, tau)
+        keep, core, wr, empty, bad = oracle.coreset(r["off"], r["idx"], r["w"], self.w.E, tau,
+                                                    max_experts=max_experts)
         r.update(keep=keep, core=core, wr=wr, empty=empty)
         return r
 

@@ -28,7 +28,10 @@ MUTATIONS = {
     "weights_not_normalised": ("w[j] = a[j] / S;", "w[j] = a[j];"),
     "coreset_ascending_mass": ("Q[order[p]] < Q[e]", "Q[order[p]] > Q[e]"),
     "threshold_floor": ("if ((q << s) != prod) q += 1;", ";"),
-    "threshold_strict": ("while (c < nt && run < theta)", "while (c < nt && run <= theta)"),
+    "threshold_strict": ("while (c < cap && run < theta)", "while (c < cap && run <= theta)"),
+    "budget_off_by_one": ("? max_experts : nt;", "? max_experts + 1 : nt;"),
+    "budget_ignored_without_tau": ("const int renorm = tau < 1.0f || cap < nt;",
+                                   "const int renorm = tau < 1.0f;"),
     "renorm_over_all_slots": ("if (idx[j] >= 0 && idx[j] < E && in_core[idx[j]]) s = s + w[j];",
                               "s = s + w[j];"),
     "disabled_redivides": ("for (int j = 0; j < k; ++j) wo[j] = w[j];\n                continue;",
@@ -52,7 +55,9 @@ PINS = [
     pins.test_coreset_threshold_is_ceiling, pins.test_coreset_disabled_is_plain_topk,
     pins.test_expert_ffn_hand_value, pins.test_expert_ffn_matches_dense_fp64,
     pins.test_forward_matches_dense_moe_fp64,
-] + [lambda m, s=s: pins.test_coreset_brute_force_random_tiny(m, s) for s in range(4)]
+    pins.test_coreset_budget_hand_example,
+] + [lambda m, s=s: pins.test_coreset_brute_force_random_tiny(m, s) for s in range(4)] \
+  + [lambda m, s=s: pins.test_coreset_budget_brute_force_random_tiny(m, s) for s in range(4)]
 
 
 def _build_mutant(name: str, tmp: str) -> str:

@@ -354,6 +354,80 @@ def test_coreset_brute_force_random_tiny(oracle_mod, seed):
             assert abs(float(wr[r].astype(np.float64).sum()) - 1.0) <= k * 2.0 ** -23
 
 
+def _random_tiny_blocks(rng):
+    E = int(rng.integers(4, 21))
+    k = int(rng.integers(1, min(E, 6) + 1))
+    nb = int(rng.integers(1, 4))
+    rows = [int(rng.integers(1, 9)) for _ in range(nb)]
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    R = int(off[-1])
+    idx = np.zeros((R, k), np.int32)
+    wt = np.zeros((R, k), np.float32)
+    for r in range(R):
+        idx[r] = rng.choice(E, size=k, replace=False)
+        a = np.sort(rng.random(k).astype(np.float32))[::-1] + np.float32(0.01)
+        wt[r] = (a / a.sum()).astype(np.float32)
+    return E, k, nb, off, idx, wt
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_coreset_budget_brute_force_random_tiny(oracle_mod, seed):
+    """Expert budget B: the kept set has size min(c, B) (c = the minimal size
+    reaching theta, by brute force) and the largest mass of any set of that
+    size (brute force), ties to lower ids; rows renormalised over it."""
+    rng = np.random.default_rng(100 + seed)
+    E, k, nb, off, idx, wt = _random_tiny_blocks(rng)
+    tau = float(np.float32(rng.choice([0.5, 0.75, 0.9, 0.999, 1.0])))
+    B = int(rng.integers(1, E + 1))
+    keep, cs, wr, ne, bad = oracle_mod.coreset(off, idx, wt, E, tau, max_experts=B)
+    for b in range(nb):
+        Q, touched = _masses(idx, wt, off[b], off[b + 1], E)
+        items = sorted(touched)
+        if tau < 1.0:
+            cmin, _ = _brute_min_size(Q, touched, _theta(tau, sum(Q)))
+        else:
+            cmin = len(items)
+        size = min(cmin, B)
+        best = max(sum(Q[e] for e in sub) for sub in itertools.combinations(items, size))
+        core = [e for e in range(E) if keep[b, e // 32] >> (e % 32) & 1]
+        assert cs[b] == len(core) == size
+        assert sum(Q[e] for e in core) == best
+        # among the sets of that mass, the one preferring lower ids at equal mass
+        order = sorted(touched, key=lambda e: (-Q[e], e))
+        assert core == sorted(order[:size])
+        renorm = tau < 1.0 or size < len(items)
+        for r in range(off[b], off[b + 1]):
+            if not renorm:
+                assert np.array_equal(wr[r].view(np.uint32), wt[r].view(np.uint32))
+                continue
+            surv = [j for j in range(k) if idx[r, j] in core]
+            s = np.float32(0)
+            for j in surv:
+                s = np.float32(s + wt[r, j])
+            for j in range(k):
+                expect = np.float32(wt[r, j] / s) if (j in surv and s > 0) else np.float32(0)
+                assert wr[r, j] == expect
+
+
+def test_coreset_budget_hand_example(oracle_mod):
+    """Hand-worked block (masses Q0 = 2^32 > Q1 = Q2 = 2^31, see below): budget 1
+    keeps expert 0 only; with tau = 1 and budget 2 experts {0, 1} (equal masses
+    go to the lower id) and the rows are renormalised; budget 0 or 3 changes
+    nothing."""
+    idx = np.array([[0, 1], [0, 2]], np.int32)
+    wt = np.full((2, 2), 0.5, np.float32)
+    off = [0, 2]
+    keep, cs, wr, ne, _ = oracle_mod.coreset(off, idx, wt, 3, 0.75, max_experts=1)
+    assert cs[0] == 1 and keep[0, 0] == 0b001
+    assert np.array_equal(wr, np.array([[1, 0], [1, 0]], np.float32))
+    keep, cs, wr, ne, _ = oracle_mod.coreset(off, idx, wt, 3, 1.0, max_experts=2)
+    assert cs[0] == 2 and keep[0, 0] == 0b011
+    assert np.array_equal(wr, np.array([[0.5, 0.5], [1, 0]], np.float32))
+    for B in (0, 3):
+        keep, cs, wr, ne, _ = oracle_mod.coreset(off, idx, wt, 3, 1.0, max_experts=B)
+        assert cs[0] == 3 and keep[0, 0] == 0b111 and np.array_equal(wr, wt)
+
+
 def test_coreset_threshold_hand_example(oracle_mod):
     """Hand-worked block: 2 rows, k = 2, weights 0.5 (q = 2^31 each).
     Row 0 -> experts {0, 1}, row 1 -> {0, 2}: Q0 = 2^32, Q1 = Q2 = 2^31, T = 2^33.
