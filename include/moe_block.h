@@ -173,6 +173,30 @@ moe_status moe_block_forward(const moe_plan* plan, const void* x, int32_t R,
                              const float* w_renorm, const uint32_t* keep, void* y, float* y_f32,
                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* Live-row reuse (InfiniLM pull 604 "Clover MoE": Summary, Motivation and the
+ * benchmark table's "expert budget/live reuse" rows).  The pages name live-row
+ * reuse with a refresh interval of five passes and define neither the live
+ * set nor the reuse; the reading taken here: between refreshes, a denoising
+ * pass recomputes the MoE output of the rows still live (positions not yet
+ * resolved) and keeps the cached output of the others.  The refresh policy
+ * (a full moe_block_forward every fifth pass) belongs to the caller.
+ *   live  [R] uint8 device: row r is evaluated iff live[r] != 0; NULL = every
+ *         row (then this is moe_block_forward).
+ * For a live row r, y[r] (and y_f32[r]) is what moe_block_forward writes, bit
+ * for bit, given the same keep mask.  For a dead row, y[r] and y_f32[r] are
+ * not written: they hold whatever the caller left there (the cached output).
+ * Dead rows contribute no (row, expert) pair and are not fed to the shared
+ * expert, so a pass with few live rows streams only the experts their pairs
+ * touch (plus the shared expert).  keep is not recomputed: pass the coreset
+ * the caller wants (e.g. one computed over the live rows only).  Other
+ * arguments, errors and the workspace are those of moe_block_forward. */
+moe_status moe_block_forward_live(const moe_plan* plan, const void* x, int32_t R,
+                                  const int32_t* block_offsets, int32_t nb,
+                                  const int32_t* topk_idx, const float* w_renorm,
+                                  const uint32_t* keep, const uint8_t* live, void* y,
+                                  float* y_f32, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream);
+
 /* Router for callers that cannot allocate device memory (no counterpart on the
  * pages: an addition for deployment).  Some callers cannot hand the library a
  * workspace, e.g. an engine that reserves all of its device memory up front,

@@ -210,6 +210,22 @@ def forward(x, block_offsets, topk_idx, w_renorm, keep, experts, shared, E, rows
     return y
 
 
+def forward_live(x, block_offsets, topk_idx, w_renorm, keep, experts, shared, E, live, y_cached,
+                 nthreads=1):
+    """One live-row pass (InfiniLM PR #604, Summary and Motivation: live-row
+    reuse with a refresh interval of five, neither defined there).  Reading:
+    rows with live[r] != 0 get the expert FFN output of ``forward`` under the
+    given keep mask; the others keep their cached output ``y_cached[r]``."""
+    live = np.asarray(live)
+    y = np.array(y_cached, dtype=np.float64, copy=True)
+    rows = [int(r) for r in np.flatnonzero(live)]
+    if rows:
+        yl = forward(x, block_offsets, topk_idx, w_renorm, keep, experts, shared, E, rows=rows,
+                     nthreads=nthreads)
+        y[rows] = yl[rows]
+    return y
+
+
 def surviving_experts(topk_idx, keep, block_offsets, E):
     """Sorted list of experts used by at least one surviving (row, slot) pair."""
     mask = keep_mask(np.asarray(keep), E)

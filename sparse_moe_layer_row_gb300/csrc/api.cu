@@ -272,6 +272,15 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
                              const int32_t* block_offsets, int32_t nb, const int32_t* topk_idx,
                              const float* w_renorm, const uint32_t* keep, void* y, float* y_f32,
                              void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    return moe_block_forward_live(p, x, R, block_offsets, nb, topk_idx, w_renorm, keep, nullptr, y,
+                                  y_f32, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_block_forward_live(const moe_plan* p, const void* x, int32_t R,
+                                  const int32_t* block_offsets, int32_t nb, const int32_t* topk_idx,
+                                  const float* w_renorm, const uint32_t* keep, const uint8_t* live,
+                                  void* y, float* y_f32, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream) {
     moe_status s = check_call(p, R, block_offsets, nb, workspace, workspace_bytes);
     if (s != MOE_OK) return s;
     if (!x || !aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
@@ -296,7 +305,9 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
                    at<int4>(workspace, L.units_gu), at<int4>(workspace, L.units_dn),
                    at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
                    at<int32_t>(workspace, L.inv),
-                   at<uint32_t>(workspace, L.status)};
+                   at<uint32_t>(workspace, L.status),
+                   live, at<int32_t>(workspace, L.shared_rows), at<int32_t>(workspace, L.shared_inv),
+                   at<int32_t>(workspace, L.live_base)};
     GemmMaps gu{}, dn{};
     const auto L2A = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
     gu.a0 = p->tm_wg; gu.a1 = p->tm_wu; gu.a2 = p->tm_sg; gu.a3 = p->tm_su;
@@ -313,7 +324,8 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
                 d.Is, R, static_cast<const __nv_bfloat16*>(x), at<__nv_bfloat16>(workspace, L.h),
                 at<__nv_bfloat16>(workspace, L.hs),
                 at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
-                at<__half>(workspace, L.ys), (int)L.max_pairs, at<uint32_t>(workspace, L.status)};
+                at<__half>(workspace, L.ys), (int)L.max_pairs, at<uint32_t>(workspace, L.status),
+                live ? at<int32_t>(workspace, L.shared_rows) : nullptr};
     // Under stream capture an event record must be an external node to be
     // recorded at every graph launch (a plain record only orders the capture).
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -337,7 +349,7 @@ moe_status moe_block_forward(const moe_plan* p, const void* x, int32_t R,
     if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
     CombineArgs ca{at<__half>(workspace, L.ys), at<int32_t>(workspace, L.inv), R, d.H, d.k,
                    (int)L.max_pairs, static_cast<__nv_bfloat16*>(y), y_f32,
-                   at<uint32_t>(workspace, L.status)};
+                   at<uint32_t>(workspace, L.status), live, at<int32_t>(workspace, L.shared_inv)};
     if ((e = mark(3)) == cudaSuccess) e = launch_combine(ca, p->num_sms, st);
     if (e == cudaSuccess) e = mark(4);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");

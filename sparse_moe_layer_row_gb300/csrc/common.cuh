@@ -34,6 +34,9 @@ struct Layout {
     size_t h;            // bf16 [max_pairs, I]       routed SwiGLU activations
     size_t hs;           // bf16 [max_rows, 2Is]      shared-expert activations, hi | lo
     size_t inv;          // int32 [max_pairs]         staging row of each (row, slot)
+    size_t shared_rows;  // int32 [max_rows]          live rows in order (the shared expert's rows)
+    size_t shared_inv;   // int32 [max_rows]          index of a row in shared_rows, or -1 (dead)
+    size_t live_base;    // int32 [max_blocks]        live rows of a block, then rows before it
     size_t ys;           // fp16 [max_pairs + max_rows, H] staged per-pair and shared outputs
     size_t total;
     int64_t max_pairs, max_units_gu, max_units_dn;
@@ -76,6 +79,9 @@ inline Layout make_layout(const moe_dims& d) {
     L.h = take(2 * (size_t)(P * d.I));
     L.hs = take(2 * (size_t)(R * 2 * d.Is));
     L.inv = take(sizeof(int32_t) * (size_t)P);
+    L.shared_rows = take(sizeof(int32_t) * (size_t)R);
+    L.shared_inv = take(sizeof(int32_t) * (size_t)R);
+    L.live_base = take(sizeof(int32_t) * (size_t)d.max_blocks);
     L.ys = take(2 * (size_t)(P + R) * (size_t)H);
     L.total = o;
     return L;

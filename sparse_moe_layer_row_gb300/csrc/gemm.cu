@@ -216,7 +216,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             // B rows actually loaded: gathered units load ceil(n/4) rows x 4; the
             // others whole boxes of kBoxRows.  Rows of the tile past n only feed
             // output columns that are never read, so they need not be loaded.
-            const bool gathered = kGather && g != a.E;
+            // gathered: routed rows (pair_row), and the shared expert's rows when
+            // only some rows are live (shared_rows)
+            const bool gathered = kGather && (g != a.E || a.shared_rows != nullptr);
             const int nb4 = (n + 3) >> 2;
             const int nbox = (n + C::kBoxRows - 1) / C::kBoxRows;
             // K steps: gate/up H; down I (routed) or, for the shared expert, Is
@@ -232,8 +234,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 // the unit's rows of x, padded to a multiple of 4 with R (read as zeros);
                 // copies of the previous unit took their coordinates when issued
                 __syncwarp();
+                const int32_t* rl = g == a.E ? a.shared_rows : a.pair_row;
                 for (int i = lane; i < nb4 * 4; i += 32)
-                    s_rows[i] = i < n ? __ldg(a.pair_row + start + i) : a.R;
+                    s_rows[i] = i < n ? __ldg(rl + start + i) : a.R;
                 __syncwarp();
             }
             for (int kb = 0; kb < (K >> 6); ++kb) {
@@ -374,7 +377,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 #pragma unroll
             for (int j = 0; j < kRowsPerThread; ++j) {
                 const int i = j * 16 + lw * 4 + r4;
-                const int row = i < n ? (g == a.E ? start + i : __ldg(a.pair_row + start + i)) : -1;
+                const int row = i >= n ? -1
+                              : g != a.E ? __ldg(a.pair_row + start + i)
+                              : (a.shared_rows ? __ldg(a.shared_rows + start + i) : start + i);
                 src[j] = row >= 0 ? a.x + (size_t)row * a.H + ch * 8 : nullptr;
             }
             for (int kb = 0; kb < (a.H >> 6); ++kb) {

@@ -67,6 +67,11 @@ struct ScatterArgs {
     float* pair_w;
     int32_t* inv;         // [R * k] staging row of (row, slot), or -1
     uint32_t* status;
+    // live-row reuse: only rows with live[r] != 0 are evaluated (NULL: all rows)
+    const uint8_t* live;
+    int32_t* shared_rows; // [R] the live rows in order: the shared expert's rows
+    int32_t* shared_inv;  // [R] position of a row in shared_rows, or -1 (dead)
+    int32_t* live_base;   // [nb] live rows per block, then live rows before the block
 };
 // y[r] = shared output + sum over surviving slots (rank order) of staged outputs
 struct CombineArgs {
@@ -76,6 +81,8 @@ struct CombineArgs {
     __nv_bfloat16* y;
     float* y_f32;
     uint32_t* status;
+    const uint8_t* live;         // rows with live[r] == 0 are left as they are (NULL: all live)
+    const int32_t* shared_inv;   // [R] staging index of a row's shared output (NULL: r)
 };
 struct GemmArgs {
     const int4* units;
@@ -90,6 +97,7 @@ struct GemmArgs {
     __half* ys;           // [max_pairs + max_rows, H] staged outputs (down GEMM)
     int shared_row0;      // staging row of the shared expert's row 0
     uint32_t* status;
+    const int32_t* shared_rows;  // row of x of the shared expert's i-th row (NULL: i)
 };
 struct GemmMaps {
     CUtensorMap a0, a1, a2, a3, b0, b1;

@@ -76,14 +76,14 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_hist(ScatterArgs a) {
     pdl_trigger();
     __shared__ uint8_t s_slot[kHistRows][kMaxExperts];
     __shared__ int s_run[kMaxExperts];
-    __shared__ int s_dup;
+    __shared__ int s_dup, s_live;
     const int b = blockIdx.x, tid = threadIdx.x;
     const int E = a.E, k = a.k;
     const int words = (E + 31) >> 5;
     int r0 = a.off[b], r1 = a.off[b + 1];
     if (!(0 <= r0 && r0 <= r1 && r1 <= a.R)) r1 = r0 = 0;  // counted by the coreset call
     for (int e = tid; e < E; e += blockDim.x) s_run[e] = 0;
-    if (tid == 0) s_dup = 0;
+    if (tid == 0) { s_dup = 0; s_live = 0; }
     if (b == 0 && tid == 0) a.misc[0] = 0;  // ticket of k_scatter_scan (next launch)
     for (int c0 = r0; c0 < r1; c0 += kHistRows) {
         const int nr = min(kHistRows, r1 - c0);
@@ -92,11 +92,13 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_hist(ScatterArgs a) {
         __syncthreads();
         for (int rr = tid; rr < nr; rr += blockDim.x) {
             const int r = c0 + rr;
+            const bool lv = !a.live || a.live[r] != 0;  // dead rows: no pairs
+            if (lv) atomicAdd(&s_live, 1);
             int dup = 0;
             for (int j = 0; j < k; ++j) {
                 const int e = a.topk_idx[(size_t)r * k + j];
                 a.prank[(size_t)r * k + j] = -1;
-                if (e < 0 || e >= E) continue;
+                if (!lv || e < 0 || e >= E) continue;
                 if (!((a.keep[(size_t)b * words + (e >> 5)] >> (e & 31)) & 1u)) continue;
                 if (s_slot[rr][e] != 0xFF) { ++dup; continue; }
                 s_slot[rr][e] = (uint8_t)j;
@@ -116,7 +118,10 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_hist(ScatterArgs a) {
     }
     __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) a.hist[(size_t)b * E + e] = s_run[e];
-    if (tid == 0) status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)s_dup);
+    if (tid == 0) {
+        a.live_base[b] = s_live;
+        status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)s_dup);
+    }
 }
 
 constexpr int kScanThreads = 256;
@@ -169,8 +174,22 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    // ---- last CTA: expert offsets and the unit lists
+    // ---- last CTA: live rows before each block, expert offsets and the unit lists
     for (int f = tid; f < E; f += blockDim.x) s_tot[f] = __ldcg(a.count + f);
+    int nl;  // live rows: the shared expert's rows
+    {
+        const int per_b = (nb + blockDim.x - 1) / blockDim.x;
+        const int b0 = min(nb, tid * per_b), b1 = min(nb, b0 + per_b);
+        int cnt = 0;
+        for (int b = b0; b < b1; ++b) cnt += __ldcg(a.live_base + b);
+        int run = block_excl_scan_i32(cnt, warp_sums, &nl);
+        for (int b = b0; b < b1; ++b) {
+            const int c = __ldcg(a.live_base + b);
+            a.live_base[b] = run;
+            run += c;
+        }
+        if (!a.live) nl = a.R;  // every row: the shared expert's rows are 0 .. R-1
+    }
     __syncthreads();
     const int mt_gu = (a.I + a.gu_rows - 1) / a.gu_rows, mt_gs = (a.Is + a.gu_rows - 1) / a.gu_rows;
     const int mt_dn = a.H / 128;
@@ -186,17 +205,17 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     int p = block_excl_scan_i32(sum, warp_sums, &tot_pairs);
     int cg = block_excl_scan_i32(ch_gu, warp_sums, &tot_gu);
     int cd = block_excl_scan_i32(ch_dn, warp_sums, &tot_dn);
-    const int sch_gu = (a.R + a.nt_gu - 1) / a.nt_gu, sch_dn = (a.R + a.nt_dn - 1) / a.nt_dn;
+    const int sch_gu = (nl + a.nt_gu - 1) / a.nt_gu, sch_dn = (nl + a.nt_dn - 1) / a.nt_dn;
     const int base_gu = sch_gu * mt_gs;
     const int base_dn = sch_dn * mt_dn;
     // shared-expert units (group E, all rows): gate/up chunk-major, down tile-major
     for (int u = tid; u < base_gu; u += blockDim.x) {
         const int c = u / mt_gs, m = u - c * mt_gs;
-        a.units_gu[u] = make_int4(E, m, c * a.nt_gu, min(a.nt_gu, a.R - c * a.nt_gu));
+        a.units_gu[u] = make_int4(E, m, c * a.nt_gu, min(a.nt_gu, nl - c * a.nt_gu));
     }
     for (int u = tid; u < base_dn; u += blockDim.x) {
         const int m = u / sch_dn, c = u - m * sch_dn;
-        a.units_dn[u] = make_int4(E, m, c * a.nt_dn, min(a.nt_dn, a.R - c * a.nt_dn));
+        a.units_dn[u] = make_int4(E, m, c * a.nt_dn, min(a.nt_dn, nl - c * a.nt_dn));
     }
     // down units: expert groups of kDownGroup, each group ordered weight-tile
     // major, so the CTAs running at one time write one 128-column slab for
@@ -239,10 +258,25 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
 __global__ void __launch_bounds__(kScatThreads) k_scatter_place(ScatterArgs a) {
     pdl_wait();  // see common.cuh: nothing global is touched before
     pdl_trigger();
+    __shared__ int warp_sums[32];
     const int b = blockIdx.x;
     const int E = a.E, k = a.k;
     int r0 = a.off[b], r1 = a.off[b + 1];
     if (!(0 <= r0 && r0 <= r1 && r1 <= a.R)) r1 = r0 = 0;
+    // the block's live rows, in order, after the live rows of earlier blocks
+    // (a.live is the same for the whole block, so the scans are block-uniform)
+    int run = a.live ? a.live_base[b] : 0;
+    for (int c0 = r0; a.live && c0 < r1; c0 += blockDim.x) {
+        const int r = c0 + threadIdx.x;
+        const int lv = (r < r1 && (!a.live || a.live[r] != 0)) ? 1 : 0;
+        int n;
+        const int pos = run + block_excl_scan_i32(lv, warp_sums, &n);
+        if (r < r1) {
+            a.shared_inv[r] = lv ? pos : -1;
+            if (lv) a.shared_rows[pos] = r;
+        }
+        run += n;
+    }
     for (int p = r0 * k + threadIdx.x; p < r1 * k; p += blockDim.x) {
         const int rk = a.prank[p];
         if (rk < 0) {
@@ -270,16 +304,28 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
     __shared__ uint8_t s_slot[kSmallRows][kMaxExperts];   // slot of expert e in row r, or 0xFF
     __shared__ int s_cnt[kMaxExperts];
     __shared__ int warp_sums[32];
-    __shared__ int s_dup;
+    __shared__ int s_dup, s_nl;
     const int tid = threadIdx.x;
     const int E = a.E, k = a.k, R = a.R;
     const int words = (E + 31) >> 5;
     for (int i = tid; i < R * E; i += blockDim.x) s_slot[i / E][i % E] = 0xFF;
     if (tid == 0) s_dup = 0;
+    if (tid < 32) {  // live rows in order (R <= 32): the shared expert's rows
+        const bool lv = tid < R && (!a.live || a.live[tid] != 0);
+        const uint32_t m = __ballot_sync(0xffffffffu, lv);
+        const int pos = __popc(m & ((1u << tid) - 1u));
+        if (tid < R) {
+            a.shared_inv[tid] = lv ? pos : -1;
+            if (lv) a.shared_rows[pos] = tid;
+        }
+        if (tid == 0) s_nl = __popc(m);
+    }
     __syncthreads();
-    // one thread per row: mark its surviving slots (first slot wins)
+    const int nl = s_nl;
+    // one thread per row: mark its surviving slots (first slot wins); dead rows none
     for (int r = tid; r < R; r += blockDim.x) {
         const int b = find_block(a.off, a.nb, r);
+        const bool lv = !a.live || a.live[r] != 0;
         int dup = 0;
         int ids[32];
 #pragma unroll
@@ -288,7 +334,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
         for (int j = 0; j < k; ++j) {
             a.inv[(size_t)r * k + j] = -1;
             const int e = ids[j];
-            if (e < 0 || e >= E) continue;
+            if (!lv || e < 0 || e >= E) continue;
             if (!((a.keep[(size_t)b * words + (e >> 5)] >> (e & 31)) & 1u)) continue;
             if (s_slot[r][e] != 0xFF) { ++dup; continue; }
             s_slot[r][e] = (uint8_t)j;
@@ -315,11 +361,11 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
     int cc = block_excl_scan_i32(ch, warp_sums, &tot_ch);
     const int mt_gu = (a.I + a.gu_rows - 1) / a.gu_rows, mt_gs = (a.Is + a.gu_rows - 1) / a.gu_rows;
     const int mt_dn = a.H / 128;
-    const int s_chunks = (R + a.nt_gu - 1) / a.nt_gu;   // nt_gu == nt_dn here
+    const int s_chunks = (nl + a.nt_gu - 1) / a.nt_gu;   // nt_gu == nt_dn here
     const int base_gu = s_chunks * mt_gs, base_dn = s_chunks * mt_dn;
     if (tid == 0) {
-        write_units(a.units_gu, 0, E, 0, R, a.nt_gu, mt_gs);
-        write_units(a.units_dn, 0, E, 0, R, a.nt_dn, mt_dn);
+        write_units(a.units_gu, 0, E, 0, nl, a.nt_gu, mt_gs);
+        write_units(a.units_dn, 0, E, 0, nl, a.nt_dn, mt_dn);
     }
     for (int f = e0; f < e1; ++f) {
         const int n = s_cnt[f];
@@ -349,7 +395,8 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
 }
 
 // One warp per (row, 256 columns): y = staged shared output + the row's staged
-// expert outputs, added in fp32 in rank order (shared first, then the slots);
+// expert outputs, added in fp32 in rank order (shared first, then the slots;
+// dead rows of a live-row call are skipped);
 // lane owns 8 consecutive columns.  All of a task's contributions are loaded
 // before they are added, eight at a time, so the loads overlap.
 __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
@@ -362,12 +409,14 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
     const int ntasks = a.R * nchunk;
     for (int t = warp; t < ntasks; t += nwarps) {
         const int r = t / nchunk;
+        if (a.live && a.live[r] == 0) continue;  // dead row: its y stays as it is
         const int c = (t - r * nchunk) * 256 + lane * 8;
         const int pos = lane < a.k ? a.inv[(size_t)r * a.k + lane] : -1;
+        const int srow = a.live ? a.shared_inv[r] : r;  // staging row of the shared output
         float acc[8];
         {
             const uint4 v =
-                *reinterpret_cast<const uint4*>(a.ys + (size_t)(a.shared_row0 + r) * a.H + c);
+                *reinterpret_cast<const uint4*>(a.ys + (size_t)(a.shared_row0 + srow) * a.H + c);
             const __half2* hv = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {

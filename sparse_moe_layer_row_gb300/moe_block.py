@@ -71,6 +71,8 @@ def load(build_if_missing: bool = False):
                                            sz, P]
     L.moe_block_forward.restype = ctypes.c_int
     L.moe_block_forward.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, sz, P]
+    L.moe_block_forward_live.restype = ctypes.c_int
+    L.moe_block_forward_live.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, P, sz, P]
     L.moe_block_route_noalloc.restype = ctypes.c_int
     L.moe_block_route_noalloc.argtypes = [P, P, i32, P, i32, P, P, P, P]
     L.moe_plan_set_forward_events.restype = ctypes.c_int
@@ -241,7 +243,9 @@ def moe_block_coreset(plan: Plan, block_offsets, topk_idx, topk_w, tau: float, k
 
 
 def moe_block_forward(plan: Plan, x, block_offsets, topk_idx, w_renorm, keep, y, y_f32, workspace,
-                      stream=None):
+                      stream=None, live=None):
+    """Expert FFN of the pass.  ``live`` (uint8 [R], or None for every row)
+    selects the rows evaluated; the others keep what ``y`` / ``y_f32`` hold."""
     d = plan.dims
     R = x.shape[0]
     nb = block_offsets.shape[0] - 1
@@ -254,6 +258,13 @@ def moe_block_forward(plan: Plan, x, block_offsets, topk_idx, w_renorm, keep, y,
     if y_f32 is not None:
         _need(y_f32, "y_f32", torch.float32, (R, d.H))
     _need(workspace, "workspace", torch.uint8)
+    if live is not None:
+        _need(live, "live", torch.uint8, (R,))
+        _check(load().moe_block_forward_live(plan.handle, _ptr(x), R, _ptr(block_offsets), nb,
+                                             _ptr(topk_idx), _ptr(w_renorm), _ptr(keep),
+                                             _ptr(live), _ptr(y), _ptr(y_f32), _ptr(workspace),
+                                             workspace.numel(), _stream(stream)))
+        return
     _check(load().moe_block_forward(plan.handle, _ptr(x), R, _ptr(block_offsets), nb,
                                     _ptr(topk_idx), _ptr(w_renorm), _ptr(keep), _ptr(y),
                                     _ptr(y_f32), _ptr(workspace), workspace.numel(),
@@ -270,6 +281,17 @@ def moe_read_device_status(workspace: torch.Tensor, stream=None) -> dict:
 def moe_clear_device_status(workspace: torch.Tensor, stream=None):
     _need(workspace, "workspace", torch.uint8)
     _check(load().moe_clear_device_status(_ptr(workspace), _stream(stream)))
+
+
+def live_pass_mask(pass_index: int, live, refresh: int = 5):
+    """Live-row reuse schedule (InfiniLM PR #604, Summary and Motivation: refresh
+    interval five).  Pass 0 and every ``refresh``-th pass after it evaluate every
+    row (returns None); the passes between evaluate the rows of ``live`` only."""
+    if refresh < 1:
+        raise ValueError("refresh interval must be >= 1")
+    if pass_index < 0:
+        raise ValueError("pass index must be >= 0")
+    return None if pass_index % refresh == 0 else live
 
 
 class MoeBlockLayer:
@@ -314,11 +336,11 @@ class MoeBlockLayer:
         return keep, core, wr, empty
 
     def forward(self, x, block_offsets, topk_idx, w_renorm, keep, y=None, y_f32=None,
-                stream=None):
+                stream=None, live=None):
         R = x.shape[0]
         y = self._y[:R] if y is None else y
         moe_block_forward(self.plan, x, block_offsets, topk_idx, w_renorm, keep, y, y_f32,
-                          self.workspace, stream)
+                          self.workspace, stream, live=live)
         return y
 
     def __call__(self, x, block_offsets, tau: float, bias=None, y=None, y_f32=None, stream=None):

@@ -98,7 +98,7 @@ def normal_bf16(seed: int, tensor_id: int, shape, sigma: float, device="cpu",
 
 
 # Tensor ids inside one seed's family of streams.
-TID_X, TID_WR, TID_WG, TID_WU, TID_WD, TID_SG, TID_SU, TID_SD, TID_PERM = range(1, 10)
+TID_X, TID_WR, TID_WG, TID_WU, TID_WD, TID_SG, TID_SU, TID_SD, TID_PERM, TID_LIVE = range(1, 11)
 
 
 @dataclass(frozen=True)
@@ -239,6 +239,15 @@ def zipf_bias(w: Workload, nb: int | None = None, seed: int | None = None) -> to
         order = torch.argsort(key, stable=True)
         bias[b, order] = logp.to(torch.float32)
     return bias
+
+
+def live_rows(R: int, frac: float, seed: int, device="cpu") -> torch.Tensor:
+    """uint8 [R] row mask for live-row passes: row r is live (1) iff the top 53
+    bits of word a of element r of stream (seed, TID_LIVE), as a fraction in
+    [0, 1), fall below ``frac``."""
+    a, _ = uniform_words(seed, TID_LIVE, 0, R)
+    u = _lsr(a, 11).to(torch.float64) * (2.0 ** -53)
+    return (u < frac).to(torch.uint8).to(device)
 
 
 def make_tensors(w: Workload, device="cpu", x_seed: int | None = None) -> Tensors:

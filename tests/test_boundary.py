@@ -123,3 +123,14 @@ def test_product_package_does_not_import_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", src, re.M), f
                 assert "moe_oracle" not in src, f
+
+
+def test_live_pass_schedule():
+    """Refresh every fifth pass: passes 0, 5, 10 evaluate every row (None)."""
+    live = object()
+    got = [mb.live_pass_mask(p, live) for p in range(11)]
+    assert [g is None for g in got] == [p % 5 == 0 for p in range(11)]
+    assert all(g is live for p, g in enumerate(got) if p % 5)
+    assert mb.live_pass_mask(3, live, refresh=1) is None
+    with pytest.raises(ValueError):
+        mb.live_pass_mask(0, live, refresh=0)

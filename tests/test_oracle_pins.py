@@ -594,6 +594,37 @@ def test_forward_linear_in_weights_and_row_subset(oracle_mod):
     assert np.all(ys[[0, 1, 2]] == 0)
 
 
+def test_forward_live_rows(oracle_mod):
+    """Live-row pass: each live row equals the dense numpy MoE of that row, each dead
+    row keeps its cached value bit for bit; all live = the full forward, none live =
+    the cache."""
+    w, T, x, idx, wt, keep, wr, experts, shared = _tiny_setup(oracle_mod, 0.9)
+    off = w.block_offsets()
+    cached = np.random.default_rng(5).standard_normal((w.R, w.H))
+    live = W.live_rows(w.R, 0.4, seed=11).numpy()
+    assert 0 < live.sum() < w.R
+    y = oracle_mod.forward_live(x, off, idx, wr, keep, experts, shared, w.E, live, cached)
+    mask = oracle_mod.keep_mask(keep, w.E)
+    for r in range(w.R):
+        if not live[r]:
+            assert np.array_equal(y[r], cached[r])
+            continue
+        xr = _f64(x[r])
+        ref = _swiglu_np(xr, *shared)
+        for j in range(w.k):
+            if mask[0, idx[r, j]]:
+                ref = ref + float(wr[r, j]) * _swiglu_np(xr, *experts[idx[r, j]])
+        assert np.allclose(y[r], ref, rtol=1e-10, atol=1e-12)
+    full = oracle_mod.forward(x, off, idx, wr, keep, experts, shared, w.E)
+    ones = np.ones(w.R, np.uint8)
+    assert np.array_equal(
+        oracle_mod.forward_live(x, off, idx, wr, keep, experts, shared, w.E, ones, cached), full)
+    zeros = np.zeros(w.R, np.uint8)
+    assert np.array_equal(
+        oracle_mod.forward_live(x, off, idx, wr, keep, experts, shared, w.E, zeros, cached),
+        cached)
+
+
 def test_forward_missing_expert_is_an_error(oracle_mod):
     w, T, x, idx, wt, keep, wr, experts, shared = _tiny_setup(oracle_mod, 0.9)
     used = oracle_mod.surviving_experts(idx, keep, w.block_offsets(), w.E)
