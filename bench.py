@@ -401,6 +401,39 @@ def run_gpu(args, w: W.Workload):
                 phase_ms[name].append(evs[j].elapsed_time(evs[j + 1]))
     torch.cuda.synchronize()
 
+    # live-row passes (informational): the forward on a seeded subset of the
+    # rows, the others keeping their cached output
+    live_us = {}
+    for frac in args.live_fracs:
+        live = W.live_rows(w.R, frac, seed=x_seed + 7, device=dev)
+        lv = live.cpu().numpy().astype(bool)
+        lused, lpairs = set(), 0
+        for b in range(w.nb):
+            for r in range(off[b], off[b + 1]):
+                if lv[r]:
+                    for e in idx[r]:
+                        if (keep[b, e // 32] >> (e % 32)) & 1:
+                            lused.add(int(e))
+                            lpairs += 1
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            layer.forward(T.x, T.block_offsets, idx_t, wr_t, keep_t, y=y, live=live)
+        torch.cuda.synchronize()
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(min(args.steps, 50) + 3):
+                flush_l2(i)
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+                b_.synchronize()
+                if i >= 3:
+                    ts.append(a_.elapsed_time(b_))
+        live_us[f"{frac:g}"] = {"live_rows": int(lv.sum()), "experts": len(lused),
+                                "pairs": lpairs, "forward_us": 1e3 * statistics.median(ts)}
+    torch.cuda.synchronize()
+
     # end to end through the public API with host buffers (pinned), no graph
     x_host = T.x.cpu().pin_memory()
     off_host = T.block_offsets.cpu().pin_memory()
@@ -477,6 +510,8 @@ def run_gpu(args, w: W.Workload):
         "e2e": {"value": w.R * ws * e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
     }
+    if live_us:
+        line["live_pass"] = live_us
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x_seed, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
@@ -495,6 +530,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--live-fracs", type=lambda v: [float(t) for t in v.split(",") if t],
+                    default=[], help="also time live-row passes with these live fractions "
+                                     "(comma separated), reported under live_pass")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -24,6 +24,15 @@
 //            weight (the weights of a row sum to 1), the shared expert's is
 //            not, and one bf16 part there too would leave almost no margin in
 //            the output tolerance.
+//  gate/up, large shape ("rows as M"): the roles swap.  A = 128 rows of x
+//            (gathered by the loader warps), B = 256 weight rows (128 gate rows,
+//            then the 128 up rows of the same intermediate indices), so one
+//            M = 128, N = 256 MMA per K = 16 does the work of two N = 128 ones
+//            at about the same cost.  TMEM lane = row of x, columns 0..127 =
+//            g and 128..255 = u of the tile's intermediate indices; each
+//            epilogue thread computes h for its row and stores it in 16-byte
+//            pieces.  Rows of the tile past the unit's count only feed TMEM
+//            lanes that are never read, so they are not loaded.
 //  down:     A = 128 rows of W_down[e] (hidden outputs), B = rows of h.  For
 //            the shared expert, D = W (h_hi + h_lo): in the large shape K runs
 //            over [hi | lo] (its 2 Is columns of h) while A wraps around its Is
@@ -315,7 +324,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const int n16 = (n + 15) & ~15;
                 const int K = MODE == kGateUp ? a.H
                                               : (g == a.E ? (C::kDualLo ? a.Is : 2 * a.Is) : a.I);
-                const uint32_t idesc = idesc_bf16_f32(128, n16);
+                // large gate/up: M = rows of x, N = 128 gate + 128 up weight rows
+                const uint32_t idesc = idesc_bf16_f32(128, C::kSplitGU ? 256 : n16);
                 if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
                     give_up();
                     break;
@@ -337,10 +347,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = smem_desc_sw128(sA + kk * 32);
                         const uint64_t bd = smem_desc_sw128(sB + kk * 32);
-                        tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
-                        if (C::kSplitGU)  // up rows into the second accumulator
-                            tc_mma_bf16(d + NMAX, smem_desc_sw128(sA + 128 * 128 + kk * 32), bd, idesc,
-                                        (kb | kk) != 0);
+                        if (C::kSplitGU)  // rows of x (B ring) as A, the 256 weight rows as B
+                            tc_mma_bf16(d, bd, ad, idesc, (kb | kk) != 0);
+                        else
+                            tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
                         if (C::kDualLo && g == a.E)  // shared expert: lo part of h
                             tc_mma_bf16(d, ad, smem_desc_sw128(sB + NMAX * 128 + kk * 32), idesc, 1u);
                     }
@@ -427,21 +437,37 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
             bool released = false;  // accumulator handed back to the MMA warp
             if (C::kSplitGU) {
-                // lane = intermediate index il: g in columns [0, N), u in [N, 2N)
-                __nv_bfloat16* out = g == a.E ? a.hs : a.h;
-                const int ld = g == a.E ? a.Is : a.I;
-                const int il = m * 128 + q * 32 + lane;
-                for (int c = 0; c < n16; c += 16) {
+                // lane = row t of the unit: g of intermediate index m*128 + c in
+                // column c, u in column 128 + c
+                const bool sh = g == a.E;
+                const int ld = sh ? a.Is : a.I;
+                const int t = q * 32 + lane;
+                __nv_bfloat16* orow = (sh ? a.hs + (size_t)(start + t) * (2 * ld)
+                                          : a.h + (size_t)(start + t) * ld) + m * 128;
+                const int cmax = min(128, ld - m * 128);  // intermediate indices of the tile
+                for (int c = 0; c < 128; c += 16) {
                     float gv[16], uv[16];
                     __syncwarp();  // tcgen05.ld is warp-collective
-                    tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(NMAX + c), gv, uv);
-                    if (il < ld) {
+                    tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(128 + c), gv, uv);
+                    if (t < n && c < cmax) {
+                        uint32_t hi[8], lo[8];
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            const int col = c + t;
-                            if (col < n) {
-                                store_h(out, g == a.E, ld, start + col, il, silu(gv[t]) * uv[t]);
-                            }
+                        for (int j = 0; j < 8; ++j) {
+                            const float h0 = silu(gv[2 * j]) * uv[2 * j];
+                            const float h1 = silu(gv[2 * j + 1]) * uv[2 * j + 1];
+                            const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+                            hi[j] = *reinterpret_cast<const uint32_t*>(&b);
+                            const __nv_bfloat162 l = __floats2bfloat162_rn(
+                                h0 - __low2float(b), h1 - __high2float(b));
+                            lo[j] = *reinterpret_cast<const uint32_t*>(&l);
+                        }
+                        uint4* o = reinterpret_cast<uint4*>(orow + c);
+                        o[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        o[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                        if (sh) {  // lo part: columns Is .. 2 Is - 1 of the shared row
+                            uint4* ol = reinterpret_cast<uint4*>(orow + ld + c);
+                            ol[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                            ol[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
                         }
                     }
                 }
