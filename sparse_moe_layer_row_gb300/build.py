@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmoeblock.so")
 SOURCES = ["api.cu", "router.cu", "router_tc.cu", "coreset.cu", "scatter.cu", "gemm.cu",
-           "noalloc.cu"]
+           "gemm_pair.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.cuh", "route_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -169,6 +169,7 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e == cudaSuccess) e = gemm_set_attributes();
+    if (e == cudaSuccess) e = gateup_pair_set_attributes(p->num_sms);
     if (e == cudaSuccess) e = route_tc_set_attributes();
     if (e != cudaSuccess) {
         delete p;
@@ -294,7 +295,7 @@ moe_status moe_block_forward_live(const moe_plan* p, const void* x, int32_t R,
     const Layout L = make_layout(d);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool small = R <= kSmallRows;
-    const int nt_gu = small ? kSmallN : kLargeN;
+    const int nt_gu = small ? kSmallN : kLargeNGU;
     const int nt_dn = small ? kSmallN : kLargeNDown;
 
     ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,

@@ -42,11 +42,12 @@ struct Layout {
     int64_t max_pairs, max_units_gu, max_units_dn;
 };
 
-// Rows of x per unit of grouped-GEMM work (the MMA N extent).  A call with
-// few rows uses kSmallN for both GEMMs; otherwise the gate/up GEMM takes
-// kLargeN rows per unit and the down GEMM kLargeNDown.
+// Rows of x per unit of grouped-GEMM work.  A call with few rows uses kSmallN
+// for both GEMMs (the MMA N extent); otherwise the gate/up GEMM takes kLargeNGU
+// rows per unit (a CTA pair, 128 rows of x each as the MMA's M) and the down
+// GEMM kLargeNDown (its N extent).
 constexpr int kSmallN = 32;
-constexpr int kLargeN = 128;
+constexpr int kLargeNGU = 256;
 constexpr int kLargeNDown = 256;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -354,6 +355,12 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float* va,
 }
 
 // ---- small math ---------------------------------------------------------------
+
+// silu(g) = g / (1 + e^-g) with the fast exponential and division intrinsics:
+// relative error near 2^-21, far below the bf16 rounding (2^-9) that h gets
+// next.  Below g = -87 the quotient is 0 (the exact value is under 1e-36);
+// NaN stays NaN.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ int find_block(const int32_t* off, int nb, int r) {
     // largest b in [0, nb) with off[b] <= r (off need not be valid: result is clamped)

@@ -24,15 +24,9 @@
 //            weight (the weights of a row sum to 1), the shared expert's is
 //            not, and one bf16 part there too would leave almost no margin in
 //            the output tolerance.
-//  gate/up, large shape ("rows as M"): the roles swap.  A = 128 rows of x
-//            (gathered by the loader warps), B = 256 weight rows (128 gate rows,
-//            then the 128 up rows of the same intermediate indices), so one
-//            M = 128, N = 256 MMA per K = 16 does the work of two N = 128 ones
-//            at about the same cost.  TMEM lane = row of x, columns 0..127 =
-//            g and 128..255 = u of the tile's intermediate indices; each
-//            epilogue thread computes h for its row and stores it in 16-byte
-//            pieces.  Rows of the tile past the unit's count only feed TMEM
-//            lanes that are never read, so they are not loaded.
+//            This kernel runs the gate/up GEMM for few rows per expert (the
+//            streaming shape); with many rows per expert it runs on CTA pairs
+//            with the rows of x as M (gemm_pair.cu).
 //  down:     A = 128 rows of W_down[e] (hidden outputs), B = rows of h.  For
 //            the shared expert, D = W (h_hi + h_lo): in the large shape K runs
 //            over [hi | lo] (its 2 Is columns of h) while A wraps around its Is
@@ -63,48 +57,37 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s when draining after 
 
 template <int MODE, int NMAX, int STAGES>
 struct GemmCfg {
-    // gate/up: the streaming shape (NMAX == kSmallN) packs 64 gate + 64 up rows
-    // into one 128-row A tile and trades g and u in the epilogue; the large
-    // shape loads 128 gate rows and 128 up rows into two accumulators, so a
-    // TMEM lane holds g and u of the same intermediate index.
-    static constexpr bool kSplitGU = MODE == kGateUp && NMAX != kSmallN;
-    static constexpr int kGURows = kSplitGU ? 128 : 64;  // intermediate rows per gate/up unit
+    // gate/up (streaming shape only; many rows per expert run on CTA pairs,
+    // gemm_pair.cu): 64 gate + 64 up rows in one 128-row A tile, g and u
+    // traded in the epilogue
+    static_assert(MODE == kDown || NMAX == kSmallN, "large gate/up runs in gemm_pair.cu");
+    static constexpr int kGURows = 64;  // intermediate rows per gate/up unit
     // rows per B box: 16 for the streaming shape, 64 for the large shape (fewer
     // TMA instructions per stage; NMAX is a multiple of it)
     static constexpr int kBoxRows = NMAX >= 64 ? 64 : 16;
-    static constexpr int kABytes = (kSplitGU ? 2 : 1) * 128 * 128;
+    static constexpr int kABytes = 128 * 128;
     // down, streaming shape: the shared expert's lo part of h rides in the same
     // stage as its hi part (a second MMA per K step); the large shape runs the
     // lo part as further K steps at the full tile width instead
     static constexpr bool kDualLo = MODE == kDown && NMAX == kSmallN;
     static constexpr int kBBytes = (kDualLo ? 2 : 1) * NMAX * 128;
-    // large gate/up: the rows of x (B) are gathered by four loader warps with
-    // 16-byte cp.async into a ring of their own, deeper than the A ring
-    static constexpr bool kLoaders = kSplitGU;
-    static constexpr int kBStages = kLoaders ? 4 : 0;
-    static constexpr int kBLag = 2;  // stages a loader thread keeps in flight
-    static constexpr int kThreads = kLoaders ? 320 : 192;
-    static constexpr int kMinBlocks = kLoaders ? 1 : 2;
-    static constexpr int kStageBytes = kLoaders ? kABytes : kABytes + kBBytes;  // A ring stride
-    static constexpr int kBRingOff = STAGES * kStageBytes;
-    static constexpr int kXchgOff = kBRingOff + kBStages * kBBytes;
-    // gate/up streaming shape: g <-> u exchange; down: the unit's fp16 output tile
-    static constexpr int kXchgBytes =
-        MODE == kGateUp ? (kSplitGU ? 0 : 2 * 64 * 9 * 4) : NMAX * 128 * 2;
+    static constexpr int kThreads = 192;
+    static constexpr int kMinBlocks = 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kXchgOff = STAGES * kStageBytes;
+    // gate/up: g <-> u exchange; down: the unit's fp16 output tile
+    static constexpr int kXchgBytes = MODE == kGateUp ? 2 * 64 * 9 * 4 : NMAX * 128 * 2;
     static constexpr int kRowsOff = kXchgOff + kXchgBytes;             // gate/up: rows of x of a unit
     static constexpr int kRowsBytes = MODE == kGateUp && NMAX == kSmallN ? NMAX * 4 : 0;
     static constexpr int kBarOff = kRowsOff + kRowsBytes;
     static constexpr int kSmem = kBarOff + 512 + 1024;
-    static constexpr int kAccCols = (kSplitGU ? 2 : 1) * NMAX;   // TMEM columns per accumulator
+    static constexpr int kAccCols = NMAX;   // TMEM columns per accumulator
     static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
-    static_assert(kBLag <= kBStages - 2 || !kLoaders, "a loader may hold back at most B stages - 2");
-    static_assert(8 * (2 * STAGES + 8 + 2 * kBStages) + 16 <= 512, "barrier region");
+    static_assert(8 * (2 * STAGES + 6) + 16 <= 512, "barrier region");
     static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
     static_assert(NMAX % 16 == 0 && NMAX <= 256 && NMAX % (NMAX >= 64 ? 64 : 16) == 0, "MMA N extent");
 };
-
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 // h of (pair or shared row) p, intermediate index il: routed rows [p][ld] bf16;
 // shared rows [p][2 ld] = hi | lo.
@@ -127,9 +110,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
        const __grid_constant__ CUtensorMap tmBg, GemmArgs a) {
     using C = GemmCfg<MODE, NMAX, STAGES>;
-    // small routed gate/up units gather their rows of x (pair_row) with TMA
-    // gather4; large ones with the loader warps (TMA gather4 moves about 7
-    // bytes per clock per SM: enough for 32-row tiles, far too few for larger)
+    // gate/up units gather their rows of x (pair_row; shared_rows on a
+    // live-row pass) with TMA gather4 (about 7 bytes per clock per SM: enough
+    // for 32-row tiles, far too few for larger ones)
     constexpr bool kGather = MODE == kGateUp && NMAX == kSmallN;
     extern __shared__ uint8_t smem_raw[];
 
@@ -141,9 +124,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* xbar = tempty + 2;  // [2] epilogue exchange (128 arrivals each)
-    uint64_t* bfull = xbar + 2;   // [kBStages] B ring (loaders)
-    uint64_t* bempty = bfull + C::kBStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bempty + C::kBStages);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;
 
@@ -155,7 +136,6 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             mbar_init(tempty + i, 128);
             mbar_init(xbar + i, 128);
         }
-        for (int s = 0; s < C::kBStages; ++s) { mbar_init(bfull + s, 128); mbar_init(bempty + s, 1); }
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -238,7 +218,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const uint32_t bbytes = gathered ? (uint32_t)nb4 * 512u
                                              : (uint32_t)(nbox * C::kBoxRows * 128);
             const int parts = C::kDualLo && g == a.E ? 2 : 1;
-            const uint32_t bytes = (uint32_t)C::kABytes + (C::kLoaders ? 0u : parts * bbytes);
+            const uint32_t bytes = (uint32_t)C::kABytes + parts * bbytes;
             if (gathered) {
                 // the unit's rows of x, padded to a multiple of 4 with R (read as zeros);
                 // copies of the previous unit took their coordinates when issued
@@ -280,7 +260,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (g == a.E) tma_load_2d(sA, &tmA2, kca, m * 128, full + stage);
                         else tma_load_3d(sA, &tmA0, kca, m * 128, g, full + stage);
                     }
-                    if (!gathered && !C::kLoaders) {
+                    if (!gathered) {
                         if (waited) issue_b(sB, g, start, nbox, K, kc, full + stage);
                         else held[nheld] = HeldB{sB, g, start, nbox, K, kc, full + stage};
                     }
@@ -315,8 +295,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------ MMA issuer
-            int stage = 0, acc = 0, bstage = 0;
-            uint32_t phase = 0, acc_phase = 0, bphase = 0;
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
                 const int4 un = __ldg(a.units + u);
@@ -324,8 +304,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const int n16 = (n + 15) & ~15;
                 const int K = MODE == kGateUp ? a.H
                                               : (g == a.E ? (C::kDualLo ? a.Is : 2 * a.Is) : a.I);
-                // large gate/up: M = rows of x, N = 128 gate + 128 up weight rows
-                const uint32_t idesc = idesc_bf16_f32(128, C::kSplitGU ? 256 : n16);
+                const uint32_t idesc = idesc_bf16_f32(128, n16);
                 if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
                     give_up();
                     break;
@@ -333,92 +312,30 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * C::kAccCols);
                 for (int kb = 0; kb < (K >> 6); ++kb) {
-                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs) ||
-                        (C::kLoaders && !mbar_wait_bounded(bfull + bstage, bphase, abort_flag, kWaitLimitNs))) {
+                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs)) {
                         give_up();
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sA = sbase + stage * C::kStageBytes;
-                    const uint32_t sB = C::kLoaders ? sbase + C::kBRingOff + bstage * C::kBBytes
-                                                    : sA + C::kABytes;
+                    const uint32_t sB = sA + C::kABytes;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = smem_desc_sw128(sA + kk * 32);
                         const uint64_t bd = smem_desc_sw128(sB + kk * 32);
-                        if (C::kSplitGU)  // rows of x (B ring) as A, the 256 weight rows as B
-                            tc_mma_bf16(d, bd, ad, idesc, (kb | kk) != 0);
-                        else
-                            tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
+                        tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
                         if (C::kDualLo && g == a.E)  // shared expert: lo part of h
                             tc_mma_bf16(d, ad, smem_desc_sw128(sB + NMAX * 128 + kk * 32), idesc, 1u);
                     }
                     tc_commit(empty + stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                    if (C::kLoaders) {
-                        tc_commit(bempty + bstage);
-                        if (++bstage == C::kBStages) { bstage = 0; bphase ^= 1u; }
-                    }
                 }
                 if (!ok) break;
                 tc_commit(tfull + acc);
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
-        }
-    } else if (warp >= 6) {
-        // ------------------------------------------- B loaders (large gate/up)
-        // Row i of a unit (its pair's row of x; the shared expert's rows are
-        // start + i) is copied by 8 threads, 16 bytes each, into the 128-byte
-        // swizzled row of the B tile: chunk c of row i lands at chunk c ^ (i & 7).
-        // A thread signals a stage once kBLag newer stages are issued, after
-        // its copies of it have landed and are fenced for the async proxy.
-        const int lt = threadIdx.x - 192;            // 0..127
-        const int lw = lt >> 5, r4 = (lt & 31) >> 3, ch = lt & 7;
-        int bstage = 0, npend = 0;
-        uint32_t bphase = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-            const int4 un = __ldg(a.units + u);
-            const int g = un.x, start = un.z, n = un.w;
-            constexpr int kRowsPerThread = NMAX / 16;
-            const __nv_bfloat16* src[kRowsPerThread];
-#pragma unroll
-            for (int j = 0; j < kRowsPerThread; ++j) {
-                const int i = j * 16 + lw * 4 + r4;
-                const int row = i >= n ? -1
-                              : g != a.E ? __ldg(a.pair_row + start + i)
-                              : (a.shared_rows ? __ldg(a.shared_rows + start + i) : start + i);
-                src[j] = row >= 0 ? a.x + (size_t)row * a.H + ch * 8 : nullptr;
-            }
-            for (int kb = 0; kb < (a.H >> 6); ++kb) {
-                if (!mbar_wait_bounded(bempty + bstage, bphase ^ 1u, abort_flag, kWaitLimitNs)) {
-                    give_up();
-                    ok = false;
-                    break;
-                }
-                const uint32_t sB = sbase + C::kBRingOff + bstage * C::kBBytes;
-#pragma unroll
-                for (int j = 0; j < kRowsPerThread; ++j) {
-                    const int i = j * 16 + lw * 4 + r4;
-                    if (src[j]) cp_async16(sB + i * 128 + ((ch ^ (i & 7)) << 4), src[j] + kb * 64);
-                }
-                cp_async_commit();
-                if (npend == C::kBLag) {
-                    cp_async_wait<C::kBLag>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(bfull + (bstage + C::kBStages - C::kBLag) % C::kBStages);
-                } else {
-                    ++npend;
-                }
-                if (++bstage == C::kBStages) { bstage = 0; bphase ^= 1u; }
-            }
-        }
-        cp_async_wait<0>();  // nothing of this thread lands after the loop
-        if (ok) {
-            fence_proxy_async_smem();
-            for (int i = npend; i > 0; --i) mbar_arrive(bfull + (bstage + C::kBStages - i) % C::kBStages);
         }
     } else {
         // ---------------------------------------------------------- epilogue
@@ -436,42 +353,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
             bool released = false;  // accumulator handed back to the MMA warp
-            if (C::kSplitGU) {
-                // lane = row t of the unit: g of intermediate index m*128 + c in
-                // column c, u in column 128 + c
-                const bool sh = g == a.E;
-                const int ld = sh ? a.Is : a.I;
-                const int t = q * 32 + lane;
-                __nv_bfloat16* orow = (sh ? a.hs + (size_t)(start + t) * (2 * ld)
-                                          : a.h + (size_t)(start + t) * ld) + m * 128;
-                const int cmax = min(128, ld - m * 128);  // intermediate indices of the tile
-                for (int c = 0; c < 128; c += 16) {
-                    float gv[16], uv[16];
-                    __syncwarp();  // tcgen05.ld is warp-collective
-                    tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(128 + c), gv, uv);
-                    if (t < n && c < cmax) {
-                        uint32_t hi[8], lo[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float h0 = silu(gv[2 * j]) * uv[2 * j];
-                            const float h1 = silu(gv[2 * j + 1]) * uv[2 * j + 1];
-                            const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
-                            hi[j] = *reinterpret_cast<const uint32_t*>(&b);
-                            const __nv_bfloat162 l = __floats2bfloat162_rn(
-                                h0 - __low2float(b), h1 - __high2float(b));
-                            lo[j] = *reinterpret_cast<const uint32_t*>(&l);
-                        }
-                        uint4* o = reinterpret_cast<uint4*>(orow + c);
-                        o[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                        o[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-                        if (sh) {  // lo part: columns Is .. 2 Is - 1 of the shared row
-                            uint4* ol = reinterpret_cast<uint4*>(orow + ld + c);
-                            ol[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                            ol[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-                        }
-                    }
-                }
-            } else if (MODE == kGateUp) {
+            if (MODE == kGateUp) {
                 for (int c = 0; alive && c < n16; c += 16) {
                     float v[16];
                     __syncwarp();  // tcgen05.ld is warp-collective
@@ -503,7 +385,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         const float gv = is_gate ? v[t] : xg[r * 9 + t];
                         const float uv = is_gate ? xu[r * 9 + t] : v[8 + t];
                         if (col < n) {
-                            store_h(out, g == a.E, ld, start + col, il, silu(gv) * uv);
+                            store_h(out, g == a.E, ld, start + col, il, silu_fast(gv) * uv);
                         }
                     }
                     mbar_arrive(xbar + 1);  // the buffer is reused by the next chunk
@@ -594,16 +476,16 @@ static cudaError_t set_attr() {
 
 // (rows per unit, pipeline depth) of each kernel shape: small = few rows per
 // expert (weight streaming: two CTAs per SM, each with its own ring, keep more
-// TMA streams in flight); large = many rows (tensor-core bound, one CTA per SM).
+// TMA streams in flight); large = many rows (tensor-core bound, one CTA per SM;
+// the large gate/up GEMM is k_gateup_pair).
 constexpr int kSmallStagesGU = 5, kSmallStagesDN = 4;
-constexpr int kLargeStagesGU = 5, kLargeStagesDN = 3;
+constexpr int kLargeStagesDN = 3;
 constexpr int kSmallCtasPerSm = 2;
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
     if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU>()) != cudaSuccess) return e;
     if ((e = set_attr<kDown, kSmallN, kSmallStagesDN>()) != cudaSuccess) return e;
-    if ((e = set_attr<kGateUp, kLargeN, kLargeStagesGU>()) != cudaSuccess) return e;
     return set_attr<kDown, kLargeNDown, kLargeStagesDN>();
 }
 
@@ -614,7 +496,7 @@ cudaError_t launch_gemm(int mode, bool small, const GemmMaps& mp, const GemmArgs
         return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStagesGU>(mp, a, grid, st)
                                : launch_one<kDown, kSmallN, kSmallStagesDN>(mp, a, grid, st);
     }
-    return mode == kGateUp ? launch_one<kGateUp, kLargeN, kLargeStagesGU>(mp, a, grid, st)
+    return mode == kGateUp ? launch_gateup_pair(mp, a, st)
                            : launch_one<kDown, kLargeNDown, kLargeStagesDN>(mp, a, grid, st);
 }
 

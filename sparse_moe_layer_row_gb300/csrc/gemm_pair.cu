@@ -1,0 +1,498 @@
+// Gate/up GEMM for many rows per expert on a CTA pair (tcgen05 cta_group::2).
+//
+// The same SwiGLU first half as k_gemm<kGateUp> (model card "Clover-35B-A3B-
+// Preview -- CMF", intro: 256 routed experts plus a shared expert), for units
+// of up to 256 rows of x.  Two CTAs on neighbouring SMs form a cluster and
+// run one MMA of M = 256, N = 256 per K = 16:
+//
+//   A (M = 256): rows of x, 128 in each CTA's shared memory (rank r holds
+//                rows 128 r .. 128 r + 127 of the unit), gathered by 16-byte
+//                cp.async from the loader warps;
+//   B (N = 256): the tile's 128 gate rows in rank 0 and its 128 up rows in
+//                rank 1, loaded by TMA;
+//   D:           each CTA's TMEM holds its own 128 rows of x: columns 0..127
+//                are g, 128..255 are u of the tile's 128 intermediate indices.
+//
+// An M = 128 MMA on one SM reads 16 KB of x and 32 KB of weights per 64-wide
+// K step; here each SM reads 16 KB + 16 KB for the same work, so the pair
+// needs two thirds of the operand bandwidth from L2 per flop.
+//
+// Roles (320 threads per CTA):
+//   warp 0 lane 0   TMA producer of the CTA's weight half; the complete-tx of
+//                   both halves lands on rank 0's `full` barrier
+//   warp 1          TMEM allocation (both ranks); lane 0 of rank 0 issues the
+//                   MMAs and the commits, which arrive on the barriers of both
+//                   ranks (stage `empty`, accumulator `tfull`); lane 0 of
+//                   rank 1 forwards its CTA's x stages to rank 0 (below)
+//   warps 2..5      epilogue: TMEM -> silu(g) * u -> h (bf16; hi + lo bf16 for
+//                   the shared expert) in 16-byte stores; release the
+//                   accumulator on rank 0's `tempty`
+//   warps 6..9      loaders: the CTA's rows of x into its x slot; each
+//                   thread's copies arrive on its own CTA's `bfull` when they
+//                   land (cp.async.mbarrier.arrive), so a loader never waits
+//                   for its own copies and the ring depth is the only limit on
+//                   the copies in flight.  In rank 1 one thread waits for that
+//                   barrier, fences the CTA's x tile for the async proxy and
+//                   arrives on rank 0's `pfull`; in rank 0 the MMA thread
+//                   waits for both and fences its own tile.
+// Each stage holds a weight half and an x tile (32 KB); both are freed by the
+// same commit.  Every wait is bounded; a role that gives up raises the CTA's
+// abort flag and the device status counter, and both CTAs leave their loops,
+// drain (bounded) and meet at a final cluster barrier before the TMEM is
+// released.
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr uint64_t kPairWaitNs = 2000000000ull;   // 2 s: far beyond any legal wait
+constexpr uint64_t kPairDrainNs = 200000000ull;   // 0.2 s when draining after an abort
+
+constexpr int kPStages = 7;
+constexpr int kPThreads = 320;
+constexpr int kPTile = 128 * 128;        // 128 rows x 64 bf16 (one SW128 tile)
+constexpr int kPStageBytes = 2 * kPTile; // weight half, then x
+constexpr int kPBarOff = kPStages * kPStageBytes;
+constexpr int kPSmem = kPBarOff + 512 + 1024;
+constexpr int kPAccCols = 256;
+constexpr int kPTmemCols = 512;
+static_assert(kPSmem <= 227 * 1024, "shared memory budget");
+static_assert(8 * (4 * kPStages + 4) + 12 <= 512, "barrier region");
+
+// ---- cluster / CTA-pair PTX -----------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// All threads of both CTAs.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier of either CTA of the pair (cluster address), with the
+// instruction's default semantics (release at CTA scope).  A cluster-scope
+// release here measured about 1,500 cycles per arrival under load (it waits
+// for the SM's memory operations in flight) and serialised the stage ring.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire (arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          volatile int* abort, uint64_t limit_ns) {
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_try_wait_cluster(addr, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(addr, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// TMA tile loads into this CTA's shared memory whose complete-tx is signalled
+// on an mbarrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                                 int c2, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the barrier at `bar`'s offset in both CTAs of the pair once every
+// MMA issued so far by this thread completes.
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+// Arrive on `bar` once all cp.async copies issued so far by this thread have
+// landed; the arrival counts toward the barrier's expected count.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kPThreads, 1)
+k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ CUtensorMap tmWu,
+              const __grid_constant__ CUtensorMap tmSg, const __grid_constant__ CUtensorMap tmSu,
+              GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;   // same offset in both CTAs
+    uint8_t* base = smem_raw + (sbase - raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + kPBarOff);  // [S] weights (rank 0)
+    uint64_t* bfull = full + kPStages;                               // [S] own x landed (both)
+    uint64_t* pfull = bfull + kPStages;                              // [S] peer's x landed (rank 0)
+    uint64_t* empty = pfull + kPStages;                              // [S] stage free (both)
+    uint64_t* tfull = empty + kPStages;                              // [2] accumulator ready (both)
+    uint64_t* tempty = tfull + 2;                                    // [2] accumulator free (rank 0)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* never = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(bfull + s, 128);   // the loader threads' copies
+            mbar_init(pfull + s, 1);     // rank 1's forwarder
+            mbar_init(empty + s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull + i, 1);
+            mbar_init(tempty + i, 256);  // 128 epilogue threads of each CTA
+        }
+        *abort_flag = 0;
+        *never = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_slot, kPTmemCols);
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmWg); prefetch_tmap(&tmWu); prefetch_tmap(&tmSg); prefetch_tmap(&tmSu);
+    }
+    pdl_wait();   // see common.cuh
+    pdl_trigger();
+    const int nunits = __ldg(a.n_units);
+    const int c0 = (int)cluster_id(), nc = (int)cluster_count();
+    const int rbase = 128 * (int)rank;   // this CTA's rows of each unit
+
+    auto give_up = [&]() {
+        if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------- weight-half producer
+        if (lane == 0) {
+            const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // rank 0's full[0]
+            const CUtensorMap* mR = leader ? &tmWg : &tmWu;
+            const CUtensorMap* mS = leader ? &tmSg : &tmSu;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = c0; ok && u < nunits; u += nc) {
+                const int4 un = __ldg(a.units + u);
+                const int g = un.x, m = un.y;
+                for (int kb = 0; kb < (a.H >> 6); ++kb) {
+                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kPairWaitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sW = sbase + stage * kPStageBytes;
+                    const uint32_t fb = full0 + stage * 8;
+                    if (leader) mbar_expect_tx(full + stage, 2u * kPTile);  // both halves
+                    for (int hb = 0; hb < 2; ++hb) {
+                        const int row = m * 128 + 64 * hb;
+                        if (g == a.E) tma_load_2d_pair(sW + hb * 64 * 128, mS, kb * 64, row, fb);
+                        else tma_load_3d_pair(sW + hb * 64 * 128, mR, kb * 64, row, g, fb);
+                    }
+                    if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // every stage released by the MMA before the CTA exits (bounded)
+            for (int i = 0; i < kPStages; ++i) {
+                const uint64_t lim = *abort_flag ? kPairDrainNs : kPairWaitNs;
+                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, never, lim)) {
+                    give_up();
+                    break;
+                }
+                if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp == 1) {
+        if (!leader && lane == 0) {
+            // ------------------------------------------ x-stage forwarder (rank 1)
+            const uint32_t pfull0 = mapa_shared(smem_u32(pfull), 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = c0; ok && u < nunits; u += nc) {
+                for (int kb = 0; kb < (a.H >> 6); ++kb) {
+                    if (!mbar_wait_bounded(bfull + stage, phase, abort_flag, kPairWaitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();   // the tile is read by rank 0's MMA
+                    mbar_arrive_cluster(pfull0 + stage * 8);
+                    if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+        if (leader && lane == 0) {
+            // ------------------------------------------------------ MMA issuer
+            const uint32_t idesc = idesc_bf16_f32(256, 256);
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int u = c0; ok && u < nunits; u += nc) {
+                if (!mbar_wait_cluster_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kPairWaitNs)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * kPAccCols);
+                for (int kb = 0; kb < (a.H >> 6); ++kb) {
+                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kPairWaitNs) ||
+                        !mbar_wait_bounded(bfull + stage, phase, abort_flag, kPairWaitNs) ||
+                        !mbar_wait_cluster_bounded(pfull + stage, phase, abort_flag, kPairWaitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();   // this CTA's x tile, written by cp.async
+                    tc_fence_after();
+                    const uint32_t sW = sbase + stage * kPStageBytes;
+                    const uint32_t sX = sW + kPTile;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16_pair(d, smem_desc_sw128(sX + kk * 32), smem_desc_sw128(sW + kk * 32),
+                                         idesc, (kb | kk) != 0);
+                    tc_commit_pair(empty + stage);
+                    if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair(tfull + acc);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+        }
+    } else if (warp >= 6) {
+        // ----------------------------------------------------------- x loaders
+        // Row i of the CTA's part of a unit is copied by 8 threads, 16 bytes
+        // each, into the 128-byte swizzled row of the x tile: chunk c of row i
+        // lands at chunk c ^ (i & 7).
+        const int lt = threadIdx.x - 192;            // 0..127
+        const int lw = lt >> 5, r4 = (lt & 31) >> 3, ch = lt & 7;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = c0; ok && u < nunits; u += nc) {
+            const int4 un = __ldg(a.units + u);
+            const int g = un.x, start = un.z + rbase;
+            const int nr = min(128, max(0, un.w - rbase));
+            const __nv_bfloat16* src[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = j * 16 + lw * 4 + r4;
+                const int row = i >= nr ? -1
+                              : g != a.E ? __ldg(a.pair_row + start + i)
+                              : (a.shared_rows ? __ldg(a.shared_rows + start + i) : start + i);
+                src[j] = row >= 0 ? a.x + (size_t)row * a.H + ch * 8 : nullptr;
+            }
+            for (int kb = 0; kb < (a.H >> 6); ++kb) {
+                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kPairWaitNs)) {
+                    give_up();
+                    ok = false;
+                    break;
+                }
+                const uint32_t sX = sbase + stage * kPStageBytes + kPTile;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int i = j * 16 + lw * 4 + r4;
+                    if (src[j]) cp_async16(sX + i * 128 + ((ch ^ (i & 7)) << 4), src[j] + kb * 64);
+                }
+                cp_async_arrive(bfull + stage);
+                if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+            }
+        }
+        cp_async_wait_all();  // nothing of this thread lands after the loop
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = c0; u < nunits; u += nc) {
+            const int4 un = __ldg(a.units + u);
+            const int g = un.x, m = un.y, start = un.z + rbase;
+            const int nr = min(128, max(0, un.w - rbase));
+            const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kPairWaitNs);
+            if (__any_sync(0xffffffffu, !ok)) { give_up(); break; }
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPAccCols);
+            // lane = row t of this CTA's part: g of intermediate index m*128 + c
+            // in column c, u in column 128 + c
+            const bool sh = g == a.E;
+            const int ld = sh ? a.Is : a.I;
+            const int t = q * 32 + lane;
+            __nv_bfloat16* orow = (sh ? a.hs + (size_t)(start + t) * (2 * ld)
+                                      : a.h + (size_t)(start + t) * ld) + m * 128;
+            const int cmax = min(128, ld - m * 128);  // intermediate indices of the tile
+            for (int c = 0; c < 128; c += 16) {
+                float gv[16], uv[16];
+                __syncwarp();  // tcgen05.ld is warp-collective
+                tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(128 + c), gv, uv);
+                if (t < nr && c < cmax) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float h0 = silu_fast(gv[2 * j]) * uv[2 * j];
+                        const float h1 = silu_fast(gv[2 * j + 1]) * uv[2 * j + 1];
+                        const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+                        hi[j] = *reinterpret_cast<const uint32_t*>(&b);
+                        const __nv_bfloat162 l =
+                            __floats2bfloat162_rn(h0 - __low2float(b), h1 - __high2float(b));
+                        lo[j] = *reinterpret_cast<const uint32_t*>(&l);
+                    }
+                    uint4* o = reinterpret_cast<uint4*>(orow + c);
+                    o[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    o[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                    if (sh) {  // lo part: columns Is .. 2 Is - 1 of the shared row
+                        uint4* ol = reinterpret_cast<uint4*>(orow + ld + c);
+                        ol[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        ol[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive_cluster(tempty0 + acc * 8);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // no CTA leaves while its peer may still signal or read it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kPTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+
+static int g_pair_clusters = 0;   // clusters resident at once (0: not yet known)
+
+cudaError_t gateup_pair_set_attributes(int num_sms) {
+    cudaError_t e = cudaFuncSetAttribute(k_gateup_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = kPSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, k_gateup_pair, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    g_pair_clusters = n < num_sms / 2 ? n : num_sms / 2;
+    return cudaSuccess;
+}
+
+cudaError_t launch_gateup_pair(const GemmMaps& mp, const GemmArgs& a, cudaStream_t st) {
+    if (g_pair_clusters <= 0) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * g_pair_clusters);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = kPSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_gateup_pair, mp.a0, mp.a1, mp.a2, mp.a3, a);
+}
+
+}  // namespace moe

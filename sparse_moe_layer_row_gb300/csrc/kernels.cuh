@@ -116,6 +116,9 @@ cudaError_t launch_combine(const CombineArgs&, int num_sms, cudaStream_t);
 cudaError_t gemm_set_attributes();
 cudaError_t launch_gemm(int mode, bool small, const GemmMaps&, const GemmArgs&, int grid,
                         cudaStream_t);
+// Gate/up of units of up to kLargeNGU rows on CTA pairs (gemm_pair.cu).
+cudaError_t gateup_pair_set_attributes(int num_sms);
+cudaError_t launch_gateup_pair(const GemmMaps&, const GemmArgs&, cudaStream_t);
 
 enum { kGateUp = 0, kDown = 1 };
 
