@@ -90,7 +90,7 @@ def load_peaks():
 
 def gemm_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("gemm.cu", "common.cuh", "kernels.cuh"):
+    for f in ("gemm.cu", "gemm_pair.cu", "common.cuh", "kernels.cuh"):
         with open(os.path.join(ROOT, "sparse_moe_layer_row_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
