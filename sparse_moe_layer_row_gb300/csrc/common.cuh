@@ -356,6 +356,18 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float* va,
 
 // ---- small math ---------------------------------------------------------------
 
+// Units of a persistent GEMM in balanced rounds: with U units and G resident
+// CTAs (or CTA pairs) the launch needs ceil(U / G) rounds; spreading the units
+// over the fewest workers that still finish in that many rounds gives every
+// active worker the same count (to within one) instead of leaving most of them
+// idle during a short last round.  Worker i takes units i, i + n, i + 2n, ...
+// with n = active_workers(U, G); workers i >= n take none.
+__device__ __forceinline__ int active_workers(int units, int workers) {
+    if (units <= 0 || workers <= 0) return 0;
+    const int rounds = (units + workers - 1) / workers;
+    return (units + rounds - 1) / rounds;
+}
+
 // silu(g) = g / (1 + e^-g) with the fast exponential and division intrinsics:
 // relative error near 2^-21, far below the bf16 rounding (2^-9) that h gets
 // next.  Below g = -87 the quotient is 0 (the exact value is under 1e-36);

@@ -163,6 +163,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         pdl_trigger();
     }
     const int nunits = __ldg(a.n_units);
+    // gate/up: balanced rounds (common.cuh); the down GEMM keeps the plain
+    // stride, which its unit order is laid out for (measured slower otherwise)
+    const int nact = MODE == kGateUp ? active_workers(nunits, gridDim.x) : (int)gridDim.x;
+    const int ufirst = (int)blockIdx.x < nact ? (int)blockIdx.x : nunits;
 
     auto give_up = [&]() {
         if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
@@ -199,7 +203,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             nheld = 0;
             waited = true;
         };
-        for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+        for (int u = ufirst; ok && u < nunits; u += nact) {
             const int4 un = __ldg(a.units + u);
             const int g = un.x, m = un.y, start = un.z, n = un.w;
             // B rows actually loaded: gathered units load ceil(n/4) rows x 4; the
@@ -298,7 +302,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+            for (int u = ufirst; ok && u < nunits; u += nact) {
                 const int4 un = __ldg(a.units + u);
                 const int g = un.x, n = un.w;
                 const int n16 = (n + 15) & ~15;
@@ -343,7 +347,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         int acc = 0;
         uint32_t acc_phase = 0, xphase = 0;
         bool alive = true;
-        for (int u = blockIdx.x; alive && u < nunits; u += gridDim.x) {
+        for (int u = ufirst; alive && u < nunits; u += nact) {
             const int4 un = __ldg(a.units + u);
             const int g = un.x, m = un.y, start = un.z, n = un.w;
             const int n16 = (n + 15) & ~15;

@@ -241,7 +241,8 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
     pdl_wait();   // see common.cuh
     pdl_trigger();
     const int nunits = __ldg(a.n_units);
-    const int c0 = (int)cluster_id(), nc = (int)cluster_count();
+    const int nc = active_workers(nunits, (int)cluster_count());   // balanced rounds
+    const int c0 = (int)cluster_id() < nc ? (int)cluster_id() : nunits;
     const int rbase = 128 * (int)rank;   // this CTA's rows of each unit
 
     auto give_up = [&]() {

@@ -301,42 +301,62 @@ constexpr int kSmallThreads = 512;
 __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) {
     pdl_wait();  // see common.cuh: nothing global is touched before
     pdl_trigger();
-    __shared__ uint8_t s_slot[kSmallRows][kMaxExperts];   // slot of expert e in row r, or 0xFF
+    // slot of expert e in row r (< 32), kFree (kept for r's block, no slot yet)
+    // or kDropped (not kept)
+    constexpr uint8_t kFree = 0xFF, kDropped = 0xFE;
+    __shared__ uint8_t s_slot[kSmallRows][kMaxExperts];
     __shared__ int s_cnt[kMaxExperts];
     __shared__ int warp_sums[32];
+    // the inputs, read before anything is written: a load issued after a store
+    // to memory that may alias waits for it, and the per-expert loops below
+    // would pay one round trip per pair
+    __shared__ int32_t s_ids[kSmallRows * 32];
+    __shared__ float s_w[kSmallRows * 32];
+    __shared__ int s_blk[kSmallRows];
+    __shared__ uint8_t s_live[kSmallRows];
     __shared__ int s_dup, s_nl;
     const int tid = threadIdx.x;
     const int E = a.E, k = a.k, R = a.R;
     const int words = (E + 31) >> 5;
-    for (int i = tid; i < R * E; i += blockDim.x) s_slot[i / E][i % E] = 0xFF;
+    if (tid < R) {
+        s_blk[tid] = find_block(a.off, a.nb, tid);
+        s_live[tid] = !a.live || a.live[tid] != 0;
+    }
+    for (int i = tid; i < R * k; i += blockDim.x) {
+        s_ids[i] = a.topk_idx[i];
+        s_w[i] = a.w_renorm[i];
+    }
     if (tid == 0) s_dup = 0;
+    __syncthreads();
+    for (int i = tid; i < R * E; i += blockDim.x) {
+        const int r = i / E, e = i - r * E;
+        const uint32_t kw = a.keep[(size_t)s_blk[r] * words + (e >> 5)];
+        s_slot[r][e] = ((kw >> (e & 31)) & 1u) ? kFree : kDropped;
+    }
     if (tid < 32) {  // live rows in order (R <= 32): the shared expert's rows
-        const bool lv = tid < R && (!a.live || a.live[tid] != 0);
+        const bool lv = tid < R && s_live[tid];
         const uint32_t m = __ballot_sync(0xffffffffu, lv);
-        const int pos = __popc(m & ((1u << tid) - 1u));
-        if (tid < R) {
-            a.shared_inv[tid] = lv ? pos : -1;
-            if (lv) a.shared_rows[pos] = tid;
-        }
         if (tid == 0) s_nl = __popc(m);
     }
     __syncthreads();
+    if (tid < R) {
+        int pos = 0;
+        for (int r = 0; r < tid; ++r) pos += s_live[r];
+        a.shared_inv[tid] = s_live[tid] ? pos : -1;
+        if (s_live[tid]) a.shared_rows[pos] = tid;
+    }
     const int nl = s_nl;
     // one thread per row: mark its surviving slots (first slot wins); dead rows none
     for (int r = tid; r < R; r += blockDim.x) {
-        const int b = find_block(a.off, a.nb, r);
-        const bool lv = !a.live || a.live[r] != 0;
+        const bool lv = s_live[r];
         int dup = 0;
-        int ids[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < k) ids[j] = a.topk_idx[(size_t)r * k + j];
         for (int j = 0; j < k; ++j) {
             a.inv[(size_t)r * k + j] = -1;
-            const int e = ids[j];
+            const int e = s_ids[r * k + j];
             if (!lv || e < 0 || e >= E) continue;
-            if (!((a.keep[(size_t)b * words + (e >> 5)] >> (e & 31)) & 1u)) continue;
-            if (s_slot[r][e] != 0xFF) { ++dup; continue; }
+            const uint8_t st = s_slot[r][e];
+            if (st == kDropped) continue;
+            if (st != kFree) { ++dup; continue; }
             s_slot[r][e] = (uint8_t)j;
         }
         if (dup) atomicAdd(&s_dup, dup);
@@ -345,7 +365,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
     // per expert: its rows (walk the rows in order)
     for (int e = tid; e < E; e += blockDim.x) {
         int n = 0;
-        for (int r = 0; r < R; ++r) n += s_slot[r][e] != 0xFF;
+        for (int r = 0; r < R; ++r) n += s_slot[r][e] < 32;
         s_cnt[e] = n;
     }
     __syncthreads();
@@ -376,9 +396,9 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
         int pos = pp;
         for (int r = 0; r < R && pos < pp + n; ++r) {
             const int j = s_slot[r][f];
-            if (j == 0xFF) continue;
+            if (j >= 32) continue;
             a.pair_row[pos] = r;
-            a.pair_w[pos] = a.w_renorm[(size_t)r * k + j];
+            a.pair_w[pos] = s_w[r * k + j];
             a.inv[(size_t)r * k + j] = pos;
             ++pos;
         }
