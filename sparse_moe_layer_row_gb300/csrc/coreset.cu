@@ -13,7 +13,11 @@
 //     fp32 encoding and the product formed in 128 bits;
 //   * experts ranked by (Q desc, id asc); the coreset is the shortest prefix
 //     of that order whose mass reaches theta: its size is the number of ranks
-//     whose exclusive prefix mass is still below theta;
+//     whose exclusive prefix mass is still below theta.  The ranks come from
+//     one 64-bit key per expert: with many blocks (CTAs sharing SMs, so
+//     throughput counts) a bitonic sort of the keys in shared memory; with
+//     few, each thread counts the keys above its own (no barriers: the
+//     single CTA's latency counts).  Both give the same ranks;
 //   * an expert budget B > 0 (InfiniLM PR #604, Summary, names it without
 //     defining it) keeps at most the first B experts of that order; rows are
 //     copied unchanged only when tau >= 1 and nothing is dropped.
@@ -24,6 +28,7 @@ namespace moe {
 
 constexpr int kCoreThreads = 256;
 constexpr int kMaxE = 1024;
+constexpr int kSortBlocks = 64;   // blocks from which the ranks come from a sort
 
 __device__ __forceinline__ uint64_t mass_threshold(float tau, uint64_t T) {
     const uint32_t u = __float_as_uint(tau);
@@ -123,36 +128,70 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
     } else {
         const uint64_t theta = disabled ? ~0ull : mass_threshold(a.tau, T);
         // Order (Q desc, id asc) as one 64-bit key per expert: (Q << 10 | (1023 - e)) + 1
-        // for touched experts, 0 otherwise (Q < 2^53: a block has fewer than 2^21 rows).
-        for (int e = tid; e < E; e += blockDim.x)
-            keys[e] = ((touched[e >> 5] >> (e & 31)) & 1u)
+        // for touched experts, 0 otherwise (Q < 2^53: a block has fewer than 2^21 rows);
+        // keys are unique, and Q and e can be read back from a key.
+        int n = 32;
+        while (n < E) n <<= 1;
+        for (int e = tid; e < n; e += blockDim.x)
+            keys[e] = (e < E && ((touched[e >> 5] >> (e & 31)) & 1u))
                           ? ((unsigned long long)Q[e] << 10 | (unsigned long long)(1023 - e)) + 1ull
                           : 0ull;
         __syncthreads();
-        // An expert is in the coreset iff the mass of the experts ranked above it
-        // is still below theta: the greedy prefix in (Q desc, id asc) order stops
-        // at the first expert whose inclusion reaches theta.
-        // ... and, under the budget, iff fewer than `cap` experts rank above it
-        for (int e = tid; e < E; e += blockDim.x) {
-            const unsigned long long ke = keys[e];
-            if (!ke) continue;
-            unsigned long long above = 0;
-            int rank = 0;
-            int f = 0;
-            for (; f + 8 <= E; f += 8) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const bool gt = keys[f + j] > ke;
-                    above += gt ? Q[f + j] : 0ull;
-                    rank += gt;
+        if (gridDim.x >= kSortBlocks) {
+            // bitonic sort, descending
+            for (int kk = 2; kk <= n; kk <<= 1) {
+                for (int j = kk >> 1; j > 0; j >>= 1) {
+                    for (int i = tid; i < n; i += blockDim.x) {
+                        const int ixj = i ^ j;
+                        if (ixj > i) {
+                            const unsigned long long x = keys[i], y = keys[ixj];
+                            if ((i & kk) == 0 ? x < y : x > y) { keys[i] = y; keys[ixj] = x; }
+                        }
+                    }
+                    __syncthreads();
                 }
             }
-            for (; f < E; ++f) {
-                const bool gt = keys[f] > ke;
-                above += gt ? Q[f] : 0ull;
-                rank += gt;
+            // rank i is kept iff the mass ranked above it is still below theta (the
+            // greedy prefix stops at the first expert whose inclusion reaches it)
+            // and, under the budget, i < cap
+            const int per = (n + blockDim.x - 1) / blockDim.x;
+            const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+            uint64_t part2 = 0;
+            for (int i = i0; i < i1; ++i) part2 += keys[i] ? (keys[i] - 1ull) >> 10 : 0ull;
+            uint64_t tot2;
+            uint64_t above = block_excl_scan_u64(part2, warp_sums, &tot2);
+            for (int i = i0; i < i1; ++i) {
+                const unsigned long long key = keys[i];
+                if (!key) break;   // untouched experts sort last
+                if ((disabled || above < theta) && i < cap) {
+                    const int e = 1023 - (int)((key - 1ull) & 1023ull);
+                    atomicOr(&incore[e >> 5], 1u << (e & 31));
+                }
+                above += (key - 1ull) >> 10;
             }
-            if ((disabled || above < theta) && rank < cap) atomicOr(&incore[e >> 5], 1u << (e & 31));
+        } else {
+            // each thread ranks its experts: the keys above it and their mass
+            for (int e = tid; e < E; e += blockDim.x) {
+                const unsigned long long ke = keys[e];
+                if (!ke) continue;
+                unsigned long long above = 0;
+                int rank = 0;
+                int f = 0;
+                for (; f + 8 <= E; f += 8) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const bool gt = keys[f + j] > ke;
+                        above += gt ? Q[f + j] : 0ull;
+                        rank += gt;
+                    }
+                }
+                for (; f < E; ++f) {
+                    const bool gt = keys[f] > ke;
+                    above += gt ? Q[f] : 0ull;
+                    rank += gt;
+                }
+                if ((disabled || above < theta) && rank < cap) atomicOr(&incore[e >> 5], 1u << (e & 31));
+            }
         }
     }
     __syncthreads();

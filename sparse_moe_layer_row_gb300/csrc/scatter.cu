@@ -328,10 +328,11 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
     }
     if (tid == 0) s_dup = 0;
     __syncthreads();
-    for (int i = tid; i < R * E; i += blockDim.x) {
-        const int r = i / E, e = i - r * E;
-        const uint32_t kw = a.keep[(size_t)s_blk[r] * words + (e >> 5)];
-        s_slot[r][e] = ((kw >> (e & 31)) & 1u) ? kFree : kDropped;
+    for (int i = tid; i < R * words; i += blockDim.x) {   // one keep word per thread
+        const int r = i / words, wd = i - r * words;
+        const uint32_t kw = a.keep[(size_t)s_blk[r] * words + wd];
+        for (int bit = 0; bit < 32 && wd * 32 + bit < E; ++bit)
+            s_slot[r][wd * 32 + bit] = ((kw >> bit) & 1u) ? kFree : kDropped;
     }
     if (tid < 32) {  // live rows in order (R <= 32): the shared expert's rows
         const bool lv = tid < R && s_live[tid];
