@@ -236,3 +236,17 @@ def test_tensor_core_router_nonfinite_rows_fall_back():
     case = Case(w, T=T, bias=bias)
     g, ref = _route_only(case)
     assert (g["idx"][:, :6] >= 26).all()
+
+
+@pytest.mark.parametrize("rows", [(32,), (8,) * 80], ids=["one-block", "80-blocks"])
+def test_largest_expert_count(rows):
+    """E = 1024 (the largest supported), k = 8: the coreset's per-thread ranking
+    (one block) and its sort over 1024 keys (80 blocks, >= 64), and the scatter's
+    1024-column slot table."""
+    w = _small(E=1024, k=8, rows=rows, H=256, I=64, Is=64)
+    _full(Case(w), rows=list(range(0, w.R, 11)))
+
+
+def test_top32_of_64():
+    """k = 32 (the largest supported) with 64 experts over 3 blocks."""
+    _full(Case(_small(E=64, k=32, rows=(32, 17, 5))))
