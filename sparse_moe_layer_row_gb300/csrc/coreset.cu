@@ -16,8 +16,8 @@
 //     whose exclusive prefix mass is still below theta.  The ranks come from
 //     one 64-bit key per expert: with many blocks (CTAs sharing SMs, so
 //     throughput counts) a bitonic sort of the keys in shared memory; with
-//     few, each thread counts the keys above its own (no barriers: the
-//     single CTA's latency counts).  Both give the same ranks;
+//     few, a group of lanes counts the keys above each expert's own (no
+//     barriers: the single CTA's latency counts).  Both give the same ranks;
 //   * an expert budget B > 0 (InfiniLM PR #604, Summary, names it without
 //     defining it) keeps at most the first B experts of that order; rows are
 //     copied unchanged only when tau >= 1 and nothing is dropped.
@@ -26,7 +26,8 @@
 
 namespace moe {
 
-constexpr int kCoreThreads = 256;
+constexpr int kCoreThreads = 1024;      // few blocks: more threads rank each expert
+constexpr int kCoreThreadsSort = 256;   // many blocks (the sorting path)
 constexpr int kMaxE = 1024;
 constexpr int kSortBlocks = 64;   // blocks from which the ranks come from a sort
 
@@ -170,27 +171,30 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
                 above += (key - 1ull) >> 10;
             }
         } else {
-            // each thread ranks its experts: the keys above it and their mass
-            for (int e = tid; e < E; e += blockDim.x) {
-                const unsigned long long ke = keys[e];
-                if (!ke) continue;
+            // tpe threads (consecutive lanes) rank an expert together: each
+            // counts the keys above it in every tpe-th slot and their mass,
+            // and the lanes add their counts
+            int tpe = 1;
+            while (tpe < 32 && tpe * 2 * E <= (int)blockDim.x) tpe <<= 1;
+            const int q = tid & (tpe - 1), per_round = blockDim.x / tpe;
+            for (int base = 0; base < E; base += per_round) {   // the same trip count for all
+                const int e = base + tid / tpe;
+                const unsigned long long ke = e < E ? keys[e] : 0ull;
                 unsigned long long above = 0;
                 int rank = 0;
-                int f = 0;
-                for (; f + 8 <= E; f += 8) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const bool gt = keys[f + j] > ke;
-                        above += gt ? Q[f + j] : 0ull;
+                if (ke) {
+                    for (int f = q; f < E; f += tpe) {
+                        const bool gt = keys[f] > ke;
+                        above += gt ? Q[f] : 0ull;
                         rank += gt;
                     }
                 }
-                for (; f < E; ++f) {
-                    const bool gt = keys[f] > ke;
-                    above += gt ? Q[f] : 0ull;
-                    rank += gt;
+                for (int o = tpe >> 1; o > 0; o >>= 1) {
+                    above += __shfl_xor_sync(0xffffffffu, above, o);
+                    rank += __shfl_xor_sync(0xffffffffu, rank, o);
                 }
-                if ((disabled || above < theta) && rank < cap) atomicOr(&incore[e >> 5], 1u << (e & 31));
+                if (ke && q == 0 && (disabled || above < theta) && rank < cap)
+                    atomicOr(&incore[e >> 5], 1u << (e & 31));
             }
         }
     }
@@ -237,7 +241,8 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
 
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t st) {
     if (a.nb <= 0) return cudaSuccess;
-    return launch_kernel(k_coreset, dim3(a.nb), dim3(kCoreThreads), 0, st, a);
+    return launch_kernel(k_coreset, dim3(a.nb),
+                         dim3(a.nb >= kSortBlocks ? kCoreThreadsSort : kCoreThreads), 0, st, a);
 }
 
 }  // namespace moe
