@@ -434,6 +434,37 @@ def run_gpu(args, w: W.Workload):
                                 "pairs": lpairs, "forward_us": 1e3 * statistics.median(ts)}
     torch.cuda.synchronize()
 
+    # several layers as one pass (informational): each layer its own weights, the
+    # pass captured as one CUDA graph and replayed behind the same L2 flush
+    stack_info = None
+    if args.layers > 1:
+        import dataclasses
+        stack_layers, biases = [layer], [T.bias]
+        for i in range(1, args.layers):
+            wi = dataclasses.replace(w, w_seed=w.w_seed + 1000 * i)
+            Ti = W.make_tensors(wi, device=dev, x_seed=x_seed)
+            stack_layers.append(moe_block.MoeBlockLayer(
+                Ti.w_router, Ti.w_gate, Ti.w_up, Ti.w_down, Ti.ws_gate, Ti.ws_up, Ti.ws_down,
+                k=w.k, max_rows=w.R, max_blocks=w.nb))
+            biases.append(Ti.bias)
+        stack = moe_block.MoeStack(stack_layers)   # every layer reads the block's x
+        g_stack, _ = stack.capture(T.x, T.block_offsets, w.tau, biases)
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(min(args.steps, 50) + 3):
+                flush_l2(i)
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                g_stack.replay()
+                b_.record(stream)
+                b_.synchronize()
+                if i >= 3:
+                    ts.append(a_.elapsed_time(b_))
+        t_pass = 1e3 * statistics.median(ts)
+        stack_info = {"layers": args.layers, "pass_us": t_pass, "per_layer_us": t_pass / args.layers,
+                      "launches_per_pass": 1}
+    torch.cuda.synchronize()
+
     # end to end through the public API with host buffers (pinned), no graph
     x_host = T.x.cpu().pin_memory()
     off_host = T.block_offsets.cpu().pin_memory()
@@ -512,6 +543,8 @@ def run_gpu(args, w: W.Workload):
     }
     if live_us:
         line["live_pass"] = live_us
+    if stack_info:
+        line["stack"] = stack_info
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x_seed, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
@@ -530,6 +563,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=1,
+                    help="also time a pass over this many layers (own weights each) captured "
+                         "as one CUDA graph, reported under stack")
     ap.add_argument("--live-fracs", type=lambda v: [float(t) for t in v.split(",") if t],
                     default=[], help="also time live-row passes with these live fractions "
                                      "(comma separated), reported under live_pass")

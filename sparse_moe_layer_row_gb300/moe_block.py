@@ -350,3 +350,46 @@ class MoeBlockLayer:
 
     def status(self, stream=None) -> dict:
         return moe_read_device_status(self.workspace, stream)
+
+
+class MoeStack:
+    """Several MoE layers of one pass, enqueued back to back on one stream with
+    no host synchronisation, so that ``capture`` can record the whole pass as
+    one CUDA graph and a replay submits it as one launch (model card
+    "Clover-35B-A3B-Preview -- CMF", Hardware: every pass as one GPU submission).
+    Layer i reads ``xs[i]``: what a model computes between its MoE layers
+    (attention, norms, the residual stream) is the caller's, and its kernels can
+    be captured into the same graph around these calls.
+    """
+
+    def __init__(self, layers):
+        self.layers = list(layers)
+        if not self.layers:
+            raise ValueError("a stack needs at least one layer")
+
+    def __call__(self, xs, block_offsets, tau: float, biases=None, stream=None):
+        """Runs every layer on its input (``xs``: one tensor per layer, or one
+        tensor for all) and returns the layers' outputs."""
+        if isinstance(xs, torch.Tensor):
+            xs = [xs] * len(self.layers)
+        if len(xs) != len(self.layers):
+            raise ValueError("one input per layer")
+        return [layer(x, block_offsets, tau, bias=None if biases is None else biases[i],
+                      stream=stream)
+                for i, (layer, x) in enumerate(zip(self.layers, xs))]
+
+    def capture(self, xs, block_offsets, tau: float, biases=None):
+        """Record one pass over the static inputs ``xs`` as a CUDA graph.  Returns
+        (graph, outputs); ``graph.replay()`` reruns the pass on whatever the inputs
+        and ``block_offsets`` then hold and rewrites ``outputs`` in place."""
+        dev = block_offsets.device
+        stream = torch.cuda.Stream(device=dev)
+        stream.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(stream):
+            self(xs, block_offsets, tau, biases)   # warm-up outside the capture
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            outs = self(xs, block_offsets, tau, biases)
+        torch.cuda.current_stream(dev).wait_stream(stream)
+        return graph, outs
