@@ -518,7 +518,9 @@ def run_gpu(args, w: W.Workload):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "algorithmic_bytes_per_launch": acc["gu_bytes"]}
-    roof = {"bound": roof.pop("bound"), "kernel": "k_gemm gate/up (tcgen05)", **roof,
+    gu_kernel = ("k_gemm<kGateUp, 32, 5> (tcgen05)" if w.R <= moe_block.SMALL_ROWS
+                 else "k_gateup_pair (tcgen05 cta_group::2)")
+    roof = {"bound": roof.pop("bound"), "kernel": gu_kernel, **roof,
             "traffic": traffic, "launch_us": t_gu * 1e6, "peak_source": peaks["source"]}
     step_frac = max(acc["step_bytes"] / (peaks["hbm_gbs"] * 1e9),
                     acc["step_flops"] / (peaks["bf16_tflops_sustained"] * 1e12)) / t_step

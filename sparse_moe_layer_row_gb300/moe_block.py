@@ -294,6 +294,9 @@ def live_pass_mask(pass_index: int, live, refresh: int = 5):
     return None if pass_index % refresh == 0 else live
 
 
+SMALL_ROWS = 32   # calls of at most this many rows take the weight-streaming kernels
+
+
 class MoeBlockLayer:
     """The whole pass: route -> coreset -> forward, with its own workspace and buffers.
 
