@@ -134,3 +134,32 @@ def test_live_pass_schedule():
     assert mb.live_pass_mask(3, live, refresh=1) is None
     with pytest.raises(ValueError):
         mb.live_pass_mask(0, live, refresh=0)
+
+
+def test_stack_dispatch_on_cpu():
+    """MoeStack hands layer i its own input and bias (host logic, fake layers)."""
+    calls = []
+
+    class Fake:
+        def __init__(self, i):
+            self.i = i
+
+        def __call__(self, x, off, tau, bias=None, stream=None):
+            calls.append((self.i, x, bias, tau))
+            return ("y", self.i)
+
+    st = mb.MoeStack([Fake(0), Fake(1), Fake(2)])
+    xs = [torch.zeros(1), torch.ones(1), torch.full((1,), 2.0)]
+    outs = st(xs, torch.zeros(2, dtype=torch.int32), 0.9, biases=["b0", None, "b2"])
+    assert outs == [("y", 0), ("y", 1), ("y", 2)]
+    assert [c[0] for c in calls] == [0, 1, 2]
+    assert all(c[1] is x for c, x in zip(calls, xs))
+    assert [c[2] for c in calls] == ["b0", None, "b2"]
+    calls.clear()
+    one = torch.zeros(1)
+    st(one, torch.zeros(2, dtype=torch.int32), 0.5)
+    assert all(c[1] is one and c[2] is None for c in calls)
+    with pytest.raises(ValueError):
+        st(xs[:2], torch.zeros(2, dtype=torch.int32), 0.9)
+    with pytest.raises(ValueError):
+        mb.MoeStack([])
