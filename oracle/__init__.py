@@ -43,9 +43,9 @@ def _configure(L):
         L.moe_oracle_logit.restype = ctypes.c_float
         L.moe_oracle_logit.argtypes = [P, P, i]
         L.moe_oracle_route.restype = ctypes.c_long
-        L.moe_oracle_route.argtypes = [P, P, P, P, i, i, i, i, i, P, P, P, i]
+        L.moe_oracle_route.argtypes = [P, P, P, P, i, i, i, i, i, P, P, P, P, i]
         L.moe_oracle_coreset.restype = ctypes.c_long
-        L.moe_oracle_coreset.argtypes = [P, i, i, i, i, P, P, ctypes.c_float, P, P, P, P, i]
+        L.moe_oracle_coreset.argtypes = [P, i, i, i, i, P, P, P, ctypes.c_float, P, P, P, P, i]
         L.moe_oracle_expert_ffn.restype = None
         L.moe_oracle_expert_ffn.argtypes = [P, P, P, P, i, i, P]
         L.moe_oracle_forward.restype = ctypes.c_int
@@ -79,12 +79,16 @@ def logit(x_row: np.ndarray, w_row: np.ndarray) -> float:
     return float(lib().moe_oracle_logit(_ptr(x_row), _ptr(w_row), x_row.shape[0]))
 
 
-def route(x, w_router, block_offsets, k, bias=None, want_logits=False, nthreads=1):
+def route(x, w_router, block_offsets, k, bias=None, want_logits=False, nthreads=1,
+          want_probs=False):
     """Router logits -> top-k (z desc, id asc) -> softmax over the selected k.
 
     Model card "Clover-35B-A3B-Preview -- CMF", intro (256 experts, top-8).
     Returns (topk_idx int32 [R,k], topk_w fp32 [R,k], logits fp32 [R,E] or None,
-    number of non-finite logits).
+    number of non-finite logits).  With ``want_probs`` a fifth value: topk_p fp32
+    [R,k], the selected experts' probabilities under the full softmax over all E
+    experts (reading 3b: the other mass reading of "90% of its routing",
+    InfiniLM PR #604, Summary).
     """
     x, w_router = _u16(x), _u16(w_router)
     R, H = x.shape
@@ -95,22 +99,27 @@ def route(x, w_router, block_offsets, k, bias=None, want_logits=False, nthreads=
     idx = np.zeros((R, k), np.int32)
     w = np.zeros((R, k), np.float32)
     z = np.zeros((R, E), np.float32) if want_logits else None
+    p = np.zeros((R, k), np.float32) if want_probs else None
     nf = lib().moe_oracle_route(_ptr(x), _ptr(w_router), _ptr(b), _ptr(off), nb, R, H, E, k,
-                                _ptr(idx), _ptr(w), _ptr(z), int(nthreads))
+                                _ptr(idx), _ptr(w), _ptr(p), _ptr(z), int(nthreads))
     if nf < 0:
         raise ValueError("oracle route: invalid arguments")
+    if want_probs:
+        return idx, w, z, int(nf), p
     return idx, w, z, int(nf)
 
 
-def coreset(block_offsets, topk_idx, topk_w, E, tau, max_experts=0):
+def coreset(block_offsets, topk_idx, topk_w, E, tau, max_experts=0, mass=None):
     """Per-block coreset carrying >= tau of the block's routing mass, then renormalise.
 
     Model card "Clover-35B-A3B-Preview -- CMF", Usage (90% of the block's
     routing); InfiniLM PR #604, Summary (block coreset routing; expert budget).
     max_experts > 0 caps the coreset at that many experts: the first ones of
     the (mass desc, id asc) order (the pages name the budget only; this is the
-    reading taken).  Returns (keep uint32 [nb, ceil(E/32)], core_size int32 [nb],
-    w_renorm fp32 [R,k], n_empty int32 [nb], n_bad_ids).
+    reading taken).  ``mass`` (fp32 [R,k], e.g. the topk_p of ``route``) gives
+    the slots' masses; None takes them from topk_w.  The renormalised weights
+    always come from topk_w.  Returns (keep uint32 [nb, ceil(E/32)], core_size
+    int32 [nb], w_renorm fp32 [R,k], n_empty int32 [nb], n_bad_ids).
     """
     off = np.ascontiguousarray(block_offsets, dtype=np.int32)
     nb = off.shape[0] - 1
@@ -122,7 +131,10 @@ def coreset(block_offsets, topk_idx, topk_w, E, tau, max_experts=0):
     cs = np.zeros(nb, np.int32)
     wr = np.zeros((R, k), np.float32)
     ne = np.zeros(nb, np.int32)
-    bad = lib().moe_oracle_coreset(_ptr(off), nb, R, E, k, _ptr(idx), _ptr(w),
+    m = None if mass is None else np.ascontiguousarray(mass, dtype=np.float32)
+    if m is not None and m.shape != idx.shape:
+        raise ValueError("mass must have the shape of topk_idx")
+    bad = lib().moe_oracle_coreset(_ptr(off), nb, R, E, k, _ptr(idx), _ptr(w), _ptr(m),
                                    ctypes.c_float(tau), _ptr(keep), _ptr(cs), _ptr(wr), _ptr(ne),
                                    int(max_experts))
     if bad < 0:

@@ -32,8 +32,17 @@
  *     w_j = a_j / S.  exp_c is a Cody-Waite reduction (ln 2 split into a
  *     12-significant-bit head and a tail) with a degree-7 Taylor polynomial
  *     evaluated by Horner's rule in fmaf, scaled by 2^n through the exponent.
- *  4. Block mass: q = trunc(w * 2^32) as an exact integer; Q_e = sum of q over
- *     the block's rows that selected e; T = sum_e Q_e.
+ *  3b. Probability mass (the other reading of "90% of its routing", InfiniLM
+ *     PR #604, Summary; model card, Usage): the mass of slot j is the
+ *     unnormalised probability p_j = a_j / D of the full softmax over all E
+ *     experts, D = sum over every expert e of exp_c(z_e - z_max) in a fixed
+ *     order: "lane" p (0..31) sums the experts e = p, p + 32, p + 64, ... in
+ *     ascending e, and the 32 lane sums are combined by the same xor
+ *     butterfly as the logits (o = 16, 8, 4, 2, 1).  Only the coreset mass
+ *     changes; the renormalised weights still come from w.
+ *  4. Block mass: q = trunc(w * 2^32) (or trunc(p * 2^32) under 3b) as an exact
+ *     integer; Q_e = sum of q over the block's rows that selected e;
+ *     T = sum_e Q_e.
  *  5. Coreset: tau >= 1 keeps every touched expert and leaves w unchanged.
  *     Otherwise theta = ceil(tau * T) computed exactly (tau is the fp32 value
  *     M * 2^-s), experts ordered by (Q descending, id ascending), and the
@@ -145,6 +154,7 @@ typedef struct {
     int R, H, E, k;
     int32_t* topk_idx;
     float* topk_w;
+    float* topk_p;      /* [R, k] probability mass (reading 3b) or NULL */
     float* logits;      /* [R, E] or NULL */
     int r0, r1;
     long nonfinite;
@@ -187,6 +197,22 @@ static void route_rows(route_job* J) {
         }
         float* w = J->topk_w + (size_t)r * J->k;
         for (int j = 0; j < J->k; ++j) w[j] = a[j] / S;
+        if (J->topk_p) {
+            /* reading 3b: the full-softmax denominator in the lane order */
+            float d[32];
+            for (int p = 0; p < 32; ++p) {
+                float acc = 0.0f;
+                for (int e = p; e < J->E; e += 32) acc = acc + moe_oracle_exp_c(z[e] - m);
+                d[p] = acc;
+            }
+            for (int o = 16; o >= 1; o >>= 1) {
+                float t[32];
+                for (int p = 0; p < 32; ++p) t[p] = d[p] + d[p ^ o];
+                memcpy(d, t, sizeof d);
+            }
+            float* pj = J->topk_p + (size_t)r * J->k;
+            for (int j = 0; j < J->k; ++j) pj[j] = a[j] / d[0];
+        }
     }
     free(z);
     free(taken);
@@ -204,11 +230,13 @@ static int check_offsets(const int32_t* off, int nb, int R) {
     return 1;
 }
 
-/* Route every row.  bias: [nb, E] fp32 or NULL.  logits: [R, E] or NULL.
+/* Route every row.  bias: [nb, E] fp32 or NULL.  topk_p: [R, k] probability
+ * mass of reading 3b, or NULL.  logits: [R, E] or NULL.
  * Returns the number of non-finite logits (>= 0) or ORC_ERR_ARG. */
 long moe_oracle_route(const uint16_t* x, const uint16_t* wr, const float* bias,
                       const int32_t* block_offsets, int nb, int R, int H, int E, int k,
-                      int32_t* topk_idx, float* topk_w, float* logits, int nthreads) {
+                      int32_t* topk_idx, float* topk_w, float* topk_p, float* logits,
+                      int nthreads) {
     if (!x || !wr || !topk_idx || !topk_w || H <= 0 || H % 256 || E <= 0 || k <= 0 ||
         k > E || k > 64 || R < 0 || !check_offsets(block_offsets, nb, R))
         return ORC_ERR_ARG;
@@ -220,7 +248,7 @@ long moe_oracle_route(const uint16_t* x, const uint16_t* wr, const float* bias,
     route_job* jobs = (route_job*)calloc((size_t)nthreads, sizeof(route_job));
     pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
     for (int t = 0; t < nthreads; ++t) {
-        route_job j = {x, wr, bias, bor, R, H, E, k, topk_idx, topk_w, logits,
+        route_job j = {x, wr, bias, bor, R, H, E, k, topk_idx, topk_w, topk_p, logits,
                        (int)((long)R * t / nthreads), (int)((long)R * (t + 1) / nthreads), 0};
         jobs[t] = j;
     }
@@ -256,10 +284,12 @@ static uint64_t mass_threshold(float tau, uint64_t T) {
     return (uint64_t)q;
 }
 
-/* One block of rows [r0, r1).  Outputs keep bits [E/32 words], core size,
- * w_renorm for the block's rows, and the number of empty rows. */
+/* Every block of rows.  Outputs keep bits [E/32 words], core size, w_renorm
+ * and the number of empty rows per block.  topk_mass: [R, k] masses of the
+ * slots (reading 3b), or NULL for the weights w themselves (reading 4). */
 long moe_oracle_coreset(const int32_t* block_offsets, int nb, int R, int E, int k,
-                        const int32_t* topk_idx, const float* topk_w, float tau,
+                        const int32_t* topk_idx, const float* topk_w,
+                        const float* topk_mass, float tau,
                         uint32_t* keep, int32_t* core_size, float* w_renorm,
                         int32_t* n_empty, int max_experts) {
     if (!topk_idx || !topk_w || !keep || !core_size || !w_renorm || E <= 0 || k <= 0 ||
@@ -281,8 +311,9 @@ long moe_oracle_coreset(const int32_t* block_offsets, int nb, int R, int E, int 
                 int e = topk_idx[(size_t)r * k + j];
                 if (e < 0 || e >= E) { bad++; continue; }
                 touched[e] = 1;
-                float wj = topk_w[(size_t)r * k + j];
-                /* w is in [0, 1]; anything else (NaN) carries no mass */
+                /* the mass of the slot: w, or p under reading 3b */
+                float wj = (topk_mass ? topk_mass : topk_w)[(size_t)r * k + j];
+                /* a mass is in [0, 1]; anything else (NaN) carries no mass */
                 if (wj >= 0.0f && wj <= 1.0f) Q[e] += (uint64_t)ldexpf(wj, 32);
             }
         int nt = 0;

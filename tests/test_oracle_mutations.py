@@ -43,6 +43,18 @@ MUTATIONS = {
                              "memset(yr, 0, sizeof(double) * (size_t)J->H);"),
     "down_proj_transposed": ("const uint16_t* dh = wd + (size_t)h * I;",
                              "const uint16_t* dh = wd + (size_t)(h % I) * I;"),
+    "weight_sum_in_id_order": (
+        "            S = S + a[j];\n        }",
+        "        }\n        for (int e = 0; e < J->E; ++e)\n"
+        "            for (int j = 0; j < J->k; ++j)\n"
+        "                if (idx[j] == e) S = S + a[j];"),
+    "prob_denominator_in_id_order": (
+        "for (int e = p; e < J->E; e += 32) acc = acc + moe_oracle_exp_c(z[e] - m);",
+        "if (p == 0) for (int e = 0; e < J->E; ++e) acc = acc + moe_oracle_exp_c(z[e] - m);"),
+    "prob_denominator_drops_butterfly": ("for (int p = 0; p < 32; ++p) t[p] = d[p] + d[p ^ o];",
+                                         "for (int p = 0; p < 32; ++p) t[p] = d[p];"),
+    "prob_mass_ignored": ("float wj = (topk_mass ? topk_mass : topk_w)[(size_t)r * k + j];",
+                          "float wj = topk_w[(size_t)r * k + j];"),
 }
 
 PINS = [
@@ -56,7 +68,11 @@ PINS = [
     pins.test_expert_ffn_hand_value, pins.test_expert_ffn_matches_dense_fp64,
     pins.test_forward_matches_dense_moe_fp64,
     pins.test_coreset_budget_hand_example,
-] + [lambda m, s=s: pins.test_coreset_brute_force_random_tiny(m, s) for s in range(4)] \
+    pins.test_weight_sum_in_rank_order_hand_case,
+    pins.test_prob_mass_denominator_in_lane_order_hand_case,
+    pins.test_prob_mass_equals_full_softmax, pins.test_coreset_prob_mass_changes_membership,
+] + [lambda m, s=s: pins.test_coreset_prob_mass_brute_force_random_tiny(m, s) for s in range(2)] \
+  + [lambda m, s=s: pins.test_coreset_brute_force_random_tiny(m, s) for s in range(4)] \
   + [lambda m, s=s: pins.test_coreset_budget_brute_force_random_tiny(m, s) for s in range(4)]
 
 

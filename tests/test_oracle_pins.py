@@ -250,6 +250,93 @@ def test_weights_equal_full_softmax_then_renormalised(oracle_mod):
         assert all(a >= b for a, b in zip(wt[r], wt[r][1:]))
 
 
+def _softmax_hand_case(name):
+    """A case of tests/golden/softmax_sums_hand.json as oracle inputs: one row with
+    x one-hot at h = 0 and router rows whose element 0 is the wanted logit."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "softmax_sums_hand.json")
+    with open(path) as f:
+        fx = json.load(f)
+    c = next(c for c in fx["cases"] if c["name"] == name)
+    x = np.zeros((1, c["H"]), np.float32)
+    x[0, 0] = 1.0
+    wr = np.zeros((c["E"], c["H"]), np.float32)
+    wr[:, 0] = c["other_logit"]
+    for e, z in c["logits"].items():
+        wr[int(e), 0] = z
+    return c, fx["delta_arg"], bf16_bits(x), bf16_bits(wr)
+
+
+def _hand_values(exprs, delta):
+    """Values of the fixture's expressions in fp32 (1, delta, 1 - 2^-23, delta / (1 + 2^-23))."""
+    one, d = np.float32(1.0), np.float32(delta)
+    table = {"1": one, "delta": d, "1 - 2^-23": np.float32(1.0 - 2.0 ** -23),
+             "delta / (1 + 2^-23)": np.float32(d / np.float32(1.0 + 2.0 ** -23))}
+    return np.array([table[e] for e in exprs], np.float32)
+
+
+def test_weight_sum_in_rank_order_hand_case(oracle_mod):
+    """S = a_0 + ... + a_(k-1) summed in rank order, pinned at the bit level by a
+    hand-worked row where rank order and id order give different fp32 sums
+    (tests/golden/softmax_sums_hand.json, "S in rank order")."""
+    c, darg, x, wr = _softmax_hand_case("S in rank order")
+    delta = oracle_mod.exp_c(darg)
+    # the derivation's premise: 1 + delta rounds to 1, 1 + 2 delta does not
+    assert 2.0 ** -25 < delta < 2.0 ** -24
+    assert np.float32(1.0) + np.float32(delta) == np.float32(1.0)
+    assert np.float32(1.0) + np.float32(2 * delta) == np.float32(1.0 + 2.0 ** -23)
+    idx, wt, _, _ = oracle_mod.route(x, wr, [0, 1], c["k"])
+    assert idx[0].tolist() == c["topk_idx"]
+    assert np.array_equal(wt[0].view(np.uint32), _hand_values(c["topk_w"], delta).view(np.uint32))
+
+
+def test_prob_mass_denominator_in_lane_order_hand_case(oracle_mod):
+    """The probability-mass reading: D = sum over all experts of exp_c(z_e - z_max)
+    in the lane order (lane p sums experts p, p + 32, ...; then the xor
+    butterfly), pinned at the bit level by a hand-worked row
+    (tests/golden/softmax_sums_hand.json, "D in lane order")."""
+    c, darg, x, wr = _softmax_hand_case("D in lane order")
+    delta = oracle_mod.exp_c(darg)
+    assert 2.0 ** -25 < delta < 2.0 ** -24
+    idx, wt, _, _, p = oracle_mod.route(x, wr, [0, 1], c["k"], want_probs=True)
+    assert idx[0].tolist() == c["topk_idx"]
+    assert np.array_equal(wt[0].view(np.uint32), _hand_values(c["topk_w"], delta).view(np.uint32))
+    assert p[0, 0].view(np.uint32) == 0x3F7FFFFE
+    assert np.array_equal(p[0].view(np.uint32), _hand_values(c["topk_p"], delta).view(np.uint32))
+
+
+def test_prob_mass_equals_full_softmax(oracle_mod):
+    """p_j = the selected experts' probabilities under the softmax over all E
+    experts (fp64 reference, within the fp32 summation and exp_c error), with
+    p_j / w_j the same ratio S / D for every slot of a row."""
+    w = W.BLOCK32
+    x = u16(W.make_x(w))
+    wr = u16(W.make_router(w))
+    idx, wt, z, nf, p = oracle_mod.route(x, wr, w.block_offsets(), w.k, want_logits=True,
+                                         want_probs=True)
+    assert nf == 0
+    for r in range(w.R):
+        zz = z[r].astype(np.float64)
+        full = np.exp(zz - zz.max())
+        full /= full.sum()
+        assert np.allclose(p[r], full[idx[r]], rtol=2e-5, atol=0)
+        ratio = p[r].astype(np.float64) / wt[r].astype(np.float64)
+        assert np.allclose(ratio, ratio[0], rtol=4e-7, atol=0)
+        assert float(p[r].astype(np.float64).sum()) < 1.0
+        assert all(a >= b for a, b in zip(p[r], p[r][1:]))
+
+
+def test_prob_mass_same_ids_and_weights(oracle_mod):
+    """Asking for the probability mass changes neither the ids nor the weights."""
+    w = W.TINY
+    T = W.make_tensors(w)
+    a = oracle_mod.route(u16(T.x), u16(T.w_router), w.block_offsets(), w.k)
+    b = oracle_mod.route(u16(T.x), u16(T.w_router), w.block_offsets(), w.k, want_probs=True)
+    assert np.array_equal(a[0], b[0])
+    assert np.array_equal(a[1].view(np.uint32), b[1].view(np.uint32))
+
+
 def test_nan_logits_rank_last(oracle_mod):
     w = W.TINY
     T = W.make_tensors(w)
@@ -407,6 +494,71 @@ def test_coreset_budget_brute_force_random_tiny(oracle_mod, seed):
             for j in range(k):
                 expect = np.float32(wt[r, j] / s) if (j in surv and s > 0) else np.float32(0)
                 assert wr[r, j] == expect
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_coreset_prob_mass_brute_force_random_tiny(oracle_mod, seed):
+    """Masses given apart from the weights (the probability-mass reading): each row's
+    masses are its weights times its own factor in (0, 1), so the rows carry unequal
+    mass.  The kept set is the minimal one reaching ceil(tau * T) of those masses
+    (brute force), the greedy prefix under (mass desc, id asc); the rows are still
+    renormalised from their weights."""
+    rng = np.random.default_rng(200 + seed)
+    E, k, nb, off, idx, wt = _random_tiny_blocks(rng)
+    R = idx.shape[0]
+    scale = (rng.random(R).astype(np.float32) * np.float32(0.9) + np.float32(0.05))
+    mass = (wt * scale[:, None]).astype(np.float32)
+    tau = float(np.float32(rng.choice([0.5, 0.75, 0.9, 0.95])))
+    B = int(rng.integers(0, E + 1)) if seed % 2 else 0
+    keep, cs, wr, ne, bad = oracle_mod.coreset(off, idx, wt, E, tau, max_experts=B, mass=mass)
+    for b in range(nb):
+        Q, touched = _masses(idx, mass, off[b], off[b + 1], E)
+        cmin, _ = _brute_min_size(Q, touched, _theta(tau, sum(Q)))
+        size = min(cmin, B) if B > 0 else cmin
+        order = sorted(touched, key=lambda e: (-Q[e], e))
+        core = [e for e in range(E) if keep[b, e // 32] >> (e % 32) & 1]
+        assert cs[b] == len(core) == size
+        assert core == sorted(order[:size])
+        for r in range(off[b], off[b + 1]):
+            surv = [j for j in range(k) if idx[r, j] in core]
+            s = np.float32(0)
+            for j in surv:
+                s = np.float32(s + wt[r, j])
+            for j in range(k):
+                expect = np.float32(wt[r, j] / s) if (j in surv and s > 0) else np.float32(0)
+                assert wr[r, j] == expect
+
+
+def test_coreset_prob_mass_changes_membership(oracle_mod):
+    """Unequal row masses change some block's coreset against the weight reading
+    (so the pin above checks the mass input and not only the weights)."""
+    changed = 0
+    for seed in range(200, 220):
+        rng = np.random.default_rng(seed)
+        E, k, nb, off, idx, wt = _random_tiny_blocks(rng)
+        scale = (rng.random(idx.shape[0]).astype(np.float32) * np.float32(0.9) + np.float32(0.05))
+        mass = (wt * scale[:, None]).astype(np.float32)
+        a = oracle_mod.coreset(off, idx, wt, E, 0.75, mass=mass)[0]
+        b = oracle_mod.coreset(off, idx, wt, E, 0.75)[0]
+        changed += not np.array_equal(a, b)
+    assert changed >= 3
+
+
+def test_coreset_prob_mass_on_full_shape_block(oracle_mod):
+    """The 32-row block under the probability mass: invariants of the cut (mass >=
+    theta, the prefix one shorter below it) on the masses q = trunc(p * 2^32)."""
+    w = W.BLOCK32
+    x = u16(W.make_x(w))
+    wrt = u16(W.make_router(w))
+    idx, wt, _, _, p = oracle_mod.route(x, wrt, w.block_offsets(), w.k, want_probs=True)
+    keep, cs, wr, ne, bad = oracle_mod.coreset(w.block_offsets(), idx, wt, w.E, w.tau, mass=p)
+    Q, touched = _masses(idx, p, 0, w.R, w.E)
+    theta = _theta(w.tau, sum(Q))
+    core = [e for e in range(w.E) if keep[0, e // 32] >> (e % 32) & 1]
+    order = sorted(touched, key=lambda e: (-Q[e], e))
+    assert core == sorted(order[:cs[0]])
+    assert sum(Q[e] for e in core) >= theta > sum(Q[e] for e in order[:cs[0] - 1])
+    assert bad == 0
 
 
 def test_coreset_budget_hand_example(oracle_mod):
