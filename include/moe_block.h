@@ -118,6 +118,28 @@ moe_status moe_block_route(const moe_plan* plan, const void* x, int32_t R,
                            int32_t* topk_idx, float* topk_w, void* workspace,
                            size_t workspace_bytes, moe_stream_t stream);
 
+/* Router with the probability mass (the other reading of the coreset's mass).
+ * (InfiniLM PR #604, Summary: preview passes use "block coreset routing";
+ * model card, Usage: "90% of its routing".  The pages do not say whether a
+ * slot's mass is its renormalised top-k weight or its probability under the
+ * softmax over all experts; moe_block_route serves the first reading, this
+ * call the second.)
+ * As moe_block_route, and in addition
+ *   topk_p  [R, k] fp32 out (device): p_j = a_j / D, the selected experts'
+ *           probabilities under the softmax over all E experts, with
+ *           a_j = exp_c(z_j - z_0) as for topk_w and D = sum over every expert e
+ *           of exp_c(z_e - z_0) in a fixed order (lane p of 32 adds the experts
+ *           p, p + 32, ... in ascending e; the 32 lane sums combine by the xor
+ *           butterfly of the logits), then one IEEE division.
+ * topk_idx and topk_w are bit-identical to moe_block_route's.  D needs the exact
+ * logit of every expert, so calls of >= 256 rows take the fixed-order router
+ * for all experts instead of the tensor-core screen (slower, same ids).
+ * topk_p NULL: this is moe_block_route.  Errors as moe_block_route. */
+moe_status moe_block_route_probs(const moe_plan* plan, const void* x, int32_t R,
+                                 const int32_t* block_offsets, int32_t nb, const float* logit_bias,
+                                 int32_t* topk_idx, float* topk_w, float* topk_p, void* workspace,
+                                 size_t workspace_bytes, moe_stream_t stream);
+
 /* Block coreset and renormalisation.
  * (Model card, Usage: the block's experts restricted to the set carrying 90% of
  * its routing; InfiniLM PR #604, Notes: full-route replay = coreset disabled.)
@@ -154,6 +176,25 @@ moe_status moe_block_coreset_budget(const moe_plan* plan, int32_t R, const int32
                                     float tau, int32_t max_experts, uint32_t* keep,
                                     int32_t* core_size, float* w_renorm, int32_t* n_empty,
                                     void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* Block coreset with the slots' masses given apart from the weights.
+ * (InfiniLM PR #604, Summary; model card, Usage: the mass "90% of its routing"
+ * is read either as the renormalised weights -- moe_block_coreset -- or as the
+ * probabilities under the full softmax -- topk_mass = the topk_p of
+ * moe_block_route_probs.)
+ * As moe_block_coreset_budget, with q = floor(topk_mass * 2^32) per (row, slot)
+ * in place of floor(topk_w * 2^32); a mass outside [0, 1] (or NaN) counts as 0.
+ * The renormalisation still divides topk_w (w_renorm is the same function of
+ * topk_w and the kept set); tau >= 1 with nothing dropped keeps topk_w bit for
+ * bit.
+ *   topk_mass  [R, k] fp32 (device), or NULL: the masses are topk_w
+ * Other arguments, outputs and errors: moe_block_coreset_budget. */
+moe_status moe_block_coreset_mass(const moe_plan* plan, int32_t R, const int32_t* block_offsets,
+                                  int32_t nb, const int32_t* topk_idx, const float* topk_w,
+                                  const float* topk_mass, float tau, int32_t max_experts,
+                                  uint32_t* keep, int32_t* core_size, float* w_renorm,
+                                  int32_t* n_empty, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream);
 
 /* Expert evaluation and combine.
  * (Model card, intro: top-8 experts plus a shared expert.)
@@ -201,8 +242,10 @@ moe_status moe_block_forward_live(const moe_plan* plan, const void* x, int32_t R
  * pages: an addition for deployment).  Some callers cannot hand the library a
  * workspace, e.g. an engine that reserves all of its device memory up front,
  * or a plugin allowed to touch only the buffers it is given.  This call does
- * what moe_block_route does, with the same kernel and bit-identical outputs,
- * but keeps the router's scratch (logits and tickets) in a 1 MiB array
+ * what moe_block_route does, with bit-identical outputs, through the
+ * fixed-order (SIMT) router (never the tensor-core screen that
+ * moe_block_route takes from 256 rows on, so it is slower there), and
+ * keeps the router's scratch (logits and tickets) in a 1 MiB array
  * compiled into the library, which every GPU that loads the library holds
  * until the library is unloaded.  The caller still passes x, block_offsets,
  * logit_bias, topk_idx and topk_w as for moe_block_route.
@@ -214,7 +257,8 @@ moe_status moe_block_forward_live(const moe_plan* plan, const void* x, int32_t R
  *     start of each call; calls that overlap on the GPU (other streams, other
  *     host threads) race on the array and must not be issued.
  *   - The first call on a device (with that device current) looks up the
- *     array's device address; make it before any stream capture.
+ *     array's device address; make it before any stream capture.  Calls
+ *     outside a capture look it up again; calls inside one reuse the last.
  *   - Non-finite logits are counted in the array, not reported. */
 moe_status moe_block_route_noalloc(const moe_plan* plan, const void* x, int32_t R,
                                    const int32_t* block_offsets, int32_t nb,

@@ -204,16 +204,27 @@ moe_status moe_block_route(const moe_plan* p, const void* x, int32_t R,
                            const int32_t* block_offsets, int32_t nb, const float* logit_bias,
                            int32_t* topk_idx, float* topk_w, void* workspace,
                            size_t workspace_bytes, moe_stream_t stream) {
+    return moe_block_route_probs(p, x, R, block_offsets, nb, logit_bias, topk_idx, topk_w, nullptr,
+                                 workspace, workspace_bytes, stream);
+}
+
+moe_status moe_block_route_probs(const moe_plan* p, const void* x, int32_t R,
+                                 const int32_t* block_offsets, int32_t nb, const float* logit_bias,
+                                 int32_t* topk_idx, float* topk_w, float* topk_p, void* workspace,
+                                 size_t workspace_bytes, moe_stream_t stream) {
     moe_status s = check_call(p, R, block_offsets, nb, workspace, workspace_bytes);
     if (s != MOE_OK) return s;
     if (!x || !aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
     if (!topk_idx || !topk_w || !aligned(topk_idx, 4) || !aligned(topk_w, 4))
         return fail(MOE_ERR_INVALID_ARG, "topk_idx/topk_w NULL or misaligned");
+    if (topk_p && !aligned(topk_p, 4)) return fail(MOE_ERR_INVALID_ARG, "topk_p misaligned");
     if (logit_bias && !aligned(logit_bias, 4)) return fail(MOE_ERR_INVALID_ARG, "logit_bias misaligned");
     if (R == 0) return ok();
     const Layout L = make_layout(p->d);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (p->tc_route && R >= kTcRouteMinRows) {
+    // the probabilities need the exact logit of every expert: the fixed-order
+    // router computes them all; the tensor-core screen only the candidates'
+    if (p->tc_route && R >= kTcRouteMinRows && !topk_p) {
         CUtensorMap tm_x;
         if (!encode_bf16(&tm_x, x, p->d.H, (uint64_t)R, 0, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
             return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for x");
@@ -232,7 +243,7 @@ moe_status moe_block_route(const moe_plan* p, const void* x, int32_t R,
     RouteArgs a{static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(p->wr),
                 logit_bias, block_offsets, R, p->d.H, p->d.E, p->d.k, nb,
                 at<float>(workspace, L.logits), at<uint32_t>(workspace, L.route_cnt), topk_idx,
-                topk_w, at<uint32_t>(workspace, L.status)};
+                topk_w, at<uint32_t>(workspace, L.status), topk_p};
     e = launch_route(a, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
     return ok();
@@ -252,18 +263,29 @@ moe_status moe_block_coreset_budget(const moe_plan* p, int32_t R, const int32_t*
                                     float tau, int32_t max_experts, uint32_t* keep,
                                     int32_t* core_size, float* w_renorm, int32_t* n_empty,
                                     void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    return moe_block_coreset_mass(p, R, block_offsets, nb, topk_idx, topk_w, nullptr, tau,
+                                  max_experts, keep, core_size, w_renorm, n_empty, workspace,
+                                  workspace_bytes, stream);
+}
+
+moe_status moe_block_coreset_mass(const moe_plan* p, int32_t R, const int32_t* block_offsets,
+                                  int32_t nb, const int32_t* topk_idx, const float* topk_w,
+                                  const float* topk_mass, float tau, int32_t max_experts,
+                                  uint32_t* keep, int32_t* core_size, float* w_renorm,
+                                  int32_t* n_empty, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream) {
     moe_status s = check_call(p, R, block_offsets, nb, workspace, workspace_bytes);
     if (s != MOE_OK) return s;
     if (!(tau > 0.0f)) return fail(MOE_ERR_INVALID_ARG, "tau=%g must be > 0 (and not NaN)", (double)tau);
     if (max_experts < 0) return fail(MOE_ERR_INVALID_ARG, "max_experts=%d must be >= 0", max_experts);
     if (!topk_idx || !topk_w || !keep || !core_size || !w_renorm)
         return fail(MOE_ERR_INVALID_ARG, "a required coreset pointer is NULL");
-    const void* ps[6] = {topk_idx, topk_w, keep, core_size, w_renorm, n_empty};
+    const void* ps[7] = {topk_idx, topk_w, keep, core_size, w_renorm, n_empty, topk_mass};
     for (const void* q : ps)
         if (q && !aligned(q, 4)) return fail(MOE_ERR_INVALID_ARG, "coreset pointer misaligned");
     const Layout L = make_layout(p->d);
-    CoresetArgs a{block_offsets, topk_idx, topk_w, R, p->d.E, p->d.k, nb, tau, max_experts, keep,
-                  core_size, w_renorm, n_empty, at<uint32_t>(workspace, L.status)};
+    CoresetArgs a{block_offsets, topk_idx, topk_w, topk_mass, R, p->d.E, p->d.k, nb, tau,
+                  max_experts, keep, core_size, w_renorm, n_empty, at<uint32_t>(workspace, L.status)};
     cudaError_t e = launch_coreset(a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "coreset launch");
     return ok();
@@ -325,7 +347,8 @@ moe_status moe_block_forward_live(const moe_plan* p, const void* x, int32_t R,
                 d.Is, R, static_cast<const __nv_bfloat16*>(x), at<__nv_bfloat16>(workspace, L.h),
                 at<__nv_bfloat16>(workspace, L.hs),
                 at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
-                at<__half>(workspace, L.ys), (int)L.max_pairs, at<uint32_t>(workspace, L.status),
+                at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
+                (int)(L.max_pairs + d.max_rows), (int)L.max_pairs, at<uint32_t>(workspace, L.status),
                 live ? at<int32_t>(workspace, L.shared_rows) : nullptr};
     // Under stream capture an event record must be an external node to be
     // recorded at every graph launch (a plain record only orders the capture).
@@ -348,7 +371,8 @@ moe_status moe_block_forward_live(const moe_plan* p, const void* x, int32_t R,
     gd.n_units = at<int32_t>(workspace, L.misc) + 2;
     if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, small, dn, gd, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
-    CombineArgs ca{at<__half>(workspace, L.ys), at<int32_t>(workspace, L.inv), R, d.H, d.k,
+    CombineArgs ca{at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
+                   (int)(L.max_pairs + d.max_rows), at<int32_t>(workspace, L.inv), R, d.H, d.k,
                    (int)L.max_pairs, static_cast<__nv_bfloat16*>(y), y_f32,
                    at<uint32_t>(workspace, L.status), live, at<int32_t>(workspace, L.shared_inv)};
     if ((e = mark(3)) == cudaSuccess) e = launch_combine(ca, p->num_sms, st);

@@ -38,6 +38,8 @@ struct Layout {
     size_t shared_inv;   // int32 [max_rows]          index of a row in shared_rows, or -1 (dead)
     size_t live_base;    // int32 [max_blocks]        live rows of a block, then rows before it
     size_t ys;           // fp16 [max_pairs + max_rows, H] staged per-pair and shared outputs
+    size_t ysx;          // uint8 [H / 32, max_pairs + max_rows] power-of-two exponent of each
+                         // 32-column quarter of a staged row (ys holds value * 2^-exponent)
     size_t total;
     int64_t max_pairs, max_units_gu, max_units_dn;
 };
@@ -84,6 +86,7 @@ inline Layout make_layout(const moe_dims& d) {
     L.shared_inv = take(sizeof(int32_t) * (size_t)R);
     L.live_base = take(sizeof(int32_t) * (size_t)d.max_blocks);
     L.ys = take(2 * (size_t)(P + R) * (size_t)H);
+    L.ysx = take((size_t)(H / 32) * (size_t)(P + R));
     L.total = o;
     return L;
 }

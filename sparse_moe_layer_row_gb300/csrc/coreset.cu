@@ -8,6 +8,10 @@
 //
 // The arithmetic is exact so that membership matches bit for bit:
 //   * q = floor(w * 2^32) per (row, slot) (w in [0, 1], the scaling is exact);
+//     w is the slot's routing weight, or, under the probability-mass reading
+//     (InfiniLM PR #604, Summary: "block coreset routing"; the pages do not fix
+//     the mass), its probability under the softmax over all experts, given
+//     apart from the weights; the renormalisation always divides the weights;
 //     Q_e = sum of q over the block (64-bit integers, any order);
 //   * theta = ceil(tau * T), T = sum_e Q_e, with tau = M * 2^-s taken from its
 //     fp32 encoding and the product formed in 128 bits;
@@ -105,7 +109,7 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
         const size_t i = (size_t)r0 * k + p;
         const int e = a.topk_idx[i];
         if (e < 0 || e >= E) { ++bad; continue; }
-        const float w = a.topk_w[i];
+        const float w = (a.mass ? a.mass : a.topk_w)[i];   // the slot's mass
         const unsigned long long q =
             (w >= 0.0f && w <= 1.0f) ? __float2ull_rz(__fmul_rn(w, 4294967296.0f)) : 0ull;
         atomicAdd(&Q[e], q);

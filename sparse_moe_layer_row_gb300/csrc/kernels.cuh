@@ -19,6 +19,7 @@ struct RouteArgs {
     int32_t* topk_idx;
     float* topk_w;
     uint32_t* status;
+    float* topk_p;        // [R, k] probabilities under the full softmax, or NULL
 };
 // Large-batch router (tensor-core screening + exact recompute of candidates).
 constexpr int kCandCap = 32;      // candidates kept per row before falling back
@@ -39,6 +40,7 @@ struct CoresetArgs {
     const int32_t* off;
     const int32_t* topk_idx;
     const float* topk_w;
+    const float* mass;    // [R, k] masses of the slots, or NULL: the masses are topk_w
     int R, E, k, nb;
     float tau;
     int max_experts;      // expert budget per block (<= 0: none)
@@ -76,6 +78,8 @@ struct ScatterArgs {
 // y[r] = shared output + sum over surviving slots (rank order) of staged outputs
 struct CombineArgs {
     const __half* ys;     // [max_pairs + max_rows, H] staged per-pair / shared outputs
+    const uint8_t* ysx;   // [H / 32, max_pairs + max_rows] exponent of each staged quarter row
+    int ld_x;             // max_pairs + max_rows (the staging rows)
     const int32_t* inv;   // [R * k]
     int R, H, k, shared_row0;
     __nv_bfloat16* y;
@@ -95,6 +99,8 @@ struct GemmArgs {
     const int32_t* pair_row;
     const float* pair_w;
     __half* ys;           // [max_pairs + max_rows, H] staged outputs (down GEMM)
+    uint8_t* ysx;         // [H / 32, max_pairs + max_rows] their quarter-row exponents
+    int ld_x;             // max_pairs + max_rows
     int shared_row0;      // staging row of the shared expert's row 0
     uint32_t* status;
     const int32_t* shared_rows;  // row of x of the shared expert's i-th row (NULL: i)

@@ -5,9 +5,11 @@
 // engine that reserves all of its device memory up front and forbids any
 // later cudaMalloc; a plugin that may only touch the buffers it is given; code
 // that must not grow its memory footprint while serving. For them this entry
-// point runs the same router kernel as moe_block_route, but its scratch (the
-// router logits and the row-group tickets) lives in a fixed array compiled into
-// the library instead of in a caller workspace.
+// point runs the fixed-order (SIMT) router, whose outputs are bit-identical to
+// moe_block_route's, with its scratch (the router logits and the row-group
+// tickets) in a fixed array compiled into the library instead of in a caller
+// workspace.  It never takes the tensor-core screen that moe_block_route uses
+// from 256 rows on, so there it is slower for the same ids and weights.
 //
 // Properties a user must know:
 //   * The array holds kNoAllocScratchBytes (1 MiB) on every GPU that loads the
@@ -22,7 +24,9 @@
 //     or different host threads) race on the array and must not be issued.
 //   * The first call on a device, with that device current, resolves the
 //     array's device address (cudaGetSymbolAddress). Make that first call
-//     before any stream capture; later calls only enqueue work.
+//     before any stream capture.  Calls outside a capture resolve the address
+//     again (it can move when the device's context is reset and the module
+//     reloaded); a call during a capture uses the address of the last call.
 //   * Non-finite logits are counted into a status word inside the array, which
 //     is not reported to the caller.
 #include <mutex>
@@ -42,17 +46,25 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices];        // device address of g_route_scratch, per device
 
-// Resolve the array's address on the current device (once per device).
-moe_status scratch_address(int device, unsigned char** out) {
+// The array's address on the current device.  Outside a stream capture it is
+// looked up every time (cheap; the address can change after a context reset);
+// during a capture, where the lookup is not allowed, the last one is used.
+moe_status scratch_address(int device, cudaStream_t st, unsigned char** out) {
     if (device < 0 || device >= kMaxDevices)
         return set_error(MOE_ERR_UNSUPPORTED, "device ordinal too large for the static scratch");
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess)
+        return set_error(MOE_ERR_CUDA, "cudaStreamIsCapturing failed");
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[device]) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
         if (e != cudaSuccess || !p)
             return set_error(MOE_ERR_CUDA, "cudaGetSymbolAddress of the router scratch failed");
         g_scratch_addr[device] = p;
+    } else if (!g_scratch_addr[device]) {
+        return set_error(MOE_ERR_INVALID_ARG,
+                         "first call on this device is inside a stream capture; call once before");
     }
     *out = static_cast<unsigned char*>(g_scratch_addr[device]);
     return MOE_OK;
@@ -91,10 +103,10 @@ extern "C" moe_status moe_block_route_noalloc(const moe_plan* plan, const void* 
     if (cudaGetDevice(&dev) != cudaSuccess || dev != pv.device)
         return set_error(MOE_ERR_INVALID_ARG, "current device is not the plan's device");
     if (R == 0) return set_error(MOE_OK, "");
-    unsigned char* base = nullptr;
-    moe_status s = scratch_address(dev, &base);
-    if (s != MOE_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char* base = nullptr;
+    moe_status s = scratch_address(dev, st, &base);
+    if (s != MOE_OK) return s;
     uint32_t* status = reinterpret_cast<uint32_t*>(base);
     uint32_t* cnt = reinterpret_cast<uint32_t*>(base + kStatusBytes);
     float* logits = reinterpret_cast<float*>(base + kStatusBytes + cnt_bytes);

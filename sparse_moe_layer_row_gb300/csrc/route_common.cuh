@@ -19,6 +19,11 @@
 //     12-significant-bit head 2839/4096 and an fp32 tail) followed by the
 //     degree-7 Taylor polynomial of e^r in Horner form with fused multiply-adds
 //     and a final scaling by 2^n through the exponent field.
+//   * on request, p_j = a_j / D, the selected experts' probabilities under the
+//     softmax over all E experts (the probability-mass reading of "90% of its
+//     routing", InfiniLM PR #604, Summary): D = sum over every expert e of
+//     exp_c(z_e - z_0), lane p adding the experts p, p + 32, ... in ascending
+//     e, the 32 lane sums combined by the same xor butterfly as the logits.
 #pragma once
 
 #include "kernels.cuh"
@@ -138,6 +143,23 @@ __device__ __forceinline__ void write_topk(int32_t* idx_out, float* w_out, int k
         idx_out[lane] = (int32_t)my_id;
         w_out[lane] = __fdiv_rn(aj, S);
     }
+}
+
+// The probability mass of the selected experts (lane j < k holds rank j):
+// p_j = exp_c(z_j - z_0) / D, with D over every expert of the row.  key[i] of
+// lane p is the key of expert p + 32 i (bit i of `valid`: the expert exists).
+template <int NI>
+__device__ __forceinline__ void write_topk_probs(float* p_out, int k, int lane,
+                                                 const uint32_t (&key)[NI], uint32_t valid,
+                                                 uint32_t my_key) {
+    const float m = __shfl_sync(0xffffffffu, key_value(my_key), 0);
+    float d = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+        if ((valid >> i) & 1u) d = __fadd_rn(d, exp_c(__fsub_rn(key_value(key[i]), m)));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) d = __fadd_rn(d, __shfl_xor_sync(0xffffffffu, d, o));
+    if (lane < k) p_out[lane] = __fdiv_rn(exp_c(__fsub_rn(key_value(my_key), m)), d);
 }
 
 }  // namespace moe

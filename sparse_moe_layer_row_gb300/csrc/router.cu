@@ -43,6 +43,7 @@ __device__ void route_topk_rows(const RouteArgs& a, int r0, int r1, int lane) {
         warp_topk<NE>(key, id, valid, a.k, lane, my_id, my_key);
         write_topk(a.topk_idx + (size_t)r * a.k, a.topk_w + (size_t)r * a.k, a.k, lane, my_id,
                    my_key);
+        if (a.topk_p) write_topk_probs<NE>(a.topk_p + (size_t)r * a.k, a.k, lane, key, valid, my_key);
     }
 }
 

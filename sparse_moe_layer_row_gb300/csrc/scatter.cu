@@ -419,7 +419,11 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
 // expert outputs, added in fp32 in rank order (shared first, then the slots;
 // dead rows of a live-row call are skipped);
 // lane owns 8 consecutive columns.  All of a task's contributions are loaded
-// before they are added, eight at a time, so the loads overlap.
+// before they are added, eight at a time, so the loads overlap.  A staged
+// value is v * 2^-s with s the exponent of its 32-column quarter (0 unless the
+// down GEMM met a magnitude of 2^15 or more there); the product by 2^s is exact.
+__device__ __forceinline__ float pow2_u8(uint32_t s) { return __uint_as_float((127u + s) << 23); }
+
 __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
     pdl_wait();  // see common.cuh: nothing global is touched before
     pdl_trigger();
@@ -434,37 +438,42 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
         const int c = (t - r * nchunk) * 256 + lane * 8;
         const int pos = lane < a.k ? a.inv[(size_t)r * a.k + lane] : -1;
         const int srow = a.live ? a.shared_inv[r] : r;  // staging row of the shared output
+        const uint8_t* xq = a.ysx + (size_t)(c >> 5) * a.ld_x;  // exponents of this quarter
         float acc[8];
         {
-            const uint4 v =
-                *reinterpret_cast<const uint4*>(a.ys + (size_t)(a.shared_row0 + srow) * a.H + c);
+            const size_t sr = (size_t)(a.shared_row0 + srow);
+            const uint4 v = *reinterpret_cast<const uint4*>(a.ys + sr * a.H + c);
+            const float sc = pow2_u8(xq[sr]);
             const __half2* hv = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float2 f = __half22float2(hv[i]);
-                acc[2 * i] = f.x;
-                acc[2 * i + 1] = f.y;
+                acc[2 * i] = f.x * sc;
+                acc[2 * i + 1] = f.y * sc;
             }
         }
         for (int j0 = 0; j0 < a.k; j0 += 8) {
             uint4 v[8];
+            uint32_t sx[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int p = __shfl_sync(0xffffffffu, pos, (j0 + j) & 31);
-                v[j] = (j0 + j < a.k && p >= 0)
-                           ? *reinterpret_cast<const uint4*>(a.ys + (size_t)p * a.H + c)
-                           : make_uint4(0, 0, 0, 0);
+                const bool on = j0 + j < a.k && p >= 0;
+                v[j] = on ? *reinterpret_cast<const uint4*>(a.ys + (size_t)p * a.H + c)
+                          : make_uint4(0, 0, 0, 0);
+                sx[j] = on ? xq[p] : 0u;
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int p = __shfl_sync(0xffffffffu, pos, (j0 + j) & 31);
                 if (j0 + j >= a.k || p < 0) continue;
+                const float sc = pow2_u8(sx[j]);
                 const __half2* hv = reinterpret_cast<const __half2*>(&v[j]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 f = __half22float2(hv[i]);
-                    acc[2 * i] += f.x;
-                    acc[2 * i + 1] += f.y;
+                    acc[2 * i] += f.x * sc;
+                    acc[2 * i + 1] += f.y * sc;
                 }
             }
         }

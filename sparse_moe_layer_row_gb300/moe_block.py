@@ -73,6 +73,11 @@ def load(build_if_missing: bool = False):
     L.moe_block_forward.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, sz, P]
     L.moe_block_forward_live.restype = ctypes.c_int
     L.moe_block_forward_live.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, P, sz, P]
+    L.moe_block_route_probs.restype = ctypes.c_int
+    L.moe_block_route_probs.argtypes = [P, P, i32, P, i32, P, P, P, P, P, sz, P]
+    L.moe_block_coreset_mass.restype = ctypes.c_int
+    L.moe_block_coreset_mass.argtypes = [P, i32, P, i32, P, P, P, ctypes.c_float, i32, P, P, P,
+                                         P, P, sz, P]
     L.moe_block_route_noalloc.restype = ctypes.c_int
     L.moe_block_route_noalloc.argtypes = [P, P, i32, P, i32, P, P, P, P]
     L.moe_plan_set_forward_events.restype = ctypes.c_int
@@ -179,7 +184,8 @@ class Plan:
 
 
 def moe_block_route(plan: Plan, x, block_offsets, logit_bias, topk_idx, topk_w, workspace,
-                    stream=None):
+                    stream=None, topk_p=None):
+    """moe_block_route, or moe_block_route_probs when ``topk_p`` (fp32 [R, k]) is given."""
     d = plan.dims
     R = x.shape[0]
     nb = block_offsets.shape[0] - 1
@@ -190,6 +196,13 @@ def moe_block_route(plan: Plan, x, block_offsets, logit_bias, topk_idx, topk_w, 
     _need(topk_idx, "topk_idx", torch.int32, (R, d.k))
     _need(topk_w, "topk_w", torch.float32, (R, d.k))
     _need(workspace, "workspace", torch.uint8)
+    if topk_p is not None:
+        _need(topk_p, "topk_p", torch.float32, (R, d.k))
+        _check(load().moe_block_route_probs(plan.handle, _ptr(x), R, _ptr(block_offsets), nb,
+                                            _ptr(logit_bias), _ptr(topk_idx), _ptr(topk_w),
+                                            _ptr(topk_p), _ptr(workspace), workspace.numel(),
+                                            _stream(stream)))
+        return
     _check(load().moe_block_route(plan.handle, _ptr(x), R, _ptr(block_offsets), nb,
                                   _ptr(logit_bias), _ptr(topk_idx), _ptr(topk_w),
                                   _ptr(workspace), workspace.numel(), _stream(stream)))
@@ -215,8 +228,10 @@ def moe_block_route_noalloc(plan: Plan, x, block_offsets, logit_bias, topk_idx, 
 
 
 def moe_block_coreset(plan: Plan, block_offsets, topk_idx, topk_w, tau: float, keep, core_size,
-                      w_renorm, n_empty, workspace, stream=None, max_experts: int = 0):
-    """moe_block_coreset, or moe_block_coreset_budget when max_experts != 0."""
+                      w_renorm, n_empty, workspace, stream=None, max_experts: int = 0,
+                      mass=None):
+    """moe_block_coreset; moe_block_coreset_budget when max_experts != 0;
+    moe_block_coreset_mass when ``mass`` (fp32 [R, k], e.g. topk_p) is given."""
     d = plan.dims
     R = topk_idx.shape[0]
     nb = block_offsets.shape[0] - 1
@@ -229,6 +244,14 @@ def moe_block_coreset(plan: Plan, block_offsets, topk_idx, topk_w, tau: float, k
     if n_empty is not None:
         _need(n_empty, "n_empty", torch.int32, (nb,))
     _need(workspace, "workspace", torch.uint8)
+    if mass is not None:
+        _need(mass, "mass", torch.float32, (R, d.k))
+        _check(load().moe_block_coreset_mass(plan.handle, R, _ptr(block_offsets), nb,
+                                             _ptr(topk_idx), _ptr(topk_w), _ptr(mass),
+                                             ctypes.c_float(tau), int(max_experts), _ptr(keep),
+                                             _ptr(core_size), _ptr(w_renorm), _ptr(n_empty),
+                                             _ptr(workspace), workspace.numel(), _stream(stream)))
+        return
     if max_experts:
         _check(load().moe_block_coreset_budget(plan.handle, R, _ptr(block_offsets), nb,
                                                _ptr(topk_idx), _ptr(topk_w), ctypes.c_float(tau),
@@ -323,19 +346,28 @@ class MoeBlockLayer:
         self._empty = torch.empty(nb, dtype=torch.int32, device=dev)
         self._y = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
 
-    def route(self, x, block_offsets, bias=None, stream=None):
+    def route(self, x, block_offsets, bias=None, stream=None, probs=False):
+        """Returns (topk_idx, topk_w), and topk_p as a third value with ``probs``."""
         R = x.shape[0]
         idx, w = self._topk_idx[:R], self._topk_w[:R]
+        if probs:
+            if not hasattr(self, "_topk_p"):
+                self._topk_p = torch.empty_like(self._topk_w)
+            p = self._topk_p[:R]
+            moe_block_route(self.plan, x, block_offsets, bias, idx, w, self.workspace, stream,
+                            topk_p=p)
+            return idx, w, p
         moe_block_route(self.plan, x, block_offsets, bias, idx, w, self.workspace, stream)
         return idx, w
 
-    def coreset(self, block_offsets, topk_idx, topk_w, tau, stream=None, max_experts=0):
+    def coreset(self, block_offsets, topk_idx, topk_w, tau, stream=None, max_experts=0,
+                mass=None):
         R = topk_idx.shape[0]
         nb = block_offsets.shape[0] - 1
         keep, core, empty = self._keep[:nb], self._core[:nb], self._empty[:nb]
         wr = self._w_renorm[:R]
         moe_block_coreset(self.plan, block_offsets, topk_idx, topk_w, tau, keep, core, wr, empty,
-                          self.workspace, stream, max_experts=max_experts)
+                          self.workspace, stream, max_experts=max_experts, mass=mass)
         return keep, core, wr, empty
 
     def forward(self, x, block_offsets, topk_idx, w_renorm, keep, y=None, y_f32=None,
@@ -370,29 +402,41 @@ class MoeStack:
         if not self.layers:
             raise ValueError("a stack needs at least one layer")
 
-    def __call__(self, xs, block_offsets, tau: float, biases=None, stream=None):
+    def __call__(self, xs, block_offsets, tau: float, biases=None, stream=None, ys=None):
         """Runs every layer on its input (``xs``: one tensor per layer, or one
-        tensor for all) and returns the layers' outputs."""
+        tensor for all) and returns the layers' outputs: ``ys`` (one bf16 [R, H]
+        tensor per layer) when given, else each layer's own output buffer, which
+        the layer's next call overwrites."""
         if isinstance(xs, torch.Tensor):
             xs = [xs] * len(self.layers)
         if len(xs) != len(self.layers):
             raise ValueError("one input per layer")
+        if ys is not None and len(ys) != len(self.layers):
+            raise ValueError("one output per layer")
         return [layer(x, block_offsets, tau, bias=None if biases is None else biases[i],
-                      stream=stream)
+                      stream=stream, y=None if ys is None else ys[i])
                 for i, (layer, x) in enumerate(zip(self.layers, xs))]
 
     def capture(self, xs, block_offsets, tau: float, biases=None):
         """Record one pass over the static inputs ``xs`` as a CUDA graph.  Returns
         (graph, outputs); ``graph.replay()`` reruns the pass on whatever the inputs
-        and ``block_offsets`` then hold and rewrites ``outputs`` in place."""
+        and ``block_offsets`` then hold and rewrites ``outputs`` in place.  The
+        outputs are tensors of the graph's own, so eager calls of the same layers
+        (or other graphs over them) do not overwrite them; the layers' workspaces
+        are shared, so replays and eager calls of the same layers must not run
+        concurrently."""
         dev = block_offsets.device
+        outs = []
+        xl = [xs] * len(self.layers) if isinstance(xs, torch.Tensor) else list(xs)
+        for layer, x in zip(self.layers, xl):
+            outs.append(torch.empty(x.shape[0], layer.dims.H, dtype=torch.bfloat16, device=dev))
         stream = torch.cuda.Stream(device=dev)
         stream.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(stream):
-            self(xs, block_offsets, tau, biases)   # warm-up outside the capture
+            self(xs, block_offsets, tau, biases, ys=outs)   # warm-up outside the capture
         stream.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            outs = self(xs, block_offsets, tau, biases)
+            self(xs, block_offsets, tau, biases, ys=outs)
         torch.cuda.current_stream(dev).wait_stream(stream)
         return graph, outs

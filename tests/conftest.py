@@ -18,3 +18,17 @@ def oracle_mod():
     import oracle
     oracle.lib()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Worst output element of every GPU parity comparison, as a fraction of the
+    tolerance (1.0 = at the tolerance)."""
+    try:
+        from tests.parity_util import WORST
+    except Exception:
+        return
+    if not WORST:
+        return
+    terminalreporter.write_sep("-", "parity: worst element / tolerance")
+    for key in sorted(WORST):
+        terminalreporter.write_line(f"{WORST[key]:.4f}  {key}")

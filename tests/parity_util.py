@@ -17,6 +17,10 @@ from sparse_moe_layer_row_gb300 import moe_block, workloads as W
 ATOL = 2e-3
 RTOL = 1e-2
 
+# worst element of each output comparison as a fraction of the tolerance,
+# keyed by test and output (printed in the session summary, see conftest.py)
+WORST: dict = {}
+
 
 def u16(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -47,11 +51,17 @@ class Case:
             self.T.ws_up, self.T.ws_down, k=w.k, max_rows=max(self.R, 1), max_blocks=self.nb)
         moe_block.moe_clear_device_status(self.layer.workspace)
 
-    def run(self, tau: float | None = None, max_experts: int = 0):
+    def run(self, tau: float | None = None, max_experts: int = 0, probs: bool = False):
+        """route -> coreset -> forward on the GPU.  ``probs``: the probability-mass
+        reading (moe_block_route_probs, then moe_block_coreset_mass with topk_p)."""
         tau = self.w.tau if tau is None else tau
         L = self.layer
-        idx, wt = L.route(self.x, self.off, self.bias)
-        keep, core, wr, empty = L.coreset(self.off, idx, wt, tau, max_experts=max_experts)
+        p = None
+        if probs:
+            idx, wt, p = L.route(self.x, self.off, self.bias, probs=True)
+        else:
+            idx, wt = L.route(self.x, self.off, self.bias)
+        keep, core, wr, empty = L.coreset(self.off, idx, wt, tau, max_experts=max_experts, mass=p)
         y32 = torch.empty(self.R, self.w.H, dtype=torch.float32, device=self.dev)
         y = L.forward(self.x, self.off, idx, wr, keep, y_f32=y32)
         torch.cuda.synchronize()
@@ -60,24 +70,30 @@ class Case:
                         wr=wr.cpu().numpy().copy(), empty=empty.cpu().numpy().copy(),
                         y=y.float().cpu().numpy().astype(np.float64),
                         y32=y32.cpu().numpy().astype(np.float64))
+        if p is not None:
+            self.gpu["p"] = p.cpu().numpy().copy()
         self.status = L.status()
         return self.gpu
 
     # ---- oracle side
-    def oracle_route(self, nthreads=None):
+    def oracle_route(self, nthreads=None, probs: bool = False):
         nthreads = nthreads or oracle.default_threads()
         off = self.off.cpu().numpy()
         bias = None if self.bias is None else self.bias.cpu().numpy()
-        idx, wt, z, nf = oracle.route(u16(self.x), u16(self.T.w_router), off, self.w.k,
-                                      bias=bias, nthreads=nthreads)
+        out = oracle.route(u16(self.x), u16(self.T.w_router), off, self.w.k, bias=bias,
+                           nthreads=nthreads, want_probs=probs)
+        idx, wt, z, nf = out[:4]
         self.ref = dict(idx=idx, w=wt, nonfinite=nf, off=off)
+        if probs:
+            self.ref["p"] = out[4]
         return self.ref
 
-    def oracle_coreset(self, tau=None, max_experts: int = 0):
+    def oracle_coreset(self, tau=None, max_experts: int = 0, probs: bool = False):
         tau = self.w.tau if tau is None else tau
         r = self.ref
         keep, core, wr, empty, bad = oracle.coreset(r["off"], r["idx"], r["w"], self.w.E, tau,
-                                                    max_experts=max_experts)
+                                                    max_experts=max_experts,
+                                                    mass=r["p"] if probs else None)
         r.update(keep=keep, core=core, wr=wr, empty=empty)
         return r
 
@@ -108,6 +124,8 @@ def assert_route_equal(gpu, ref):
     assert np.array_equal(gpu["idx"], ref["idx"]), (
         f"top-k ids differ in {int((gpu['idx'] != ref['idx']).any(axis=1).sum())} rows")
     assert np.array_equal(bits32(gpu["w"]), bits32(ref["w"])), "router weights differ"
+    if "p" in gpu or "p" in ref:
+        assert np.array_equal(bits32(gpu["p"]), bits32(ref["p"])), "probability masses differ"
 
 
 def assert_coreset_equal(gpu, ref):
@@ -118,10 +136,19 @@ def assert_coreset_equal(gpu, ref):
 
 
 def assert_close(got, ref, rows=None, what="y"):
+    """Elementwise |got - ref| <= ATOL + RTOL |ref| on every element (or on ``rows``).
+    Records the worst element as a fraction of its tolerance under the running
+    test's name; returns the largest absolute error."""
+    import os
     if rows is not None:
         got, ref = got[list(rows)], ref[list(rows)]
     err = np.abs(got - ref)
-    bad = err > ATOL + RTOL * np.abs(ref)
+    tol = ATOL + RTOL * np.abs(ref)
+    bad = err > tol
+    frac = float((err / tol).max()) if err.size else 0.0
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    key = f"{test} {what} ({got.shape[0]} rows)"
+    WORST[key] = max(WORST.get(key, 0.0), frac)
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "
-                           f"max abs err {err.max():.3e}")
+                           f"max abs err {err.max():.3e}, worst {frac:.3f} of the tolerance")
     return float(err.max())

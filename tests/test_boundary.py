@@ -144,9 +144,9 @@ def test_stack_dispatch_on_cpu():
         def __init__(self, i):
             self.i = i
 
-        def __call__(self, x, off, tau, bias=None, stream=None):
-            calls.append((self.i, x, bias, tau))
-            return ("y", self.i)
+        def __call__(self, x, off, tau, bias=None, stream=None, y=None):
+            calls.append((self.i, x, bias, tau, y))
+            return ("y", self.i) if y is None else y
 
     st = mb.MoeStack([Fake(0), Fake(1), Fake(2)])
     xs = [torch.zeros(1), torch.ones(1), torch.full((1,), 2.0)]
@@ -161,5 +161,12 @@ def test_stack_dispatch_on_cpu():
     assert all(c[1] is one and c[2] is None for c in calls)
     with pytest.raises(ValueError):
         st(xs[:2], torch.zeros(2, dtype=torch.int32), 0.9)
+    # given outputs go to the layers in order and come back
+    calls.clear()
+    ys = ["o0", "o1", "o2"]
+    assert st(one, torch.zeros(2, dtype=torch.int32), 0.5, ys=ys) == ys
+    assert [c[4] for c in calls] == ys
+    with pytest.raises(ValueError):
+        st(one, torch.zeros(2, dtype=torch.int32), 0.5, ys=ys[:1])
     with pytest.raises(ValueError):
         mb.MoeStack([])

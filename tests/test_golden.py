@@ -106,3 +106,47 @@ def test_cuda_coreset_hand_cases(c):
     assert keep[:, 0].cpu().tolist() == c["keep_bits"]
     assert np.array_equal(wr.cpu().numpy(), np.array(c["w_renorm"], np.float32))
     assert ne.cpu().tolist() == c["n_empty"]
+
+
+SOFTMAX = _load("softmax_sums_hand.json")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", SOFTMAX["cases"], ids=lambda c: c["name"])
+def test_cuda_softmax_sums_hand_cases(c):
+    """The CUDA router (moe_block_route_probs) on the hand-worked rows of
+    softmax_sums_hand.json: the weight sum in rank order and the full-softmax
+    denominator in lane order, bit for bit."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import oracle
+    from sparse_moe_layer_row_gb300 import moe_block
+    dev = torch.device("cuda", 0)
+    E, k, H, I = c["E"], c["k"], c["H"], 64
+    wr = torch.zeros(E, H, dtype=torch.float32)
+    wr[:, 0] = c["other_logit"]
+    for e, z in c["logits"].items():
+        wr[int(e), 0] = z
+    x = torch.zeros(1, H, dtype=torch.float32)
+    x[0, 0] = 1.0
+    z = torch.zeros(E, I, H, dtype=torch.bfloat16, device=dev)
+    zs = torch.zeros(I, H, dtype=torch.bfloat16, device=dev)
+    plan = moe_block.Plan(moe_block.moe_dims(H, E, k, I, I, 1, 1), wr.to(torch.bfloat16).to(dev),
+                          z, z, torch.zeros(E, H, I, dtype=torch.bfloat16, device=dev), zs, zs,
+                          torch.zeros(H, I, dtype=torch.bfloat16, device=dev))
+    ws = plan.new_workspace()
+    idx = torch.empty(1, k, dtype=torch.int32, device=dev)
+    w = torch.empty(1, k, dtype=torch.float32, device=dev)
+    p = torch.empty(1, k, dtype=torch.float32, device=dev)
+    off = torch.tensor([0, 1], dtype=torch.int32, device=dev)
+    moe_block.moe_block_route(plan, x.to(torch.bfloat16).to(dev), off, None, idx, w, ws, topk_p=p)
+    torch.cuda.synchronize()
+    delta = np.float32(oracle.exp_c(SOFTMAX["delta_arg"]))
+    table = {"1": np.float32(1.0), "delta": delta, "1 - 2^-23": np.float32(1.0 - 2.0 ** -23),
+             "delta / (1 + 2^-23)": np.float32(delta / np.float32(1.0 + 2.0 ** -23))}
+    assert idx[0].cpu().tolist() == c["topk_idx"]
+    want_w = np.array([table[e] for e in c["topk_w"]], np.float32)
+    assert np.array_equal(w[0].cpu().numpy().view(np.uint32), want_w.view(np.uint32))
+    if "topk_p" in c:
+        want_p = np.array([table[e] for e in c["topk_p"]], np.float32)
+        assert np.array_equal(p[0].cpu().numpy().view(np.uint32), want_p.view(np.uint32))

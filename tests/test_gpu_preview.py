@@ -1,9 +1,12 @@
 """Preview variants of the routing (InfiniLM PR #604): top-4 preview routing
-(Motivation) and an expert budget on the block coreset (Summary; the pages name
+(Motivation), an expert budget on the block coreset (Summary; the pages name
 the budget without defining it: here a cap on the experts a block keeps, the
-first ones of the coreset order).  The CUDA path through the C ABI against the
-oracle on the same seeded inputs: routing, membership and weights bit for bit,
-outputs within the tolerance of parity_util."""
+first ones of the coreset order) and the probability-mass reading of the
+coreset (Summary "block coreset routing", model card Usage "90% of its
+routing": a slot's mass is its probability under the softmax over all
+experts).  The CUDA path through the C ABI against the oracle on the same
+seeded inputs: routing, probabilities, membership and weights bit for bit,
+outputs on every row within the tolerance of parity_util."""
 from __future__ import annotations
 
 import dataclasses
@@ -78,9 +81,9 @@ def test_top4_preview_many_blocks():
     assert_route_equal(gpu, case.ref)
     case.oracle_coreset(max_experts=48)
     assert_coreset_equal(gpu, case.ref)
-    rows = list(range(0, w.R, 97))
-    y = case.oracle_forward(rows=rows)
-    assert_close(gpu["y32"], y, rows=rows, what="y_f32")
+    y = case.oracle_forward()
+    assert_close(gpu["y32"], y, what="y_f32")
+    assert_close(gpu["y"], y, what="y")
 
 
 def test_budget_rejects_negative():
@@ -88,3 +91,49 @@ def test_budget_rejects_negative():
     idx, wt = case.layer.route(case.x, case.off)
     with pytest.raises(moe_block.MoeError):
         case.layer.coreset(case.off, idx, wt, 0.9, max_experts=-1)
+
+
+PROB_WORKLOADS = [W.TINY, W.BLOCK32, W.BLOCKS16_ZIPF, W.BY_NAME["rows2048-b8-tau0.9"],
+                  W.PREFILL8192]
+
+
+@pytest.mark.parametrize("w", PROB_WORKLOADS, ids=lambda w: w.name)
+def test_prob_mass_bit_exact(w):
+    """moe_block_route_probs + moe_block_coreset_mass: ids, weights and the
+    full-softmax probabilities bit for bit, the coreset under those masses bit for
+    bit, and the outputs of every row within tolerance."""
+    case = Case(w)
+    gpu = case.run(probs=True)
+    case.oracle_route(probs=True)
+    assert_route_equal(gpu, case.ref)
+    case.oracle_coreset(probs=True)
+    assert_coreset_equal(gpu, case.ref)
+    y = case.oracle_forward()
+    assert_close(gpu["y32"], y, what="y_f32")
+    assert_close(gpu["y"], y, what="y")
+    assert case.status["wait_timeout"] == 0 and case.status["bad_expert_id"] == 0
+
+
+def test_prob_mass_with_budget_and_same_ids():
+    """The probability router gives the ids and weights of the plain router bit for
+    bit; with a budget the coreset still follows the oracle."""
+    case = Case(W.BLOCKS16_ZIPF)
+    plain = {k: v.copy() for k, v in case.run().items()}
+    gpu = case.run(probs=True, max_experts=12)
+    assert np.array_equal(plain["idx"], gpu["idx"])
+    assert np.array_equal(plain["w"].view(np.uint32), gpu["w"].view(np.uint32))
+    case.oracle_route(probs=True)
+    case.oracle_coreset(probs=True, max_experts=12)
+    assert_coreset_equal(gpu, case.ref)
+    assert (gpu["core"] <= 12).all()
+
+
+def test_prob_mass_rejects_misaligned():
+    case = Case(W.TINY)
+    L = case.layer
+    idx, wt, p = L.route(case.x, case.off, probs=True)
+    buf = torch.empty(p.numel() + 1, dtype=torch.float32, device=p.device)
+    bad = buf[1:].view(p.shape)
+    with pytest.raises(moe_block.MoeError):
+        moe_block.moe_block_coreset(L.plan, case.off, idx, wt, 0.9, L._keep[:1], L._core[:1],
+                                    L._w_renorm[:case.R], None, L.workspace, mass=bad)

@@ -74,3 +74,9 @@ def test_stack_graph_replay_is_one_submission():
     torch.cuda.synchronize()
     for a, b in zip(replayed, again):
         assert torch.equal(a, b)
+    # the graph's outputs are its own: eager calls of the layers leave them alone
+    x.copy_(W.make_x(base, device="cuda", seed=base.x_seed + 2))
+    stack(x, off, base.tau)
+    torch.cuda.synchronize()
+    for a, b in zip(outs, replayed):
+        assert torch.equal(a, b)

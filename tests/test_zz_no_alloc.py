@@ -74,3 +74,23 @@ def test_noalloc_route_rejects_calls_beyond_its_scratch(setup):
     moe_block.moe_block_route_noalloc(layer.plan, x, off, None, idx, wt)
     torch.cuda.synchronize()
     assert torch.equal(idx, ref_idx) and torch.equal(wt, ref_w)
+
+
+def test_noalloc_route_with_non_finite_logits_is_silent(setup):
+    """A NaN and a -inf logit in one row (through the bias): the call still returns
+    MOE_OK (the non-finite count stays inside the library's array and is not
+    reported), that row ranks them last as moe_block_route does, and every row
+    matches moe_block_route bit for bit."""
+    w, T, layer = setup
+    R = w.R
+    bias = torch.zeros(1, w.E, dtype=torch.float32, device="cuda")
+    bias[0, 7] = float("nan")
+    bias[0, 11] = float("-inf")
+    ref_idx, ref_w = _reference(layer, T.x, T.block_offsets, bias)
+    idx = torch.full((R, w.k), -1, dtype=torch.int32, device="cuda")
+    wt = torch.full((R, w.k), float("nan"), dtype=torch.float32, device="cuda")
+    moe_block.moe_block_route_noalloc(layer.plan, T.x, T.block_offsets, bias, idx, wt)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, ref_idx)
+    assert torch.equal(wt.view(torch.int32), ref_w.view(torch.int32))
+    assert not bool(((idx == 7) | (idx == 11)).any())
