@@ -11,7 +11,9 @@ starts with no dirty lines to write back.  Prints ONE JSON line.
 
 Under torchrun (N > 1) every rank runs the same workload shape on its own
 GPU with its own rows (weak scaling); rank 0 prints the line with the
-maximum time over ranks.
+maximum time over ranks.  On one GPU the line also carries, under
+"workloads", the other full-size workloads (512 Zipf rows, 2048 rows with the
+coreset on and off, 8192 rows) timed the same way in the same run.
 """
 from __future__ import annotations
 
@@ -279,6 +281,210 @@ def config_of(w: W.Workload, l2: str):
 
 # --------------------------------------------------------------------------- GPU arm
 
+class StepTimer:
+    """The launch stream and the L2 flush run between timed steps (a 256 MiB
+    write, then a 256 MiB read of another buffer, so no dirty lines are left)."""
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.stream = torch.cuda.Stream(device=dev)
+        self._wr = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self._rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self._out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2(self, i):
+        self._wr.fill_(float(i))
+        torch.sum(self._rd, dim=0, out=self._out)
+
+    def median_us(self, replay, n):
+        """Median of n replays (after 3 untimed ones), each behind the flush."""
+        ts = []
+        with torch.cuda.stream(self.stream):
+            for i in range(n + 3):
+                self.flush_l2(i)
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(self.stream)
+                replay()
+                b_.record(self.stream)
+                b_.synchronize()
+                if i >= 3:
+                    ts.append(a_.elapsed_time(b_))
+        return 1e3 * statistics.median(ts)
+
+
+def routing_facts(w: W.Workload, layer, live=None):
+    """Experts kept and (row, expert) pairs evaluated, from the routing on the device."""
+    idx = layer._topk_idx[:w.R].cpu().numpy()
+    keep = layer._keep[:w.nb].cpu().numpy().view(np.uint32)
+    off = np.asarray(w.block_offsets())
+    used, pairs = set(), 0
+    for b in range(w.nb):
+        for r in range(off[b], off[b + 1]):
+            if live is not None and not live[r]:
+                continue
+            for e in idx[r]:
+                if (keep[b, e // 32] >> (e % 32)) & 1:
+                    used.add(int(e))
+                    pairs += 1
+    return used, pairs
+
+
+def measure(w: W.Workload, T, layer, steps: int, tm: StepTimer, clock_index: int, warmup: int,
+            ws: int = 1):
+    """One step (route -> coreset -> forward through the C ABI) as a CUDA graph,
+    replayed `steps` times behind the L2 flush, CUDA events on the launch stream;
+    then the forward's kernels timed by its own event records, and the three
+    calls as separate graphs.  Returns the raw times and the routing facts."""
+    stream, dev = tm.stream, tm.dev
+    y = torch.empty(w.R, w.H, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        layer(T.x, T.block_offsets, w.tau, bias=T.bias, y=y)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            step()
+    torch.cuda.synchronize()
+    st = layer.status()
+    if st["wait_timeout"] or st["bad_expert_id"]:
+        raise RuntimeError(f"device status after warm-up of {w.name}: {st}")
+    used, pairs = routing_facts(w, layer)
+
+    # the step as a graph (timed); and the same step with the forward's 5 event
+    # records around its kernels (the records sit between the kernels, so that
+    # graph is replayed separately)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    fwd_ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    layer.plan.set_forward_events(fwd_ev)
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev, stream=stream):
+        step()
+    layer.plan.set_forward_events(None)
+    torch.cuda.synchronize()
+
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(clock_index) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                tm.flush_l2(i)
+                step_ev[i][0].record(stream)
+                graph.replay()
+                step_ev[i][1].record(stream)
+            torch.cuda.synchronize()
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    barrier(ws)
+    total_ms = reduce_max(sum(step_ms), ws, dev)
+    kern = {"scatter": [], "gate_up": [], "down": [], "combine": []}
+    with torch.cuda.stream(stream):
+        for i in range(min(steps, 100)):
+            tm.flush_l2(i)
+            graph_ev.replay()
+            fwd_ev[4].synchronize()   # the next replay overwrites the events
+            for j, name in enumerate(kern):
+                kern[name].append(fwd_ev[j].elapsed_time(fwd_ev[j + 1]))
+    torch.cuda.synchronize()
+
+    # per-phase breakdown (not the headline): the three calls as separate graphs,
+    # replayed back to back behind the L2 flush so no host gap falls inside
+    phase_ms = {"route": [], "coreset": [], "forward": []}
+    idx_t, w_t = layer._topk_idx[:w.R], layer._topk_w[:w.R]
+    keep_t, wr_t = layer._keep[:w.nb], layer._w_renorm[:w.R]
+    calls = {
+        "route": lambda: layer.route(T.x, T.block_offsets, T.bias),
+        "coreset": lambda: layer.coreset(T.block_offsets, idx_t, w_t, w.tau),
+        "forward": lambda: layer.forward(T.x, T.block_offsets, idx_t, wr_t, keep_t, y=y),
+    }
+    graphs = {}
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs[name] = g
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(min(steps, 50)):
+            tm.flush_l2(i)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            evs[0].record(stream)
+            for j, name in enumerate(phase_ms):
+                graphs[name].replay()
+                evs[j + 1].record(stream)
+            evs[3].synchronize()
+            for j, name in enumerate(phase_ms):
+                phase_ms[name].append(evs[j].elapsed_time(evs[j + 1]))
+    torch.cuda.synchronize()
+    return dict(total_ms=total_ms, steps=steps, kern=kern, phase_ms=phase_ms, used=used,
+                pairs=pairs, clocks=clk.summary(), y=y)
+
+
+def summarize(w: W.Workload, m: dict, peaks: dict, ws: int = 1) -> dict:
+    """Throughput, the gate/up kernel's roofline and the whole step's fraction."""
+    from sparse_moe_layer_row_gb300 import moe_block
+    acc = accounting(w, w.R, len(m["used"]), m["pairs"])
+    t_step = m["total_ms"] / 1e3 / m["steps"]
+    t_gu = statistics.mean(m["kern"]["gate_up"]) / 1e3
+    traffic = recorded_traffic(w.name)
+    if w.R >= TENSOR_BOUND_ROWS:
+        # many rows per expert: the gate/up GEMM is a dense contraction; its
+        # roofline is the burst bf16 tensor peak (the kernel's own time)
+        achieved = acc["gu_flops"] / t_gu / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "algorithmic_flops_per_launch": acc["gu_flops"],
+                "hbm_gbs_alongside": acc["gu_bytes"] / t_gu / 1e9}
+    else:
+        achieved = acc["gu_bytes"] / t_gu / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"],
+                "algorithmic_bytes_per_launch": acc["gu_bytes"]}
+    gu_kernel = ("k_gemm<kGateUp, 32, 5> (tcgen05)" if w.R <= moe_block.SMALL_ROWS
+                 else "k_gateup_pair (tcgen05 cta_group::2)")
+    roof = {"bound": roof.pop("bound"), "kernel": gu_kernel, **roof,
+            "traffic": traffic, "launch_us": t_gu * 1e6, "peak_source": peaks["source"]}
+    step_frac = max(acc["step_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                    acc["step_flops"] / (peaks["bf16_tflops_sustained"] * 1e12)) / t_step
+    return {
+        "value": w.R * ws * m["steps"] / (m["total_ms"] / 1e3), "unit": "rows/s",
+        "ms_per_step": m["total_ms"] / m["steps"],
+        "expert_weight_gbs": acc["weight_bytes"] / t_step / 1e9,
+        "step_roofline_frac": step_frac,
+        "step_roofline_bound": ("hbm" if acc["step_bytes"] / (peaks["hbm_gbs"] * 1e9) >=
+                                acc["step_flops"] / (peaks["bf16_tflops_sustained"] * 1e12)
+                                else "tensor"),
+        "roofline": roof,
+        "kernel_us": {k: 1e3 * statistics.mean(v) for k, v in m["kern"].items()},
+        "phase_us": {k: 1e3 * statistics.median(v) for k, v in m["phase_ms"].items()},
+        "coreset": {"experts": len(m["used"]), "pairs": m["pairs"]},
+        "clocks": m["clocks"],
+    }
+
+
+# Workloads timed in the same run next to the main one (their own JSON object,
+# not the headline): the 512-row Zipf batch, 2048 rows in 32-row blocks with
+# the coreset on and off, and the 8192-row prefill shape.
+EXTRA_WORKLOADS = ("blocks16x32-zipf1.1", "rows2048-b32-tau0.9", "rows2048-b32-tau1",
+                   "prefill8192-b32")
+
+
+def tensors_like(we: W.Workload, base: W.Workload, T, dev, x_seed: int):
+    """Inputs of workload `we`, sharing the weights of `base` when they are the same
+    synthetic layer (same shapes and weight seed)."""
+    same = (we.H, we.E, we.k, we.I, we.Is, we.w_seed, we.sigma_w, we.sigma_r) == \
+        (base.H, base.E, base.k, base.I, base.Is, base.w_seed, base.sigma_w, base.sigma_r)
+    if not same:
+        return W.make_tensors(we, device=dev, x_seed=x_seed)
+    bias = W.zipf_bias(we, seed=x_seed)
+    return W.Tensors(W.make_x(we, dev, seed=x_seed), T.w_router, T.w_gate, T.w_up, T.w_down,
+                     T.ws_gate, T.ws_up, T.ws_down, None if bias is None else bias.to(dev),
+                     torch.tensor(we.block_offsets(), dtype=torch.int32, device=dev))
+
+
 def run_gpu(args, w: W.Workload):
     from sparse_moe_layer_row_gb300 import moe_block
 
@@ -294,112 +500,11 @@ def run_gpu(args, w: W.Workload):
     T = W.make_tensors(w, device=dev, x_seed=x_seed)
     layer = moe_block.MoeBlockLayer(T.w_router, T.w_gate, T.w_up, T.w_down, T.ws_gate, T.ws_up,
                                     T.ws_down, k=w.k, max_rows=w.R, max_blocks=w.nb)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_out = torch.empty((), dtype=torch.float32, device=dev)
-
-    def flush_l2(i):
-        flush.fill_(float(i))
-        torch.sum(flush_rd, dim=0, out=flush_out)
-    stream = torch.cuda.Stream(device=dev)
-    y = torch.empty(w.R, w.H, dtype=torch.bfloat16, device=dev)
-
-    def step():
-        layer(T.x, T.block_offsets, w.tau, bias=T.bias, y=y)
-
-    with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            step()
-    torch.cuda.synchronize()
-    st = layer.status()
-    if st["wait_timeout"] or st["bad_expert_id"]:
-        raise RuntimeError(f"device status after warm-up: {st}")
-
-    # routing facts for the accounting (deterministic, identical every step)
-    idx = layer._topk_idx[:w.R].cpu().numpy()
-    keep = layer._keep[:w.nb].cpu().numpy().view(np.uint32)
-    off = np.asarray(w.block_offsets())
-    used, pairs = set(), 0
-    for b in range(w.nb):
-        for r in range(off[b], off[b + 1]):
-            for e in idx[r]:
-                if (keep[b, e // 32] >> (e % 32)) & 1:
-                    used.add(int(e))
-                    pairs += 1
-    acc = accounting(w, w.R, len(used), pairs)
-
-    # one step as a graph (timed); and the same step with the forward's 5 event
-    # records around its kernels (for the per-kernel times: the records sit
-    # between the kernels, so that graph is replayed separately)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    fwd_ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-    layer.plan.set_forward_events(fwd_ev)
-    graph_ev = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_ev, stream=stream):
-        step()
-    layer.plan.set_forward_events(None)
-    torch.cuda.synchronize()
-
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    step_ms, gu_ms, dn_ms, sc_ms = [], [], [], []
-    barrier(ws)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                flush_l2(i)
-                step_ev[i][0].record(stream)
-                graph.replay()
-                step_ev[i][1].record(stream)
-            torch.cuda.synchronize()
-            step_ms = [a.elapsed_time(b) for a, b in step_ev]
-        torch.cuda.synchronize()
-    barrier(ws)
-    total_ms = reduce_max(sum(step_ms), ws, dev)
-    clocks = clk.summary()
-    with torch.cuda.stream(stream):
-        for i in range(min(args.steps, 100)):
-            flush_l2(i)
-            graph_ev.replay()
-            # kernel events are overwritten by the next replay: read them now
-            fwd_ev[4].synchronize()
-            sc_ms.append(fwd_ev[0].elapsed_time(fwd_ev[1]))
-            gu_ms.append(fwd_ev[1].elapsed_time(fwd_ev[2]))
-            dn_ms.append(fwd_ev[2].elapsed_time(fwd_ev[3]))
-    torch.cuda.synchronize()
-
-    # per-phase breakdown (not the headline): the three calls as separate graphs,
-    # replayed back to back behind the L2 flush so no host gap falls inside
-    phase_ms = {"route": [], "coreset": [], "forward": []}
-    graphs = {}
-    idx_t, w_t = layer._topk_idx[:w.R], layer._topk_w[:w.R]
-    keep_t, wr_t = layer._keep[:w.nb], layer._w_renorm[:w.R]
-    calls = {
-        "route": lambda: layer.route(T.x, T.block_offsets, T.bias),
-        "coreset": lambda: layer.coreset(T.block_offsets, idx_t, w_t, w.tau),
-        "forward": lambda: layer.forward(T.x, T.block_offsets, idx_t, wr_t, keep_t, y=y),
-    }
-    for name, fn in calls.items():
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            fn()
-        graphs[name] = g
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for i in range(min(args.steps, 50)):
-            flush_l2(i)
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-            evs[0].record(stream)
-            for j, name in enumerate(("route", "coreset", "forward")):
-                graphs[name].replay()
-                evs[j + 1].record(stream)
-            evs[3].synchronize()
-            for j, name in enumerate(("route", "coreset", "forward")):
-                phase_ms[name].append(evs[j].elapsed_time(evs[j + 1]))
-    torch.cuda.synchronize()
+    tm = StepTimer(dev)
+    stream = tm.stream
+    m = measure(w, T, layer, args.steps, tm, local, args.warmup, ws)
+    y = m["y"]
+    idx_t, keep_t, wr_t = layer._topk_idx[:w.R], layer._keep[:w.nb], layer._w_renorm[:w.R]
 
     # live-row passes (informational): the forward on a seeded subset of the
     # rows, the others keeping their cached output
@@ -407,31 +512,14 @@ def run_gpu(args, w: W.Workload):
     for frac in args.live_fracs:
         live = W.live_rows(w.R, frac, seed=x_seed + 7, device=dev)
         lv = live.cpu().numpy().astype(bool)
-        lused, lpairs = set(), 0
-        for b in range(w.nb):
-            for r in range(off[b], off[b + 1]):
-                if lv[r]:
-                    for e in idx[r]:
-                        if (keep[b, e // 32] >> (e % 32)) & 1:
-                            lused.add(int(e))
-                            lpairs += 1
+        lused, lpairs = routing_facts(w, layer, live=lv)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             layer.forward(T.x, T.block_offsets, idx_t, wr_t, keep_t, y=y, live=live)
         torch.cuda.synchronize()
-        ts = []
-        with torch.cuda.stream(stream):
-            for i in range(min(args.steps, 50) + 3):
-                flush_l2(i)
-                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a_.record(stream)
-                g.replay()
-                b_.record(stream)
-                b_.synchronize()
-                if i >= 3:
-                    ts.append(a_.elapsed_time(b_))
         live_us[f"{frac:g}"] = {"live_rows": int(lv.sum()), "experts": len(lused),
-                                "pairs": lpairs, "forward_us": 1e3 * statistics.median(ts)}
+                                "pairs": lpairs,
+                                "forward_us": tm.median_us(g.replay, min(args.steps, 50))}
     torch.cuda.synchronize()
 
     # several layers as one pass (informational): each layer its own weights, the
@@ -449,18 +537,7 @@ def run_gpu(args, w: W.Workload):
             biases.append(Ti.bias)
         stack = moe_block.MoeStack(stack_layers)   # every layer reads the block's x
         g_stack, _ = stack.capture(T.x, T.block_offsets, w.tau, biases)
-        ts = []
-        with torch.cuda.stream(stream):
-            for i in range(min(args.steps, 50) + 3):
-                flush_l2(i)
-                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a_.record(stream)
-                g_stack.replay()
-                b_.record(stream)
-                b_.synchronize()
-                if i >= 3:
-                    ts.append(a_.elapsed_time(b_))
-        t_pass = 1e3 * statistics.median(ts)
+        t_pass = tm.median_us(g_stack.replay, min(args.steps, 50))
         stack_info = {"layers": args.layers, "pass_us": t_pass, "per_layer_us": t_pass / args.layers,
                       "launches_per_pass": 1}
     torch.cuda.synchronize()
@@ -482,7 +559,7 @@ def run_gpu(args, w: W.Workload):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2e_ms = 0.0
         for i in range(e2e_steps):
-            flush_l2(i)
+            tm.flush_l2(i)
             e0.record(stream)
             x_dev.copy_(x_host, non_blocking=True)
             off_dev.copy_(off_host, non_blocking=True)
@@ -501,45 +578,18 @@ def run_gpu(args, w: W.Workload):
         return 0
 
     peaks = load_peaks()
-    t_step = total_ms / 1e3 / args.steps
-    t_gu = statistics.mean(gu_ms) / 1e3
-    value = w.R * ws * args.steps / (total_ms / 1e3)
-    traffic = recorded_traffic(w.name)
-    if w.R >= TENSOR_BOUND_ROWS:
-        # many rows per expert: the gate/up GEMM is a dense contraction; its
-        # roofline is the burst bf16 tensor peak (the kernel's own time)
-        achieved = acc["gu_flops"] / t_gu / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "algorithmic_flops_per_launch": acc["gu_flops"],
-                "hbm_gbs_alongside": acc["gu_bytes"] / t_gu / 1e9}
-    else:
-        achieved = acc["gu_bytes"] / t_gu / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"],
-                "algorithmic_bytes_per_launch": acc["gu_bytes"]}
-    gu_kernel = ("k_gemm<kGateUp, 32, 5> (tcgen05)" if w.R <= moe_block.SMALL_ROWS
-                 else "k_gateup_pair (tcgen05 cta_group::2)")
-    roof = {"bound": roof.pop("bound"), "kernel": gu_kernel, **roof,
-            "traffic": traffic, "launch_us": t_gu * 1e6, "peak_source": peaks["source"]}
-    step_frac = max(acc["step_bytes"] / (peaks["hbm_gbs"] * 1e9),
-                    acc["step_flops"] / (peaks["bf16_tflops_sustained"] * 1e12)) / t_step
+    summ = summarize(w, m, peaks, ws)
     line = {
-        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "metric": METRIC, "value": summ["value"], "unit": "rows/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": summ["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,s) bf16 inputs and weights; no trained weights)",
         "config": config_of(w, f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, then "
                                f"{FLUSH_BYTES >> 20} MiB read of another buffer)"),
-        "expert_weight_gbs": acc["weight_bytes"] / t_step / 1e9,
-        "step_roofline_frac": step_frac,
-        "roofline": roof,
-        "kernel_us": {"scatter": 1e3 * statistics.mean(sc_ms), "gate_up": t_gu * 1e6,
-                      "down": 1e3 * statistics.mean(dn_ms)},
-        "phase_us": {k: 1e3 * statistics.median(v) for k, v in phase_ms.items()},
-        "coreset": {"experts": len(used), "pairs": pairs},
+        **{k: summ[k] for k in ("expert_weight_gbs", "step_roofline_frac", "roofline",
+                                "kernel_us", "phase_us", "coreset")},
         "gpu_launches": kernels_per_step(w) * args.steps,
-        "clocks": clocks,
+        "clocks": summ["clocks"],
         "e2e": {"value": w.R * ws * e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
     }
@@ -547,6 +597,27 @@ def run_gpu(args, w: W.Workload):
         line["live_pass"] = live_us
     if stack_info:
         line["stack"] = stack_info
+    # the other full-size workloads, timed in the same run (1 GPU only)
+    if ws == 1 and not args.no_extra_workloads:
+        extra = {}
+        for name in EXTRA_WORKLOADS:
+            we = W.BY_NAME[name]
+            if we.name == w.name:
+                continue
+            Te = tensors_like(we, w, T, dev, rank_workload(we, rank))
+            le = moe_block.MoeBlockLayer(Te.w_router, Te.w_gate, Te.w_up, Te.w_down, Te.ws_gate,
+                                         Te.ws_up, Te.ws_down, k=we.k, max_rows=we.R,
+                                         max_blocks=we.nb)
+            me = measure(we, Te, le, args.extra_steps, tm, local, args.warmup)
+            se = summarize(we, me, peaks)
+            se["gpu_launches_per_step"] = kernels_per_step(we)
+            se["config"] = {"rows": we.R, "blocks": we.nb, "block_rows": we.block_rows[0],
+                            "coreset_mass": we.tau, "zipf_bias": we.zipf_s or None,
+                            "steps": args.extra_steps}
+            extra[name] = se
+            del le, Te, me
+            torch.cuda.empty_cache()
+        line["workloads"] = extra
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x_seed, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
@@ -564,6 +635,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="skip the other full-size workloads (reported under workloads)")
+    ap.add_argument("--extra-steps", type=int, default=30,
+                    help="timed steps of each extra workload")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=1,
                     help="also time a pass over this many layers (own weights each) captured "

@@ -278,6 +278,19 @@ typedef struct CUevent_st* moe_event_t;
 moe_status moe_plan_set_forward_events(moe_plan* plan, moe_event_t const* events,
                                        int32_t n_events);
 
+/* Limit of the kernels' pipeline waits, for tests of the failure path.
+ * (No counterpart on the pages: part of this library's failure handling.)
+ * Every wait of the GEMM and tensor-core router pipelines gives up after a
+ * limit (built in: 2 s, far beyond any legal wait); the kernel then counts
+ * MOE_STATUS_WAIT_TIMEOUT, leaves its loops, waits for its own copies and
+ * MMAs in flight (with their own fixed limit) and releases its tensor memory,
+ * so the call returns and the context stays usable; the outputs of that call
+ * are not valid.  A test sets a tiny limit to make the waits run out and
+ * checks that path; limit_ns == 0 restores the built-in limit.  Applies to
+ * calls enqueued after it; not thread-safe against concurrent calls on the
+ * plan. */
+moe_status moe_plan_set_wait_limit(moe_plan* plan, uint64_t limit_ns);
+
 /* Copy the MOE_STATUS_WORDS counters to out[] (host); synchronises `stream`. */
 moe_status moe_read_device_status(const void* workspace, moe_stream_t stream, uint32_t* out);
 

@@ -22,6 +22,7 @@ struct moe_plan {
     bool tc_route;        // the large-batch router applies to this shape
     cudaEvent_t fwd_events[5];
     int n_fwd_events;
+    uint64_t wait_ns;     // limit of the kernels' pipeline waits (0: built in)
 };
 
 namespace {
@@ -232,7 +233,7 @@ moe_status moe_block_route_probs(const moe_plan* p, const void* x, int32_t R,
                        static_cast<const __nv_bfloat16*>(p->wr), logit_bias, block_offsets, R,
                        p->d.H, p->d.E, p->d.k, nb,
                        at<float>(workspace, L.wnorm), at<float>(workspace, L.logits), topk_idx, topk_w,
-                       at<uint32_t>(workspace, L.status)};
+                       at<uint32_t>(workspace, L.status), p->wait_ns};
         cudaError_t e = launch_route_tc(ta, tm_x, p->tm_wr, p->num_sms, st);
         if (e != cudaSuccess) return cuda_fail(e, "route launch");
         return ok();
@@ -349,7 +350,7 @@ moe_status moe_block_forward_live(const moe_plan* p, const void* x, int32_t R,
                 at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
                 at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
                 (int)(L.max_pairs + d.max_rows), (int)L.max_pairs, at<uint32_t>(workspace, L.status),
-                live ? at<int32_t>(workspace, L.shared_rows) : nullptr};
+                live ? at<int32_t>(workspace, L.shared_rows) : nullptr, p->wait_ns};
     // Under stream capture an event record must be an external node to be
     // recorded at every graph launch (a plain record only orders the capture).
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -394,6 +395,12 @@ moe_status moe_plan_set_forward_events(moe_plan* p, moe_event_t const* events,
         p->fwd_events[i] = reinterpret_cast<cudaEvent_t>(events[i]);
     }
     p->n_fwd_events = 5;
+    return ok();
+}
+
+moe_status moe_plan_set_wait_limit(moe_plan* p, uint64_t limit_ns) {
+    if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+    p->wait_ns = limit_ns;
     return ok();
 }
 

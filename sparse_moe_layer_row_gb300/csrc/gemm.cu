@@ -47,8 +47,12 @@
 //   warps 2..5     epilogue: tcgen05.ld 32 lanes x 16 columns, math, stores
 // Every wait is bounded (see mbar_wait_bounded): a wait that gives up raises
 // a CTA-wide abort flag and a device status counter; all roles then leave
-// their loops, the producer waits (bounded) for the stages in flight, and the
-// TMEM is released before the CTA exits.
+// their loops.  Before the CTA exits, whether it aborted or not, the producer
+// waits for the `full` phase of the last fill of every stage (a TMA copy
+// completes whether or not the MMA consumes it, so no copy is left in flight)
+// and the MMA thread commits once more to a drain barrier and waits for it
+// (every MMA it issued has completed); only then is the TMEM released.  These
+// drain waits have their own limit, apart from the pipeline waits'.
 #include "kernels.cuh"
 
 namespace moe {
@@ -85,7 +89,7 @@ struct GemmCfg {
     static constexpr int kAccCols = NMAX;   // TMEM columns per accumulator
     static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
-    static_assert(8 * (2 * STAGES + 6) + 16 <= 512, "barrier region");
+    static_assert(8 * (2 * STAGES + 7) + 16 <= 512, "barrier region");
     static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
     static_assert(NMAX % 16 == 0 && NMAX <= 256 && NMAX % (NMAX >= 64 ? 64 : 16) == 0, "MMA N extent");
 };
@@ -125,7 +129,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* xbar = tempty + 2;  // [2] epilogue exchange (128 arrivals each)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2);
+    uint64_t* dbar = xbar + 2;    // MMA drain: every MMA issued has completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dbar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;
 
@@ -137,6 +142,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             mbar_init(tempty + i, 128);
             mbar_init(xbar + i, 128);
         }
+        mbar_init(dbar, 1);
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -172,6 +178,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     auto give_up = [&]() {
         if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
     };
+    const uint64_t kWaitNs = a.wait_ns ? a.wait_ns : kWaitLimitNs;   // pipeline waits
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
@@ -179,6 +186,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
+        int nfills = 0;   // stages filled (TMA issued) so far
         int* s_rows = reinterpret_cast<int*>(base + C::kRowsOff);
         // B copies of the first stages, held back until the wait (down GEMM)
         struct HeldB { uint32_t sB; int g, start, nbox, K, kc; uint64_t* bar; };
@@ -234,7 +242,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 __syncwarp();
             }
             for (int kb = 0; kb < (K >> 6); ++kb) {
-                const bool w_ok = mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitLimitNs);
+                const bool w_ok = mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitNs);
                 if (__any_sync(0xffffffffu, !w_ok)) {
                     if (lane == 0) give_up();
                     ok = false;
@@ -280,21 +288,21 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         tma_gather4(sB + t * 512, &tmBg, kc, rr.x, rr.y, rr.z, rr.w, full + stage);
                     }
                 }
+                ++nfills;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
         if (!waited) release_held();
-        // Drain: every stage must be released by the MMA before the CTA
-        // exits (all copies landed, all reads done).  Bounded; after an
-        // abort the MMA may never release, so the wait gives up quickly.
+        // Drain: the last fill of every stage completes its `full` phase when
+        // its copies land, consumed or not; wait for each (bounded), so no
+        // copy into this CTA's shared memory is in flight when it exits.
+        // Stage s < stage was last filled in this wrap (parity `phase`), the
+        // others in the wrap before (if filled at all).
         if (lane == 0) {
-            for (int i = 0; i < STAGES; ++i) {
-                const uint64_t lim = *abort_flag ? kDrainLimitNs : kWaitLimitNs;
-                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, never, lim)) {
-                    give_up();
-                    break;
-                }
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            for (int s = 0; s < STAGES; ++s) {
+                if (nfills < STAGES && s >= nfills) break;
+                const uint32_t par = s < stage ? phase : (phase ^ 1u);
+                if (!mbar_wait_bounded(full + s, par, never, kDrainLimitNs)) give_up();
             }
         }
     } else if (warp == 1) {
@@ -310,14 +318,14 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const int K = MODE == kGateUp ? a.H
                                               : (g == a.E ? (C::kDualLo ? a.Is : 2 * a.Is) : a.I);
                 const uint32_t idesc = idesc_bf16_f32(128, n16);
-                if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitNs)) {
                     give_up();
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * C::kAccCols);
                 for (int kb = 0; kb < (K >> 6); ++kb) {
-                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
                         break;
@@ -341,6 +349,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
+            // drain: arrives once every MMA issued above has completed
+            tc_commit(dbar);
+            if (!mbar_wait_bounded(dbar, 0, never, kDrainLimitNs)) give_up();
         }
     } else {
         // ---------------------------------------------------------- epilogue
@@ -352,7 +363,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const int4 un = __ldg(a.units + u);
             const int g = un.x, m = un.y, start = un.z, n = un.w;
             const int n16 = (n + 15) & ~15;
-            const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitLimitNs);
+            const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitNs);
             if (__any_sync(0xffffffffu, !ok)) { give_up(); break; }
             __syncwarp();
             tc_fence_after();
@@ -376,7 +387,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     // the four epilogue warps meet through an mbarrier (bounded wait)
                     mbar_arrive(xbar);
                     if (__any_sync(0xffffffffu,
-                                   !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitLimitNs))) {
+                                   !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitNs))) {
                         give_up();
                         alive = false;
                         break;
@@ -395,7 +406,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                     mbar_arrive(xbar + 1);  // the buffer is reused by the next chunk
                     if (__any_sync(0xffffffffu,
-                                   !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitLimitNs))) {
+                                   !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitNs))) {
                         give_up();
                         alive = false;
                         break;

@@ -18,8 +18,8 @@
 // needs two thirds of the operand bandwidth from L2 per flop.
 //
 // Roles (320 threads per CTA):
-//   warp 0 lane 0   TMA producer of the CTA's weight half; the complete-tx of
-//                   both halves lands on rank 0's `full` barrier
+//   warp 0 lane 0   TMA producer of the CTA's weight half, completing on the
+//                   CTA's own `full` barrier
 //   warp 1          TMEM allocation (both ranks); lane 0 of rank 0 issues the
 //                   MMAs and the commits, which arrive on the barriers of both
 //                   ranks (stage `empty`, accumulator `tfull`); lane 0 of
@@ -32,14 +32,18 @@
 //                   land (cp.async.mbarrier.arrive), so a loader never waits
 //                   for its own copies and the ring depth is the only limit on
 //                   the copies in flight.  In rank 1 one thread waits for that
-//                   barrier, fences the CTA's x tile for the async proxy and
-//                   arrives on rank 0's `pfull`; in rank 0 the MMA thread
-//                   waits for both and fences its own tile.
+//                   barrier and for the CTA's `full` (its weight half), fences
+//                   the CTA's x tile for the async proxy and arrives on rank
+//                   0's `pfull`; in rank 0 the MMA thread waits for its own
+//                   `full` and `bfull` and for `pfull`, and fences its own tile.
 // Each stage holds a weight half and an x tile (32 KB); both are freed by the
 // same commit.  Every wait is bounded; a role that gives up raises the CTA's
-// abort flag and the device status counter, and both CTAs leave their loops,
-// drain (bounded) and meet at a final cluster barrier before the TMEM is
-// released.
+// abort flag and the device status counter, and both CTAs leave their loops.
+// Before the final cluster barrier, aborted or not, each CTA's producer waits
+// for the `full` phase of the last fill of every stage (each CTA's weight
+// copies complete on its own barrier, so it can see that they landed), the
+// loaders wait for their own copies, and rank 0's MMA thread commits once more
+// to a drain barrier and waits for it; only then is the TMEM released.
 #include "kernels.cuh"
 
 namespace moe {
@@ -58,7 +62,7 @@ constexpr int kPSmem = kPBarOff + 512 + 1024;
 constexpr int kPAccCols = 256;
 constexpr int kPTmemCols = 512;
 static_assert(kPSmem <= 227 * 1024, "shared memory budget");
-static_assert(8 * (4 * kPStages + 4) + 12 <= 512, "barrier region");
+static_assert(8 * (4 * kPStages + 5) + 12 <= 512, "barrier region");
 
 // ---- cluster / CTA-pair PTX -----------------------------------------------------
 
@@ -128,26 +132,6 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
     }
 }
 
-// TMA tile loads into this CTA's shared memory whose complete-tx is signalled
-// on an mbarrier of either CTA of the pair (cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                                 uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                                 int c2, uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster)
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(slot)),
@@ -181,6 +165,15 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
         : "memory");
 }
 
+// Arrive on `bar` of this CTA only, once every MMA issued so far by this
+// thread completes.
+__device__ __forceinline__ void tc_commit_pair_local(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
 // Arrive on `bar` once all cp.async copies issued so far by this thread have
 // landed; the arrival counts toward the barrier's expected count.
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
@@ -202,13 +195,14 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;   // same offset in both CTAs
     uint8_t* base = smem_raw + (sbase - raw);
-    uint64_t* full = reinterpret_cast<uint64_t*>(base + kPBarOff);  // [S] weights (rank 0)
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + kPBarOff);  // [S] own weight half landed
     uint64_t* bfull = full + kPStages;                               // [S] own x landed (both)
     uint64_t* pfull = bfull + kPStages;                              // [S] peer's x landed (rank 0)
     uint64_t* empty = pfull + kPStages;                              // [S] stage free (both)
     uint64_t* tfull = empty + kPStages;                              // [2] accumulator ready (both)
     uint64_t* tempty = tfull + 2;                                    // [2] accumulator free (rank 0)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* dbar = tempty + 2;                                     // MMA drain (rank 0)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dbar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;
 
@@ -226,6 +220,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             mbar_init(tfull + i, 1);
             mbar_init(tempty + i, 256);  // 128 epilogue threads of each CTA
         }
+        mbar_init(dbar, 1);
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -248,44 +243,42 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
     auto give_up = [&]() {
         if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
     };
+    const uint64_t kWaitNs = a.wait_ns ? a.wait_ns : kPairWaitNs;   // pipeline waits
 
     if (warp == 0) {
         // ------------------------------------------------- weight-half producer
         if (lane == 0) {
-            const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // rank 0's full[0]
             const CUtensorMap* mR = leader ? &tmWg : &tmWu;
             const CUtensorMap* mS = leader ? &tmSg : &tmSu;
-            int stage = 0;
+            int stage = 0, nfills = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int u = c0; ok && u < nunits; u += nc) {
                 const int4 un = __ldg(a.units + u);
                 const int g = un.x, m = un.y;
                 for (int kb = 0; kb < (a.H >> 6); ++kb) {
-                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kPairWaitNs)) {
+                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
                         break;
                     }
                     const uint32_t sW = sbase + stage * kPStageBytes;
-                    const uint32_t fb = full0 + stage * 8;
-                    if (leader) mbar_expect_tx(full + stage, 2u * kPTile);  // both halves
+                    mbar_expect_tx(full + stage, (uint32_t)kPTile);  // this CTA's half
                     for (int hb = 0; hb < 2; ++hb) {
                         const int row = m * 128 + 64 * hb;
-                        if (g == a.E) tma_load_2d_pair(sW + hb * 64 * 128, mS, kb * 64, row, fb);
-                        else tma_load_3d_pair(sW + hb * 64 * 128, mR, kb * 64, row, g, fb);
+                        if (g == a.E) tma_load_2d(sW + hb * 64 * 128, mS, kb * 64, row, full + stage);
+                        else tma_load_3d(sW + hb * 64 * 128, mR, kb * 64, row, g, full + stage);
                     }
+                    ++nfills;
                     if (++stage == kPStages) { stage = 0; phase ^= 1u; }
                 }
             }
-            // every stage released by the MMA before the CTA exits (bounded)
-            for (int i = 0; i < kPStages; ++i) {
-                const uint64_t lim = *abort_flag ? kPairDrainNs : kPairWaitNs;
-                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, never, lim)) {
-                    give_up();
-                    break;
-                }
-                if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+            // drain: the last fill of every stage has landed (consumed or not),
+            // so no copy into this CTA's shared memory is in flight at exit
+            for (int s = 0; s < kPStages; ++s) {
+                if (nfills < kPStages && s >= nfills) break;
+                const uint32_t par = s < stage ? phase : (phase ^ 1u);
+                if (!mbar_wait_bounded(full + s, par, never, kPairDrainNs)) give_up();
             }
         }
     } else if (warp == 1) {
@@ -297,12 +290,14 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             bool ok = true;
             for (int u = c0; ok && u < nunits; u += nc) {
                 for (int kb = 0; kb < (a.H >> 6); ++kb) {
-                    if (!mbar_wait_bounded(bfull + stage, phase, abort_flag, kPairWaitNs)) {
+                    // this CTA's x tile and weight half, both read by rank 0's MMA
+                    if (!mbar_wait_bounded(bfull + stage, phase, abort_flag, kWaitNs) ||
+                        !mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
                         break;
                     }
-                    fence_proxy_async_smem();   // the tile is read by rank 0's MMA
+                    fence_proxy_async_smem();   // the x tile was written by cp.async
                     mbar_arrive_cluster(pfull0 + stage * 8);
                     if (++stage == kPStages) { stage = 0; phase ^= 1u; }
                 }
@@ -315,16 +310,16 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int u = c0; ok && u < nunits; u += nc) {
-                if (!mbar_wait_cluster_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kPairWaitNs)) {
+                if (!mbar_wait_cluster_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitNs)) {
                     give_up();
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * kPAccCols);
                 for (int kb = 0; kb < (a.H >> 6); ++kb) {
-                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kPairWaitNs) ||
-                        !mbar_wait_bounded(bfull + stage, phase, abort_flag, kPairWaitNs) ||
-                        !mbar_wait_cluster_bounded(pfull + stage, phase, abort_flag, kPairWaitNs)) {
+                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs) ||
+                        !mbar_wait_bounded(bfull + stage, phase, abort_flag, kWaitNs) ||
+                        !mbar_wait_cluster_bounded(pfull + stage, phase, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
                         break;
@@ -345,6 +340,10 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
+            // drain: arrives (on this CTA's barrier) once every MMA issued
+            // above has completed
+            tc_commit_pair_local(dbar);
+            if (!mbar_wait_bounded(dbar, 0, never, kPairDrainNs)) give_up();
         }
     } else if (warp >= 6) {
         // ----------------------------------------------------------- x loaders
@@ -370,7 +369,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
                 src[j] = row >= 0 ? a.x + (size_t)row * a.H + ch * 8 : nullptr;
             }
             for (int kb = 0; kb < (a.H >> 6); ++kb) {
-                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kPairWaitNs)) {
+                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) {
                     give_up();
                     ok = false;
                     break;
@@ -396,7 +395,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             const int4 un = __ldg(a.units + u);
             const int g = un.x, m = un.y, start = un.z + rbase;
             const int nr = min(128, max(0, un.w - rbase));
-            const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kPairWaitNs);
+            const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitNs);
             if (__any_sync(0xffffffffu, !ok)) { give_up(); break; }
             __syncwarp();
             tc_fence_after();

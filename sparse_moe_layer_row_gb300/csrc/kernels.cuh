@@ -35,6 +35,7 @@ struct RouteTcArgs {
     int32_t* topk_idx;
     float* topk_w;
     uint32_t* status;
+    uint64_t wait_ns;     // limit of a pipeline wait (0: the built-in limit)
 };
 struct CoresetArgs {
     const int32_t* off;
@@ -104,6 +105,7 @@ struct GemmArgs {
     int shared_row0;      // staging row of the shared expert's row 0
     uint32_t* status;
     const int32_t* shared_rows;  // row of x of the shared expert's i-th row (NULL: i)
+    uint64_t wait_ns;     // limit of a pipeline wait (0: the built-in limit)
 };
 struct GemmMaps {
     CUtensorMap a0, a1, a2, a3, b0, b1;

@@ -92,7 +92,8 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     uint64_t* empty = full + kTcStages;
     uint64_t* tfull = empty + kTcStages;
     uint64_t* tempty = tfull + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* dbar = tempty + 2;   // MMA drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dbar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -100,6 +101,7 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) { mbar_init(full + s, 1); mbar_init(empty + s, 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(tfull + i, 1); mbar_init(tempty + i, 128); }
+        mbar_init(dbar, 1);
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -117,17 +119,18 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
     };
     const int nkb = a.H >> 6;
+    const uint64_t kWaitNs = a.wait_ns ? a.wait_ns : kTcWaitNs;   // pipeline waits
 
     if (warp == 0) {
         if (lane == 0) {
-            int stage = 0;
+            int stage = 0, nfills = 0;
             uint32_t phase = 0;
             bool ok = true;
             const uint32_t bytes = (uint32_t)(C::kABytes + NH * 128);
             for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
                 const int t = u / nsplit, sp = u - t * nsplit;
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kTcWaitNs)) {
+                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
                         break;
@@ -136,13 +139,16 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                     const uint32_t sA = sbase + stage * C::kStageBytes;
                     tma_load_2d(sA, &tm_x, kb * 64, t * 128, full + stage);
                     tma_load_2d(sA + C::kABytes, &tm_w, kb * 64, sp * NH, full + stage);
+                    ++nfills;
                     if (++stage == kTcStages) { stage = 0; phase ^= 1u; }
                 }
             }
-            for (int i = 0; i < kTcStages; ++i) {
-                const uint64_t lim = *abort_flag ? kTcDrainNs : kTcWaitNs;
-                if (!mbar_wait_bounded(empty + stage, phase ^ 1u, never, lim)) { give_up(); break; }
-                if (++stage == kTcStages) { stage = 0; phase ^= 1u; }
+            // drain: the last fill of every stage has landed (consumed or not),
+            // so no copy into this CTA's shared memory is in flight at exit
+            for (int s = 0; s < kTcStages; ++s) {
+                if (nfills < kTcStages && s >= nfills) break;
+                const uint32_t par = s < stage ? phase : (phase ^ 1u);
+                if (!mbar_wait_bounded(full + s, par, never, kTcDrainNs)) give_up();
             }
         }
     } else if (warp == 1) {
@@ -152,14 +158,14 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             bool ok = true;
             const uint32_t idesc = idesc_bf16_f32(128, NH);
             for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-                if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kTcWaitNs)) {
+                if (!mbar_wait_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitNs)) {
                     give_up();
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * 256);
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kTcWaitNs)) {
+                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
                         break;
@@ -179,6 +185,9 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
+            // drain: arrives once every MMA issued above has completed
+            tc_commit(dbar);
+            if (!mbar_wait_bounded(dbar, 0, never, kTcDrainNs)) give_up();
         }
     } else {
         // epilogue: thread = row; store the approximate logits
@@ -187,7 +196,7 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
             const int t = u / nsplit, sp = u - t * nsplit;
-            const bool okw = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kTcWaitNs);
+            const bool okw = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitNs);
             if (__any_sync(0xffffffffu, !okw)) { give_up(); break; }
             __syncwarp();
             tc_fence_after();

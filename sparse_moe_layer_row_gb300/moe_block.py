@@ -82,6 +82,8 @@ def load(build_if_missing: bool = False):
     L.moe_block_route_noalloc.argtypes = [P, P, i32, P, i32, P, P, P, P]
     L.moe_plan_set_forward_events.restype = ctypes.c_int
     L.moe_plan_set_forward_events.argtypes = [P, P, i32]
+    L.moe_plan_set_wait_limit.restype = ctypes.c_int
+    L.moe_plan_set_wait_limit.argtypes = [P, ctypes.c_uint64]
     L.moe_read_device_status.restype = ctypes.c_int
     L.moe_read_device_status.argtypes = [P, P, P]
     L.moe_clear_device_status.restype = ctypes.c_int
@@ -174,6 +176,11 @@ class Plan:
         arr = (ctypes.c_void_p * 5)(*[ev.cuda_event for ev in events])
         _check(load().moe_plan_set_forward_events(self.handle, arr, 5))
         self._events = events
+
+    def set_wait_limit(self, limit_ns: int):
+        """moe_plan_set_wait_limit: the limit of the pipeline waits (0: built in).
+        For tests of the failure path."""
+        _check(load().moe_plan_set_wait_limit(self.handle, int(limit_ns)))
 
     def workspace_bytes(self) -> int:
         return moe_workspace_bytes(self.dims)

@@ -135,15 +135,15 @@ def assert_coreset_equal(gpu, ref):
     assert np.array_equal(gpu["empty"], ref["empty"]), "empty-row counts differ"
 
 
-def assert_close(got, ref, rows=None, what="y"):
-    """Elementwise |got - ref| <= ATOL + RTOL |ref| on every element (or on ``rows``).
+def assert_close(got, ref, rows=None, what="y", atol=ATOL):
+    """Elementwise |got - ref| <= atol + RTOL |ref| on every element (or on ``rows``).
     Records the worst element as a fraction of its tolerance under the running
     test's name; returns the largest absolute error."""
     import os
     if rows is not None:
         got, ref = got[list(rows)], ref[list(rows)]
     err = np.abs(got - ref)
-    tol = ATOL + RTOL * np.abs(ref)
+    tol = atol + RTOL * np.abs(ref)
     bad = err > tol
     frac = float((err / tol).max()) if err.size else 0.0
     test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]

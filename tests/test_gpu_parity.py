@@ -14,7 +14,8 @@ import pytest
 import torch
 
 from sparse_moe_layer_row_gb300 import moe_block, workloads as W
-from tests.parity_util import (Case, assert_close, assert_coreset_equal, assert_route_equal)
+from tests.parity_util import (ATOL, Case, assert_close, assert_coreset_equal,
+                               assert_route_equal)
 
 pytestmark = pytest.mark.gpu
 
@@ -82,22 +83,38 @@ def test_prefill8192():
 @pytest.mark.parametrize("base", [W.TINY, W.BLOCK32, W.BY_NAME["rows2048-b32-tau0.9"]],
                          ids=lambda w: w.name)
 def test_outputs_beyond_fp16_range(base):
-    """Expert and shared weights N(0, 2) (a hundred times the synthetic layer's):
-    expert outputs reach far past fp16's largest value 65504.  The staged outputs
-    keep a power-of-two exponent per 32 columns, so every row of y stays within
-    tolerance and none becomes non-finite (small path, and the CTA-pair / 256-row
-    kernels of the large path)."""
-    w = dataclasses.replace(base, name=base.name + "-wide", sigma_w=2.0)
-    case = Case(w)
-    _full(case)
-    assert np.abs(case.ref["y"]).max() > 4 * 65504
-    assert case.status["nonfinite_output"] == 0
-
-
-
-def _small(H=256, E=16, k=4, I=128, Is=128, rows=(32,), tau=0.9, seed=5, sigma_r=0.05):
-    return W.Workload(name="edge", H=H, E=E, k=k, I=I, Is=Is, block_rows=tuple(rows), tau=tau,
-                      sigma_r=sigma_r, x_seed=seed, w_seed=seed)
+    """The down projections (routed and shared) times an exact power of two 2^s,
+    chosen so that the expert outputs reach past fp16's largest value 65504 (at
+    least four times).  Routing and h are unchanged and the layer is linear in
+    those weights, so y scales by exactly 2^s: the staged outputs keep a
+    power-of-two exponent per 32 columns, and
+      * y equals 2^s times the unscaled layer's y up to fp16's resolution;
+      * every row matches the oracle of the scaled layer, the tolerance's
+        absolute part scaled by the same 2^s (the unscaled comparison, exactly);
+      * no output is non-finite.
+    Small path, and the CTA-pair / 256-row kernels of the large path."""
+    T = W.make_tensors(base, device="cuda")
+    small = Case(base, T=T)
+    gs = small.run()
+    ys = {k: gs[k].copy() for k in ("y32", "idx", "keep", "wr")}
+    s = int(np.ceil(np.log2(4 * 65504 / np.abs(ys["y32"]).max()))) + 1
+    big_T = dataclasses.replace(T, w_down=(T.w_down.float() * 2.0 ** s).to(torch.bfloat16),
+                                ws_down=(T.ws_down.float() * 2.0 ** s).to(torch.bfloat16))
+    assert torch.equal(big_T.w_down.float(), T.w_down.float() * 2.0 ** s)  # exact in bf16
+    big = Case(base, T=big_T)
+    gb = big.run()
+    assert np.array_equal(gb["idx"], ys["idx"]) and np.array_equal(gb["keep"], ys["keep"])
+    assert np.abs(gb["y32"]).max() > 4 * 65504
+    assert big.status["nonfinite_output"] == 0
+    # exact scaling up to the staging's rounding (fp16: 11 significant bits)
+    assert np.allclose(gb["y32"], ys["y32"] * 2.0 ** s, rtol=2.0 ** -10, atol=2.0 ** (s - 20))
+    ref = big.oracle_route()
+    assert_route_equal(gb, ref)
+    big.oracle_coreset()
+    assert_coreset_equal(gb, ref)
+    big.oracle_forward()
+    assert_close(gb["y32"], ref["y"], what="y_f32 (scaled)", atol=ATOL * 2.0 ** s)
+    assert_close(gb["y"], ref["y"], what="y (scaled)", atol=ATOL * 2.0 ** s)
 
 
 @pytest.mark.parametrize("rows", [(1,), (3,), (5, 0, 7), (13, 1, 1, 30), (37, 64, 50)],

@@ -129,11 +129,17 @@ def test_prob_mass_with_budget_and_same_ids():
 
 
 def test_prob_mass_rejects_misaligned():
+    """A mass pointer off the 4-byte grid is refused on the host (nothing launched)."""
+    import ctypes
     case = Case(W.TINY)
     L = case.layer
     idx, wt, p = L.route(case.x, case.off, probs=True)
-    buf = torch.empty(p.numel() + 1, dtype=torch.float32, device=p.device)
-    bad = buf[1:].view(p.shape)
-    with pytest.raises(moe_block.MoeError):
-        moe_block.moe_block_coreset(L.plan, case.off, idx, wt, 0.9, L._keep[:1], L._core[:1],
-                                    L._w_renorm[:case.R], None, L.workspace, mass=bad)
+    lib = moe_block.load()
+    rc = lib.moe_block_coreset_mass(
+        L.plan.handle, case.R, ctypes.c_void_p(case.off.data_ptr()), 1,
+        ctypes.c_void_p(idx.data_ptr()), ctypes.c_void_p(wt.data_ptr()),
+        ctypes.c_void_p(p.data_ptr() + 2), ctypes.c_float(0.9), 0,
+        ctypes.c_void_p(L._keep.data_ptr()), ctypes.c_void_p(L._core.data_ptr()),
+        ctypes.c_void_p(L._w_renorm.data_ptr()), None, ctypes.c_void_p(L.workspace.data_ptr()),
+        L.workspace.numel(), None)
+    assert rc == -1 and b"misaligned" in lib.moe_last_error()
