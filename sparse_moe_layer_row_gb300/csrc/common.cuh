@@ -172,12 +172,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-suspending test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Limits below this are the short ones a test of the failure path sets: such
+// waits poll without suspending (try_wait may suspend the thread until the
+// phase completes, so a short limit would rarely be seen to run out).
+constexpr uint64_t kShortWaitNs = 1000000ull;
+
 // Wait for the phase with the given parity to complete, for at most
 // `limit_ns`, giving up early when another role of the CTA raised `abort`.
 // Returns false when it gave up (the caller then records the timeout and
 // leaves its loop); no wait in this library is unbounded.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, uint64_t limit_ns) {
+    if (limit_ns < kShortWaitNs) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_test_wait(bar, parity)) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+        return true;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {

@@ -117,10 +117,31 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t pa
     return ok != 0;
 }
 
-// Bounded wait with cluster-scope acquire (arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t addr, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire (arrivals from the peer CTA); short
+// limits poll without suspending, as in mbar_wait_bounded.
 __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
                                                           volatile int* abort, uint64_t limit_ns) {
     const uint32_t addr = smem_u32(bar);
+    if (limit_ns < kShortWaitNs) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_test_wait_cluster(addr, parity)) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+        return true;
+    }
     if (mbar_try_wait_cluster(addr, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {

@@ -162,4 +162,112 @@ __device__ __forceinline__ void write_topk_probs(float* p_out, int k, int lane,
     if (lane < k) p_out[lane] = __fdiv_rn(exp_c(__fsub_rn(key_value(my_key), m)), d);
 }
 
+// Top-k and softmax weights (and, on request, probabilities) of rows r0..r1-1
+// from their finished logits in a.logits (before the bias); one warp.
+template <int NE>
+__device__ __forceinline__ void route_topk_rows(const RouteArgs& a, int r0, int r1, int lane) {
+    for (int r = r0; r < r1; ++r) {
+        const float* brow = a.bias ? a.bias + (size_t)find_block(a.off, a.nb, r) * a.E : nullptr;
+        uint32_t key[NE], id[NE];
+        uint32_t valid = 0, nonfinite = 0;
+#pragma unroll
+        for (int i = 0; i < NE; ++i) {
+            const int e = lane + 32 * i;
+            id[i] = (uint32_t)e;
+            key[i] = 0;
+            if (e < a.E) {
+                const float z = finish_logit(__ldcg(a.logits + (size_t)r * a.E + e), brow, e);
+                if (!isfinite(z)) ++nonfinite;
+                key[i] = order_key(z);
+                valid |= 1u << i;
+            }
+        }
+        nonfinite = __reduce_add_sync(0xffffffffu, nonfinite);
+        if (lane == 0) status_add(a.status, MOE_STATUS_NONFINITE_LOGITS, nonfinite);
+        uint32_t my_id, my_key;
+        warp_topk<NE>(key, id, valid, a.k, lane, my_id, my_key);
+        write_topk(a.topk_idx + (size_t)r * a.k, a.topk_w + (size_t)r * a.k, a.k, lane, my_id,
+                   my_key);
+        if (a.topk_p) write_topk_probs<NE>(a.topk_p + (size_t)r * a.k, a.k, lane, key, valid, my_key);
+    }
+}
+
+__device__ __forceinline__ void route_topk(const RouteArgs& a, int r0, int r1, int lane) {
+    const int ne = (a.E + 31) >> 5;
+    if (ne <= 1) route_topk_rows<1>(a, r0, r1, lane);
+    else if (ne <= 2) route_topk_rows<2>(a, r0, r1, lane);
+    else if (ne <= 4) route_topk_rows<4>(a, r0, r1, lane);
+    else if (ne <= 8) route_topk_rows<8>(a, r0, r1, lane);
+    else if (ne <= 16) route_topk_rows<16>(a, r0, r1, lane);
+    else route_topk_rows<32>(a, r0, r1, lane);
+}
+
+
+// Logits of one row for four experts (eg * 4 .. eg * 4 + 3), one warp: its
+// stripes' loads are issued four stripes at a time (registers), and every
+// later stripe of the row is prefetched into L1 first, so the warp pays about
+// one memory round trip.  The four accumulators are reduced by two transposed
+// halving steps and three plain butterfly steps (the same pairs as the
+// contract's butterfly); the logits go to a.logits (before the bias).
+constexpr int kSmET = 4;   // experts per warp task
+constexpr int kSmPD = 4;   // stripes held in registers at a time
+
+__device__ __forceinline__ void prefetch_l1_line(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ void route_logits_1x4(const RouteArgs& a, int row, int eg, int lane) {
+    const __nv_bfloat16* xr = a.x + (size_t)row * a.H;
+    // L1 prefetch of stripes kSmPD.. of x and the four router rows: one
+    // 128-byte line per lane and step (a stripe of a row is 4 lines)
+    for (int l = lane; (kSmPD + l / 20) * 256 < a.H; l += 32) {
+        const int st = kSmPD + l / 20, r5 = (l % 20) >> 2, q = l & 3;
+        const int ex = eg * kSmET + r5 - 1;
+        const __nv_bfloat16* base = r5 == 0 ? xr : a.wr + (size_t)(ex < a.E ? ex : 0) * a.H;
+        prefetch_l1_line(base + st * 256 + q * 64);
+    }
+    float acc[kSmET];
+#pragma unroll
+    for (int i = 0; i < kSmET; ++i) acc[i] = 0.0f;
+    for (int s0 = 0; s0 < a.H; s0 += kSmPD * 256) {
+        uint4 xv[kSmPD], wv[kSmPD][kSmET];
+#pragma unroll
+        for (int si = 0; si < kSmPD; ++si) {
+            const int col = s0 + si * 256 + lane * 8;
+            const bool in = col < a.H;
+            xv[si] = in ? __ldg(reinterpret_cast<const uint4*>(xr + col)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int e = 0; e < kSmET; ++e) {
+                const int ex = eg * kSmET + e;
+                wv[si][e] = (in && ex < a.E)
+                    ? __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)ex * a.H + col))
+                    : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int si = 0; si < kSmPD; ++si) {
+            if (s0 + si * 256 >= a.H) break;
+#pragma unroll
+            for (int e = 0; e < kSmET; ++e) acc[e] = dot8_bf16(xv[si], wv[si][e], acc[e]);
+        }
+    }
+    // halving at partner distances 16 and 8 (4 -> 1 accumulators), then
+    // plain butterfly steps at 4, 2, 1; lane holds expert (lane >> 3) & 3
+#pragma unroll
+    for (int o = 16, h = 2; o >= 8; o >>= 1, h >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = upper ? acc[i] : acc[i + h];
+            const float keep = upper ? acc[i + h] : acc[i];
+            acc[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+        }
+    }
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1) acc[0] = __fadd_rn(acc[0], __shfl_xor_sync(0xffffffffu, acc[0], o));
+    {
+        const int ex = eg * kSmET + ((lane >> 3) & 3);
+        if ((lane & 7) == 0 && ex < a.E) a.logits[(size_t)row * a.E + ex] = acc[0];
+    }}
+
 }  // namespace moe

@@ -8,11 +8,21 @@
 //   z~[r,e] = tcgen05 bf16 MMA with fp32 accumulation (+ bias), and
 //   |z~ - z| <= beta(r,e) = (H * 2^-21) * |x_r|_2 * |w_e|_2 (+ a rounding slack)
 //
-// where z is the exact-order contract logit.  The bound is a conservative
-// assumption about the tensor core (products exact, fp32-class accumulation:
-// the worst case of K/16 accumulation steps, each off by a few units in the
-// last place of a partial sum no larger than sum|x w| <= |x| |w|, is below it
-// by a wide margin); the parity tests against the CPU oracle check it.
+// where z is the exact-order contract logit.  The accumulation model the bound
+// assumes: each tcgen05.mma (K = 16) adds its 16 products, exact in fp32
+// (bf16 x bf16), to the fp32 accumulator with an error of at most four units
+// of 2^-23 relative to |accumulator| + sum|products of the slice|, whatever
+// its internal order, alignment or truncation.  Both terms are at most
+// sum_h |x_h w_h| <= |x| |w| (Cauchy-Schwarz), so H/16 steps err by at most
+// (H/16) 2^-21 2 |x||w| = H 2^-24 |x||w|.  The contract's fixed-order fp32 sum is
+// within (H/32 + 5) 2^-24 sum|x w| of the exact dot product (recursive
+// summation over H/32 terms per lane, then five butterfly additions).  So
+// |z~ - z| <= (H + H/32 + 5) 2^-24 |x||w| < beta = 8 H 2^-24 |x||w| for every
+// H >= 256: beta covers that model about seven times over.  The norms are
+// fp32 sums times 1.001, which covers their own rounding.  The model is not
+// a documented property of the hardware; the parity tests against the CPU
+// oracle, including rows built to put twin experts on the k-th place at gaps
+// from 1/100 to 10 times beta, check it.
 // With T the k-th largest z~ of the row and bmax = max_e beta(r,e), every
 // expert of the exact top-k satisfies z~ + beta >= T - bmax, and every expert
 // failing that test has z < the k-th largest z, so the exact top-k is the

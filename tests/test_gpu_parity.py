@@ -14,8 +14,9 @@ import pytest
 import torch
 
 from sparse_moe_layer_row_gb300 import moe_block, workloads as W
+import oracle
 from tests.parity_util import (ATOL, Case, assert_close, assert_coreset_equal,
-                               assert_route_equal)
+                               assert_route_equal, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -115,6 +116,11 @@ def test_outputs_beyond_fp16_range(base):
     big.oracle_forward()
     assert_close(gb["y32"], ref["y"], what="y_f32 (scaled)", atol=ATOL * 2.0 ** s)
     assert_close(gb["y"], ref["y"], what="y (scaled)", atol=ATOL * 2.0 ** s)
+
+
+def _small(H=256, E=16, k=4, I=128, Is=128, rows=(32,), tau=0.9, seed=5, sigma_r=0.05):
+    return W.Workload(name="edge", H=H, E=E, k=k, I=I, Is=Is, block_rows=tuple(rows), tau=tau,
+                      sigma_r=sigma_r, x_seed=seed, w_seed=seed)
 
 
 @pytest.mark.parametrize("rows", [(1,), (3,), (5, 0, 7), (13, 1, 1, 30), (37, 64, 50)],
@@ -268,6 +274,58 @@ def test_tensor_core_router_nonfinite_rows_fall_back():
     case = Case(w, T=T, bias=bias)
     g, ref = _route_only(case)
     assert (g["idx"][:, :6] >= 26).all()
+
+
+def test_tensor_core_router_near_ties_around_the_bound():
+    """Adversarial rows for the tensor-core screen (>= 256 rows): its approximate
+    logits are within beta = H 2^-21 |x| |w| of the exact ones, and the exact top-k
+    is recomputed over the experts within that bound of the k-th.  Here every row
+    puts a twin pair of router rows at ranks k and k + 1: expert b is expert a
+    with one element raised by one bf16 ulp, so their gap is x[h*] times that ulp,
+    and x[h*] varies over the rows to sweep the gap from 1/100 of the row's beta to
+    ten times it (both signs, so either twin wins).  Ids and weights stay bit-exact
+    against the oracle on every row."""
+    H, E, k, R = 256, 64, 8, 512
+    g = torch.Generator().manual_seed(11)
+    x0 = torch.randn(H, generator=g)
+    hs = int(torch.argmax(x0.abs()))
+    u = x0 / x0.norm()
+    wr = torch.randn(E, H, generator=g) * 0.002
+    for e in range(7):                       # ranks 1..7 for every row
+        wr[e] = u * (0.06 + 0.01 * e) * 16
+    a, b = 20, 41                            # the twins, ranks 8 and 9
+    wr[a] = u * 0.04 * 16
+    wr = wr.to(torch.bfloat16)
+    wb = wr[a].clone()
+    up = (wb[hs].view(torch.int16) + (1 if wb[hs] > 0 else -1)).view(torch.bfloat16)
+    wb[hs] = up                              # one ulp away from zero
+    wr[b] = wb
+    delta = float(wr[b, hs].float() - wr[a, hs].float())
+    # x[h*] per row: the gap x[h*] * delta against beta of the row
+    xs = x0.repeat(R, 1)
+    G = H * 2.0 ** -21
+    wmax = float(wr.float().norm(dim=1).max()) * 1.001
+    frac = torch.logspace(-2, 1, R // 2, generator=None)
+    targets = torch.cat([frac, -frac])
+    for r in range(R):
+        xn = float(x0.norm()) * 1.001
+        xs[r, hs] = float(targets[r]) * G * xn * wmax / abs(delta)
+    x = xs.to(torch.bfloat16)
+    w = _small(H=H, E=E, k=k, rows=(R,), sigma_r=0.02)
+    T = W.make_tensors(w, device="cuda")
+    T.w_router.copy_(wr.to("cuda"))
+    case = Case(w, T=T, x=x.to("cuda").contiguous())
+    g_, ref = _route_only(case)
+    # the construction did what it says: the twins hold ranks k and k + 1 and
+    # their exact gaps straddle the screen's thresholds
+    z = oracle.route(u16(x), u16(wr), [0, R], k, want_logits=True)[2]
+    xn = np.linalg.norm(x.float().numpy(), axis=1) * 1.001
+    gap = np.abs(z[:, a] - z[:, b]) / (G * xn * wmax)
+    top = ref["idx"]
+    on_edge = [(a in top[r]) != (b in top[r]) for r in range(R)]
+    assert sum(on_edge) > 0.9 * R
+    for lo, hi in ((0.01, 0.5), (0.5, 1.0), (1.0, 2.0), (2.0, 4.0)):
+        assert ((gap > lo) & (gap < hi)).sum() >= 10, (lo, hi)
 
 
 @pytest.mark.parametrize("rows", [(32,), (8,) * 80], ids=["one-block", "80-blocks"])
