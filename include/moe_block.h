@@ -214,6 +214,25 @@ moe_status moe_block_forward(const moe_plan* plan, const void* x, int32_t R,
                              const float* w_renorm, const uint32_t* keep, void* y, float* y_f32,
                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* One denoising pass of the layer: route, coreset and forward in one call.
+ * (Model card, Hardware: every pass as one GPU submission; intro and Usage for
+ * the three steps.)
+ * Does what moe_block_route_probs, moe_block_coreset_mass and
+ * moe_block_forward do in sequence, with the same arguments, outputs and
+ * errors (topk_p NULL: the weight mass; non-NULL: the probability mass, and
+ * topk_p is written), bit for bit the same results.  For R <= 32 the router,
+ * the coreset and the forward's bookkeeping run as one kernel (the last CTA
+ * of the router grid carries on with the top-k, the coreset and the pair
+ * lists), so a pass is four launches; larger calls run the three calls'
+ * kernels.  All outputs (topk_idx, topk_w, topk_p, keep, core_size, w_renorm,
+ * n_empty, y, y_f32) are written as by those calls. */
+moe_status moe_block_pass(const moe_plan* plan, const void* x, int32_t R,
+                          const int32_t* block_offsets, int32_t nb, const float* logit_bias,
+                          float tau, int32_t max_experts, int32_t* topk_idx, float* topk_w,
+                          float* topk_p, uint32_t* keep, int32_t* core_size, float* w_renorm,
+                          int32_t* n_empty, void* y, float* y_f32, void* workspace,
+                          size_t workspace_bytes, moe_stream_t stream);
+
 /* Live-row reuse (InfiniLM pull 604 "Clover MoE": Summary, Motivation and the
  * benchmark table's "expert budget/live reuse" rows).  The pages name live-row
  * reuse with a refresh interval of five passes and define neither the live
@@ -268,10 +287,12 @@ moe_status moe_block_route_noalloc(const moe_plan* plan, const void* x, int32_t 
 /* Same type as cudaEvent_t. */
 typedef struct CUevent_st* moe_event_t;
 
-/* Optional per-kernel timing of moe_block_forward.  With n_events == 5 the
- * forward records, on its stream, events[0] before the pair scatter,
- * events[1] before the gate/up GEMM, events[2] before the down GEMM,
- * events[3] before the final bf16 store and events[4] after it.  The events
+/* Optional per-kernel timing of moe_block_forward and moe_block_pass.  With
+ * n_events == 5 the call records, on its stream, events[0] before the pair
+ * scatter (moe_block_pass: before the fused front end, or before the router
+ * for calls of more than 32 rows), events[1] before the gate/up GEMM,
+ * events[2] before the down GEMM, events[3] before the final bf16 store and
+ * events[4] after it.  The events
  * belong to the caller and must outlive every forward that records them;
  * n_events == 0 (events NULL) turns the recording off.  Not thread-safe
  * against concurrent forwards on the same plan. */

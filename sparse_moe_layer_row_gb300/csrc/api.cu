@@ -141,6 +141,96 @@ moe_status moe::set_error(moe_status s, const char* msg) {
     return s;
 }
 
+namespace {
+
+// Record forward event i of the plan on `st`, if the plan has events.  Under
+// stream capture an event record must be an external node to be recorded at
+// every graph launch (a plain record only orders the capture).
+cudaError_t mark_event(const moe_plan* p, int i, cudaStream_t st) {
+    if (p->n_fwd_events != 5) return cudaSuccess;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cap);
+    if (e != cudaSuccess) return e;
+    return cudaEventRecordWithFlags(
+        p->fwd_events[i], st,
+        cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
+}
+
+// The forward's launches after validation: the scatter (or, with `front`,
+// the fused front end that does the routing and coreset too), the two grouped
+// GEMMs and the combine.  `marked`: event 0 of the plan's forward events was
+// already recorded by the caller.
+moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
+                           const int32_t* block_offsets, int32_t nb, const int32_t* topk_idx,
+                           const float* w_renorm, const uint32_t* keep, const uint8_t* live,
+                           void* y, float* y_f32, void* workspace, cudaStream_t st,
+                           const FrontArgs* front, bool marked) {
+    const moe_dims& d = p->d;
+    const Layout L = make_layout(d);
+    const bool small = R <= kSmallRows;
+    const int nt_gu = small ? kSmallN : kLargeNGU;
+    const int nt_dn = small ? kSmallN : kLargeNDown;
+
+    ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
+                   small ? 64 : 128,
+                   at<int32_t>(workspace, L.prank), at<int32_t>(workspace, L.hist),
+                   at<int32_t>(workspace, L.count),
+                   at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
+                   at<int4>(workspace, L.units_gu), at<int4>(workspace, L.units_dn),
+                   at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
+                   at<int32_t>(workspace, L.inv),
+                   at<uint32_t>(workspace, L.status),
+                   live, at<int32_t>(workspace, L.shared_rows), at<int32_t>(workspace, L.shared_inv),
+                   at<int32_t>(workspace, L.live_base)};
+    GemmMaps gu{}, dn{};
+    const auto L2A = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+    gu.a0 = p->tm_wg; gu.a1 = p->tm_wu; gu.a2 = p->tm_sg; gu.a3 = p->tm_su;
+    dn.a0 = p->tm_wd; dn.a1 = p->tm_wd; dn.a2 = p->tm_sd; dn.a3 = p->tm_sd;
+    const uint32_t box = small ? 16 : 64;   // B rows per TMA box (see k_gemm)
+    bool good = encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
+                encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
+                encode_bf16(&dn.b0, at<void>(workspace, L.h), (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
+                            box, L2A) &&
+                encode_bf16(&dn.b1, at<void>(workspace, L.hs), 2 * (uint64_t)d.Is,
+                            (uint64_t)d.max_rows, 0, box, L2A);
+    if (!good) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation tensor");
+    GemmArgs ga{at<int4>(workspace, L.units_gu), at<int32_t>(workspace, L.misc) + 1, d.E, d.H, d.I,
+                d.Is, R, static_cast<const __nv_bfloat16*>(x), at<__nv_bfloat16>(workspace, L.h),
+                at<__nv_bfloat16>(workspace, L.hs),
+                at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
+                at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
+                (int)(L.max_pairs + d.max_rows), (int)L.max_pairs, at<uint32_t>(workspace, L.status),
+                live ? at<int32_t>(workspace, L.shared_rows) : nullptr, p->wait_ns};
+    auto mark = [&](int i) { return mark_event(p, i, st); };
+    cudaError_t e = marked ? cudaSuccess : mark(0);
+    if (front) {
+        FrontArgs fa = *front;
+        fa.s = sa;
+        if (e == cudaSuccess) e = launch_front(fa, p->num_sms, st);
+        if (e != cudaSuccess) return cuda_fail(e, "front-end launch");
+    } else {
+        if (e == cudaSuccess) e = launch_scatter(sa, small, p->num_sms, st);
+        if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
+    }
+    if ((e = mark(1)) == cudaSuccess) e = launch_gemm(kGateUp, small, gu, ga, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
+    GemmArgs gd = ga;
+    gd.units = at<int4>(workspace, L.units_dn);
+    gd.n_units = at<int32_t>(workspace, L.misc) + 2;
+    if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, small, dn, gd, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
+    CombineArgs ca{at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
+                   (int)(L.max_pairs + d.max_rows), at<int32_t>(workspace, L.inv), R, d.H, d.k,
+                   (int)L.max_pairs, static_cast<__nv_bfloat16*>(y), y_f32,
+                   at<uint32_t>(workspace, L.status), live, at<int32_t>(workspace, L.shared_inv)};
+    if ((e = mark(3)) == cudaSuccess) e = launch_combine(ca, p->num_sms, st);
+    if (e == cudaSuccess) e = mark(4);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return ok();
+}
+
+}  // namespace
+
 extern "C" {
 
 int32_t moe_version(void) { return 100; }
@@ -314,72 +404,59 @@ moe_status moe_block_forward_live(const moe_plan* p, const void* x, int32_t R,
         !aligned(keep, 4))
         return fail(MOE_ERR_INVALID_ARG, "topk_idx/w_renorm/keep NULL or misaligned");
     if (R == 0) return ok();
-    const moe_dims& d = p->d;
-    const Layout L = make_layout(d);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const bool small = R <= kSmallRows;
-    const int nt_gu = small ? kSmallN : kLargeNGU;
-    const int nt_dn = small ? kSmallN : kLargeNDown;
+    return enqueue_forward(p, x, R, block_offsets, nb, topk_idx, w_renorm, keep, live, y, y_f32,
+                           workspace, reinterpret_cast<cudaStream_t>(stream), nullptr, false);
+}
 
-    ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
-                   small ? 64 : 128,
-                   at<int32_t>(workspace, L.prank), at<int32_t>(workspace, L.hist),
-                   at<int32_t>(workspace, L.count),
-                   at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
-                   at<int4>(workspace, L.units_gu), at<int4>(workspace, L.units_dn),
-                   at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
-                   at<int32_t>(workspace, L.inv),
-                   at<uint32_t>(workspace, L.status),
-                   live, at<int32_t>(workspace, L.shared_rows), at<int32_t>(workspace, L.shared_inv),
-                   at<int32_t>(workspace, L.live_base)};
-    GemmMaps gu{}, dn{};
-    const auto L2A = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
-    gu.a0 = p->tm_wg; gu.a1 = p->tm_wu; gu.a2 = p->tm_sg; gu.a3 = p->tm_su;
-    dn.a0 = p->tm_wd; dn.a1 = p->tm_wd; dn.a2 = p->tm_sd; dn.a3 = p->tm_sd;
-    const uint32_t box = small ? 16 : 64;   // B rows per TMA box (see k_gemm)
-    bool good = encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
-                encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
-                encode_bf16(&dn.b0, at<void>(workspace, L.h), (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
-                            box, L2A) &&
-                encode_bf16(&dn.b1, at<void>(workspace, L.hs), 2 * (uint64_t)d.Is,
-                            (uint64_t)d.max_rows, 0, box, L2A);
-    if (!good) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation tensor");
-    GemmArgs ga{at<int4>(workspace, L.units_gu), at<int32_t>(workspace, L.misc) + 1, d.E, d.H, d.I,
-                d.Is, R, static_cast<const __nv_bfloat16*>(x), at<__nv_bfloat16>(workspace, L.h),
-                at<__nv_bfloat16>(workspace, L.hs),
-                at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
-                at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
-                (int)(L.max_pairs + d.max_rows), (int)L.max_pairs, at<uint32_t>(workspace, L.status),
-                live ? at<int32_t>(workspace, L.shared_rows) : nullptr, p->wait_ns};
-    // Under stream capture an event record must be an external node to be
-    // recorded at every graph launch (a plain record only orders the capture).
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (p->n_fwd_events == 5 && cudaStreamIsCapturing(st, &cap) != cudaSuccess)
-        return fail(MOE_ERR_CUDA, "cudaStreamIsCapturing failed");
-    const unsigned ev_flags =
-        cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
-    auto mark = [&](int i) {
-        return p->n_fwd_events == 5 ? cudaEventRecordWithFlags(p->fwd_events[i], st, ev_flags)
-                                    : cudaSuccess;
-    };
-    cudaError_t e = mark(0);
-    if (e == cudaSuccess) e = launch_scatter(sa, small, p->num_sms, st);
-    if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
-    if ((e = mark(1)) == cudaSuccess) e = launch_gemm(kGateUp, small, gu, ga, p->num_sms, st);
-    if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
-    GemmArgs gd = ga;
-    gd.units = at<int4>(workspace, L.units_dn);
-    gd.n_units = at<int32_t>(workspace, L.misc) + 2;
-    if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, small, dn, gd, p->num_sms, st);
-    if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
-    CombineArgs ca{at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
-                   (int)(L.max_pairs + d.max_rows), at<int32_t>(workspace, L.inv), R, d.H, d.k,
-                   (int)L.max_pairs, static_cast<__nv_bfloat16*>(y), y_f32,
-                   at<uint32_t>(workspace, L.status), live, at<int32_t>(workspace, L.shared_inv)};
-    if ((e = mark(3)) == cudaSuccess) e = launch_combine(ca, p->num_sms, st);
-    if (e == cudaSuccess) e = mark(4);
-    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-    return ok();
+moe_status moe_block_pass(const moe_plan* p, const void* x, int32_t R, const int32_t* block_offsets,
+                          int32_t nb, const float* logit_bias, float tau, int32_t max_experts,
+                          int32_t* topk_idx, float* topk_w, float* topk_p, uint32_t* keep,
+                          int32_t* core_size, float* w_renorm, int32_t* n_empty, void* y,
+                          float* y_f32, void* workspace, size_t workspace_bytes,
+                          moe_stream_t stream) {
+    moe_status s = check_call(p, R, block_offsets, nb, workspace, workspace_bytes);
+    if (s != MOE_OK) return s;
+    if (!x || !aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x is NULL or not 16-byte aligned");
+    if (!y || !aligned(y, 16)) return fail(MOE_ERR_INVALID_ARG, "y is NULL or not 16-byte aligned");
+    if (y_f32 && !aligned(y_f32, 16)) return fail(MOE_ERR_INVALID_ARG, "y_f32 not 16-byte aligned");
+    if (!topk_idx || !topk_w || !keep || !core_size || !w_renorm)
+        return fail(MOE_ERR_INVALID_ARG, "a required pass output is NULL");
+    const void* ps[8] = {topk_idx, topk_w, keep, core_size, w_renorm, n_empty, topk_p, logit_bias};
+    for (const void* q : ps)
+        if (q && !aligned(q, 4)) return fail(MOE_ERR_INVALID_ARG, "pass pointer misaligned");
+    if (!(tau > 0.0f)) return fail(MOE_ERR_INVALID_ARG, "tau=%g must be > 0 (and not NaN)", (double)tau);
+    if (max_experts < 0) return fail(MOE_ERR_INVALID_ARG, "max_experts=%d must be >= 0", max_experts);
+    if (R == 0) return ok();
+    const moe_dims& d = p->d;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (R <= kSmallRows) {
+        // one launch for the router, the coreset and the bookkeeping (front.cu)
+        const Layout L = make_layout(d);
+        uint32_t* ticket = at<uint32_t>(workspace, L.route_cnt);
+        cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(uint32_t), st);
+        if (e != cudaSuccess) return cuda_fail(e, "front-end ticket");
+        uint32_t* status = at<uint32_t>(workspace, L.status);
+        FrontArgs fa{};
+        fa.r = RouteArgs{static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(p->wr),
+                         logit_bias, block_offsets, R, d.H, d.E, d.k, nb,
+                         at<float>(workspace, L.logits), ticket, topk_idx, topk_w, status, topk_p};
+        fa.c = CoresetArgs{block_offsets, topk_idx, topk_w, topk_p, R, d.E, d.k, nb, tau,
+                           max_experts, keep, core_size, w_renorm, n_empty, status};
+        fa.ticket = ticket;
+        return enqueue_forward(p, x, R, block_offsets, nb, topk_idx, w_renorm, keep, nullptr, y,
+                               y_f32, workspace, st, &fa, false);
+    }
+    // larger calls: the router, coreset and forward kernels of the three calls
+    cudaError_t e = mark_event(p, 0, st);
+    if (e != cudaSuccess) return cuda_fail(e, "event record");
+    s = moe_block_route_probs(p, x, R, block_offsets, nb, logit_bias, topk_idx, topk_w, topk_p,
+                              workspace, workspace_bytes, stream);
+    if (s != MOE_OK) return s;
+    s = moe_block_coreset_mass(p, R, block_offsets, nb, topk_idx, topk_w, topk_p, tau, max_experts,
+                               keep, core_size, w_renorm, n_empty, workspace, workspace_bytes, stream);
+    if (s != MOE_OK) return s;
+    return enqueue_forward(p, x, R, block_offsets, nb, topk_idx, w_renorm, keep, nullptr, y, y_f32,
+                           workspace, st, nullptr, true);
 }
 
 moe_status moe_plan_set_forward_events(moe_plan* p, moe_event_t const* events,

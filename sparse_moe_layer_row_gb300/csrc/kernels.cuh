@@ -111,6 +111,14 @@ struct GemmMaps {
     CUtensorMap a0, a1, a2, a3, b0, b1;
     CUtensorMap bg;   // x with a one-row box: TMA gather4 of routed rows (small batches)
 };
+// The fused front end of a small call (front.cu): router, coreset and
+// forward bookkeeping in one launch.
+struct FrontArgs {
+    RouteArgs r;
+    CoresetArgs c;
+    ScatterArgs s;
+    uint32_t* ticket;     // CTA ticket, zero at launch
+};
 // Small batches (R <= kSmallRows): one-CTA bookkeeping and gathered x rows.
 constexpr int kSmallRows = 32;
 constexpr int kMaxExperts = 1024;
@@ -120,6 +128,7 @@ cudaError_t launch_route_tc(const RouteTcArgs&, const CUtensorMap& tm_x, const C
                             int num_sms, cudaStream_t);
 cudaError_t launch_coreset(const CoresetArgs&, cudaStream_t);
 cudaError_t launch_scatter(const ScatterArgs&, bool small, int num_sms, cudaStream_t);
+cudaError_t launch_front(const FrontArgs&, int num_sms, cudaStream_t);
 cudaError_t launch_combine(const CombineArgs&, int num_sms, cudaStream_t);
 cudaError_t gemm_set_attributes();
 cudaError_t launch_gemm(int mode, bool small, const GemmMaps&, const GemmArgs&, int grid,

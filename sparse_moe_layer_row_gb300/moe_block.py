@@ -78,6 +78,9 @@ def load(build_if_missing: bool = False):
     L.moe_block_coreset_mass.restype = ctypes.c_int
     L.moe_block_coreset_mass.argtypes = [P, i32, P, i32, P, P, P, ctypes.c_float, i32, P, P, P,
                                          P, P, sz, P]
+    L.moe_block_pass.restype = ctypes.c_int
+    L.moe_block_pass.argtypes = [P, P, i32, P, i32, P, ctypes.c_float, i32, P, P, P, P, P, P, P,
+                                 P, P, P, sz, P]
     L.moe_block_route_noalloc.restype = ctypes.c_int
     L.moe_block_route_noalloc.argtypes = [P, P, i32, P, i32, P, P, P, P]
     L.moe_plan_set_forward_events.restype = ctypes.c_int
@@ -301,6 +304,39 @@ def moe_block_forward(plan: Plan, x, block_offsets, topk_idx, w_renorm, keep, y,
                                     _stream(stream)))
 
 
+def moe_block_pass(plan: Plan, x, block_offsets, logit_bias, tau: float, max_experts: int,
+                   topk_idx, topk_w, topk_p, keep, core_size, w_renorm, n_empty, y, y_f32,
+                   workspace, stream=None):
+    """One pass: route -> coreset -> forward in one call (four launches for <= 32 rows).
+    ``topk_p`` None: the weight mass; a tensor: the probability mass."""
+    d = plan.dims
+    R = x.shape[0]
+    nb = block_offsets.shape[0] - 1
+    _need(x, "x", torch.bfloat16, (R, d.H))
+    _need(block_offsets, "block_offsets", torch.int32)
+    if logit_bias is not None:
+        _need(logit_bias, "logit_bias", torch.float32, (nb, d.E))
+    _need(topk_idx, "topk_idx", torch.int32, (R, d.k))
+    _need(topk_w, "topk_w", torch.float32, (R, d.k))
+    if topk_p is not None:
+        _need(topk_p, "topk_p", torch.float32, (R, d.k))
+    _need(keep, "keep", torch.int32, (nb, (d.E + 31) // 32))
+    _need(core_size, "core_size", torch.int32, (nb,))
+    _need(w_renorm, "w_renorm", torch.float32, (R, d.k))
+    if n_empty is not None:
+        _need(n_empty, "n_empty", torch.int32, (nb,))
+    _need(y, "y", torch.bfloat16, (R, d.H))
+    if y_f32 is not None:
+        _need(y_f32, "y_f32", torch.float32, (R, d.H))
+    _need(workspace, "workspace", torch.uint8)
+    _check(load().moe_block_pass(plan.handle, _ptr(x), R, _ptr(block_offsets), nb,
+                                 _ptr(logit_bias), ctypes.c_float(tau), int(max_experts),
+                                 _ptr(topk_idx), _ptr(topk_w), _ptr(topk_p), _ptr(keep),
+                                 _ptr(core_size), _ptr(w_renorm), _ptr(n_empty), _ptr(y),
+                                 _ptr(y_f32), _ptr(workspace), workspace.numel(),
+                                 _stream(stream)))
+
+
 def moe_read_device_status(workspace: torch.Tensor, stream=None) -> dict:
     _need(workspace, "workspace", torch.uint8)
     out = (ctypes.c_uint32 * STATUS_WORDS)()
@@ -385,10 +421,23 @@ class MoeBlockLayer:
                           self.workspace, stream, live=live)
         return y
 
-    def __call__(self, x, block_offsets, tau: float, bias=None, y=None, y_f32=None, stream=None):
-        idx, w = self.route(x, block_offsets, bias, stream)
-        keep, _, wr, _ = self.coreset(block_offsets, idx, w, tau, stream)
-        return self.forward(x, block_offsets, idx, wr, keep, y, y_f32, stream)
+    def __call__(self, x, block_offsets, tau: float, bias=None, y=None, y_f32=None, stream=None,
+                 max_experts: int = 0, probs: bool = False):
+        """One pass (moe_block_pass): route -> coreset -> forward; returns y.  The
+        routing outputs stay in the layer's buffers (topk_idx, topk_w, keep,
+        w_renorm ...) until the next call."""
+        R = x.shape[0]
+        nb = block_offsets.shape[0] - 1
+        y = self._y[:R] if y is None else y
+        p = None
+        if probs:
+            if not hasattr(self, "_topk_p"):
+                self._topk_p = torch.empty_like(self._topk_w)
+            p = self._topk_p[:R]
+        moe_block_pass(self.plan, x, block_offsets, bias, tau, max_experts, self._topk_idx[:R],
+                       self._topk_w[:R], p, self._keep[:nb], self._core[:nb], self._w_renorm[:R],
+                       self._empty[:nb], y, y_f32, self.workspace, stream)
+        return y
 
     def status(self, stream=None) -> dict:
         return moe_read_device_status(self.workspace, stream)

@@ -25,7 +25,7 @@ def test_accounting_full_shape_block():
 
 def _meas(w, used, pairs, step_ms, gu_ms):
     return dict(total_ms=step_ms * 10, steps=10, used=set(range(used)), pairs=pairs,
-                kern={"scatter": [0.01], "gate_up": [gu_ms], "down": [0.02], "combine": [0.005]},
+                kern={"front": [0.01], "gate_up": [gu_ms], "down": [0.02], "combine": [0.005]},
                 phase_ms={"route": [0.01], "coreset": [0.01], "forward": [0.1]}, clocks=None)
 
 
@@ -39,7 +39,7 @@ def test_summarize_hbm_bound_block():
     assert math.isclose(s["value"], 32 * 10 / (1.76e-3))
     assert math.isclose(s["step_roofline_frac"], acc["step_bytes"] / 6800e9 / 176e-6)
     assert s["step_roofline_bound"] == "hbm"
-    assert set(s["kernel_us"]) == {"scatter", "gate_up", "down", "combine"}
+    assert set(s["kernel_us"]) == {"front", "gate_up", "down", "combine"}
 
 
 def test_summarize_tensor_bound_prefill():

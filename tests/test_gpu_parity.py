@@ -305,7 +305,7 @@ def test_tensor_core_router_near_ties_around_the_bound():
     xs = x0.repeat(R, 1)
     G = H * 2.0 ** -21
     wmax = float(wr.float().norm(dim=1).max()) * 1.001
-    frac = torch.logspace(-2, 1, R // 2, generator=None)
+    frac = torch.logspace(-2, 1, R // 2)
     targets = torch.cat([frac, -frac])
     for r in range(R):
         xn = float(x0.norm()) * 1.001
