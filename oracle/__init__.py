@@ -48,6 +48,8 @@ def _configure(L):
         L.moe_oracle_coreset.argtypes = [P, i, i, i, i, P, P, P, ctypes.c_float, P, P, P, P, i]
         L.moe_oracle_expert_ffn.restype = None
         L.moe_oracle_expert_ffn.argtypes = [P, P, P, P, i, i, P]
+        L.moe_oracle_dequant.restype = ctypes.c_int
+        L.moe_oracle_dequant.argtypes = [P, P, i, i, i, P]
         L.moe_oracle_forward.restype = ctypes.c_int
         L.moe_oracle_forward.argtypes = [P, P, i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, P,
                                          P, i]
@@ -148,6 +150,31 @@ def keep_mask(keep: np.ndarray, E: int) -> np.ndarray:
     out = np.zeros((nb, E), bool)
     for e in range(E):
         out[:, e] = (keep[:, e // 32] >> np.uint32(e % 32)) & 1
+    return out
+
+
+def dequant(q, d, bits):
+    """Quantised weights back to bf16 bit patterns (reading 8 of moe_oracle.c: blocks
+    of 32 along the input dimension, one bf16 scale each, weight = bf16(q * d)).
+
+    q: int8 [..., rows, K] (bits 8) or uint8 [..., rows, K / 2] (bits 4, two per
+    byte, even element in the low nibble); d: bf16 bits (uint16) [..., K / 32, rows].
+    Returns uint16 [..., rows, K]."""
+    q = np.ascontiguousarray(q)
+    d = np.ascontiguousarray(d, dtype=np.uint16)
+    lead = q.shape[:-2]
+    rows = q.shape[-2]
+    K = q.shape[-1] * (2 if bits == 4 else 1)
+    out = np.zeros(lead + (rows, K), np.uint16)
+    qf = q.reshape((-1,) + q.shape[-2:])
+    df = d.reshape((-1,) + d.shape[-2:])
+    of = out.reshape((-1, rows, K))
+    for i in range(qf.shape[0]):
+        qi, di = np.ascontiguousarray(qf[i]), np.ascontiguousarray(df[i])
+        oi = np.zeros((rows, K), np.uint16)
+        if lib().moe_oracle_dequant(_ptr(qi), _ptr(di), int(bits), rows, K, _ptr(oi)) != 0:
+            raise ValueError("oracle dequant: invalid arguments")
+        of[i] = oi
     return out
 
 

@@ -53,6 +53,14 @@
  *  6. Renormalise: per row, s' = sum of surviving w_j in rank order (fp32),
  *     w'_j = w_j / s', 0 for dropped j; a row with s' == 0 keeps only the
  *     shared expert and is counted as empty.
+ *  8. Quantised experts (model card, Files: 8-bit and 4-bit expert files; the
+ *     page gives no codec).  Reading: along a weight row's input dimension,
+ *     blocks of 32 weights share one bf16 scale d; the weight is stored as a
+ *     signed integer q (int8, or a 4-bit two's-complement nibble, two per byte,
+ *     the even element in the low nibble) and stands for q * d rounded once to
+ *     bf16 (round to nearest, ties to even; q * d itself is exact in fp32).  The
+ *     scales are stored block-major: d[block][row].  The FFN of step 7 then runs
+ *     on those bf16 weights.
  *  7. Expert FFN in fp64: E_e(x) = Wd_e (silu(Wg_e x) * (Wu_e x)); the shared
  *     expert S is the same form; y_r = S(x_r) + sum_j w'_j E_(e_j)(x_r), with j
  *     in rank order, over surviving j only.
@@ -381,6 +389,41 @@ long moe_oracle_coreset(const int32_t* block_offsets, int nb, int R, int E, int 
     free(in_core);
     free(order);
     return bad;
+}
+
+/* ------------------------------------------------------------------------- */
+/* quantised weights (reading 8)                                             */
+
+/* fp32 -> bf16 bits, round to nearest, ties to even (NaN stays NaN). */
+static uint16_t float_to_bf16_rne(float f) {
+    uint32_t u = float_bits(f);
+    if ((u & 0x7F800000u) == 0x7F800000u)
+        return (uint16_t)((u >> 16) | ((u & 0x7FFFFFu) ? 0x40u : 0u));
+    uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+}
+
+/* One weight matrix [rows, K] back to bf16 bits: q is int8 [rows, K] (bits 8)
+ * or packed nibbles uint8 [rows, K / 2] (bits 4); d is bf16 [K / 32, rows].
+ * Returns 0, or ORC_ERR_ARG. */
+int moe_oracle_dequant(const void* q, const uint16_t* d, int bits, int rows, int K,
+                       uint16_t* out) {
+    if (!q || !d || !out || rows <= 0 || K <= 0 || K % 32 || (bits != 8 && bits != 4))
+        return ORC_ERR_ARG;
+    for (int r = 0; r < rows; ++r)
+        for (int k = 0; k < K; ++k) {
+            int qv;
+            if (bits == 8) {
+                qv = (int)((const int8_t*)q)[(size_t)r * K + k];
+            } else {
+                uint8_t byte = ((const uint8_t*)q)[(size_t)r * (K / 2) + k / 2];
+                int nib = (k & 1) ? (byte >> 4) : (byte & 0xF);
+                qv = nib >= 8 ? nib - 16 : nib;
+            }
+            float scale = bf16_to_float(d[(size_t)(k / 32) * rows + r]);
+            out[(size_t)r * K + k] = float_to_bf16_rne((float)qv * scale);
+        }
+    return ORC_OK;
 }
 
 /* ------------------------------------------------------------------------- */

@@ -262,3 +262,89 @@ def make_tensors(w: Workload, device="cpu", x_seed: int | None = None) -> Tensor
         bias = bias.to(device)
     off = torch.tensor(w.block_offsets(), dtype=torch.int32, device=device)
     return Tensors(x, wr, wg, wu, wd, sg, su, sd, bias, off)
+
+
+# --------------------------------------------------------------------------- quantised experts
+#
+# The 8-bit and 4-bit expert files of the model card ("Clover-35B-A3B-Preview
+# -- CMF", Files: q8_2f, q4tp) store the experts in 8 and 4 bits; the page
+# does not give the codecs.  The format used here: along each weight row's
+# input dimension, blocks of 32 weights share one bf16 scale d; a weight is
+# stored as a signed integer q (int8, or a 4-bit two's-complement nibble, two
+# per byte, the even element in the low nibble) and stands for q * d rounded
+# to bf16.  Synthetic quantised layers come from the synthetic bf16 layer by
+# rounding to nearest (no calibration data): d = bf16(max|w| / qmax) per block,
+# q = clamp(round(w / d)).  These functions only prepare inputs; the
+# dequantisation itself belongs to each side (the kernels and the oracle).
+
+QBLOCK = 32                   # weights per scale, along the input dimension
+QMAX = {8: 127, 4: 7}
+
+
+def quantize_rows(w: torch.Tensor, bits: int):
+    """Round-to-nearest block quantisation of bf16 weights [..., rows, K].
+    Returns (q int8 [..., rows, K] in [-qmax, qmax], d bf16 [..., rows, K / 32])."""
+    if bits not in QMAX:
+        raise ValueError("bits must be 8 or 4")
+    *lead, rows, K = w.shape
+    if K % QBLOCK:
+        raise ValueError("the input dimension must be a multiple of 32")
+    wf = w.float().reshape(*lead, rows, K // QBLOCK, QBLOCK)
+    amax = wf.abs().amax(dim=-1)
+    d = (amax / QMAX[bits]).to(torch.bfloat16)
+    d = torch.where(d.float() > 0, d, torch.ones_like(d))   # all-zero block: any scale
+    q = torch.round(wf / d.float().unsqueeze(-1)).clamp(-QMAX[bits], QMAX[bits]).to(torch.int8)
+    return q.reshape(*lead, rows, K), d
+
+
+def pack_int4(q: torch.Tensor) -> torch.Tensor:
+    """int8 values in [-8, 7], last dim even -> uint8 with two per byte (element 2i
+    in the low nibble, 2i + 1 in the high nibble, two's complement)."""
+    u = (q.to(torch.int16) & 0xF).to(torch.uint8)
+    return (u[..., 0::2] | (u[..., 1::2] << 4)).contiguous()
+
+
+def unpack_int4(p: torch.Tensor) -> torch.Tensor:
+    """Inverse of pack_int4: uint8 [..., K/2] -> int8 [..., K]."""
+    lo = (p & 0xF).to(torch.int16)
+    hi = (p >> 4).to(torch.int16)
+    lo = torch.where(lo >= 8, lo - 16, lo)
+    hi = torch.where(hi >= 8, hi - 16, hi)
+    out = torch.stack([lo, hi], dim=-1).reshape(*p.shape[:-1], p.shape[-1] * 2)
+    return out.to(torch.int8)
+
+
+def scales_k_major(d: torch.Tensor) -> torch.Tensor:
+    """Scales [..., rows, K/32] -> [..., K/32, rows] (the device layout: for one
+    block of 32 along K, the scales of consecutive rows are contiguous)."""
+    return d.transpose(-1, -2).contiguous()
+
+
+@dataclass
+class QuantExperts:
+    """Quantised expert weights in the device layout.  q: int8 [E, rows, K] (8 bits)
+    or uint8 [E, rows, K / 2] (4 bits, packed); d: bf16 [E, K / 32, rows]."""
+    bits: int
+    gate: torch.Tensor
+    up: torch.Tensor
+    down: torch.Tensor
+    gate_scale: torch.Tensor
+    up_scale: torch.Tensor
+    down_scale: torch.Tensor
+    shared_gate: torch.Tensor
+    shared_up: torch.Tensor
+    shared_down: torch.Tensor
+    shared_gate_scale: torch.Tensor
+    shared_up_scale: torch.Tensor
+    shared_down_scale: torch.Tensor
+
+
+def quantize_experts(T: "Tensors", bits: int) -> QuantExperts:
+    """The routed and shared experts of `T` quantised (router untouched)."""
+    def one(w):
+        q, d = quantize_rows(w, bits)
+        return (pack_int4(q) if bits == 4 else q.contiguous()), scales_k_major(d)
+    parts = [one(w) for w in (T.w_gate, T.w_up, T.w_down, T.ws_gate, T.ws_up, T.ws_down)]
+    return QuantExperts(bits, parts[0][0], parts[1][0], parts[2][0], parts[0][1], parts[1][1],
+                        parts[2][1], parts[3][0], parts[4][0], parts[5][0], parts[3][1],
+                        parts[4][1], parts[5][1])

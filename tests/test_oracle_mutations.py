@@ -55,6 +55,12 @@ MUTATIONS = {
                                          "for (int p = 0; p < 32; ++p) t[p] = d[p];"),
     "prob_mass_ignored": ("float wj = (topk_mass ? topk_mass : topk_w)[(size_t)r * k + j];",
                           "float wj = topk_w[(size_t)r * k + j];"),
+    "dequant_nibble_order": ("int nib = (k & 1) ? (byte >> 4) : (byte & 0xF);",
+                             "int nib = (k & 1) ? (byte & 0xF) : (byte >> 4);"),
+    "dequant_nibble_unsigned": ("qv = nib >= 8 ? nib - 16 : nib;", "qv = nib;"),
+    "dequant_scales_row_major": ("d[(size_t)(k / 32) * rows + r]", "d[(size_t)r * (K / 32) + k / 32]"),
+    "dequant_truncates": ("return (uint16_t)((u + 0x7FFFu + lsb) >> 16);",
+                          "return (uint16_t)(u >> 16);"),
 }
 
 PINS = [
@@ -71,6 +77,7 @@ PINS = [
     pins.test_weight_sum_in_rank_order_hand_case,
     pins.test_prob_mass_denominator_in_lane_order_hand_case,
     pins.test_prob_mass_equals_full_softmax, pins.test_coreset_prob_mass_changes_membership,
+    pins.test_dequant_hand_cases,
 ] + [lambda m, s=s: pins.test_coreset_prob_mass_brute_force_random_tiny(m, s) for s in range(2)] \
   + [lambda m, s=s: pins.test_coreset_brute_force_random_tiny(m, s) for s in range(4)] \
   + [lambda m, s=s: pins.test_coreset_budget_brute_force_random_tiny(m, s) for s in range(4)]

@@ -786,3 +786,55 @@ def test_forward_missing_expert_is_an_error(oracle_mod):
     only = {e: experts[e] for e in used}
     y = oracle_mod.forward(x, w.block_offsets(), idx, wr, keep, only, shared, w.E)
     assert np.isfinite(y).all()
+
+
+# --------------------------------------------------------------------------- quantised experts
+
+def _quant_hand_cases():
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "quant_hand.json")
+    with open(path) as f:
+        return json.load(f)["cases"]
+
+
+def test_dequant_hand_cases(oracle_mod):
+    """Quantised weights back to bf16 against the hand-worked blocks of
+    tests/golden/quant_hand.json: products, a rounding, a tie to even, the nibble
+    order and sign, and the block-major scale layout."""
+    for c in _quant_hand_cases():
+        rows, K, bits = c["rows"], c["K"], c["bits"]
+        d = bf16_bits(np.array(c["scales_block_major"], np.float32).reshape(-1)).reshape(K // 32, rows)
+        if bits == 8:
+            q = np.zeros((rows, K), np.int8)
+            for r, cols in c["q"].items():
+                for k, v in cols.items():
+                    q[int(r), int(k)] = v
+        else:
+            q = np.zeros((rows, K // 2), np.uint8)
+            for r, cols in c["bytes"].items():
+                for k, v in cols.items():
+                    q[int(r), int(k)] = int(v, 16)
+        want = np.zeros((rows, K), np.float32)
+        for r, cols in c["w"].items():
+            for k, v in cols.items():
+                want[int(r), int(k)] = v
+        got = oracle_mod.dequant(q, d, bits)
+        assert np.array_equal(got, bf16_bits(want)), c["name"]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_dequant_round_trip_of_the_synthetic_quantiser(oracle_mod, bits):
+    """The synthetic quantiser followed by the oracle's dequantisation: every weight
+    within half a step (d / 2) plus its bf16 rounding of the original, and the
+    all-zero q of a zero block gives +0."""
+    w = W.TINY
+    T = W.make_tensors(w)
+    q, d = W.quantize_rows(T.w_gate[:2], bits)
+    qs = W.pack_int4(q) if bits == 4 else q
+    dq = oracle_mod.dequant(qs.numpy(), u16(W.scales_k_major(d)), bits)
+    back = torch.from_numpy(dq.view(np.int16)).view(torch.bfloat16).float()
+    step = d.float().repeat_interleave(32, dim=-1)
+    orig = T.w_gate[:2].float()
+    assert torch.all((back - orig).abs() <= step / 2 + orig.abs() * 2.0 ** -8 + 1e-30)
+    assert not torch.equal(back, orig)   # it is a real quantisation
