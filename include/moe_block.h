@@ -101,6 +101,39 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
 
 void moe_plan_destroy(moe_plan* plan);
 
+/* Quantised expert weights (model card "Clover-35B-A3B-Preview -- CMF",
+ * Files: the 8-bit and 4-bit expert files; the page gives no codec).  Along
+ * each weight row's input dimension, blocks of 32 weights share one bf16 scale
+ * d; a weight is stored as a signed integer q and stands for q * d rounded
+ * once to bf16 (round to nearest, ties to even).  bits == 8: q is int8;
+ * bits == 4: q is a 4-bit two's-complement nibble, two per byte, the even
+ * element in the low nibble, so the last dimension below is halved (in bytes).
+ * Scales are bf16, block-major: d[block][row] (the scales of consecutive rows
+ * of one block of 32 are contiguous).  Device pointers, 16-byte aligned:
+ *   gate, up        [E, I, H]    codes       gate_scale, up_scale    [E, H/32, I]
+ *   down            [E, H, I]    codes       down_scale              [E, I/32, H]
+ *   shared_gate/up  [Is, H]      codes       shared_gate/up_scale    [H/32, Is]
+ *   shared_down     [H, Is]      codes       shared_down_scale       [Is/32, H]
+ * The router stays bf16. */
+typedef struct moe_quant_weights {
+    int32_t bits;
+    const void *gate, *up, *down;
+    const void *gate_scale, *up_scale, *down_scale;
+    const void *shared_gate, *shared_up, *shared_down;
+    const void *shared_gate_scale, *shared_up_scale, *shared_down_scale;
+} moe_quant_weights;
+
+/* Create a plan whose routed and shared experts are quantised (see
+ * moe_quant_weights); w_router is bf16 [E, H] as for moe_plan_create.  Every
+ * call works on such a plan as on a bf16 one: the routing is the same, and
+ * the expert GEMMs read the codes and scales (half or a quarter of the bf16
+ * bytes) and turn them into bf16 weights in shared memory before the tensor
+ * cores use them.  All call sizes run the streaming kernels (units of 32
+ * rows).  Errors: MOE_ERR_UNSUPPORTED for bits other than 8 or 4, otherwise
+ * as moe_plan_create. */
+moe_status moe_plan_create_quantized(const moe_dims* dims, const void* w_router,
+                                     const moe_quant_weights* qw, moe_plan** out);
+
 /* Router: logits, top-k and weights for every row.
  * (Model card, intro: "256 experts top-8".)
  *   x             [R, H] bf16 rows; R <= max_rows

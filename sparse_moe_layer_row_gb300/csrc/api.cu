@@ -23,6 +23,10 @@ struct moe_plan {
     cudaEvent_t fwd_events[5];
     int n_fwd_events;
     uint64_t wait_ns;     // limit of the kernels' pipeline waits (0: built in)
+    // quantised experts (qbits 8 or 4; 0: bf16): tm_wg .. tm_sd map the codes,
+    // these the scales
+    int qbits;
+    CUtensorMap tm_cg, tm_cu, tm_cd, tm_csg, tm_csu, tm_csd;
 };
 
 namespace {
@@ -75,6 +79,23 @@ bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims,
                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// A tensor map without swizzle: dims[0] innermost (elements), box[i] elements;
+// rank 2 or 3; out-of-bounds elements read as zero.
+bool encode_plain(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* ptr,
+                  uint32_t rank, const uint64_t* dims, const uint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[3], strides[2];
+    cuuint32_t b[3], estr[3] = {1, 1, 1};
+    for (uint32_t i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+    strides[0] = dims[0] * esize;
+    strides[1] = dims[0] * dims[1] * esize;
+    CUresult r = fn(m, dt, rank, const_cast<void*>(ptr), d, strides, b, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -168,11 +189,13 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
     const moe_dims& d = p->d;
     const Layout L = make_layout(d);
     const bool small = R <= kSmallRows;
-    const int nt_gu = small ? kSmallN : kLargeNGU;
-    const int nt_dn = small ? kSmallN : kLargeNDown;
+    // units of the streaming shape: small calls, and quantised weights at any size
+    const bool su = small || p->qbits != 0;
+    const int nt_gu = su ? kSmallN : kLargeNGU;
+    const int nt_dn = su ? kSmallN : kLargeNDown;
 
     ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
-                   small ? 64 : 128,
+                   su ? 64 : 128,
                    at<int32_t>(workspace, L.prank), at<int32_t>(workspace, L.hist),
                    at<int32_t>(workspace, L.count),
                    at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
@@ -186,7 +209,14 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
     const auto L2A = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
     gu.a0 = p->tm_wg; gu.a1 = p->tm_wu; gu.a2 = p->tm_sg; gu.a3 = p->tm_su;
     dn.a0 = p->tm_wd; dn.a1 = p->tm_wd; dn.a2 = p->tm_sd; dn.a3 = p->tm_sd;
-    const uint32_t box = small ? 16 : 64;   // B rows per TMA box (see k_gemm)
+    if (p->qbits) {
+        gu.s0 = p->tm_cg; gu.s1 = p->tm_cu; gu.s2 = p->tm_csg; gu.s3 = p->tm_csu;
+        dn.s0 = p->tm_cd; dn.s1 = p->tm_cd; dn.s2 = p->tm_csd; dn.s3 = p->tm_csd;
+    } else {
+        gu.s0 = gu.s1 = gu.s2 = gu.s3 = p->tm_wg;   // unused by the bf16 kernels
+        dn.s0 = dn.s1 = dn.s2 = dn.s3 = p->tm_wd;
+    }
+    const uint32_t box = su ? 16 : 64;   // B rows per TMA box (see k_gemm)
     bool good = encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
                 encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
                 encode_bf16(&dn.b0, at<void>(workspace, L.h), (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
@@ -212,12 +242,12 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
         if (e == cudaSuccess) e = launch_scatter(sa, small, p->num_sms, st);
         if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
     }
-    if ((e = mark(1)) == cudaSuccess) e = launch_gemm(kGateUp, small, gu, ga, p->num_sms, st);
+    if ((e = mark(1)) == cudaSuccess) e = launch_gemm(kGateUp, su, p->qbits, gu, ga, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
     GemmArgs gd = ga;
     gd.units = at<int4>(workspace, L.units_dn);
     gd.n_units = at<int32_t>(workspace, L.misc) + 2;
-    if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, small, dn, gd, p->num_sms, st);
+    if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, su, p->qbits, dn, gd, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
     CombineArgs ca{at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
                    (int)(L.max_pairs + d.max_rows), at<int32_t>(workspace, L.inv), R, d.H, d.k,
@@ -284,6 +314,79 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
     if (!good) {
         delete p;
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight tensor");
+    }
+    *out = p;
+    return ok();
+}
+
+moe_status moe_plan_create_quantized(const moe_dims* dims, const void* w_router,
+                                     const moe_quant_weights* qw, moe_plan** out) {
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    moe_status s = check_dims(dims);
+    if (s != MOE_OK) return s;
+    if (!qw) return fail(MOE_ERR_INVALID_ARG, "quantised weights are NULL");
+    if (qw->bits != 8 && qw->bits != 4)
+        return fail(MOE_ERR_UNSUPPORTED, "bits=%d: quantised experts are 8 or 4 bits", qw->bits);
+    const void* ws[13] = {w_router, qw->gate, qw->up, qw->down, qw->gate_scale, qw->up_scale,
+                          qw->down_scale, qw->shared_gate, qw->shared_up, qw->shared_down,
+                          qw->shared_gate_scale, qw->shared_up_scale, qw->shared_down_scale};
+    const char* names[13] = {"w_router", "gate", "up", "down", "gate_scale", "up_scale",
+                             "down_scale", "shared_gate", "shared_up", "shared_down",
+                             "shared_gate_scale", "shared_up_scale", "shared_down_scale"};
+    for (int i = 0; i < 13; ++i)
+        if (!ws[i] || !aligned(ws[i], 16))
+            return fail(MOE_ERR_INVALID_ARG, "%s is NULL or not 16-byte aligned", names[i]);
+    moe_plan* p = new moe_plan();
+    p->d = *dims;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e == cudaSuccess) e = gemm_set_attributes();
+    if (e == cudaSuccess) e = gateup_pair_set_attributes(p->num_sms);
+    if (e == cudaSuccess) e = route_tc_set_attributes();
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "device query");
+    }
+    const moe_dims& d = *dims;
+    p->qbits = qw->bits;
+    p->wr = w_router;
+    p->wg = qw->gate; p->wu = qw->up; p->wd = qw->down;
+    p->sg = qw->shared_gate; p->su = qw->shared_up; p->sd = qw->shared_down;
+    // codes: uint8, K in bytes (halved for 4 bits), boxes of 64 K x (64 gate/up
+    // or 128 down) rows; scales: bf16 [blocks][rows], boxes of rows x 2 blocks
+    const uint64_t kb = qw->bits == 8 ? 1 : 2;
+    const uint32_t cbox = (uint32_t)(64 / kb);
+    const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const auto B16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t dg[3] = {d.H / kb, (uint64_t)d.I, (uint64_t)d.E}, dd[3] = {d.I / kb, (uint64_t)d.H, (uint64_t)d.E};
+    const uint64_t dsg[2] = {d.H / kb, (uint64_t)d.Is}, dsd[2] = {d.Is / kb, (uint64_t)d.H};
+    const uint32_t bg[3] = {cbox, 64, 1}, bd[3] = {cbox, 128, 1};
+    const uint64_t cg[3] = {(uint64_t)d.I, (uint64_t)(d.H / 32), (uint64_t)d.E};
+    const uint64_t cd[3] = {(uint64_t)d.H, (uint64_t)(d.I / 32), (uint64_t)d.E};
+    const uint64_t csg[2] = {(uint64_t)d.Is, (uint64_t)(d.H / 32)}, csd[2] = {(uint64_t)d.H, (uint64_t)(d.Is / 32)};
+    const uint32_t sbg[3] = {64, 2, 1}, sbd[3] = {128, 2, 1};
+    bool good = encode_plain(&p->tm_wg, U8, 1, qw->gate, 3, dg, bg) &&
+                encode_plain(&p->tm_wu, U8, 1, qw->up, 3, dg, bg) &&
+                encode_plain(&p->tm_wd, U8, 1, qw->down, 3, dd, bd) &&
+                encode_plain(&p->tm_sg, U8, 1, qw->shared_gate, 2, dsg, bg) &&
+                encode_plain(&p->tm_su, U8, 1, qw->shared_up, 2, dsg, bg) &&
+                encode_plain(&p->tm_sd, U8, 1, qw->shared_down, 2, dsd, bd) &&
+                encode_plain(&p->tm_cg, B16, 2, qw->gate_scale, 3, cg, sbg) &&
+                encode_plain(&p->tm_cu, B16, 2, qw->up_scale, 3, cg, sbg) &&
+                encode_plain(&p->tm_cd, B16, 2, qw->down_scale, 3, cd, sbd) &&
+                encode_plain(&p->tm_csg, B16, 2, qw->shared_gate_scale, 2, csg, sbg) &&
+                encode_plain(&p->tm_csu, B16, 2, qw->shared_up_scale, 2, csg, sbg) &&
+                encode_plain(&p->tm_csd, B16, 2, qw->shared_down_scale, 2, csd, sbd);
+    p->tc_route = d.E <= 256 && d.E % 16 == 0 && d.k <= 16 && d.H <= 8192;
+    if (good && p->tc_route)
+        good = encode_bf16(&p->tm_wr, w_router, d.H, d.E, 0,
+                           (uint32_t)((d.E > 128 && d.E % 32 == 0) ? d.E / 2 : d.E),
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    if (!good) {
+        delete p;
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for a quantised weight tensor");
     }
     *out = p;
     return ok();

@@ -60,7 +60,7 @@ namespace moe {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far beyond any legal wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s when draining after an abort
 
-template <int MODE, int NMAX, int STAGES>
+template <int MODE, int NMAX, int STAGES, int QB = 0>
 struct GemmCfg {
     // gate/up (streaming shape only; many rows per expert run on CTA pairs,
     // gemm_pair.cu): 64 gate + 64 up rows in one 128-row A tile, g and u
@@ -76,10 +76,22 @@ struct GemmCfg {
     // lo part as further K steps at the full tile width instead
     static constexpr bool kDualLo = MODE == kDown && NMAX == kSmallN;
     static constexpr int kBBytes = (kDualLo ? 2 : 1) * NMAX * 128;
-    static constexpr int kThreads = 192;
+    // quantised weights (QB = 8 or 4 bits, streaming shape only): a stage holds
+    // the B tile, the 128 weight rows' raw codes for its 64 K and their scales
+    // (two blocks of 32 per row); converter warps dequantise the codes into one
+    // of kNA bf16 A slots, which the MMA reads
+    static constexpr bool kQuant = QB != 0;
+    static_assert(QB == 0 || ((QB == 8 || QB == 4) && NMAX == kSmallN), "quantised: streaming shape");
+    static constexpr int kRawBytes = QB == 8 ? 128 * 64 : (QB == 4 ? 128 * 32 : 0);
+    static constexpr int kScaleBytes = kQuant ? 2 * 128 * 2 : 0;
+    static constexpr int kNA = kQuant ? 2 : 0;
+    static constexpr int kScaleRows = MODE == kGateUp ? 64 : 128;   // rows per scale box
+    static constexpr int kThreads = kQuant ? 320 : 192;
     static constexpr int kMinBlocks = 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kXchgOff = STAGES * kStageBytes;
+    static constexpr int kStageBytes =
+        kQuant ? (kBBytes + kRawBytes + kScaleBytes + 1023) / 1024 * 1024 : kABytes + kBBytes;
+    static constexpr int kAOff = STAGES * kStageBytes;                 // quantised: the A slots
+    static constexpr int kXchgOff = kAOff + kNA * kABytes;
     // gate/up: g <-> u exchange; down: the unit's fp16 output tile
     static constexpr int kXchgBytes = MODE == kGateUp ? 2 * 64 * 9 * 4 : NMAX * 128 * 2;
     static constexpr int kRowsOff = kXchgOff + kXchgBytes;             // gate/up: rows of x of a unit
@@ -89,7 +101,7 @@ struct GemmCfg {
     static constexpr int kAccCols = NMAX;   // TMEM columns per accumulator
     static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
-    static_assert(8 * (2 * STAGES + 7) + 16 <= 512, "barrier region");
+    static_assert(8 * (2 * STAGES + 2 * kNA + 7) + 16 <= 512, "barrier region");
     static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
     static_assert(NMAX % 16 == 0 && NMAX <= 256 && NMAX % (NMAX >= 64 ? 64 : 16) == 0, "MMA N extent");
 };
@@ -107,14 +119,71 @@ __device__ __forceinline__ void store_h(__nv_bfloat16* out, bool shared, int ld,
     }
 }
 
-template <int MODE, int NMAX, int STAGES>
-__global__ void __launch_bounds__(GemmCfg<MODE, NMAX, STAGES>::kThreads,
-                                  GemmCfg<MODE, NMAX, STAGES>::kMinBlocks)
+// Weights bf16(q * d) of a pair of codes (the product is exact in fp32: at
+// most 7 + 8 significant bits; one rounding, to nearest even).
+__device__ __forceinline__ uint32_t dq_pair(int q0, int q1, float d) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn((float)q0 * d, (float)q1 * d);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Dequantise one stage: 128 weight rows x 64 K of codes (row r at raw + r * 64
+// bytes for 8 bits, r * 32 for 4) with their scales (bf16, boxes of SR rows x
+// two blocks of 32 along K, block-major within a box) into a bf16 tile of 128
+// rows of 128 bytes in the 128-byte swizzle (16-byte chunk j of row r at chunk
+// j ^ (r & 7)), the layout the MMA's descriptor expects.  The 128 converter
+// threads take (row, 16-byte chunk of codes) items, consecutive threads
+// consecutive chunks, so a warp reads 512 contiguous bytes.
+template <int QB, int SR>
+__device__ __forceinline__ void dequant_tile(const uint8_t* raw, const __nv_bfloat16* sc, uint8_t* A,
+                                             int ct) {
+    constexpr int kChunks = QB == 8 ? 4 : 2;   // 16-byte chunks of codes per row
+#pragma unroll
+    for (int it = ct; it < 128 * kChunks; it += 128) {
+        const int r = it / kChunks, c = it % kChunks;
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + r * (16 * kChunks) + c * 16);
+        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+        uint8_t* row = A + r * 128;
+        if (QB == 8) {
+            // 16 codes = K elements 16c .. 16c + 15, all in block c / 2
+            const float d = __bfloat162float(sc[((r / SR) * 2 + (c >> 1)) * SR + (r % SR)]);
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t x = wd[i >> 1];
+                const int sh = (i & 1) * 16;
+                o[i] = dq_pair((int)((int32_t)(x << (24 - sh)) >> 24),
+                               (int)((int32_t)(x << (16 - sh)) >> 24), d);
+            }
+            *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        } else {
+            // 32 codes (two per byte, even element low) = K elements 32c .. 32c + 31: block c
+            const float d = __bfloat162float(sc[((r / SR) * 2 + c) * SR + (r % SR)]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {   // 16-byte output chunk 4c + j: elements 8j .. 8j + 7
+                const uint32_t x = wd[j];
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = dq_pair((int)((int32_t)(x << (28 - 8 * i)) >> 28),
+                                   (int)((int32_t)(x << (24 - 8 * i)) >> 28), d);
+                *reinterpret_cast<uint4*>(row + (((4 * c + j) ^ (r & 7)) << 4)) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+}
+
+template <int MODE, int NMAX, int STAGES, int QB>
+__global__ void __launch_bounds__(GemmCfg<MODE, NMAX, STAGES, QB>::kThreads,
+                                  GemmCfg<MODE, NMAX, STAGES, QB>::kMinBlocks)
 k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
        const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
-       const __grid_constant__ CUtensorMap tmBg, GemmArgs a) {
-    using C = GemmCfg<MODE, NMAX, STAGES>;
+       const __grid_constant__ CUtensorMap tmBg, const __grid_constant__ CUtensorMap tmS0,
+       const __grid_constant__ CUtensorMap tmS1, const __grid_constant__ CUtensorMap tmS2,
+       const __grid_constant__ CUtensorMap tmS3, GemmArgs a) {
+    using C = GemmCfg<MODE, NMAX, STAGES, QB>;
     // gate/up units gather their rows of x (pair_row; shared_rows on a
     // live-row pass) with TMA gather4 (about 7 bytes per clock per SM: enough
     // for 32-row tiles, far too few for larger ones)
@@ -130,7 +199,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     uint64_t* tempty = tfull + 2;
     uint64_t* xbar = tempty + 2;  // [2] epilogue exchange (128 arrivals each)
     uint64_t* dbar = xbar + 2;    // MMA drain: every MMA issued has completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dbar + 1);
+    uint64_t* conv = dbar + 1;    // [kNA] A slot dequantised (quantised weights)
+    uint64_t* aempty = conv + C::kNA;   // [kNA] A slot free
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aempty + C::kNA);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;
 
@@ -143,6 +214,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             mbar_init(xbar + i, 128);
         }
         mbar_init(dbar, 1);
+        for (int i = 0; i < C::kNA; ++i) {
+            mbar_init(conv + i, 128);   // the converter threads
+            mbar_init(aempty + i, 1);
+        }
         *abort_flag = 0;
         *never = 0;
         fence_mbar_init();
@@ -155,6 +230,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmA0); prefetch_tmap(&tmA1); prefetch_tmap(&tmA2);
         prefetch_tmap(&tmA3); prefetch_tmap(&tmB1);
+        if (C::kQuant) {
+            prefetch_tmap(&tmS0); prefetch_tmap(&tmS1); prefetch_tmap(&tmS2); prefetch_tmap(&tmS3);
+        }
         if (kGather) prefetch_tmap(&tmBg);
         if (MODE == kDown) prefetch_tmap(&tmB0);  // h
     }
@@ -231,7 +309,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const uint32_t bbytes = gathered ? (uint32_t)nb4 * 512u
                                              : (uint32_t)(nbox * C::kBoxRows * 128);
             const int parts = C::kDualLo && g == a.E ? 2 : 1;
-            const uint32_t bytes = (uint32_t)C::kABytes + parts * bbytes;
+            const uint32_t abytes = C::kQuant ? (uint32_t)(C::kRawBytes + C::kScaleBytes)
+                                              : (uint32_t)C::kABytes;
+            const uint32_t bytes = abytes + parts * bbytes;
             if (gathered) {
                 // the unit's rows of x, padded to a multiple of 4 with R (read as zeros);
                 // copies of the previous unit took their coordinates when issued
@@ -249,11 +329,42 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     break;
                 }
                 const uint32_t sA = sbase + stage * C::kStageBytes;
-                const uint32_t sB = sA + C::kABytes;
+                // quantised: [B | raw codes | scales]; bf16: [A | B]
+                const uint32_t sB = C::kQuant ? sA : sA + C::kABytes;
                 const int kc = kb * 64;
                 if (lane == 0) {
                     mbar_expect_tx(full + stage, bytes);
-                    if (MODE == kGateUp) {
+                    if (C::kQuant) {
+                        // raw codes: K bytes kc (8 bits) or kc / 2 (4 bits); scales:
+                        // blocks kc / 32 and kc / 32 + 1 of the rows (block-major)
+                        const uint32_t sR = sA + C::kBBytes, sS = sR + C::kRawBytes;
+                        const int kq = QB == 8 ? kc : kc / 2;
+                        if (MODE == kGateUp) {
+                            const int rows = m * C::kGURows;
+                            const uint32_t half = 64 * (QB == 8 ? 64 : 32);
+                            if (g == a.E) {
+                                tma_load_2d(sR, &tmA2, kq, rows, full + stage);
+                                tma_load_2d(sR + half, &tmA3, kq, rows, full + stage);
+                                tma_load_2d(sS, &tmS2, rows, kc / 32, full + stage);
+                                tma_load_2d(sS + 256, &tmS3, rows, kc / 32, full + stage);
+                            } else {
+                                tma_load_3d(sR, &tmA0, kq, rows, g, full + stage);
+                                tma_load_3d(sR + half, &tmA1, kq, rows, g, full + stage);
+                                tma_load_3d(sS, &tmS0, rows, kc / 32, g, full + stage);
+                                tma_load_3d(sS + 256, &tmS1, rows, kc / 32, g, full + stage);
+                            }
+                        } else {
+                            const int Kc = g == a.E ? a.Is : a.I;
+                            const int kca = kc % Kc, kqa = QB == 8 ? kca : kca / 2;
+                            if (g == a.E) {
+                                tma_load_2d(sR, &tmA2, kqa, m * 128, full + stage);
+                                tma_load_2d(sS, &tmS2, m * 128, kca / 32, full + stage);
+                            } else {
+                                tma_load_3d(sR, &tmA0, kqa, m * 128, g, full + stage);
+                                tma_load_3d(sS, &tmS0, m * 128, kca / 32, g, full + stage);
+                            }
+                        }
+                    } else if (MODE == kGateUp) {
                         // 64-row boxes: gate rows, then up rows (rows past I read as zeros)
                         constexpr int kHalf = C::kGURows / 64;  // boxes per weight
                         const int rows = m * C::kGURows;
@@ -308,8 +419,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------ MMA issuer
-            int stage = 0, acc = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            int stage = 0, acc = 0, aslot = 0;
+            uint32_t phase = 0, acc_phase = 0, aphase = 0;
             bool ok = true;
             for (int u = ufirst; ok && u < nunits; u += nact) {
                 const int4 un = __ldg(a.units + u);
@@ -325,14 +436,18 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * C::kAccCols);
                 for (int kb = 0; kb < (K >> 6); ++kb) {
-                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs)) {
+                    // quantised: the converter's A slot (it waited for the stage's
+                    // copies, the B tile included); bf16: the stage itself
+                    if (!mbar_wait_bounded(C::kQuant ? conv + aslot : full + stage,
+                                           C::kQuant ? aphase : phase, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sA = sbase + stage * C::kStageBytes;
-                    const uint32_t sB = sA + C::kABytes;
+                    const uint32_t sSt = sbase + stage * C::kStageBytes;
+                    const uint32_t sA = C::kQuant ? sbase + C::kAOff + aslot * C::kABytes : sSt;
+                    const uint32_t sB = C::kQuant ? sSt : sSt + C::kABytes;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = smem_desc_sw128(sA + kk * 32);
@@ -343,6 +458,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                     tc_commit(empty + stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (C::kQuant) {
+                        tc_commit(aempty + aslot);
+                        if (++aslot == C::kNA) { aslot = 0; aphase ^= 1u; }
+                    }
                 }
                 if (!ok) break;
                 tc_commit(tfull + acc);
@@ -352,6 +471,36 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             // drain: arrives once every MMA issued above has completed
             tc_commit(dbar);
             if (!mbar_wait_bounded(dbar, 0, never, kDrainLimitNs)) give_up();
+        }
+    } else if (C::kQuant && warp >= 6) {
+        // ---------------------------------------------------------- converter
+        // Stage by stage, in the MMA's order: wait for the stage's copies and a
+        // free A slot, turn the 128 rows x 64 K codes into bf16 weights
+        // bf16(q * d) in the slot's 128-byte swizzled layout, fence them for
+        // the async proxy and hand the slot to the MMA.
+        const int ct = threadIdx.x - 192;   // 0..127
+        int stage = 0, aslot = 0;
+        uint32_t phase = 0, aphase = 0;
+        bool ok = true;
+        for (int u = ufirst; ok && u < nunits; u += nact) {
+            const int g = __ldg(a.units + u).x;
+            const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
+            for (int kb = 0; kb < (K >> 6); ++kb) {
+                if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs) ||
+                    !mbar_wait_bounded(aempty + aslot, aphase ^ 1u, abort_flag, kWaitNs)) {
+                    give_up();
+                    ok = false;
+                    break;
+                }
+                const uint8_t* raw = base + stage * C::kStageBytes + C::kBBytes;
+                const __nv_bfloat16* sc = reinterpret_cast<const __nv_bfloat16*>(raw + C::kRawBytes);
+                uint8_t* A = base + C::kAOff + aslot * C::kABytes;
+                dequant_tile<QB, C::kScaleRows>(raw, sc, A, ct);
+                fence_proxy_async_smem();
+                mbar_arrive(conv + aslot);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++aslot == C::kNA) { aslot = 0; aphase ^= 1u; }
+            }
         }
     } else {
         // ---------------------------------------------------------- epilogue
@@ -489,24 +638,26 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 
 // ---------------------------------------------------------------------------
 
-template <int MODE, int NMAX, int STAGES>
+template <int MODE, int NMAX, int STAGES, int QB = 0>
 static cudaError_t launch_one(const GemmMaps& mp, const GemmArgs& a, int grid, cudaStream_t st) {
-    using C = GemmCfg<MODE, NMAX, STAGES>;
-    return launch_kernel(k_gemm<MODE, NMAX, STAGES>, dim3(grid), dim3(C::kThreads), C::kSmem, st, mp.a0, mp.a1,
-                      mp.a2, mp.a3, mp.b0, mp.b1, mp.bg, a);
+    using C = GemmCfg<MODE, NMAX, STAGES, QB>;
+    return launch_kernel(k_gemm<MODE, NMAX, STAGES, QB>, dim3(grid), dim3(C::kThreads), C::kSmem, st,
+                         mp.a0, mp.a1, mp.a2, mp.a3, mp.b0, mp.b1, mp.bg, mp.s0, mp.s1, mp.s2, mp.s3,
+                         a);
 }
 
-template <int MODE, int NMAX, int STAGES>
+template <int MODE, int NMAX, int STAGES, int QB = 0>
 static cudaError_t set_attr() {
-    using C = GemmCfg<MODE, NMAX, STAGES>;
-    return cudaFuncSetAttribute(k_gemm<MODE, NMAX, STAGES>,
+    using C = GemmCfg<MODE, NMAX, STAGES, QB>;
+    return cudaFuncSetAttribute(k_gemm<MODE, NMAX, STAGES, QB>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
 }
 
 // (rows per unit, pipeline depth) of each kernel shape: small = few rows per
 // expert (weight streaming: two CTAs per SM, each with its own ring, keep more
 // TMA streams in flight); large = many rows (tensor-core bound, one CTA per SM;
-// the large gate/up GEMM is k_gateup_pair).
+// the large gate/up GEMM is k_gateup_pair).  Quantised weights stream with the
+// small shape at every row count.
 constexpr int kSmallStagesGU = 5, kSmallStagesDN = 4;
 constexpr int kLargeStagesDN = 3;
 constexpr int kSmallCtasPerSm = 2;
@@ -515,11 +666,23 @@ cudaError_t gemm_set_attributes() {
     cudaError_t e;
     if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU>()) != cudaSuccess) return e;
     if ((e = set_attr<kDown, kSmallN, kSmallStagesDN>()) != cudaSuccess) return e;
+    if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU, 8>()) != cudaSuccess) return e;
+    if ((e = set_attr<kDown, kSmallN, kSmallStagesDN, 8>()) != cudaSuccess) return e;
+    if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU, 4>()) != cudaSuccess) return e;
+    if ((e = set_attr<kDown, kSmallN, kSmallStagesDN, 4>()) != cudaSuccess) return e;
     return set_attr<kDown, kLargeNDown, kLargeStagesDN>();
 }
 
-cudaError_t launch_gemm(int mode, bool small, const GemmMaps& mp, const GemmArgs& a, int grid,
-                        cudaStream_t st) {
+cudaError_t launch_gemm(int mode, bool small, int qbits, const GemmMaps& mp, const GemmArgs& a,
+                        int grid, cudaStream_t st) {
+    if (qbits) {
+        grid *= kSmallCtasPerSm;
+        if (qbits == 8)
+            return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStagesGU, 8>(mp, a, grid, st)
+                                   : launch_one<kDown, kSmallN, kSmallStagesDN, 8>(mp, a, grid, st);
+        return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStagesGU, 4>(mp, a, grid, st)
+                               : launch_one<kDown, kSmallN, kSmallStagesDN, 4>(mp, a, grid, st);
+    }
     if (small) {
         grid *= kSmallCtasPerSm;
         return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStagesGU>(mp, a, grid, st)

@@ -110,6 +110,8 @@ struct GemmArgs {
 struct GemmMaps {
     CUtensorMap a0, a1, a2, a3, b0, b1;
     CUtensorMap bg;   // x with a one-row box: TMA gather4 of routed rows (small batches)
+    // quantised weights: a0..a3 are the codes, s0..s3 their scales (unused for bf16)
+    CUtensorMap s0, s1, s2, s3;
 };
 // The fused front end of a small call (front.cu): router, coreset and
 // forward bookkeeping in one launch.
@@ -131,8 +133,8 @@ cudaError_t launch_scatter(const ScatterArgs&, bool small, int num_sms, cudaStre
 cudaError_t launch_front(const FrontArgs&, int num_sms, cudaStream_t);
 cudaError_t launch_combine(const CombineArgs&, int num_sms, cudaStream_t);
 cudaError_t gemm_set_attributes();
-cudaError_t launch_gemm(int mode, bool small, const GemmMaps&, const GemmArgs&, int grid,
-                        cudaStream_t);
+cudaError_t launch_gemm(int mode, bool small, int qbits, const GemmMaps&, const GemmArgs&,
+                        int grid, cudaStream_t);
 // Gate/up of units of up to kLargeNGU rows on CTA pairs (gemm_pair.cu).
 cudaError_t gateup_pair_set_attributes(int num_sms);
 cudaError_t launch_gateup_pair(const GemmMaps&, const GemmArgs&, cudaStream_t);

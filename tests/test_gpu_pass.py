@@ -64,12 +64,10 @@ def run_pass(case: Case, tau=None, max_experts=0, probs=False, graph=False):
     else:
         call()
     torch.cuda.synchronize()
-    res = {k: (v.cpu().numpy().copy() if v is not None else None) for k, v in out.items()}
+    res = {k: v.cpu().numpy().copy() for k, v in out.items() if v is not None and k != "y"}
     res["keep"] = bits32(res["keep"]).copy()
-    res["y"] = out["y"].float().cpu().numpy().astype(np.float64)
+    res["y"] = out["y"].float().cpu().numpy().astype(np.float64)   # bf16 -> exact in fp64
     res["y32"] = res["y32"].astype(np.float64)
-    if res["p"] is None:
-        del res["p"]
     return res
 
 
