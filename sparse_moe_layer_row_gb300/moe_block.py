@@ -33,6 +33,15 @@ class moe_dims(ctypes.Structure):
                 ("max_blocks", ctypes.c_int32)]
 
 
+_QFIELDS = ("gate", "up", "down", "gate_scale", "up_scale", "down_scale", "shared_gate",
+            "shared_up", "shared_down", "shared_gate_scale", "shared_up_scale",
+            "shared_down_scale")
+
+
+class moe_quant_weights(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_int32)] + [(n, ctypes.c_void_p) for n in _QFIELDS]
+
+
 _lib = None
 
 
@@ -60,6 +69,9 @@ def load(build_if_missing: bool = False):
     L.moe_plan_create.restype = ctypes.c_int
     L.moe_plan_create.argtypes = [ctypes.POINTER(moe_dims), P, P, P, P, P, P, P,
                                   ctypes.POINTER(P)]
+    L.moe_plan_create_quantized.restype = ctypes.c_int
+    L.moe_plan_create_quantized.argtypes = [ctypes.POINTER(moe_dims), P,
+                                            ctypes.POINTER(moe_quant_weights), ctypes.POINTER(P)]
     L.moe_plan_destroy.restype = None
     L.moe_plan_destroy.argtypes = [P]
     L.moe_block_route.restype = ctypes.c_int
@@ -134,8 +146,46 @@ def moe_workspace_bytes(dims: moe_dims) -> int:
 class Plan:
     """moe_plan_create / moe_plan_destroy.  Keeps the weight tensors alive."""
 
+    @classmethod
+    def quantized(cls, dims: moe_dims, w_router, q):
+        """moe_plan_create_quantized: ``q`` holds ``bits`` (8 or 4) and the codes and
+        scales named as in moe_quant_weights (e.g. workloads.QuantExperts)."""
+        d = dims
+        bits = int(q.bits)
+        if bits not in (8, 4):
+            raise ValueError("bits must be 8 or 4")
+        kb = 1 if bits == 8 else 2
+        code = torch.int8 if bits == 8 else torch.uint8
+        _need(w_router, "w_router", torch.bfloat16, (d.E, d.H))
+        shapes = {"gate": (code, (d.E, d.I, d.H // kb)), "up": (code, (d.E, d.I, d.H // kb)),
+                  "down": (code, (d.E, d.H, d.I // kb)),
+                  "gate_scale": (torch.bfloat16, (d.E, d.H // 32, d.I)),
+                  "up_scale": (torch.bfloat16, (d.E, d.H // 32, d.I)),
+                  "down_scale": (torch.bfloat16, (d.E, d.I // 32, d.H)),
+                  "shared_gate": (code, (d.Is, d.H // kb)), "shared_up": (code, (d.Is, d.H // kb)),
+                  "shared_down": (code, (d.H, d.Is // kb)),
+                  "shared_gate_scale": (torch.bfloat16, (d.H // 32, d.Is)),
+                  "shared_up_scale": (torch.bfloat16, (d.H // 32, d.Is)),
+                  "shared_down_scale": (torch.bfloat16, (d.Is // 32, d.H))}
+        tensors = [getattr(q, n) for n in _QFIELDS]
+        for n, t in zip(_QFIELDS, tensors):
+            _need(t, n, *shapes[n])
+        self = cls.__new__(cls)
+        self.dims = d
+        self.weights = (w_router, *tensors)
+        self.device = w_router.device
+        self.bits = bits
+        qw = moe_quant_weights(bits, *[t.data_ptr() for t in tensors])
+        h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _check(load().moe_plan_create_quantized(ctypes.byref(d), _ptr(w_router),
+                                                    ctypes.byref(qw), ctypes.byref(h)))
+        self.handle = h
+        return self
+
     def __init__(self, dims: moe_dims, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down):
         d = dims
+        self.bits = 16
         _need(w_router, "w_router", torch.bfloat16, (d.E, d.H))
         _need(w_gate, "w_gate", torch.bfloat16, (d.E, d.I, d.H))
         _need(w_up, "w_up", torch.bfloat16, (d.E, d.I, d.H))
@@ -372,13 +422,31 @@ class MoeBlockLayer:
     """
 
     def __init__(self, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, k: int,
-                 max_rows: int, max_blocks: int):
+                 max_rows: int, max_blocks: int, plan=None):
         E, H = w_router.shape
         I = w_gate.shape[1]
         Is = ws_gate.shape[0]
         self.dims = moe_dims(H, E, k, I, Is, max_rows, max_blocks)
-        self.plan = Plan(self.dims, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down)
-        dev = w_router.device
+        self.plan = plan if plan is not None else Plan(self.dims, w_router, w_gate, w_up, w_down,
+                                                       ws_gate, ws_up, ws_down)
+        self._init_buffers(w_router.device)
+
+    @classmethod
+    def quantized(cls, w_router, q, k: int, max_rows: int, max_blocks: int):
+        """A layer whose experts are quantised (moe_plan_create_quantized; ``q`` as
+        for Plan.quantized, e.g. workloads.QuantExperts)."""
+        E, H = w_router.shape
+        I = q.gate_scale.shape[-1]
+        Is = q.shared_gate_scale.shape[-1]
+        self = cls.__new__(cls)
+        self.dims = moe_dims(H, E, k, I, Is, max_rows, max_blocks)
+        self.plan = Plan.quantized(self.dims, w_router, q)
+        self._init_buffers(w_router.device)
+        return self
+
+    def _init_buffers(self, dev):
+        E, H, k = self.dims.E, self.dims.H, self.dims.k
+        max_rows, max_blocks = self.dims.max_rows, self.dims.max_blocks
         self.workspace = self.plan.new_workspace()
         R, nb, words = max_rows, max_blocks, (E + 31) // 32
         self._topk_idx = torch.empty(R, k, dtype=torch.int32, device=dev)

@@ -36,8 +36,12 @@ class Case:
     """One workload on the GPU: inputs, a layer with its workspace, and GPU results."""
 
     def __init__(self, w: W.Workload, device="cuda", T: W.Tensors | None = None,
-                 block_offsets=None, bias=None, x=None):
+                 block_offsets=None, bias=None, x=None, quant: W.QuantExperts | None = None):
+        """``quant``: the experts quantised (workloads.quantize_experts of T); the GPU
+        layer reads those codes and the oracle's FFN runs on the oracle's own
+        dequantisation of them."""
         self.w = w
+        self.quant = quant
         self.dev = torch.device(device)
         self.T = T if T is not None else W.make_tensors(w, device=self.dev)
         self.x = self.T.x if x is None else x
@@ -46,9 +50,13 @@ class Case:
         self.bias = self.T.bias if bias is None else bias
         self.R = self.x.shape[0]
         self.nb = self.off.shape[0] - 1
-        self.layer = moe_block.MoeBlockLayer(
-            self.T.w_router, self.T.w_gate, self.T.w_up, self.T.w_down, self.T.ws_gate,
-            self.T.ws_up, self.T.ws_down, k=w.k, max_rows=max(self.R, 1), max_blocks=self.nb)
+        if quant is not None:
+            self.layer = moe_block.MoeBlockLayer.quantized(
+                self.T.w_router, quant, k=w.k, max_rows=max(self.R, 1), max_blocks=self.nb)
+        else:
+            self.layer = moe_block.MoeBlockLayer(
+                self.T.w_router, self.T.w_gate, self.T.w_up, self.T.w_down, self.T.ws_gate,
+                self.T.ws_up, self.T.ws_down, k=w.k, max_rows=max(self.R, 1), max_blocks=self.nb)
         moe_block.moe_clear_device_status(self.layer.workspace)
 
     def run(self, tau: float | None = None, max_experts: int = 0, probs: bool = False):
@@ -110,9 +118,19 @@ class Case:
                 e = int(r["idx"][row, j])
                 if mask[bor[row], e]:
                     used.add(e)
-        experts = {e: (u16(self.T.w_gate[e]), u16(self.T.w_up[e]), u16(self.T.w_down[e]))
-                   for e in sorted(used)}
-        shared = (u16(self.T.ws_gate), u16(self.T.ws_up), u16(self.T.ws_down))
+        if self.quant is not None:
+            Q, b = self.quant, self.quant.bits
+
+            def dq(codes, scale):
+                return oracle.dequant(codes.detach().cpu().numpy(), u16(scale), b)
+            experts = {e: (dq(Q.gate[e], Q.gate_scale[e]), dq(Q.up[e], Q.up_scale[e]),
+                           dq(Q.down[e], Q.down_scale[e])) for e in sorted(used)}
+            shared = (dq(Q.shared_gate, Q.shared_gate_scale), dq(Q.shared_up, Q.shared_up_scale),
+                      dq(Q.shared_down, Q.shared_down_scale))
+        else:
+            experts = {e: (u16(self.T.w_gate[e]), u16(self.T.w_up[e]), u16(self.T.w_down[e]))
+                       for e in sorted(used)}
+            shared = (u16(self.T.ws_gate), u16(self.T.ws_up), u16(self.T.ws_down))
         y = oracle.forward(u16(self.x), off, r["idx"], r["wr"], r["keep"], experts, shared,
                            self.w.E, rows=None if rows is None else list(rows),
                            nthreads=nthreads)
