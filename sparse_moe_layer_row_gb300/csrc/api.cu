@@ -229,7 +229,8 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
                 at<__nv_bfloat16>(workspace, L.hs),
                 at<int32_t>(workspace, L.pair_row), at<float>(workspace, L.pair_w),
                 at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
-                (int)(L.max_pairs + d.max_rows), (int)L.max_pairs, at<uint32_t>(workspace, L.status),
+                (int)(L.max_pairs + d.max_rows), at<int32_t>(workspace, L.misc) + 4,
+                (int)L.max_pairs, at<uint32_t>(workspace, L.status),
                 live ? at<int32_t>(workspace, L.shared_rows) : nullptr, p->wait_ns};
     auto mark = [&](int i) { return mark_event(p, i, st); };
     cudaError_t e = marked ? cudaSuccess : mark(0);
@@ -250,7 +251,8 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
     if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, su, p->qbits, dn, gd, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
     CombineArgs ca{at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
-                   (int)(L.max_pairs + d.max_rows), at<int32_t>(workspace, L.inv), R, d.H, d.k,
+                   (int)(L.max_pairs + d.max_rows), at<int32_t>(workspace, L.misc) + 4,
+                   at<int32_t>(workspace, L.inv), R, d.H, d.k,
                    (int)L.max_pairs, static_cast<__nv_bfloat16*>(y), y_f32,
                    at<uint32_t>(workspace, L.status), live, at<int32_t>(workspace, L.shared_inv)};
     if ((e = mark(3)) == cudaSuccess) e = launch_combine(ca, p->num_sms, st);

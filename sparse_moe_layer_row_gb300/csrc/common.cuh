@@ -26,7 +26,8 @@ struct Layout {
     size_t hist;         // int32 [max_blocks, E]     pairs per (block, expert) / bases
     size_t count;        // int32 [E]                 surviving pairs per expert
     size_t expert_off;   // int32 [E + 1]
-    size_t misc;         // int32[16]: [0] ticket, [1] units gate/up, [2] units down, [3] pairs
+    size_t misc;         // int32[16]: [0] ticket, [1] units gate/up, [2] units down, [3] pairs,
+                         // [4] set when a staged output quarter needed an exponent
     size_t units_gu;     // int4 [max_units_gu]
     size_t units_dn;     // int4 [max_units_dn]
     size_t pair_row;     // int32 [max_pairs]

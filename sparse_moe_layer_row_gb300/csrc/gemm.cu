@@ -563,20 +563,21 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     xphase ^= 1u;
                 }
             } else {
-                // Weighted fp16 outputs of the unit's pairs.  Each warp owns 32
-                // hidden columns (its TMEM lane quadrant) of every pair: it
-                // stages them in shared memory ([pair][128 hidden]) and copies
-                // them out itself, 64 bytes per pair, so the warps need no
-                // barrier between them.  fp16 holds |v| < 65504: a 32-column
-                // quarter of a pair row with a value of 2^15 or more (or a
-                // non-finite one) is stored as v * 2^-s with the smallest s
-                // that brings its largest magnitude below 2^15, and s goes to
-                // ysx; k_combine multiplies it back exactly.  Values below 2^15
-                // are stored as they are (s = 0).
+                // Weighted fp16 outputs of the unit's pairs, staged in shared
+                // memory ([pair][128 hidden]) so each pair's 128 columns leave as
+                // one 256-byte segment; the accumulator is released before the
+                // copy-out.  fp16 holds |v| < 65504: each warp owns a 32-column
+                // quarter (its TMEM lane quadrant) of every pair, and a quarter
+                // with a value of 2^15 or more (or a non-finite one) is stored as
+                // v * 2^-s with the smallest s that brings its largest magnitude
+                // below 2^15; s goes to ysx and the call's `scaled` flag is set;
+                // k_combine multiplies it back exactly.  Values below 2^15 are
+                // stored as they are (s = 0).
                 __half* xs = reinterpret_cast<__half*>(base + C::kXchgOff);
                 const int hl = q * 32 + lane;
                 const size_t row0 = (size_t)(g == a.E ? a.shared_row0 : 0) + start;
                 uint8_t* xq = a.ysx + (size_t)(m * 4 + q) * a.ld_x + row0;  // this quarter's exponents
+                bool any_big = false;
                 for (int c = 0; c < n16; c += 16) {
                     // the chunk's pair weights first (not reordered across stores)
                     float wv[16];
@@ -590,10 +591,11 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         v[t] = wv[t] * v[t];
-                        big |= !(fabsf(v[t]) < 32768.0f);
+                        big |= !(fabsf(v[t]) < 32768.0f) && c + t < n;
                     }
                     uint32_t my_s = 0;  // lane t: the exponent of pair c + t
                     if (__any_sync(0xffffffffu, big)) {
+                        any_big = true;
 #pragma unroll
                         for (int t = 0; t < 16; ++t) {
                             const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[t])));
@@ -607,17 +609,30 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     for (int t = 0; t < 16; ++t) xs[(c + t) * 128 + hl] = __float2half_rn(v[t]);
                     if (lane < 16 && c + lane < n) xq[c + lane] = (uint8_t)my_s;
                 }
+                if (any_big && lane == 0) *a.scaled = 1;
                 tc_fence_before();
                 mbar_arrive(tempty + acc);
                 released = true;
-                __syncwarp();
-                // n rows x 4 segments of 16 B of this warp's columns
-                for (int idx = lane; idx < n * 4; idx += 32) {
-                    const int t = idx >> 2, seg = idx & 3;
-                    const uint4 val = *reinterpret_cast<const uint4*>(xs + t * 128 + q * 32 + seg * 8);
-                    *reinterpret_cast<uint4*>(a.ys + (row0 + t) * a.H + m * 128 + q * 32 + seg * 8) = val;
+                mbar_arrive(xbar);
+                if (__any_sync(0xffffffffu, !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitNs))) {
+                    give_up();
+                    alive = false;
+                    break;
                 }
-                __syncwarp();  // the warp's columns of the tile are rewritten by the next unit
+                const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue warps
+                for (int idx = et; idx < n * 16; idx += 128) {  // n rows x 16 segments of 16 B
+                    const int t = idx >> 4, seg = idx & 15;
+                    const uint4 val = *reinterpret_cast<const uint4*>(xs + t * 128 + seg * 8);
+                    *reinterpret_cast<uint4*>(a.ys + (row0 + t) * a.H + m * 128 + seg * 8) = val;
+                }
+                mbar_arrive(xbar + 1);  // the tile is rewritten by the next unit
+                if (__any_sync(0xffffffffu,
+                               !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitNs))) {
+                    give_up();
+                    alive = false;
+                    break;
+                }
+                xphase ^= 1u;
             }
             if (!alive) break;
             if (!released) {

@@ -81,6 +81,7 @@ struct CombineArgs {
     const __half* ys;     // [max_pairs + max_rows, H] staged per-pair / shared outputs
     const uint8_t* ysx;   // [H / 32, max_pairs + max_rows] exponent of each staged quarter row
     int ld_x;             // max_pairs + max_rows (the staging rows)
+    const int32_t* scaled;   // nonzero: some exponent is not 0 (else ysx need not be read)
     const int32_t* inv;   // [R * k]
     int R, H, k, shared_row0;
     __nv_bfloat16* y;
@@ -102,6 +103,7 @@ struct GemmArgs {
     __half* ys;           // [max_pairs + max_rows, H] staged outputs (down GEMM)
     uint8_t* ysx;         // [H / 32, max_pairs + max_rows] their quarter-row exponents
     int ld_x;             // max_pairs + max_rows
+    int32_t* scaled;      // set to 1 when some exponent is not 0 (zeroed by the scatter)
     int shared_row0;      // staging row of the shared expert's row 0
     uint32_t* status;
     const int32_t* shared_rows;  // row of x of the shared expert's i-th row (NULL: i)

@@ -46,7 +46,10 @@ __global__ void __launch_bounds__(kScatThreads) k_scatter_hist(ScatterArgs a) {
     if (!(0 <= r0 && r0 <= r1 && r1 <= a.R)) r1 = r0 = 0;  // counted by the coreset call
     for (int e = tid; e < E; e += blockDim.x) s_run[e] = 0;
     if (tid == 0) { s_dup = 0; s_live = 0; }
-    if (b == 0 && tid == 0) a.misc[0] = 0;  // ticket of k_scatter_scan (next launch)
+    if (b == 0 && tid == 0) {
+        a.misc[0] = 0;  // ticket of k_scatter_scan (next launch)
+        a.misc[4] = 0;  // no staged output scaled yet (the down GEMM sets it)
+    }
     for (int c0 = r0; c0 < r1; c0 += kHistRows) {
         const int nr = min(kHistRows, r1 - c0);
         __syncthreads();
@@ -269,9 +272,10 @@ __global__ void __launch_bounds__(kSmallThreads) k_scatter_small(ScatterArgs a) 
 // down GEMM met a magnitude of 2^15 or more there); the product by 2^s is exact.
 __device__ __forceinline__ float pow2_u8(uint32_t s) { return __uint_as_float((127u + s) << 23); }
 
-__global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
-    pdl_wait();  // see common.cuh: nothing global is touched before
-    pdl_trigger();
+// The combine of one call; kScaled: some staged quarter carries an exponent
+// (the down GEMM's flag), so each contribution's exponent is read too.
+template <bool kScaled>
+__device__ __forceinline__ void combine_rows(const CombineArgs& a) {
     const int lane = threadIdx.x & 31;
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -288,13 +292,13 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
         {
             const size_t sr = (size_t)(a.shared_row0 + srow);
             const uint4 v = *reinterpret_cast<const uint4*>(a.ys + sr * a.H + c);
-            const float sc = pow2_u8(xq[sr]);
+            const float sc = kScaled ? pow2_u8(xq[sr]) : 1.0f;
             const __half2* hv = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float2 f = __half22float2(hv[i]);
-                acc[2 * i] = f.x * sc;
-                acc[2 * i + 1] = f.y * sc;
+                acc[2 * i] = kScaled ? f.x * sc : f.x;
+                acc[2 * i + 1] = kScaled ? f.y * sc : f.y;
             }
         }
         for (int j0 = 0; j0 < a.k; j0 += 8) {
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
                 const bool on = j0 + j < a.k && p >= 0;
                 v[j] = on ? *reinterpret_cast<const uint4*>(a.ys + (size_t)p * a.H + c)
                           : make_uint4(0, 0, 0, 0);
-                sx[j] = on ? xq[p] : 0u;
+                sx[j] = kScaled && on ? xq[p] : 0u;
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -317,8 +321,8 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 f = __half22float2(hv[i]);
-                    acc[2 * i] += f.x * sc;
-                    acc[2 * i + 1] += f.y * sc;
+                    acc[2 * i] += kScaled ? f.x * sc : f.x;
+                    acc[2 * i + 1] += kScaled ? f.y * sc : f.y;
                 }
             }
         }
@@ -339,6 +343,13 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
         if (__any_sync(0xffffffffu, !finite) && lane == 0)
             status_add(a.status, MOE_STATUS_NONFINITE_OUTPUT, 1);
     }
+}
+
+__global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
+    pdl_wait();  // see common.cuh: nothing global is touched before
+    pdl_trigger();
+    if (*a.scaled) combine_rows<true>(a);
+    else combine_rows<false>(a);
 }
 
 cudaError_t launch_scatter(const ScatterArgs& a, bool small, int num_sms, cudaStream_t st) {

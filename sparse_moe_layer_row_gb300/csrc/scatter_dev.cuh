@@ -178,6 +178,7 @@ __device__ __forceinline__ void scatter_small(const ScatterArgs& a, ScatterSmall
         a.misc[1] = base_gu + tot_ch * mt_gu;
         a.misc[2] = base_dn + tot_ch * mt_dn;
         a.misc[3] = tot_pairs;
+        a.misc[4] = 0;  // no staged output scaled yet (the down GEMM sets it)
         status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)s_dup);
     }
 }
