@@ -43,8 +43,8 @@ TENSOR_BOUND_ROWS = 4096  # from here on the roofline of the gate/up GEMM is its
 
 def kernels_per_step(w: W.Workload) -> int:
     """This library's kernels in one step (one moe_block_pass) of the workload."""
-    if w.R <= 32:  # small path: fused front end (router + coreset + scatter), gate/up, down, combine
-        return 4
+    if w.R <= 32:  # small path: router, coreset, one-CTA scatter, gate/up, down, combine
+        return 6
     tc_route = w.R >= 256 and w.E <= 256 and w.E % 16 == 0 and w.k <= 16 and w.H <= 8192
     route = 3 if tc_route else 1  # norms + tensor-core screen + exact; or the SIMT router
     return route + 1 + 3 + 3      # coreset; hist, scan, place; gate/up, down, combine
@@ -380,7 +380,7 @@ def measure(w: W.Workload, T, layer, steps: int, tm: StepTimer, clock_index: int
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     barrier(ws)
     total_ms = reduce_max(sum(step_ms), ws, dev)
-    # front: router + coreset + scatter (one fused kernel up to 32 rows)
+    # front: router + coreset + scatter (the kernels before the gate/up GEMM)
     kern = {"front": [], "gate_up": [], "down": [], "combine": []}
     with torch.cuda.stream(stream):
         for i in range(min(steps, 100)):

@@ -253,12 +253,11 @@ moe_status moe_block_forward(const moe_plan* plan, const void* x, int32_t R,
  * Does what moe_block_route_probs, moe_block_coreset_mass and
  * moe_block_forward do in sequence, with the same arguments, outputs and
  * errors (topk_p NULL: the weight mass; non-NULL: the probability mass, and
- * topk_p is written), bit for bit the same results.  For R <= 32 the router,
- * the coreset and the forward's bookkeeping run as one kernel (the last CTA
- * of the router grid carries on with the top-k, the coreset and the pair
- * lists), so a pass is four launches; larger calls run the three calls'
- * kernels.  All outputs (topk_idx, topk_w, topk_p, keep, core_size, w_renorm,
- * n_empty, y, y_f32) are written as by those calls. */
+ * topk_p is written), bit for bit the same results, with one validation and
+ * the kernels enqueued back to back (programmatic dependent launch between
+ * them, no host synchronisation).  All outputs (topk_idx, topk_w, topk_p,
+ * keep, core_size, w_renorm, n_empty, y, y_f32) are written as by those
+ * calls. */
 moe_status moe_block_pass(const moe_plan* plan, const void* x, int32_t R,
                           const int32_t* block_offsets, int32_t nb, const float* logit_bias,
                           float tau, int32_t max_experts, int32_t* topk_idx, float* topk_w,
@@ -322,8 +321,7 @@ typedef struct CUevent_st* moe_event_t;
 
 /* Optional per-kernel timing of moe_block_forward and moe_block_pass.  With
  * n_events == 5 the call records, on its stream, events[0] before the pair
- * scatter (moe_block_pass: before the fused front end, or before the router
- * for calls of more than 32 rows), events[1] before the gate/up GEMM,
+ * scatter (moe_block_pass: before the router), events[1] before the gate/up GEMM,
  * events[2] before the down GEMM, events[3] before the final bf16 store and
  * events[4] after it.  The events
  * belong to the caller and must outlive every forward that records them;

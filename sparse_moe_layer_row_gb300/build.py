@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmoeblock.so")
-SOURCES = ["api.cu", "router.cu", "router_tc.cu", "coreset.cu", "scatter.cu", "front.cu",
+SOURCES = ["api.cu", "router.cu", "router_tc.cu", "coreset.cu", "scatter.cu",
            "gemm.cu", "gemm_pair.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.cuh", "route_common.cuh", "coreset_dev.cuh", "scatter_dev.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

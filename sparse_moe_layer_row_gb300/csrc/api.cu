@@ -177,15 +177,14 @@ cudaError_t mark_event(const moe_plan* p, int i, cudaStream_t st) {
         cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
 }
 
-// The forward's launches after validation: the scatter (or, with `front`,
-// the fused front end that does the routing and coreset too), the two grouped
-// GEMMs and the combine.  `marked`: event 0 of the plan's forward events was
-// already recorded by the caller.
+// The forward's launches after validation: the scatter, the two grouped GEMMs
+// and the combine.  `marked`: event 0 of the plan's forward events was already
+// recorded by the caller.
 moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
                            const int32_t* block_offsets, int32_t nb, const int32_t* topk_idx,
                            const float* w_renorm, const uint32_t* keep, const uint8_t* live,
                            void* y, float* y_f32, void* workspace, cudaStream_t st,
-                           const FrontArgs* front, bool marked) {
+                           bool marked) {
     const moe_dims& d = p->d;
     const Layout L = make_layout(d);
     const bool small = R <= kSmallRows;
@@ -234,15 +233,8 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
                 live ? at<int32_t>(workspace, L.shared_rows) : nullptr, p->wait_ns};
     auto mark = [&](int i) { return mark_event(p, i, st); };
     cudaError_t e = marked ? cudaSuccess : mark(0);
-    if (front) {
-        FrontArgs fa = *front;
-        fa.s = sa;
-        if (e == cudaSuccess) e = launch_front(fa, p->num_sms, st);
-        if (e != cudaSuccess) return cuda_fail(e, "front-end launch");
-    } else {
-        if (e == cudaSuccess) e = launch_scatter(sa, small, p->num_sms, st);
-        if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
-    }
+    if (e == cudaSuccess) e = launch_scatter(sa, small, p->num_sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "scatter launch");
     if ((e = mark(1)) == cudaSuccess) e = launch_gemm(kGateUp, su, p->qbits, gu, ga, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
     GemmArgs gd = ga;
@@ -510,7 +502,7 @@ moe_status moe_block_forward_live(const moe_plan* p, const void* x, int32_t R,
         return fail(MOE_ERR_INVALID_ARG, "topk_idx/w_renorm/keep NULL or misaligned");
     if (R == 0) return ok();
     return enqueue_forward(p, x, R, block_offsets, nb, topk_idx, w_renorm, keep, live, y, y_f32,
-                           workspace, reinterpret_cast<cudaStream_t>(stream), nullptr, false);
+                           workspace, reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 moe_status moe_block_pass(const moe_plan* p, const void* x, int32_t R, const int32_t* block_offsets,
@@ -534,24 +526,8 @@ moe_status moe_block_pass(const moe_plan* p, const void* x, int32_t R, const int
     if (R == 0) return ok();
     const moe_dims& d = p->d;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (R <= kSmallRows) {
-        // one launch for the router, the coreset and the bookkeeping (front.cu)
-        const Layout L = make_layout(d);
-        uint32_t* ticket = at<uint32_t>(workspace, L.route_cnt);
-        cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(uint32_t), st);
-        if (e != cudaSuccess) return cuda_fail(e, "front-end ticket");
-        uint32_t* status = at<uint32_t>(workspace, L.status);
-        FrontArgs fa{};
-        fa.r = RouteArgs{static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(p->wr),
-                         logit_bias, block_offsets, R, d.H, d.E, d.k, nb,
-                         at<float>(workspace, L.logits), ticket, topk_idx, topk_w, status, topk_p};
-        fa.c = CoresetArgs{block_offsets, topk_idx, topk_w, topk_p, R, d.E, d.k, nb, tau,
-                           max_experts, keep, core_size, w_renorm, n_empty, status};
-        fa.ticket = ticket;
-        return enqueue_forward(p, x, R, block_offsets, nb, topk_idx, w_renorm, keep, nullptr, y,
-                               y_f32, workspace, st, &fa, false);
-    }
-    // larger calls: the router, coreset and forward kernels of the three calls
+    // the router, coreset and forward kernels of the three calls, back to back with
+    // programmatic dependent launch between them (no host synchronisation)
     cudaError_t e = mark_event(p, 0, st);
     if (e != cudaSuccess) return cuda_fail(e, "event record");
     s = moe_block_route_probs(p, x, R, block_offsets, nb, logit_bias, topk_idx, topk_w, topk_p,
@@ -561,7 +537,7 @@ moe_status moe_block_pass(const moe_plan* p, const void* x, int32_t R, const int
                                keep, core_size, w_renorm, n_empty, workspace, workspace_bytes, stream);
     if (s != MOE_OK) return s;
     return enqueue_forward(p, x, R, block_offsets, nb, topk_idx, w_renorm, keep, nullptr, y, y_f32,
-                           workspace, st, nullptr, true);
+                           workspace, st, true);
 }
 
 moe_status moe_plan_set_forward_events(moe_plan* p, moe_event_t const* events,

@@ -115,14 +115,6 @@ struct GemmMaps {
     // quantised weights: a0..a3 are the codes, s0..s3 their scales (unused for bf16)
     CUtensorMap s0, s1, s2, s3;
 };
-// The fused front end of a small call (front.cu): router, coreset and
-// forward bookkeeping in one launch.
-struct FrontArgs {
-    RouteArgs r;
-    CoresetArgs c;
-    ScatterArgs s;
-    uint32_t* ticket;     // CTA ticket, zero at launch
-};
 // Small batches (R <= kSmallRows): one-CTA bookkeeping and gathered x rows.
 constexpr int kSmallRows = 32;
 constexpr int kMaxExperts = 1024;
@@ -132,7 +124,6 @@ cudaError_t launch_route_tc(const RouteTcArgs&, const CUtensorMap& tm_x, const C
                             int num_sms, cudaStream_t);
 cudaError_t launch_coreset(const CoresetArgs&, cudaStream_t);
 cudaError_t launch_scatter(const ScatterArgs&, bool small, int num_sms, cudaStream_t);
-cudaError_t launch_front(const FrontArgs&, int num_sms, cudaStream_t);
 cudaError_t launch_combine(const CombineArgs&, int num_sms, cudaStream_t);
 cudaError_t gemm_set_attributes();
 cudaError_t launch_gemm(int mode, bool small, int qbits, const GemmMaps&, const GemmArgs&,

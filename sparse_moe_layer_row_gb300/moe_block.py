@@ -357,7 +357,7 @@ def moe_block_forward(plan: Plan, x, block_offsets, topk_idx, w_renorm, keep, y,
 def moe_block_pass(plan: Plan, x, block_offsets, logit_bias, tau: float, max_experts: int,
                    topk_idx, topk_w, topk_p, keep, core_size, w_renorm, n_empty, y, y_f32,
                    workspace, stream=None):
-    """One pass: route -> coreset -> forward in one call (four launches for <= 32 rows).
+    """One pass: route -> coreset -> forward in one call.
     ``topk_p`` None: the weight mass; a tensor: the probability mass."""
     d = plan.dims
     R = x.shape[0]

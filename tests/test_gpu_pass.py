@@ -1,8 +1,6 @@
-"""moe_block_pass: one denoising pass (route -> coreset -> forward) in one call.
-For calls of at most 32 rows the router, the coreset and the forward's
-bookkeeping run as one kernel (the last CTA of the router grid carries on);
-larger calls run the three calls' kernels.  Every output must equal the three
-separate calls bit for bit, on every path, and match the oracle."""
+"""moe_block_pass: one denoising pass (route -> coreset -> forward) in one call,
+the kernels enqueued back to back.  Every output must equal the three separate
+calls bit for bit, on every path, and match the oracle."""
 from __future__ import annotations
 
 import dataclasses
@@ -89,7 +87,7 @@ SMALL = [W.TINY, W.BLOCK32, _small(rows=(5, 0, 7)), _small(rows=(13, 1, 1, 17)),
 
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: f"{w.name}-{w.E}-{w.k}-{w.block_rows}")
-def test_fused_front_end_equals_three_calls(w):
+def test_small_pass_equals_three_calls(w):
     case = Case(w)
     got = _equal_to_calls(case)
     ref = case.oracle_route()
@@ -102,13 +100,13 @@ def test_fused_front_end_equals_three_calls(w):
 
 
 @pytest.mark.parametrize("tau", [0.5, 1.0])
-def test_fused_front_end_tau_and_budget(tau):
+def test_pass_tau_and_budget(tau):
     case = Case(W.BLOCK32)
     _equal_to_calls(case, tau=tau)
     _equal_to_calls(case, tau=tau, max_experts=20)
 
 
-def test_fused_front_end_probability_mass():
+def test_pass_probability_mass():
     case = Case(W.BLOCK32)
     got = _equal_to_calls(case, probs=True)
     ref = case.oracle_route(probs=True)
@@ -124,8 +122,8 @@ def test_large_pass_equals_three_calls(w):
 
 
 def test_pass_repeats_and_replays_bit_identically():
-    """The front end's ticket is cleared by the call itself: repeated passes and a
-    CUDA-graph replay give the same bits."""
+    """Repeated passes and a CUDA-graph replay give the same bits (the router's
+    tickets are cleared by the call itself)."""
     case = Case(W.BLOCK32)
     a = run_pass(case)
     b = run_pass(case)
