@@ -53,6 +53,40 @@ __device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t* wa
     return before + incl - v;
 }
 
+// Sort 256 64-bit keys held eight per lane (slot i = 8 * lane + r) into
+// descending order across the warp: a bitonic network whose strides below 8
+// compare registers of one lane and whose strides of 8 and more trade a
+// register with lane ^ (stride / 8).  36 steps, no shared memory, no barrier.
+__device__ __forceinline__ void warp_sort256_desc(unsigned long long (&k)[8], int lane) {
+#pragma unroll
+    for (int size = 2; size <= 256; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride >= 8) {
+                const int lm = stride >> 3;                       // lane distance
+                const bool lower = (lane & lm) == 0;              // the lower slot of the pair
+                const bool desc = ((8 * lane) & size) == 0;       // this run sorts descending
+                const bool keep_max = lower == desc;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, k[r], lm);
+                    k[r] = keep_max ? (k[r] > o ? k[r] : o) : (k[r] < o ? k[r] : o);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int pr = r ^ stride;
+                    if (pr > r) {
+                        const bool desc = ((8 * lane + r) & size) == 0;
+                        const unsigned long long a = k[r], b = k[pr];
+                        if (desc ? a < b : a > b) { k[r] = b; k[pr] = a; }
+                    }
+                }
+            }
+        }
+    }
+}
+
 // Shared memory of one block's coreset.
 struct CoresetSmem {
     unsigned long long Q[kMaxE];
@@ -127,14 +161,47 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
         // Order (Q desc, id asc) as one 64-bit key per expert: (Q << 10 | (1023 - e)) + 1
         // for touched experts, 0 otherwise (Q < 2^53: a block has fewer than 2^21 rows);
         // keys are unique, and Q and e can be read back from a key.
+        const bool warp_sort = E <= 256;   // one warp sorts every key in registers
         int n = 32;
         while (n < E) n <<= 1;
+        if (warp_sort) n = 256;
         for (int e = tid; e < n; e += blockDim.x)
             keys[e] = (e < E && ((touched[e >> 5] >> (e & 31)) & 1u))
                           ? ((unsigned long long)Q[e] << 10 | (unsigned long long)(1023 - e)) + 1ull
                           : 0ull;
         __syncthreads();
-        if (sort_ranks) {
+        if (warp_sort) {
+            // warp 0: sort, then the exclusive prefix of the masses in that order;
+            // slot i is kept iff the mass ranked above it is still below theta
+            // (the greedy prefix) and, under the budget, i < cap
+            if (tid < 32) {
+                unsigned long long kk[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) kk[r] = keys[8 * tid + r];
+                warp_sort256_desc(kk, tid);
+                unsigned long long pre[8], run = 0;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    pre[r] = run;
+                    run += kk[r] ? (kk[r] - 1ull) >> 10 : 0ull;
+                }
+                unsigned long long incl = run;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += t;
+                }
+                const unsigned long long lane_excl = incl - run;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const unsigned long long key = kk[r];
+                    if (key && (disabled || lane_excl + pre[r] < theta) && 8 * tid + r < cap) {
+                        const int e = 1023 - (int)((key - 1ull) & 1023ull);
+                        atomicOr(&incore[e >> 5], 1u << (e & 31));
+                    }
+                }
+            }
+        } else if (sort_ranks) {
             // bitonic sort, descending
             for (int kk = 2; kk <= n; kk <<= 1) {
                 for (int j = kk >> 1; j > 0; j >>= 1) {
@@ -200,30 +267,32 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
     __syncthreads();
     for (int w = tid; w < words; w += blockDim.x) a.keep[(size_t)b * words + w] = incore[w];
     if (tid == 0) a.core_size[b] = c;
-    // renormalise rows
+    // renormalise rows: a warp per row, lane j holding slot j (k <= 32); the sum
+    // of the surviving weights is taken in rank order, one fp32 add at a time
     int empty = 0;
-    for (int r = r0 + tid; r < r1; r += blockDim.x) {
-        const int32_t* idx = a.topk_idx + (size_t)r * k;
-        const float* w = a.topk_w + (size_t)r * k;
-        float* wo = a.w_renorm + (size_t)r * k;
-        if (!renorm) {
-            for (int j = 0; j < k; ++j) wo[j] = w[j];
-            continue;
-        }
-        float s = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const int e = idx[j];
-            if (e >= 0 && e < E && ((incore[e >> 5] >> (e & 31)) & 1u)) s = __fadd_rn(s, w[j]);
-        }
-        if (s == 0.0f) {
-            for (int j = 0; j < k; ++j) wo[j] = 0.0f;
-            ++empty;
-            continue;
-        }
-        for (int j = 0; j < k; ++j) {
-            const int e = idx[j];
+    {
+        const int lane = tid & 31, nw = blockDim.x >> 5;
+        for (int r = r0 + (tid >> 5); r < r1; r += nw) {
+            const int e = lane < k ? a.topk_idx[(size_t)r * k + lane] : -1;
+            const float wj = lane < k ? a.topk_w[(size_t)r * k + lane] : 0.0f;
+            float* wo = a.w_renorm + (size_t)r * k;
+            if (!renorm) {
+                if (lane < k) wo[lane] = wj;
+                continue;
+            }
             const bool in = e >= 0 && e < E && ((incore[e >> 5] >> (e & 31)) & 1u);
-            wo[j] = in ? __fdiv_rn(w[j], s) : 0.0f;
+            const uint32_t inm = __ballot_sync(0xffffffffu, in);
+            float s = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                const float v = __shfl_sync(0xffffffffu, wj, j);
+                if ((inm >> j) & 1u) s = __fadd_rn(s, v);
+            }
+            if (s == 0.0f) {
+                if (lane < k) wo[lane] = 0.0f;
+                if (lane == 0) ++empty;
+                continue;
+            }
+            if (lane < k) wo[lane] = in ? __fdiv_rn(wj, s) : 0.0f;
         }
     }
     if (empty) atomicAdd(&s_empty, empty);
