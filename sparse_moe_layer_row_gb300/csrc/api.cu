@@ -524,7 +524,6 @@ moe_status moe_block_pass(const moe_plan* p, const void* x, int32_t R, const int
     if (!(tau > 0.0f)) return fail(MOE_ERR_INVALID_ARG, "tau=%g must be > 0 (and not NaN)", (double)tau);
     if (max_experts < 0) return fail(MOE_ERR_INVALID_ARG, "max_experts=%d must be >= 0", max_experts);
     if (R == 0) return ok();
-    const moe_dims& d = p->d;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the router, coreset and forward kernels of the three calls, back to back with
     // programmatic dependent launch between them (no host synchronisation)

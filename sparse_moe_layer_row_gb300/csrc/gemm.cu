@@ -512,6 +512,16 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const int4 un = __ldg(a.units + u);
             const int g = un.x, m = un.y, start = un.z, n = un.w;
             const int n16 = (n + 15) & ~15;
+            // down: the unit's pair weights, lane l of wreg[j] holding pair
+            // 32 j + l (0 past the unit's pairs), loaded while the MMA runs
+            float wreg[MODE == kDown ? NMAX / 32 : 1];
+            if (MODE == kDown) {
+#pragma unroll
+                for (int j = 0; j < NMAX / 32; ++j) {
+                    const int t = 32 * j + lane;
+                    wreg[j] = t < n ? (g == a.E ? 1.0f : __ldg(a.pair_w + start + t)) : 0.0f;
+                }
+            }
             const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitNs);
             if (__any_sync(0xffffffffu, !ok)) { give_up(); break; }
             __syncwarp();
@@ -568,37 +578,41 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 // one 256-byte segment; the accumulator is released before the
                 // copy-out.  fp16 holds |v| < 65504: each warp owns a 32-column
                 // quarter (its TMEM lane quadrant) of every pair, and a quarter
-                // with a value of 2^15 or more (or a non-finite one) is stored as
-                // v * 2^-s with the smallest s that brings its largest magnitude
-                // below 2^15; s goes to ysx and the call's `scaled` flag is set;
-                // k_combine multiplies it back exactly.  Values below 2^15 are
-                // stored as they are (s = 0).
+                // whose largest finite magnitude is 2^15 or more is stored as
+                // v * 2^-s with the smallest s that brings that magnitude below
+                // 2^15; s goes to ysx and the call's `scaled` flag is set;
+                // k_combine multiplies it back exactly.  Other quarters are
+                // stored as they are (s = 0); infinities and NaNs pass through
+                // the scaling unchanged.  The common case costs one max per
+                // value: the exact per-pair exponents are only worked out for
+                // a group of 32 pairs in which some lane saw 2^15 or more.
                 __half* xs = reinterpret_cast<__half*>(base + C::kXchgOff);
                 const int hl = q * 32 + lane;
                 const size_t row0 = (size_t)(g == a.E ? a.shared_row0 : 0) + start;
                 uint8_t* xq = a.ysx + (size_t)(m * 4 + q) * a.ld_x + row0;  // this quarter's exponents
                 bool any_big = false;
-                for (int c = 0; c < n16; c += 16) {
-                    // the chunk's pair weights first (not reordered across stores)
-                    float wv[16];
 #pragma unroll
-                    for (int t = 0; t < 16; ++t)
-                        wv[t] = (g == a.E || c + t >= n) ? 1.0f : __ldg(a.pair_w + start + c + t);
-                    float v[16];
+                for (int j = 0; j < NMAX / 32; ++j) {
+                    const int c = 32 * j;
+                    if (c >= n16) break;
+                    float v[32];
                     __syncwarp();  // tcgen05.ld is warp-collective
-                    tmem_ld16(tb + (uint32_t)c, v);
-                    bool big = false;
+                    // columns c .. c + 31 (those past n16 are inside the
+                    // accumulator and never copied out)
+                    tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(c + 16), v, v + 16);
+                    float mx = 0.0f;   // fmaxf skips NaN: the tail's 0 * garbage
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        v[t] = wv[t] * v[t];
-                        big |= !(fabsf(v[t]) < 32768.0f) && c + t < n;
+                    for (int t = 0; t < 32; ++t) {
+                        v[t] *= __shfl_sync(0xffffffffu, wreg[j], t);
+                        mx = fmaxf(mx, fabsf(v[t]));
                     }
                     uint32_t my_s = 0;  // lane t: the exponent of pair c + t
-                    if (__any_sync(0xffffffffu, big)) {
+                    if (__any_sync(0xffffffffu, mx >= 32768.0f)) {
                         any_big = true;
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            const uint32_t mb = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[t])));
+                        for (int t = 0; t < 32; ++t) {
+                            const uint32_t ab = __float_as_uint(v[t]) & 0x7FFFFFFFu;
+                            const uint32_t mb = __reduce_max_sync(0xffffffffu, ab < 0x7F800000u ? ab : 0u);
                             const int sh = (int)(mb >> 23) - 141;   // biased exponent - (127 + 14)
                             const uint32_t st = sh > 0 ? (uint32_t)sh : 0u;
                             v[t] *= __uint_as_float((127u - st) << 23);   // 2^-s, exact
@@ -606,8 +620,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         }
                     }
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) xs[(c + t) * 128 + hl] = __float2half_rn(v[t]);
-                    if (lane < 16 && c + lane < n) xq[c + lane] = (uint8_t)my_s;
+                    for (int t = 0; t < 32; ++t) xs[(c + t) * 128 + hl] = __float2half_rn(v[t]);
+                    if (c + lane < n) xq[c + lane] = (uint8_t)my_s;
                 }
                 if (any_big && lane == 0) *a.scaled = 1;
                 tc_fence_before();
