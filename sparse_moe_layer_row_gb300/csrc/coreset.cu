@@ -16,12 +16,14 @@
 //   * theta = ceil(tau * T), T = sum_e Q_e, with tau = M * 2^-s taken from its
 //     fp32 encoding and the product formed in 128 bits;
 //   * experts ranked by (Q desc, id asc); the coreset is the shortest prefix
-//     of that order whose mass reaches theta: its size is the number of ranks
-//     whose exclusive prefix mass is still below theta.  The ranks come from
-//     one 64-bit key per expert: with many blocks (CTAs sharing SMs, so
-//     throughput counts) a bitonic sort of the keys in shared memory; with
-//     few, a group of lanes counts the keys above each expert's own (no
-//     barriers: the single CTA's latency counts).  Both give the same ranks;
+//     of that order whose mass reaches theta: an expert is in it iff the mass
+//     of the experts ranked above it is still below theta.  The ranks come
+//     from one 64-bit key per expert.  Up to 256 experts: a thread per expert
+//     counts, over the compacted keys of the block's touched experts, the
+//     keys above its own and their mass.  More experts: with many blocks
+//     (CTAs sharing SMs, so throughput counts) a bitonic sort of the keys in
+//     shared memory; with few, a group of lanes counts the keys above each
+//     expert's own.  All give the same ranks;
 //   * an expert budget B > 0 (InfiniLM PR #604, Summary, names it without
 //     defining it) keeps at most the first B experts of that order; rows are
 //     copied unchanged only when tau >= 1 and nothing is dropped.
@@ -39,8 +41,8 @@ __global__ void __launch_bounds__(kCoreThreads) k_coreset(CoresetArgs a) {
 
 cudaError_t launch_coreset(const CoresetArgs& a, cudaStream_t st) {
     if (a.nb <= 0) return cudaSuccess;
-    return launch_kernel(k_coreset, dim3(a.nb),
-                         dim3(a.nb >= kSortBlocks ? kCoreThreadsSort : kCoreThreads), 0, st, a);
+    const int threads = a.E <= 256 ? kCoreThreadsSmallE : (a.nb >= kSortBlocks ? kCoreThreadsSort : kCoreThreads);
+    return launch_kernel(k_coreset, dim3(a.nb), dim3(threads), 0, st, a);
 }
 
 }  // namespace moe

@@ -1,5 +1,4 @@
-// Device code of the block coreset, shared by k_coreset (one CTA per block)
-// and the fused front end of small calls (one CTA for every block).  The
+// Device code of the block coreset (k_coreset: one CTA per block).  The
 // method and its arithmetic are described in coreset.cu.
 #pragma once
 
@@ -7,8 +6,9 @@
 
 namespace moe {
 
-constexpr int kCoreThreads = 1024;      // few blocks: more threads rank each expert
-constexpr int kCoreThreadsSort = 256;   // many blocks (the sorting path)
+constexpr int kCoreThreads = 1024;      // E > 256, few blocks: more threads rank each expert
+constexpr int kCoreThreadsSort = 256;   // E > 256, many blocks (the sorting path)
+constexpr int kCoreThreadsSmallE = 256; // E <= 256: a thread per expert
 constexpr int kMaxE = 1024;
 constexpr int kSortBlocks = 64;   // blocks from which the ranks come from a sort
 
@@ -53,40 +53,6 @@ __device__ __forceinline__ uint64_t block_excl_scan_u64(uint64_t v, uint64_t* wa
     return before + incl - v;
 }
 
-// Sort 256 64-bit keys held eight per lane (slot i = 8 * lane + r) into
-// descending order across the warp: a bitonic network whose strides below 8
-// compare registers of one lane and whose strides of 8 and more trade a
-// register with lane ^ (stride / 8).  36 steps, no shared memory, no barrier.
-__device__ __forceinline__ void warp_sort256_desc(unsigned long long (&k)[8], int lane) {
-#pragma unroll
-    for (int size = 2; size <= 256; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            if (stride >= 8) {
-                const int lm = stride >> 3;                       // lane distance
-                const bool lower = (lane & lm) == 0;              // the lower slot of the pair
-                const bool desc = ((8 * lane) & size) == 0;       // this run sorts descending
-                const bool keep_max = lower == desc;
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, k[r], lm);
-                    k[r] = keep_max ? (k[r] > o ? k[r] : o) : (k[r] < o ? k[r] : o);
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int pr = r ^ stride;
-                    if (pr > r) {
-                        const bool desc = ((8 * lane + r) & size) == 0;
-                        const unsigned long long a = k[r], b = k[pr];
-                        if (desc ? a < b : a > b) { k[r] = b; k[pr] = a; }
-                    }
-                }
-            }
-        }
-    }
-}
-
 // Shared memory of one block's coreset.
 struct CoresetSmem {
     unsigned long long Q[kMaxE];
@@ -94,14 +60,16 @@ struct CoresetSmem {
     uint32_t incore[kMaxE / 32];
     unsigned long long keys[kMaxE];
     uint64_t warp_sums[32];
+    int warp_cnt[32];
     int s_bad, s_empty;
 };
 
 // The coreset of block b and its rows' renormalised weights, by the whole CTA
-// (every thread calls it).  sort_ranks: rank the experts by a bitonic sort
-// (many CTAs share the SMs) rather than by lanes counting the keys above each
-// expert (few CTAs: latency counts); both give the same ranks.  The shared
-// memory may be reused after the call returns.
+// (every thread calls it).  With E <= 256 and kCoreThreadsSmallE threads a
+// thread ranks each expert; otherwise sort_ranks picks a bitonic sort (many
+// CTAs share the SMs) rather than lanes counting the keys above each expert
+// (few CTAs: latency counts); all give the same ranks.  The shared memory may
+// be reused after the call returns.
 __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, CoresetSmem& sm,
                                               bool sort_ranks) {
     unsigned long long* Q = sm.Q;
@@ -109,6 +77,7 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
     uint32_t* incore = sm.incore;
     unsigned long long* keys = sm.keys;
     uint64_t* warp_sums = sm.warp_sums;
+    int* warp_cnt = sm.warp_cnt;
     int& s_bad = sm.s_bad;
     int& s_empty = sm.s_empty;
     const int tid = threadIdx.x;
@@ -143,6 +112,68 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
     }
     if (bad) atomicAdd(&s_bad, bad);
     __syncthreads();
+    bool renorm;   // else the rows keep their weights bit for bit
+    if (E <= 256 && (int)blockDim.x == kCoreThreadsSmallE) {
+        // A thread per expert.  The touched experts' keys are compacted into
+        // `keys` (warp ballots), T and their number come from per-warp sums,
+        // and each touched expert counts the keys above its own and their
+        // mass; its keep bit goes straight into the warp's ballot word.
+        const int lane = tid & 31, warp = tid >> 5;
+        const int e = tid;
+        const bool tch = e < E && ((touched[e >> 5] >> (e & 31)) & 1u);
+        const unsigned long long qe = tch ? Q[e] : 0ull;
+        const uint32_t tm = __ballot_sync(0xffffffffu, tch);
+        unsigned long long wq = qe;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) wq += __shfl_xor_sync(0xffffffffu, wq, o);
+        if (lane == 0) {
+            warp_cnt[warp] = __popc(tm);
+            warp_sums[warp] = wq;
+        }
+        __syncthreads();
+        uint64_t T = 0;
+        int nt = 0, before = 0;
+#pragma unroll
+        for (int w = 0; w < kCoreThreadsSmallE / 32; ++w) {
+            T += warp_sums[w];
+            before += w < warp ? warp_cnt[w] : 0;
+            nt += warp_cnt[w];
+        }
+        const bool disabled = !(a.tau < 1.0f);
+        const int cap = (a.max_experts > 0 && a.max_experts < nt) ? a.max_experts : nt;
+        renorm = !disabled || cap < nt;
+        // (Q desc, id asc) as one 64-bit key, as below
+        const unsigned long long key = ((unsigned long long)qe << 10 | (unsigned long long)(1023 - e)) + 1ull;
+        if (renorm && tch) keys[before + __popc(tm & ((1u << lane) - 1u))] = key;
+        __syncthreads();
+        bool in = tch;
+        if (renorm && tch) {
+            const uint64_t theta = disabled ? ~0ull : mass_threshold(a.tau, T);
+            unsigned long long above = 0;
+            int rank = 0;
+            int f = 0;
+            for (; f + 4 <= nt; f += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const unsigned long long kf = keys[f + u];
+                    const bool gt = kf > key;
+                    rank += gt;
+                    above += gt ? (kf - 1ull) >> 10 : 0ull;
+                }
+            }
+            for (; f < nt; ++f) {
+                const unsigned long long kf = keys[f];
+                const bool gt = kf > key;
+                rank += gt;
+                above += gt ? (kf - 1ull) >> 10 : 0ull;
+            }
+            // kept iff the mass ranked above is still below theta (the greedy
+            // prefix) and, under the budget, the rank is below the cap
+            in = (disabled || above < theta) && rank < cap;
+        }
+        const uint32_t word = __ballot_sync(0xffffffffu, in);
+        if (lane == 0 && warp < words) incore[warp] = word;
+    } else {
     // block total T and touched count
     uint64_t part = 0;
     for (int e = tid; e < E; e += blockDim.x) part += Q[e];
@@ -153,7 +184,7 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
 
     const bool disabled = !(a.tau < 1.0f);
     const int cap = (a.max_experts > 0 && a.max_experts < nt) ? a.max_experts : nt;
-    const bool renorm = !disabled || cap < nt;  // else the rows keep their weights bit for bit
+    renorm = !disabled || cap < nt;
     if (!renorm) {
         for (int w = tid; w < words; w += blockDim.x) incore[w] = touched[w];
     } else {
@@ -161,47 +192,14 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
         // Order (Q desc, id asc) as one 64-bit key per expert: (Q << 10 | (1023 - e)) + 1
         // for touched experts, 0 otherwise (Q < 2^53: a block has fewer than 2^21 rows);
         // keys are unique, and Q and e can be read back from a key.
-        const bool warp_sort = E <= 256;   // one warp sorts every key in registers
         int n = 32;
         while (n < E) n <<= 1;
-        if (warp_sort) n = 256;
         for (int e = tid; e < n; e += blockDim.x)
             keys[e] = (e < E && ((touched[e >> 5] >> (e & 31)) & 1u))
                           ? ((unsigned long long)Q[e] << 10 | (unsigned long long)(1023 - e)) + 1ull
                           : 0ull;
         __syncthreads();
-        if (warp_sort) {
-            // warp 0: sort, then the exclusive prefix of the masses in that order;
-            // slot i is kept iff the mass ranked above it is still below theta
-            // (the greedy prefix) and, under the budget, i < cap
-            if (tid < 32) {
-                unsigned long long kk[8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) kk[r] = keys[8 * tid + r];
-                warp_sort256_desc(kk, tid);
-                unsigned long long pre[8], run = 0;
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    pre[r] = run;
-                    run += kk[r] ? (kk[r] - 1ull) >> 10 : 0ull;
-                }
-                unsigned long long incl = run;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (tid >= o) incl += t;
-                }
-                const unsigned long long lane_excl = incl - run;
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const unsigned long long key = kk[r];
-                    if (key && (disabled || lane_excl + pre[r] < theta) && 8 * tid + r < cap) {
-                        const int e = 1023 - (int)((key - 1ull) & 1023ull);
-                        atomicOr(&incore[e >> 5], 1u << (e & 31));
-                    }
-                }
-            }
-        } else if (sort_ranks) {
+        if (sort_ranks) {
             // bitonic sort, descending
             for (int kk = 2; kk <= n; kk <<= 1) {
                 for (int j = kk >> 1; j > 0; j >>= 1) {
@@ -260,6 +258,7 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
                     atomicOr(&incore[e >> 5], 1u << (e & 31));
             }
         }
+    }
     }
     __syncthreads();
     int c = 0;

@@ -97,35 +97,56 @@ __device__ __forceinline__ float finish_logit(float dot, const float* bias_row, 
     return __fadd_rn(z, 0.0f);
 }
 
+// In-lane bitonic sort of NI (a power of two) 64-bit values, descending.
+template <int NI>
+__device__ __forceinline__ void lane_sort_desc(unsigned long long (&c)[NI]) {
+#pragma unroll
+    for (int size = 2; size <= NI; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;
+                    const unsigned long long a = c[i], b = c[j];
+                    const bool sw = desc ? a < b : a > b;
+                    c[i] = sw ? b : a;
+                    c[j] = sw ? a : b;
+                }
+            }
+}
+
 // Warp top-k over entries spread across lanes: lane entry i holds (key[i],
 // id[i]) when bit i of `valid` is set.  Order: key descending, id ascending.
 // Lane j < k receives the j-th entry in my_id / my_key.  k must not exceed
-// the number of valid entries in the warp.
+// the number of valid entries in the warp.  Each entry becomes one 64-bit
+// value (key, ~id) -- larger means earlier in the order, 0 for an invalid
+// entry (a valid one is never 0: ids are below 2^31) -- each lane sorts its
+// own values, and every round the warp takes the largest lane head (the key
+// by one reduction, the id among the lanes holding that key by another) and
+// that lane drops its head.  No divergent branch.
 template <int NI>
 __device__ __forceinline__ void warp_topk(const uint32_t (&key)[NI], const uint32_t (&id)[NI],
                                           uint32_t valid, int k, int lane, uint32_t& my_id,
                                           uint32_t& my_key) {
-    uint32_t taken = ~valid;
+    unsigned long long c[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+        c[i] = ((valid >> i) & 1u) ? ((unsigned long long)key[i] << 32 | (uint32_t)~id[i]) : 0ull;
+    lane_sort_desc<NI>(c);
     my_id = 0;
     my_key = 0;
     for (int j = 0; j < k; ++j) {
-        uint32_t bk = 0, bid = 0xFFFFFFFFu;
-        int bi = -1;
+        const uint32_t hk = (uint32_t)(c[0] >> 32), hl = (uint32_t)c[0];
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
+        const uint32_t ml = __reduce_max_sync(0xffffffffu, hk == mk ? hl : 0u);
+        const bool win = c[0] != 0ull && hk == mk && hl == ml;
 #pragma unroll
-        for (int i = 0; i < NI; ++i) {
-            if ((taken >> i) & 1u) continue;
-            if (bi < 0 || key[i] > bk || (key[i] == bk && id[i] < bid)) {
-                bk = key[i];
-                bid = id[i];
-                bi = i;
-            }
-        }
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
-        const uint32_t cand = (bi >= 0 && bk == mk) ? bid : 0xFFFFFFFFu;
-        const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-        if (bi >= 0 && bid == win) taken |= 1u << bi;
+        for (int i = 0; i + 1 < NI; ++i) c[i] = win ? c[i + 1] : c[i];
+        c[NI - 1] = win ? 0ull : c[NI - 1];
         if (lane == j) {
-            my_id = win;
+            my_id = ~ml;
             my_key = mk;
         }
     }

@@ -1,6 +1,6 @@
-// Device code of the forward bookkeeping shared by the scatter kernels
-// (scatter.cu) and the fused front end of small calls: block scans, the GEMM
-// unit lists, and the whole small-call scatter in one CTA.
+// Device code of the forward bookkeeping of the scatter kernels (scatter.cu):
+// block scans, the GEMM unit lists, and the whole small-call scatter in one
+// CTA.
 #pragma once
 
 #include "kernels.cuh"
@@ -49,137 +49,134 @@ __device__ __forceinline__ void write_units(int4* out, int base, int g, int star
 // Same outputs as the three-kernel path: pair lists in row order per expert,
 // expert offsets and unit lists.  A row that names the same expert twice
 // contributes its first slot only (later duplicates are counted as bad ids),
-// so the counts and the lists always agree.
+// so the counts and the lists always agree.  Every expert has at most one
+// pair per row, so at most kSmallRows <= kSmallN pairs: one chunk (one unit
+// per weight tile) per expert.  The rows holding an expert's pairs are one
+// 32-bit mask; a pair's place in its expert's list is the number of rows
+// below its own in that mask.
 constexpr int kSmallThreads = 512;
+static_assert(kSmallRows <= 32 && kSmallRows <= kSmallN, "a row per mask bit, one chunk per expert");
 
 // Shared memory of the small-call scatter.
 struct ScatterSmallSmem {
-    uint8_t s_slot[kSmallRows][kMaxExperts];
-    int s_cnt[kMaxExperts];
+    uint32_t mask[kMaxExperts];                    // rows with a surviving pair of e
+    int off[kMaxExperts];                          // e's first place in the pair list
+    int chunk_exp[kMaxExperts];                    // expert of each non-empty chunk
+    uint32_t keepw[kSmallRows][kMaxExperts / 32];  // keep words of each row's block
+    int32_t ids[kSmallRows * 32];
+    float w[kSmallRows * 32];
+    uint8_t ok[kSmallRows * 32];                   // the pair survives (and is its row's first of e)
+    uint8_t live[kSmallRows];
     int warp_sums[32];
-    // the inputs, read before anything is written: a load issued after a store
-    // to memory that may alias waits for it, and the per-expert loops below
-    // would pay one round trip per pair
-    int32_t s_ids[kSmallRows * 32];
-    float s_w[kSmallRows * 32];
-    int s_blk[kSmallRows];
-    uint8_t s_live[kSmallRows];
     int s_dup, s_nl;
 };
 
 // The small-call scatter by the whole CTA (every thread calls it; written for
 // kSmallThreads threads, correct for any multiple of 32).
 __device__ __forceinline__ void scatter_small(const ScatterArgs& a, ScatterSmallSmem& sm) {
-    // slot of expert e in row r (< 32), kFree (kept for r's block, no slot yet)
-    // or kDropped (not kept)
-    constexpr uint8_t kFree = 0xFF, kDropped = 0xFE;
-    auto& s_slot = sm.s_slot;
-    int* s_cnt = sm.s_cnt;
-    int* warp_sums = sm.warp_sums;
-    int32_t* s_ids = sm.s_ids;
-    float* s_w = sm.s_w;
-    int* s_blk = sm.s_blk;
-    uint8_t* s_live = sm.s_live;
-    int& s_dup = sm.s_dup;
-    int& s_nl = sm.s_nl;
     const int tid = threadIdx.x;
     const int E = a.E, k = a.k, R = a.R;
     const int words = (E + 31) >> 5;
-    if (tid < R) {
-        s_blk[tid] = find_block(a.off, a.nb, tid);
-        s_live[tid] = !a.live || a.live[tid] != 0;
-    }
+    // 1. inputs: slot lists, liveness, the keep words of each row's block
     for (int i = tid; i < R * k; i += blockDim.x) {
-        s_ids[i] = a.topk_idx[i];
-        s_w[i] = a.w_renorm[i];
+        sm.ids[i] = a.topk_idx[i];
+        sm.w[i] = a.w_renorm[i];
     }
-    if (tid == 0) s_dup = 0;
-    __syncthreads();
-    for (int i = tid; i < R * words; i += blockDim.x) {   // one keep word per thread
+    for (int i = tid; i < R * words; i += blockDim.x) {
         const int r = i / words, wd = i - r * words;
-        const uint32_t kw = a.keep[(size_t)s_blk[r] * words + wd];
-        for (int bit = 0; bit < 32 && wd * 32 + bit < E; ++bit)
-            s_slot[r][wd * 32 + bit] = ((kw >> bit) & 1u) ? kFree : kDropped;
+        sm.keepw[r][wd] = a.keep[(size_t)find_block(a.off, a.nb, r) * words + wd];
     }
-    if (tid < 32) {  // live rows in order (R <= 32): the shared expert's rows
-        const bool lv = tid < R && s_live[tid];
+    if (tid < R) sm.live[tid] = !a.live || a.live[tid] != 0;
+    for (int e = tid; e < E; e += blockDim.x) sm.mask[e] = 0u;
+    if (tid == 0) sm.s_dup = 0;
+    __syncthreads();
+    // 2. a thread per (row, slot): the pair survives if its row is live, its
+    // expert valid and kept for the row's block, and no earlier slot of the
+    // row names the same expert; warp 0 lists the live rows (the shared
+    // expert's rows) in order
+    for (int i = tid; i < R * k; i += blockDim.x) {
+        const int r = i / k, j = i - r * k;
+        const int e = sm.ids[i];
+        const bool kept = sm.live[r] && e >= 0 && e < E && ((sm.keepw[r][e >> 5] >> (e & 31)) & 1u);
+        bool dup = false;
+        if (kept)
+            for (int jj = 0; jj < j; ++jj) dup |= sm.ids[r * k + jj] == e;
+        const bool ok = kept && !dup;
+        sm.ok[i] = ok;
+        if (ok) atomicOr(&sm.mask[e], 1u << r);
+        else a.inv[i] = -1;
+        if (dup) atomicAdd(&sm.s_dup, 1);
+    }
+    if (tid < 32) {
+        const bool lv = tid < R && sm.live[tid];
         const uint32_t m = __ballot_sync(0xffffffffu, lv);
-        if (tid == 0) s_nl = __popc(m);
+        const int pos = __popc(m & ((1u << tid) - 1u));
+        if (tid < R) a.shared_inv[tid] = lv ? pos : -1;
+        if (lv) a.shared_rows[pos] = tid;
+        if (tid == 0) sm.s_nl = __popc(m);
     }
     __syncthreads();
-    if (tid < R) {
-        int pos = 0;
-        for (int r = 0; r < tid; ++r) pos += s_live[r];
-        a.shared_inv[tid] = s_live[tid] ? pos : -1;
-        if (s_live[tid]) a.shared_rows[pos] = tid;
-    }
-    const int nl = s_nl;
-    // one thread per row: mark its surviving slots (first slot wins); dead rows none
-    for (int r = tid; r < R; r += blockDim.x) {
-        const bool lv = s_live[r];
-        int dup = 0;
-        for (int j = 0; j < k; ++j) {
-            a.inv[(size_t)r * k + j] = -1;
-            const int e = s_ids[r * k + j];
-            if (!lv || e < 0 || e >= E) continue;
-            const uint8_t st = s_slot[r][e];
-            if (st == kDropped) continue;
-            if (st != kFree) { ++dup; continue; }
-            s_slot[r][e] = (uint8_t)j;
-        }
-        if (dup) atomicAdd(&s_dup, dup);
-    }
-    __syncthreads();
-    // per expert: its rows (walk the rows in order)
-    for (int e = tid; e < E; e += blockDim.x) {
-        int n = 0;
-        for (int r = 0; r < R; ++r) n += s_slot[r][e] < 32;
-        s_cnt[e] = n;
-    }
-    __syncthreads();
+    // 3. per expert: its pair count, and (one scan of count << 16 | non-empty)
+    // its place in the pair list and its chunk index
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-    int sum = 0, ch = 0;
-    for (int f = e0; f < e1; ++f) {
-        sum += s_cnt[f];
-        ch += (s_cnt[f] + a.nt_gu - 1) / a.nt_gu;
+    int packed = 0;
+    for (int e = e0; e < e1; ++e) {
+        const int n = __popc(sm.mask[e]);
+        packed += n << 16 | (n > 0);
     }
-    int tot_pairs, tot_ch;
-    int pp = block_excl_scan_i32(sum, warp_sums, &tot_pairs);
-    int cc = block_excl_scan_i32(ch, warp_sums, &tot_ch);
+    int tot;
+    int before = block_excl_scan_i32(packed, sm.warp_sums, &tot);
+    for (int e = e0; e < e1; ++e) {
+        const int n = __popc(sm.mask[e]);
+        const int pp = before >> 16, ch = before & 0xFFFF;
+        sm.off[e] = pp;
+        if (n) sm.chunk_exp[ch] = e;
+        a.expert_off[e] = pp;
+        a.count[e] = n;
+        before += n << 16 | (n > 0);
+    }
+    const int tot_pairs = tot >> 16, nch = tot & 0xFFFF;
+    __syncthreads();
+    // 4. the pair lists, then the unit lists (consecutive threads write
+    // consecutive entries): the shared expert's chunk first, then one chunk
+    // per non-empty expert, each as its weight tiles in order
+    for (int i = tid; i < R * k; i += blockDim.x) {
+        if (!sm.ok[i]) continue;
+        const int r = i / k, e = sm.ids[i];
+        const int pos = sm.off[e] + __popc(sm.mask[e] & ((1u << r) - 1u));
+        a.pair_row[pos] = r;
+        a.pair_w[pos] = sm.w[i];
+        a.inv[i] = pos;
+    }
+    const int nl = sm.s_nl;
+    const int s_chunks = nl > 0 ? 1 : 0;   // nl <= kSmallRows <= nt
     const int mt_gu = (a.I + a.gu_rows - 1) / a.gu_rows, mt_gs = (a.Is + a.gu_rows - 1) / a.gu_rows;
     const int mt_dn = a.H / 128;
-    const int s_chunks = (nl + a.nt_gu - 1) / a.nt_gu;   // nt_gu == nt_dn here
     const int base_gu = s_chunks * mt_gs, base_dn = s_chunks * mt_dn;
-    if (tid == 0) {
-        write_units(a.units_gu, 0, E, 0, nl, a.nt_gu, mt_gs);
-        write_units(a.units_dn, 0, E, 0, nl, a.nt_dn, mt_dn);
-    }
-    for (int f = e0; f < e1; ++f) {
-        const int n = s_cnt[f];
-        a.expert_off[f] = pp;
-        a.count[f] = n;
-        write_units(a.units_gu, base_gu + cc * mt_gu, f, pp, n, a.nt_gu, mt_gu);
-        write_units(a.units_dn, base_dn + cc * mt_dn, f, pp, n, a.nt_dn, mt_dn);
-        int pos = pp;
-        for (int r = 0; r < R && pos < pp + n; ++r) {
-            const int j = s_slot[r][f];
-            if (j >= 32) continue;
-            a.pair_row[pos] = r;
-            a.pair_w[pos] = s_w[r * k + j];
-            a.inv[(size_t)r * k + j] = pos;
-            ++pos;
+    const int n_gu = base_gu + nch * mt_gu, n_dn = base_dn + nch * mt_dn;
+    for (int u = tid; u < n_gu + n_dn; u += blockDim.x) {
+        const bool gu = u < n_gu;
+        const int v = gu ? u : u - n_gu;
+        const int base = gu ? base_gu : base_dn, mt = gu ? mt_gu : mt_dn;
+        int4 un;
+        if (v < base) {
+            un = make_int4(E, v, 0, nl);
+        } else {
+            const int c = (v - base) / mt, m = (v - base) - c * mt;
+            const int g = sm.chunk_exp[c];
+            un = make_int4(g, m, sm.off[g], __popc(sm.mask[g]));
         }
-        pp += n;
-        cc += (n + a.nt_gu - 1) / a.nt_gu;
+        if (gu) a.units_gu[v] = un;
+        else a.units_dn[v] = un;
     }
     if (tid == 0) {
         a.expert_off[E] = tot_pairs;
-        a.misc[1] = base_gu + tot_ch * mt_gu;
-        a.misc[2] = base_dn + tot_ch * mt_dn;
+        a.misc[1] = n_gu;
+        a.misc[2] = n_dn;
         a.misc[3] = tot_pairs;
         a.misc[4] = 0;  // no staged output scaled yet (the down GEMM sets it)
-        status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)s_dup);
+        status_add(a.status, MOE_STATUS_BAD_EXPERT_ID, (uint32_t)sm.s_dup);
     }
 }
 
