@@ -11,6 +11,7 @@ constexpr int kCoreThreadsSort = 256;   // E > 256, many blocks (the sorting pat
 constexpr int kCoreThreadsSmallE = 256; // E <= 256: a thread per expert
 constexpr int kMaxE = 1024;
 constexpr int kSortBlocks = 64;   // blocks from which the ranks come from a sort
+constexpr int kPairCache = 2048;  // slots of a block kept in shared memory for the renormalisation
 
 __device__ __forceinline__ uint64_t mass_threshold(float tau, uint64_t T) {
     const uint32_t u = __float_as_uint(tau);
@@ -58,9 +59,12 @@ struct CoresetSmem {
     unsigned long long Q[kMaxE];
     uint32_t touched[kMaxE / 32];
     uint32_t incore[kMaxE / 32];
-    unsigned long long keys[kMaxE];
+    __align__(16) unsigned long long keys[kMaxE];
     uint64_t warp_sums[32];
     int warp_cnt[32];
+    int32_t pe[kPairCache];   // the block's slots (expert, weight) when they fit
+    float pw[kPairCache];
+    uint8_t in_flag[256];     // E <= 256: the expert is in the coreset
     int s_bad, s_empty;
 };
 
@@ -78,6 +82,7 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
     unsigned long long* keys = sm.keys;
     uint64_t* warp_sums = sm.warp_sums;
     int* warp_cnt = sm.warp_cnt;
+    uint8_t* in_flag = sm.in_flag;
     int& s_bad = sm.s_bad;
     int& s_empty = sm.s_empty;
     const int tid = threadIdx.x;
@@ -99,12 +104,18 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
     if (tid == 0) { s_bad = 0; s_empty = 0; }
     __syncthreads();
     const int npairs = (r1 - r0) * k;
+    const bool cached = npairs <= kPairCache;
     int bad = 0;
     for (int p = tid; p < npairs; p += blockDim.x) {
         const size_t i = (size_t)r0 * k + p;
         const int e = a.topk_idx[i];
+        const float wt = a.topk_w[i];
+        if (cached) {
+            sm.pe[p] = e;
+            sm.pw[p] = wt;
+        }
         if (e < 0 || e >= E) { ++bad; continue; }
-        const float w = (a.mass ? a.mass : a.topk_w)[i];   // the slot's mass
+        const float w = a.mass ? a.mass[i] : wt;   // the slot's mass
         const unsigned long long q =
             (w >= 0.0f && w <= 1.0f) ? __float2ull_rz(__fmul_rn(w, 4294967296.0f)) : 0ull;
         atomicAdd(&Q[e], q);
@@ -114,63 +125,81 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
     __syncthreads();
     bool renorm;   // else the rows keep their weights bit for bit
     if (E <= 256 && (int)blockDim.x == kCoreThreadsSmallE) {
-        // A thread per expert.  The touched experts' keys are compacted into
-        // `keys` (warp ballots), T and their number come from per-warp sums,
-        // and each touched expert counts the keys above its own and their
-        // mass; its keep bit goes straight into the warp's ballot word.
+        // A thread per expert.  Each warp sorts its 32 keys (one per lane,
+        // a shuffle bitonic network) and keeps the run with its exclusive
+        // prefix masses; an expert's rank is its place in its own run plus,
+        // for every other run, the number of keys above its own there (a
+        // binary search), and the mass above it the matching prefix masses.
         const int lane = tid & 31, warp = tid >> 5;
+        constexpr int kRuns = kCoreThreadsSmallE / 32;
+        unsigned long long* runk = keys;         // [kRuns][32] sorted keys
+        unsigned long long* runp = keys + 256;   // [kRuns][32] mass before each
         const int e = tid;
         const bool tch = e < E && ((touched[e >> 5] >> (e & 31)) & 1u);
-        const unsigned long long qe = tch ? Q[e] : 0ull;
-        const uint32_t tm = __ballot_sync(0xffffffffu, tch);
-        unsigned long long wq = qe;
+        // (Q desc, id asc) as one 64-bit key, as below; 0 for an untouched expert
+        unsigned long long x =
+            tch ? ((unsigned long long)Q[e] << 10 | (unsigned long long)(1023 - e)) + 1ull : 0ull;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) wq += __shfl_xor_sync(0xffffffffu, wq, o);
-        if (lane == 0) {
-            warp_cnt[warp] = __popc(tm);
-            warp_sums[warp] = wq;
+        for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, x, stride);
+                const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+                x = keep_max ? (x > o ? x : o) : (x < o ? x : o);
+            }
+        const unsigned long long qx = x ? (x - 1ull) >> 10 : 0ull;
+        unsigned long long incl = qx;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
         }
+        runk[warp * 32 + lane] = x;
+        runp[warp * 32 + lane] = incl - qx;
+        const uint32_t tm = __ballot_sync(0xffffffffu, x != 0ull);
+        if (lane == 31) {
+            warp_cnt[warp] = __popc(tm);
+            warp_sums[warp] = incl;
+        }
+        in_flag[e] = 0;
         __syncthreads();
         uint64_t T = 0;
-        int nt = 0, before = 0;
+        int nt = 0;
 #pragma unroll
-        for (int w = 0; w < kCoreThreadsSmallE / 32; ++w) {
+        for (int w = 0; w < kRuns; ++w) {
             T += warp_sums[w];
-            before += w < warp ? warp_cnt[w] : 0;
             nt += warp_cnt[w];
         }
         const bool disabled = !(a.tau < 1.0f);
         const int cap = (a.max_experts > 0 && a.max_experts < nt) ? a.max_experts : nt;
         renorm = !disabled || cap < nt;
-        // (Q desc, id asc) as one 64-bit key, as below
-        const unsigned long long key = ((unsigned long long)qe << 10 | (unsigned long long)(1023 - e)) + 1ull;
-        if (renorm && tch) keys[before + __popc(tm & ((1u << lane) - 1u))] = key;
-        __syncthreads();
-        bool in = tch;
-        if (renorm && tch) {
+        if (renorm && x) {
             const uint64_t theta = disabled ? ~0ull : mass_threshold(a.tau, T);
-            unsigned long long above = 0;
-            int rank = 0;
-            int f = 0;
-            for (; f + 4 <= nt; f += 4) {
+            // runs are descending: cnt[w] = number of keys of run w above x
+            // (32 when its last one is; else a binary search over 0 .. 31)
+            int cnt[kRuns];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const unsigned long long kf = keys[f + u];
-                    const bool gt = kf > key;
-                    rank += gt;
-                    above += gt ? (kf - 1ull) >> 10 : 0ull;
-                }
-            }
-            for (; f < nt; ++f) {
-                const unsigned long long kf = keys[f];
-                const bool gt = kf > key;
-                rank += gt;
-                above += gt ? (kf - 1ull) >> 10 : 0ull;
+            for (int w = 0; w < kRuns; ++w) cnt[w] = (w != warp && runk[w * 32 + 31] > x) ? 32 : 0;
+#pragma unroll
+            for (int step = 16; step >= 1; step >>= 1)
+#pragma unroll
+                for (int w = 0; w < kRuns; ++w)
+                    if (w != warp && cnt[w] < 32 && runk[w * 32 + cnt[w] + step - 1] > x) cnt[w] += step;
+            int rank = lane;
+            unsigned long long above = runp[warp * 32 + lane];
+#pragma unroll
+            for (int w = 0; w < kRuns; ++w) {
+                if (w == warp) continue;
+                rank += cnt[w];
+                above += cnt[w] < 32 ? runp[w * 32 + cnt[w]] : warp_sums[w];
             }
             // kept iff the mass ranked above is still below theta (the greedy
             // prefix) and, under the budget, the rank is below the cap
-            in = (disabled || above < theta) && rank < cap;
+            const int ex = 1023 - (int)((x - 1ull) & 1023ull);
+            in_flag[ex] = (disabled || above < theta) && rank < cap;
         }
+        __syncthreads();
+        const bool in = renorm ? (e < E && in_flag[e]) : tch;
         const uint32_t word = __ballot_sync(0xffffffffu, in);
         if (lane == 0 && warp < words) incore[warp] = word;
     } else {
@@ -263,35 +292,45 @@ __device__ __forceinline__ void coreset_block(const CoresetArgs& a, int b, Cores
     __syncthreads();
     int c = 0;
     for (int w = 0; w < words; ++w) c += __popc(incore[w]);
-    __syncthreads();
     for (int w = tid; w < words; w += blockDim.x) a.keep[(size_t)b * words + w] = incore[w];
     if (tid == 0) a.core_size[b] = c;
-    // renormalise rows: a warp per row, lane j holding slot j (k <= 32); the sum
-    // of the surviving weights is taken in rank order, one fp32 add at a time
+    // renormalise rows: lanes in groups of kp (the power of two >= k), a row
+    // per group and 32 / kp rows per warp at a time, lane j of a group holding
+    // slot j; the sum of the surviving weights is taken in rank order, one
+    // fp32 add at a time
     int empty = 0;
     {
         const int lane = tid & 31, nw = blockDim.x >> 5;
-        for (int r = r0 + (tid >> 5); r < r1; r += nw) {
-            const int e = lane < k ? a.topk_idx[(size_t)r * k + lane] : -1;
-            const float wj = lane < k ? a.topk_w[(size_t)r * k + lane] : 0.0f;
+        int kp = 1;
+        while (kp < k) kp <<= 1;
+        const int gpw = 32 / kp, grp = lane / kp, j = lane - grp * kp;
+        const uint32_t gmask = kp == 32 ? 0xFFFFFFFFu : ((1u << kp) - 1u);
+        for (int rb = r0 + (tid >> 5) * gpw; rb < r1; rb += nw * gpw) {
+            const int r = rb + grp;
+            const bool act = r < r1 && j < k;
+            const int p = (r - r0) * k + j;
+            const int e = act ? (cached ? sm.pe[p] : a.topk_idx[(size_t)r * k + j]) : -1;
+            const float wj = act ? (cached ? sm.pw[p] : a.topk_w[(size_t)r * k + j]) : 0.0f;
             float* wo = a.w_renorm + (size_t)r * k;
             if (!renorm) {
-                if (lane < k) wo[lane] = wj;
+                if (act) wo[j] = wj;
                 continue;
             }
             const bool in = e >= 0 && e < E && ((incore[e >> 5] >> (e & 31)) & 1u);
-            const uint32_t inm = __ballot_sync(0xffffffffu, in);
+            const uint32_t inm = (__ballot_sync(0xffffffffu, in) >> (grp * kp)) & gmask;
             float s = 0.0f;
-            for (int j = 0; j < k; ++j) {
-                const float v = __shfl_sync(0xffffffffu, wj, j);
-                if ((inm >> j) & 1u) s = __fadd_rn(s, v);
+            for (int jj = 0; jj < k; ++jj) {
+                const float v = __shfl_sync(0xffffffffu, wj, grp * kp + jj);
+                if ((inm >> jj) & 1u) s = __fadd_rn(s, v);
             }
-            if (s == 0.0f) {
-                if (lane < k) wo[lane] = 0.0f;
-                if (lane == 0) ++empty;
-                continue;
+            if (act) {
+                if (s == 0.0f) {
+                    wo[j] = 0.0f;
+                    if (j == 0) ++empty;
+                } else {
+                    wo[j] = in ? __fdiv_rn(wj, s) : 0.0f;
+                }
             }
-            if (lane < k) wo[lane] = in ? __fdiv_rn(wj, s) : 0.0f;
         }
     }
     if (empty) atomicAdd(&s_empty, empty);

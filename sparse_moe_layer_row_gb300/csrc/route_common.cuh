@@ -90,11 +90,15 @@ __device__ __forceinline__ float dot8_bf16(uint4 x, uint4 w, float acc) {
     return fma_bf16x2(x.w, w.w, acc);
 }
 
-// z -> z + bias, + 0, as the contract states.
-__device__ __forceinline__ float finish_logit(float dot, const float* bias_row, int e) {
+// z -> z + bias, + 0, as the contract states (the bias value already loaded).
+__device__ __forceinline__ float finish_logit_v(float dot, bool has_bias, float bias) {
     float z = dot;
-    if (bias_row) z = __fadd_rn(z, __ldg(bias_row + e));
+    if (has_bias) z = __fadd_rn(z, bias);
     return __fadd_rn(z, 0.0f);
+}
+
+__device__ __forceinline__ float finish_logit(float dot, const float* bias_row, int e) {
+    return finish_logit_v(dot, bias_row != nullptr, bias_row ? __ldg(bias_row + e) : 0.0f);
 }
 
 // In-lane bitonic sort of NI (a power of two) 64-bit values, descending.
@@ -191,15 +195,24 @@ __device__ __forceinline__ void route_topk_rows(const RouteArgs& a, int r0, int 
         const float* brow = a.bias ? a.bias + (size_t)find_block(a.off, a.nb, r) * a.E : nullptr;
         uint32_t key[NE], id[NE];
         uint32_t valid = 0, nonfinite = 0;
+        // every load first (one memory round trip), then the keys
+        float z[NE], bz[NE];
+#pragma unroll
+        for (int i = 0; i < NE; ++i) {
+            const int e = lane + 32 * i;
+            const int ec = e < a.E ? e : 0;
+            z[i] = __ldcg(a.logits + (size_t)r * a.E + ec);
+            bz[i] = brow ? __ldg(brow + ec) : 0.0f;
+        }
 #pragma unroll
         for (int i = 0; i < NE; ++i) {
             const int e = lane + 32 * i;
             id[i] = (uint32_t)e;
             key[i] = 0;
             if (e < a.E) {
-                const float z = finish_logit(__ldcg(a.logits + (size_t)r * a.E + e), brow, e);
-                if (!isfinite(z)) ++nonfinite;
-                key[i] = order_key(z);
+                const float zi = finish_logit_v(z[i], brow != nullptr, bz[i]);
+                if (!isfinite(zi)) ++nonfinite;
+                key[i] = order_key(zi);
                 valid |= 1u << i;
             }
         }
