@@ -168,17 +168,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def accounting(w: W.Workload, R: int, n_core_experts: int, n_pairs: int):
+def weight_bytes_per_element(qbits: int = 0) -> float:
+    """Bytes per expert weight as stored: bf16, or a b-bit code plus a bf16
+    scale per 32 weights."""
+    return 2.0 if not qbits else qbits / 8.0 + 2.0 / W.QBLOCK
+
+
+def accounting(w: W.Workload, R: int, n_core_experts: int, n_pairs: int, qbits: int = 0):
     """Algorithmic bytes and flops of one step and of one gate/up launch."""
     H, E, I, Is = w.H, w.E, w.I, w.Is
-    expert_bytes = 3 * H * I * 2
-    shared_bytes = 3 * H * Is * 2
+    wb = weight_bytes_per_element(qbits)
+    expert_bytes = 3 * H * I * wb
+    shared_bytes = 3 * H * Is * wb
     router_bytes = E * H * 2
     step_bytes = n_core_experts * expert_bytes + shared_bytes + router_bytes + 2 * R * H * 2
     step_flops = 2.0 * R * H * E + n_pairs * 6.0 * H * I + R * 6.0 * H * Is
     # gate/up launch: the touched experts' and the shared expert's gate and up
     # weights plus the rows of x, each read once (intermediates are not counted)
-    gu_bytes = n_core_experts * 2 * H * I * 2 + 2 * H * Is * 2 + R * H * 2
+    gu_bytes = n_core_experts * 2 * H * I * wb + 2 * H * Is * wb + R * H * 2
     # gate/up FLOPs: two H x I products per surviving pair, two H x Is per row
     gu_flops = 4.0 * H * (n_pairs * I + R * Is)
     weight_bytes = n_core_experts * expert_bytes + shared_bytes + router_bytes
@@ -424,10 +431,10 @@ def measure(w: W.Workload, T, layer, steps: int, tm: StepTimer, clock_index: int
                 pairs=pairs, clocks=clk.summary(), y=y)
 
 
-def summarize(w: W.Workload, m: dict, peaks: dict, ws: int = 1) -> dict:
+def summarize(w: W.Workload, m: dict, peaks: dict, ws: int = 1, qbits: int = 0) -> dict:
     """Throughput, the gate/up kernel's roofline and the whole step's fraction."""
     from sparse_moe_layer_row_gb300 import moe_block
-    acc = accounting(w, w.R, len(m["used"]), m["pairs"])
+    acc = accounting(w, w.R, len(m["used"]), m["pairs"], qbits)
     t_step = m["total_ms"] / 1e3 / m["steps"]
     t_gu = statistics.mean(m["kern"]["gate_up"]) / 1e3
     traffic = recorded_traffic(w.name)
@@ -444,7 +451,8 @@ def summarize(w: W.Workload, m: dict, peaks: dict, ws: int = 1) -> dict:
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "algorithmic_bytes_per_launch": acc["gu_bytes"]}
-    gu_kernel = ("k_gemm<kGateUp, 32, 5> (tcgen05)" if w.R <= moe_block.SMALL_ROWS
+    gu_kernel = (f"k_gemm<kGateUp, 32, 5, {qbits}> (tcgen05, {qbits}-bit experts)" if qbits
+                 else "k_gemm<kGateUp, 32, 5> (tcgen05)" if w.R <= moe_block.SMALL_ROWS
                  else "k_gateup_pair (tcgen05 cta_group::2)")
     roof = {"bound": roof.pop("bound"), "kernel": gu_kernel, **roof,
             "traffic": traffic, "launch_us": t_gu * 1e6, "peak_source": peaks["source"]}
@@ -468,9 +476,11 @@ def summarize(w: W.Workload, m: dict, peaks: dict, ws: int = 1) -> dict:
 
 # Workloads timed in the same run next to the main one (their own JSON object,
 # not the headline): the 512-row Zipf batch, 2048 rows in 32-row blocks with
-# the coreset on and off, and the 8192-row prefill shape.
+# the coreset on and off, and the 8192-row prefill shape; on request, the main
+# workload's layer with 8-bit and 4-bit experts (same router and inputs).
 EXTRA_WORKLOADS = ("blocks16x32-zipf1.1", "rows2048-b32-tau0.9", "rows2048-b32-tau1",
                    "prefill8192-b32")
+QUANT_BITS = (8, 4)
 
 
 def tensors_like(we: W.Workload, base: W.Workload, T, dev, x_seed: int):
@@ -618,6 +628,20 @@ def run_gpu(args, w: W.Workload):
             extra[name] = se
             del le, Te, me
             torch.cuda.empty_cache()
+        for bits in (QUANT_BITS if args.quant_workloads else ()):
+            qe = W.quantize_experts(T, bits)
+            lq = moe_block.MoeBlockLayer.quantized(T.w_router, qe, k=w.k, max_rows=w.R,
+                                                   max_blocks=w.nb)
+            mq = measure(w, T, lq, args.extra_steps, tm, local, args.warmup)
+            sq = summarize(w, mq, peaks, qbits=bits)
+            sq["gpu_launches_per_step"] = kernels_per_step(w)
+            sq["config"] = {"rows": w.R, "blocks": w.nb, "block_rows": w.block_rows[0],
+                            "coreset_mass": w.tau, "expert_bits": bits,
+                            "expert_bytes_per_weight": weight_bytes_per_element(bits),
+                            "steps": args.extra_steps}
+            extra[f"{w.name}-q{bits}"] = sq
+            del lq, qe, mq
+            torch.cuda.empty_cache()
         line["workloads"] = extra
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, x_seed, budget_s=args.cpu_budget)
@@ -636,6 +660,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quant-workloads", action="store_true",
+                    help="also time the main workload's layer with 8-bit and 4-bit experts")
     ap.add_argument("--no-extra-workloads", action="store_true",
                     help="skip the other full-size workloads (reported under workloads)")
     ap.add_argument("--extra-steps", type=int, default=30,
