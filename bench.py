@@ -344,6 +344,9 @@ def measure(w: W.Workload, T, layer, steps: int, tm: StepTimer, clock_index: int
     calls as separate graphs.  Returns the raw times and the routing facts."""
     stream, dev = tm.stream, tm.dev
     y = torch.empty(w.R, w.H, dtype=torch.bfloat16, device=dev)
+    # the layer's weights and buffers (zeroed workspace, quantised codes) were
+    # made on the default stream: finish that work before `stream` uses them
+    torch.cuda.synchronize()
 
     def step():
         layer(T.x, T.block_offsets, w.tau, bias=T.bias, y=y)

@@ -79,6 +79,9 @@ enum {
     MOE_STATUS_EMPTY_ROWS = 3,        /* rows left with only the shared expert */
     MOE_STATUS_WAIT_TIMEOUT = 4,      /* GEMM pipeline waits that gave up */
     MOE_STATUS_NONFINITE_OUTPUT = 5,  /* 256-column pieces of y with a non-finite value */
+    MOE_STATUS_BAD_UNIT = 6,          /* GEMM work units found invalid and skipped: the
+                                         workspace was overwritten during the call (e.g.
+                                         by work on another stream not ordered before it) */
     MOE_STATUS_WORDS = 8
 };
 

@@ -119,11 +119,19 @@ __device__ __forceinline__ void store_h(__nv_bfloat16* out, bool shared, int ld,
     }
 }
 
-// Weights bf16(q * d) of a pair of codes (the product is exact in fp32: at
-// most 7 + 8 significant bits; one rounding, to nearest even).
-__device__ __forceinline__ uint32_t dq_pair(int q0, int q1, float d) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn((float)q0 * d, (float)q1 * d);
+// Weights bf16(q * d) of a pair of codes given as exact floats (the product
+// is exact in fp32: at most 8 + 8 significant bits; one rounding, to nearest
+// even).
+__device__ __forceinline__ uint32_t dq_pair(float q0, float q1, float d) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(q0 * d, q1 * d);
     return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// A code as an exact float without an integer-to-float conversion: the byte
+// of `xb` that `sel` picks (the code plus `bias`, as an unsigned byte) goes
+// into the low mantissa bits of 2^23, and 2^23 + bias is subtracted (exact).
+__device__ __forceinline__ float code_float(uint32_t xb, uint32_t sel, float two23_plus_bias) {
+    return __uint_as_float(__byte_perm(xb, 0x4B000000u, sel)) - two23_plus_bias;
 }
 
 // Dequantise one stage: 128 weight rows x 64 K of codes (row r at raw + r * 64
@@ -148,11 +156,11 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* raw, const __nv_bflo
             const float d = __bfloat162float(sc[((r / SR) * 2 + (c >> 1)) * SR + (r % SR)]);
             uint32_t o[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t x = wd[i >> 1];
-                const int sh = (i & 1) * 16;
-                o[i] = dq_pair((int)((int32_t)(x << (24 - sh)) >> 24),
-                               (int)((int32_t)(x << (16 - sh)) >> 24), d);
+            for (int w4 = 0; w4 < 4; ++w4) {   // codes 4 w4 .. 4 w4 + 3 (bytes, in order)
+                const uint32_t xb = wd[w4] ^ 0x80808080u;   // q + 128 per byte
+                constexpr float kB = 8388736.0f;             // 2^23 + 128
+                o[2 * w4] = dq_pair(code_float(xb, 0x7650u, kB), code_float(xb, 0x7651u, kB), d);
+                o[2 * w4 + 1] = dq_pair(code_float(xb, 0x7652u, kB), code_float(xb, 0x7653u, kB), d);
             }
             *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -161,12 +169,14 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* raw, const __nv_bflo
             const float d = __bfloat162float(sc[((r / SR) * 2 + c) * SR + (r % SR)]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {   // 16-byte output chunk 4c + j: elements 8j .. 8j + 7
-                const uint32_t x = wd[j];
+                const uint32_t xb = wd[j] ^ 0x88888888u;     // q + 8 per nibble
+                const uint32_t lo = xb & 0x0F0F0F0Fu;          // byte i: element 2i
+                const uint32_t hi = (xb >> 4) & 0x0F0F0F0Fu;   // byte i: element 2i + 1
+                constexpr float kB = 8388616.0f;               // 2^23 + 8
                 uint32_t o[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    o[i] = dq_pair((int)((int32_t)(x << (28 - 8 * i)) >> 28),
-                                   (int)((int32_t)(x << (24 - 8 * i)) >> 28), d);
+                    o[i] = dq_pair(code_float(lo, 0x7650u + i, kB), code_float(hi, 0x7650u + i, kB), d);
                 *reinterpret_cast<uint4*>(row + (((4 * c + j) ^ (r & 7)) << 4)) =
                     make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -292,6 +302,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         };
         for (int u = ufirst; ok && u < nunits; u += nact) {
             const int4 un = __ldg(a.units + u);
+            if (!unit_valid(un, a, NMAX, MODE == kDown, C::kGURows)) continue;
             const int g = un.x, m = un.y, start = un.z, n = un.w;
             // B rows actually loaded: gathered units load ceil(n/4) rows x 4; the
             // others whole boxes of kBoxRows.  Rows of the tile past n only feed
@@ -424,6 +435,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             bool ok = true;
             for (int u = ufirst; ok && u < nunits; u += nact) {
                 const int4 un = __ldg(a.units + u);
+                if (!unit_valid(un, a, NMAX, MODE == kDown, C::kGURows)) {
+                    status_add(a.status, MOE_STATUS_BAD_UNIT, 1);
+                    continue;
+                }
                 const int g = un.x, n = un.w;
                 const int n16 = (n + 15) & ~15;
                 const int K = MODE == kGateUp ? a.H
@@ -483,7 +498,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         uint32_t phase = 0, aphase = 0;
         bool ok = true;
         for (int u = ufirst; ok && u < nunits; u += nact) {
-            const int g = __ldg(a.units + u).x;
+            const int4 un = __ldg(a.units + u);
+            if (!unit_valid(un, a, NMAX, MODE == kDown, C::kGURows)) continue;
+            const int g = un.x;
             const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
             for (int kb = 0; kb < (K >> 6); ++kb) {
                 if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs) ||
@@ -510,6 +527,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         bool alive = true;
         for (int u = ufirst; alive && u < nunits; u += nact) {
             const int4 un = __ldg(a.units + u);
+            if (!unit_valid(un, a, NMAX, MODE == kDown, C::kGURows)) continue;
             const int g = un.x, m = un.y, start = un.z, n = un.w;
             const int n16 = (n + 15) & ~15;
             // down: the unit's pair weights, lane l of wreg[j] holding pair

@@ -276,6 +276,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             bool ok = true;
             for (int u = c0; ok && u < nunits; u += nc) {
                 const int4 un = __ldg(a.units + u);
+                if (!unit_valid(un, a, kLargeNGU, false, 128)) continue;
                 const int g = un.x, m = un.y;
                 for (int kb = 0; kb < (a.H >> 6); ++kb) {
                     if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) {
@@ -310,6 +311,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             uint32_t phase = 0;
             bool ok = true;
             for (int u = c0; ok && u < nunits; u += nc) {
+                if (!unit_valid(__ldg(a.units + u), a, kLargeNGU, false, 128)) continue;
                 for (int kb = 0; kb < (a.H >> 6); ++kb) {
                     // this CTA's x tile and weight half, both read by rank 0's MMA
                     if (!mbar_wait_bounded(bfull + stage, phase, abort_flag, kWaitNs) ||
@@ -331,6 +333,10 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int u = c0; ok && u < nunits; u += nc) {
+                if (!unit_valid(__ldg(a.units + u), a, kLargeNGU, false, 128)) {
+                    status_add(a.status, MOE_STATUS_BAD_UNIT, 1);
+                    continue;
+                }
                 if (!mbar_wait_cluster_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitNs)) {
                     give_up();
                     break;
@@ -378,6 +384,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
         bool ok = true;
         for (int u = c0; ok && u < nunits; u += nc) {
             const int4 un = __ldg(a.units + u);
+            if (!unit_valid(un, a, kLargeNGU, false, 128)) continue;
             const int g = un.x, start = un.z + rbase;
             const int nr = min(128, max(0, un.w - rbase));
             const __nv_bfloat16* src[8];
@@ -414,6 +421,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
         uint32_t acc_phase = 0;
         for (int u = c0; u < nunits; u += nc) {
             const int4 un = __ldg(a.units + u);
+            if (!unit_valid(un, a, kLargeNGU, false, 128)) continue;
             const int g = un.x, m = un.y, start = un.z + rbase;
             const int nr = min(128, max(0, un.w - rbase));
             const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitNs);

@@ -109,6 +109,21 @@ struct GemmArgs {
     const int32_t* shared_rows;  // row of x of the shared expert's i-th row (NULL: i)
     uint64_t wait_ns;     // limit of a pipeline wait (0: the built-in limit)
 };
+// A unit (expert g, weight tile m, first row `start`, n rows) as the scatter
+// writes it: g in [0, E] (E: the shared expert), 1 <= n <= nmax, rows inside
+// h / hs and the staging buffer, m inside the weights.  Every role of a GEMM
+// checks each unit it reads and skips one that fails (it can only fail if the
+// workspace was overwritten while the call ran), so such a unit never drives a
+// zero-width MMA or a store past a buffer; one role counts it.
+__device__ __forceinline__ bool unit_valid(const int4 un, const GemmArgs& a, int nmax, bool down,
+                                           int gu_rows) {
+    const int g = un.x, m = un.y, start = un.z, n = un.w;
+    if (g < 0 || g > a.E || n < 1 || n > nmax || start < 0) return false;
+    const int cap = g == a.E ? a.ld_x - a.shared_row0 : a.shared_row0;
+    if (start > cap - n) return false;
+    const int mt = down ? a.H / 128 : ((g == a.E ? a.Is : a.I) + gu_rows - 1) / gu_rows;
+    return m >= 0 && m < mt;
+}
 struct GemmMaps {
     CUtensorMap a0, a1, a2, a3, b0, b1;
     CUtensorMap bg;   // x with a one-row box: TMA gather4 of routed rows (small batches)

@@ -17,7 +17,7 @@ from . import build as _build
 
 MOE_OK = 0
 STATUS_NAMES = ("nonfinite_logits", "bad_expert_id", "bad_offsets", "empty_rows", "wait_timeout",
-                "nonfinite_output")
+                "nonfinite_output", "bad_unit")
 STATUS_WORDS = 8
 
 
