@@ -258,9 +258,11 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         pdl_trigger();
     }
     const int nunits = __ldg(a.n_units);
-    // gate/up: balanced rounds (common.cuh); the down GEMM keeps the plain
-    // stride, which its unit order is laid out for (measured slower otherwise)
-    const int nact = MODE == kGateUp ? active_workers(nunits, gridDim.x) : (int)gridDim.x;
+    // balanced rounds (common.cuh), except the large down GEMM, which keeps the
+    // plain stride its unit order is laid out for (neighbouring CTAs share rows
+    // of h; measured slower otherwise)
+    const int nact = (MODE == kGateUp || NMAX == kSmallN) ? active_workers(nunits, gridDim.x)
+                                                           : (int)gridDim.x;
     const int ufirst = (int)blockIdx.x < nact ? (int)blockIdx.x : nunits;
 
     auto give_up = [&]() {
