@@ -17,13 +17,12 @@
 // K step; here each SM reads 16 KB + 16 KB for the same work, so the pair
 // needs two thirds of the operand bandwidth from L2 per flop.
 //
-// Roles (320 threads per CTA):
+// Roles (352 threads per CTA):
 //   warp 0 lane 0   TMA producer of the CTA's weight half, completing on the
 //                   CTA's own `full` barrier
 //   warp 1          TMEM allocation (both ranks); lane 0 of rank 0 issues the
 //                   MMAs and the commits, which arrive on the barriers of both
-//                   ranks (stage `empty`, accumulator `tfull`); lane 0 of
-//                   rank 1 forwards its CTA's x stages to rank 0 (below)
+//                   ranks (stage `empty`, accumulator `tfull`)
 //   warps 2..5      epilogue: TMEM -> silu(g) * u -> h (bf16; hi + lo bf16 for
 //                   the shared expert) in 16-byte stores; release the
 //                   accumulator on rank 0's `tempty`
@@ -31,11 +30,12 @@
 //                   thread's copies arrive on its own CTA's `bfull` when they
 //                   land (cp.async.mbarrier.arrive), so a loader never waits
 //                   for its own copies and the ring depth is the only limit on
-//                   the copies in flight.  In rank 1 one thread waits for that
-//                   barrier and for the CTA's `full` (its weight half), fences
-//                   the CTA's x tile for the async proxy and arrives on rank
-//                   0's `pfull`; in rank 0 the MMA thread waits for its own
-//                   `full` and `bfull` and for `pfull`, and fences its own tile.
+//                   the copies in flight
+//   warp 10 lane 0  forwarder: waits for the CTA's `bfull` and `full` of a
+//                   stage, fences the CTA's x tile for the async proxy and
+//                   arrives on rank 0's `pfull` (two arrivals per stage, one
+//                   per rank); the MMA thread waits for `pfull` alone, so no
+//                   fence and only one wait sit between its stages.
 // Each stage holds a weight half and an x tile (32 KB); both are freed by the
 // same commit.  Every wait is bounded; a role that gives up raises the CTA's
 // abort flag and the device status counter, and both CTAs leave their loops.
@@ -54,7 +54,7 @@ constexpr uint64_t kPairWaitNs = 2000000000ull;   // 2 s: far beyond any legal w
 constexpr uint64_t kPairDrainNs = 200000000ull;   // 0.2 s when draining after an abort
 
 constexpr int kPStages = 7;
-constexpr int kPThreads = 320;
+constexpr int kPThreads = 352;
 constexpr int kPTile = 128 * 128;        // 128 rows x 64 bf16 (one SW128 tile)
 constexpr int kPStageBytes = 2 * kPTile; // weight half, then x
 constexpr int kPBarOff = kPStages * kPStageBytes;
@@ -234,7 +234,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(full + s, 1);
             mbar_init(bfull + s, 128);   // the loader threads' copies
-            mbar_init(pfull + s, 1);     // rank 1's forwarder
+            mbar_init(pfull + s, 2);     // the forwarders of both ranks
             mbar_init(empty + s, 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -304,28 +304,6 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             }
         }
     } else if (warp == 1) {
-        if (!leader && lane == 0) {
-            // ------------------------------------------ x-stage forwarder (rank 1)
-            const uint32_t pfull0 = mapa_shared(smem_u32(pfull), 0);
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int u = c0; ok && u < nunits; u += nc) {
-                if (!unit_valid(__ldg(a.units + u), a, kLargeNGU, false, 128)) continue;
-                for (int kb = 0; kb < (a.H >> 6); ++kb) {
-                    // this CTA's x tile and weight half, both read by rank 0's MMA
-                    if (!mbar_wait_bounded(bfull + stage, phase, abort_flag, kWaitNs) ||
-                        !mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs)) {
-                        give_up();
-                        ok = false;
-                        break;
-                    }
-                    fence_proxy_async_smem();   // the x tile was written by cp.async
-                    mbar_arrive_cluster(pfull0 + stage * 8);
-                    if (++stage == kPStages) { stage = 0; phase ^= 1u; }
-                }
-            }
-        }
         if (leader && lane == 0) {
             // ------------------------------------------------------ MMA issuer
             const uint32_t idesc = idesc_bf16_f32(256, 256);
@@ -344,14 +322,12 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * kPAccCols);
                 for (int kb = 0; kb < (a.H >> 6); ++kb) {
-                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs) ||
-                        !mbar_wait_bounded(bfull + stage, phase, abort_flag, kWaitNs) ||
-                        !mbar_wait_cluster_bounded(pfull + stage, phase, abort_flag, kWaitNs)) {
+                    // both ranks' x tiles and weight halves (the forwarders)
+                    if (!mbar_wait_cluster_bounded(pfull + stage, phase, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
                         break;
                     }
-                    fence_proxy_async_smem();   // this CTA's x tile, written by cp.async
                     tc_fence_after();
                     const uint32_t sW = sbase + stage * kPStageBytes;
                     const uint32_t sX = sW + kPTile;
@@ -372,7 +348,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             tc_commit_pair_local(dbar);
             if (!mbar_wait_bounded(dbar, 0, never, kPairDrainNs)) give_up();
         }
-    } else if (warp >= 6) {
+    } else if (warp >= 6 && warp < 10) {
         // ----------------------------------------------------------- x loaders
         // Row i of the CTA's part of a unit is copied by 8 threads, 16 bytes
         // each, into the 128-byte swizzled row of the x tile: chunk c of row i
@@ -413,6 +389,31 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
             }
         }
         cp_async_wait_all();  // nothing of this thread lands after the loop
+    } else if (warp == 10) {
+        if (lane == 0) {
+            // ------------------------------------------- x-stage forwarder
+            // Once the CTA's x tile and weight half of a stage have landed, fence
+            // the x tile (written by cp.async) for the async proxy and arrive on
+            // rank 0's `pfull`; the MMA thread waits for that barrier alone.
+            const uint32_t pfull0 = mapa_shared(smem_u32(pfull), 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = c0; ok && u < nunits; u += nc) {
+                if (!unit_valid(__ldg(a.units + u), a, kLargeNGU, false, 128)) continue;
+                for (int kb = 0; kb < (a.H >> 6); ++kb) {
+                    if (!mbar_wait_bounded(bfull + stage, phase, abort_flag, kWaitNs) ||
+                        !mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();   // the x tile was written by cp.async
+                    mbar_arrive_cluster(pfull0 + stage * 8);
+                    if (++stage == kPStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
