@@ -215,7 +215,7 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
         gu.s0 = gu.s1 = gu.s2 = gu.s3 = p->tm_wg;   // unused by the bf16 kernels
         dn.s0 = dn.s1 = dn.s2 = dn.s3 = p->tm_wd;
     }
-    const uint32_t box = su ? 16 : 64;   // B rows per TMA box (see k_gemm)
+    const uint32_t box = su ? 16 : 256;   // B rows per TMA box (see k_gemm)
     bool good = encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
                 encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
                 encode_bf16(&dn.b0, at<void>(workspace, L.h), (uint64_t)d.I, (uint64_t)L.max_pairs, 0,

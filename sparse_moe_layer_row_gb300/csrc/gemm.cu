@@ -67,9 +67,12 @@ struct GemmCfg {
     // traded in the epilogue
     static_assert(MODE == kDown || NMAX == kSmallN, "large gate/up runs in gemm_pair.cu");
     static constexpr int kGURows = 64;  // intermediate rows per gate/up unit
-    // rows per B box: 16 for the streaming shape, 64 for the large shape (fewer
-    // TMA instructions per stage; NMAX is a multiple of it)
-    static constexpr int kBoxRows = NMAX >= 64 ? 64 : 16;
+    // rows per B box: 16 for the streaming shape; the whole 256-row tile in one
+    // box for the large shape (NMAX is a multiple of it).  Each TMA instruction
+    // costs the producer about 200 cycles to issue under load, which bound the
+    // large down GEMM's stage rate with four 64-row boxes; the rows past the
+    // unit's count come from L2 (or read as zeros past the end of h).
+    static constexpr int kBoxRows = NMAX >= 256 ? 256 : NMAX >= 64 ? 64 : 16;
     static constexpr int kABytes = 128 * 128;
     // down, streaming shape: the shared expert's lo part of h rides in the same
     // stage as its hi part (a second MMA per K step); the large shape runs the
