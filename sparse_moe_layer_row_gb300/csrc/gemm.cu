@@ -95,8 +95,11 @@ struct GemmCfg {
         kQuant ? (kBBytes + kRawBytes + kScaleBytes + 1023) / 1024 * 1024 : kABytes + kBBytes;
     static constexpr int kAOff = STAGES * kStageBytes;                 // quantised: the A slots
     static constexpr int kXchgOff = kAOff + kNA * kABytes;
-    // gate/up: g <-> u exchange; down: the unit's fp16 output tile
-    static constexpr int kXchgBytes = MODE == kGateUp ? 2 * 64 * 9 * 4 : NMAX * 128 * 2;
+    // down: pairs of the output tile staged at a time (the large shape in two
+    // halves, so the space saved holds one more stage)
+    static constexpr int kStageRows = MODE == kDown && NMAX > 128 ? 128 : NMAX;
+    // gate/up: g <-> u exchange; down: fp16 output rows of kStageRows pairs
+    static constexpr int kXchgBytes = MODE == kGateUp ? 2 * 64 * 9 * 4 : kStageRows * 128 * 2;
     static constexpr int kRowsOff = kXchgOff + kXchgBytes;             // gate/up: rows of x of a unit
     static constexpr int kRowsBytes = MODE == kGateUp && NMAX == kSmallN ? NMAX * 4 : 0;
     static constexpr int kBarOff = kRowsOff + kRowsBytes;
@@ -597,9 +600,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 }
             } else {
                 // Weighted fp16 outputs of the unit's pairs, staged in shared
-                // memory ([pair][128 hidden]) so each pair's 128 columns leave as
-                // one 256-byte segment; the accumulator is released before the
-                // copy-out.  fp16 holds |v| < 65504: each warp owns a 32-column
+                // memory ([pair][128 hidden]) kStageRows pairs at a time, so each
+                // pair's 128 columns leave as one 256-byte segment; the
+                // accumulator is released before the last part's copy-out.
+                // fp16 holds |v| < 65504: each warp owns a 32-column
                 // quarter (its TMEM lane quadrant) of every pair, and a quarter
                 // whose largest finite magnitude is 2^15 or more is stored as
                 // v * 2^-s with the smallest s that brings that magnitude below
@@ -613,63 +617,74 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                 const int hl = q * 32 + lane;
                 const size_t row0 = (size_t)(g == a.E ? a.shared_row0 : 0) + start;
                 uint8_t* xq = a.ysx + (size_t)(m * 4 + q) * a.ld_x + row0;  // this quarter's exponents
+                const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue warps
                 bool any_big = false;
+                constexpr int kParts = NMAX / C::kStageRows, kGroups = C::kStageRows / 32;
 #pragma unroll
-                for (int j = 0; j < NMAX / 32; ++j) {
-                    const int c = 32 * j;
-                    if (c >= n16) break;
-                    float v[32];
-                    __syncwarp();  // tcgen05.ld is warp-collective
-                    // columns c .. c + 31 (those past n16 are inside the
-                    // accumulator and never copied out)
-                    tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(c + 16), v, v + 16);
-                    float mx = 0.0f;   // fmaxf skips NaN: the tail's 0 * garbage
+                for (int hp = 0; hp < kParts; ++hp) {
+                    const int p0 = hp * C::kStageRows;   // first pair of this part
+                    if (p0 >= n16) break;
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        v[t] *= __shfl_sync(0xffffffffu, wreg[j], t);
-                        mx = fmaxf(mx, fabsf(v[t]));
-                    }
-                    uint32_t my_s = 0;  // lane t: the exponent of pair c + t
-                    if (__any_sync(0xffffffffu, mx >= 32768.0f)) {
-                        any_big = true;
+                    for (int jj = 0; jj < kGroups; ++jj) {
+                        const int j = hp * kGroups + jj;
+                        const int c = 32 * j;
+                        if (c >= n16) break;
+                        float v[32];
+                        __syncwarp();  // tcgen05.ld is warp-collective
+                        // columns c .. c + 31 (those past n16 are inside the
+                        // accumulator and never copied out)
+                        tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(c + 16), v, v + 16);
+                        float mx = 0.0f;   // fmaxf skips NaN: the tail's 0 * garbage
 #pragma unroll
                         for (int t = 0; t < 32; ++t) {
-                            const uint32_t ab = __float_as_uint(v[t]) & 0x7FFFFFFFu;
-                            const uint32_t mb = __reduce_max_sync(0xffffffffu, ab < 0x7F800000u ? ab : 0u);
-                            const int sh = (int)(mb >> 23) - 141;   // biased exponent - (127 + 14)
-                            const uint32_t st = sh > 0 ? (uint32_t)sh : 0u;
-                            v[t] *= __uint_as_float((127u - st) << 23);   // 2^-s, exact
-                            if (lane == t) my_s = st;
+                            v[t] *= __shfl_sync(0xffffffffu, wreg[j], t);
+                            mx = fmaxf(mx, fabsf(v[t]));
                         }
-                    }
+                        uint32_t my_s = 0;  // lane t: the exponent of pair c + t
+                        if (__any_sync(0xffffffffu, mx >= 32768.0f)) {
+                            any_big = true;
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) xs[(c + t) * 128 + hl] = __float2half_rn(v[t]);
-                    if (c + lane < n) xq[c + lane] = (uint8_t)my_s;
+                            for (int t = 0; t < 32; ++t) {
+                                const uint32_t ab = __float_as_uint(v[t]) & 0x7FFFFFFFu;
+                                const uint32_t mb = __reduce_max_sync(0xffffffffu, ab < 0x7F800000u ? ab : 0u);
+                                const int sh = (int)(mb >> 23) - 141;   // biased exponent - (127 + 14)
+                                const uint32_t st = sh > 0 ? (uint32_t)sh : 0u;
+                                v[t] *= __uint_as_float((127u - st) << 23);   // 2^-s, exact
+                                if (lane == t) my_s = st;
+                            }
+                        }
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) xs[(c - p0 + t) * 128 + hl] = __float2half_rn(v[t]);
+                        if (c + lane < n) xq[c + lane] = (uint8_t)my_s;
+                    }
+                    if (hp == kParts - 1 || p0 + C::kStageRows >= n16) {
+                        // the last TMEM read of the unit: hand the accumulator back
+                        if (any_big && lane == 0) *a.scaled = 1;
+                        tc_fence_before();
+                        mbar_arrive(tempty + acc);
+                        released = true;
+                    }
+                    mbar_arrive(xbar);
+                    if (__any_sync(0xffffffffu, !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitNs))) {
+                        give_up();
+                        alive = false;
+                        break;
+                    }
+                    const int np = min(C::kStageRows, n - p0);   // pairs of this part
+                    for (int idx = et; idx < np * 16; idx += 128) {  // np rows x 16 segments of 16 B
+                        const int t = idx >> 4, seg = idx & 15;
+                        const uint4 val = *reinterpret_cast<const uint4*>(xs + t * 128 + seg * 8);
+                        *reinterpret_cast<uint4*>(a.ys + (row0 + p0 + t) * a.H + m * 128 + seg * 8) = val;
+                    }
+                    mbar_arrive(xbar + 1);  // the rows are rewritten by the next part
+                    if (__any_sync(0xffffffffu,
+                                   !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitNs))) {
+                        give_up();
+                        alive = false;
+                        break;
+                    }
+                    xphase ^= 1u;
                 }
-                if (any_big && lane == 0) *a.scaled = 1;
-                tc_fence_before();
-                mbar_arrive(tempty + acc);
-                released = true;
-                mbar_arrive(xbar);
-                if (__any_sync(0xffffffffu, !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitNs))) {
-                    give_up();
-                    alive = false;
-                    break;
-                }
-                const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue warps
-                for (int idx = et; idx < n * 16; idx += 128) {  // n rows x 16 segments of 16 B
-                    const int t = idx >> 4, seg = idx & 15;
-                    const uint4 val = *reinterpret_cast<const uint4*>(xs + t * 128 + seg * 8);
-                    *reinterpret_cast<uint4*>(a.ys + (row0 + t) * a.H + m * 128 + seg * 8) = val;
-                }
-                mbar_arrive(xbar + 1);  // the tile is rewritten by the next unit
-                if (__any_sync(0xffffffffu,
-                               !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitNs))) {
-                    give_up();
-                    alive = false;
-                    break;
-                }
-                xphase ^= 1u;
             }
             if (!alive) break;
             if (!released) {
@@ -711,7 +726,7 @@ static cudaError_t set_attr() {
 // the large gate/up GEMM is k_gateup_pair).  Quantised weights stream with the
 // small shape at every row count.
 constexpr int kSmallStagesGU = 5, kSmallStagesDN = 4;
-constexpr int kLargeStagesDN = 3;
+constexpr int kLargeStagesDN = 4;
 constexpr int kSmallCtasPerSm = 2;
 
 cudaError_t gemm_set_attributes() {
