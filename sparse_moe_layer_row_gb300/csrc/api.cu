@@ -194,7 +194,7 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
     const int nt_dn = su ? kSmallN : kLargeNDown;
 
     ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
-                   su ? 64 : 128,
+                   su ? 64 : 128, su ? 128 : 256,
                    at<int32_t>(workspace, L.prank), at<int32_t>(workspace, L.hist),
                    at<int32_t>(workspace, L.count),
                    at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
@@ -215,7 +215,7 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
         gu.s0 = gu.s1 = gu.s2 = gu.s3 = p->tm_wg;   // unused by the bf16 kernels
         dn.s0 = dn.s1 = dn.s2 = dn.s3 = p->tm_wd;
     }
-    const uint32_t box = su ? 16 : 256;   // B rows per TMA box (see k_gemm)
+    const uint32_t box = su ? 16 : 128;   // B rows per TMA box (k_gemm; k_down_pair: a rank's half)
     bool good = encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
                 encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
                 encode_bf16(&dn.b0, at<void>(workspace, L.h), (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
@@ -285,6 +285,7 @@ moe_status moe_plan_create(const moe_dims* dims, const void* w_router, const voi
         e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e == cudaSuccess) e = gemm_set_attributes();
     if (e == cudaSuccess) e = gateup_pair_set_attributes(p->num_sms);
+    if (e == cudaSuccess) e = down_pair_set_attributes(p->num_sms);
     if (e == cudaSuccess) e = route_tc_set_attributes();
     if (e != cudaSuccess) {
         delete p;
@@ -338,6 +339,7 @@ moe_status moe_plan_create_quantized(const moe_dims* dims, const void* w_router,
         e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
     if (e == cudaSuccess) e = gemm_set_attributes();
     if (e == cudaSuccess) e = gateup_pair_set_attributes(p->num_sms);
+    if (e == cudaSuccess) e = down_pair_set_attributes(p->num_sms);
     if (e == cudaSuccess) e = route_tc_set_attributes();
     if (e != cudaSuccess) {
         delete p;

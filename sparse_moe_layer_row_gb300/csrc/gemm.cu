@@ -722,11 +722,10 @@ static cudaError_t set_attr() {
 
 // (rows per unit, pipeline depth) of each kernel shape: small = few rows per
 // expert (weight streaming: two CTAs per SM, each with its own ring, keep more
-// TMA streams in flight); large = many rows (tensor-core bound, one CTA per SM;
-// the large gate/up GEMM is k_gateup_pair).  Quantised weights stream with the
-// small shape at every row count.
+// TMA streams in flight); many rows per expert run on CTA pairs
+// (k_gateup_pair, k_down_pair).  Quantised weights stream with the small shape
+// at every row count.
 constexpr int kSmallStagesGU = 5, kSmallStagesDN = 4;
-constexpr int kLargeStagesDN = 4;
 constexpr int kSmallCtasPerSm = 2;
 
 cudaError_t gemm_set_attributes() {
@@ -736,8 +735,7 @@ cudaError_t gemm_set_attributes() {
     if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU, 8>()) != cudaSuccess) return e;
     if ((e = set_attr<kDown, kSmallN, kSmallStagesDN, 8>()) != cudaSuccess) return e;
     if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU, 4>()) != cudaSuccess) return e;
-    if ((e = set_attr<kDown, kSmallN, kSmallStagesDN, 4>()) != cudaSuccess) return e;
-    return set_attr<kDown, kLargeNDown, kLargeStagesDN>();
+    return set_attr<kDown, kSmallN, kSmallStagesDN, 4>();
 }
 
 cudaError_t launch_gemm(int mode, bool small, int qbits, const GemmMaps& mp, const GemmArgs& a,
@@ -755,8 +753,7 @@ cudaError_t launch_gemm(int mode, bool small, int qbits, const GemmMaps& mp, con
         return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStagesGU>(mp, a, grid, st)
                                : launch_one<kDown, kSmallN, kSmallStagesDN>(mp, a, grid, st);
     }
-    return mode == kGateUp ? launch_gateup_pair(mp, a, st)
-                           : launch_one<kDown, kLargeNDown, kLargeStagesDN>(mp, a, grid, st);
+    return mode == kGateUp ? launch_gateup_pair(mp, a, st) : launch_down_pair(mp, a, st);
 }
 
 }  // namespace moe

@@ -1,4 +1,5 @@
-// Gate/up GEMM for many rows per expert on a CTA pair (tcgen05 cta_group::2).
+// Gate/up GEMM (k_gateup_pair) and down GEMM (k_down_pair, below) for many
+// rows per expert on CTA pairs (tcgen05 cta_group::2).
 //
 // The same SwiGLU first half as k_gemm<kGateUp> (model card "Clover-35B-A3B-
 // Preview -- CMF", intro: 256 routed experts plus a shared expert), for units
@@ -480,6 +481,352 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------
+// Down GEMM for many pairs per expert on a CTA pair.
+//
+// A unit is (group g, 256 hidden outputs m, up to 256 pairs of the group).  Two
+// CTAs on neighbouring SMs run one tcgen05.mma.cta_group::2 of M = 256, N = 256
+// per 16 of K:
+//
+//   A (M = 256): W_down rows m * 256 + 128 r .. + 127 in rank r (TMA);
+//   B (N = 256): h rows start + 128 r .. + 127 of the unit's pairs in rank r
+//                (TMA; rows past the unit's count feed accumulator columns that
+//                are never read);
+//   D:           each CTA's TMEM holds its 128 hidden outputs x 256 pairs.
+//
+// A single-SM M = 128, N = 256 tile loads 16 KB of weights and 32 KB of h per
+// 64-wide K step; here each SM loads 16 + 16 KB for the same work, so six
+// stages fit beside the output staging.  For the shared expert, K runs over
+// [hi | lo] (2 Is columns of hs) while A wraps around its Is columns.  The
+// epilogue is the one of k_gemm<kDown>: each CTA scales its 128 outputs of
+// every pair by the pair's weight, stages them in fp16 (with a power-of-two
+// exponent per 32-column quarter beyond fp16's range) 128 pairs at a time and
+// copies them out in 256-byte row segments.
+//
+// Roles (224 threads per CTA):
+//   warp 0 lane 0   TMA producer of the CTA's A and B halves, completing on the
+//                   CTA's own `full`; the first stages' W_down tiles are issued
+//                   before the wait for the gate/up GEMM (their h is held back)
+//   warp 1          TMEM allocation (both ranks); lane 0 of rank 0 issues the
+//                   MMAs and the commits (stage `empty`, accumulator `tfull`,
+//                   multicast to both ranks)
+//   warps 2..5      epilogue; the accumulator is released on rank 0's `tempty`
+//   warp 6 lane 0   forwarder: waits for the CTA's `full` and arrives on rank
+//                   0's `pfull` (one arrival per rank and stage), which the MMA
+//                   thread waits for alone
+// Waits, abort and drain as in k_gateup_pair.
+constexpr int kDStages = 6;
+constexpr int kDThreads = 224;
+constexpr int kDStageBytes = 2 * kPTile;   // A half (weights), then B half (h)
+constexpr int kDStageRows = 128;           // pairs staged at a time
+constexpr int kDXchgOff = kDStages * kDStageBytes;
+constexpr int kDBarOff = kDXchgOff + kDStageRows * 128 * 2;
+constexpr int kDSmem = kDBarOff + 512 + 1024;
+static_assert(kDSmem <= 227 * 1024, "shared memory budget");
+static_assert(8 * (3 * kDStages + 7) + 12 <= 512, "barrier region");
+static_assert(kLargeNDown == 256, "N = 256: 128 pairs per rank");
+
+__global__ void __launch_bounds__(kDThreads, 1)
+k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
+            const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmHs,
+            GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;   // same offset in both CTAs
+    uint8_t* base = smem_raw + (sbase - raw);
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + kDBarOff);  // [S] own halves landed
+    uint64_t* pfull = full + kDStages;                               // [S] both ranks' (rank 0)
+    uint64_t* empty = pfull + kDStages;                              // [S] stage free (both)
+    uint64_t* tfull = empty + kDStages;                              // [2] accumulator ready (both)
+    uint64_t* tempty = tfull + 2;                                    // [2] accumulator free (rank 0)
+    uint64_t* xbar = tempty + 2;                                     // [2] epilogue warps (own)
+    uint64_t* dbar = xbar + 2;                                       // MMA drain (rank 0)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dbar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* never = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kDStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(pfull + s, 2);     // the forwarders of both ranks
+            mbar_init(empty + s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(tfull + i, 1);
+            mbar_init(tempty + i, 256);  // 128 epilogue threads of each CTA
+            mbar_init(xbar + i, 128);    // this CTA's epilogue threads
+        }
+        mbar_init(dbar, 1);
+        *abort_flag = 0;
+        *never = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_slot, kPTmemCols);
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised, TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmW); prefetch_tmap(&tmS); prefetch_tmap(&tmH); prefetch_tmap(&tmHs);
+    }
+    // Nothing written by the gate/up GEMM is touched before the wait, except by
+    // the producer, which reads only the unit list (written by the scatter,
+    // which the gate/up GEMM waited for before letting this kernel start) and
+    // the weights before its own wait.
+    if (warp != 0) {
+        pdl_wait();
+        pdl_trigger();
+    }
+    const int nunits = __ldg(a.n_units);
+    const int nc = (int)cluster_count();   // plain stride: neighbouring units share h
+    const int c0 = (int)cluster_id();
+    const int half = 128 * (int)rank;      // this CTA's rows of A and of B
+
+    auto give_up = [&]() {
+        if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
+    };
+    auto valid = [&](int4 un) { return unit_valid(un, a, kLargeNDown, true, 128, 256); };
+    const uint64_t kWaitNs = a.wait_ns ? a.wait_ns : kPairWaitNs;   // pipeline waits
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            struct HeldB { uint32_t sB; const CUtensorMap* map; int kc, row; uint64_t* bar; };
+            HeldB held[kDStages];
+            int nheld = 0;
+            bool waited = false;
+            auto release_held = [&]() {
+                pdl_wait();
+                pdl_trigger();
+                for (int i = 0; i < nheld; ++i)
+                    tma_load_2d(held[i].sB, held[i].map, held[i].kc, held[i].row, held[i].bar);
+                nheld = 0;
+                waited = true;
+            };
+            int stage = 0, nfills = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = c0; ok && u < nunits; u += nc) {
+                const int4 un = __ldg(a.units + u);
+                if (!valid(un)) continue;
+                const int g = un.x, m = un.y, start = un.z;
+                const bool sh = g == a.E;
+                const int Ka = sh ? a.Is : a.I;      // A's K extent
+                const int K = sh ? 2 * a.Is : a.I;   // B's: [hi | lo] for the shared expert
+                for (int kb = 0; kb < (K >> 6); ++kb) {
+                    if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sA = sbase + stage * kDStageBytes, sB = sA + kPTile;
+                    mbar_expect_tx(full + stage, (uint32_t)kDStageBytes);
+                    const int kca = (kb * 64) % Ka, rowA = m * 256 + half;
+                    if (sh) tma_load_2d(sA, &tmS, kca, rowA, full + stage);
+                    else tma_load_3d(sA, &tmW, kca, rowA, g, full + stage);
+                    const HeldB hb{sB, sh ? &tmHs : &tmH, kb * 64, start + half, full + stage};
+                    if (waited) tma_load_2d(hb.sB, hb.map, hb.kc, hb.row, hb.bar);
+                    else held[nheld++] = hb;
+                    if (!waited && nheld == kDStages) release_held();
+                    ++nfills;
+                    if (++stage == kDStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!waited) release_held();   // every posted byte count gets its copies
+            // drain: the last fill of every stage has landed (consumed or not)
+            for (int s = 0; s < kDStages; ++s) {
+                if (nfills < kDStages && s >= nfills) break;
+                const uint32_t par = s < stage ? phase : (phase ^ 1u);
+                if (!mbar_wait_bounded(full + s, par, never, kPairDrainNs)) give_up();
+            }
+        } else {
+            pdl_wait();
+            pdl_trigger();
+        }
+    } else if (warp == 1) {
+        if (leader && lane == 0) {
+            // ------------------------------------------------------ MMA issuer
+            const uint32_t idesc = idesc_bf16_f32(256, 256);
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int u = c0; ok && u < nunits; u += nc) {
+                const int4 un = __ldg(a.units + u);
+                if (!valid(un)) {
+                    status_add(a.status, MOE_STATUS_BAD_UNIT, 1);
+                    continue;
+                }
+                const int K = un.x == a.E ? 2 * a.Is : a.I;
+                if (!mbar_wait_cluster_bounded(tempty + acc, acc_phase ^ 1u, abort_flag, kWaitNs)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * kPAccCols);
+                for (int kb = 0; kb < (K >> 6); ++kb) {
+                    // both ranks' halves of the stage (the forwarders)
+                    if (!mbar_wait_cluster_bounded(pfull + stage, phase, abort_flag, kWaitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = sbase + stage * kDStageBytes, sB = sA + kPTile;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma_bf16_pair(d, smem_desc_sw128(sA + kk * 32), smem_desc_sw128(sB + kk * 32),
+                                         idesc, (kb | kk) != 0);
+                    tc_commit_pair(empty + stage);
+                    if (++stage == kDStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair(tfull + acc);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // drain: arrives (on this CTA's barrier) once every MMA issued
+            // above has completed
+            tc_commit_pair_local(dbar);
+            if (!mbar_wait_bounded(dbar, 0, never, kPairDrainNs)) give_up();
+        }
+    } else if (warp == 6) {
+        if (lane == 0) {
+            // ---------------------------------------------------- forwarder
+            const uint32_t pfull0 = mapa_shared(smem_u32(pfull), 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int u = c0; ok && u < nunits; u += nc) {
+                const int4 un = __ldg(a.units + u);
+                if (!valid(un)) continue;
+                const int K = un.x == a.E ? 2 * a.Is : a.I;
+                for (int kb = 0; kb < (K >> 6); ++kb) {
+                    if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster(pfull0 + stage * 8);
+                    if (++stage == kDStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        // This CTA's 128 hidden outputs mo = 256 m + 128 rank + (TMEM lane) of
+        // every pair of the unit, weighted by the pair's renormalised weight
+        // (1 for the shared expert), staged in fp16 ([pair][128]) 128 pairs at
+        // a time and copied out as one 256-byte segment per pair.  A 32-column
+        // quarter whose largest finite magnitude is 2^15 or more is stored as
+        // v * 2^-s (s to ysx, the call's `scaled` flag set; k_combine
+        // multiplies it back exactly), as in k_gemm<kDown>.
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
+        __half* xs = reinterpret_cast<__half*>(base + kDXchgOff);
+        const int hl = q * 32 + lane;
+        const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue warps
+        int acc = 0;
+        uint32_t acc_phase = 0, xphase = 0;
+        bool alive = true;
+        for (int u = c0; alive && u < nunits; u += nc) {
+            const int4 un = __ldg(a.units + u);
+            if (!valid(un)) continue;
+            const int g = un.x, start = un.z, n = un.w;
+            const int mcol = 2 * un.y + (int)rank;   // this CTA's 128-column tile of H
+            const int n16 = (n + 15) & ~15;
+            float wreg[8];   // lane l of wreg[j]: the weight of pair 32 j + l (0 past n)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = 32 * j + lane;
+                wreg[j] = t < n ? (g == a.E ? 1.0f : __ldg(a.pair_w + start + t)) : 0.0f;
+            }
+            const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitNs);
+            if (__any_sync(0xffffffffu, !ok)) { give_up(); break; }
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPAccCols);
+            const size_t row0 = (size_t)(g == a.E ? a.shared_row0 : 0) + start;
+            uint8_t* xq = a.ysx + (size_t)(mcol * 4 + q) * a.ld_x + row0;  // this quarter's exponents
+            bool any_big = false;
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+                const int p0 = hp * kDStageRows;   // first pair of this part
+                if (p0 >= n16) break;
+#pragma unroll
+                for (int jj = 0; jj < kDStageRows / 32; ++jj) {
+                    const int j = hp * (kDStageRows / 32) + jj;
+                    const int c = 32 * j;
+                    if (c >= n16) break;
+                    float v[32];
+                    __syncwarp();  // tcgen05.ld is warp-collective
+                    tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(c + 16), v, v + 16);
+                    float mx = 0.0f;   // fmaxf skips NaN: the tail's 0 * garbage
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        v[t] *= __shfl_sync(0xffffffffu, wreg[j], t);
+                        mx = fmaxf(mx, fabsf(v[t]));
+                    }
+                    uint32_t my_s = 0;  // lane t: the exponent of pair c + t
+                    if (__any_sync(0xffffffffu, mx >= 32768.0f)) {
+                        any_big = true;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            const uint32_t ab = __float_as_uint(v[t]) & 0x7FFFFFFFu;
+                            const uint32_t mb = __reduce_max_sync(0xffffffffu, ab < 0x7F800000u ? ab : 0u);
+                            const int sh = (int)(mb >> 23) - 141;   // biased exponent - (127 + 14)
+                            const uint32_t st = sh > 0 ? (uint32_t)sh : 0u;
+                            v[t] *= __uint_as_float((127u - st) << 23);   // 2^-s, exact
+                            if (lane == t) my_s = st;
+                        }
+                    }
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) xs[(c - p0 + t) * 128 + hl] = __float2half_rn(v[t]);
+                    if (c + lane < n) xq[c + lane] = (uint8_t)my_s;
+                }
+                if (hp == 1 || p0 + kDStageRows >= n16) {
+                    // the unit's last TMEM read: hand the accumulator back
+                    if (any_big && lane == 0) *a.scaled = 1;
+                    tc_fence_before();
+                    mbar_arrive_cluster(tempty0 + acc * 8);
+                }
+                mbar_arrive(xbar);
+                if (__any_sync(0xffffffffu, !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitNs))) {
+                    give_up();
+                    alive = false;
+                    break;
+                }
+                const int np = min(kDStageRows, n - p0);   // pairs of this part
+                for (int idx = et; idx < np * 16; idx += 128) {  // np rows x 16 segments of 16 B
+                    const int t = idx >> 4, seg = idx & 15;
+                    const uint4 val = *reinterpret_cast<const uint4*>(xs + t * 128 + seg * 8);
+                    *reinterpret_cast<uint4*>(a.ys + (row0 + p0 + t) * a.H + mcol * 128 + seg * 8) = val;
+                }
+                mbar_arrive(xbar + 1);  // the rows are rewritten by the next part
+                if (__any_sync(0xffffffffu,
+                               !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitNs))) {
+                    give_up();
+                    alive = false;
+                    break;
+                }
+                xphase ^= 1u;
+            }
+            if (!alive) break;   // (n16 >= 16: the first or the second part handed it back)
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // no CTA leaves while its peer may still signal or read it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kPTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
 
 static int g_pair_clusters = 0;   // clusters resident at once (0: not yet known)
 
@@ -523,6 +870,52 @@ cudaError_t launch_gateup_pair(const GemmMaps& mp, const GemmArgs& a, cudaStream
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k_gateup_pair, mp.a0, mp.a1, mp.a2, mp.a3, a);
+}
+
+static int g_down_clusters = 0;   // clusters resident at once (0: not yet known)
+
+cudaError_t down_pair_set_attributes(int num_sms) {
+    cudaError_t e = cudaFuncSetAttribute(k_down_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kDSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    cfg.blockDim = dim3(kDThreads);
+    cfg.dynamicSmemBytes = kDSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, k_down_pair, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n <= 0) return cudaErrorInvalidConfiguration;
+    g_down_clusters = n < num_sms / 2 ? n : num_sms / 2;
+    return cudaSuccess;
+}
+
+// mp.a0 / a2: W_down and the shared W_down (128-row boxes); mp.b0 / b1: h and
+// hs (128-row boxes).
+cudaError_t launch_down_pair(const GemmMaps& mp, const GemmArgs& a, cudaStream_t st) {
+    if (g_down_clusters <= 0) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * g_down_clusters);
+    cfg.blockDim = dim3(kDThreads);
+    cfg.dynamicSmemBytes = kDSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_down_pair, mp.a0, mp.a2, mp.b0, mp.b1, a);
 }
 
 }  // namespace moe

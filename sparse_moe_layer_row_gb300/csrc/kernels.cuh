@@ -59,6 +59,7 @@ struct ScatterArgs {
     int R, H, E, k, I, Is, nb;
     int nt_gu, nt_dn;   // rows per unit of the gate/up and of the down GEMM
     int gu_rows;        // intermediate rows per gate/up unit (64 or 128)
+    int dn_cols;        // hidden outputs per down unit (128, or 256 on CTA pairs)
     int32_t* prank;       // [R * k] rank of a pair among its block's pairs of its expert, or -1
     int32_t* hist;        // [nb, E] pairs per (block, expert), then bases within the expert
     int32_t* count;       // [E] surviving pairs per expert
@@ -115,13 +116,14 @@ struct GemmArgs {
 // checks each unit it reads and skips one that fails (it can only fail if the
 // workspace was overwritten while the call ran), so such a unit never drives a
 // zero-width MMA or a store past a buffer; one role counts it.
+// dn_cols: hidden outputs per down unit (128, or 256 on CTA pairs).
 __device__ __forceinline__ bool unit_valid(const int4 un, const GemmArgs& a, int nmax, bool down,
-                                           int gu_rows) {
+                                           int gu_rows, int dn_cols = 128) {
     const int g = un.x, m = un.y, start = un.z, n = un.w;
     if (g < 0 || g > a.E || n < 1 || n > nmax || start < 0) return false;
     const int cap = g == a.E ? a.ld_x - a.shared_row0 : a.shared_row0;
     if (start > cap - n) return false;
-    const int mt = down ? a.H / 128 : ((g == a.E ? a.Is : a.I) + gu_rows - 1) / gu_rows;
+    const int mt = down ? a.H / dn_cols : ((g == a.E ? a.Is : a.I) + gu_rows - 1) / gu_rows;
     return m >= 0 && m < mt;
 }
 struct GemmMaps {
@@ -146,6 +148,10 @@ cudaError_t launch_gemm(int mode, bool small, int qbits, const GemmMaps&, const 
 // Gate/up of units of up to kLargeNGU rows on CTA pairs (gemm_pair.cu).
 cudaError_t gateup_pair_set_attributes(int num_sms);
 cudaError_t launch_gateup_pair(const GemmMaps&, const GemmArgs&, cudaStream_t);
+// Down GEMM of units of up to kLargeNDown pairs x 256 hidden outputs on CTA
+// pairs (gemm_pair.cu).
+cudaError_t down_pair_set_attributes(int num_sms);
+cudaError_t launch_down_pair(const GemmMaps&, const GemmArgs&, cudaStream_t);
 
 enum { kGateUp = 0, kDown = 1 };
 

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
     }
     __syncthreads();
     const int mt_gu = (a.I + a.gu_rows - 1) / a.gu_rows, mt_gs = (a.Is + a.gu_rows - 1) / a.gu_rows;
-    const int mt_dn = a.H / 128;
+    const int mt_dn = a.H / a.dn_cols;
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
     int sum = 0, ch_gu = 0, ch_dn = 0;
@@ -183,9 +183,9 @@ __global__ void __launch_bounds__(kScanThreads) k_scatter_scan(ScatterArgs a) {
         a.units_dn[u] = make_int4(E, m, c * a.nt_dn, min(a.nt_dn, nl - c * a.nt_dn));
     }
     // down units: expert groups of kDownGroup, each group ordered weight-tile
-    // major, so the CTAs running at one time write one 128-column slab for
-    // the group's pairs and each group's activations are reused from L2
-    // across its weight tiles.
+    // major, so the CTAs (or CTA pairs) running at one time write one slab of
+    // dn_cols columns for the group's pairs and each group's activations are
+    // reused from L2 across its weight tiles.
     {  // chunk prefix of each expert
         int q = cd;
         for (int f = e0; f < e1; ++f) {

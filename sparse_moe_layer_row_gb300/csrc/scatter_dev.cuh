@@ -152,7 +152,7 @@ __device__ __forceinline__ void scatter_small(const ScatterArgs& a, ScatterSmall
     const int nl = sm.s_nl;
     const int s_chunks = nl > 0 ? 1 : 0;   // nl <= kSmallRows <= nt
     const int mt_gu = (a.I + a.gu_rows - 1) / a.gu_rows, mt_gs = (a.Is + a.gu_rows - 1) / a.gu_rows;
-    const int mt_dn = a.H / 128;
+    const int mt_dn = a.H / a.dn_cols;
     const int base_gu = s_chunks * mt_gs, base_dn = s_chunks * mt_dn;
     const int n_gu = base_gu + nch * mt_gu, n_dn = base_dn + nch * mt_dn;
     for (int u = tid; u < n_gu + n_dn; u += blockDim.x) {
