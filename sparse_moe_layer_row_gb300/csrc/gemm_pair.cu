@@ -487,25 +487,29 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
 // CTAs on neighbouring SMs run one tcgen05.mma.cta_group::2 of M = 256, N = 256
 // per 16 of K:
 //
-//   A (M = 256): W_down rows m * 256 + 128 r .. + 127 in rank r (TMA);
-//   B (N = 256): h rows start + 128 r .. + 127 of the unit's pairs in rank r
-//                (TMA; rows past the unit's count feed accumulator columns that
-//                are never read);
-//   D:           each CTA's TMEM holds its 128 hidden outputs x 256 pairs.
+//   A (M = 256): h rows start + 128 r .. + 127 of the unit's pairs in rank r
+//                (TMA; rows past the unit's count feed TMEM lanes that are
+//                never read);
+//   B (N = 256): W_down rows m * 256 + 128 r .. + 127 in rank r (TMA);
+//   D:           each CTA's TMEM holds its 128 pairs x the unit's 256 hidden
+//                outputs.
 //
 // A single-SM M = 128, N = 256 tile loads 16 KB of weights and 32 KB of h per
-// 64-wide K step; here each SM loads 16 + 16 KB for the same work, so six
-// stages fit beside the output staging.  For the shared expert, K runs over
-// [hi | lo] (2 Is columns of hs) while A wraps around its Is columns.  The
-// epilogue is the one of k_gemm<kDown>: each CTA scales its 128 outputs of
-// every pair by the pair's weight, stages them in fp16 (with a power-of-two
-// exponent per 32-column quarter beyond fp16's range) 128 pairs at a time and
-// copies them out in 256-byte row segments.
+// 64-wide K step; here each SM loads 16 + 16 KB for the same work.  For the
+// shared expert, K runs over [hi | lo] (2 Is columns of hs) while the weights
+// wrap around their Is columns.  An epilogue thread owns one pair (a TMEM
+// lane): it scales the pair's outputs by its renormalised weight (1 for the
+// shared expert) and writes them in fp16 straight to the pair's staging row,
+// 64 bytes per 32-column quarter; a quarter whose largest finite magnitude is
+// 2^15 or more is stored as v * 2^-s with the smallest s that brings it below
+// 2^15 (s to ysx, the call's `scaled` flag set; k_combine multiplies it back
+// exactly); infinities and NaNs pass through the scaling unchanged.
 //
 // Roles (224 threads per CTA):
-//   warp 0 lane 0   TMA producer of the CTA's A and B halves, completing on the
-//                   CTA's own `full`; the first stages' W_down tiles are issued
-//                   before the wait for the gate/up GEMM (their h is held back)
+//   warp 0 lane 0   TMA producer of the CTA's weight and h halves, completing
+//                   on the CTA's own `full`; the first stages' W_down tiles are
+//                   issued before the wait for the gate/up GEMM (their h is
+//                   held back)
 //   warp 1          TMEM allocation (both ranks); lane 0 of rank 0 issues the
 //                   MMAs and the commits (stage `empty`, accumulator `tfull`,
 //                   multicast to both ranks)
@@ -514,15 +518,13 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
 //                   0's `pfull` (one arrival per rank and stage), which the MMA
 //                   thread waits for alone
 // Waits, abort and drain as in k_gateup_pair.
-constexpr int kDStages = 6;
+constexpr int kDStages = 7;
 constexpr int kDThreads = 224;
-constexpr int kDStageBytes = 2 * kPTile;   // A half (weights), then B half (h)
-constexpr int kDStageRows = 128;           // pairs staged at a time
-constexpr int kDXchgOff = kDStages * kDStageBytes;
-constexpr int kDBarOff = kDXchgOff + kDStageRows * 128 * 2;
+constexpr int kDStageBytes = 2 * kPTile;   // the weight half, then the h half
+constexpr int kDBarOff = kDStages * kDStageBytes;
 constexpr int kDSmem = kDBarOff + 512 + 1024;
 static_assert(kDSmem <= 227 * 1024, "shared memory budget");
-static_assert(8 * (3 * kDStages + 7) + 12 <= 512, "barrier region");
+static_assert(8 * (3 * kDStages + 5) + 12 <= 512, "barrier region");
 static_assert(kLargeNDown == 256, "N = 256: 128 pairs per rank");
 
 __global__ void __launch_bounds__(kDThreads, 1)
@@ -538,8 +540,7 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
     uint64_t* empty = pfull + kDStages;                              // [S] stage free (both)
     uint64_t* tfull = empty + kDStages;                              // [2] accumulator ready (both)
     uint64_t* tempty = tfull + 2;                                    // [2] accumulator free (rank 0)
-    uint64_t* xbar = tempty + 2;                                     // [2] epilogue warps (own)
-    uint64_t* dbar = xbar + 2;                                       // MMA drain (rank 0)
+    uint64_t* dbar = tempty + 2;                                     // MMA drain (rank 0)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dbar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* never = abort_flag + 1;
@@ -556,7 +557,6 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
         for (int i = 0; i < 2; ++i) {
             mbar_init(tfull + i, 1);
             mbar_init(tempty + i, 256);  // 128 epilogue threads of each CTA
-            mbar_init(xbar + i, 128);    // this CTA's epilogue threads
         }
         mbar_init(dbar, 1);
         *abort_flag = 0;
@@ -613,20 +613,20 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
                 if (!valid(un)) continue;
                 const int g = un.x, m = un.y, start = un.z;
                 const bool sh = g == a.E;
-                const int Ka = sh ? a.Is : a.I;      // A's K extent
-                const int K = sh ? 2 * a.Is : a.I;   // B's: [hi | lo] for the shared expert
+                const int Kw = sh ? a.Is : a.I;      // the weights' K extent
+                const int K = sh ? 2 * a.Is : a.I;   // h's: [hi | lo] for the shared expert
                 for (int kb = 0; kb < (K >> 6); ++kb) {
                     if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
                         break;
                     }
-                    const uint32_t sA = sbase + stage * kDStageBytes, sB = sA + kPTile;
+                    const uint32_t sW = sbase + stage * kDStageBytes, sH = sW + kPTile;
                     mbar_expect_tx(full + stage, (uint32_t)kDStageBytes);
-                    const int kca = (kb * 64) % Ka, rowA = m * 256 + half;
-                    if (sh) tma_load_2d(sA, &tmS, kca, rowA, full + stage);
-                    else tma_load_3d(sA, &tmW, kca, rowA, g, full + stage);
-                    const HeldB hb{sB, sh ? &tmHs : &tmH, kb * 64, start + half, full + stage};
+                    const int kcw = (kb * 64) % Kw, roww = m * 256 + half;
+                    if (sh) tma_load_2d(sW, &tmS, kcw, roww, full + stage);
+                    else tma_load_3d(sW, &tmW, kcw, roww, g, full + stage);
+                    const HeldB hb{sH, sh ? &tmHs : &tmH, kb * 64, start + half, full + stage};
                     if (waited) tma_load_2d(hb.sB, hb.map, hb.kc, hb.row, hb.bar);
                     else held[nheld++] = hb;
                     if (!waited && nheld == kDStages) release_held();
@@ -673,10 +673,10 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sA = sbase + stage * kDStageBytes, sB = sA + kPTile;
+                    const uint32_t sW = sbase + stage * kDStageBytes, sH = sW + kPTile;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma_bf16_pair(d, smem_desc_sw128(sA + kk * 32), smem_desc_sw128(sB + kk * 32),
+                    for (int kk = 0; kk < 4; ++kk)   // A = pairs (h), B = hidden outputs (W)
+                        tc_mma_bf16_pair(d, smem_desc_sw128(sH + kk * 32), smem_desc_sw128(sW + kk * 32),
                                          idesc, (kb | kk) != 0);
                     tc_commit_pair(empty + stage);
                     if (++stage == kDStages) { stage = 0; phase ^= 1u; }
@@ -715,104 +715,69 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
         }
     } else {
         // ---------------------------------------------------------- epilogue
-        // This CTA's 128 hidden outputs mo = 256 m + 128 rank + (TMEM lane) of
-        // every pair of the unit, weighted by the pair's renormalised weight
-        // (1 for the shared expert), staged in fp16 ([pair][128]) 128 pairs at
-        // a time and copied out as one 256-byte segment per pair.  A 32-column
-        // quarter whose largest finite magnitude is 2^15 or more is stored as
-        // v * 2^-s (s to ysx, the call's `scaled` flag set; k_combine
-        // multiplies it back exactly), as in k_gemm<kDown>.
         const int q = warp & 3;  // TMEM lane quadrant this warp may read
         const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
-        __half* xs = reinterpret_cast<__half*>(base + kDXchgOff);
-        const int hl = q * 32 + lane;
-        const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue warps
         int acc = 0;
-        uint32_t acc_phase = 0, xphase = 0;
-        bool alive = true;
-        for (int u = c0; alive && u < nunits; u += nc) {
+        uint32_t acc_phase = 0;
+        for (int u = c0; u < nunits; u += nc) {
             const int4 un = __ldg(a.units + u);
             if (!valid(un)) continue;
-            const int g = un.x, start = un.z, n = un.w;
-            const int mcol = 2 * un.y + (int)rank;   // this CTA's 128-column tile of H
-            const int n16 = (n + 15) & ~15;
-            float wreg[8];   // lane l of wreg[j]: the weight of pair 32 j + l (0 past n)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int t = 32 * j + lane;
-                wreg[j] = t < n ? (g == a.E ? 1.0f : __ldg(a.pair_w + start + t)) : 0.0f;
-            }
+            const int g = un.x, m = un.y, start = un.z, n = un.w;
+            const int pi = half + q * 32 + lane;   // this thread's pair of the unit
+            const bool live = pi < n;
+            const float wv = !live ? 0.0f : g == a.E ? 1.0f : __ldg(a.pair_w + start + pi);
             const bool ok = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitNs);
             if (__any_sync(0xffffffffu, !ok)) { give_up(); break; }
             __syncwarp();
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPAccCols);
-            const size_t row0 = (size_t)(g == a.E ? a.shared_row0 : 0) + start;
-            uint8_t* xq = a.ysx + (size_t)(mcol * 4 + q) * a.ld_x + row0;  // this quarter's exponents
+            const size_t row = (size_t)(g == a.E ? a.shared_row0 : 0) + start + pi;
+            __half* out = a.ys + row * a.H + m * 256;
+            uint8_t* xq = a.ysx + (size_t)(m * 8) * a.ld_x + row;   // quarter j at + j * ld_x
             bool any_big = false;
+#pragma unroll 1
+            for (int j = 0; j < 8; ++j) {   // 32-column quarters of the unit's outputs
+                float v[32];
+                __syncwarp();  // tcgen05.ld is warp-collective
+                tmem_ld16x2(tb + (uint32_t)(32 * j), tb + (uint32_t)(32 * j + 16), v, v + 16);
+                if (!live) continue;
+                float mx = 0.0f;   // fmaxf skips NaN
 #pragma unroll
-            for (int hp = 0; hp < 2; ++hp) {
-                const int p0 = hp * kDStageRows;   // first pair of this part
-                if (p0 >= n16) break;
-#pragma unroll
-                for (int jj = 0; jj < kDStageRows / 32; ++jj) {
-                    const int j = hp * (kDStageRows / 32) + jj;
-                    const int c = 32 * j;
-                    if (c >= n16) break;
-                    float v[32];
-                    __syncwarp();  // tcgen05.ld is warp-collective
-                    tmem_ld16x2(tb + (uint32_t)c, tb + (uint32_t)(c + 16), v, v + 16);
-                    float mx = 0.0f;   // fmaxf skips NaN: the tail's 0 * garbage
+                for (int t = 0; t < 32; ++t) {
+                    v[t] *= wv;
+                    mx = fmaxf(mx, fabsf(v[t]));
+                }
+                uint32_t sc = 0;
+                if (mx >= 32768.0f) {   // the quarter's largest finite magnitude sets s
+                    uint32_t mb = 0;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
-                        v[t] *= __shfl_sync(0xffffffffu, wreg[j], t);
-                        mx = fmaxf(mx, fabsf(v[t]));
+                        const uint32_t ab = __float_as_uint(v[t]) & 0x7FFFFFFFu;
+                        mb = max(mb, ab < 0x7F800000u ? ab : 0u);
                     }
-                    uint32_t my_s = 0;  // lane t: the exponent of pair c + t
-                    if (__any_sync(0xffffffffu, mx >= 32768.0f)) {
-                        any_big = true;
+                    const int sh = (int)(mb >> 23) - 141;   // biased exponent - (127 + 14)
+                    sc = sh > 0 ? (uint32_t)sh : 0u;
+                    const float f = __uint_as_float((127u - sc) << 23);   // 2^-s, exact
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) {
-                            const uint32_t ab = __float_as_uint(v[t]) & 0x7FFFFFFFu;
-                            const uint32_t mb = __reduce_max_sync(0xffffffffu, ab < 0x7F800000u ? ab : 0u);
-                            const int sh = (int)(mb >> 23) - 141;   // biased exponent - (127 + 14)
-                            const uint32_t st = sh > 0 ? (uint32_t)sh : 0u;
-                            v[t] *= __uint_as_float((127u - st) << 23);   // 2^-s, exact
-                            if (lane == t) my_s = st;
-                        }
+                    for (int t = 0; t < 32; ++t) v[t] *= f;
+                    any_big = true;
+                }
+                uint4* o = reinterpret_cast<uint4*>(out + 32 * j);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; ++i2) {
+                        const __half2 hv = __floats2half2_rn(v[8 * c + 2 * i2], v[8 * c + 2 * i2 + 1]);
+                        w4[i2] = *reinterpret_cast<const uint32_t*>(&hv);
                     }
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) xs[(c - p0 + t) * 128 + hl] = __float2half_rn(v[t]);
-                    if (c + lane < n) xq[c + lane] = (uint8_t)my_s;
+                    o[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
-                if (hp == 1 || p0 + kDStageRows >= n16) {
-                    // the unit's last TMEM read: hand the accumulator back
-                    if (any_big && lane == 0) *a.scaled = 1;
-                    tc_fence_before();
-                    mbar_arrive_cluster(tempty0 + acc * 8);
-                }
-                mbar_arrive(xbar);
-                if (__any_sync(0xffffffffu, !mbar_wait_bounded(xbar, xphase, abort_flag, kWaitNs))) {
-                    give_up();
-                    alive = false;
-                    break;
-                }
-                const int np = min(kDStageRows, n - p0);   // pairs of this part
-                for (int idx = et; idx < np * 16; idx += 128) {  // np rows x 16 segments of 16 B
-                    const int t = idx >> 4, seg = idx & 15;
-                    const uint4 val = *reinterpret_cast<const uint4*>(xs + t * 128 + seg * 8);
-                    *reinterpret_cast<uint4*>(a.ys + (row0 + p0 + t) * a.H + mcol * 128 + seg * 8) = val;
-                }
-                mbar_arrive(xbar + 1);  // the rows are rewritten by the next part
-                if (__any_sync(0xffffffffu,
-                               !mbar_wait_bounded(xbar + 1, xphase, abort_flag, kWaitNs))) {
-                    give_up();
-                    alive = false;
-                    break;
-                }
-                xphase ^= 1u;
+                xq[(size_t)j * a.ld_x] = (uint8_t)sc;
             }
-            if (!alive) break;   // (n16 >= 16: the first or the second part handed it back)
+            if (__any_sync(0xffffffffu, any_big) && lane == 0) *a.scaled = 1;
+            tc_fence_before();
+            mbar_arrive_cluster(tempty0 + acc * 8);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
