@@ -499,8 +499,9 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
 // shared expert, K runs over [hi | lo] (2 Is columns of hs) while the weights
 // wrap around their Is columns.  An epilogue thread owns one pair (a TMEM
 // lane): it scales the pair's outputs by its renormalised weight (1 for the
-// shared expert) and writes them in fp16 straight to the pair's staging row,
-// 64 bytes per 32-column quarter; a quarter whose largest finite magnitude is
+// shared expert) and converts them to fp16; the warp trades its 32 pairs' rows
+// through shared memory (128-byte swizzle) so that eight lanes write each
+// 128-byte line of the staging rows; a quarter whose largest finite magnitude is
 // 2^15 or more is stored as v * 2^-s with the smallest s that brings it below
 // 2^15 (s to ysx, the call's `scaled` flag set; k_combine multiplies it back
 // exactly); infinities and NaNs pass through the scaling unchanged.
@@ -518,10 +519,11 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
 //                   0's `pfull` (one arrival per rank and stage), which the MMA
 //                   thread waits for alone
 // Waits, abort and drain as in k_gateup_pair.
-constexpr int kDStages = 7;
+constexpr int kDStages = 6;
 constexpr int kDThreads = 224;
 constexpr int kDStageBytes = 2 * kPTile;   // the weight half, then the h half
-constexpr int kDBarOff = kDStages * kDStageBytes;
+constexpr int kDXOff = kDStages * kDStageBytes;   // per epilogue warp: 32 rows x 128 B
+constexpr int kDBarOff = kDXOff + 4 * 32 * 128;
 constexpr int kDSmem = kDBarOff + 512 + 1024;
 static_assert(kDSmem <= 227 * 1024, "shared memory budget");
 static_assert(8 * (3 * kDStages + 5) + 12 <= 512, "barrier region");
@@ -731,49 +733,63 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
             __syncwarp();
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPAccCols);
-            const size_t row = (size_t)(g == a.E ? a.shared_row0 : 0) + start + pi;
-            __half* out = a.ys + row * a.H + m * 256;
-            uint8_t* xq = a.ysx + (size_t)(m * 8) * a.ld_x + row;   // quarter j at + j * ld_x
+            const size_t row0 = (size_t)(g == a.E ? a.shared_row0 : 0) + start + half + q * 32;
+            uint8_t* xq = a.ysx + (size_t)(m * 8) * a.ld_x + row0 + lane;   // quarter j at + j * ld_x
+            uint8_t* xw = base + kDXOff + (warp - 2) * 32 * 128;   // this warp's rows
             bool any_big = false;
 #pragma unroll 1
-            for (int j = 0; j < 8; ++j) {   // 32-column quarters of the unit's outputs
-                float v[32];
-                __syncwarp();  // tcgen05.ld is warp-collective
-                tmem_ld16x2(tb + (uint32_t)(32 * j), tb + (uint32_t)(32 * j + 16), v, v + 16);
-                if (!live) continue;
-                float mx = 0.0f;   // fmaxf skips NaN
+            for (int jp = 0; jp < 4; ++jp) {   // 64-column pieces of the unit's outputs
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    v[t] *= wv;
-                    mx = fmaxf(mx, fabsf(v[t]));
-                }
-                uint32_t sc = 0;
-                if (mx >= 32768.0f) {   // the quarter's largest finite magnitude sets s
-                    uint32_t mb = 0;
+                for (int hq = 0; hq < 2; ++hq) {   // its two 32-column quarters
+                    const int j = 2 * jp + hq;
+                    float v[32];
+                    __syncwarp();  // tcgen05.ld is warp-collective
+                    tmem_ld16x2(tb + (uint32_t)(32 * j), tb + (uint32_t)(32 * j + 16), v, v + 16);
+                    float mx = 0.0f;   // fmaxf skips NaN
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
-                        const uint32_t ab = __float_as_uint(v[t]) & 0x7FFFFFFFu;
-                        mb = max(mb, ab < 0x7F800000u ? ab : 0u);
+                        v[t] *= wv;
+                        mx = fmaxf(mx, fabsf(v[t]));
                     }
-                    const int sh = (int)(mb >> 23) - 141;   // biased exponent - (127 + 14)
-                    sc = sh > 0 ? (uint32_t)sh : 0u;
-                    const float f = __uint_as_float((127u - sc) << 23);   // 2^-s, exact
+                    uint32_t sc = 0;
+                    if (live && mx >= 32768.0f) {   // the quarter's largest finite magnitude sets s
+                        uint32_t mb = 0;
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) v[t] *= f;
-                    any_big = true;
-                }
-                uint4* o = reinterpret_cast<uint4*>(out + 32 * j);
+                        for (int t = 0; t < 32; ++t) {
+                            const uint32_t ab = __float_as_uint(v[t]) & 0x7FFFFFFFu;
+                            mb = max(mb, ab < 0x7F800000u ? ab : 0u);
+                        }
+                        const int sh = (int)(mb >> 23) - 141;   // biased exponent - (127 + 14)
+                        sc = sh > 0 ? (uint32_t)sh : 0u;
+                        const float f = __uint_as_float((127u - sc) << 23);   // 2^-s, exact
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int i2 = 0; i2 < 4; ++i2) {
-                        const __half2 hv = __floats2half2_rn(v[8 * c + 2 * i2], v[8 * c + 2 * i2 + 1]);
-                        w4[i2] = *reinterpret_cast<const uint32_t*>(&hv);
+                        for (int t = 0; t < 32; ++t) v[t] *= f;
+                        any_big = true;
                     }
-                    o[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    // row `lane`, 16-byte chunk c4 of the 128-byte piece at c4 ^ (lane & 7)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int i2 = 0; i2 < 4; ++i2) {
+                            const __half2 hv = __floats2half2_rn(v[8 * c + 2 * i2], v[8 * c + 2 * i2 + 1]);
+                            w4[i2] = *reinterpret_cast<const uint32_t*>(&hv);
+                        }
+                        const int c4 = 4 * hq + c;
+                        *reinterpret_cast<uint4*>(xw + lane * 128 + ((c4 ^ (lane & 7)) << 4)) =
+                            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    if (live) xq[(size_t)j * a.ld_x] = (uint8_t)sc;
                 }
-                xq[(size_t)j * a.ld_x] = (uint8_t)sc;
+                __syncwarp();
+                // lanes 8 i .. 8 i + 7 write row 4 s + i's 128 bytes
+#pragma unroll
+                for (int s4 = 0; s4 < 8; ++s4) {
+                    const int r = 4 * s4 + (lane >> 3), c8 = lane & 7;
+                    const uint4 val = *reinterpret_cast<const uint4*>(xw + r * 128 + ((c8 ^ (r & 7)) << 4));
+                    if (half + q * 32 + r < n)
+                        *reinterpret_cast<uint4*>(a.ys + (row0 + r) * a.H + m * 256 + jp * 64 + c8 * 8) = val;
+                }
             }
             if (__any_sync(0xffffffffu, any_big) && lane == 0) *a.scaled = 1;
             tc_fence_before();
