@@ -188,13 +188,16 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
     const moe_dims& d = p->d;
     const Layout L = make_layout(d);
     const bool small = R <= kSmallRows;
-    // units of the streaming shape: small calls, and quantised weights at any size
+    // units of the streaming shape (32 rows, two CTAs per SM): small calls, and
+    // quantised weights at any size; the down GEMM also up to kStreamDownRows
+    // rows (few pairs per expert: its CTA-pair units would be mostly empty)
     const bool su = small || p->qbits != 0;
+    const bool sd = su || R <= kStreamDownRows;
     const int nt_gu = su ? kSmallN : kLargeNGU;
-    const int nt_dn = su ? kSmallN : kLargeNDown;
+    const int nt_dn = sd ? kSmallN : kLargeNDown;
 
     ScatterArgs sa{block_offsets, topk_idx, w_renorm, keep, R, d.H, d.E, d.k, d.I, d.Is, nb, nt_gu, nt_dn,
-                   su ? 64 : 128, su ? 128 : 256,
+                   su ? 64 : 128, sd ? 128 : 256,
                    at<int32_t>(workspace, L.prank), at<int32_t>(workspace, L.hist),
                    at<int32_t>(workspace, L.count),
                    at<int32_t>(workspace, L.expert_off), at<int32_t>(workspace, L.misc),
@@ -215,13 +218,14 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
         gu.s0 = gu.s1 = gu.s2 = gu.s3 = p->tm_wg;   // unused by the bf16 kernels
         dn.s0 = dn.s1 = dn.s2 = dn.s3 = p->tm_wd;
     }
-    const uint32_t box = su ? 16 : 128;   // B rows per TMA box (k_gemm; k_down_pair: a rank's half)
-    bool good = encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box, L2A) &&
+    // B rows per TMA box: 16 for k_gemm's streaming shape, a rank's 128 for k_down_pair
+    const uint32_t box_gu = su ? 16 : 128, box_dn = sd ? 16 : 128;
+    bool good = encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box_gu, L2A) &&
                 encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
                 encode_bf16(&dn.b0, at<void>(workspace, L.h), (uint64_t)d.I, (uint64_t)L.max_pairs, 0,
-                            box, L2A) &&
+                            box_dn, L2A) &&
                 encode_bf16(&dn.b1, at<void>(workspace, L.hs), 2 * (uint64_t)d.Is,
-                            (uint64_t)d.max_rows, 0, box, L2A);
+                            (uint64_t)d.max_rows, 0, box_dn, L2A);
     if (!good) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation tensor");
     GemmArgs ga{at<int4>(workspace, L.units_gu), at<int32_t>(workspace, L.misc) + 1, d.E, d.H, d.I,
                 d.Is, R, static_cast<const __nv_bfloat16*>(x), at<__nv_bfloat16>(workspace, L.h),
@@ -240,7 +244,7 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
     GemmArgs gd = ga;
     gd.units = at<int4>(workspace, L.units_dn);
     gd.n_units = at<int32_t>(workspace, L.misc) + 2;
-    if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, su, p->qbits, dn, gd, p->num_sms, st);
+    if ((e = mark(2)) == cudaSuccess) e = launch_gemm(kDown, sd, p->qbits, dn, gd, p->num_sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
     CombineArgs ca{at<__half>(workspace, L.ys), at<uint8_t>(workspace, L.ysx),
                    (int)(L.max_pairs + d.max_rows), at<int32_t>(workspace, L.misc) + 4,

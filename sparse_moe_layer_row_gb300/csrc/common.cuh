@@ -52,6 +52,9 @@ struct Layout {
 constexpr int kSmallN = 32;
 constexpr int kLargeNGU = 256;
 constexpr int kLargeNDown = 256;
+// Calls of up to this many rows run the down GEMM in the streaming shape
+// (kSmallN rows per unit) even when the gate/up GEMM runs on CTA pairs.
+constexpr int kStreamDownRows = 512;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
