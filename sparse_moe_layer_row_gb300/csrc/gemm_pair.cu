@@ -207,6 +207,25 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// L2 eviction policies for cache-hinted copies: the weight stream of the
+// CTA-pair gate/up GEMM (the routed experts' tiles, each read once) goes first,
+// so the gathered rows of x (each read by k experts' units at different times)
+// and the shared expert's tiles (read by every chunk of rows) stay in L2.
+// Without the hint about 150 MB of x were read again from DRAM at 8192 rows.
+__device__ __forceinline__ uint64_t l2_policy_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void tma_load_3d_h(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                              int c2, uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -270,6 +289,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
     if (warp == 0) {
         // ------------------------------------------------- weight-half producer
         if (lane == 0) {
+            const uint64_t pol = l2_policy_first();   // routed weights: evict first
             const CUtensorMap* mR = leader ? &tmWg : &tmWu;
             const CUtensorMap* mS = leader ? &tmSg : &tmSu;
             int stage = 0, nfills = 0;
@@ -290,7 +310,7 @@ k_gateup_pair(const __grid_constant__ CUtensorMap tmWg, const __grid_constant__ 
                     for (int hb = 0; hb < 2; ++hb) {
                         const int row = m * 128 + 64 * hb;
                         if (g == a.E) tma_load_2d(sW + hb * 64 * 128, mS, kb * 64, row, full + stage);
-                        else tma_load_3d(sW + hb * 64 * 128, mR, kb * 64, row, g, full + stage);
+                        else tma_load_3d_h(sW + hb * 64 * 128, mR, kb * 64, row, g, full + stage, pol);
                     }
                     ++nfills;
                     if (++stage == kPStages) { stage = 0; phase ^= 1u; }
