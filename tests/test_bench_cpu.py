@@ -42,12 +42,24 @@ def test_summarize_hbm_bound_block():
     assert set(s["kernel_us"]) == {"front", "gate_up", "down", "combine"}
 
 
-def test_summarize_tensor_bound_prefill():
+def test_summarize_binding_roof():
+    """The gate/up roofline is the tighter roof: the larger of the kernel's HBM
+    time and its tensor time at the measured peaks."""
     w = W.PREFILL8192
+    # 56,651 pairs over 256 experts: 1.11 GB at 6.8 TB/s (164 us) outlasts
+    # 272 GFLOP at 1.9 PFLOP/s (143 us), so HBM binds
     s = bench.summarize(w, _meas(w, 256, 56651, 0.65, 0.26), PEAKS)
     acc = bench.accounting(w, 8192, 256, 56651)
+    assert acc["gu_bytes"] / 6800e9 > acc["gu_flops"] / 1900e12
+    assert s["roofline"]["bound"] == "hbm" and s["roofline"]["unit"] == "GB/s"
+    assert math.isclose(s["roofline"]["achieved"], acc["gu_bytes"] / 0.26e-3 / 1e9)
+    assert math.isclose(s["roofline"]["tflops_alongside"], acc["gu_flops"] / 0.26e-3 / 1e12)
+    # four times the pairs: the FLOPs bind
+    s = bench.summarize(w, _meas(w, 256, 4 * 56651, 0.65, 0.5), PEAKS)
+    acc = bench.accounting(w, 8192, 256, 4 * 56651)
+    assert acc["gu_flops"] / 1900e12 > acc["gu_bytes"] / 6800e9
     assert s["roofline"]["bound"] == "tensor" and s["roofline"]["unit"] == "TFLOP/s"
-    assert math.isclose(s["roofline"]["achieved"], acc["gu_flops"] / 0.26e-3 / 1e12)
+    assert math.isclose(s["roofline"]["achieved"], acc["gu_flops"] / 0.5e-3 / 1e12)
     assert s["roofline"]["frac"] == pytest.approx(s["roofline"]["achieved"] / 1900.0)
 
 
