@@ -58,7 +58,14 @@ def test_wait_limit_small_path():
 
 def test_wait_limit_large_path():
     """300 rows: the tensor-core router screen (k_route_tc), the CTA-pair gate/up
-    GEMM and the 256-row down GEMM abort and drain."""
+    GEMM and the streaming down GEMM (up to 512 rows) abort and drain."""
     w = W.Workload(name="abort-300", H=256, E=16, k=4, I=128, Is=128, block_rows=(300,),
                    tau=0.9, sigma_r=0.02, x_seed=9, w_seed=9)
+    _abort_and_recover(Case(w))
+
+
+def test_wait_limit_pair_down():
+    """600 rows: the CTA-pair down GEMM (k_down_pair) aborts and drains too."""
+    w = W.Workload(name="abort-600", H=256, E=16, k=4, I=128, Is=128, block_rows=(300, 300),
+                   tau=0.9, sigma_r=0.02, x_seed=10, w_seed=9)
     _abort_and_recover(Case(w))
