@@ -139,6 +139,16 @@ def test_hidden_and_intermediate_sizes(H, I, Is):
     _full(Case(_small(H=H, I=I, Is=Is, rows=(24, 8))))
 
 
+@pytest.mark.parametrize("H,I,Is,rows", [(768, 320, 192, (300, 300)), (512, 64, 192, (300, 300)),
+                                         (256, 576, 128, (200, 100))], ids=str)
+def test_hidden_and_intermediate_sizes_large(H, I, Is, rows):
+    """The many-row kernels at other sizes: intermediate tiles cut short by I or
+    Is (rows past them read as zeros), three 256-column down tiles (H = 768),
+    the shared expert's K wrapping at Is != I; 600 rows take the CTA-pair down
+    GEMM, 300 rows the streaming one beside the CTA-pair gate/up GEMM."""
+    _full(Case(_small(H=H, I=I, Is=Is, rows=rows, E=16, k=4)))
+
+
 def test_many_rows_small_shape_multichunk():
     """More than 256 rows per expert: several row chunks per expert and per shared unit."""
     w = _small(E=4, k=2, rows=(200, 300, 100), H=256, I=128, Is=64)
