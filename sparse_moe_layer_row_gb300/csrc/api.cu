@@ -426,7 +426,8 @@ moe_status moe_block_route_probs(const moe_plan* p, const void* x, int32_t R,
                        static_cast<const __nv_bfloat16*>(p->wr), logit_bias, block_offsets, R,
                        p->d.H, p->d.E, p->d.k, nb,
                        at<float>(workspace, L.wnorm), at<float>(workspace, L.logits), topk_idx, topk_w,
-                       at<uint32_t>(workspace, L.status), p->wait_ns};
+                       at<uint32_t>(workspace, L.status), p->wait_ns,
+                       route_tc_parts(R, p->d.E, p->d.H, logit_rows(p->d.max_rows), p->num_sms)};
         cudaError_t e = launch_route_tc(ta, tm_x, p->tm_wr, p->num_sms, st);
         if (e != cudaSuccess) return cuda_fail(e, "route launch");
         return ok();

@@ -56,7 +56,21 @@ constexpr int kLargeNDown = 256;
 // (kSmallN rows per unit) even when the gate/up GEMM runs on CTA pairs.
 constexpr int kStreamDownRows = 512;
 
+// Large-batch router: calls of at least kTcRouteMinRows rows screen with the
+// tensor cores.  Few rows give few 128-row tiles, so the screen splits H over
+// several CTAs per tile; its partial logits ([parts][R, E]) take at most
+// kTcSplitRows rows' worth of the logits region.
+constexpr int kTcRouteMinRows = 256;
+constexpr int kTcSplitRows = 16384;
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Rows of E fp32 logits the workspace holds for plans of up to max_rows rows.
+inline int64_t logit_rows(int64_t max_rows) {
+    if (max_rows < kTcRouteMinRows) return max_rows;
+    const int64_t r8 = 8 * max_rows;
+    return r8 < kTcSplitRows ? r8 : (max_rows > kTcSplitRows ? max_rows : kTcSplitRows);
+}
 
 inline Layout make_layout(const moe_dims& d) {
     Layout L{};
@@ -72,7 +86,7 @@ inline Layout make_layout(const moe_dims& d) {
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 1024); return at; };
     L.status = take(sizeof(uint32_t) * 64);
     L.route_cnt = take(sizeof(uint32_t) * (size_t)R);
-    L.logits = take(sizeof(float) * (size_t)(R * E));
+    L.logits = take(sizeof(float) * (size_t)(logit_rows(R) * E));
     L.wnorm = take(sizeof(float) * (size_t)E);
     L.prank = take(sizeof(int32_t) * (size_t)P);
     L.hist = take(sizeof(int32_t) * (size_t)d.max_blocks * (size_t)E);

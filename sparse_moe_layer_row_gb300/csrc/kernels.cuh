@@ -23,7 +23,6 @@ struct RouteArgs {
 };
 // Large-batch router (tensor-core screening + exact recompute of candidates).
 constexpr int kCandCap = 32;      // candidates kept per row before falling back
-constexpr int kTcRouteMinRows = 256;
 struct RouteTcArgs {
     const __nv_bfloat16* x;
     const __nv_bfloat16* wr;
@@ -31,11 +30,12 @@ struct RouteTcArgs {
     const int32_t* off;
     int R, H, E, k, nb;
     float* wnorm;         // [E]
-    float* logits;        // [R, E] approximate logits (tensor cores)
+    float* logits;        // [nk][R, E] approximate logits (tensor cores), one slice per K part
     int32_t* topk_idx;
     float* topk_w;
     uint32_t* status;
     uint64_t wait_ns;     // limit of a pipeline wait (0: the built-in limit)
+    int nk;               // parts the screen's K range is split into (summed in order by the exact pass)
 };
 struct CoresetArgs {
     const int32_t* off;
@@ -139,6 +139,7 @@ cudaError_t launch_route(const RouteArgs&, int num_sms, cudaStream_t);
 cudaError_t route_tc_set_attributes();
 cudaError_t launch_route_tc(const RouteTcArgs&, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                             int num_sms, cudaStream_t);
+int route_tc_parts(int R, int E, int H, int64_t cap_rows, int num_sms);
 cudaError_t launch_coreset(const CoresetArgs&, cudaStream_t);
 cudaError_t launch_scatter(const ScatterArgs&, bool small, int num_sms, cudaStream_t);
 cudaError_t launch_combine(const CombineArgs&, int num_sms, cudaStream_t);

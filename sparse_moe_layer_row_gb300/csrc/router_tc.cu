@@ -14,9 +14,14 @@
 // of 2^-23 relative to |accumulator| + sum|products of the slice|, whatever
 // its internal order, alignment or truncation.  Both terms are at most
 // sum_h |x_h w_h| <= |x| |w| (Cauchy-Schwarz), so H/16 steps err by at most
-// (H/16) 2^-21 2 |x||w| = H 2^-24 |x||w|.  The contract's fixed-order fp32 sum is
-// within (H/32 + 5) 2^-24 sum|x w| of the exact dot product (recursive
-// summation over H/32 terms per lane, then five butterfly additions).  So
+// (H/16) 2^-21 2 |x||w| = H 2^-24 |x||w|.  When few rows leave SMs idle, the
+// screen splits H into nk parts (one CTA each); part p's accumulator errs by
+// at most (H/nk) 2^-24 |x_p||w_p|, the parts by (H/nk) 2^-24 |x||w| together
+// (Cauchy-Schwarz over the parts), and the nk - 1 fp32 additions of the part
+// sums in part order by (nk - 1) 2^-24 |x||w|: H 2^-24 |x||w| still bounds
+// it.  The contract's fixed-order fp32 sum is within (H/32 + 5) 2^-24
+// sum|x w| of the exact dot product (recursive summation over H/32 terms per
+// lane, then five butterfly additions).  So
 // |z~ - z| <= (H + H/32 + 5) 2^-24 |x||w| < beta = 8 H 2^-24 |x||w| for every
 // H >= 256: beta covers that model about seven times over.  The norms are
 // fp32 sums times 1.001, which covers their own rounding.  The model is not
@@ -30,9 +35,10 @@
 // fewer than k comparable logits) are recomputed over all experts.
 //
 // Kernels: k_route_norms (|x_r| and |w_e|), k_route_tc (persistent; TMA ->
-// tcgen05 -> TMEM; a unit is a 128-row tile times one half (or all) of the
-// experts; the epilogue stores the approximate logits) and k_route_exact (one
-// warp per row: the k-th approximate value by warp reductions, the candidate
+// tcgen05 -> TMEM; a unit is a 128-row tile times one part of H times one
+// half (or all) of the experts; the epilogue stores the approximate logits,
+// one slice per part) and k_route_exact (one warp per row: the parts added,
+// the k-th approximate value by warp reductions, the candidate
 // list by ballots, then the candidates 16 at a time in the contract order,
 // top-k and softmax).
 #include "route_common.cuh"
@@ -91,7 +97,10 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     using C = TcCfg;
     extern __shared__ uint8_t smem_raw[];
     const int ntiles = (a.R + 127) / 128;
-    const int nunits = ntiles * nsplit;
+    // a unit: (128-row tile t, K part kp, expert slice sp); the K parts of a
+    // tile write their partial logits to slices kp of a.logits
+    const int nk = a.nk;
+    const int nunits = ntiles * nk * nsplit;
     const int NH = a.E / nsplit;  // experts per unit (MMA N)
     if ((int)blockIdx.x >= nunits) return;
     const uint32_t raw = smem_u32(smem_raw);
@@ -127,7 +136,7 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     auto give_up = [&]() {
         if (!*abort_flag) { *abort_flag = 1; status_add(a.status, MOE_STATUS_WAIT_TIMEOUT, 1); }
     };
-    const int nkb = a.H >> 6;
+    const int nkb = (a.H >> 6) / nk;   // 64-wide K steps of a part
     const uint64_t kWaitNs = a.wait_ns ? a.wait_ns : kTcWaitNs;   // pipeline waits
 
     if (warp == 0) {
@@ -137,8 +146,8 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             bool ok = true;
             const uint32_t bytes = (uint32_t)(C::kABytes + NH * 128);
             for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-                const int t = u / nsplit, sp = u - t * nsplit;
-                for (int kb = 0; kb < nkb; ++kb) {
+                const int t = u / (nk * nsplit), kp = (u / nsplit) % nk, sp = u % nsplit;
+                for (int kb = kp * nkb; kb < (kp + 1) * nkb; ++kb) {
                     if (!mbar_wait_bounded(empty + stage, phase ^ 1u, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
@@ -173,7 +182,7 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(acc * 256);
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = 0; kb < nkb; ++kb) {   // the part's K steps, from its start
                     if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs)) {
                         give_up();
                         ok = false;
@@ -204,14 +213,14 @@ k_route_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-            const int t = u / nsplit, sp = u - t * nsplit;
+            const int t = u / (nk * nsplit), kp = (u / nsplit) % nk, sp = u % nsplit;
             const bool okw = mbar_wait_bounded(tfull + acc, acc_phase, abort_flag, kWaitNs);
             if (__any_sync(0xffffffffu, !okw)) { give_up(); break; }
             __syncwarp();
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
             const int row = t * 128 + q * 32 + lane;
-            float* out = a.logits + (size_t)row * a.E + sp * NH;
+            float* out = a.logits + ((size_t)kp * a.R + row) * a.E + sp * NH;
             for (int c = 0; c < NH; c += 16) {
                 float v[16];
                 __syncwarp();
@@ -331,11 +340,19 @@ __global__ void __launch_bounds__(256, 2) k_route_exact(RouteTcArgs a) {
             __nv_bfloat16* sx = s_x + (size_t)w * a.H;
             const int blk = a.bias ? find_block(a.off, a.nb, r) : 0;
             const float* brow = a.bias ? a.bias + (size_t)blk * a.E : nullptr;
+            // the screen's K parts, added in part order (all eight loads of a
+            // part are issued before they are used)
             float az[8];
+            for (int s2 = 0; s2 < a.nk; ++s2) {
+                const float* lp = a.logits + ((size_t)s2 * a.R + r) * a.E;
+                float v[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = lane + 32 * i;
-                az[i] = e < a.E ? __ldg(a.logits + (size_t)r * a.E + e) : 0.0f;
+                for (int i = 0; i < 8; ++i) {
+                    const int e = lane + 32 * i;
+                    v[i] = e < a.E ? __ldg(lp + e) : 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) az[i] = s2 == 0 ? v[i] : __fadd_rn(az[i], v[i]);
             }
             float ss = 0.0f;
             for (int c0 = 0; c0 < a.H; c0 += 8 * 256) {
@@ -514,12 +531,25 @@ cudaError_t route_tc_set_attributes() {
                                 kExRows * kExMaxH * 2);
 }
 
+// Parts of H for the screen: the most (up to 8) that still leave every unit
+// on its own SM, divide the 64-wide K steps evenly and fit the partial
+// logits in the workspace (cap_rows rows of E logits).
+int route_tc_parts(int R, int E, int H, int64_t cap_rows, int num_sms) {
+    const int ntiles = (R + 127) / 128;
+    const int nsplit = (E > 128 && E % 32 == 0) ? 2 : 1;
+    int nk = 8;
+    while (nk > 1 && ((H / 64) % nk != 0 || (int64_t)ntiles * nsplit * nk > num_sms ||
+                      (int64_t)nk * R > cap_rows))
+        nk >>= 1;
+    return nk;
+}
+
 cudaError_t launch_route_tc(const RouteTcArgs& a, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                             int num_sms, cudaStream_t st) {
     cudaError_t e = launch_kernel(k_route_norms, dim3((unsigned)((a.E + 7) / 8)), dim3(256), 0, st, a);
     const int ntiles = (a.R + 127) / 128;
     const int nsplit = (a.E > 128 && a.E % 32 == 0) ? 2 : 1;
-    const int nunits = ntiles * nsplit;
+    const int nunits = ntiles * a.nk * nsplit;
     const int grid = nunits < num_sms ? nunits : num_sms;
     if (e == cudaSuccess)
         e = launch_kernel(k_route_tc, dim3(grid), dim3(192), TcCfg::kSmem, st, tm_x, tm_w, a, nsplit);
