@@ -218,8 +218,9 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
         gu.s0 = gu.s1 = gu.s2 = gu.s3 = p->tm_wg;   // unused by the bf16 kernels
         dn.s0 = dn.s1 = dn.s2 = dn.s3 = p->tm_wd;
     }
-    // B rows per TMA box: 16 for k_gemm's streaming shape, a rank's 128 for k_down_pair
-    const uint32_t box_gu = su ? 16 : 128, box_dn = sd ? 16 : 128;
+    // B rows per TMA box: k_gemm's streaming shape 32 (gate/up: x) and 16 (down:
+    // h); k_down_pair a rank's 128
+    const uint32_t box_gu = su ? 32 : 128, box_dn = sd ? 16 : 128;
     bool good = encode_bf16(&gu.b1, x, d.H, (uint64_t)R, 0, box_gu, L2A) &&
                 encode_bf16(&gu.bg, x, d.H, (uint64_t)R, 0, 1, L2A) &&
                 encode_bf16(&dn.b0, at<void>(workspace, L.h), (uint64_t)d.I, (uint64_t)L.max_pairs, 0,

@@ -375,6 +375,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Sixteen single columns cols[j] (the same in every lane) of a 32-lane TMEM
+// slice, one wait.
+__device__ __forceinline__ void tmem_ld_cols16(uint32_t taddr, const int* cols, float* v) {
+    uint32_t r[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                     : "=r"(r[j])
+                     : "r"(taddr + (uint32_t)cols[j]));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Two 32-lane x 16-column loads (e.g. the gate and the up accumulator of the
 // same rows), one wait.
 __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float* va, float* vb) {

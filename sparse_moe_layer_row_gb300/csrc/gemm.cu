@@ -67,12 +67,13 @@ struct GemmCfg {
     // traded in the epilogue
     static_assert(MODE == kDown || NMAX == kSmallN, "large gate/up runs in gemm_pair.cu");
     static constexpr int kGURows = 64;  // intermediate rows per gate/up unit
-    // rows per B box: 16 for the streaming shape; the whole 256-row tile in one
+    // rows per B box: 16 for the streaming shape (32 for its gate/up GEMM: the
+    // whole tile, or all of x when a call has at most 32 rows); the whole 256-row tile in one
     // box for the large shape (NMAX is a multiple of it).  Each TMA instruction
     // costs the producer about 200 cycles to issue under load, which bound the
     // large down GEMM's stage rate with four 64-row boxes; the rows past the
     // unit's count come from L2 (or read as zeros past the end of h).
-    static constexpr int kBoxRows = NMAX >= 256 ? 256 : NMAX >= 64 ? 64 : 16;
+    static constexpr int kBoxRows = NMAX >= 256 ? 256 : NMAX >= 64 ? 64 : MODE == kGateUp ? 32 : 16;
     static constexpr int kABytes = 128 * 128;
     // down, streaming shape: the shared expert's lo part of h rides in the same
     // stage as its hi part (a second MMA per K step); the large shape runs the
@@ -204,6 +205,10 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     // live-row pass) with TMA gather4 (about 7 bytes per clock per SM: enough
     // for 32-row tiles, far too few for larger ones)
     constexpr bool kGather = MODE == kGateUp && NMAX == kSmallN;
+    // A call of at most NMAX rows: every gate/up unit's B is all of x (one
+    // 32-row box per stage, no gathers), the MMA runs every row, and the
+    // epilogue reads the accumulator column of each pair's row of x.
+    const bool allrows = kGather && a.R <= NMAX;
     extern __shared__ uint8_t smem_raw[];
 
     const uint32_t raw = smem_u32(smem_raw);
@@ -317,7 +322,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             // output columns that are never read, so they need not be loaded.
             // gathered: routed rows (pair_row), and the shared expert's rows when
             // only some rows are live (shared_rows)
-            const bool gathered = kGather && (g != a.E || a.shared_rows != nullptr);
+            const bool gathered = kGather && !allrows && (g != a.E || a.shared_rows != nullptr);
             const int nb4 = (n + 3) >> 2;
             const int nbox = (n + C::kBoxRows - 1) / C::kBoxRows;
             // K steps: gate/up H; down I (routed) or, for the shared expert, Is
@@ -325,8 +330,9 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             // A wrapping around its Is columns)
             const int Ka = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
             const int K = MODE == kDown && g == a.E && !C::kDualLo ? 2 * a.Is : Ka;
-            const uint32_t bbytes = gathered ? (uint32_t)nb4 * 512u
-                                             : (uint32_t)(nbox * C::kBoxRows * 128);
+            const uint32_t bbytes = gathered  ? (uint32_t)nb4 * 512u
+                                    : allrows ? (uint32_t)(C::kBoxRows * 128)
+                                              : (uint32_t)(nbox * C::kBoxRows * 128);
             const int parts = C::kDualLo && g == a.E ? 2 : 1;
             const uint32_t abytes = C::kQuant ? (uint32_t)(C::kRawBytes + C::kScaleBytes)
                                               : (uint32_t)C::kABytes;
@@ -403,7 +409,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         if (g == a.E) tma_load_2d(sA, &tmA2, kca, m * 128, full + stage);
                         else tma_load_3d(sA, &tmA0, kca, m * 128, g, full + stage);
                     }
-                    if (!gathered) {
+                    if (allrows) tma_load_2d(sB, &tmB1, kc, 0, full + stage);   // all of x
+                    else if (!gathered) {
                         if (waited) issue_b(sB, g, start, nbox, K, kc, full + stage);
                         else held[nheld] = HeldB{sB, g, start, nbox, K, kc, full + stage};
                     }
@@ -448,7 +455,7 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     continue;
                 }
                 const int g = un.x, n = un.w;
-                const int n16 = (n + 15) & ~15;
+                const int n16 = allrows ? ((a.R + 15) & ~15) : (n + 15) & ~15;   // MMA N
                 const int K = MODE == kGateUp ? a.H
                                               : (g == a.E ? (C::kDualLo ? a.Is : 2 * a.Is) : a.I);
                 const uint32_t idesc = idesc_bf16_f32(128, n16);
@@ -555,10 +562,24 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccCols);
             bool released = false;  // accumulator handed back to the MMA warp
             if (MODE == kGateUp) {
+                // all rows of x in the accumulator: lane l holds the column (row
+                // of x) of pair start + l
+                int pcol = 0;
+                if (allrows && lane < n) {
+                    const int32_t* rl = g == a.E ? a.shared_rows : a.pair_row;
+                    pcol = rl ? __ldg(rl + start + lane) : start + lane;
+                }
                 for (int c = 0; alive && c < n16; c += 16) {
                     float v[16];
                     __syncwarp();  // tcgen05.ld is warp-collective
-                    tmem_ld16(tb + (uint32_t)c, v);
+                    if (allrows) {
+                        int cols[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) cols[j] = __shfl_sync(0xffffffffu, pcol, (c + j) & 31);
+                        tmem_ld_cols16(tb, cols, v);
+                    } else {
+                        tmem_ld16(tb + (uint32_t)c, v);
+                    }
                     // quadrants 0-1: gate rows, 2-3: up rows of intermediate index r
                     const bool is_gate = q < 2;
                     const int r = (q & 1) * 32 + lane;
