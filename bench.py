@@ -90,10 +90,15 @@ def load_peaks():
 
 
 def gemm_source_hash() -> str:
+    """Hash of the GEMM kernels' code: their sources without comments and blank
+    lines (a comment edit leaves recorded counters valid)."""
     h = hashlib.sha256()
     for f in ("gemm.cu", "gemm_pair.cu", "common.cuh", "kernels.cuh"):
-        with open(os.path.join(ROOT, "sparse_moe_layer_row_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "sparse_moe_layer_row_gb300", "csrc", f)) as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -593,10 +593,10 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmW); prefetch_tmap(&tmS); prefetch_tmap(&tmH); prefetch_tmap(&tmHs);
     }
-    // Nothing written by the gate/up GEMM is touched before the wait, except by
-    // the producer, which reads only the unit list (written by the scatter,
+    // Every role but the producer waits for the gate/up GEMM first.  Before its
+    // own wait the producer reads only the unit list (written by the scatter,
     // which the gate/up GEMM waited for before letting this kernel start) and
-    // the weights before its own wait.
+    // the weights.
     if (warp != 0) {
         pdl_wait();
         pdl_trigger();
