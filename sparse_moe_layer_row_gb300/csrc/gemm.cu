@@ -24,22 +24,18 @@
 //            weight (the weights of a row sum to 1), the shared expert's is
 //            not, and one bf16 part there too would leave almost no margin in
 //            the output tolerance.
-//            This kernel runs the gate/up GEMM for few rows per expert (the
-//            streaming shape); with many rows per expert it runs on CTA pairs
-//            with the rows of x as M (gemm_pair.cu).
 //  down:     A = 128 rows of W_down[e] (hidden outputs), B = rows of h.  For
-//            the shared expert, D = W (h_hi + h_lo): in the large shape K runs
-//            over [hi | lo] (its 2 Is columns of h) while A wraps around its Is
-//            columns, with full-width N tiles (an M = 128 MMA costs about the
-//            same for any N up to 256; measured: 535 cycles per four MMAs at
-//            N = 64, 582 at N = 256); the streaming shape, bound by weight
-//            bytes, loads both parts in one stage and issues two MMAs per K
-//            step instead (W read once).  The epilogue scales by the pair's renormalised weight
+//            the shared expert, D = W (h_hi + h_lo): both parts of h are loaded
+//            in one stage and two MMAs are issued per K step (W read once).
+//            The epilogue scales by the pair's renormalised weight
 //            and stages the pair's output row in fp16 (the shared expert with
 //            weight 1, in its own rows), with a power-of-two exponent per 32
 //            columns for values beyond fp16's range; k_combine sums the rows.
+// This kernel is the streaming shape: units of up to 32 rows, the weights
+// streamed once per call.  With many rows per expert both GEMMs run on CTA
+// pairs (gemm_pair.cu); calls of up to 512 rows keep this down GEMM.
 //
-// Pipeline (one CTA per SM, persistent over the unit list):
+// Pipeline (two CTAs per SM, persistent over the unit list):
 //   warp 0 lane 0  TMA producer: STAGES-deep ring of (A tile, B tile) stages
 //   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per 64-wide stage,
 //                  tcgen05.commit frees the stage; accumulators double-buffered
@@ -62,23 +58,20 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s when draining after 
 
 template <int MODE, int NMAX, int STAGES, int QB = 0>
 struct GemmCfg {
-    // gate/up (streaming shape only; many rows per expert run on CTA pairs,
-    // gemm_pair.cu): 64 gate + 64 up rows in one 128-row A tile, g and u
-    // traded in the epilogue
-    static_assert(MODE == kDown || NMAX == kSmallN, "large gate/up runs in gemm_pair.cu");
+    // the streaming shape only (many rows per expert run on CTA pairs,
+    // gemm_pair.cu); gate/up: 64 gate + 64 up rows in one 128-row A tile, g and
+    // u traded in the epilogue
+    static_assert(NMAX == kSmallN, "the streaming shape; many rows run in gemm_pair.cu");
     static constexpr int kGURows = 64;  // intermediate rows per gate/up unit
-    // rows per B box: 16 for the streaming shape (32 for its gate/up GEMM: the
-    // whole tile, or all of x when a call has at most 32 rows); the whole 256-row tile in one
-    // box for the large shape (NMAX is a multiple of it).  Each TMA instruction
-    // costs the producer about 200 cycles to issue under load, which bound the
-    // large down GEMM's stage rate with four 64-row boxes; the rows past the
-    // unit's count come from L2 (or read as zeros past the end of h).
-    static constexpr int kBoxRows = NMAX >= 256 ? 256 : NMAX >= 64 ? 64 : MODE == kGateUp ? 32 : 16;
+    // rows per B box: the gate/up GEMM's whole 32-row tile (or all of x when a
+    // call has at most 32 rows); 16 for the down GEMM's h rows.  Each TMA
+    // instruction costs the producer on the order of 200 cycles to issue under
+    // load, so a stage takes as few as it can.
+    static constexpr int kBoxRows = MODE == kGateUp ? 32 : 16;
     static constexpr int kABytes = 128 * 128;
-    // down, streaming shape: the shared expert's lo part of h rides in the same
-    // stage as its hi part (a second MMA per K step); the large shape runs the
-    // lo part as further K steps at the full tile width instead
-    static constexpr bool kDualLo = MODE == kDown && NMAX == kSmallN;
+    // down: the shared expert's lo part of h rides in the same stage as its hi
+    // part (a second MMA per K step, the weight tile read once)
+    static constexpr bool kDualLo = MODE == kDown;
     static constexpr int kBBytes = (kDualLo ? 2 : 1) * NMAX * 128;
     // quantised weights (QB = 8 or 4 bits, streaming shape only): a stage holds
     // the B tile, the 128 weight rows' raw codes for its 64 K and their scales
@@ -96,9 +89,8 @@ struct GemmCfg {
         kQuant ? (kBBytes + kRawBytes + kScaleBytes + 1023) / 1024 * 1024 : kABytes + kBBytes;
     static constexpr int kAOff = STAGES * kStageBytes;                 // quantised: the A slots
     static constexpr int kXchgOff = kAOff + kNA * kABytes;
-    // down: pairs of the output tile staged at a time (the large shape in two
-    // halves, so the space saved holds one more stage)
-    static constexpr int kStageRows = MODE == kDown && NMAX > 128 ? 128 : NMAX;
+    // down: pairs of the output tile staged at a time (all of them)
+    static constexpr int kStageRows = NMAX;
     // gate/up: g <-> u exchange; down: fp16 output rows of kStageRows pairs
     static constexpr int kXchgBytes = MODE == kGateUp ? 2 * 64 * 9 * 4 : kStageRows * 128 * 2;
     static constexpr int kRowsOff = kXchgOff + kXchgBytes;             // gate/up: rows of x of a unit
@@ -269,11 +261,8 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
         pdl_trigger();
     }
     const int nunits = __ldg(a.n_units);
-    // balanced rounds (common.cuh), except the large down GEMM, which keeps the
-    // plain stride its unit order is laid out for (neighbouring CTAs share rows
-    // of h; measured slower otherwise)
-    const int nact = (MODE == kGateUp || NMAX == kSmallN) ? active_workers(nunits, gridDim.x)
-                                                           : (int)gridDim.x;
+    // balanced rounds (common.cuh)
+    const int nact = active_workers(nunits, gridDim.x);
     const int ufirst = (int)blockIdx.x < nact ? (int)blockIdx.x : nunits;
 
     auto give_up = [&]() {
