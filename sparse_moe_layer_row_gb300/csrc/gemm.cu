@@ -118,11 +118,11 @@ __device__ __forceinline__ void store_h(__nv_bfloat16* out, bool shared, int ld,
     }
 }
 
-// Weights bf16(q * d) of a pair of codes given as exact floats (the product
-// is exact in fp32: at most 8 + 8 significant bits; one rounding, to nearest
-// even).
-__device__ __forceinline__ uint32_t dq_pair(float q0, float q1, float d) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(q0 * d, q1 * d);
+// Weights bf16(q * d) of a pair of codes given as exact floats: the codes are
+// exact in bf16 (|q| <= 128, at most 8 significant bits), and one bf16x2
+// product rounds the exact q * d once, to nearest even.
+__device__ __forceinline__ uint32_t dq_pair(float q0, float q1, __nv_bfloat162 d2) {
+    const __nv_bfloat162 v = __hmul2(__floats2bfloat162_rn(q0, q1), d2);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
@@ -152,30 +152,37 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* raw, const __nv_bflo
         uint8_t* row = A + r * 128;
         if (QB == 8) {
             // 16 codes = K elements 16c .. 16c + 15, all in block c / 2
-            const float d = __bfloat162float(sc[((r / SR) * 2 + (c >> 1)) * SR + (r % SR)]);
+            const __nv_bfloat162 d2 = __bfloat162bfloat162(sc[((r / SR) * 2 + (c >> 1)) * SR + (r % SR)]);
             uint32_t o[8];
 #pragma unroll
             for (int w4 = 0; w4 < 4; ++w4) {   // codes 4 w4 .. 4 w4 + 3 (bytes, in order)
                 const uint32_t xb = wd[w4] ^ 0x80808080u;   // q + 128 per byte
                 constexpr float kB = 8388736.0f;             // 2^23 + 128
-                o[2 * w4] = dq_pair(code_float(xb, 0x7650u, kB), code_float(xb, 0x7651u, kB), d);
-                o[2 * w4 + 1] = dq_pair(code_float(xb, 0x7652u, kB), code_float(xb, 0x7653u, kB), d);
+                o[2 * w4] = dq_pair(code_float(xb, 0x7650u, kB), code_float(xb, 0x7651u, kB), d2);
+                o[2 * w4 + 1] = dq_pair(code_float(xb, 0x7652u, kB), code_float(xb, 0x7653u, kB), d2);
             }
             *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         } else {
             // 32 codes (two per byte, even element low) = K elements 32c .. 32c + 31: block c
-            const float d = __bfloat162float(sc[((r / SR) * 2 + c) * SR + (r % SR)]);
+            const __nv_bfloat162 d2 = __bfloat162bfloat162(sc[((r / SR) * 2 + c) * SR + (r % SR)]);
+            // q + 8 (0..15) as the low mantissa bits of bf16 128 (0x4300): the
+            // value 128 + q + 8, exact; minus 136 gives q exactly
+            const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {   // 16-byte output chunk 4c + j: elements 8j .. 8j + 7
                 const uint32_t xb = wd[j] ^ 0x88888888u;     // q + 8 per nibble
                 const uint32_t lo = xb & 0x0F0F0F0Fu;          // byte i: element 2i
                 const uint32_t hi = (xb >> 4) & 0x0F0F0F0Fu;   // byte i: element 2i + 1
-                constexpr float kB = 8388616.0f;               // 2^23 + 8
                 uint32_t o[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    o[i] = dq_pair(code_float(lo, 0x7650u + i, kB), code_float(hi, 0x7650u + i, kB), d);
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t t = __byte_perm(lo, hi, (uint32_t)(i | ((4 + i) << 4)));
+                    const uint32_t m2 = __byte_perm(t, 0x43434343u, 0x5140u);   // {0x43 m0, 0x43 m1}
+                    const __nv_bfloat162 q2 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&m2), k136);
+                    const __nv_bfloat162 v = __hmul2(q2, d2);
+                    o[i] = *reinterpret_cast<const uint32_t*>(&v);
+                }
                 *reinterpret_cast<uint4*>(row + (((4 * c + j) ^ (r & 7)) << 4)) =
                     make_uint4(o[0], o[1], o[2], o[3]);
             }
