@@ -118,28 +118,16 @@ __device__ __forceinline__ void store_h(__nv_bfloat16* out, bool shared, int ld,
     }
 }
 
-// Weights bf16(q * d) of a pair of codes given as exact floats: the codes are
-// exact in bf16 (|q| <= 128, at most 8 significant bits), and one bf16x2
-// product rounds the exact q * d once, to nearest even.
-__device__ __forceinline__ uint32_t dq_pair(float q0, float q1, __nv_bfloat162 d2) {
-    const __nv_bfloat162 v = __hmul2(__floats2bfloat162_rn(q0, q1), d2);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// A code as an exact float without an integer-to-float conversion: the byte
-// of `xb` that `sel` picks (the code plus `bias`, as an unsigned byte) goes
-// into the low mantissa bits of 2^23, and 2^23 + bias is subtracted (exact).
-__device__ __forceinline__ float code_float(uint32_t xb, uint32_t sel, float two23_plus_bias) {
-    return __uint_as_float(__byte_perm(xb, 0x4B000000u, sel)) - two23_plus_bias;
-}
-
 // Dequantise one stage: 128 weight rows x 64 K of codes (row r at raw + r * 64
 // bytes for 8 bits, r * 32 for 4) with their scales (bf16, boxes of SR rows x
 // two blocks of 32 along K, block-major within a box) into a bf16 tile of 128
 // rows of 128 bytes in the 128-byte swizzle (16-byte chunk j of row r at chunk
 // j ^ (r & 7)), the layout the MMA's descriptor expects.  The 128 converter
 // threads take (row, 16-byte chunk of codes) items, consecutive threads
-// consecutive chunks, so a warp reads 512 contiguous bytes.
+// consecutive chunks, so a warp reads 512 contiguous bytes.  The arithmetic is
+// bf16x2: a pair of codes becomes two exact bf16 integers (|q| <= 128 has at
+// most 8 significant bits) by byte permutes and one subtraction, and one
+// bf16x2 product rounds each exact q * d once, to nearest even.
 template <int QB, int SR>
 __device__ __forceinline__ void dequant_tile(const uint8_t* raw, const __nv_bfloat16* sc, uint8_t* A,
                                              int ct) {
@@ -154,12 +142,22 @@ __device__ __forceinline__ void dequant_tile(const uint8_t* raw, const __nv_bflo
             // 16 codes = K elements 16c .. 16c + 15, all in block c / 2
             const __nv_bfloat162 d2 = __bfloat162bfloat162(sc[((r / SR) * 2 + (c >> 1)) * SR + (r % SR)]);
             uint32_t o[8];
+            // a code byte b (two's complement) as bf16: 128 + (b & 0x7F) (its low
+            // seven bits in the mantissa of 128, exact) minus 128, or minus 256
+            // when b's top bit is set (0x4300 or 0x4380): q exactly
 #pragma unroll
             for (int w4 = 0; w4 < 4; ++w4) {   // codes 4 w4 .. 4 w4 + 3 (bytes, in order)
-                const uint32_t xb = wd[w4] ^ 0x80808080u;   // q + 128 per byte
-                constexpr float kB = 8388736.0f;             // 2^23 + 128
-                o[2 * w4] = dq_pair(code_float(xb, 0x7650u, kB), code_float(xb, 0x7651u, kB), d2);
-                o[2 * w4 + 1] = dq_pair(code_float(xb, 0x7652u, kB), code_float(xb, 0x7653u, kB), d2);
+                const uint32_t lo7 = wd[w4] & 0x7F7F7F7Fu, top = wd[w4] & 0x80808080u;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {   // codes 4 w4 + 2 h2, 4 w4 + 2 h2 + 1
+                    const uint32_t sel = h2 ? 0x5342u : 0x5140u;
+                    const uint32_t m2 = __byte_perm(lo7, 0x43434343u, sel);
+                    const uint32_t c2 = __byte_perm(top, 0x43434343u, sel);
+                    const __nv_bfloat162 q2 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&m2),
+                                                      *reinterpret_cast<const __nv_bfloat162*>(&c2));
+                    const __nv_bfloat162 v = __hmul2(q2, d2);
+                    o[2 * w4 + h2] = *reinterpret_cast<const uint32_t*>(&v);
+                }
             }
             *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
