@@ -112,18 +112,21 @@ void moe_plan_destroy(moe_plan* plan);
  * bits == 4: q is a 4-bit two's-complement nibble, two per byte, the even
  * element in the low nibble, so the last dimension below is halved (in bytes).
  * Scales are bf16, block-major: d[block][row] (the scales of consecutive rows
- * of one block of 32 are contiguous).  Device pointers, 16-byte aligned:
- *   gate, up        [E, I, H]    codes       gate_scale, up_scale    [E, H/32, I]
+ * of one block of 32 are contiguous).  The gate and up matrices of an expert
+ * are one tensor (codes, and scales), their rows interleaved in groups of 64:
+ * rows 128 j .. 128 j + 63 are gate rows 64 j .. 64 j + 63 and rows
+ * 128 j + 64 .. 128 j + 127 the up rows of the same indices (so I and Is are
+ * multiples of 64); one 128-row tile is then the gate and up rows a GEMM stage
+ * needs.  Device pointers, 16-byte aligned:
+ *   gate_up         [E, 2I, H]   codes       gate_up_scale           [E, H/32, 2I]
  *   down            [E, H, I]    codes       down_scale              [E, I/32, H]
- *   shared_gate/up  [Is, H]      codes       shared_gate/up_scale    [H/32, Is]
+ *   shared_gate_up  [2Is, H]     codes       shared_gate_up_scale    [H/32, 2Is]
  *   shared_down     [H, Is]      codes       shared_down_scale       [Is/32, H]
  * The router stays bf16. */
 typedef struct moe_quant_weights {
     int32_t bits;
-    const void *gate, *up, *down;
-    const void *gate_scale, *up_scale, *down_scale;
-    const void *shared_gate, *shared_up, *shared_down;
-    const void *shared_gate_scale, *shared_up_scale, *shared_down_scale;
+    const void *gate_up, *down, *gate_up_scale, *down_scale;
+    const void *shared_gate_up, *shared_down, *shared_gate_up_scale, *shared_down_scale;
 } moe_quant_weights;
 
 /* Create a plan whose routed and shared experts are quantised (see
@@ -132,8 +135,8 @@ typedef struct moe_quant_weights {
  * the expert GEMMs read the codes and scales (half or a quarter of the bf16
  * bytes) and turn them into bf16 weights in shared memory before the tensor
  * cores use them.  All call sizes run the streaming kernels (units of 32
- * rows).  Errors: MOE_ERR_UNSUPPORTED for bits other than 8 or 4, otherwise
- * as moe_plan_create. */
+ * rows).  Errors: MOE_ERR_UNSUPPORTED for bits other than 8 or 4, or I or Is
+ * not a multiple of 64; otherwise as moe_plan_create. */
 moe_status moe_plan_create_quantized(const moe_dims* dims, const void* w_router,
                                      const moe_quant_weights* qw, moe_plan** out);
 

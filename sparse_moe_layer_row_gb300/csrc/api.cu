@@ -328,13 +328,13 @@ moe_status moe_plan_create_quantized(const moe_dims* dims, const void* w_router,
     if (!qw) return fail(MOE_ERR_INVALID_ARG, "quantised weights are NULL");
     if (qw->bits != 8 && qw->bits != 4)
         return fail(MOE_ERR_UNSUPPORTED, "bits=%d: quantised experts are 8 or 4 bits", qw->bits);
-    const void* ws[13] = {w_router, qw->gate, qw->up, qw->down, qw->gate_scale, qw->up_scale,
-                          qw->down_scale, qw->shared_gate, qw->shared_up, qw->shared_down,
-                          qw->shared_gate_scale, qw->shared_up_scale, qw->shared_down_scale};
-    const char* names[13] = {"w_router", "gate", "up", "down", "gate_scale", "up_scale",
-                             "down_scale", "shared_gate", "shared_up", "shared_down",
-                             "shared_gate_scale", "shared_up_scale", "shared_down_scale"};
-    for (int i = 0; i < 13; ++i)
+    const void* ws[9] = {w_router, qw->gate_up, qw->down, qw->gate_up_scale, qw->down_scale,
+                         qw->shared_gate_up, qw->shared_down, qw->shared_gate_up_scale,
+                         qw->shared_down_scale};
+    const char* names[9] = {"w_router", "gate_up", "down", "gate_up_scale", "down_scale",
+                            "shared_gate_up", "shared_down", "shared_gate_up_scale",
+                            "shared_down_scale"};
+    for (int i = 0; i < 9; ++i)
         if (!ws[i] || !aligned(ws[i], 16))
             return fail(MOE_ERR_INVALID_ARG, "%s is NULL or not 16-byte aligned", names[i]);
     moe_plan* p = new moe_plan();
@@ -353,33 +353,32 @@ moe_status moe_plan_create_quantized(const moe_dims* dims, const void* w_router,
     const moe_dims& d = *dims;
     p->qbits = qw->bits;
     p->wr = w_router;
-    p->wg = qw->gate; p->wu = qw->up; p->wd = qw->down;
-    p->sg = qw->shared_gate; p->su = qw->shared_up; p->sd = qw->shared_down;
-    // codes: uint8, K in bytes (halved for 4 bits), boxes of 64 K x (64 gate/up
-    // or 128 down) rows; scales: bf16 [blocks][rows], boxes of rows x 2 blocks
+    p->wg = qw->gate_up; p->wu = qw->gate_up; p->wd = qw->down;
+    p->sg = qw->shared_gate_up; p->su = qw->shared_gate_up; p->sd = qw->shared_down;
+    // codes: uint8, K in bytes (halved for 4 bits), boxes of 64 K x 128 rows
+    // (gate/up: 64 gate rows and their 64 up rows, interleaved); scales: bf16
+    // [blocks][rows], boxes of 128 rows x 2 blocks.  The up maps (tm_wu, tm_su,
+    // tm_cu, tm_csu) repeat the gate/up ones: the interleaved tensor holds both.
     const uint64_t kb = qw->bits == 8 ? 1 : 2;
     const uint32_t cbox = (uint32_t)(64 / kb);
     const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const auto B16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const uint64_t dg[3] = {d.H / kb, (uint64_t)d.I, (uint64_t)d.E}, dd[3] = {d.I / kb, (uint64_t)d.H, (uint64_t)d.E};
-    const uint64_t dsg[2] = {d.H / kb, (uint64_t)d.Is}, dsd[2] = {d.Is / kb, (uint64_t)d.H};
-    const uint32_t bg[3] = {cbox, 64, 1}, bd[3] = {cbox, 128, 1};
-    const uint64_t cg[3] = {(uint64_t)d.I, (uint64_t)(d.H / 32), (uint64_t)d.E};
+    const uint64_t dg[3] = {d.H / kb, 2 * (uint64_t)d.I, (uint64_t)d.E}, dd[3] = {d.I / kb, (uint64_t)d.H, (uint64_t)d.E};
+    const uint64_t dsg[2] = {d.H / kb, 2 * (uint64_t)d.Is}, dsd[2] = {d.Is / kb, (uint64_t)d.H};
+    const uint32_t bt[3] = {cbox, 128, 1};
+    const uint64_t cg[3] = {2 * (uint64_t)d.I, (uint64_t)(d.H / 32), (uint64_t)d.E};
     const uint64_t cd[3] = {(uint64_t)d.H, (uint64_t)(d.I / 32), (uint64_t)d.E};
-    const uint64_t csg[2] = {(uint64_t)d.Is, (uint64_t)(d.H / 32)}, csd[2] = {(uint64_t)d.H, (uint64_t)(d.Is / 32)};
-    const uint32_t sbg[3] = {64, 2, 1}, sbd[3] = {128, 2, 1};
-    bool good = encode_plain(&p->tm_wg, U8, 1, qw->gate, 3, dg, bg) &&
-                encode_plain(&p->tm_wu, U8, 1, qw->up, 3, dg, bg) &&
-                encode_plain(&p->tm_wd, U8, 1, qw->down, 3, dd, bd) &&
-                encode_plain(&p->tm_sg, U8, 1, qw->shared_gate, 2, dsg, bg) &&
-                encode_plain(&p->tm_su, U8, 1, qw->shared_up, 2, dsg, bg) &&
-                encode_plain(&p->tm_sd, U8, 1, qw->shared_down, 2, dsd, bd) &&
-                encode_plain(&p->tm_cg, B16, 2, qw->gate_scale, 3, cg, sbg) &&
-                encode_plain(&p->tm_cu, B16, 2, qw->up_scale, 3, cg, sbg) &&
-                encode_plain(&p->tm_cd, B16, 2, qw->down_scale, 3, cd, sbd) &&
-                encode_plain(&p->tm_csg, B16, 2, qw->shared_gate_scale, 2, csg, sbg) &&
-                encode_plain(&p->tm_csu, B16, 2, qw->shared_up_scale, 2, csg, sbg) &&
-                encode_plain(&p->tm_csd, B16, 2, qw->shared_down_scale, 2, csd, sbd);
+    const uint64_t csg[2] = {2 * (uint64_t)d.Is, (uint64_t)(d.H / 32)}, csd[2] = {(uint64_t)d.H, (uint64_t)(d.Is / 32)};
+    const uint32_t sb[3] = {128, 2, 1};
+    bool good = encode_plain(&p->tm_wg, U8, 1, qw->gate_up, 3, dg, bt) &&
+                encode_plain(&p->tm_wd, U8, 1, qw->down, 3, dd, bt) &&
+                encode_plain(&p->tm_sg, U8, 1, qw->shared_gate_up, 2, dsg, bt) &&
+                encode_plain(&p->tm_sd, U8, 1, qw->shared_down, 2, dsd, bt) &&
+                encode_plain(&p->tm_cg, B16, 2, qw->gate_up_scale, 3, cg, sb) &&
+                encode_plain(&p->tm_cd, B16, 2, qw->down_scale, 3, cd, sb) &&
+                encode_plain(&p->tm_csg, B16, 2, qw->shared_gate_up_scale, 2, csg, sb) &&
+                encode_plain(&p->tm_csd, B16, 2, qw->shared_down_scale, 2, csd, sb);
+    p->tm_wu = p->tm_wg; p->tm_su = p->tm_sg; p->tm_cu = p->tm_cg; p->tm_csu = p->tm_csg;
     p->tc_route = d.E <= 256 && d.E % 16 == 0 && d.k <= 16 && d.H <= 8192;
     if (good && p->tc_route)
         good = encode_bf16(&p->tm_wr, w_router, d.H, d.E, 0,

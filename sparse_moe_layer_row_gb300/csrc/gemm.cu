@@ -82,7 +82,7 @@ struct GemmCfg {
     static constexpr int kRawBytes = QB == 8 ? 128 * 64 : (QB == 4 ? 128 * 32 : 0);
     static constexpr int kScaleBytes = kQuant ? 2 * 128 * 2 : 0;
     static constexpr int kNA = kQuant ? 2 : 0;
-    static constexpr int kScaleRows = MODE == kGateUp ? 64 : 128;   // rows per scale box
+    static constexpr int kScaleRows = 128;   // rows per scale box
     static constexpr int kThreads = kQuant ? 320 : 192;
     static constexpr int kMinBlocks = 2;
     static constexpr int kStageBytes =
@@ -359,18 +359,15 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                         const uint32_t sR = sA + C::kBBytes, sS = sR + C::kRawBytes;
                         const int kq = QB == 8 ? kc : kc / 2;
                         if (MODE == kGateUp) {
-                            const int rows = m * C::kGURows;
-                            const uint32_t half = 64 * (QB == 8 ? 64 : 32);
+                            // the interleaved gate/up tensor: rows 128 m .. 128 m + 127
+                            // are gate rows 64 m .. 64 m + 63, then the same up rows
+                            const int rows = m * 128;
                             if (g == a.E) {
                                 tma_load_2d(sR, &tmA2, kq, rows, full + stage);
-                                tma_load_2d(sR + half, &tmA3, kq, rows, full + stage);
                                 tma_load_2d(sS, &tmS2, rows, kc / 32, full + stage);
-                                tma_load_2d(sS + 256, &tmS3, rows, kc / 32, full + stage);
                             } else {
                                 tma_load_3d(sR, &tmA0, kq, rows, g, full + stage);
-                                tma_load_3d(sR + half, &tmA1, kq, rows, g, full + stage);
                                 tma_load_3d(sS, &tmS0, rows, kc / 32, g, full + stage);
-                                tma_load_3d(sS + 256, &tmS1, rows, kc / 32, g, full + stage);
                             }
                         } else {
                             const int Kc = g == a.E ? a.Is : a.I;

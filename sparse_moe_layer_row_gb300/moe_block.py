@@ -33,9 +33,8 @@ class moe_dims(ctypes.Structure):
                 ("max_blocks", ctypes.c_int32)]
 
 
-_QFIELDS = ("gate", "up", "down", "gate_scale", "up_scale", "down_scale", "shared_gate",
-            "shared_up", "shared_down", "shared_gate_scale", "shared_up_scale",
-            "shared_down_scale")
+_QFIELDS = ("gate_up", "down", "gate_up_scale", "down_scale", "shared_gate_up", "shared_down",
+            "shared_gate_up_scale", "shared_down_scale")
 
 
 class moe_quant_weights(ctypes.Structure):
@@ -157,15 +156,13 @@ class Plan:
         kb = 1 if bits == 8 else 2
         code = torch.int8 if bits == 8 else torch.uint8
         _need(w_router, "w_router", torch.bfloat16, (d.E, d.H))
-        shapes = {"gate": (code, (d.E, d.I, d.H // kb)), "up": (code, (d.E, d.I, d.H // kb)),
+        shapes = {"gate_up": (code, (d.E, 2 * d.I, d.H // kb)),
                   "down": (code, (d.E, d.H, d.I // kb)),
-                  "gate_scale": (torch.bfloat16, (d.E, d.H // 32, d.I)),
-                  "up_scale": (torch.bfloat16, (d.E, d.H // 32, d.I)),
+                  "gate_up_scale": (torch.bfloat16, (d.E, d.H // 32, 2 * d.I)),
                   "down_scale": (torch.bfloat16, (d.E, d.I // 32, d.H)),
-                  "shared_gate": (code, (d.Is, d.H // kb)), "shared_up": (code, (d.Is, d.H // kb)),
+                  "shared_gate_up": (code, (2 * d.Is, d.H // kb)),
                   "shared_down": (code, (d.H, d.Is // kb)),
-                  "shared_gate_scale": (torch.bfloat16, (d.H // 32, d.Is)),
-                  "shared_up_scale": (torch.bfloat16, (d.H // 32, d.Is)),
+                  "shared_gate_up_scale": (torch.bfloat16, (d.H // 32, 2 * d.Is)),
                   "shared_down_scale": (torch.bfloat16, (d.Is // 32, d.H))}
         tensors = [getattr(q, n) for n in _QFIELDS]
         for n, t in zip(_QFIELDS, tensors):
@@ -436,8 +433,8 @@ class MoeBlockLayer:
         """A layer whose experts are quantised (moe_plan_create_quantized; ``q`` as
         for Plan.quantized, e.g. workloads.QuantExperts)."""
         E, H = w_router.shape
-        I = q.gate_scale.shape[-1]
-        Is = q.shared_gate_scale.shape[-1]
+        I = q.gate_up_scale.shape[-1] // 2
+        Is = q.shared_gate_up_scale.shape[-1] // 2
         self = cls.__new__(cls)
         self.dims = moe_dims(H, E, k, I, Is, max_rows, max_blocks)
         self.plan = Plan.quantized(self.dims, w_router, q)

@@ -320,23 +320,61 @@ def scales_k_major(d: torch.Tensor) -> torch.Tensor:
     return d.transpose(-1, -2).contiguous()
 
 
+GU_GROUP = 64   # gate and up rows interleave in groups of this many
+
+
+def interleave_gate_up(g: torch.Tensor, u: torch.Tensor, axis: int) -> torch.Tensor:
+    """Gate and up tensors (same shape) as one, their rows along ``axis``
+    interleaved in groups of GU_GROUP: group j holds gate rows 64 j .. 64 j + 63,
+    then the up rows of the same indices."""
+    axis = axis % g.dim()
+    n = g.shape[axis]
+    if n % GU_GROUP:
+        raise ValueError("the gate/up rows must be a multiple of 64")
+    shp = list(g.shape)
+    grouped = shp[:axis] + [n // GU_GROUP, 1, GU_GROUP] + shp[axis + 1:]
+    both = torch.cat((g.reshape(grouped), u.reshape(grouped)), dim=axis + 1)
+    return both.reshape(shp[:axis] + [2 * n] + shp[axis + 1:]).contiguous()
+
+
+def split_gate_up(t: torch.Tensor, axis: int):
+    """Inverse of interleave_gate_up: (gate, up)."""
+    axis = axis % t.dim()
+    n2 = t.shape[axis]
+    shp = list(t.shape)
+    grouped = t.reshape(shp[:axis] + [n2 // (2 * GU_GROUP), 2, GU_GROUP] + shp[axis + 1:])
+    out = shp[:axis] + [n2 // 2] + shp[axis + 1:]
+    return (grouped.select(axis + 1, 0).reshape(out).contiguous(),
+            grouped.select(axis + 1, 1).reshape(out).contiguous())
+
+
 @dataclass
 class QuantExperts:
-    """Quantised expert weights in the device layout.  q: int8 [E, rows, K] (8 bits)
-    or uint8 [E, rows, K / 2] (4 bits, packed); d: bf16 [E, K / 32, rows]."""
+    """Quantised expert weights in the device layout.  Codes: int8 [E, rows, K] (8
+    bits) or uint8 [E, rows, K / 2] (4 bits, packed); scales: bf16 [E, K / 32,
+    rows].  The gate and up matrices are one tensor each for codes and scales, rows
+    interleaved in groups of 64 (interleave_gate_up): gate_up [E, 2 I, K],
+    gate_up_scale [E, K / 32, 2 I]; the shared expert's likewise."""
     bits: int
-    gate: torch.Tensor
-    up: torch.Tensor
+    gate_up: torch.Tensor
     down: torch.Tensor
-    gate_scale: torch.Tensor
-    up_scale: torch.Tensor
+    gate_up_scale: torch.Tensor
     down_scale: torch.Tensor
-    shared_gate: torch.Tensor
-    shared_up: torch.Tensor
+    shared_gate_up: torch.Tensor
     shared_down: torch.Tensor
-    shared_gate_scale: torch.Tensor
-    shared_up_scale: torch.Tensor
+    shared_gate_up_scale: torch.Tensor
     shared_down_scale: torch.Tensor
+
+    def gate_and_up(self, e: int | None = None):
+        """(gate codes, gate scales, up codes, up scales) of expert e, or of the
+        shared expert (e None), each in the one-matrix layout."""
+        if e is None:
+            gq, uq = split_gate_up(self.shared_gate_up, -2)
+            gd, ud = split_gate_up(self.shared_gate_up_scale, -1)
+        else:
+            gq, uq = split_gate_up(self.gate_up[e], -2)
+            gd, ud = split_gate_up(self.gate_up_scale[e], -1)
+        return gq, gd, uq, ud
 
 
 def quantize_experts(T: "Tensors", bits: int) -> QuantExperts:
@@ -344,7 +382,7 @@ def quantize_experts(T: "Tensors", bits: int) -> QuantExperts:
     def one(w):
         q, d = quantize_rows(w, bits)
         return (pack_int4(q) if bits == 4 else q.contiguous()), scales_k_major(d)
-    parts = [one(w) for w in (T.w_gate, T.w_up, T.w_down, T.ws_gate, T.ws_up, T.ws_down)]
-    return QuantExperts(bits, parts[0][0], parts[1][0], parts[2][0], parts[0][1], parts[1][1],
-                        parts[2][1], parts[3][0], parts[4][0], parts[5][0], parts[3][1],
-                        parts[4][1], parts[5][1])
+    (gq, gd), (uq, ud), (dq, dd), (sgq, sgd), (suq, sud), (sdq, sdd) = [
+        one(w) for w in (T.w_gate, T.w_up, T.w_down, T.ws_gate, T.ws_up, T.ws_down)]
+    return QuantExperts(bits, interleave_gate_up(gq, uq, -2), dq, interleave_gate_up(gd, ud, -1), dd,
+                        interleave_gate_up(sgq, suq, -2), sdq, interleave_gate_up(sgd, sud, -1), sdd)

@@ -123,10 +123,11 @@ class Case:
 
             def dq(codes, scale):
                 return oracle.dequant(codes.detach().cpu().numpy(), u16(scale), b)
-            experts = {e: (dq(Q.gate[e], Q.gate_scale[e]), dq(Q.up[e], Q.up_scale[e]),
-                           dq(Q.down[e], Q.down_scale[e])) for e in sorted(used)}
-            shared = (dq(Q.shared_gate, Q.shared_gate_scale), dq(Q.shared_up, Q.shared_up_scale),
-                      dq(Q.shared_down, Q.shared_down_scale))
+            def gud(e):   # the gate and up matrices of the interleaved layout
+                gq, gd, uq, ud = Q.gate_and_up(e)
+                return dq(gq, gd), dq(uq, ud)
+            experts = {e: (*gud(e), dq(Q.down[e], Q.down_scale[e])) for e in sorted(used)}
+            shared = (*gud(None), dq(Q.shared_down, Q.shared_down_scale))
         else:
             experts = {e: (u16(self.T.w_gate[e]), u16(self.T.w_up[e]), u16(self.T.w_down[e]))
                        for e in sorted(used)}

@@ -170,3 +170,51 @@ def test_stack_dispatch_on_cpu():
         st(one, torch.zeros(2, dtype=torch.int32), 0.5, ys=ys[:1])
     with pytest.raises(ValueError):
         mb.MoeStack([])
+
+
+def test_gate_up_interleave_layout():
+    """The quantised gate/up tensor: rows 128 j .. 128 j + 63 are gate rows
+    64 j .. 64 j + 63, the next 64 the up rows of the same indices, along the
+    rows axis of codes (-2) and of block-major scales (-1); split inverts it."""
+    from sparse_moe_layer_row_gb300 import workloads as W
+    g = torch.arange(3 * 192 * 5).reshape(3, 192, 5)
+    u = -1 - g
+    t = W.interleave_gate_up(g, u, -2)
+    assert t.shape == (3, 384, 5)
+    for j in range(3):
+        assert torch.equal(t[:, 128 * j:128 * j + 64], g[:, 64 * j:64 * j + 64])
+        assert torch.equal(t[:, 128 * j + 64:128 * j + 128], u[:, 64 * j:64 * j + 64])
+    g2, u2 = W.split_gate_up(t, -2)
+    assert torch.equal(g2, g) and torch.equal(u2, u)
+    s = W.interleave_gate_up(g.transpose(1, 2), u.transpose(1, 2), -1)
+    assert torch.equal(s, t.transpose(1, 2))
+    with pytest.raises(ValueError):
+        W.interleave_gate_up(g[:, :96], u[:, :96], -2)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantised_experts_device_shapes(bits):
+    """quantize_experts gives the shapes the quantised plan's tensor maps read,
+    and gate_and_up(e) returns the per-matrix codes and scales it interleaved."""
+    from sparse_moe_layer_row_gb300 import workloads as W
+    w = W.TINY
+    T = W.make_tensors(w)
+    Q = W.quantize_experts(T, bits)
+    kb = 1 if bits == 8 else 2
+    assert Q.gate_up.shape == (w.E, 2 * w.I, w.H // kb)
+    assert Q.gate_up_scale.shape == (w.E, w.H // 32, 2 * w.I)
+    assert Q.shared_gate_up.shape == (2 * w.Is, w.H // kb)
+    assert Q.shared_gate_up_scale.shape == (w.H // 32, 2 * w.Is)
+    assert Q.down.shape == (w.E, w.H, w.I // kb) and Q.down_scale.shape == (w.E, w.I // 32, w.H)
+    gq, gd, uq, ud = Q.gate_and_up(1)
+    q, d = W.quantize_rows(T.w_gate[1], bits)
+    assert torch.equal(gq, W.pack_int4(q) if bits == 4 else q)
+    assert torch.equal(gd, W.scales_k_major(d))
+    q, d = W.quantize_rows(T.w_up[1], bits)
+    assert torch.equal(uq, W.pack_int4(q) if bits == 4 else q)
+    assert torch.equal(ud, W.scales_k_major(d))
+    # the binding's struct has the header's fields in the header's order
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "moe_block.h")).read()
+    body = re.search(r"typedef struct moe_quant_weights \{(.*?)\}", hdr, re.S).group(1)
+    assert re.findall(r"(\w+)\s*[,;]", body) == [f for f, _ in mb.moe_quant_weights._fields_]
