@@ -85,7 +85,8 @@ bool encode_bf16(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint
 // A tensor map without swizzle: dims[0] innermost (elements), box[i] elements;
 // rank 2 or 3; out-of-bounds elements read as zero.
 bool encode_plain(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const void* ptr,
-                  uint32_t rank, const uint64_t* dims, const uint32_t* box) {
+                  uint32_t rank, const uint64_t* dims, const uint32_t* box,
+                  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t d[3], strides[2];
@@ -94,7 +95,7 @@ bool encode_plain(CUtensorMap* m, CUtensorMapDataType dt, uint32_t esize, const 
     strides[0] = dims[0] * esize;
     strides[1] = dims[0] * dims[1] * esize;
     CUresult r = fn(m, dt, rank, const_cast<void*>(ptr), d, strides, b, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -356,7 +357,8 @@ moe_status moe_plan_create_quantized(const moe_dims* dims, const void* w_router,
     p->wg = qw->gate_up; p->wu = qw->gate_up; p->wd = qw->down;
     p->sg = qw->shared_gate_up; p->su = qw->shared_gate_up; p->sd = qw->shared_down;
     // codes: uint8, K in bytes (halved for 4 bits), boxes of 64 K x 128 rows
-    // (gate/up: 64 gate rows and their 64 up rows, interleaved); scales: bf16
+    // (gate/up: 64 gate rows and their 64 up rows, interleaved), swizzled over
+    // the box's row width (64 or 32 bytes) for the converters' row reads; scales: bf16
     // [blocks][rows], boxes of 128 rows x 2 blocks.  The up maps (tm_wu, tm_su,
     // tm_cu, tm_csu) repeat the gate/up ones: the interleaved tensor holds both.
     const uint64_t kb = qw->bits == 8 ? 1 : 2;
@@ -366,14 +368,15 @@ moe_status moe_plan_create_quantized(const moe_dims* dims, const void* w_router,
     const uint64_t dg[3] = {d.H / kb, 2 * (uint64_t)d.I, (uint64_t)d.E}, dd[3] = {d.I / kb, (uint64_t)d.H, (uint64_t)d.E};
     const uint64_t dsg[2] = {d.H / kb, 2 * (uint64_t)d.Is}, dsd[2] = {d.Is / kb, (uint64_t)d.H};
     const uint32_t bt[3] = {cbox, 128, 1};
+    const CUtensorMapSwizzle csw = qw->bits == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
     const uint64_t cg[3] = {2 * (uint64_t)d.I, (uint64_t)(d.H / 32), (uint64_t)d.E};
     const uint64_t cd[3] = {(uint64_t)d.H, (uint64_t)(d.I / 32), (uint64_t)d.E};
     const uint64_t csg[2] = {2 * (uint64_t)d.Is, (uint64_t)(d.H / 32)}, csd[2] = {(uint64_t)d.H, (uint64_t)(d.Is / 32)};
     const uint32_t sb[3] = {128, 2, 1};
-    bool good = encode_plain(&p->tm_wg, U8, 1, qw->gate_up, 3, dg, bt) &&
-                encode_plain(&p->tm_wd, U8, 1, qw->down, 3, dd, bt) &&
-                encode_plain(&p->tm_sg, U8, 1, qw->shared_gate_up, 2, dsg, bt) &&
-                encode_plain(&p->tm_sd, U8, 1, qw->shared_down, 2, dsd, bt) &&
+    bool good = encode_plain(&p->tm_wg, U8, 1, qw->gate_up, 3, dg, bt, csw) &&
+                encode_plain(&p->tm_wd, U8, 1, qw->down, 3, dd, bt, csw) &&
+                encode_plain(&p->tm_sg, U8, 1, qw->shared_gate_up, 2, dsg, bt, csw) &&
+                encode_plain(&p->tm_sd, U8, 1, qw->shared_down, 2, dsd, bt, csw) &&
                 encode_plain(&p->tm_cg, B16, 2, qw->gate_up_scale, 3, cg, sb) &&
                 encode_plain(&p->tm_cd, B16, 2, qw->down_scale, 3, cd, sb) &&
                 encode_plain(&p->tm_csg, B16, 2, qw->shared_gate_up_scale, 2, csg, sb) &&

@@ -74,21 +74,20 @@ struct GemmCfg {
     static constexpr bool kDualLo = MODE == kDown;
     static constexpr int kBBytes = (kDualLo ? 2 : 1) * NMAX * 128;
     // quantised weights (QB = 8 or 4 bits, streaming shape only): a stage holds
-    // the B tile, the 128 weight rows' raw codes for its 64 K and their scales
-    // (two blocks of 32 per row); converter warps dequantise the codes into one
-    // of kNA bf16 A slots, which the MMA reads
+    // the B tile, the 128 weight rows' raw codes for its 64 K (swizzled by the
+    // copy: 64-byte mode for 8 bits, 32-byte for 4) and their scales (two
+    // blocks of 32 per row); converter warps dequantise the codes into one of
+    // kNA bf16 A slots in tensor memory, from which the MMA reads A
     static constexpr bool kQuant = QB != 0;
     static_assert(QB == 0 || ((QB == 8 || QB == 4) && NMAX == kSmallN), "quantised: streaming shape");
     static constexpr int kRawBytes = QB == 8 ? 128 * 64 : (QB == 4 ? 128 * 32 : 0);
     static constexpr int kScaleBytes = kQuant ? 2 * 128 * 2 : 0;
-    static constexpr int kNA = kQuant ? 2 : 0;
-    static constexpr int kScaleRows = 128;   // rows per scale box
+    static constexpr int kNA = kQuant ? 4 : 0;
     static constexpr int kThreads = kQuant ? 320 : 192;
     static constexpr int kMinBlocks = 2;
     static constexpr int kStageBytes =
         kQuant ? (kBBytes + kRawBytes + kScaleBytes + 1023) / 1024 * 1024 : kABytes + kBBytes;
-    static constexpr int kAOff = STAGES * kStageBytes;                 // quantised: the A slots
-    static constexpr int kXchgOff = kAOff + kNA * kABytes;
+    static constexpr int kXchgOff = STAGES * kStageBytes;
     // down: pairs of the output tile staged at a time (all of them)
     static constexpr int kStageRows = NMAX;
     // gate/up: g <-> u exchange; down: fp16 output rows of kStageRows pairs
@@ -98,8 +97,14 @@ struct GemmCfg {
     static constexpr int kBarOff = kRowsOff + kRowsBytes;
     static constexpr int kSmem = kBarOff + 512 + 1024;
     static constexpr int kAccCols = NMAX;   // TMEM columns per accumulator
-    static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
-    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    // quantised: the A slots after the two accumulators, 32 columns (64 K of
+    // bf16) each
+    static constexpr int kACol = 2 * kAccCols;
+    static constexpr int kTmemNeed = kACol + kNA * 32;
+    static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128 : 256;
+    static_assert(kTmemNeed <= kTmemCols, "TMEM columns");
+    // two CTAs per SM: their shared memory (each with 1 KB reserved) and TMEM
+    static_assert(kSmem + 1024 <= 233472 / kMinBlocks && kTmemCols * kMinBlocks <= 512, "two CTAs per SM");
     static_assert(8 * (2 * STAGES + 2 * kNA + 7) + 16 <= 512, "barrier region");
     static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
     static_assert(NMAX % 16 == 0 && NMAX <= 256 && NMAX % (NMAX >= 64 ? 64 : 16) == 0, "MMA N extent");
@@ -118,72 +123,79 @@ __device__ __forceinline__ void store_h(__nv_bfloat16* out, bool shared, int ld,
     }
 }
 
-// Dequantise one stage: 128 weight rows x 64 K of codes (row r at raw + r * 64
-// bytes for 8 bits, r * 32 for 4) with their scales (bf16, boxes of SR rows x
-// two blocks of 32 along K, block-major within a box) into a bf16 tile of 128
-// rows of 128 bytes in the 128-byte swizzle (16-byte chunk j of row r at chunk
-// j ^ (r & 7)), the layout the MMA's descriptor expects.  The 128 converter
-// threads take (row, 16-byte chunk of codes) items, consecutive threads
-// consecutive chunks, so a warp reads 512 contiguous bytes.  The arithmetic is
-// bf16x2: a pair of codes becomes two exact bf16 integers (|q| <= 128 has at
-// most 8 significant bits) by byte permutes and one subtraction, and one
-// bf16x2 product rounds each exact q * d once, to nearest even.
-template <int QB, int SR>
-__device__ __forceinline__ void dequant_tile(const uint8_t* raw, const __nv_bfloat16* sc, uint8_t* A,
-                                             int ct) {
-    constexpr int kChunks = QB == 8 ? 4 : 2;   // 16-byte chunks of codes per row
+// Dequantise weight row r of one stage (thread r of the 128 converter
+// threads): its 64 K codes (row r at raw + r * 64 bytes for 8 bits, r * 32 for
+// 4, 16-byte chunks in the copy's swizzle: chunk c of row r at c ^ ((r >> 1) & 3)
+// for 8 bits, c ^ ((r >> 2) & 1) for 4, so the 8 rows a quarter-warp reads
+// together fall in distinct banks) and its two scales (bf16, block-major:
+// block j of row r at sc[128 j + r]) become 64 bf16 weights, stored as 32
+// columns of tensor memory from taddr on (column j: K elements 2j and 2j + 1,
+// the even one in the low half), the A operand layout of the MMA.  The
+// arithmetic is bf16x2: a pair of codes becomes two exact bf16 integers (|q| <=
+// 128 has at most 8 significant bits) by byte permutes and one subtraction,
+// and one bf16x2 product rounds each exact q * d once, to nearest even.
+template <int QB>
+__device__ __forceinline__ void dequant_row(const uint8_t* raw, const __nv_bfloat16* sc, int r,
+                                            uint32_t taddr) {
+    if (QB == 8) {
+        const uint8_t* row = raw + r * 64;
+        const int sw = (r >> 1) & 3;
 #pragma unroll
-    for (int it = ct; it < 128 * kChunks; it += 128) {
-        const int r = it / kChunks, c = it % kChunks;
-        const uint4 w = *reinterpret_cast<const uint4*>(raw + r * (16 * kChunks) + c * 16);
-        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
-        uint8_t* row = A + r * 128;
-        if (QB == 8) {
-            // 16 codes = K elements 16c .. 16c + 15, all in block c / 2
-            const __nv_bfloat162 d2 = __bfloat162bfloat162(sc[((r / SR) * 2 + (c >> 1)) * SR + (r % SR)]);
-            uint32_t o[8];
-            // a code byte b (two's complement) as bf16: 128 + (b & 0x7F) (its low
-            // seven bits in the mantissa of 128, exact) minus 128, or minus 256
-            // when b's top bit is set (0x4300 or 0x4380): q exactly
+        for (int blk = 0; blk < 2; ++blk) {   // K elements 32 blk .. 32 blk + 31: chunks 2 blk, 2 blk + 1
+            const __nv_bfloat162 d2 = __bfloat162bfloat162(sc[blk * 128 + r]);
+            uint32_t o[16];
 #pragma unroll
-            for (int w4 = 0; w4 < 4; ++w4) {   // codes 4 w4 .. 4 w4 + 3 (bytes, in order)
-                const uint32_t lo7 = wd[w4] & 0x7F7F7F7Fu, top = wd[w4] & 0x80808080u;
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * blk + cc;
+                const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+                const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+                // a code byte b (two's complement) as bf16: 128 + (b & 0x7F) (its low
+                // seven bits in the mantissa of 128, exact) minus 128, or minus 256
+                // when b's top bit is set (0x4300 or 0x4380): q exactly
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {   // codes 4 w4 + 2 h2, 4 w4 + 2 h2 + 1
-                    const uint32_t sel = h2 ? 0x5342u : 0x5140u;
-                    const uint32_t m2 = __byte_perm(lo7, 0x43434343u, sel);
-                    const uint32_t c2 = __byte_perm(top, 0x43434343u, sel);
-                    const __nv_bfloat162 q2 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&m2),
-                                                      *reinterpret_cast<const __nv_bfloat162*>(&c2));
-                    const __nv_bfloat162 v = __hmul2(q2, d2);
-                    o[2 * w4 + h2] = *reinterpret_cast<const uint32_t*>(&v);
+                for (int w4 = 0; w4 < 4; ++w4) {   // codes 4 w4 .. 4 w4 + 3 of the chunk (bytes, in order)
+                    const uint32_t lo7 = wd[w4] & 0x7F7F7F7Fu, top = wd[w4] & 0x80808080u;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {   // codes 4 w4 + 2 h2, 4 w4 + 2 h2 + 1
+                        const uint32_t sel = h2 ? 0x5342u : 0x5140u;
+                        const uint32_t m2 = __byte_perm(lo7, 0x43434343u, sel);
+                        const uint32_t c2 = __byte_perm(top, 0x43434343u, sel);
+                        const __nv_bfloat162 q2 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&m2),
+                                                          *reinterpret_cast<const __nv_bfloat162*>(&c2));
+                        const __nv_bfloat162 v = __hmul2(q2, d2);
+                        o[8 * cc + 2 * w4 + h2] = *reinterpret_cast<const uint32_t*>(&v);
+                    }
                 }
             }
-            *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-        } else {
-            // 32 codes (two per byte, even element low) = K elements 32c .. 32c + 31: block c
-            const __nv_bfloat162 d2 = __bfloat162bfloat162(sc[((r / SR) * 2 + c) * SR + (r % SR)]);
-            // q + 8 (0..15) as the low mantissa bits of bf16 128 (0x4300): the
-            // value 128 + q + 8, exact; minus 136 gives q exactly
-            const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
+            tmem_st16(taddr + 16 * blk, o);
+        }
+    } else {
+        const uint8_t* row = raw + r * 32;
+        const int sw = (r >> 2) & 1;
+        // q + 8 (0..15) as the low mantissa bits of bf16 128 (0x4300): the
+        // value 128 + q + 8, exact; minus 136 gives q exactly
+        const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.0f, 136.0f);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {   // 16-byte output chunk 4c + j: elements 8j .. 8j + 7
+        for (int c = 0; c < 2; ++c) {   // 32 codes (two per byte, even element low) = block c
+            const __nv_bfloat162 d2 = __bfloat162bfloat162(sc[c * 128 + r]);
+            const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+            const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+            uint32_t o[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {   // elements 8j .. 8j + 7 of the block
                 const uint32_t xb = wd[j] ^ 0x88888888u;     // q + 8 per nibble
                 const uint32_t lo = xb & 0x0F0F0F0Fu;          // byte i: element 2i
                 const uint32_t hi = (xb >> 4) & 0x0F0F0F0Fu;   // byte i: element 2i + 1
-                uint32_t o[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t t = __byte_perm(lo, hi, (uint32_t)(i | ((4 + i) << 4)));
                     const uint32_t m2 = __byte_perm(t, 0x43434343u, 0x5140u);   // {0x43 m0, 0x43 m1}
                     const __nv_bfloat162 q2 = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&m2), k136);
                     const __nv_bfloat162 v = __hmul2(q2, d2);
-                    o[i] = *reinterpret_cast<const uint32_t*>(&v);
+                    o[4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
                 }
-                *reinterpret_cast<uint4*>(row + (((4 * c + j) ^ (r & 7)) << 4)) =
-                    make_uint4(o[0], o[1], o[2], o[3]);
             }
+            tmem_st16(taddr + 16 * c, o);
         }
     }
 }
@@ -467,15 +479,23 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
                     }
                     tc_fence_after();
                     const uint32_t sSt = sbase + stage * C::kStageBytes;
-                    const uint32_t sA = C::kQuant ? sbase + C::kAOff + aslot * C::kABytes : sSt;
                     const uint32_t sB = C::kQuant ? sSt : sSt + C::kABytes;
+                    // quantised: A in tensor memory, 8 columns per 16 K
+                    const uint32_t ta = tmem + (uint32_t)(C::kACol + aslot * 32);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(sA + kk * 32);
                         const uint64_t bd = smem_desc_sw128(sB + kk * 32);
-                        tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
-                        if (C::kDualLo && g == a.E)  // shared expert: lo part of h
-                            tc_mma_bf16(d, ad, smem_desc_sw128(sB + NMAX * 128 + kk * 32), idesc, 1u);
+                        const uint64_t bdl = smem_desc_sw128(sB + NMAX * 128 + kk * 32);
+                        if (C::kQuant) {
+                            tc_mma_bf16_ta(d, ta + kk * 8, bd, idesc, (kb | kk) != 0);
+                            if (C::kDualLo && g == a.E)  // shared expert: lo part of h
+                                tc_mma_bf16_ta(d, ta + kk * 8, bdl, idesc, 1u);
+                        } else {
+                            const uint64_t ad = smem_desc_sw128(sSt + kk * 32);
+                            tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0);
+                            if (C::kDualLo && g == a.E)  // shared expert: lo part of h
+                                tc_mma_bf16(d, ad, bdl, idesc, 1u);
+                        }
                     }
                     tc_commit(empty + stage);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -496,10 +516,14 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
     } else if (C::kQuant && warp >= 6) {
         // ---------------------------------------------------------- converter
         // Stage by stage, in the MMA's order: wait for the stage's copies and a
-        // free A slot, turn the 128 rows x 64 K codes into bf16 weights
-        // bf16(q * d) in the slot's 128-byte swizzled layout, fence them for
-        // the async proxy and hand the slot to the MMA.
-        const int ct = threadIdx.x - 192;   // 0..127
+        // free A slot; thread r turns weight row r's 64 K codes into bf16
+        // weights bf16(q * d) in lane r of the slot's tensor-memory columns
+        // and, once its stores are complete, hands the slot to the MMA.  A
+        // warp may only reach the 32 lanes of its quadrant (warp & 3), so that
+        // sets its rows; its waits are voted, since the tensor-memory stores
+        // are warp-wide instructions.
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)C::kACol;
         int stage = 0, aslot = 0;
         uint32_t phase = 0, aphase = 0;
         bool ok = true;
@@ -509,17 +533,19 @@ k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtenso
             const int g = un.x;
             const int K = MODE == kGateUp ? a.H : (g == a.E ? a.Is : a.I);
             for (int kb = 0; kb < (K >> 6); ++kb) {
-                if (!mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs) ||
-                    !mbar_wait_bounded(aempty + aslot, aphase ^ 1u, abort_flag, kWaitNs)) {
-                    give_up();
+                const bool w_ok = mbar_wait_bounded(full + stage, phase, abort_flag, kWaitNs) &&
+                                  mbar_wait_bounded(aempty + aslot, aphase ^ 1u, abort_flag, kWaitNs);
+                if (__any_sync(0xffffffffu, !w_ok)) {
+                    if (!w_ok) give_up();
                     ok = false;
                     break;
                 }
+                tc_fence_after();   // the MMA that last read the slot has completed
                 const uint8_t* raw = base + stage * C::kStageBytes + C::kBBytes;
                 const __nv_bfloat16* sc = reinterpret_cast<const __nv_bfloat16*>(raw + C::kRawBytes);
-                uint8_t* A = base + C::kAOff + aslot * C::kABytes;
-                dequant_tile<QB, C::kScaleRows>(raw, sc, A, ct);
-                fence_proxy_async_smem();
+                dequant_row<QB>(raw, sc, r, tq + (uint32_t)(aslot * 32));
+                tmem_st_wait();
+                tc_fence_before();
                 mbar_arrive(conv + aslot);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 if (++aslot == C::kNA) { aslot = 0; aphase ^= 1u; }
@@ -739,15 +765,17 @@ static cudaError_t set_attr() {
 // at every row count.
 constexpr int kSmallStagesGU = 5, kSmallStagesDN = 4;
 constexpr int kSmallCtasPerSm = 2;
+// quantised stages hold no A tile (it is built in tensor memory), so more fit
+constexpr int kQuantStagesGU = 7, kQuantStagesDN = 5;
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
     if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU>()) != cudaSuccess) return e;
     if ((e = set_attr<kDown, kSmallN, kSmallStagesDN>()) != cudaSuccess) return e;
-    if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU, 8>()) != cudaSuccess) return e;
-    if ((e = set_attr<kDown, kSmallN, kSmallStagesDN, 8>()) != cudaSuccess) return e;
-    if ((e = set_attr<kGateUp, kSmallN, kSmallStagesGU, 4>()) != cudaSuccess) return e;
-    return set_attr<kDown, kSmallN, kSmallStagesDN, 4>();
+    if ((e = set_attr<kGateUp, kSmallN, kQuantStagesGU, 8>()) != cudaSuccess) return e;
+    if ((e = set_attr<kDown, kSmallN, kQuantStagesDN, 8>()) != cudaSuccess) return e;
+    if ((e = set_attr<kGateUp, kSmallN, kQuantStagesGU, 4>()) != cudaSuccess) return e;
+    return set_attr<kDown, kSmallN, kQuantStagesDN, 4>();
 }
 
 cudaError_t launch_gemm(int mode, bool small, int qbits, const GemmMaps& mp, const GemmArgs& a,
@@ -755,10 +783,10 @@ cudaError_t launch_gemm(int mode, bool small, int qbits, const GemmMaps& mp, con
     if (qbits) {
         grid *= kSmallCtasPerSm;
         if (qbits == 8)
-            return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStagesGU, 8>(mp, a, grid, st)
-                                   : launch_one<kDown, kSmallN, kSmallStagesDN, 8>(mp, a, grid, st);
-        return mode == kGateUp ? launch_one<kGateUp, kSmallN, kSmallStagesGU, 4>(mp, a, grid, st)
-                               : launch_one<kDown, kSmallN, kSmallStagesDN, 4>(mp, a, grid, st);
+            return mode == kGateUp ? launch_one<kGateUp, kSmallN, kQuantStagesGU, 8>(mp, a, grid, st)
+                                   : launch_one<kDown, kSmallN, kQuantStagesDN, 8>(mp, a, grid, st);
+        return mode == kGateUp ? launch_one<kGateUp, kSmallN, kQuantStagesGU, 4>(mp, a, grid, st)
+                               : launch_one<kDown, kSmallN, kQuantStagesDN, 4>(mp, a, grid, st);
     }
     if (small) {
         grid *= kSmallCtasPerSm;
