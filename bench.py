@@ -623,7 +623,7 @@ def run_gpu(args, w: W.Workload):
     # the other full-size workloads, timed in the same run (1 GPU only)
     if ws == 1 and not args.no_extra_workloads:
         extra = {}
-        for name in EXTRA_WORKLOADS:
+        for name in (EXTRA_WORKLOADS if args.extras is None else args.extras):
             we = W.BY_NAME[name]
             if we.name == w.name:
                 continue
@@ -676,6 +676,10 @@ def main(argv=None):
                     help="also time the main workload's layer with 8-bit and 4-bit experts")
     ap.add_argument("--no-extra-workloads", action="store_true",
                     help="skip the other full-size workloads (reported under workloads)")
+    ap.add_argument("--extras", type=lambda v: [t for t in v.split(",") if t and t != "none"],
+                    default=None,
+                    help="comma-separated names of the other full-size workloads to time "
+                         "(default: all of them; 'none': none, e.g. with --quant-workloads only)")
     ap.add_argument("--extra-steps", type=int, default=30,
                     help="timed steps of each extra workload")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
@@ -688,6 +692,9 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    for name in args.extras or ():
+        if name not in W.BY_NAME:
+            ap.error(f"--extras: unknown workload {name!r}")
     w = W.BY_NAME[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
