@@ -253,7 +253,7 @@ moe_status enqueue_forward(const moe_plan* p, const void* x, int32_t R,
                    at<int32_t>(workspace, L.inv), R, d.H, d.k,
                    (int)L.max_pairs, static_cast<__nv_bfloat16*>(y), y_f32,
                    at<uint32_t>(workspace, L.status), live, at<int32_t>(workspace, L.shared_inv)};
-    if ((e = mark(3)) == cudaSuccess) e = launch_combine(ca, p->num_sms, st);
+    if ((e = mark(3)) == cudaSuccess) e = launch_combine(ca, p->num_sms, !sd, st);
     if (e == cudaSuccess) e = mark(4);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
     return ok();

@@ -134,7 +134,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // global memory that another kernel writes or reads; the only thing done
 // before it is reading the weights (read-only for every kernel).  pdl_trigger()
 // lets the next kernel be scheduled; it is called right after the wait, so at
-// most two kernels of a stream overlap.
+// most two kernels of a stream overlap.  The down GEMM on CTA pairs
+// (k_down_pair, bf16 calls over kStreamDownRows rows) does not call it: the
+// combine then launches when the down GEMM ends, since combine CTAs made
+// resident early, waiting, slowed the down GEMM's last units (8192 rows: step
+// 556 -> 545 us without the early trigger, with the four-CTA combine).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

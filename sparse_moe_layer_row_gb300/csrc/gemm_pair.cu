@@ -596,11 +596,9 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
     // Every role but the producer waits for the gate/up GEMM first.  Before its
     // own wait the producer reads only the unit list (written by the scatter,
     // which the gate/up GEMM waited for before letting this kernel start) and
-    // the weights.
-    if (warp != 0) {
-        pdl_wait();
-        pdl_trigger();
-    }
+    // the weights.  No role triggers the combine's launch: it launches when
+    // this kernel ends (common.cuh).
+    if (warp != 0) pdl_wait();
     const int nunits = __ldg(a.n_units);
     const int nc = (int)cluster_count();   // plain stride: neighbouring units share h
     const int c0 = (int)cluster_id();
@@ -621,7 +619,6 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
             bool waited = false;
             auto release_held = [&]() {
                 pdl_wait();
-                pdl_trigger();
                 for (int i = 0; i < nheld; ++i)
                     tma_load_2d(held[i].sB, held[i].map, held[i].kc, held[i].row, held[i].bar);
                 nheld = 0;
@@ -665,7 +662,6 @@ k_down_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUt
             }
         } else {
             pdl_wait();
-            pdl_trigger();
         }
     } else if (warp == 1) {
         if (leader && lane == 0) {

@@ -142,7 +142,8 @@ cudaError_t launch_route_tc(const RouteTcArgs&, const CUtensorMap& tm_x, const C
 int route_tc_parts(int R, int E, int H, int64_t cap_rows, int num_sms);
 cudaError_t launch_coreset(const CoresetArgs&, cudaStream_t);
 cudaError_t launch_scatter(const ScatterArgs&, bool small, int num_sms, cudaStream_t);
-cudaError_t launch_combine(const CombineArgs&, int num_sms, cudaStream_t);
+// after_pair_down: the down GEMM before it ran on CTA pairs (k_down_pair)
+cudaError_t launch_combine(const CombineArgs&, int num_sms, bool after_pair_down, cudaStream_t);
 cudaError_t gemm_set_attributes();
 cudaError_t launch_gemm(int mode, bool small, int qbits, const GemmMaps&, const GemmArgs&,
                         int grid, cudaStream_t);

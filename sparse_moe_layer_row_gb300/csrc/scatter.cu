@@ -345,7 +345,13 @@ __device__ __forceinline__ void combine_rows(const CombineArgs& a) {
     }
 }
 
-__global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
+// kMinCtas CTAs per SM: after the CTA-pair down GEMM four, registers capped at 64, 32 warps per SM to keep
+// more loads in flight (8192 rows: 69.6 -> 62.7 us); that down GEMM lets the
+// combine launch only when it ends (common.cuh).  Otherwise one: launched
+// early, four CTAs per SM waiting beside the streaming down GEMM slowed the
+// step.
+template <int kMinCtas>
+__global__ void __launch_bounds__(256, kMinCtas) k_combine(CombineArgs a) {
     pdl_wait();  // see common.cuh: nothing global is touched before
     pdl_trigger();
     if (*a.scaled) combine_rows<true>(a);
@@ -363,11 +369,13 @@ cudaError_t launch_scatter(const ScatterArgs& a, bool small, int num_sms, cudaSt
     return e;
 }
 
-cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st) {
+cudaError_t launch_combine(const CombineArgs& a, int num_sms, bool after_pair_down, cudaStream_t st) {
     long blocks = ((long)a.R * (a.H / 256) + 7) / 8;
     if (blocks > (long)num_sms * 16) blocks = (long)num_sms * 16;
     if (blocks < 1) blocks = 1;
-    return launch_kernel(k_combine, dim3((unsigned)blocks), dim3(256), 0, st, a);
+    if (after_pair_down)
+        return launch_kernel(k_combine<4>, dim3((unsigned)blocks), dim3(256), 0, st, a);
+    return launch_kernel(k_combine<1>, dim3((unsigned)blocks), dim3(256), 0, st, a);
 }
 
 }  // namespace moe
