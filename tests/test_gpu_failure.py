@@ -69,3 +69,14 @@ def test_wait_limit_pair_down():
     w = W.Workload(name="abort-600", H=256, E=16, k=4, I=128, Is=128, block_rows=(300, 300),
                    tau=0.9, sigma_r=0.02, x_seed=10, w_seed=9)
     _abort_and_recover(Case(w))
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_wait_limit_quantised(bits):
+    """Quantised experts: the converter warps (voted waits, tensor-memory A
+    slots) give up with the producer and the MMA thread, and the next call is
+    unaffected (200 rows: a unit list of several rounds per CTA)."""
+    w = W.Workload(name=f"abort-q{bits}", H=256, E=16, k=4, I=128, Is=128, block_rows=(100, 100),
+                   tau=0.9, sigma_r=0.02, x_seed=11, w_seed=9)
+    T = W.make_tensors(w, device="cuda")
+    _abort_and_recover(Case(w, T=T, quant=W.quantize_experts(T, bits)))
